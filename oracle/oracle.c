@@ -1,0 +1,541 @@
+/*
+ * oracle.c -- plain, slow, CPU reference for the KOSMOS fused operators.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  It shares no code, header,
+ * table or helper with the CUDA path (comm_persistent_gemm_gb300/csrc).
+ *
+ * Every floating-point result is accumulated in IEEE double from the same bf16
+ * (or MXFP8-quantised) inputs the GPU receives; outputs are NOT rounded to
+ * bf16.  Loops follow the definitions with no blocking, fusion or reordering
+ * of a sum: each output element is summed over K in ascending order (and, for
+ * the reduce-scatter, over ranks r = 0..P-1 in that order).
+ *
+ * Sources (web pages on "KOSMOS: Self-scheduling Persistent Kernels for
+ * Communication-Compute Overlap"):
+ *   [explainer]  learnaivisually.com "KOSMOS -- Self-scheduling persistent
+ *                kernels -- What does it mean?", paragraphs named by their
+ *                opening words ("Start with the problem", "KOSMOS removes the
+ *                manager", "Role switching only works", ...).
+ *   [abstract]   the authors' arXiv abstract (2611.07477v1).
+ *
+ * Parity pins live in tests/test_oracle_*.py.  Functions whose exact values
+ * have no independent pin are marked "parity unpinned" below (none at
+ * present: every function has at least one pin).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_EXPORT __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16 is the upper half of an IEEE binary32 word. */
+ORC_EXPORT double orc_bf16_to_f64(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP FP8 E4M3 ("fn" variant): 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+ * exponent field 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; no infinity;
+ * largest finite 1.75 * 2^8 = 448. */
+ORC_EXPORT double orc_e4m3_to_f64(uint8_t q) {
+    int s = (q >> 7) & 1;
+    int e = (q >> 3) & 15;
+    int m = q & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to even mantissa, saturating to +-448 (the
+ * quantiser below never reaches the saturation branch: its scale keeps every
+ * scaled element within +-448). */
+ORC_EXPORT uint8_t orc_f64_to_e4m3(double v) {
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal grid: multiples of 2^-9; 8 * 2^-9 is the smallest normal,
+         * whose code (exponent 1, mantissa 0) is also the integer 8 */
+        double mq = nearbyint(a * 512.0);
+        return (uint8_t)(sign | (uint8_t)mq);
+    }
+    int ex;
+    frexp(a, &ex);               /* a = f * 2^ex, f in [0.5, 1) */
+    int E = ex - 1;              /* a = (1 + t) * 2^E, t in [0, 1) */
+    double t = a / ldexp(1.0, E) - 1.0;
+    double mq = nearbyint(t * 8.0);
+    if (mq == 8.0) { mq = 0.0; E += 1; }
+    int be = E + 7;
+    if (be > 15 || (be == 15 && mq == 7.0)) return (uint8_t)(sign | 0x7E);
+    return (uint8_t)(sign | (uint8_t)(be << 3) | (uint8_t)mq);
+}
+
+/* Shared exponent of one 32-element block: the smallest integer e with
+ * blockmax <= 448 * 2^e (that is, 2^ceil(log2(blockmax / 448))), clamped to the
+ * E8M0 range [-127, 127].  An all-zero block takes e = 0. */
+ORC_EXPORT int orc_mx_scale_exp(double blockmax) {
+    if (!(blockmax > 0.0)) return 0;
+    int e = (int)ceil(log2(blockmax / 448.0));
+    while (blockmax > ldexp(448.0, e)) e++;
+    while (blockmax <= ldexp(448.0, e - 1)) e--;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* MXFP8 quantisation of a row-major bf16 matrix [rows, cols].
+ *   along_cols = 1: blocks are 32 contiguous columns of one row (an activation
+ *                   X[m, K]); scales are [rows, cols/32].
+ *   along_cols = 0: blocks are 32 contiguous rows of one column (a weight
+ *                   W[K, n]); scales are [cols, rows/32].
+ * q keeps the input's [rows, cols] layout.  Scale byte = e + 127 (E8M0). */
+ORC_EXPORT int orc_mxfp8_quantize(int64_t rows, int64_t cols, const uint16_t *x,
+                                  int along_cols, uint8_t *q, uint8_t *scales) {
+    if (along_cols) {
+        if (cols % 32) return 1;
+        for (int64_t i = 0; i < rows; i++)
+            for (int64_t b = 0; b < cols / 32; b++) {
+                double mx = 0.0;
+                for (int j = 0; j < 32; j++) {
+                    double a = fabs(orc_bf16_to_f64(x[i * cols + b * 32 + j]));
+                    if (a > mx) mx = a;
+                }
+                int e = orc_mx_scale_exp(mx);
+                scales[i * (cols / 32) + b] = (uint8_t)(e + 127);
+                for (int j = 0; j < 32; j++) {
+                    double v = orc_bf16_to_f64(x[i * cols + b * 32 + j]);
+                    q[i * cols + b * 32 + j] = orc_f64_to_e4m3(ldexp(v, -e));
+                }
+            }
+    } else {
+        if (rows % 32) return 1;
+        for (int64_t c = 0; c < cols; c++)
+            for (int64_t b = 0; b < rows / 32; b++) {
+                double mx = 0.0;
+                for (int j = 0; j < 32; j++) {
+                    double a = fabs(orc_bf16_to_f64(x[(b * 32 + j) * cols + c]));
+                    if (a > mx) mx = a;
+                }
+                int e = orc_mx_scale_exp(mx);
+                scales[c * (rows / 32) + b] = (uint8_t)(e + 127);
+                for (int j = 0; j < 32; j++) {
+                    double v = orc_bf16_to_f64(x[(b * 32 + j) * cols + c]);
+                    q[(b * 32 + j) * cols + c] = orc_f64_to_e4m3(ldexp(v, -e));
+                }
+            }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* All-gather + GEMM                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* [explainer, "Start with the problem"]: each layer gathers the pieces of its
+ * input from the other ranks before the matrix multiplication.  The gathered
+ * input is the row concatenation [X_0; X_1; ...; X_{P-1}] and
+ *     Y = concat_r(X_r) . W,      X_r: [m, k],  W: [k, n],  Y: [P*m, n].
+ * rows: global row indices of Y to compute (NULL -> all P*m rows, in order);
+ * y: [nrows, n] doubles. */
+ORC_EXPORT int orc_ag_gemm(int P, int64_t m, int64_t k, int64_t n,
+                           const uint16_t *const *x, const uint16_t *w,
+                           const int64_t *rows, int64_t nrows, double *y) {
+    if (!rows) nrows = (int64_t)P * m;
+    double *wd = (double *)malloc(sizeof(double) * (size_t)(k * n));
+    if (!wd) return 2;
+    for (int64_t i = 0; i < k * n; i++) wd[i] = orc_bf16_to_f64(w[i]);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < nrows; t++) {
+        int64_t g = rows ? rows[t] : t;
+        if (g < 0 || g >= (int64_t)P * m) { bad = 1; continue; }
+        int64_t r = g / m, i = g % m;
+        const uint16_t *xr = x[r] + i * k;
+        double *acc = y + t * n;
+        for (int64_t j = 0; j < n; j++) acc[j] = 0.0;
+        for (int64_t kk = 0; kk < k; kk++) {
+            double a = orc_bf16_to_f64(xr[kk]);
+            const double *wrow = wd + kk * n;
+            for (int64_t j = 0; j < n; j++) acc[j] += a * wrow[j];
+        }
+    }
+    free(wd);
+    return bad ? 1 : 0;
+}
+
+/* The MXFP8 variant [abstract: "1.10-1.25x in MXFP8"]: the same product on the
+ * dequantised operands, X_q[i][kk] = e4m3(qx) * 2^(sx[i][kk/32] - 127) and
+ * W_q[kk][j] = e4m3(qw) * 2^(sw[j][kk/32] - 127), both exact in double.
+ * Scale layouts: sx_r [m, k/32], sw [n, k/32]. */
+ORC_EXPORT int orc_ag_gemm_mxfp8(int P, int64_t m, int64_t k, int64_t n,
+                                 const uint8_t *const *qx, const uint8_t *const *sx,
+                                 const uint8_t *qw, const uint8_t *sw,
+                                 const int64_t *rows, int64_t nrows, double *y) {
+    if (k % 32) return 1;
+    if (!rows) nrows = (int64_t)P * m;
+    int64_t kb = k / 32;
+    double *wd = (double *)malloc(sizeof(double) * (size_t)(k * n));
+    if (!wd) return 2;
+    for (int64_t kk = 0; kk < k; kk++)
+        for (int64_t j = 0; j < n; j++)
+            wd[kk * n + j] = ldexp(orc_e4m3_to_f64(qw[kk * n + j]), (int)sw[j * kb + kk / 32] - 127);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < nrows; t++) {
+        int64_t g = rows ? rows[t] : t;
+        if (g < 0 || g >= (int64_t)P * m) { bad = 1; continue; }
+        int64_t r = g / m, i = g % m;
+        double *acc = y + t * n;
+        for (int64_t j = 0; j < n; j++) acc[j] = 0.0;
+        for (int64_t kk = 0; kk < k; kk++) {
+            double a = ldexp(orc_e4m3_to_f64(qx[r][i * k + kk]), (int)sx[r][i * kb + kk / 32] - 127);
+            const double *wrow = wd + kk * n;
+            for (int64_t j = 0; j < n; j++) acc[j] += a * wrow[j];
+        }
+    }
+    free(wd);
+    return bad ? 1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* GEMM + reduce-scatter                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* [explainer, "Start with the problem"]: after the multiplication each rank
+ * holds a partial result; the partials are scattered and added.  With rank r
+ * holding X_r [m, k] and W_r [k, n]:
+ *     Y = sum_{r=0..P-1} X_r . W_r   (summed in rank order),
+ * and rank c receives chunk c = rows [c*m/P, (c+1)*m/P) of Y.
+ * rows: global rows of Y (NULL -> all m); y: [nrows, n]. */
+ORC_EXPORT int orc_gemm_rs(int P, int64_t m, int64_t k, int64_t n,
+                           const uint16_t *const *x, const uint16_t *const *w,
+                           const int64_t *rows, int64_t nrows, double *y) {
+    if (!rows) nrows = m;
+    double *wd = (double *)malloc(sizeof(double) * (size_t)(P * k * n));
+    if (!wd) return 2;
+    for (int r = 0; r < P; r++)
+        for (int64_t i = 0; i < k * n; i++) wd[(int64_t)r * k * n + i] = orc_bf16_to_f64(w[r][i]);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *part = (double *)malloc(sizeof(double) * (size_t)n);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < nrows; t++) {
+            int64_t g = rows ? rows[t] : t;
+            if (g < 0 || g >= m || !part) { bad = 1; continue; }
+            double *acc = y + t * n;
+            for (int64_t j = 0; j < n; j++) acc[j] = 0.0;
+            for (int r = 0; r < P; r++) {
+                const uint16_t *xr = x[r] + g * k;
+                for (int64_t j = 0; j < n; j++) part[j] = 0.0;
+                for (int64_t kk = 0; kk < k; kk++) {
+                    double a = orc_bf16_to_f64(xr[kk]);
+                    const double *wrow = wd + (int64_t)r * k * n + kk * n;
+                    for (int64_t j = 0; j < n; j++) part[j] += a * wrow[j];
+                }
+                for (int64_t j = 0; j < n; j++) acc[j] += part[j];
+            }
+        }
+        free(part);
+    }
+    free(wd);
+    return bad ? 1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* MoE expert layer (forward)                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Top-k of one row of scores: the k largest values, emitted in descending
+ * order; equal values are ordered by the lower index first.  Selection on the
+ * logits equals selection on the softmax probabilities (softmax is strictly
+ * increasing in each logit). */
+static void orc_topk_row(int E, int K, const double *s, int32_t *idx) {
+    char *taken = (char *)calloc((size_t)E, 1);
+    for (int kk = 0; kk < K; kk++) {
+        int best = -1;
+        for (int e = 0; e < E; e++) {
+            if (taken[e]) continue;
+            if (best < 0 || s[e] > s[best]) best = e;   /* strict: ties keep the lower index */
+        }
+        idx[kk] = best;
+        taken[best] = 1;
+    }
+    free(taken);
+}
+
+/* Top-k over float32 scores (used to check the kernel's index decisions in
+ * the kernel's own precision: the comparison of two floats is exact in
+ * double). */
+ORC_EXPORT int orc_topk_f32(int64_t T, int E, int K, const float *scores, int32_t *idx) {
+    if (K < 1 || K > E) return 1;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)E);
+#pragma omp for
+        for (int64_t t = 0; t < T; t++) {
+            for (int e = 0; e < E; e++) s[e] = (double)scores[t * E + e];
+            orc_topk_row(E, K, s, idx + t * K);
+        }
+        free(s);
+    }
+    return 0;
+}
+
+/* Expert-parallel dispatch tables [explainer, "Start with the problem": the
+ * all-to-all sends each token to the rank holding its expert].  Given the
+ * top-k indices:
+ *   counts[e]   = number of (t, k) slots routed to expert e;
+ *   offsets[e]  = exclusive prefix sum of counts in expert order (expert e of
+ *                 rank q = e / (E/P) is received contiguously, experts in
+ *                 ascending order, so rank q's receive buffer is a contiguous
+ *                 slice);
+ *   pos[t][k]   = offsets[e] + #{t' < t routed to e}  (receive order: expert
+ *                 ascending, then token ascending). */
+ORC_EXPORT int orc_moe_dispatch_tables(int64_t T, int E, int K, const int32_t *idx,
+                                       int32_t *counts, int32_t *offsets, int32_t *pos) {
+    for (int e = 0; e < E; e++) counts[e] = 0;
+    for (int64_t i = 0; i < T * K; i++) {
+        if (idx[i] < 0 || idx[i] >= E) return 1;
+        counts[idx[i]]++;
+    }
+    int32_t run = 0;
+    for (int e = 0; e < E; e++) { offsets[e] = run; run += counts[e]; }
+    int32_t *seen = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (int64_t t = 0; t < T; t++)
+        for (int kk = 0; kk < K; kk++) {
+            int e = idx[t * K + kk];
+            pos[t * K + kk] = offsets[e] + seen[e]++;
+        }
+    free(seen);
+    return 0;
+}
+
+/* Router [abstract: "an entire expert layer, from router to fold"]:
+ *   logits = X . W_router                  (fp64)
+ *   p      = softmax(logits) over experts  (fp64)
+ *   idx    = top-K of the logits (ties to the lower expert index), emitted in
+ *            descending order
+ *   gate_k = p[idx_k] / sum_{j<K} p[idx_j]  (renormalised over the top-K)
+ * followed by the dispatch tables above. */
+ORC_EXPORT int orc_moe_route(int64_t T, int64_t H, int E, int K,
+                             const uint16_t *x, const uint16_t *wr,
+                             double *logits, int32_t *idx, double *gate,
+                             int32_t *counts, int32_t *offsets, int32_t *pos) {
+    if (K < 1 || K > E) return 1;
+    double *wd = (double *)malloc(sizeof(double) * (size_t)(H * E));
+    if (!wd) return 2;
+    for (int64_t i = 0; i < H * E; i++) wd[i] = orc_bf16_to_f64(wr[i]);
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)E);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < T; t++) {
+            double *l = logits + t * E;
+            for (int e = 0; e < E; e++) l[e] = 0.0;
+            for (int64_t h = 0; h < H; h++) {
+                double a = orc_bf16_to_f64(x[t * H + h]);
+                for (int e = 0; e < E; e++) l[e] += a * wd[h * E + e];
+            }
+            double mx = l[0];
+            for (int e = 1; e < E; e++) if (l[e] > mx) mx = l[e];
+            double z = 0.0;
+            for (int e = 0; e < E; e++) { p[e] = exp(l[e] - mx); z += p[e]; }
+            for (int e = 0; e < E; e++) p[e] /= z;
+            orc_topk_row(E, K, l, idx + t * K);
+            double zs = 0.0;
+            for (int kk = 0; kk < K; kk++) zs += p[idx[t * K + kk]];
+            for (int kk = 0; kk < K; kk++) gate[t * K + kk] = p[idx[t * K + kk]] / zs;
+        }
+        free(p);
+    }
+    free(wd);
+    return orc_moe_dispatch_tables(T, E, K, idx, counts, offsets, pos);
+}
+
+/* SwiGLU expert, gate input first: silu(a) = a / (1 + exp(-a)). */
+static double orc_silu(double a) { return a / (1.0 + exp(-a)); }
+
+/* Expert computation and gate-weighted combine ("fold") for selected tokens:
+ *   out[t] = sum_{k<K} gate[t][k] * ( silu(x_t W_g[e]) * (x_t W_u[e]) ) W_d[e],
+ *            e = idx[t][k], summed in k order.
+ * Weights per EP rank q (experts q*Eq .. q*Eq+Eq-1):
+ *   wg[q], wu[q]: [Eq, H, I];  wd[q]: [Eq, I, H].
+ * identity != 0 replaces every expert by the identity map (out[t] = x_t *
+ * sum_k gate[t][k]), the check named by the method's description.
+ * tokens: token indices (NULL -> all T); out: [ntok, H]. */
+ORC_EXPORT int orc_moe_experts(int64_t T, int64_t H, int E, int K, int64_t I, int P,
+                               const uint16_t *x, const int32_t *idx, const double *gate,
+                               const uint16_t *const *wg, const uint16_t *const *wu,
+                               const uint16_t *const *wd, int identity,
+                               const int64_t *tokens, int64_t ntok, double *out) {
+    if (E % P) return 1;
+    int Eq = E / P;
+    if (!tokens) ntok = T;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *u = (double *)malloc(sizeof(double) * (size_t)I);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t s = 0; s < ntok; s++) {
+            int64_t t = tokens ? tokens[s] : s;
+            if (t < 0 || t >= T) { bad = 1; continue; }
+            double *o = out + s * H;
+            for (int64_t h = 0; h < H; h++) { xt[h] = orc_bf16_to_f64(x[t * H + h]); o[h] = 0.0; }
+            for (int kk = 0; kk < K; kk++) {
+                int e = idx[t * K + kk];
+                double gk = gate[t * K + kk];
+                if (identity) {
+                    for (int64_t h = 0; h < H; h++) o[h] += gk * xt[h];
+                    continue;
+                }
+                int q = e / Eq, le = e % Eq;
+                const uint16_t *Wg = wg[q] + (int64_t)le * H * I;
+                const uint16_t *Wu = wu[q] + (int64_t)le * H * I;
+                const uint16_t *Wd = wd[q] + (int64_t)le * I * H;
+                for (int64_t i = 0; i < I; i++) { g[i] = 0.0; u[i] = 0.0; }
+                for (int64_t h = 0; h < H; h++) {
+                    double a = xt[h];
+                    for (int64_t i = 0; i < I; i++) {
+                        g[i] += a * orc_bf16_to_f64(Wg[h * I + i]);
+                        u[i] += a * orc_bf16_to_f64(Wu[h * I + i]);
+                    }
+                }
+                for (int64_t hh = 0; hh < H; hh++) y[hh] = 0.0;
+                for (int64_t i = 0; i < I; i++) {
+                    double hv = orc_silu(g[i]) * u[i];
+                    for (int64_t hh = 0; hh < H; hh++) y[hh] += hv * orc_bf16_to_f64(Wd[i * H + hh]);
+                }
+                for (int64_t hh = 0; hh < H; hh++) o[hh] += gk * y[hh];
+            }
+        }
+        free(xt); free(g); free(u); free(y);
+    }
+    return bad ? 1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Work rails ("the order of the rail is the schedule")                      */
+/* ------------------------------------------------------------------------ */
+/* [explainer, "Role switching only works"]: data is produced in the order its
+ * consumers claim it.  Entries are written as 4 int32 fields
+ * {kind, a, b, c}; kinds: 1 TRANSFER(shard, piece), 2 TILE, 3 REDUCE.
+ * Tile and piece heights are R rows; output tiles are BN columns wide. */
+
+enum { ORC_TRANSFER = 1, ORC_TILE = 2, ORC_REDUCE = 3 };
+
+static int64_t orc_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+/* All-gather rails.
+ * Transfer rail: remote shards s = 1..P-1 in the order the multiplication
+ * consumes them, each cut into pieces j of R rows; then the local shard's own
+ * pieces (copied into the gathered buffer; nothing waits on them).
+ * Tile rail: output tiles TILE(shard, tile-row, tile-col), row-major over tile
+ * rows with the local shard (s = 0) first, then s = 1, 2, ...
+ * Returns the number of entries written (transfer rail then tile rail), or
+ * the count only when out == NULL. */
+ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN,
+                               int32_t *transfer_out, int64_t *n_transfer,
+                               int32_t *tile_out, int64_t *n_tile) {
+    int64_t pieces = orc_cdiv(m, R), tn = orc_cdiv(n, BN);
+    int64_t nt = 0, nb = 0;
+    for (int s = 1; s <= P; s++) {
+        int shard = (s == P) ? 0 : s;
+        for (int64_t j = 0; j < pieces; j++) {
+            if (transfer_out) {
+                int32_t *e = transfer_out + 4 * nt;
+                e[0] = ORC_TRANSFER; e[1] = shard; e[2] = (int32_t)j; e[3] = 0;
+            }
+            nt++;
+        }
+    }
+    for (int s = 0; s < P; s++)
+        for (int64_t i = 0; i < pieces; i++)
+            for (int64_t c = 0; c < tn; c++) {
+                if (tile_out) {
+                    int32_t *e = tile_out + 4 * nb;
+                    e[0] = ORC_TILE; e[1] = s; e[2] = (int32_t)i; e[3] = (int32_t)c;
+                }
+                nb++;
+            }
+    if (n_transfer) *n_transfer = nt;
+    if (n_tile) *n_tile = nb;
+    return nt + nb;
+}
+
+/* Reduce-scatter rails for one rank r.
+ * Tile rail of rank r: TILE(chunk c, band b, column tile j) over the whole
+ * [m, n] partial of rank r.
+ *   band order (order = 0): band b outermost, then chunk c, then j
+ *     [explainer, "Role switching only works": output produced band by band
+ *     across every rank's chunk];
+ *   row order  (order = 1): chunk c, then band b, then j (global row order).
+ * Reduce rail of rank r: REDUCE(c = r, band b, column tile j), b outer, j inner.
+ * Bands are R rows of a chunk of m/P rows. */
+ORC_EXPORT int64_t orc_rail_rs(int P, int64_t m, int64_t n, int R, int BN, int order, int rank,
+                               int32_t *tile_out, int64_t *n_tile,
+                               int32_t *reduce_out, int64_t *n_reduce) {
+    (void)rank;
+    if (m % P) return -1;
+    int64_t mc = m / P, bands = orc_cdiv(mc, R), tn = orc_cdiv(n, BN);
+    int64_t nb = 0, nr = 0;
+    if (order == 0) {
+        for (int64_t b = 0; b < bands; b++)
+            for (int c = 0; c < P; c++)
+                for (int64_t j = 0; j < tn; j++) {
+                    if (tile_out) {
+                        int32_t *e = tile_out + 4 * nb;
+                        e[0] = ORC_TILE; e[1] = c; e[2] = (int32_t)b; e[3] = (int32_t)j;
+                    }
+                    nb++;
+                }
+    } else {
+        for (int c = 0; c < P; c++)
+            for (int64_t b = 0; b < bands; b++)
+                for (int64_t j = 0; j < tn; j++) {
+                    if (tile_out) {
+                        int32_t *e = tile_out + 4 * nb;
+                        e[0] = ORC_TILE; e[1] = c; e[2] = (int32_t)b; e[3] = (int32_t)j;
+                    }
+                    nb++;
+                }
+    }
+    for (int64_t b = 0; b < bands; b++)
+        for (int64_t j = 0; j < tn; j++) {
+            if (reduce_out) {
+                int32_t *e = reduce_out + 4 * nr;
+                e[0] = ORC_REDUCE; e[1] = rank; e[2] = (int32_t)b; e[3] = (int32_t)j;
+            }
+            nr++;
+        }
+    if (n_tile) *n_tile = nb;
+    if (n_reduce) *n_reduce = nr;
+    return nb + nr;
+}
+
+/* Number of OpenMP threads the oracle runs with. */
+ORC_EXPORT int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,144 @@
+"""Pins for the oracle's MoE layer: top-k (brute force over subsets, ties),
+dispatch tables (definitions, bijection), router (numpy softmax), identity
+experts (out = token * sum of gates) and the E = P = 1, top-1 reduction to a
+dense SwiGLU MLP."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from kosmos_inputs import bf16_bits, moe_inputs
+
+
+def _order_key(vals, e):
+    # larger value first, equal values: lower index first
+    return (-vals[e], e)
+
+
+def _brute_topk(vals, K):
+    E = len(vals)
+    winners = []
+    for S in itertools.combinations(range(E), K):
+        rest = [e for e in range(E) if e not in S]
+        if all(_order_key(vals, a) < _order_key(vals, b) for a in S for b in rest):
+            winners.append(S)
+    assert len(winners) == 1
+    return sorted(winners[0], key=lambda e: _order_key(vals, e))
+
+
+def test_topk_bruteforce_with_ties(orc):
+    rng = np.random.default_rng(0)
+    for trial in range(200):
+        E = int(rng.integers(2, 11))
+        K = int(rng.integers(1, E + 1))
+        vals = rng.integers(-3, 4, size=E).astype(np.float32)  # many ties
+        got = orc.topk_f32(vals[None, :], K)[0]
+        assert list(got) == _brute_topk(vals, K), (vals, K)
+
+
+def test_topk_hand_ties(orc):
+    s = np.array([[1.0, 2.0, 2.0, 0.5, 2.0]], dtype=np.float32)
+    assert list(orc.topk_f32(s, 2)[0]) == [1, 2]
+    assert list(orc.topk_f32(s, 4)[0]) == [1, 2, 4, 0]
+    s = np.zeros((1, 6), dtype=np.float32)
+    assert list(orc.topk_f32(s, 3)[0]) == [0, 1, 2]
+
+
+def test_dispatch_tables_definition(orc):
+    rng = np.random.default_rng(1)
+    T, E, K = 50, 12, 3
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    counts, offsets, pos = orc.moe_dispatch_tables(idx, E)
+    assert counts.sum() == T * K
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+    assert offsets[0] == 0 and np.array_equal(offsets[1:], np.cumsum(counts)[:-1])
+    # bijection onto 0..T*K-1
+    assert np.array_equal(np.sort(pos.ravel()), np.arange(T * K))
+    # receive order: expert ascending, then token ascending
+    order = sorted(((int(idx[t, k]), t, k) for t in range(T) for k in range(K)))
+    for p, (e, t, k) in enumerate(order):
+        assert pos[t, k] == p
+
+
+def test_dispatch_tables_empty_expert(orc):
+    idx = np.array([[0, 2], [2, 0], [0, 2]], dtype=np.int32)
+    counts, offsets, pos = orc.moe_dispatch_tables(idx, 4)
+    assert list(counts) == [3, 0, 3, 0]
+    assert list(offsets) == [0, 3, 3, 6]
+    assert pos.tolist() == [[0, 3], [4, 1], [2, 5]]
+
+
+def _small_moe(T=24, H=32, E=8, I=16, seed=42):
+    return moe_inputs(T=T, H=H, E=E, I=I, seed=seed)
+
+
+def test_route_vs_numpy(orc):
+    inp = _small_moe()
+    K = 3
+    r = orc.moe_route(bf16_bits(inp["x"]), bf16_bits(inp["w_router"]), K)
+    X = inp["x"].double().numpy()
+    Wr = inp["w_router"].double().numpy()
+    L = X @ Wr
+    np.testing.assert_allclose(r["logits"], L, rtol=1e-12, atol=1e-12)
+    p = np.exp(L - L.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    for t in range(L.shape[0]):
+        order = sorted(range(L.shape[1]), key=lambda e: (-L[t, e], e))[:K]
+        assert list(r["idx"][t]) == order
+        g = p[t, order] / p[t, order].sum()
+        np.testing.assert_allclose(r["gate"][t], g, rtol=1e-12)
+    np.testing.assert_allclose(r["gate"].sum(axis=1), 1.0, rtol=1e-13)
+    assert r["counts"].sum() == L.shape[0] * K
+
+
+def _split_ranks(w, P):
+    E = w.shape[0]
+    return [bf16_bits(w[q * (E // P):(q + 1) * (E // P)]) for q in range(P)]
+
+
+def test_identity_experts_return_token_times_gate_sum(orc):
+    inp = _small_moe()
+    K, P, E = 3, 2, 8
+    x = bf16_bits(inp["x"])
+    r = orc.moe_route(x, bf16_bits(inp["w_router"]), K)
+    out = orc.moe_experts(x, r["idx"], r["gate"], _split_ranks(inp["w_gate"], P),
+                          _split_ranks(inp["w_up"], P), _split_ranks(inp["w_down"], P),
+                          E=E, identity=True)
+    X = inp["x"].double().numpy()
+    np.testing.assert_allclose(out, X * r["gate"].sum(axis=1, keepdims=True), rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(out, X, rtol=1e-13, atol=1e-13)
+
+
+def test_single_expert_top1_is_dense_swiglu(orc):
+    T, H, I = 10, 24, 20
+    inp = moe_inputs(T=T, H=H, E=1, I=I, seed=3)
+    x = bf16_bits(inp["x"])
+    r = orc.moe_route(x, bf16_bits(inp["w_router"]), 1)
+    assert np.all(r["idx"] == 0) and np.allclose(r["gate"], 1.0)
+    out = orc.moe_experts(x, r["idx"], r["gate"], [bf16_bits(inp["w_gate"])],
+                          [bf16_bits(inp["w_up"])], [bf16_bits(inp["w_down"])], E=1)
+    X = torch.from_numpy(inp["x"].double().numpy())
+    g = X @ inp["w_gate"][0].double()
+    u = X @ inp["w_up"][0].double()
+    ref = (torch.nn.functional.silu(g) * u) @ inp["w_down"][0].double()
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_experts_vs_numpy_per_token(orc):
+    inp = _small_moe(T=12, H=16, E=4, I=8, seed=8)
+    K, P, E = 2, 2, 4
+    x = bf16_bits(inp["x"])
+    r = orc.moe_route(x, bf16_bits(inp["w_router"]), K)
+    tokens = np.array([0, 5, 11], dtype=np.int64)
+    out = orc.moe_experts(x, r["idx"], r["gate"], _split_ranks(inp["w_gate"], P),
+                          _split_ranks(inp["w_up"], P), _split_ranks(inp["w_down"], P),
+                          E=E, tokens=tokens)
+    X = inp["x"].double()
+    for s, t in enumerate(tokens):
+        acc = torch.zeros(X.shape[1], dtype=torch.float64)
+        for kk in range(K):
+            e = int(r["idx"][t, kk])
+            h = torch.nn.functional.silu(X[t] @ inp["w_gate"][e].double()) * (X[t] @ inp["w_up"][e].double())
+            acc += r["gate"][t, kk] * (h @ inp["w_down"][e].double())
+        np.testing.assert_allclose(out[s], acc.numpy(), rtol=1e-11, atol=1e-12)

@@ -1,0 +1,65 @@
+"""Pins for the oracle's rails: every entry appears exactly once, and the
+order follows consumer demand (the explainer's queue-order paragraph):
+  * AG: remote transfers are ordered by the first tile that consumes them, the
+    local shard's tiles come first, and no tile's input is transferred after a
+    later tile's input;
+  * RS band order: every rank finishes band b of every chunk before band b+1;
+    row order finishes chunk c before chunk c+1."""
+import numpy as np
+import pytest
+
+
+@pytest.mark.parametrize("P,m,n", [(2, 64, 128), (8, 1024, 3584), (3, 320, 200)])
+def test_ag_rail_exactly_once_and_demand_order(orc, P, m, n):
+    R, BN = 128, 256
+    tr, tl = orc.rail_ag(P, m, n, R=R, BN=BN)
+    pieces = -(-m // R)
+    tn = -(-n // BN)
+    assert len(tr) == P * pieces
+    assert len({tuple(e) for e in tr}) == len(tr)
+    assert len(tl) == P * pieces * tn
+    assert len({tuple(e) for e in tl}) == len(tl)
+    assert np.all(tr[:, 0] == 1) and np.all(tl[:, 0] == 2)
+    # local shard tiles first
+    assert np.all(tl[: pieces * tn, 1] == 0)
+    # first consumer ticket of each remote transfer is non-decreasing along the rail
+    first = {}
+    for t, (_, s, i, c) in enumerate(tl):
+        first.setdefault((int(s), int(i)), t)
+    remote = [(int(s), int(j)) for (_, s, j, _) in tr if s != 0]
+    cons = [first[x] for x in remote]
+    assert cons == sorted(cons)
+    # the local shard's own copies come last (nothing waits on them)
+    assert all(int(s) == 0 for (_, s, _, _) in tr[len(remote):])
+
+
+@pytest.mark.parametrize("order", [0, 1])
+def test_rs_rails(orc, order):
+    P, m, n = 8, 8192, 8192
+    R, BN = 128, 256
+    bands = (m // P) // R
+    tn = n // BN
+    done_band = []
+    for r in range(P):
+        tl, rd = orc.rail_rs(P, m, n, rank=r, order=order, R=R, BN=BN)
+        assert len(tl) == P * bands * tn and len({tuple(e) for e in tl}) == len(tl)
+        assert len(rd) == bands * tn and len({tuple(e) for e in rd}) == len(rd)
+        assert np.all(rd[:, 1] == r)
+        # reducer rail follows the order in which its chunk's tiles complete
+        pos = {(int(c), int(b), int(j)): t for t, (_, c, b, j) in enumerate(tl)}
+        mine = [pos[(r, int(b), int(j))] for (_, _, b, j) in rd]
+        assert mine == sorted(mine)
+        if order == 0:
+            # band-major: all chunks' band b before any band b+1
+            assert list(tl[:, 2]) == sorted(tl[:, 2])
+            done_band.append(pos[(r, 0, tn - 1)])
+        else:
+            assert list(tl[:, 1]) == sorted(tl[:, 1])
+    if order == 0:
+        # every rank's first band completes within the first P*tn tickets
+        assert max(done_band) < P * tn
+
+
+def test_rs_rail_rejects_indivisible(orc):
+    with pytest.raises(ValueError):
+        orc.rail_rs(3, 100, 256, rank=0, order=0)
