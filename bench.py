@@ -1,0 +1,339 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused all-gather + GEMM persistent kernel (KOSMOS method)
+on the 8-rank workload X_r [1024, 8192] x 8, W [8192, 3584] (bf16, fp32
+accumulate), with the fixed-split and unfused baselines, the GEMM+RS and MoE
+kernels when built, the CPU oracle timed on the host cores, and the
+roofline of the dominant kernel.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line (rank 0).  N > 1 (under torchrun) runs N independent
+replicas, one per GPU: the emulated ranks live in one GPU's HBM, so nothing
+shards across GPUs ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "ag_bf16_p8"
+METRIC = "Fused AG/RS-GEMM TFLOP/s & % BF16 tensor peak on 1 GB300; MoE layer tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) of one ag_gemm_kernel launch on the 8-rank AG
+# workload, from an ncu capture; valid only while the kernel sources hash to
+# src_sha (otherwise the bench reports traffic = null).
+TRAFFIC_CAPTURE = {"bytes": None, "src_sha": None}
+KERNEL_SOURCES = ["comm_persistent_gemm_gb300/csrc/ag_gemm.cu", "comm_persistent_gemm_gb300/csrc/engine.cuh",
+                  "comm_persistent_gemm_gb300/csrc/ptx.cuh", "comm_persistent_gemm_gb300/csrc/common.cuh"]
+
+
+def kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kosmos_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        busy = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def time_oracle_ag(inp, target_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of output rows of the
+    AG workload; returns TFLOP/s on the host cores."""
+    import numpy as np
+    import oracle
+    from kosmos_inputs import bf16_bits
+    oracle.build()
+    xs = [bf16_bits(x) for x in inp["x"]]
+    w = bf16_bits(inp["w"])
+    P = len(xs)
+    m, k = xs[0].shape
+    n = w.shape[1]
+    rows = np.arange(0, P * m, max(1, (P * m) // 32), dtype=np.int64)[:32]
+    t0 = time.perf_counter()
+    oracle.ag_gemm(xs, w, rows=rows)
+    dt = time.perf_counter() - t0
+    want = int(min(P * m, max(32, len(rows) * target_s / max(dt, 1e-3))))
+    rows = np.linspace(0, P * m - 1, want).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.ag_gemm(xs, w, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * len(rows) * k * n
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} of {P * m} output rows of Y = concat(X_r) W (fp64, {dt:.1f} s)"}
+
+
+# --------------------------------------------------------------------------- GPU timing
+def time_kernel_steps(fn, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step
+    (outside the events)."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if ws > 1 and rank != 0:
+        return 0
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS[WORKLOAD]
+    inp = workload_inputs(w)
+    vals = []
+    info = None
+    for _ in range(args.warmup):
+        time_oracle_ag(inp, target_s=2.0)
+    for _ in range(args.steps):
+        info = time_oracle_ag(inp, target_s=max(2.0, 60.0 / max(args.steps, 1)))
+        vals.append(info["value"])
+    v = statistics.mean(vals)
+    tflop = w.flops() / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tflop / v * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,var) bf16)",
+            "config": {"workload": WORKLOAD, "P": w.P, "m_per_shard": w.m, "k": w.k, "n": w.n},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_kosmos(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import comm_persistent_gemm_gb300 as K
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    K.build()
+    w = WORKLOADS[WORKLOAD]
+    inp = workload_inputs(w)
+    P, m, k, n = w.P, w.m, w.k, w.n
+    xs = [x.to(dev) for x in inp["x"]]
+    W = inp["w"].to(dev)
+    xg = torch.empty(P * m, k, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(P * m, n, dtype=torch.bfloat16, device=dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def make(o):
+        wsb = K.workspace(K.OP_AG_GEMM, P, m, n, k, o=o, device=dev)
+        return (lambda: K.ag_gemm(xs, W, xg, y, wsb, o, stream=stream)), wsb
+
+    flops = w.flops()
+    sms = K.num_sms()
+    o_self = K.opts()
+    f_self, ws_self = make(o_self)
+    # warm up + correctness gate of the timed configuration
+    f_self()
+    K.check(ws_self, "ag_gemm")
+
+    # ---- timed region (the method), barrier + sync on both sides, max over ranks
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        times = time_kernel_steps(f_self, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    K.check(ws_self, "ag_gemm")
+    step_ms = statistics.mean(times)
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * flops / (step_ms * 1e-3) / 1e12
+    clocks = clk.summary()
+
+    # ---- baselines on the same inputs (not the headline)
+    base = {}
+    fixed = {}
+    for crew in sorted({max(1, sms // 16), max(1, sms // 8), max(1, sms // P), max(1, sms // 4)}):
+        f, wsb = make(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=crew))
+        tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
+        K.check(wsb, "ag_gemm fixed")
+        fixed[str(crew)] = flops / (statistics.mean(tt) * 1e-3) / 1e12
+    best_crew = max(fixed, key=fixed.get)
+    base["fixed_split_best"] = {"tflops": fixed[best_crew], "crew": int(best_crew), "sweep": fixed}
+    f, wsb = make(K.opts(sched=K.SCHED_UNFUSED))
+    tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
+    K.check(wsb, "ag_gemm unfused")
+    base["unfused"] = {"tflops": flops / (statistics.mean(tt) * 1e-3) / 1e12,
+                       "launches_per_step": 2}
+    sweep = {}
+    for nc in sorted({max(1, sms // 16), max(1, sms // 8), max(1, sms // 4)}):
+        f, wsb = make(K.opts(n_comm0=nc))
+        tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
+        K.check(wsb, "ag_gemm n_comm0")
+        sweep[str(nc)] = flops / (statistics.mean(tt) * 1e-3) / 1e12
+    base["self_n_comm0_sweep"] = sweep
+
+    # ---- e2e through the C ABI with host buffers (pinned), copies inside the timed region
+    hx = [x.pin_memory() for x in inp["x"]]
+    hy = torch.empty(P * m, n, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(x.numel() * 2 for x in hx)
+    d2h = hy.numel() * 2
+
+    def e2e_step():
+        for i in range(P):
+            xs[i].copy_(hx[i], non_blocking=True)
+        f_self()
+        hy.copy_(y, non_blocking=True)
+
+    et = time_kernel_steps(e2e_step, args.steps, args.warmup, flush, stream)
+    K.check(ws_self, "ag_gemm e2e")
+    e2e_ms = statistics.mean(et)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    peaks, src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    achieved = flops / (step_ms * 1e-3) / 1e12
+    traffic = TRAFFIC_CAPTURE["bytes"] if TRAFFIC_CAPTURE["src_sha"] == kernel_src_sha() else None
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": traffic, "peak_source": f"{src} bf16 dense (burst)", "kernel": "ag_gemm_kernel",
+            "flop_per_launch": flops}
+
+    line = None
+    if rank == 0:
+        cpu = time_oracle_ag(inp) if world == 1 else None
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,var) bf16)",
+                "config": {"workload": WORKLOAD, "P": P, "m_per_shard": m, "k": k, "n": n, "sched": "self",
+                           "n_comm0": "ceil(S/P)", "sms": sms, "l2": "flushed (256 MiB write) before every step"},
+                "frac_of_peak": achieved / peak,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "gpu_launches": args.steps, "baselines": base,
+                "vs_fixed_split_best": value / world / base["fixed_split_best"]["tflops"],
+                "vs_unfused": value / world / base["unfused"]["tflops"]}
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kosmos", choices=["kosmos", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_kosmos(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,268 @@
+"""Python binding of libkosmos.so (C ABI in include/kosmos.h).
+
+Argument marshalling only: every step of the fused operators runs in the
+CUDA kernels of the library.  Tensors are torch CUDA tensors (PyTorch supplies
+device memory and streams).  There is no fallback: if the library is missing
+or a call fails, a KosmosError is raised.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import List, Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkosmos.so")
+
+KOSMOS_MAX_P = 8
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(7)
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT",
+                6: "DEVICE"}
+BF16, MXFP8_E4M3 = 0, 1
+OP_AG_GEMM, OP_GEMM_RS, OP_MOE_FWD = 0, 1, 2
+SCHED_SELF, SCHED_FIXED, SCHED_UNFUSED = 0, 1, 2
+ORDER_BAND, ORDER_ROW = 0, 1
+INJECT_DROP_TRANSFER = 0x1
+INJECT_DROP_PARTIAL = 0x2
+KIND_NAMES = {1: "TRANSFER", 2: "TILE", 3: "REDUCE", 4: "ROUTE", 5: "DISPATCH", 6: "TILE_GU", 7: "TILE_D",
+              8: "PUSH", 9: "FOLD"}
+
+EXPORTS = ["kosmos_default_opts", "kosmos_num_sms", "kosmos_workspace_bytes", "kosmos_workspace_init",
+           "kosmos_ag_gemm", "kosmos_gemm_rs", "kosmos_moe_fwd", "kosmos_mxfp8_quantize", "kosmos_status_sync",
+           "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device"]
+
+
+class KosmosError(RuntimeError):
+    def __init__(self, status: int, what: str, entry: int = -1):
+        self.status = status
+        self.entry = entry
+        super().__init__(f"{what}: KOSMOS_{STATUS_NAMES.get(status, status)}"
+                         + (f" (entry {entry})" if entry >= 0 else ""))
+
+
+class Opts(C.Structure):
+    _fields_ = [("sched", C.c_int32), ("n_comm0", C.c_int32), ("fixed_comm_ctas", C.c_int32),
+                ("order", C.c_int32), ("num_ctas", C.c_int32), ("trace", C.c_int32),
+                ("wait_limit_ns", C.c_uint64), ("inject", C.c_uint64)]
+
+
+class TraceRec(C.Structure):
+    _fields_ = [("t_claim", C.c_int64), ("t_ready", C.c_int64), ("t_done", C.c_int64),
+                ("kind", C.c_int32), ("ticket", C.c_int32), ("cta", C.c_int32), ("pad", C.c_int32)]
+
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    from . import buildlib as _b
+    return _b.build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with comm_persistent_gemm_gb300.build()")
+    L = C.CDLL(LIB_PATH)
+    vp, i64, i32 = C.c_void_p, C.c_int64, C.c_int
+    L.kosmos_default_opts.argtypes = [C.POINTER(Opts)]
+    L.kosmos_default_opts.restype = None
+    L.kosmos_num_sms.restype = i32
+    L.kosmos_workspace_bytes.argtypes = [i32, i32, i64, i64, i64, i32, C.POINTER(Opts)]
+    L.kosmos_workspace_bytes.restype = C.c_size_t
+    L.kosmos_workspace_init.argtypes = [vp, C.c_size_t, vp]
+    L.kosmos_workspace_init.restype = i32
+    L.kosmos_ag_gemm.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, i32, vp, vp, vp, C.c_size_t,
+                                 C.POINTER(Opts), vp]
+    L.kosmos_ag_gemm.restype = i32
+    L.kosmos_gemm_rs.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, C.c_size_t, C.POINTER(Opts), vp]
+    L.kosmos_gemm_rs.restype = i32
+    L.kosmos_moe_fwd.argtypes = [vp, vp, i32, i64, i64, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                 C.c_size_t, C.POINTER(Opts), vp]
+    L.kosmos_moe_fwd.restype = i32
+    L.kosmos_mxfp8_quantize.argtypes = [vp, i64, i64, i32, vp, vp, vp]
+    L.kosmos_mxfp8_quantize.restype = i32
+    L.kosmos_status_sync.argtypes = [vp, vp, C.POINTER(i64)]
+    L.kosmos_status_sync.restype = i32
+    L.kosmos_trace_info.argtypes = [i32, i32, i64, i64, i64, i32, C.POINTER(Opts), vp, C.POINTER(vp),
+                                    C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
+    L.kosmos_trace_info.restype = i32
+    L.kosmos_rail_decode.argtypes = [i32, i32, i64, i64, i32, i32, i32, vp, i64]
+    L.kosmos_rail_decode.restype = i64
+    L.kosmos_rail_decode_device.argtypes = [i32, i32, i64, i64, i32, i32, i32, vp, i64, vp]
+    L.kosmos_rail_decode_device.restype = i64
+    _lib = L
+    return L
+
+
+def opts(**kw) -> Opts:
+    o = Opts()
+    lib().kosmos_default_opts(C.byref(o))
+    for k, v in kw.items():
+        if v is None:
+            continue
+        if not hasattr(o, k):
+            raise TypeError(f"unknown option {k}")
+        setattr(o, k, int(v))
+    return o
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptrs(ts: Sequence) -> C.Array:
+    return (C.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("kosmos tensors must be contiguous CUDA tensors")
+
+
+def _raise(rc: int, what: str):
+    if rc != OK:
+        raise KosmosError(rc, what)
+
+
+def num_sms() -> int:
+    return int(lib().kosmos_num_sms())
+
+
+def workspace_bytes(op: int, P: int, m: int, n: int, k: int, dtype: int = BF16, o: Optional[Opts] = None) -> int:
+    return int(lib().kosmos_workspace_bytes(op, P, m, n, k, dtype, C.byref(o) if o is not None else None))
+
+
+def workspace(op: int, P: int, m: int, n: int, k: int, dtype: int = BF16, o: Optional[Opts] = None,
+              device=None):
+    """A zeroed workspace tensor (uint8) sized for this call."""
+    import torch
+    nbytes = workspace_bytes(op, P, m, n, k, dtype, o)
+    if nbytes == 0:
+        raise KosmosError(ERR_INVALID_ARG, "workspace_bytes")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def workspace_init(ws, stream=None):
+    _raise(lib().kosmos_workspace_init(ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "kosmos_workspace_init")
+
+
+def ag_gemm(x_shards: List, w, x_gathered, y, ws, o: Optional[Opts] = None, dtype: int = BF16,
+            x_scales: Optional[List] = None, w_scales=None, stream=None):
+    """Y = concat_r(x_shards[r]) @ w; x_gathered receives the concatenation."""
+    _check_cuda(*x_shards, w, x_gathered, y, ws, *(x_scales or []), w_scales)
+    P = len(x_shards)
+    m, k = x_shards[0].shape
+    n = w.shape[1]
+    xs = _ptrs(x_shards)
+    xsc = _ptrs(x_scales) if x_scales is not None else None
+    rc = lib().kosmos_ag_gemm(xs, xsc, P, m, k, n, w.data_ptr(),
+                              w_scales.data_ptr() if w_scales is not None else None, dtype,
+                              x_gathered.data_ptr(), y.data_ptr(), ws.data_ptr(), ws.numel(),
+                              C.byref(o) if o is not None else None, _stream(stream))
+    _raise(rc, "kosmos_ag_gemm")
+
+
+def gemm_rs(x_shards: List, w_shards: List, y_chunks: List, ws, o: Optional[Opts] = None, stream=None):
+    """y_chunks[c] = rows [c*m/P, (c+1)*m/P) of sum_r x_shards[r] @ w_shards[r]."""
+    _check_cuda(*x_shards, *w_shards, *y_chunks, ws)
+    P = len(x_shards)
+    m, k = x_shards[0].shape
+    n = w_shards[0].shape[1]
+    rc = lib().kosmos_gemm_rs(_ptrs(x_shards), _ptrs(w_shards), P, m, k, n, BF16, _ptrs(y_chunks),
+                              ws.data_ptr(), ws.numel(), C.byref(o) if o is not None else None, _stream(stream))
+    _raise(rc, "kosmos_gemm_rs")
+
+
+def moe_fwd(x_shards: List, w_router, w_gate: List, w_up: List, w_down: List, y_shards: List, topk_idx,
+            topk_gate, expert_counts, dispatch_pos, ws, topk: int, o: Optional[Opts] = None, stream=None):
+    _check_cuda(*x_shards, w_router, *w_gate, *w_up, *w_down, *y_shards, topk_idx, topk_gate, expert_counts,
+                dispatch_pos, ws)
+    P = len(x_shards)
+    tokens = x_shards[0].shape[0] * P
+    hidden = x_shards[0].shape[1]
+    E = w_router.shape[1]
+    inter = w_gate[0].shape[2]
+    rc = lib().kosmos_moe_fwd(_ptrs(x_shards), w_router.data_ptr(), P, tokens, hidden, E, topk, inter,
+                              _ptrs(w_gate), _ptrs(w_up), _ptrs(w_down), _ptrs(y_shards), topk_idx.data_ptr(),
+                              topk_gate.data_ptr(), expert_counts.data_ptr(), dispatch_pos.data_ptr(),
+                              ws.data_ptr(), ws.numel(), C.byref(o) if o is not None else None, _stream(stream))
+    _raise(rc, "kosmos_moe_fwd")
+
+
+def mxfp8_quantize(x, q, scales, along_cols: bool, stream=None):
+    _check_cuda(x, q, scales)
+    rows, cols = x.shape
+    rc = lib().kosmos_mxfp8_quantize(x.data_ptr(), rows, cols, 1 if along_cols else 0, q.data_ptr(),
+                                     scales.data_ptr(), _stream(stream))
+    _raise(rc, "kosmos_mxfp8_quantize")
+
+
+def status_sync(ws, stream=None):
+    """(status, failing_entry) of the last call that used ws (synchronises)."""
+    e = C.c_int64(-1)
+    rc = lib().kosmos_status_sync(ws.data_ptr(), _stream(stream), C.byref(e))
+    return int(rc), int(e.value)
+
+
+def check(ws, what: str = "kosmos", stream=None):
+    st, ent = status_sync(ws, stream)
+    if st != OK:
+        raise KosmosError(st, what, ent)
+
+
+def trace_records(op: int, P: int, m: int, n: int, k: int, ws, o: Opts):
+    """Copies the role trace out of the workspace: list of dicts, one per
+    recorded entry (CTA ring order)."""
+    import numpy as np
+    import torch
+    ptr = C.c_void_p()
+    cap = C.c_int32()
+    nct = C.c_int32()
+    rc = lib().kosmos_trace_info(op, P, m, n, k, BF16, C.byref(o), ws.data_ptr(), C.byref(ptr), C.byref(cap),
+                                 C.byref(nct))
+    _raise(rc, "kosmos_trace_info")
+    off = ptr.value - ws.data_ptr()
+    nbytes = nct.value * cap.value * C.sizeof(TraceRec)
+    raw = ws[off:off + nbytes].cpu().numpy()
+    dt = np.dtype([("t_claim", "<i8"), ("t_ready", "<i8"), ("t_done", "<i8"), ("kind", "<i4"),
+                   ("ticket", "<i4"), ("cta", "<i4"), ("pad", "<i4")])
+    recs = raw.view(dt).reshape(nct.value, cap.value)
+    return recs[recs["kind"] != 0]
+
+
+def rail_decode(op: int, P: int, m: int, n: int, rail: int, order: int = ORDER_BAND, rank: int = 0):
+    """Host-compiled decode of one rail: int32 array [len, 4]."""
+    import numpy as np
+    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, None, 0)
+    if ln < 0:
+        raise KosmosError(ERR_INVALID_ARG, "kosmos_rail_decode")
+    out = np.zeros((ln, 4), dtype=np.int32)
+    lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, out.ctypes.data, ln)
+    return out
+
+
+def rail_decode_device(op: int, P: int, m: int, n: int, rail: int, order: int = ORDER_BAND, rank: int = 0,
+                       stream=None):
+    import torch
+    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, None, 0)
+    if ln < 0:
+        raise KosmosError(ERR_INVALID_ARG, "kosmos_rail_decode")
+    out = torch.zeros((max(ln, 1), 4), dtype=torch.int32, device="cuda")
+    r = lib().kosmos_rail_decode_device(op, P, m, n, order, rank, rail, out.data_ptr(), ln, _stream(stream))
+    if r < 0:
+        raise KosmosError(ERR_CUDA, "kosmos_rail_decode_device")
+    torch.cuda.synchronize()
+    return out[:ln].cpu().numpy()

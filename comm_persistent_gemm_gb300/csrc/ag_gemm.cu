@@ -1,0 +1,298 @@
+// ag_gemm.cu -- all-gather + GEMM as one self-scheduling persistent launch.
+//
+// Y = concat_r(X_r) . W from rank 0's view (KOSMOS explainer, paragraph
+// "Start with the problem").  Two rails:
+//   transfer rail  TRANSFER(shard, piece): copy 128 rows of a remote shard
+//                  into the gathered buffer, then release that piece's flag;
+//                  remote shards in the order the tiles consume them, the
+//                  local shard's own copy last (explainer, "Role switching
+//                  only works");
+//   tile rail      TILE(shard, tile_row, tile_col), local shard first.
+// The first n_comm CTAs start as movers and become builders when the
+// transfer rail runs out (one-way, explainer "KOSMOS removes the manager");
+// the others are builders from the start.  A builder acquires the flag of
+// the piece its tile reads before loading it.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "engine.cuh"
+#include "launch.h"
+
+namespace kosmos {
+
+struct AgParams {
+    CUtensorMap tmA_local;  // x_shards[0]: dims {k, m}, box {64, 128}, 128B swizzle
+    CUtensorMap tmA_gath;   // x_gathered: dims {k, m, P}, box {64, 128, 1}, 128B swizzle
+    CUtensorMap tmB;        // W: dims {n, k}, box {64, 64}, 128B swizzle
+    const uint8_t *x_src[KOSMOS_MAX_P];
+    uint8_t *x_gath;
+    __nv_bfloat16 *y;
+    WsHeader *ws;
+    uint32_t *flags;
+    TraceRec *trace;
+    AgGeom g;
+    int nkb;
+    int sched;
+    int n_comm;
+    int pad;
+    uint64_t wait_limit_ns;
+    uint64_t inject;
+};
+
+// Mover: copy one piece (<= 128 rows of one shard, contiguous in both the
+// shard and the gathered buffer) through the four stage buffers with bulk
+// async copies, then release the piece's flag with value epoch + 1.
+__device__ __noinline__ bool ag_transfer(const AgParams &p, const Smem &sm, int t, uint32_t &cphase,
+                                         uint32_t epoch) {
+    int shard, piece;
+    ag_decode_transfer(p.g, t, shard, piece);
+    const int64_t row_bytes = p.g.k * 2;
+    const int64_t row0 = static_cast<int64_t>(piece) * PIECE_ROWS;
+    const int64_t rows = (p.g.m - row0 < PIECE_ROWS) ? (p.g.m - row0) : PIECE_ROWS;
+    const int64_t bytes = rows * row_bytes;
+    const uint8_t *src = p.x_src[shard] + row0 * row_bytes;
+    uint8_t *dst = p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes;
+    constexpr int64_t CH = STAGE_BYTES;
+    const int64_t nch = cdiv(bytes, CH);
+    auto chunk_bytes = [&](int64_t c) -> uint32_t {
+        const int64_t rem = bytes - c * CH;
+        return static_cast<uint32_t>(rem < CH ? rem : CH);
+    };
+    for (int64_t c = 0; c < nch && c < NSTAGE; ++c) {
+        mbar_arrive_expect_tx(&sm.cbar[c], chunk_bytes(c));
+        bulk_g2s(sm.stages + c * CH, src + c * CH, chunk_bytes(c), &sm.cbar[c]);
+    }
+    for (int64_t c = 0; c < nch; ++c) {
+        const int b = static_cast<int>(c % NSTAGE);
+        if (!mbar_wait(&sm.cbar[b], (cphase >> b) & 1u, PIPE_LIMIT_NS)) {
+            bulk_wait<0>();
+            set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+            return false;
+        }
+        cphase ^= (1u << b);
+        bulk_s2g(dst + c * CH, sm.stages + b * CH, chunk_bytes(c));
+        bulk_commit();
+        // refill the buffer of the previous chunk once its store has read it
+        const int64_t refill = c - 1 + NSTAGE;
+        if (c >= 1 && refill < nch) {
+            bulk_wait_read<1>();
+            const int rb = static_cast<int>((c - 1) % NSTAGE);
+            mbar_arrive_expect_tx(&sm.cbar[rb], chunk_bytes(refill));
+            bulk_g2s(sm.stages + rb * CH, src + refill * CH, chunk_bytes(refill), &sm.cbar[rb]);
+        }
+    }
+    bulk_wait<0>();
+    fence_proxy_async_global();
+    __threadfence();
+    const bool drop = (p.inject & KOSMOS_INJECT_DROP_TRANSFER) && static_cast<int64_t>(p.inject >> 32) == t;
+    if (!drop) st_release_gpu(&p.flags[shard * p.g.pieces + piece], epoch + 1u);
+    return true;
+}
+
+__device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, uint32_t epoch) {
+    const int cta = blockIdx.x;
+    bool mover = (p.sched != KOSMOS_SCHED_UNFUSED) && cta < p.n_comm;
+    uint32_t cphase = 0;
+    PipeState ps;
+    RingState rs;
+    int nrec = 0;
+    while (true) {
+        if (failed(p.ws)) break;
+        if (mover) {
+            const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
+            if (t < static_cast<uint32_t>(p.g.n_transfer)) {
+                const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+                if (!ag_transfer(p, sm, static_cast<int>(t), cphase, epoch)) break;
+                if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
+                    r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
+                    r->kind = K_TRANSFER; r->ticket = static_cast<int32_t>(t); r->cta = cta;
+                }
+                ++nrec;
+                continue;
+            }
+            if (p.sched == KOSMOS_SCHED_FIXED) break;  // a fixed crew never builds
+            mover = false;                             // one-way switch: mover -> builder
+        }
+        const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
+        if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
+        int s, i, c;
+        ag_decode_tile(p.g, static_cast<int>(t), s, i, c);
+        const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+        if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0) {
+            if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], epoch + 1u, p.wait_limit_ns, t)) break;
+        }
+        int slot = -1;
+        if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
+            r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
+            r->kind = K_TILE; r->ticket = static_cast<int32_t>(t); r->cta = cta;
+            slot = nrec;
+        }
+        ++nrec;
+        SchedEntry e;
+        e.kind = K_TILE; e.a = s; e.b = i; e.c = c; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
+        e.slot = slot; e.d = 0;
+        if (!ring_push(sm, rs, e, p.ws)) break;
+        const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+        bool ok = true;
+        for (int kb = 0; kb < p.nkb; ++kb) {
+            if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                ok = false;
+                break;
+            }
+            uint8_t *sa = sm.stages + ps.stage * STAGE_BYTES;
+            uint8_t *sb = sa + A_STAGE_BYTES;
+            uint64_t *bar = &sm.full[ps.stage];
+            mbar_arrive_expect_tx(bar, STAGE_BYTES);
+            if (local)
+                tma_load_2d(sa, &p.tmA_local, bar, kb * BK, i * BM);
+            else
+                tma_load_3d(sa, &p.tmA_gath, bar, kb * BK, i * BM, s);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sb + j * (64 * BK * 2), &p.tmB, bar, c * BN + j * 64, kb * BK);
+            ps.advance();
+        }
+        if (!ok) break;
+    }
+    SchedEntry done;
+    done.kind = K_DONE; done.a = done.b = done.c = 0; done.nstage = 0; done.ticket = -1; done.slot = -1; done.d = 0;
+    ring_push(sm, rs, done, p.ws);
+}
+
+__device__ __forceinline__ void ag_epilogue(const AgParams &p, const Smem &sm, uint32_t tmem_base, int warp,
+                                            int lane) {
+    const int grp = warp & 3;  // TMEM lane group this warp may access
+    const int row = grp * 32 + lane;
+    RingState rs;
+    uint32_t acc = 0, acc_phase = 0;
+    while (true) {
+        if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -6);
+            break;
+        }
+        const SchedEntry e = sm.sched[rs.idx];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sempty[rs.idx]);
+        rs.advance();
+        if (e.kind == K_DONE) break;
+        if (e.kind != K_TILE) continue;
+        if (!mbar_wait(&sm.tfull[acc], acc_phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
+            break;
+        }
+        tc_fence_after();
+        const int s = e.a, i = e.b, c = e.c;
+        const int64_t rloc = static_cast<int64_t>(i) * BM + row;
+        const bool valid = rloc < p.g.m;
+        __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + (valid ? rloc : 0)) * p.g.n;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+            const int64_t col0 = static_cast<int64_t>(c) * BN + ch * 32;
+            if (col0 >= p.g.n) break;
+            const int64_t left = p.g.n - col0;
+            tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (e.slot >= 0 && lane == 0 && grp == 0) {
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_kernel(const __grid_constant__ AgParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem sm = carve_smem(smem_raw);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&p.tmA_local);
+        prefetch_tmap(&p.tmA_gath);
+        prefetch_tmap(&p.tmB);
+    }
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
+    engine_setup(sm, warp);
+    const uint32_t tmem_base = *sm.tmem_slot;
+    if (warp == 0) {
+        if (lane == 0) ag_producer(p, sm, epoch);
+    } else if (warp == 1) {
+        if (lane == 0) mma_loop(sm, tmem_base, p.ws);
+    } else {
+        ag_epilogue(p, sm, tmem_base, warp, lane);
+    }
+    engine_teardown(sm, warp, tmem_base);
+    if (threadIdx.x == 0) engine_finish(p.ws, epoch, 2);
+}
+
+// Unfused baseline, first launch: gather every shard into x_gathered with
+// plain 16-byte vector copies over all SMs.
+__global__ void __launch_bounds__(256) ag_gather_copy_kernel(const AgParams p) {
+    const int64_t shard_bytes = p.g.m * p.g.k * 2;
+    const int64_t per = shard_bytes / 16;
+    const int64_t total = per * p.g.P;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += stride) {
+        const int64_t s = v / per;
+        const int64_t o = v - s * per;
+        const uint4 x = reinterpret_cast<const uint4 *>(p.x_src[s])[o];
+        reinterpret_cast<uint4 *>(p.x_gath + s * shard_bytes)[o] = x;
+    }
+}
+
+// ---------------------------------------------------------------- host launcher
+kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
+    AgParams p;
+    memset(&p, 0, sizeof(p));
+    p.g = ag_geom(L.P, L.m, L.k, L.n);
+    // tensor maps
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(L.k), static_cast<uint64_t>(L.m)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(L.k) * 2};
+        const uint32_t box[2] = {BK, BM};
+        if (!encode_tmap(&p.tmA_local, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(L.x[0]), dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(L.k), static_cast<uint64_t>(L.m), static_cast<uint64_t>(L.P)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(L.k) * 2, static_cast<uint64_t>(L.m * L.k) * 2};
+        const uint32_t box[3] = {BK, BM, 1};
+        if (!encode_tmap(&p.tmA_gath, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, L.x_gathered, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(L.n), static_cast<uint64_t>(L.k)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(L.n) * 2};
+        const uint32_t box[2] = {64, BK};
+        if (!encode_tmap(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(L.w), dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    for (int r = 0; r < L.P; ++r) p.x_src[r] = static_cast<const uint8_t *>(L.x[r]);
+    p.x_gath = static_cast<uint8_t *>(L.x_gathered);
+    p.y = static_cast<__nv_bfloat16 *>(L.y);
+    const AgWsLayout W = ag_ws_layout(p.g, L.trace != 0);
+    uint8_t *ws = static_cast<uint8_t *>(L.ws);
+    p.ws = reinterpret_cast<WsHeader *>(ws);
+    p.flags = reinterpret_cast<uint32_t *>(ws + W.flags_off);
+    p.trace = L.trace ? reinterpret_cast<TraceRec *>(ws + W.trace_off) : nullptr;
+    p.nkb = static_cast<int>(L.k / BK);
+    p.sched = L.sched;
+    p.n_comm = L.n_comm;
+    p.wait_limit_ns = L.wait_limit_ns;
+    p.inject = L.inject;
+
+    if (L.sched == KOSMOS_SCHED_UNFUSED) {
+        const int sms = L.grid;
+        ag_gather_copy_kernel<<<sms * 4, 256, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return KOSMOS_ERR_CUDA;
+    }
+    return launch_persistent(reinterpret_cast<const void *>(&ag_gemm_kernel), &p, L.grid, SMEM_BYTES, stream);
+}
+
+}  // namespace kosmos

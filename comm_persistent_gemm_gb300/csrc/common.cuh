@@ -1,0 +1,181 @@
+// common.cuh -- workspace layout, entry kinds, tile geometry and the rail
+// decode shared by the host library and the kernels.
+//
+// A rail is the ordered list of entries of one queue.  Entries are never
+// stored: a claimed ticket t is decoded arithmetically into its entry
+// ("the order of the rail is the schedule", KOSMOS explainer, paragraph
+// "Role switching only works").
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/kosmos.h"
+
+#ifdef __CUDACC__
+#define KOS_HD __host__ __device__ __forceinline__
+#else
+#define KOS_HD inline
+#endif
+
+namespace kosmos {
+
+// ---------------------------------------------------------------- tiles
+constexpr int BM = 128;            // tile rows (= tcgen05 M, = TMEM lanes)
+constexpr int BN = 256;            // tile columns (= tcgen05 N)
+constexpr int BK = 64;             // K per pipeline stage (bf16: 128 bytes = one swizzle row)
+constexpr int UMMA_K = 16;         // K per tcgen05.mma (kind::f16)
+constexpr int NSTAGE = 4;          // shared-memory pipeline depth
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BK * BN * 2;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int PIECE_ROWS = BM;     // all-gather transfer piece height (one tile row)
+constexpr int NSCHED = 4;          // depth of the in-CTA entry ring
+constexpr int NUM_THREADS = 192;   // warp 0 scheduler/producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int NUM_EPI_THREADS = 128;
+constexpr int TMEM_COLS = 512;     // two 128x256 fp32 accumulators
+constexpr int RED_ROWS = 8;        // rows of one reduce stage (P x 8 x 256 bf16 <= 32 KB)
+constexpr int MAX_CTAS = 256;
+constexpr int TRACE_CAP = 1024;    // trace records per CTA
+
+enum EntryKind : int32_t {
+    K_NONE = 0,
+    K_TRANSFER = 1,
+    K_TILE = 2,
+    K_REDUCE = 3,
+    K_ROUTE = 4,
+    K_DISPATCH = 5,
+    K_TILE_GU = 6,
+    K_TILE_D = 7,
+    K_PUSH = 8,
+    K_FOLD = 9,
+    K_DONE = 15
+};
+
+// ---------------------------------------------------------------- workspace
+// Offset 0 of every workspace.  Tickets and done_ctas are returned to zero by
+// the last CTA of every successful launch; epoch then advances, so readiness
+// flags written as (epoch + 1) need no clearing between calls.
+struct WsHeader {
+    uint32_t epoch;
+    uint32_t status;       // kosmos_status of the device side (0 = OK)
+    uint32_t done_ctas;
+    uint32_t pad0;
+    int64_t fail_entry;    // ticket (or encoded entry) that failed, -1 none
+    uint32_t tickets[40];  // rail counters
+    uint32_t aux[4];
+};
+static_assert(sizeof(WsHeader) <= 256, "header must fit its 256-byte slot");
+
+struct TraceRec {
+    int64_t t_claim, t_ready, t_done;
+    int32_t kind, ticket, cta, pad;
+};
+static_assert(sizeof(TraceRec) == sizeof(kosmos_trace_rec), "trace record layout");
+
+KOS_HD int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+KOS_HD int64_t align_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+// ---------------------------------------------------------------- AG geometry / rails
+struct AgGeom {
+    int P;
+    int64_t m, k, n;
+    int pieces;      // tile rows (= transfer pieces) per shard
+    int tiles_n;
+    int n_transfer;  // P * pieces: remote shards first, the local shard's copies last
+    int n_tile;      // P * pieces * tiles_n
+};
+KOS_HD AgGeom ag_geom(int P, int64_t m, int64_t k, int64_t n) {
+    AgGeom g;
+    g.P = P; g.m = m; g.k = k; g.n = n;
+    g.pieces = static_cast<int>(cdiv(m, PIECE_ROWS));
+    g.tiles_n = static_cast<int>(cdiv(n, BN));
+    g.n_transfer = P * g.pieces;
+    g.n_tile = P * g.pieces * g.tiles_n;
+    return g;
+}
+// Transfer rail: shards 1..P-1 in the order the tiles consume them, then shard 0.
+KOS_HD void ag_decode_transfer(const AgGeom &g, int t, int &shard, int &piece) {
+    const int sidx = t / g.pieces;
+    piece = t - sidx * g.pieces;
+    shard = (sidx + 1 < g.P) ? sidx + 1 : 0;
+}
+// Tile rail: shard-major (local shard 0 first), tile rows, then tile columns.
+KOS_HD void ag_decode_tile(const AgGeom &g, int t, int &shard, int &trow, int &tcol) {
+    const int per_shard = g.pieces * g.tiles_n;
+    shard = t / per_shard;
+    const int r = t - shard * per_shard;
+    trow = r / g.tiles_n;
+    tcol = r - trow * g.tiles_n;
+}
+
+// ---------------------------------------------------------------- RS geometry / rails
+struct RsGeom {
+    int P;
+    int64_t m, k, n;
+    int64_t mc;       // rows per chunk = m / P
+    int bands;        // tile rows per chunk
+    int tiles_n;
+    int n_tile;       // per rank: P * bands * tiles_n
+    int n_reduce;     // per rank: bands * tiles_n
+};
+KOS_HD RsGeom rs_geom(int P, int64_t m, int64_t k, int64_t n) {
+    RsGeom g;
+    g.P = P; g.m = m; g.k = k; g.n = n;
+    g.mc = m / P;
+    g.bands = static_cast<int>(cdiv(g.mc, BM));
+    g.tiles_n = static_cast<int>(cdiv(n, BN));
+    g.n_tile = P * g.bands * g.tiles_n;
+    g.n_reduce = g.bands * g.tiles_n;
+    return g;
+}
+// Tile rail of one rank.  Band order: band, chunk, column.  Row order: chunk, band, column.
+KOS_HD void rs_decode_tile(const RsGeom &g, int order, int t, int &chunk, int &band, int &tcol) {
+    if (order == KOSMOS_ORDER_BAND) {
+        const int per_band = g.P * g.tiles_n;
+        band = t / per_band;
+        const int r = t - band * per_band;
+        chunk = r / g.tiles_n;
+        tcol = r - chunk * g.tiles_n;
+    } else {
+        const int per_chunk = g.bands * g.tiles_n;
+        chunk = t / per_chunk;
+        const int r = t - chunk * per_chunk;
+        band = r / g.tiles_n;
+        tcol = r - band * g.tiles_n;
+    }
+}
+// Reduce rail of rank r (its own chunk): band, then column.
+KOS_HD void rs_decode_reduce(const RsGeom &g, int t, int &band, int &tcol) {
+    band = t / g.tiles_n;
+    tcol = t - band * g.tiles_n;
+}
+
+// ---------------------------------------------------------------- workspace layouts
+struct AgWsLayout {
+    size_t flags_off, trace_off, total;
+};
+inline AgWsLayout ag_ws_layout(const AgGeom &g, bool trace) {
+    AgWsLayout L;
+    L.flags_off = 256;
+    size_t off = L.flags_off + static_cast<size_t>(align_up(static_cast<int64_t>(g.P) * g.pieces * 4, 256));
+    L.trace_off = off;
+    if (trace) off += static_cast<size_t>(MAX_CTAS) * TRACE_CAP * sizeof(TraceRec);
+    L.total = off;
+    return L;
+}
+struct RsWsLayout {
+    size_t arrive_off, partial_off, trace_off, total;
+};
+inline RsWsLayout rs_ws_layout(const RsGeom &g, bool trace) {
+    RsWsLayout L;
+    L.arrive_off = 256;
+    size_t off = L.arrive_off + static_cast<size_t>(align_up(static_cast<int64_t>(g.P) * g.bands * g.tiles_n * 4, 1024));
+    L.partial_off = off;
+    off += static_cast<size_t>(align_up(static_cast<int64_t>(g.P) * g.m * g.n * 2, 1024));
+    L.trace_off = off;
+    if (trace) off += static_cast<size_t>(MAX_CTAS) * TRACE_CAP * sizeof(TraceRec);
+    L.total = off;
+    return L;
+}
+
+}  // namespace kosmos

@@ -1,0 +1,272 @@
+// engine.cuh -- the persistent CTA engine shared by the fused operators.
+//
+// One CTA per SM, 192 threads, warp-specialised:
+//   warp 0 (lane 0)  scheduler + producer: claims tickets from the rails,
+//                    performs mover transfers itself, waits for readiness
+//                    flags, pushes TILE/REDUCE entries into an in-CTA ring and
+//                    streams their operands into the shared-memory pipeline
+//                    with TMA;
+//   warp 1 (lane 0)  MMA issuer: tcgen05.mma over the staged K blocks into one
+//                    of two TMEM accumulators (double-buffered);
+//   warps 2..5       epilogue: tcgen05.ld of the accumulator (one row per
+//                    thread), conversion and stores; reduction entries are
+//                    summed here from the staged partial tiles.
+// Every wait is bounded: on expiry the CTA records an error in the workspace
+// header and leaves its loops; nothing traps.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace kosmos {
+
+struct SchedEntry {
+    int32_t kind;     // EntryKind (K_DONE ends the CTA's loops)
+    int32_t a, b, c;  // decoded entry fields
+    int32_t nstage;   // pipeline stages the entry occupies
+    int32_t ticket;
+    int32_t slot;     // trace record index of this CTA, -1 when untraced
+    int32_t d;        // extra field (op specific)
+};
+
+struct Smem {
+    uint8_t *stages;   // NSTAGE * STAGE_BYTES, 1024-byte aligned
+    uint64_t *full;    // [NSTAGE] operands landed (TMA complete_tx)
+    uint64_t *empty;   // [NSTAGE] stage consumed (tcgen05.commit or epilogue)
+    uint64_t *cbar;    // [NSTAGE] mover copy buffers landed
+    uint64_t *tfull;   // [2] accumulator ready (tcgen05.commit)
+    uint64_t *tempty;  // [2] accumulator drained (4 epilogue warps)
+    uint64_t *sfull;   // [NSCHED] entry published
+    uint64_t *sempty;  // [NSCHED] entry read by MMA + 4 epilogue warps
+    SchedEntry *sched; // [NSCHED]
+    uint32_t *tmem_slot;
+};
+constexpr int SMEM_CTRL_BYTES = 1024;
+constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + SMEM_CTRL_BYTES + 1024;
+constexpr uint64_t PIPE_LIMIT_NS = 4000000000ull;  // internal pipeline waits: 4 s
+
+__device__ __forceinline__ Smem carve_smem(uint8_t *raw) {
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
+    uint8_t *p = reinterpret_cast<uint8_t *>(base);
+    Smem s;
+    s.stages = p;
+    p += NSTAGE * STAGE_BYTES;
+    uint64_t *b = reinterpret_cast<uint64_t *>(p);
+    s.full = b; b += NSTAGE;
+    s.empty = b; b += NSTAGE;
+    s.cbar = b; b += NSTAGE;
+    s.tfull = b; b += 2;
+    s.tempty = b; b += 2;
+    s.sfull = b; b += NSCHED;
+    s.sempty = b; b += NSCHED;
+    s.sched = reinterpret_cast<SchedEntry *>(b);
+    s.tmem_slot = reinterpret_cast<uint32_t *>(s.sched + NSCHED);
+    return s;
+}
+
+struct PipeState {
+    uint32_t stage = 0, phase = 0;
+    __device__ __forceinline__ void advance() {
+        if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
+    }
+    __device__ __forceinline__ void advance(int n) {
+        for (int i = 0; i < n; ++i) advance();
+    }
+};
+
+struct RingState {
+    uint32_t idx = 0, phase = 0;
+    __device__ __forceinline__ void advance() {
+        if (++idx == NSCHED) { idx = 0; phase ^= 1; }
+    }
+};
+
+// ---------------------------------------------------------------- status
+__device__ __forceinline__ void set_error(WsHeader *ws, uint32_t code, int64_t entry) {
+    if (atomicCAS(&ws->status, 0u, code) == 0u) {
+        ws->fail_entry = entry;
+        __threadfence();
+    }
+}
+__device__ __forceinline__ bool failed(WsHeader *ws) { return ld_relaxed_gpu(&ws->status) != 0u; }
+
+// Bounded acquire-wait until *flag == target.  On success the caller may read
+// the guarded data with TMA (the proxy fence orders the async-proxy reads
+// after the acquire).  On expiry: status = TIMEOUT, fail_entry = entry.
+__device__ __forceinline__ bool wait_flag_eq(WsHeader *ws, const uint32_t *flag, uint32_t target,
+                                             uint64_t limit_ns, int64_t entry) {
+    uint32_t it = 0;
+    uint64_t t0 = 0;
+    while (ld_acquire_gpu(flag) != target) {
+        if ((++it & 15u) == 0u) {
+            if (failed(ws)) return false;
+            const uint64_t now = globaltimer();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                set_error(ws, KOSMOS_ERR_TIMEOUT, entry);
+                return false;
+            }
+        }
+    }
+    fence_proxy_async_global();
+    return true;
+}
+
+// ---------------------------------------------------------------- setup / teardown
+__device__ __forceinline__ void engine_setup(const Smem &sm, int warp) {
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+            mbar_init(&sm.cbar[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.tfull[i], 1);
+            mbar_init(&sm.tempty[i], 4);
+        }
+        for (int i = 0; i < NSCHED; ++i) {
+            mbar_init(&sm.sfull[i], 1);
+            mbar_init(&sm.sempty[i], 5);
+        }
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(sm.tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// The last CTA to finish returns the rail counters to zero and advances the
+// epoch, leaving the workspace ready for the next stream-ordered call.
+__device__ __forceinline__ void engine_finish(WsHeader *ws, uint32_t epoch, int n_tickets) {
+    __threadfence();
+    const uint32_t prev = atomicAdd(&ws->done_ctas, 1u);
+    if (prev == gridDim.x - 1) {
+        __threadfence();
+        volatile uint32_t *t = ws->tickets;
+        for (int i = 0; i < n_tickets; ++i) t[i] = 0u;
+        *reinterpret_cast<volatile uint32_t *>(&ws->done_ctas) = 0u;
+        __threadfence();
+        *reinterpret_cast<volatile uint32_t *>(&ws->epoch) = epoch + 1u;
+        __threadfence();
+    }
+}
+
+__device__ __forceinline__ void engine_teardown(const Smem &sm, int warp, uint32_t tmem_base) {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- ring (producer side)
+__device__ __forceinline__ bool ring_push(const Smem &sm, RingState &rs, const SchedEntry &e, WsHeader *ws) {
+    if (!mbar_wait(&sm.sempty[rs.idx], rs.phase ^ 1u, PIPE_LIMIT_NS)) {
+        set_error(ws, KOSMOS_ERR_DEVICE, -2);
+        return false;
+    }
+    sm.sched[rs.idx] = e;
+    mbar_arrive(&sm.sfull[rs.idx]);
+    rs.advance();
+    return true;
+}
+
+// ---------------------------------------------------------------- MMA warp
+// Issues, for each TILE entry, nstage K blocks of BM x BN x BK into accumulator
+// acc (TMEM columns acc*BN .. acc*BN+BN-1).  A: K-major, 128-byte swizzle
+// (rows of 128 bytes, 8-row atoms of 1024 bytes).  B: N-major, 128-byte
+// swizzle, four 64-column slabs of 8 KB (LBO = 8 KB between slabs,
+// SBO = 1 KB between 8-row K groups).
+__device__ __forceinline__ void mma_loop(const Smem &sm, uint32_t tmem_base, WsHeader *ws) {
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, true);
+    PipeState ps;
+    RingState rs;
+    uint32_t acc = 0, acc_phase = 0;
+    while (true) {
+        if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
+            set_error(ws, KOSMOS_ERR_DEVICE, -3);
+            break;
+        }
+        const SchedEntry e = sm.sched[rs.idx];
+        mbar_arrive(&sm.sempty[rs.idx]);
+        rs.advance();
+        if (e.kind == K_DONE) break;
+        if (e.kind != K_TILE) {
+            ps.advance(e.nstage);
+            continue;
+        }
+        if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, PIPE_LIMIT_NS)) {
+            set_error(ws, KOSMOS_ERR_DEVICE, -4);
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < e.nstage; ++kb) {
+            if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+                set_error(ws, KOSMOS_ERR_DEVICE, -5);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sm.stages + ps.stage * STAGE_BYTES);
+            const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+                const uint64_t ad = sdesc_sw128(a_addr + k * (UMMA_K * 2), 16, 1024);
+                const uint64_t bd = sdesc_sw128(b_addr + k * (UMMA_K * 128), 64 * 128, 1024);
+                mma_bf16_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            }
+            mma_commit(&sm.empty[ps.stage]);
+            ps.advance();
+        }
+        if (!ok) break;
+        mma_commit(&sm.tfull[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+}
+
+// ---------------------------------------------------------------- epilogue helpers
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Reads 32 fp32 columns of this thread's accumulator row and stores them as
+// bf16 at dst (16-byte stores; columns >= ncols_valid are skipped in groups
+// of 8).  tcgen05.ld is warp-collective: every lane calls this.
+__device__ __forceinline__ void tmem_row_chunk_to_bf16(uint32_t taddr, bool row_valid, __nv_bfloat16 *dst,
+                                                       int ncols_valid) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr, r);
+    tmem_ld_wait();
+    if (row_valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (q * 8 < ncols_valid) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(r[q * 8 + 0]), __uint_as_float(r[q * 8 + 1]));
+                v.y = pack_bf16x2(__uint_as_float(r[q * 8 + 2]), __uint_as_float(r[q * 8 + 3]));
+                v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]), __uint_as_float(r[q * 8 + 5]));
+                v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]), __uint_as_float(r[q * 8 + 7]));
+                *reinterpret_cast<uint4 *>(dst + q * 8) = v;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ TraceRec *trace_rec(TraceRec *base, int cta, int slot) {
+    return (base != nullptr && slot >= 0 && slot < TRACE_CAP) ? base + static_cast<int64_t>(cta) * TRACE_CAP + slot
+                                                              : nullptr;
+}
+
+}  // namespace kosmos

@@ -1,0 +1,342 @@
+// host.cu -- the C ABI: argument validation, workspace sizing, status
+// read-back, rail decode, and dispatch to the operator launchers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+
+using namespace kosmos;
+
+namespace kosmos {
+
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                      const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                      CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                      CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled_t get_encode_fn() {
+    static PFN_encodeTiled_t fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_encodeTiled_t>(p);
+    }
+    return fn;
+}
+
+bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, void *base, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle) {
+    PFN_encodeTiled_t fn = get_encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t d[5], s[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    const CUresult r = fn(map, dt, static_cast<cuuint32_t>(rank), base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream) {
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+        return KOSMOS_ERR_CUDA;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[1] = {params};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, func, args);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KOSMOS_ERR_CUDA;
+    }
+    return KOSMOS_OK;
+}
+
+}  // namespace kosmos
+
+namespace {
+
+int device_sms() {
+    static int cached_dev = -1;
+    static int cached_sms = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev != cached_dev) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        cached_dev = dev;
+        cached_sms = sms;
+    }
+    return cached_sms;
+}
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kosmos_opts resolve_opts(const kosmos_opts *o) {
+    kosmos_opts r;
+    kosmos_default_opts(&r);
+    if (o) r = *o;
+    if (r.wait_limit_ns == 0) r.wait_limit_ns = 2000000000ull;
+    return r;
+}
+
+int grid_for(const kosmos_opts &o) {
+    const int sms = device_sms();
+    if (sms <= 0) return -1;
+    int g = (o.num_ctas > 0 && o.num_ctas < sms) ? o.num_ctas : sms;
+    if (g > MAX_CTAS) g = MAX_CTAS;
+    return g;
+}
+
+// Movers at start (SELF) or the fixed crew size (FIXED): ceil(S/P) by default,
+// kept within [1, grid-1] so at least one builder exists.
+int resolve_comm(const kosmos_opts &o, int grid, int P, bool fixed) {
+    int n = o.n_comm0 >= 0 ? o.n_comm0 : static_cast<int>((grid + P - 1) / P);
+    if (fixed && o.fixed_comm_ctas >= 0) n = o.fixed_comm_ctas;
+    if (n < 1) n = 1;
+    if (grid > 1 && n > grid - 1) n = grid - 1;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+void kosmos_default_opts(kosmos_opts *opts) {
+    if (!opts) return;
+    memset(opts, 0, sizeof(*opts));
+    opts->sched = KOSMOS_SCHED_SELF;
+    opts->n_comm0 = -1;
+    opts->fixed_comm_ctas = -1;
+    opts->order = KOSMOS_ORDER_BAND;
+    opts->num_ctas = -1;
+    opts->trace = 0;
+    opts->wait_limit_ns = 0;
+    opts->inject = 0;
+}
+
+int kosmos_num_sms(void) { return device_sms(); }
+
+size_t kosmos_workspace_bytes(int op, int P, int64_t m, int64_t n, int64_t k, int dtype, const kosmos_opts *opts) {
+    const kosmos_opts o = resolve_opts(opts);
+    if (P < 1 || P > KOSMOS_MAX_P || m < 1 || n < 1 || k < 1) return 0;
+    (void)dtype;
+    if (op == KOSMOS_OP_AG_GEMM) {
+        return ag_ws_layout(ag_geom(P, m, k, n), o.trace != 0).total;
+    }
+    if (op == KOSMOS_OP_GEMM_RS) {
+        if (m % P) return 0;
+        return rs_ws_layout(rs_geom(P, m, k, n), o.trace != 0).total;
+    }
+    return 0;
+}
+
+kosmos_status kosmos_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+    if (!aligned16(ws) || ws_bytes < 256) return KOSMOS_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KOSMOS_ERR_CUDA;
+    return KOSMOS_OK;
+}
+
+kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_scales, int P, int64_t m_per_shard,
+                             int64_t k, int64_t n, const void *w, const void *w_scales, int dtype, void *x_gathered,
+                             void *y, void *ws, size_t ws_bytes, const kosmos_opts *opts, void *stream) {
+    if (P < 1 || P > KOSMOS_MAX_P || x_shards == nullptr) return KOSMOS_ERR_INVALID_ARG;
+    if (m_per_shard < 1 || k < BK || n < 8 || n % 8 != 0) return KOSMOS_ERR_INVALID_ARG;
+    if (m_per_shard > (1ll << 30) || k > (1ll << 24) || n > (1ll << 24)) return KOSMOS_ERR_INVALID_ARG;
+    if (dtype != KOSMOS_BF16 && dtype != KOSMOS_MXFP8_E4M3) return KOSMOS_ERR_INVALID_ARG;
+    if (dtype == KOSMOS_BF16 && k % BK != 0) return KOSMOS_ERR_INVALID_ARG;
+    if (dtype == KOSMOS_MXFP8_E4M3 && (k % 128 != 0 || n % 16 != 0)) return KOSMOS_ERR_INVALID_ARG;
+    for (int r = 0; r < P; ++r) {
+        if (!aligned16(x_shards[r])) return KOSMOS_ERR_INVALID_ARG;
+        if (dtype == KOSMOS_MXFP8_E4M3 && (x_scales == nullptr || !aligned16(x_scales[r])))
+            return KOSMOS_ERR_INVALID_ARG;
+    }
+    if (!aligned16(w) || !aligned16(x_gathered) || !aligned16(y)) return KOSMOS_ERR_INVALID_ARG;
+    if (dtype == KOSMOS_MXFP8_E4M3 && !aligned16(w_scales)) return KOSMOS_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
+    const kosmos_opts o = resolve_opts(opts);
+    if (o.sched < KOSMOS_SCHED_SELF || o.sched > KOSMOS_SCHED_UNFUSED) return KOSMOS_ERR_INVALID_ARG;
+    if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_AG_GEMM, P, m_per_shard, n, k, dtype, &o))
+        return KOSMOS_ERR_WORKSPACE;
+    const int grid = grid_for(o);
+    if (grid < 1) return KOSMOS_ERR_CUDA;
+    if (o.sched == KOSMOS_SCHED_FIXED && grid < 2) return KOSMOS_ERR_INVALID_ARG;
+    AgLaunch L;
+    memset(&L, 0, sizeof(L));
+    L.P = P; L.m = m_per_shard; L.k = k; L.n = n;
+    for (int r = 0; r < P; ++r) {
+        L.x[r] = x_shards[r];
+        L.xs[r] = x_scales ? x_scales[r] : nullptr;
+    }
+    L.w = w; L.wsc = w_scales; L.x_gathered = x_gathered; L.y = y; L.ws = ws;
+    L.dtype = dtype; L.sched = o.sched;
+    L.n_comm = resolve_comm(o, grid, P, o.sched == KOSMOS_SCHED_FIXED);
+    L.trace = o.trace; L.grid = grid; L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dtype == KOSMOS_BF16 ? launch_ag_bf16(L, s) : launch_ag_mxfp8(L, s);
+}
+
+kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_shards, int P, int64_t m,
+                             int64_t k_per_rank, int64_t n, int dtype, void *const *y_chunks, void *ws,
+                             size_t ws_bytes, const kosmos_opts *opts, void *stream) {
+    if (P < 1 || P > KOSMOS_MAX_P || x_shards == nullptr || w_shards == nullptr || y_chunks == nullptr)
+        return KOSMOS_ERR_INVALID_ARG;
+    if (m < P || m % P != 0 || k_per_rank < BK || k_per_rank % BK != 0 || n < 8 || n % 8 != 0)
+        return KOSMOS_ERR_INVALID_ARG;
+    if (m > (1ll << 30) || k_per_rank > (1ll << 24) || n > (1ll << 24)) return KOSMOS_ERR_INVALID_ARG;
+    if (dtype != KOSMOS_BF16) return dtype == KOSMOS_MXFP8_E4M3 ? KOSMOS_ERR_UNSUPPORTED : KOSMOS_ERR_INVALID_ARG;
+    for (int r = 0; r < P; ++r)
+        if (!aligned16(x_shards[r]) || !aligned16(w_shards[r]) || !aligned16(y_chunks[r]))
+            return KOSMOS_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
+    const kosmos_opts o = resolve_opts(opts);
+    if (o.sched < KOSMOS_SCHED_SELF || o.sched > KOSMOS_SCHED_UNFUSED) return KOSMOS_ERR_INVALID_ARG;
+    if (o.order != KOSMOS_ORDER_BAND && o.order != KOSMOS_ORDER_ROW) return KOSMOS_ERR_INVALID_ARG;
+    if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_GEMM_RS, P, m, n, k_per_rank, dtype, &o))
+        return KOSMOS_ERR_WORKSPACE;
+    const int grid = grid_for(o);
+    if (grid < 1) return KOSMOS_ERR_CUDA;
+    if (grid < P) return KOSMOS_ERR_INVALID_ARG;  // every emulated rank needs a CTA
+    RsLaunch L;
+    memset(&L, 0, sizeof(L));
+    L.P = P; L.m = m; L.k = k_per_rank; L.n = n;
+    for (int r = 0; r < P; ++r) {
+        L.x[r] = x_shards[r];
+        L.w[r] = w_shards[r];
+        L.y[r] = y_chunks[r];
+    }
+    L.ws = ws;
+    L.sched = o.sched;
+    {
+        const int per_rank = grid / P;
+        int n_red = o.n_comm0 >= 0 ? o.n_comm0 : 1;
+        if (o.sched == KOSMOS_SCHED_FIXED && o.fixed_comm_ctas >= 0) n_red = o.fixed_comm_ctas;
+        if (n_red < 1) n_red = 1;
+        if (per_rank > 1 && n_red > per_rank - 1) n_red = per_rank - 1;
+        if (per_rank == 1 && o.sched == KOSMOS_SCHED_FIXED) return KOSMOS_ERR_INVALID_ARG;
+        L.n_comm = n_red;
+    }
+    L.order = o.order; L.trace = o.trace; L.grid = grid;
+    L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
+    return launch_rs_bf16(L, static_cast<cudaStream_t>(stream));
+}
+
+kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, int P, int64_t tokens, int64_t hidden,
+                             int n_experts, int topk, int64_t inter, const void *const *w_gate,
+                             const void *const *w_up, const void *const *w_down, void *const *y_shards,
+                             int32_t *topk_idx, float *topk_gate, int32_t *expert_counts, int32_t *dispatch_pos,
+                             void *ws, size_t ws_bytes, const kosmos_opts *opts, void *stream) {
+    (void)x_shards; (void)w_router; (void)P; (void)tokens; (void)hidden; (void)n_experts; (void)topk;
+    (void)inter; (void)w_gate; (void)w_up; (void)w_down; (void)y_shards; (void)topk_idx; (void)topk_gate;
+    (void)expert_counts; (void)dispatch_pos; (void)ws; (void)ws_bytes; (void)opts; (void)stream;
+    return KOSMOS_ERR_UNSUPPORTED;
+}
+
+kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q, void *scales,
+                                    void *stream) {
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || rows < 1 || cols < 1) return KOSMOS_ERR_INVALID_ARG;
+    if (along_cols ? (cols % 32 != 0) : (rows % 32 != 0)) return KOSMOS_ERR_INVALID_ARG;
+    return launch_mxfp8_quantize(x, rows, cols, along_cols, q, scales, static_cast<cudaStream_t>(stream));
+}
+
+kosmos_status kosmos_status_sync(void *ws, void *stream, int64_t *failing_entry) {
+    if (!aligned16(ws)) return KOSMOS_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KOSMOS_ERR_CUDA;
+    WsHeader h;
+    if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return KOSMOS_ERR_CUDA;
+    if (failing_entry) *failing_entry = h.status ? h.fail_entry : -1;
+    return static_cast<kosmos_status>(h.status);
+}
+
+kosmos_status kosmos_trace_info(int op, int P, int64_t m, int64_t n, int64_t k, int dtype, const kosmos_opts *opts,
+                                void *ws, void **records, int32_t *per_cta_capacity, int32_t *num_ctas) {
+    const kosmos_opts o = resolve_opts(opts);
+    if (!o.trace || ws == nullptr) return KOSMOS_ERR_INVALID_ARG;
+    size_t off = 0;
+    (void)dtype;
+    if (op == KOSMOS_OP_AG_GEMM)
+        off = ag_ws_layout(ag_geom(P, m, k, n), true).trace_off;
+    else if (op == KOSMOS_OP_GEMM_RS)
+        off = rs_ws_layout(rs_geom(P, m, k, n), true).trace_off;
+    else
+        return KOSMOS_ERR_UNSUPPORTED;
+    if (records) *records = static_cast<uint8_t *>(ws) + off;
+    if (per_cta_capacity) *per_cta_capacity = TRACE_CAP;
+    if (num_ctas) *num_ctas = grid_for(o);
+    return KOSMOS_OK;
+}
+
+int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int32_t *out,
+                           int64_t max_entries) {
+    if (P < 1 || P > KOSMOS_MAX_P || m < 1 || n < 1) return -1;
+    if (op == KOSMOS_OP_AG_GEMM) {
+        const AgGeom g = ag_geom(P, m, 64, n);
+        const int64_t len = rail == 0 ? g.n_transfer : g.n_tile;
+        if (out) {
+            for (int64_t t = 0; t < len && t < max_entries; ++t) {
+                int32_t *e = out + 4 * t;
+                if (rail == 0) {
+                    int s, j;
+                    ag_decode_transfer(g, static_cast<int>(t), s, j);
+                    e[0] = K_TRANSFER; e[1] = s; e[2] = j; e[3] = 0;
+                } else {
+                    int s, i, c;
+                    ag_decode_tile(g, static_cast<int>(t), s, i, c);
+                    e[0] = K_TILE; e[1] = s; e[2] = i; e[3] = c;
+                }
+            }
+        }
+        return len;
+    }
+    if (op == KOSMOS_OP_GEMM_RS) {
+        if (m % P || rank < 0 || rank >= P) return -1;
+        const RsGeom g = rs_geom(P, m, 64, n);
+        const int64_t len = rail == 0 ? g.n_tile : g.n_reduce;
+        if (out) {
+            for (int64_t t = 0; t < len && t < max_entries; ++t) {
+                int32_t *e = out + 4 * t;
+                if (rail == 0) {
+                    int c, b, j;
+                    rs_decode_tile(g, order, static_cast<int>(t), c, b, j);
+                    e[0] = K_TILE; e[1] = c; e[2] = b; e[3] = j;
+                } else {
+                    int b, j;
+                    rs_decode_reduce(g, static_cast<int>(t), b, j);
+                    e[0] = K_REDUCE; e[1] = rank; e[2] = b; e[3] = j;
+                }
+            }
+        }
+        return len;
+    }
+    return -1;
+}
+
+int64_t kosmos_rail_decode_device(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int32_t *out,
+                                  int64_t max_entries, void *stream) {
+    const int64_t len = kosmos_rail_decode(op, P, m, n, order, rank, rail, nullptr, 0);
+    if (len < 0 || out == nullptr) return len;
+    const int64_t cnt = len < max_entries ? len : max_entries;
+    if (launch_rail_decode(op, P, m, n, order, rank, rail, out, cnt, static_cast<cudaStream_t>(stream)) != KOSMOS_OK)
+        return -1;
+    return len;
+}
+
+}  // extern "C"

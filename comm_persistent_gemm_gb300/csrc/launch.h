@@ -1,0 +1,87 @@
+// launch.h -- host-side interfaces between the C ABI (host.cu) and the
+// per-operator launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/kosmos.h"
+
+namespace kosmos {
+
+struct AgLaunch {
+    int P;
+    int64_t m, k, n;
+    const void *x[KOSMOS_MAX_P];
+    const void *xs[KOSMOS_MAX_P];  // MXFP8 scales
+    const void *w;
+    const void *wsc;               // MXFP8 scales
+    void *x_gathered;
+    void *y;
+    void *ws;
+    int dtype;
+    int sched;
+    int n_comm;
+    int trace;
+    int grid;
+    uint64_t wait_limit_ns;
+    uint64_t inject;
+};
+
+struct RsLaunch {
+    int P;
+    int64_t m, k, n;
+    const void *x[KOSMOS_MAX_P];
+    const void *w[KOSMOS_MAX_P];
+    void *y[KOSMOS_MAX_P];
+    void *ws;
+    int sched;
+    int n_comm;
+    int order;
+    int trace;
+    int grid;
+    uint64_t wait_limit_ns;
+    uint64_t inject;
+};
+
+struct MoeLaunch {
+    int P;
+    int64_t T, H, I;
+    int E, K;
+    const void *x[KOSMOS_MAX_P];
+    const void *wr;
+    const void *wg[KOSMOS_MAX_P];
+    const void *wu[KOSMOS_MAX_P];
+    const void *wd[KOSMOS_MAX_P];
+    void *y[KOSMOS_MAX_P];
+    int32_t *topk_idx;
+    float *topk_gate;
+    int32_t *counts;
+    int32_t *pos;
+    void *ws;
+    int sched;
+    int n_comm;
+    int trace;
+    int grid;
+    uint64_t wait_limit_ns;
+    uint64_t inject;
+};
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, void *base, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
+
+// Cooperative launch of a persistent kernel whose only argument is *params.
+kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream);
+
+kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream);
+kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream);
+kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream);
+kosmos_status launch_moe_fwd(const MoeLaunch &L, cudaStream_t stream);
+kosmos_status launch_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q,
+                                    void *scales, cudaStream_t stream);
+kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail,
+                                 int32_t *out, int64_t count, cudaStream_t stream);
+
+}  // namespace kosmos

@@ -1,0 +1,250 @@
+/*
+ * kosmos.h -- C ABI of the GB300 (sm_103a) self-scheduling persistent kernels.
+ *
+ * The method: "KOSMOS: Self-scheduling Persistent Kernels for
+ * Communication-Compute Overlap" (arXiv 2611.07477, abstract), explained on
+ * learnaivisually.com ("KOSMOS -- Self-scheduling persistent kernels -- What
+ * does it mean?").  Each fused operator is ONE persistent launch with one CTA
+ * resident per SM; CTAs take work by atomically claiming the next entry of a
+ * shared queue ("rail") that is ordered by consumer demand, and switch role
+ * (mover / builder / reducer) when their own work runs out (explainer,
+ * paragraphs "KOSMOS removes the manager" and "Role switching only works").
+ *
+ * Emulated ranks.  On one GPU the P "ranks" are P shard buffers in the same
+ * HBM; a transfer between ranks is a device-to-device copy made by mover CTAs
+ * inside the persistent kernel.  Nothing here talks to a second GPU.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are row-major, caller-owned DEVICE memory; every pointer must
+ *     be 16-byte aligned.  bf16 = IEEE bfloat16 bit patterns (uint16).
+ *   - `stream` is a cudaStream_t passed as void*; NULL = legacy default stream.
+ *     Calls are stream-ordered and asynchronous: a KOSMOS_OK return means the
+ *     arguments were accepted and the work was enqueued.
+ *   - Argument errors are detected on the host, return synchronously and
+ *     launch nothing.  Errors found on the device (a bounded wait that ran
+ *     out, a device-side check) are written to the workspace status word and
+ *     read back with kosmos_status_sync().
+ *   - The library allocates no memory and keeps no state between calls other
+ *     than cached device attributes and driver entry points.  The workspace
+ *     holds ticket counters, readiness flags, the status word, the optional
+ *     role trace and (GEMM+RS only) the per-rank partial products.  One
+ *     workspace serves one stream at a time; it must be zeroed once with
+ *     kosmos_workspace_init() before first use and again after any call whose
+ *     status was not KOSMOS_OK.  Successful calls leave it ready for the next.
+ */
+#ifndef KOSMOS_H
+#define KOSMOS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KOSMOS_MAX_P 8
+
+#if defined(__GNUC__)
+#define KOSMOS_API __attribute__((visibility("default")))
+#else
+#define KOSMOS_API
+#endif
+
+typedef enum kosmos_status {
+    KOSMOS_OK = 0,
+    KOSMOS_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad shape, P out of range */
+    KOSMOS_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+    KOSMOS_ERR_WORKSPACE = 3,    /* workspace missing or smaller than kosmos_workspace_bytes() */
+    KOSMOS_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, copy) */
+    KOSMOS_ERR_TIMEOUT = 5,      /* device: a readiness wait exceeded opts.wait_limit_ns */
+    KOSMOS_ERR_DEVICE = 6        /* device: an internal pipeline wait or check failed */
+} kosmos_status;
+
+typedef enum kosmos_dtype {
+    KOSMOS_BF16 = 0,
+    KOSMOS_MXFP8_E4M3 = 1        /* E4M3 bytes + one E8M0 scale byte per 32 K-elements */
+} kosmos_dtype;
+
+typedef enum kosmos_op {
+    KOSMOS_OP_AG_GEMM = 0,
+    KOSMOS_OP_GEMM_RS = 1,
+    KOSMOS_OP_MOE_FWD = 2
+} kosmos_op;
+
+/* Scheduling policy.  SELF is the method; FIXED and UNFUSED are the two
+ * baselines the explainer contrasts it with (paragraph "Picture a restaurant
+ * kitchen": a manager fixes the mover/builder split at launch; paragraph
+ * "Start with the problem": transfer, then multiply). */
+enum {
+    KOSMOS_SCHED_SELF = 0,     /* one-way role switching driven by readiness */
+    KOSMOS_SCHED_FIXED = 1,    /* static partition: movers/reducers never switch */
+    KOSMOS_SCHED_UNFUSED = 2   /* separate copy (or reduce) launch and GEMM launch */
+};
+
+/* Output order of the reduce-scatter tile rails (explainer, "Role switching
+ * only works": band by band across every rank's chunk; the row-by-row order
+ * is the ablation). */
+enum { KOSMOS_ORDER_BAND = 0, KOSMOS_ORDER_ROW = 1 };
+
+/* Fault injection bits for tests (host-set; the failure is a flag that is
+ * never released, so the waiting side's bounded wait runs out). */
+#define KOSMOS_INJECT_DROP_TRANSFER 0x1ull  /* AG: transfer ticket (inject >> 32) never releases its flag */
+#define KOSMOS_INJECT_DROP_PARTIAL  0x2ull  /* RS: rank (inject >> 32) never signals its partial tiles */
+
+typedef struct kosmos_opts {
+    int32_t sched;            /* KOSMOS_SCHED_* */
+    int32_t n_comm0;          /* CTAs that start as movers (AG) / reducers per rank (RS); -1 = default */
+    int32_t fixed_comm_ctas;  /* FIXED: size of the static mover / reducer crew (per rank for RS); -1 = n_comm0 */
+    int32_t order;            /* KOSMOS_ORDER_* (GEMM+RS) */
+    int32_t num_ctas;         /* -1 = one CTA per SM */
+    int32_t trace;            /* nonzero: record a per-entry role trace in the workspace */
+    uint64_t wait_limit_ns;   /* bound on every readiness wait; 0 = 2e9 (2 s) */
+    uint64_t inject;          /* KOSMOS_INJECT_* bits | (argument << 32); 0 = none */
+} kosmos_opts;
+
+/* Fills *opts with the defaults (SELF, band order, all SMs, no trace). */
+KOSMOS_API void kosmos_default_opts(kosmos_opts *opts);
+
+/* Number of SMs of the current device (the persistent grid size), or -1. */
+KOSMOS_API int kosmos_num_sms(void);
+
+/* Workspace size in bytes for one call of `op` with these sizes (same
+ * meaning as the op's own arguments; MoE: m = tokens, n = hidden, k = inter,
+ * P = EP ranks).  opts may be NULL.  Returns 0 for invalid sizes. */
+KOSMOS_API size_t kosmos_workspace_bytes(int op, int P, int64_t m, int64_t n, int64_t k, int dtype,
+                              const kosmos_opts *opts);
+
+/* Zeroes the workspace (stream-ordered). */
+KOSMOS_API kosmos_status kosmos_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * All-gather + GEMM  (explainer, "Start with the problem": gather the input
+ * pieces from the other ranks before the multiplication; "Role switching only
+ * works": builders start on the local shard while movers fetch the remote
+ * shards in the order the multiplication consumes them).
+ *
+ *   Y = concat_{r=0..P-1}(X_r) . W          computed from rank 0's view
+ *
+ *   x_shards[r]  : P pointers, X_r [m_per_shard, k]; x_shards[0] is the local shard.
+ *                  BF16: bf16.  MXFP8: E4M3 bytes.
+ *   x_scales[r]  : MXFP8 only: [m_per_shard, k/32] E8M0 bytes; else NULL.
+ *   w            : [k, n] (BF16: bf16; MXFP8: E4M3 bytes).
+ *   w_scales     : MXFP8 only: [n, k/32] E8M0, one byte per 32 consecutive
+ *                  K-elements of a column; else NULL.
+ *   x_gathered   : out, [P*m_per_shard, k], same element type as X: the
+ *                  gathered input (kept for the backward pass).
+ *   y            : out, [P*m_per_shard, n] bf16, fp32 accumulation, one
+ *                  round-to-nearest-even per element.
+ *   Requirements: 1 <= P <= 8, m_per_shard >= 1, k % 64 == 0, n % 8 == 0
+ *   (MXFP8: k % 128 == 0, n % 16 == 0).
+ */
+KOSMOS_API kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_scales, int P,
+                             int64_t m_per_shard, int64_t k, int64_t n,
+                             const void *w, const void *w_scales, int dtype,
+                             void *x_gathered, void *y, void *ws, size_t ws_bytes,
+                             const kosmos_opts *opts, void *stream);
+
+/*
+ * GEMM + reduce-scatter  (explainer, "Start with the problem": scatter and
+ * add the partial results; "KOSMOS removes the manager": builders join the
+ * reduction when the multiplication tiles run out).
+ *
+ *   Y = sum_{r=0..P-1} X_r . W_r,  chunk c = rows [c*m/P, (c+1)*m/P) of Y
+ *
+ *   x_shards[r]  : X_r [m, k_per_rank] bf16
+ *   w_shards[r]  : W_r [k_per_rank, n] bf16
+ *   y_chunks[c]  : out, [m/P, n] bf16: each rank's partial rounded once to
+ *                  bf16, the P partials summed in fp32 in rank order 0..P-1,
+ *                  the sum rounded once to bf16.
+ *   Requirements: 1 <= P <= 8, m % P == 0, k_per_rank % 64 == 0, n % 8 == 0;
+ *   BF16 only.
+ */
+KOSMOS_API kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_shards, int P,
+                             int64_t m, int64_t k_per_rank, int64_t n, int dtype,
+                             void *const *y_chunks, void *ws, size_t ws_bytes,
+                             const kosmos_opts *opts, void *stream);
+
+/*
+ * MoE expert layer forward in one launch  (abstract: "runs an entire expert
+ * layer, from router to fold, in one launch per direction"; explainer,
+ * "KOSMOS removes the manager": in the combine step a CTA pushes any ready
+ * result and otherwise builds a tile).
+ *
+ *   x_shards[q]   : EP rank q's tokens [tokens/P, hidden] bf16 (token t lives on
+ *                   rank t / (tokens/P)).
+ *   w_router      : [hidden, n_experts] bf16.
+ *   w_gate[q], w_up[q] : rank q's experts [n_experts/P, hidden, inter] bf16.
+ *   w_down[q]     : [n_experts/P, inter, hidden] bf16.
+ *   y_shards[q]   : out, [tokens/P, hidden] bf16.
+ *   topk_idx      : out, [tokens, topk] int32, descending router score, ties to the lower index.
+ *   topk_gate     : out, [tokens, topk] fp32, softmax probabilities renormalised over the top-k.
+ *   expert_counts : out, [n_experts] int32.
+ *   dispatch_pos  : out, [tokens, topk] int32: row of (t, k) in the expert-ordered
+ *                   receive buffer (experts ascending, then tokens ascending).
+ *   Requirements: P in {1..8}, n_experts % P == 0, tokens % P == 0,
+ *   hidden % 256 == 0, inter % 128 == 0, 1 <= topk <= 8, n_experts <= 256.
+ */
+KOSMOS_API kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, int P,
+                             int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter,
+                             const void *const *w_gate, const void *const *w_up,
+                             const void *const *w_down, void *const *y_shards,
+                             int32_t *topk_idx, float *topk_gate, int32_t *expert_counts,
+                             int32_t *dispatch_pos, void *ws, size_t ws_bytes,
+                             const kosmos_opts *opts, void *stream);
+
+/*
+ * MXFP8 quantiser for the MXFP8 all-gather+GEMM operands.  For each block of
+ * 32 consecutive K-elements: e = smallest integer with blockmax <= 448 * 2^e
+ * (clamped to [-127, 127]; an all-zero block takes e = 0), scale byte e + 127,
+ * element byte = E4M3(x / 2^e) rounded to nearest even.
+ *   along_cols = 1: x [rows, cols], blocks along a row (activations X[m, k]);
+ *                   scales [rows, cols/32].
+ *   along_cols = 0: x [rows, cols], blocks along a column (weights W[k, n]);
+ *                   scales [cols, rows/32].
+ *   q keeps x's [rows, cols] layout.  Requirements: the blocked extent % 32 == 0.
+ */
+KOSMOS_API kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols,
+                                    void *q, void *scales, void *stream);
+
+/* Synchronises `stream`, then returns the device status of the last call
+ * that used `ws` (KOSMOS_OK, KOSMOS_ERR_TIMEOUT or KOSMOS_ERR_DEVICE) and,
+ * if failing_entry is not NULL, the ticket of the entry that failed (-1 if
+ * none). */
+KOSMOS_API kosmos_status kosmos_status_sync(void *ws, void *stream, int64_t *failing_entry);
+
+/* Role trace.  When opts.trace is set, every claimed entry appends one record
+ * to its CTA's ring in the workspace:
+ *   int64 t_claim, t_ready, t_done  (%globaltimer, ns)
+ *   int32 kind (1 TRANSFER, 2 TILE, 3 REDUCE, 4 ROUTE, 5 DISPATCH, 6 TILE_GU,
+ *               7 TILE_D, 8 PUSH, 9 FOLD), ticket, cta, pad.
+ * kosmos_trace_info() gives the ring's device address, the per-CTA capacity
+ * and the CTA count for the workspace of a call with these sizes. */
+typedef struct kosmos_trace_rec {
+    int64_t t_claim, t_ready, t_done;
+    int32_t kind, ticket, cta, pad;
+} kosmos_trace_rec;
+
+KOSMOS_API kosmos_status kosmos_trace_info(int op, int P, int64_t m, int64_t n, int64_t k, int dtype,
+                                const kosmos_opts *opts, void *ws, void **records,
+                                int32_t *per_cta_capacity, int32_t *num_ctas);
+
+/* Rail decode, for checking ticket order against an independent rail
+ * builder.  Writes 4 int32 {kind, a, b, c} per ticket of one rail:
+ *   op AG_GEMM: rail 0 = transfers {1, shard, piece, 0}; rail 1 = tiles
+ *               {2, shard, tile_row, tile_col}.  args: m = m_per_shard.
+ *   op GEMM_RS: rail 0 = tiles of rank `rank` {2, chunk, band, tile_col};
+ *               rail 1 = reductions of rank `rank` {3, rank, band, tile_col}.
+ * out is HOST memory of max_entries*4 int32; returns the rail length or -1.
+ * Runs the same decode functions the kernels use, compiled for the host. */
+KOSMOS_API int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail,
+                           int32_t *out, int64_t max_entries);
+
+/* Same decode executed by a device kernel (out is DEVICE memory). */
+KOSMOS_API int64_t kosmos_rail_decode_device(int op, int P, int64_t m, int64_t n, int order, int rank,
+                                  int rail, int32_t *out, int64_t max_entries, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KOSMOS_H */

@@ -1,0 +1,83 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/kosmos.h declares, validates arguments on the host, and its
+rail decode (the same functions the kernels run, compiled for the host)
+matches the oracle's independently built rails bit for bit."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+from _helpers import header_exports, kosmos
+
+
+@pytest.fixture(scope="module")
+def K():
+    return kosmos()
+
+
+def test_exports_every_declared_symbol(K):
+    names = header_exports()
+    assert len(names) >= 12
+    lib = C.CDLL(K.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(K.EXPORTS) == names
+
+
+def test_default_opts(K):
+    o = K.opts()
+    assert o.sched == K.SCHED_SELF and o.n_comm0 == -1 and o.order == K.ORDER_BAND
+    assert o.num_ctas == -1 and o.trace == 0 and o.inject == 0
+
+
+def test_workspace_sizes(K):
+    ag = K.workspace_bytes(K.OP_AG_GEMM, 8, 1024, 3584, 8192)
+    assert ag >= 256 + 8 * 8 * 4
+    rs = K.workspace_bytes(K.OP_GEMM_RS, 8, 8192, 8192, 3584)
+    assert rs >= 8 * 8192 * 8192 * 2  # bf16 partials of every rank
+    assert K.workspace_bytes(K.OP_GEMM_RS, 3, 100, 256, 64) == 0  # m % P != 0
+    assert K.workspace_bytes(K.OP_AG_GEMM, 9, 64, 64, 64) == 0     # P > 8
+    t = K.workspace_bytes(K.OP_AG_GEMM, 8, 1024, 3584, 8192, o=K.opts(trace=1))
+    assert t > ag
+
+
+def test_host_validation_rejects_bad_args(K):
+    lib = K.lib()
+    P = 2
+    buf = (C.c_uint8 * 4096)()
+    base = (C.addressof(buf) + 15) // 16 * 16
+    xs = (C.c_void_p * P)(base, base)
+    # P out of range
+    assert lib.kosmos_ag_gemm(xs, None, 0, 64, 128, 128, base, None, 0, base, base, base, 4096, None, None) == 1
+    assert lib.kosmos_ag_gemm(xs, None, 9, 64, 128, 128, base, None, 0, base, base, base, 4096, None, None) == 1
+    # k not a multiple of 64, n not a multiple of 8
+    assert lib.kosmos_ag_gemm(xs, None, P, 64, 100, 128, base, None, 0, base, base, base, 4096, None, None) == 1
+    assert lib.kosmos_ag_gemm(xs, None, P, 64, 128, 100, base, None, 0, base, base, base, 4096, None, None) == 1
+    # misaligned pointer
+    bad = (C.c_void_p * P)(base + 2, base)
+    assert lib.kosmos_ag_gemm(bad, None, P, 64, 128, 128, base, None, 0, base, base, base, 4096, None, None) == 1
+    # null output
+    assert lib.kosmos_ag_gemm(xs, None, P, 64, 128, 128, base, None, 0, base, None, base, 4096, None, None) == 1
+    # workspace too small
+    assert lib.kosmos_ag_gemm(xs, None, P, 64, 128, 128, base, None, 0, base, base, base, 16, None, None) == 3
+    # RS: m not divisible by P
+    ys = (C.c_void_p * P)(base, base)
+    assert lib.kosmos_gemm_rs(xs, xs, P, 63, 64, 64, 0, ys, base, 1 << 20, None, None) == 1
+    # quantiser: blocked extent not a multiple of 32
+    assert lib.kosmos_mxfp8_quantize(base, 4, 48, 1, base, base, None) == 1
+
+
+@pytest.mark.parametrize("P,m,n", [(2, 64, 128), (8, 1024, 3584), (3, 200, 264), (1, 5, 8)])
+def test_ag_rail_decode_matches_oracle(K, orc, P, m, n):
+    tr, tl = orc.rail_ag(P, m, n, R=128, BN=256)
+    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=0), tr)
+    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=1), tl)
+
+
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("P,m,n", [(8, 8192, 8192), (3, 600, 520), (1, 128, 256)])
+def test_rs_rail_decode_matches_oracle(K, orc, P, m, n, order):
+    for r in range(P):
+        tl, rd = orc.rail_rs(P, m, n, rank=r, order=order, R=128, BN=256)
+        assert np.array_equal(K.rail_decode(K.OP_GEMM_RS, P, m, n, rail=0, order=order, rank=r), tl)
+        assert np.array_equal(K.rail_decode(K.OP_GEMM_RS, P, m, n, rail=1, order=order, rank=r), rd)

@@ -1,0 +1,143 @@
+"""GPU parity of the all-gather + GEMM kernel against the fp64 CPU oracle.
+
+Tolerance: max|y - ref| <= 1e-2 * max|ref| (bf16 output, fp32 accumulation).
+The gathered buffer must equal the concatenated shards byte for byte, and
+repeated runs must be bit-identical (fixed K order per tile, no split-K)."""
+import numpy as np
+import pytest
+import torch
+
+from _helpers import bf16_tensor_to_f64, kosmos, rel_err
+from kosmos_inputs import WORKLOADS, ag_inputs, bf16_bits, sample_indices
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return kosmos()
+
+
+def _run(K, inp, o, reps=1):
+    xs = [x.cuda() for x in inp["x"]]
+    w = inp["w"].cuda()
+    P = len(xs)
+    m, k = xs[0].shape
+    n = w.shape[1]
+    xg = torch.empty(P * m, k, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(P * m, n, dtype=torch.bfloat16, device="cuda")
+    ws = K.workspace(K.OP_AG_GEMM, P, m, n, k, o=o)
+    outs = []
+    for _ in range(reps):
+        y.fill_(float("nan"))
+        xg.zero_()
+        K.ag_gemm(xs, w, xg, y, ws, o)
+        K.check(ws, "ag_gemm")
+        outs.append(y.clone())
+    return xs, xg, outs, ws
+
+
+def _check_full(orc, K, inp, o):
+    xs, xg, outs, _ = _run(K, inp, o, reps=2)
+    ref = orc.ag_gemm([bf16_bits(x) for x in inp["x"]], bf16_bits(inp["w"]))
+    got = bf16_tensor_to_f64(outs[0])
+    assert not np.isnan(got).any()
+    assert rel_err(got, ref) <= TOL, rel_err(got, ref)
+    assert torch.equal(outs[0], outs[1]), "reruns differ"
+    assert torch.equal(xg.cpu(), torch.cat(inp["x"], 0)), "gathered buffer differs from the shards"
+
+
+SCHEDS = {"self": 0, "fixed": 1, "unfused": 2}
+
+
+@pytest.mark.parametrize("sched", list(SCHEDS))
+def test_ag_tiny_workload(K, orc, sched):
+    w = WORKLOADS["ag_tiny_p2"]
+    inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
+    _check_full(orc, K, inp, K.opts(sched=SCHEDS[sched]))
+
+
+@pytest.mark.parametrize("sched", list(SCHEDS))
+@pytest.mark.parametrize("P,m,k,n", [(3, 200, 192, 264), (1, 130, 128, 256), (4, 128, 320, 512),
+                                     (2, 37, 64, 8)])
+def test_ag_ragged_multi_tile(K, orc, sched, P, m, k, n):
+    inp = ag_inputs(P, m, k, n, seed=1000 + P * m + n, var_w=1.0 / k)
+    _check_full(orc, K, inp, K.opts(sched=SCHEDS[sched]))
+
+
+@pytest.mark.parametrize("n_comm0", [1, 8, 40])
+def test_ag_mover_counts(K, orc, n_comm0):
+    inp = ag_inputs(8, 256, 256, 512, seed=77, var_w=1.0 / 256)
+    _check_full(orc, K, inp, K.opts(n_comm0=n_comm0))
+
+
+def test_ag_few_ctas(K, orc):
+    """A grid much smaller than the tile count: CTAs loop over many entries."""
+    inp = ag_inputs(4, 384, 256, 768, seed=5, var_w=1.0 / 256)
+    _check_full(orc, K, inp, K.opts(num_ctas=6, n_comm0=2))
+    _check_full(orc, K, inp, K.opts(num_ctas=3, sched=1, fixed_comm_ctas=1))
+
+
+@pytest.mark.parametrize("sched", list(SCHEDS))
+def test_ag_full_size_sampled(K, orc, sched):
+    """The 8-rank 1024x8192 . 8192x3584 workload in the benchmark's launch
+    configuration, checked on sampled rows (every shard's first and last row
+    included) and for bit-identical reruns."""
+    w = WORKLOADS["ag_bf16_p8"]
+    inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
+    xs, xg, outs, _ = _run(K, inp, K.opts(sched=SCHEDS[sched]), reps=2)
+    rows = np.unique(np.concatenate([sample_indices(w.P * w.m, 24, seed=1),
+                                     np.arange(w.P) * w.m, np.arange(w.P) * w.m + w.m - 1]))
+    ref = orc.ag_gemm([bf16_bits(x) for x in inp["x"]], bf16_bits(inp["w"]), rows=rows)
+    got = bf16_tensor_to_f64(outs[0][torch.from_numpy(rows).cuda()])
+    assert rel_err(got, ref) <= TOL, rel_err(got, ref)
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(xg, torch.cat(xs, 0))
+
+
+def test_ag_rail_decode_device_matches_oracle(K, orc):
+    for (P, m, n) in [(8, 1024, 3584), (3, 200, 264)]:
+        tr, tl = orc.rail_ag(P, m, n)
+        assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=0), tr)
+        assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=1), tl)
+
+
+def test_ag_trace_every_entry_once(K, orc):
+    inp = ag_inputs(4, 256, 128, 512, seed=3, var_w=1.0 / 128)
+    o = K.opts(trace=1)
+    xs, xg, outs, ws = _run(K, inp, o)
+    recs = K.trace_records(K.OP_AG_GEMM, 4, 256, 512, 128, ws, o)
+    tr, tl = orc.rail_ag(4, 256, 512)
+    tiles = np.sort(recs["ticket"][recs["kind"] == 2])
+    transfers = np.sort(recs["ticket"][recs["kind"] == 1])
+    assert np.array_equal(tiles, np.arange(len(tl)))
+    assert np.array_equal(transfers, np.arange(len(tr)))
+    t = recs[recs["kind"] == 2]
+    assert np.all(t["t_done"] >= t["t_ready"]) and np.all(t["t_ready"] >= t["t_claim"])
+
+
+def test_ag_dropped_transfer_times_out_then_recovers(K, orc):
+    """A transfer whose flag is never released: the waiting tile's bounded wait
+    runs out, the call reports TIMEOUT with that tile's ticket, and after a
+    workspace re-init the next call is correct."""
+    P, m, k, n = 2, 128, 128, 256
+    inp = ag_inputs(P, m, k, n, seed=9, var_w=1.0 / k)
+    xs = [x.cuda() for x in inp["x"]]
+    w = inp["w"].cuda()
+    xg = torch.empty(P * m, k, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(P * m, n, dtype=torch.bfloat16, device="cuda")
+    o = K.opts(inject=K.INJECT_DROP_TRANSFER | (0 << 32), wait_limit_ns=2_000_000)
+    ws = K.workspace(K.OP_AG_GEMM, P, m, n, k, o=o)
+    K.ag_gemm(xs, w, xg, y, ws, o)
+    st, entry = K.status_sync(ws)
+    assert st == K.ERR_TIMEOUT
+    # transfer 0 is shard 1 piece 0, consumed by tile tickets 1 (shard 1, row 0, col 0)
+    assert entry == 1
+    K.workspace_init(ws)
+    K.ag_gemm(xs, w, xg, y, ws, K.opts())
+    K.check(ws)
+    ref = orc.ag_gemm([bf16_bits(x) for x in inp["x"]], bf16_bits(inp["w"]))
+    assert rel_err(bf16_tensor_to_f64(y), ref) <= TOL
