@@ -1,12 +1,326 @@
 // gemm_rs.cu -- GEMM + reduce-scatter as one self-scheduling persistent launch.
+//
+// Y = sum_r X_r . W_r, scattered as P row chunks (KOSMOS explainer, paragraph
+// "Start with the problem": scatter and add the partial results).  All P
+// emulated ranks run in one launch: CTA c plays rank c mod P.  Per rank r two
+// rails:
+//   tile rail    TILE(chunk, band, col): the partial X_r . W_r on one 128x256
+//                tile, rounded to bf16 into rank r's partial buffer, then one
+//                release-increment of that output tile's arrival counter;
+//                band order (band, chunk, col) or the row-order ablation
+//                (chunk, band, col) (explainer, "Role switching only works");
+//   reduce rail  REDUCE(band, col) of rank r's own chunk: acquire counter == P,
+//                sum the P partials in rank order 0..P-1 in fp32, round once
+//                to bf16 into y_chunks[r].
+// Builders whose tile rail runs out join their rank's reduction (one-way,
+// explainer "KOSMOS removes the manager"); n_comm CTAs per rank reduce from
+// the start.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
 #include "engine.cuh"
 #include "launch.h"
 
 namespace kosmos {
 
+enum RsMode : int { RS_FUSED = 0, RS_TILES_ONLY = 1, RS_REDUCE_ONLY = 2 };
+
+struct RsParams {
+    CUtensorMap tmX[KOSMOS_MAX_P];  // X_r viewed [P chunks][mc][k]: dims {k, mc, P}, box {64, 128, 1}, 128B swizzle
+    CUtensorMap tmW[KOSMOS_MAX_P];  // W_r: dims {n, k}, box {64, 64}, 128B swizzle
+    CUtensorMap tmPart;             // partials [rank][chunk][mc][n]: dims {n, mc, P, P}, box {256, 8, 1, P}
+    __nv_bfloat16 *part;            // [P ranks][m][n]
+    __nv_bfloat16 *y[KOSMOS_MAX_P]; // chunk c: [mc][n]
+    WsHeader *ws;
+    uint32_t *arrive;               // [chunk][band][col] arrival counters
+    TraceRec *trace;
+    RsGeom g;
+    int nkb;
+    int sched;
+    int n_red;
+    int order;
+    int mode;
+    int pad;
+    uint64_t wait_limit_ns;
+    uint64_t inject;
+};
+
+__device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
+    const int cta = blockIdx.x;
+    const int P = p.g.P;
+    const int rank = cta % P;
+    const int local = cta / P;
+    bool reducer = (p.mode == RS_REDUCE_ONLY) || (p.mode == RS_FUSED && local < p.n_red);
+    PipeState ps;
+    RingState rs;
+    int nrec = 0;
+    const uint32_t red_bytes = static_cast<uint32_t>(BN * RED_ROWS * 2 * P);
+    while (true) {
+        if (failed(p.ws)) break;
+        if (!reducer) {
+            const uint32_t t = atomicAdd(&p.ws->tickets[rank], 1u);
+            if (t < static_cast<uint32_t>(p.g.n_tile)) {
+                int chunk, band, tcol;
+                rs_decode_tile(p.g, p.order, static_cast<int>(t), chunk, band, tcol);
+                int slot = -1;
+                if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
+                    const int64_t now = static_cast<int64_t>(globaltimer());
+                    r->t_claim = now; r->t_ready = now; r->t_done = 0;
+                    r->kind = K_TILE; r->ticket = static_cast<int32_t>(t); r->cta = cta;
+                    slot = nrec;
+                }
+                ++nrec;
+                SchedEntry e;
+                e.kind = K_TILE; e.a = chunk; e.b = band; e.c = tcol; e.d = rank; e.nstage = p.nkb;
+                e.ticket = static_cast<int32_t>(t); e.slot = slot;
+                if (!ring_push(sm, rs, e, p.ws)) break;
+                bool ok = true;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                        set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = sm.stages + ps.stage * STAGE_BYTES;
+                    uint8_t *sb = sa + A_STAGE_BYTES;
+                    uint64_t *bar = &sm.full[ps.stage];
+                    mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                    tma_load_3d(sa, &p.tmX[rank], bar, kb * BK, band * BM, chunk);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sb + j * (64 * BK * 2), &p.tmW[rank], bar, tcol * BN + j * 64, kb * BK);
+                    ps.advance();
+                }
+                if (!ok) break;
+                continue;
+            }
+            if (p.mode == RS_TILES_ONLY || p.sched == KOSMOS_SCHED_FIXED) break;
+            reducer = true;  // one-way switch: builder -> reducer
+        }
+        const uint32_t t = atomicAdd(&p.ws->tickets[KOSMOS_MAX_P + rank], 1u);
+        if (t >= static_cast<uint32_t>(p.g.n_reduce)) break;
+        int band, tcol;
+        rs_decode_reduce(p.g, static_cast<int>(t), band, tcol);
+        const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+        if (p.mode == RS_FUSED) {
+            uint32_t *ctr = &p.arrive[(static_cast<int64_t>(rank) * p.g.bands + band) * p.g.tiles_n + tcol];
+            if (!wait_flag_eq(p.ws, ctr, static_cast<uint32_t>(P), p.wait_limit_ns,
+                              (static_cast<int64_t>(1) << 40) | (static_cast<int64_t>(rank) << 32) | t))
+                break;
+            st_relaxed_gpu(ctr, 0u);  // sole consumer: return the counter to zero for the next call
+        }
+        int slot = -1;
+        if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
+            r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
+            r->kind = K_REDUCE; r->ticket = static_cast<int32_t>(t); r->cta = cta;
+            slot = nrec;
+        }
+        ++nrec;
+        const int64_t rows = (p.g.mc - static_cast<int64_t>(band) * BM) < BM ? (p.g.mc - static_cast<int64_t>(band) * BM) : BM;
+        const int nsub = static_cast<int>(cdiv(rows, RED_ROWS));
+        SchedEntry e;
+        e.kind = K_REDUCE; e.a = rank; e.b = band; e.c = tcol; e.d = rank; e.nstage = nsub;
+        e.ticket = static_cast<int32_t>(t); e.slot = slot;
+        if (!ring_push(sm, rs, e, p.ws)) break;
+        bool ok = true;
+        for (int s = 0; s < nsub; ++s) {
+            if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                ok = false;
+                break;
+            }
+            uint64_t *bar = &sm.full[ps.stage];
+            mbar_arrive_expect_tx(bar, red_bytes);
+            tma_load_4d(sm.stages + ps.stage * STAGE_BYTES, &p.tmPart, bar, tcol * BN, band * BM + s * RED_ROWS,
+                        rank, 0);
+            ps.advance();
+        }
+        if (!ok) break;
+    }
+    SchedEntry done;
+    done.kind = K_DONE; done.a = done.b = done.c = done.d = 0; done.nstage = 0; done.ticket = -1; done.slot = -1;
+    ring_push(sm, rs, done, p.ws);
+}
+
+__device__ __forceinline__ void rs_epilogue(const RsParams &p, const Smem &sm, uint32_t tmem_base, int warp,
+                                            int lane) {
+    const int grp = warp & 3;
+    const int row = grp * 32 + lane;       // accumulator row of this thread
+    const int et = (warp - 2) * 32 + lane; // 0..127 within the epilogue warps
+    const int P = p.g.P;
+    RingState rs;
+    PipeState ps;
+    uint32_t acc = 0, acc_phase = 0;
+    while (true) {
+        if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -6);
+            break;
+        }
+        const SchedEntry e = sm.sched[rs.idx];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sempty[rs.idx]);
+        rs.advance();
+        if (e.kind == K_DONE) break;
+        if (e.kind == K_TILE) {
+            if (!mbar_wait(&sm.tfull[acc], acc_phase, PIPE_LIMIT_NS)) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
+                break;
+            }
+            tc_fence_after();
+            const int chunk = e.a, band = e.b, tcol = e.c, rank = e.d;
+            const int64_t rloc = static_cast<int64_t>(band) * BM + row;
+            const bool valid = rloc < p.g.mc;
+            __nv_bfloat16 *dst = p.part + (static_cast<int64_t>(rank) * p.g.m + static_cast<int64_t>(chunk) * p.g.mc +
+                                           (valid ? rloc : 0)) * p.g.n;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                const int64_t col0 = static_cast<int64_t>(tcol) * BN + ch * 32;
+                if (col0 >= p.g.n) break;
+                const int64_t left = p.g.n - col0;
+                tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + col0, left < 32 ? static_cast<int>(left) : 32);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            ps.advance(e.nstage);
+            if (p.mode == RS_FUSED) {
+                __threadfence();
+                named_bar_sync(1, NUM_EPI_THREADS);
+                const bool drop = (p.inject & KOSMOS_INJECT_DROP_PARTIAL) && static_cast<int>(p.inject >> 32) == rank;
+                if (et == 0 && !drop)
+                    red_release_add_gpu(&p.arrive[(static_cast<int64_t>(chunk) * p.g.bands + band) * p.g.tiles_n + tcol], 1u);
+            }
+            if (e.slot >= 0 && et == 0) {
+                if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+            }
+        } else if (e.kind == K_REDUCE) {
+            const int chunk = e.a, band = e.b, tcol = e.c;
+            const int cg = et & 31;           // 16-byte column group of the 256-wide tile
+            const int64_t col = static_cast<int64_t>(tcol) * BN + cg * 8;
+            bool ok = true;
+            for (int s = 0; s < e.nstage; ++s) {
+                if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
+                    ok = false;
+                    break;
+                }
+                const uint8_t *buf = sm.stages + ps.stage * STAGE_BYTES;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r8 = (et >> 5) * 2 + rr;  // row within the 8-row stage
+                    float a[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) a[q] = 0.f;
+                    for (int rk = 0; rk < P; ++rk) {    // fixed rank order 0..P-1
+                        const uint4 v = *reinterpret_cast<const uint4 *>(buf + ((rk * RED_ROWS + r8) * BN + cg * 8) * 2);
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            a[2 * q] += __uint_as_float(w[q] << 16);
+                            a[2 * q + 1] += __uint_as_float(w[q] & 0xFFFF0000u);
+                        }
+                    }
+                    const int64_t grow = static_cast<int64_t>(band) * BM + s * RED_ROWS + r8;
+                    if (grow < p.g.mc && col < p.g.n) {
+                        uint4 o;
+                        o.x = pack_bf16x2(a[0], a[1]);
+                        o.y = pack_bf16x2(a[2], a[3]);
+                        o.z = pack_bf16x2(a[4], a[5]);
+                        o.w = pack_bf16x2(a[6], a[7]);
+                        *reinterpret_cast<uint4 *>(p.y[chunk] + grow * p.g.n + col) = o;
+                    }
+                }
+                named_bar_sync(1, NUM_EPI_THREADS);
+                if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
+                ps.advance();
+            }
+            if (!ok) break;
+            if (e.slot >= 0 && et == 0) {
+                if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+            }
+        } else {
+            ps.advance(e.nstage);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_rs_kernel(const __grid_constant__ RsParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem sm = carve_smem(smem_raw);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
+    engine_setup(sm, warp);
+    const uint32_t tmem_base = *sm.tmem_slot;
+    if (warp == 0) {
+        if (lane == 0) rs_producer(p, sm);
+    } else if (warp == 1) {
+        if (lane == 0) mma_loop(sm, tmem_base, p.ws);
+    } else {
+        rs_epilogue(p, sm, tmem_base, warp, lane);
+    }
+    engine_teardown(sm, warp, tmem_base);
+    if (threadIdx.x == 0) engine_finish(p.ws, epoch, 2 * KOSMOS_MAX_P);
+}
+
 kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
-    (void)L; (void)stream;
-    return KOSMOS_ERR_UNSUPPORTED;
+    RsParams p;
+    memset(&p, 0, sizeof(p));
+    p.g = rs_geom(L.P, L.m, L.k, L.n);
+    const int64_t mc = p.g.mc;
+    for (int r = 0; r < L.P; ++r) {
+        {
+            const uint64_t dims[3] = {static_cast<uint64_t>(L.k), static_cast<uint64_t>(mc), static_cast<uint64_t>(L.P)};
+            const uint64_t strides[2] = {static_cast<uint64_t>(L.k) * 2, static_cast<uint64_t>(mc * L.k) * 2};
+            const uint32_t box[3] = {BK, BM, 1};
+            if (!encode_tmap(&p.tmX[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(L.x[r]), dims, strides,
+                             box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return KOSMOS_ERR_CUDA;
+        }
+        {
+            const uint64_t dims[2] = {static_cast<uint64_t>(L.n), static_cast<uint64_t>(L.k)};
+            const uint64_t strides[1] = {static_cast<uint64_t>(L.n) * 2};
+            const uint32_t box[2] = {64, BK};
+            if (!encode_tmap(&p.tmW[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(L.w[r]), dims, strides,
+                             box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return KOSMOS_ERR_CUDA;
+        }
+        p.y[r] = static_cast<__nv_bfloat16 *>(L.y[r]);
+    }
+    const RsWsLayout W = rs_ws_layout(p.g, L.trace != 0);
+    uint8_t *ws = static_cast<uint8_t *>(L.ws);
+    p.ws = reinterpret_cast<WsHeader *>(ws);
+    p.arrive = reinterpret_cast<uint32_t *>(ws + W.arrive_off);
+    p.part = reinterpret_cast<__nv_bfloat16 *>(ws + W.partial_off);
+    p.trace = L.trace ? reinterpret_cast<TraceRec *>(ws + W.trace_off) : nullptr;
+    {
+        const uint64_t dims[4] = {static_cast<uint64_t>(L.n), static_cast<uint64_t>(mc), static_cast<uint64_t>(L.P),
+                                  static_cast<uint64_t>(L.P)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(L.n) * 2, static_cast<uint64_t>(mc * L.n) * 2,
+                                     static_cast<uint64_t>(L.m * L.n) * 2};
+        const uint32_t box[4] = {BN, RED_ROWS, 1, static_cast<uint32_t>(L.P)};
+        if (!encode_tmap(&p.tmPart, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.part, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return KOSMOS_ERR_CUDA;
+    }
+    p.nkb = static_cast<int>(L.k / BK);
+    p.sched = L.sched;
+    p.n_red = L.n_comm;
+    p.order = L.order;
+    p.wait_limit_ns = L.wait_limit_ns;
+    p.inject = L.inject;
+    if (L.sched == KOSMOS_SCHED_UNFUSED) {
+        p.mode = RS_TILES_ONLY;
+        const kosmos_status s1 = launch_persistent(reinterpret_cast<const void *>(&gemm_rs_kernel), &p, L.grid,
+                                                   SMEM_BYTES, stream);
+        if (s1 != KOSMOS_OK) return s1;
+        p.mode = RS_REDUCE_ONLY;
+        return launch_persistent(reinterpret_cast<const void *>(&gemm_rs_kernel), &p, L.grid, SMEM_BYTES, stream);
+    }
+    p.mode = RS_FUSED;
+    return launch_persistent(reinterpret_cast<const void *>(&gemm_rs_kernel), &p, L.grid, SMEM_BYTES, stream);
 }
 
 }  // namespace kosmos
