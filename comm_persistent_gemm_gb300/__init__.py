@@ -29,7 +29,7 @@ KIND_NAMES = {1: "TRANSFER", 2: "TILE", 3: "REDUCE", 4: "ROUTE", 5: "DISPATCH", 
 
 EXPORTS = ["kosmos_default_opts", "kosmos_num_sms", "kosmos_workspace_bytes", "kosmos_workspace_init",
            "kosmos_ag_gemm", "kosmos_gemm_rs", "kosmos_moe_fwd", "kosmos_mxfp8_quantize", "kosmos_status_sync",
-           "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device"]
+           "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device", "kosmos_ag_gemm_noalloc"]
 
 
 class KosmosError(RuntimeError):
@@ -94,6 +94,8 @@ def lib():
     L.kosmos_rail_decode.restype = i64
     L.kosmos_rail_decode_device.argtypes = [i32, i32, i64, i64, i32, i32, i32, vp, i64, vp]
     L.kosmos_rail_decode_device.restype = i64
+    L.kosmos_ag_gemm_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, i32, vp, vp, C.POINTER(Opts), vp]
+    L.kosmos_ag_gemm_noalloc.restype = i32
     _lib = L
     return L
 
@@ -173,6 +175,22 @@ def ag_gemm(x_shards: List, w, x_gathered, y, ws, o: Optional[Opts] = None, dtyp
                               x_gathered.data_ptr(), y.data_ptr(), ws.data_ptr(), ws.numel(),
                               C.byref(o) if o is not None else None, _stream(stream))
     _raise(rc, "kosmos_ag_gemm")
+
+
+def ag_gemm_noalloc(x_shards: List, w, x_gathered, y, o: Optional[Opts] = None, dtype: int = BF16,
+                    x_scales: Optional[List] = None, w_scales=None, stream=None):
+    """ag_gemm with the library's own static scratch instead of a workspace
+    (for callers that cannot allocate device memory)."""
+    _check_cuda(*x_shards, w, x_gathered, y, *(x_scales or []), w_scales)
+    P = len(x_shards)
+    m, k = x_shards[0].shape
+    n = w.shape[1]
+    xsc = _ptrs(x_scales) if x_scales is not None else None
+    rc = lib().kosmos_ag_gemm_noalloc(_ptrs(x_shards), xsc, P, m, k, n, w.data_ptr(),
+                                      w_scales.data_ptr() if w_scales is not None else None, dtype,
+                                      x_gathered.data_ptr(), y.data_ptr(), C.byref(o) if o is not None else None,
+                                      _stream(stream))
+    _raise(rc, "kosmos_ag_gemm_noalloc")
 
 
 def gemm_rs(x_shards: List, w_shards: List, y_chunks: List, ws, o: Optional[Opts] = None, stream=None):

@@ -1,0 +1,77 @@
+// static_ws.cu -- all-gather + GEMM for callers that cannot allocate device
+// memory.
+//
+// Some callers cannot hand this library a workspace: a plugin behind an
+// operator interface with no scratch argument, or code that must not call the
+// device allocator while it runs (a caller whose allocator owns all device
+// memory, or a latency-critical path that forbids allocation).  For them,
+// kosmos_ag_gemm_noalloc keeps the ticket counters, readiness flags and
+// status word in the file-scope array below instead of a caller workspace.
+//
+// The array is a __device__ symbol: in host code its name is only a host-side
+// stand-in, never a device address.  The device address is obtained once per
+// device with cudaGetSymbolAddress (with that device current) and passed to
+// the kernel like any workspace pointer.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/kosmos.h"
+
+namespace {
+
+// Held by every GPU that loads this library until the process exits.
+__device__ __align__(256) unsigned char g_kosmos_static_ws[KOSMOS_STATIC_WS_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void *g_ws_ptr[kMaxDevices] = {};
+
+// Device address of g_kosmos_static_ws on the current device, looked up on
+// the first call made with that device current.
+kosmos_status static_ws_address(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return KOSMOS_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_ws_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_kosmos_static_ws);
+        if (e != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            return KOSMOS_ERR_CUDA;
+        }
+        g_ws_ptr[dev] = p;
+    }
+    *out = g_ws_ptr[dev];
+    return KOSMOS_OK;
+}
+
+}  // namespace
+
+extern "C" KOSMOS_API kosmos_status kosmos_ag_gemm_noalloc(const void *const *x_shards, const void *const *x_scales,
+                                                           int P, int64_t m_per_shard, int64_t k, int64_t n,
+                                                           const void *w, const void *w_scales, int dtype,
+                                                           void *x_gathered, void *y, const kosmos_opts *opts,
+                                                           void *stream) {
+    kosmos_opts o;
+    kosmos_default_opts(&o);
+    if (opts) o = *opts;
+    if (o.trace) return KOSMOS_ERR_UNSUPPORTED;  // the trace ring does not fit the static scratch
+    const size_t need = kosmos_workspace_bytes(KOSMOS_OP_AG_GEMM, P, m_per_shard, n, k, dtype, &o);
+    if (need == 0) return KOSMOS_ERR_INVALID_ARG;
+    if (need > static_cast<size_t>(KOSMOS_STATIC_WS_BYTES)) return KOSMOS_ERR_WORKSPACE;
+    void *ws = nullptr;
+    const kosmos_status s = static_ws_address(&ws);
+    if (s != KOSMOS_OK) return s;
+    // The array keeps the previous call's counters, flags and status: clear the
+    // part this call uses so it starts from zero.
+    if (cudaMemsetAsync(ws, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KOSMOS_ERR_CUDA;
+    }
+    return kosmos_ag_gemm(x_shards, x_scales, P, m_per_shard, k, n, w, w_scales, dtype, x_gathered, y, ws,
+                          static_cast<size_t>(KOSMOS_STATIC_WS_BYTES), &o, stream);
+}

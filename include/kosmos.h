@@ -206,6 +206,40 @@ KOSMOS_API kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void 
 KOSMOS_API kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols,
                                     void *q, void *scales, void *stream);
 
+/* Size in bytes of the scratch array that kosmos_ag_gemm_noalloc uses. */
+#define KOSMOS_STATIC_WS_BYTES 65536
+
+/*
+ * All-gather + GEMM without a workspace, for callers that cannot allocate
+ * device memory (a plugin behind an operator interface with no scratch
+ * argument, or code that must not call the device allocator while it runs).
+ * The KOSMOS pages have no counterpart to this entry point: it is a
+ * packaging variant of kosmos_ag_gemm with the same arguments, minus ws and
+ * ws_bytes, and the same results.
+ *
+ * Scratch: a file-scope __device__ array of KOSMOS_STATIC_WS_BYTES (64 KiB)
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  Calls whose workspace would exceed it (see
+ * kosmos_workspace_bytes) return KOSMOS_ERR_WORKSPACE; opts.trace is not
+ * supported (KOSMOS_ERR_UNSUPPORTED).  The 8-rank 1024 x 8192 x 3584 call
+ * needs 512 bytes.
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.
+ * Every call shares the one array per device: each call first clears the part
+ * it uses on `stream`, so calls that overlap on the GPU (different streams,
+ * or different host threads without ordering) race and give wrong results.
+ * Device-side wait failures are not reported back (the array is cleared by
+ * the next call); use kosmos_ag_gemm with a workspace when the device status
+ * is needed.  Allocates no memory: no cudaMalloc, cudaFree or allocating
+ * library routine.
+ */
+KOSMOS_API kosmos_status kosmos_ag_gemm_noalloc(const void *const *x_shards, const void *const *x_scales, int P,
+                                                int64_t m_per_shard, int64_t k, int64_t n,
+                                                const void *w, const void *w_scales, int dtype,
+                                                void *x_gathered, void *y, const kosmos_opts *opts,
+                                                void *stream);
+
 /* Synchronises `stream`, then returns the device status of the last call
  * that used `ws` (KOSMOS_OK, KOSMOS_ERR_TIMEOUT or KOSMOS_ERR_DEVICE) and,
  * if failing_entry is not NULL, the ticket of the entry that failed (-1 if
