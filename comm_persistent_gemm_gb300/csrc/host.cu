@@ -230,8 +230,8 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
         int n_red = o.n_comm0 >= 0 ? o.n_comm0 : 1;
         if (o.sched == KOSMOS_SCHED_FIXED && o.fixed_comm_ctas >= 0) n_red = o.fixed_comm_ctas;
         if (n_red < 1) n_red = 1;
-        if (per_rank > 1 && n_red > per_rank - 1) n_red = per_rank - 1;
-        if (per_rank == 1 && o.sched == KOSMOS_SCHED_FIXED) return KOSMOS_ERR_INVALID_ARG;
+        if (n_red > per_rank - 1) n_red = per_rank - 1;  // keep a builder on every rank
+        if (n_red < 1 && o.sched == KOSMOS_SCHED_FIXED) return KOSMOS_ERR_INVALID_ARG;
         L.n_comm = n_red;
     }
     L.order = o.order; L.trace = o.trace; L.grid = grid;
