@@ -165,6 +165,102 @@ def time_kernel_steps(fn, steps, warmup, flush, stream):
     return times
 
 
+def _split_experts(w, P):
+    E = w.shape[0]
+    return [w[q * (E // P):(q + 1) * (E // P)].contiguous() for q in range(P)]
+
+
+def bench_rs(K, dev, steps, warmup, flush, stream, peak):
+    """GEMM + reduce-scatter, 8 ranks x [8192, 3584] . [3584, 8192]: band order
+    (the method), the row-order ablation, the fixed-split crew sweep and the
+    unfused GEMM-then-reduce baseline."""
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS["rs_bf16_p8"]
+    inp = workload_inputs(w)
+    P, m, k, n = w.P, w.m, w.k, w.n
+    xs = [x.to(dev) for x in inp["x"]]
+    ws_ = [x.to(dev) for x in inp["w"]]
+    del inp
+    ys = [torch.empty(m // P, n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    flops = w.flops()
+
+    def timed(o):
+        wsb = K.workspace(K.OP_GEMM_RS, P, m, n, k, o=o, device=dev)
+        f = lambda: K.gemm_rs(xs, ws_, ys, wsb, o, stream=stream)
+        f()
+        K.check(wsb, "gemm_rs")
+        t = time_kernel_steps(f, steps, warmup, flush, stream)
+        K.check(wsb, "gemm_rs")
+        del wsb
+        return statistics.mean(t)
+
+    band = timed(K.opts(order=K.ORDER_BAND))
+    row = timed(K.opts(order=K.ORDER_ROW))
+    fixed = {}
+    for crew in (1, 2, 4, 6):
+        fixed[str(crew)] = flops / (timed(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=crew)) * 1e-3) / 1e12
+    unf = timed(K.opts(sched=K.SCHED_UNFUSED))
+    tf = flops / (band * 1e-3) / 1e12
+    best = max(fixed, key=fixed.get)
+    return {"workload": "rs_bf16_p8", "ms": band, "tflops": tf, "frac_of_peak": tf / peak,
+            "row_order_ms": row, "row_over_band": row / band,
+            "fixed_split_best": {"tflops": fixed[best], "crew_per_rank": int(best), "sweep": fixed},
+            "unfused": {"tflops": flops / (unf * 1e-3) / 1e12, "launches_per_step": 2},
+            "vs_fixed_split_best": tf / fixed[best], "vs_unfused": tf / (flops / (unf * 1e-3) / 1e12)}
+
+
+# Algorithmic HBM bytes of one MoE forward step (2048 tokens, hidden 4096,
+# 128 experts top-8, inter 1536, bf16): every expert weight read once
+# (128 x 3 x 4096 x 1536 x 2 = 4.83 GB), router weights, token reads and
+# writes of the dispatch (read x rows, write received rows), the grouped GEMMs'
+# reads of received rows, h writes and reads, y writes, push reads and writes,
+# fold reads of the slots and the output write.
+def moe_algorithmic_bytes(T, H, E, K, I):
+    rows = T * K
+    weights = E * 3 * H * I * 2 + H * E * 2
+    dispatch = 2 * rows * H * 2
+    gemm_in = rows * H * 2 + rows * I * 2
+    h_out = rows * I * 2
+    y_out = rows * H * 2
+    push = 2 * rows * H * 2
+    fold = rows * H * 2 + T * H * 2
+    router_in = T * H * 2
+    return weights + dispatch + gemm_in + h_out + y_out + push + fold + router_in
+
+
+def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak):
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS["moe_fwd_p8"]
+    inp = workload_inputs(w)
+    P, T, H, E, Kt, I = w.P, w.T, w.H, w.E, w.topk, w.I
+    xs = [t.to(dev) for t in torch.chunk(inp["x"], P, 0)]
+    wr = inp["w_router"].to(dev)
+    wg = [t.to(dev) for t in _split_experts(inp["w_gate"], P)]
+    wu = [t.to(dev) for t in _split_experts(inp["w_up"], P)]
+    wd = [t.to(dev) for t in _split_experts(inp["w_down"], P)]
+    del inp
+    ys = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    idx = torch.empty(T, Kt, dtype=torch.int32, device=dev)
+    gate = torch.empty(T, Kt, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    pos = torch.empty(T, Kt, dtype=torch.int32, device=dev)
+    wsb = K.moe_workspace(P, T, H, E, Kt, I, device=dev)
+    f = lambda: K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, wsb, Kt, stream=stream)
+    f()
+    K.check(wsb, "moe_fwd")
+    t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
+    K.check(wsb, "moe_fwd")
+    byt = moe_algorithmic_bytes(T, H, E, Kt, I)
+    gbs = byt / (t * 1e-3) / 1e9
+    return {"workload": "moe_fwd_p8", "ms": t, "tokens_per_s": T / (t * 1e-3),
+            "tflops": w.flops() / (t * 1e-3) / 1e12, "frac_of_tensor_peak": w.flops() / (t * 1e-3) / 1e12 / tensor_peak,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "bytes_per_launch": byt},
+            "launches_per_step": 1}
+
+
 def run_reference(args):
     ws, rank, local = dist_env()
     if ws > 1 and rank != 0:
@@ -224,6 +320,8 @@ def run_kosmos(args):
 
     flops = w.flops()
     sms = K.num_sms()
+    peaks, src = load_peaks()
+    peak = peaks["bf16_tflops"]
     o_self = K.opts()
     f_self, ws_self = make(o_self)
     # warm up + correctness gate of the timed configuration
@@ -299,13 +397,19 @@ def run_kosmos(args):
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
-    peaks, src = load_peaks()
-    peak = peaks["bf16_tflops"]
+
     achieved = flops / (step_ms * 1e-3) / 1e12
     traffic = TRAFFIC_CAPTURE["bytes"] if TRAFFIC_CAPTURE["src_sha"] == kernel_src_sha() else None
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic, "peak_source": f"{src} bf16 dense (burst)", "kernel": "ag_gemm_kernel",
             "flop_per_launch": flops}
+
+    also = {}
+    if not args.ag_only:
+        also["gemm_rs"] = bench_rs(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
+        torch.cuda.empty_cache()
+        also["moe_fwd"] = bench_moe(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"], peak)
+        torch.cuda.empty_cache()
 
     line = None
     if rank == 0:
@@ -319,7 +423,7 @@ def run_kosmos(args):
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": args.steps, "baselines": base,
                 "vs_fixed_split_best": value / world / base["fixed_split_best"]["tflops"],
-                "vs_unfused": value / world / base["unfused"]["tflops"]}
+                "vs_unfused": value / world / base["unfused"]["tflops"], "also": also}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.barrier()
@@ -333,6 +437,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kosmos", choices=["kosmos", "reference"])
+    ap.add_argument("--ag-only", action="store_true", help="skip the GEMM+RS and MoE measurements")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed region of the fused kernel (no baselines, e2e or CPU oracle): "
                          "a short launch list for profilers")

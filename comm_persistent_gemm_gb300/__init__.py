@@ -24,12 +24,15 @@ SCHED_SELF, SCHED_FIXED, SCHED_UNFUSED = 0, 1, 2
 ORDER_BAND, ORDER_ROW = 0, 1
 INJECT_DROP_TRANSFER = 0x1
 INJECT_DROP_PARTIAL = 0x2
+INJECT_IDENTITY_EXPERTS = 0x4
+MOE_VIEW_LOGITS, MOE_VIEW_RECV, MOE_VIEW_H, MOE_VIEW_Y, MOE_VIEW_SLOT, MOE_VIEW_OFFSETS, MOE_VIEW_TRACE = range(7)
 KIND_NAMES = {1: "TRANSFER", 2: "TILE", 3: "REDUCE", 4: "ROUTE", 5: "DISPATCH", 6: "TILE_GU", 7: "TILE_D",
               8: "PUSH", 9: "FOLD"}
 
 EXPORTS = ["kosmos_default_opts", "kosmos_num_sms", "kosmos_workspace_bytes", "kosmos_workspace_init",
            "kosmos_ag_gemm", "kosmos_gemm_rs", "kosmos_moe_fwd", "kosmos_mxfp8_quantize", "kosmos_status_sync",
-           "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device", "kosmos_ag_gemm_noalloc"]
+           "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device", "kosmos_ag_gemm_noalloc",
+           "kosmos_moe_workspace_bytes", "kosmos_moe_debug_view"]
 
 
 class KosmosError(RuntimeError):
@@ -96,6 +99,10 @@ def lib():
     L.kosmos_rail_decode_device.restype = i64
     L.kosmos_ag_gemm_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, i32, vp, vp, C.POINTER(Opts), vp]
     L.kosmos_ag_gemm_noalloc.restype = i32
+    L.kosmos_moe_workspace_bytes.argtypes = [i32, i64, i64, i32, i32, i64, C.POINTER(Opts)]
+    L.kosmos_moe_workspace_bytes.restype = C.c_size_t
+    L.kosmos_moe_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, vp, C.POINTER(vp), C.POINTER(i64)]
+    L.kosmos_moe_debug_view.restype = i32
     _lib = L
     return L
 
@@ -218,6 +225,28 @@ def moe_fwd(x_shards: List, w_router, w_gate: List, w_up: List, w_down: List, y_
                               topk_gate.data_ptr(), expert_counts.data_ptr(), dispatch_pos.data_ptr(),
                               ws.data_ptr(), ws.numel(), C.byref(o) if o is not None else None, _stream(stream))
     _raise(rc, "kosmos_moe_fwd")
+
+
+def moe_workspace(P: int, tokens: int, hidden: int, n_experts: int, topk: int, inter: int,
+                  o: Optional[Opts] = None, device=None):
+    """A zeroed workspace tensor (uint8) for kosmos_moe_fwd."""
+    import torch
+    nbytes = int(lib().kosmos_moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter,
+                                                  C.byref(o) if o is not None else None))
+    if nbytes == 0:
+        raise KosmosError(ERR_INVALID_ARG, "kosmos_moe_workspace_bytes")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_debug_view(what: int, P: int, tokens: int, hidden: int, n_experts: int, topk: int, inter: int, ws):
+    """A uint8 view (torch tensor slice of ws) of one internal MoE buffer."""
+    ptr = C.c_void_p()
+    nb = C.c_int64()
+    rc = lib().kosmos_moe_debug_view(what, P, tokens, hidden, n_experts, topk, inter, ws.data_ptr(),
+                                     C.byref(ptr), C.byref(nb))
+    _raise(rc, "kosmos_moe_debug_view")
+    off = ptr.value - ws.data_ptr()
+    return ws[off:off + nb.value]
 
 
 def mxfp8_quantize(x, q, scales, along_cols: bool, stream=None):

@@ -130,7 +130,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
         ++nrec;
         SchedEntry e;
         e.kind = K_TILE; e.a = s; e.b = i; e.c = c; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
-        e.slot = slot; e.d = 0;
+        e.slot = slot; e.d = 0; e.nmma = 0; e.x0 = e.x1 = e.x2 = 0;
         if (!ring_push(sm, rs, e, p.ws)) break;
         const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
         bool ok = true;
@@ -157,6 +157,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
     }
     SchedEntry done;
     done.kind = K_DONE; done.a = done.b = done.c = 0; done.nstage = 0; done.ticket = -1; done.slot = -1; done.d = 0;
+    done.nmma = 0; done.x0 = done.x1 = done.x2 = 0;
     ring_push(sm, rs, done, p.ws);
 }
 

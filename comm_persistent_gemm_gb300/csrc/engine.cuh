@@ -28,7 +28,13 @@ struct SchedEntry {
     int32_t ticket;
     int32_t slot;     // trace record index of this CTA, -1 when untraced
     int32_t d;        // extra field (op specific)
+    int32_t nmma;     // N of the MMA (0 = BN)
+    int32_t x0, x1, x2;  // extra fields (op specific)
 };
+
+__host__ __device__ __forceinline__ bool is_mma_kind(int32_t k) {
+    return k == K_TILE || k == K_ROUTE || k == K_TILE_GU || k == K_TILE_D;
+}
 
 struct Smem {
     uint8_t *stages;   // NSTAGE * STAGE_BYTES, 1024-byte aligned
@@ -42,7 +48,7 @@ struct Smem {
     SchedEntry *sched; // [NSCHED]
     uint32_t *tmem_slot;
 };
-constexpr int SMEM_CTRL_BYTES = 1024;
+constexpr int SMEM_CTRL_BYTES = 1024;  // barriers, entry ring, TMEM slot
 constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + SMEM_CTRL_BYTES + 1024;
 constexpr uint64_t PIPE_LIMIT_NS = 4000000000ull;  // internal pipeline waits: 4 s
 
@@ -200,10 +206,12 @@ __device__ __forceinline__ void mma_loop(const Smem &sm, uint32_t tmem_base, WsH
         mbar_arrive(&sm.sempty[rs.idx]);
         rs.advance();
         if (e.kind == K_DONE) break;
-        if (e.kind != K_TILE) {
+        if (!is_mma_kind(e.kind)) {
             ps.advance(e.nstage);
             continue;
         }
+        // N of this entry's MMA: a multiple of 16 in [16, 256] (0 selects BN)
+        const uint32_t idesc = (e.nmma > 0 && e.nmma < BN) ? idesc_bf16_f32(BM, e.nmma, false, true) : IDESC;
         if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, PIPE_LIMIT_NS)) {
             set_error(ws, KOSMOS_ERR_DEVICE, -4);
             break;
@@ -224,7 +232,7 @@ __device__ __forceinline__ void mma_loop(const Smem &sm, uint32_t tmem_base, WsH
             for (int k = 0; k < BK / UMMA_K; ++k) {
                 const uint64_t ad = sdesc_sw128(a_addr + k * (UMMA_K * 2), 16, 1024);
                 const uint64_t bd = sdesc_sw128(b_addr + k * (UMMA_K * 128), 64 * 128, 1024);
-                mma_bf16_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
             mma_commit(&sm.empty[ps.stage]);
             ps.advance();

@@ -72,7 +72,7 @@ __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
                 ++nrec;
                 SchedEntry e;
                 e.kind = K_TILE; e.a = chunk; e.b = band; e.c = tcol; e.d = rank; e.nstage = p.nkb;
-                e.ticket = static_cast<int32_t>(t); e.slot = slot;
+                e.ticket = static_cast<int32_t>(t); e.slot = slot; e.nmma = 0; e.x0 = e.x1 = e.x2 = 0;
                 if (!ring_push(sm, rs, e, p.ws)) break;
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb) {
@@ -120,7 +120,7 @@ __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
         const int nsub = static_cast<int>(cdiv(rows, RED_ROWS));
         SchedEntry e;
         e.kind = K_REDUCE; e.a = rank; e.b = band; e.c = tcol; e.d = rank; e.nstage = nsub;
-        e.ticket = static_cast<int32_t>(t); e.slot = slot;
+        e.ticket = static_cast<int32_t>(t); e.slot = slot; e.nmma = 0; e.x0 = e.x1 = e.x2 = 0;
         if (!ring_push(sm, rs, e, p.ws)) break;
         bool ok = true;
         for (int s = 0; s < nsub; ++s) {
@@ -139,6 +139,7 @@ __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
     }
     SchedEntry done;
     done.kind = K_DONE; done.a = done.b = done.c = done.d = 0; done.nstage = 0; done.ticket = -1; done.slot = -1;
+    done.nmma = 0; done.x0 = done.x1 = done.x2 = 0;
     ring_push(sm, rs, done, p.ws);
 }
 

@@ -239,15 +239,70 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
     return launch_rs_bf16(L, static_cast<cudaStream_t>(stream));
 }
 
+static bool moe_sizes_ok(int P, int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter) {
+    if (P < 1 || P > KOSMOS_MAX_P) return false;
+    if (n_experts < 1 || n_experts > 256 || n_experts % 64 != 0 || n_experts % P != 0) return false;
+    if (topk < 1 || topk > 8 || topk > n_experts) return false;
+    if (tokens < P || tokens % P != 0 || tokens > (1ll << 24)) return false;
+    if (hidden < 256 || hidden % 256 != 0 || hidden > 24576) return false;
+    if (inter < 128 || inter % 128 != 0 || inter > (1ll << 16)) return false;
+    return true;
+}
+
+size_t kosmos_moe_workspace_bytes(int P, int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter,
+                                  const kosmos_opts *opts) {
+    const kosmos_opts o = resolve_opts(opts);
+    if (!moe_sizes_ok(P, tokens, hidden, n_experts, topk, inter)) return 0;
+    return moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, o.trace != 0);
+}
+
+kosmos_status kosmos_moe_debug_view(int what, int P, int64_t tokens, int64_t hidden, int n_experts, int topk,
+                                    int64_t inter, void *ws, void **ptr, int64_t *bytes) {
+    if (!moe_sizes_ok(P, tokens, hidden, n_experts, topk, inter) || ws == nullptr || ptr == nullptr ||
+        bytes == nullptr)
+        return KOSMOS_ERR_INVALID_ARG;
+    return moe_debug_view(what, P, tokens, hidden, n_experts, topk, inter, ws, ptr, bytes) ? KOSMOS_OK
+                                                                                          : KOSMOS_ERR_INVALID_ARG;
+}
+
 kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, int P, int64_t tokens, int64_t hidden,
                              int n_experts, int topk, int64_t inter, const void *const *w_gate,
                              const void *const *w_up, const void *const *w_down, void *const *y_shards,
                              int32_t *topk_idx, float *topk_gate, int32_t *expert_counts, int32_t *dispatch_pos,
                              void *ws, size_t ws_bytes, const kosmos_opts *opts, void *stream) {
-    (void)x_shards; (void)w_router; (void)P; (void)tokens; (void)hidden; (void)n_experts; (void)topk;
-    (void)inter; (void)w_gate; (void)w_up; (void)w_down; (void)y_shards; (void)topk_idx; (void)topk_gate;
-    (void)expert_counts; (void)dispatch_pos; (void)ws; (void)ws_bytes; (void)opts; (void)stream;
-    return KOSMOS_ERR_UNSUPPORTED;
+    if (!moe_sizes_ok(P, tokens, hidden, n_experts, topk, inter)) return KOSMOS_ERR_INVALID_ARG;
+    if (x_shards == nullptr || w_gate == nullptr || w_up == nullptr || w_down == nullptr || y_shards == nullptr)
+        return KOSMOS_ERR_INVALID_ARG;
+    for (int q = 0; q < P; ++q)
+        if (!aligned16(x_shards[q]) || !aligned16(w_gate[q]) || !aligned16(w_up[q]) || !aligned16(w_down[q]) ||
+            !aligned16(y_shards[q]))
+            return KOSMOS_ERR_INVALID_ARG;
+    if (!aligned16(w_router) || !aligned16(topk_idx) || !aligned16(topk_gate) || !aligned16(expert_counts) ||
+        !aligned16(dispatch_pos))
+        return KOSMOS_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
+    const kosmos_opts o = resolve_opts(opts);
+    if (o.sched != KOSMOS_SCHED_SELF) return KOSMOS_ERR_UNSUPPORTED;
+    if (ws_bytes < kosmos_moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, &o))
+        return KOSMOS_ERR_WORKSPACE;
+    const int grid = grid_for(o);
+    if (grid < 1) return KOSMOS_ERR_CUDA;
+    if (grid < P) return KOSMOS_ERR_INVALID_ARG;  // every emulated rank needs a CTA
+    MoeLaunch L;
+    memset(&L, 0, sizeof(L));
+    L.P = P; L.T = tokens; L.H = hidden; L.I = inter; L.E = n_experts; L.K = topk;
+    for (int q = 0; q < P; ++q) {
+        L.x[q] = x_shards[q];
+        L.wg[q] = w_gate[q];
+        L.wu[q] = w_up[q];
+        L.wd[q] = w_down[q];
+        L.y[q] = y_shards[q];
+    }
+    L.wr = w_router;
+    L.topk_idx = topk_idx; L.topk_gate = topk_gate; L.counts = expert_counts; L.pos = dispatch_pos;
+    L.ws = ws; L.sched = o.sched; L.n_comm = 0; L.trace = o.trace; L.grid = grid;
+    L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
+    return launch_moe_fwd(L, static_cast<cudaStream_t>(stream));
 }
 
 kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q, void *scales,

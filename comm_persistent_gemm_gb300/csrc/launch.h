@@ -79,6 +79,9 @@ kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream);
 kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream);
 kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream);
 kosmos_status launch_moe_fwd(const MoeLaunch &L, cudaStream_t stream);
+size_t moe_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool trace);
+bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t I, void *ws, void **ptr,
+                    int64_t *bytes);
 kosmos_status launch_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q,
                                     void *scales, cudaStream_t stream);
 kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail,

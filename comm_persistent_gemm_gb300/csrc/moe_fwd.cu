@@ -1,12 +1,1024 @@
-// moe_fwd.cu -- MoE expert layer forward, router to fold, in one launch.
+// moe_fwd.cu -- MoE expert layer forward, router to fold, in ONE persistent
+// launch (KOSMOS abstract: "runs an entire expert layer, from router to fold,
+// in one launch per direction").
+//
+// P emulated expert-parallel ranks; CTA c plays rank q = c mod P.  Rank q owns
+// tokens [q*Tq, (q+1)*Tq) and experts [q*Eq, (q+1)*Eq).
+//
+// Main rail of rank q (claimed in ticket order by rank q's CTAs):
+//   ROUTE(b)        router GEMM of 128 tokens x W_router (tcgen05), epilogue:
+//                   fp32 softmax, top-k (ties to the lower expert), gates
+//                   renormalised over the top-k, per-block expert counts and
+//                   each slot's rank inside its block.  The CTA that finishes
+//                   the last ROUTE of all ranks runs PLAN: expert counts,
+//                   exclusive offsets (receive order expert-major, then
+//                   token), per-block bases, per-rank row-block units.
+//   DISPATCH(b, k)  the all-to-all to the expert ranks: slot k of 128 tokens is
+//                   copied (bulk async copies) to row pos = base + rank of the
+//                   expert-ordered receive buffer; per (expert, row block)
+//                   arrival counters are released.
+//   TILE_GU / TILE_D  per unit u = (expert, 128-row block), consumer-ordered
+//                   with a lag of one unit: GU(u0) | GU(u1) D(u0) | ... | D(uN-1).
+//                   GU: [rows x H] . [W_gate | W_up] (128 + 128 columns) with a
+//                   SwiGLU epilogue h = silu(gate) * up; D: [rows x I] . W_down.
+// Ready queues of rank q (the combine step, two-way role switching; explainer
+// paragraph "KOSMOS removes the manager": push any ready result, otherwise
+// build a tile):
+//   PUSH(e, rb, dn) queued when a TILE_D finishes; copies the 256-column
+//                   slice of each row back to its source slot[t][k];
+//   FOLD(g, dn)     queued when all k slots of token block g have arrived for
+//                   column tile dn; out[t] = sum_k gate[t][k] * slot[t][k] in
+//                   fp32, k in emission order, one rounding to bf16.
+// A CTA takes a ready PUSH first, else its next main-rail entry, else a ready
+// FOLD, and exits when its rank's rail and queues are drained.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
 #include "engine.cuh"
 #include "launch.h"
 
 namespace kosmos {
 
-kosmos_status launch_moe_fwd(const MoeLaunch &L, cudaStream_t stream) {
-    (void)L; (void)stream;
-    return KOSMOS_ERR_UNSUPPORTED;
+constexpr int MOE_MAXK = 8;
+constexpr int MOE_SCRATCH = 12288;          // epilogue 8 KB + producer 4 KB
+constexpr int MOE_SMEM_BYTES = SMEM_BYTES + MOE_SCRATCH;
+
+struct MoeGeom {
+    int P, E, Eq, K;
+    int64_t T, Tq, H, I;
+    int RB;          // route blocks per rank
+    int NB;          // route blocks in total
+    int NGU;         // TILE_GU column blocks (I / 128)
+    int ND;          // TILE_D column blocks = push / fold column tiles (H / 256)
+    int MAXRB;       // row blocks an expert can need (ceil(T / 128))
+    int64_t rows_cap;
+    int push_cap;    // per rank
+    int fold_cap;    // per rank
+    int n_head;      // RB + RB*K main-rail entries before the tiles
+    int nkb_h;       // H / 64
+    int nkb_i;       // I / 64
+};
+
+inline MoeGeom moe_geom(int P, int64_t T, int64_t H, int E, int K, int64_t I) {
+    MoeGeom g;
+    g.P = P; g.E = E; g.Eq = E / P; g.K = K;
+    g.T = T; g.Tq = T / P; g.H = H; g.I = I;
+    g.RB = static_cast<int>(cdiv(g.Tq, BM));
+    g.NB = P * g.RB;
+    g.NGU = static_cast<int>(I / 128);
+    g.ND = static_cast<int>(H / BN);
+    g.MAXRB = static_cast<int>(cdiv(T, BM));
+    g.rows_cap = T * K + BM;
+    g.push_cap = static_cast<int>((g.Eq + cdiv(T * K, BM)) * g.ND);
+    g.fold_cap = g.RB * g.ND;
+    g.n_head = g.RB + g.RB * K;
+    g.nkb_h = static_cast<int>(H / BK);
+    g.nkb_i = static_cast<int>(I / BK);
+    return g;
+}
+
+struct MoeWsLayout {
+    size_t ctr, ctr_bytes, disp_cnt, gu_cnt, fold_cnt, qctl, route_done;
+    size_t blk_counts, rank_in_blk, base, offsets, counts, unit_start, inv_pos;
+    size_t push_items, push_flags, fold_items, fold_flags;
+    size_t logits, recv, h, ybuf, slot, trace, total;
+};
+
+inline MoeWsLayout moe_ws_layout(const MoeGeom &g, bool trace) {
+    MoeWsLayout L;
+    size_t off = 256;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = static_cast<size_t>(align_up(static_cast<int64_t>(off + bytes), 256));
+        return at;
+    };
+    // counters returned to zero by the last CTA of every launch
+    L.ctr = off;
+    size_t c = off;
+    L.disp_cnt = c; c += 4ull * g.E * g.MAXRB;
+    L.gu_cnt = c; c += 4ull * g.E * g.MAXRB;
+    L.fold_cnt = c; c += 4ull * g.NB * g.ND;
+    L.qctl = c; c += 4ull * 4 * g.P;
+    L.route_done = c; c += 4;
+    L.ctr_bytes = static_cast<size_t>(align_up(static_cast<int64_t>(c - L.ctr), 16));
+    off = L.ctr;
+    take(L.ctr_bytes);
+    L.blk_counts = take(4ull * g.NB * g.E);
+    L.rank_in_blk = take(4ull * g.T * g.K);
+    L.base = take(4ull * g.NB * g.E);
+    L.offsets = take(4ull * (g.E + 1));
+    L.counts = take(4ull * g.E);
+    L.unit_start = take(4ull * g.P * (g.Eq + 1));
+    L.inv_pos = take(4ull * g.T * g.K);
+    L.push_items = take(4ull * g.P * g.push_cap);
+    L.push_flags = take(4ull * g.P * g.push_cap);
+    L.fold_items = take(4ull * g.P * g.fold_cap);
+    L.fold_flags = take(4ull * g.P * g.fold_cap);
+    L.logits = take(4ull * g.T * g.E);
+    L.recv = take(2ull * g.rows_cap * g.H);
+    L.h = take(2ull * g.rows_cap * g.I);
+    L.ybuf = take(2ull * g.rows_cap * g.H);
+    L.slot = take(2ull * g.T * g.K * g.H);
+    L.trace = off;
+    if (trace) take(static_cast<size_t>(MAX_CTAS) * TRACE_CAP * sizeof(TraceRec));
+    L.total = off;
+    return L;
+}
+
+struct MoeParams {
+    CUtensorMap tmX[KOSMOS_MAX_P];   // x_shards[q]: dims {H, Tq}, box {64, 128}
+    CUtensorMap tmWr;                // w_router: dims {E, H}, box {64, 64}
+    CUtensorMap tmRecv;              // receive buffer: dims {H, rows_cap}, box {64, 128}
+    CUtensorMap tmH;                 // SwiGLU output: dims {I, rows_cap}, box {64, 128}
+    CUtensorMap tmWg[KOSMOS_MAX_P];  // w_gate[q]: dims {I, H, Eq}, box {64, 64, 1}
+    CUtensorMap tmWu[KOSMOS_MAX_P];  // w_up[q]:   dims {I, H, Eq}, box {64, 64, 1}
+    CUtensorMap tmWd[KOSMOS_MAX_P];  // w_down[q]: dims {H, I, Eq}, box {64, 64, 1}
+    const __nv_bfloat16 *x[KOSMOS_MAX_P];
+    __nv_bfloat16 *y[KOSMOS_MAX_P];
+    int32_t *topk_idx;
+    float *topk_gate;
+    int32_t *counts_out;
+    int32_t *pos_out;
+    WsHeader *ws;
+    uint8_t *ctr;
+    int ctr_bytes;
+    int identity;
+    uint32_t *disp_cnt, *gu_cnt, *fold_cnt, *qctl, *route_done;
+    int32_t *blk_counts, *rank_in_blk, *base, *offsets, *counts, *unit_start, *inv_pos;
+    int32_t *push_items, *fold_items;
+    uint32_t *push_flags, *fold_flags;
+    float *logits;
+    __nv_bfloat16 *recv, *h, *ybuf, *slot;
+    TraceRec *trace;
+    MoeGeom g;
+    uint64_t wait_limit_ns;
+    uint64_t inject;
+};
+
+// Data written earlier in the same launch by other CTAs is read through L2
+// only (ld.global.cg): an L1 line filled before the writer finished would be
+// stale.
+__device__ __forceinline__ int32_t ldcg_i32(const int32_t *p) { return __ldcg(p); }
+__device__ __forceinline__ float ldcg_f32(const float *p) { return __ldcg(p); }
+__device__ __forceinline__ uint4 ldcg_u4(const void *p) { return __ldcg(reinterpret_cast<const uint4 *>(p)); }
+
+__device__ __forceinline__ uint32_t atom_add_acqrel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Publish one item into a ready queue: reserve an index, write the item, then
+// release its per-item flag (epoch-tagged).
+__device__ __forceinline__ void queue_put(uint32_t *tail, int32_t *items, uint32_t *flags, int cap, int32_t code,
+                                          uint32_t epoch, WsHeader *ws) {
+    const uint32_t idx = atomicAdd(tail, 1u);
+    if (idx >= static_cast<uint32_t>(cap)) {
+        set_error(ws, KOSMOS_ERR_DEVICE, -20);
+        return;
+    }
+    items[idx] = code;
+    st_release_gpu(&flags[idx], epoch + 1u);
+}
+
+// Take the next item if one has been published; non-blocking except for the
+// few cycles between a publisher's reservation and its flag release.
+__device__ __forceinline__ bool queue_try_take(uint32_t *head, uint32_t *tail, const int32_t *items,
+                                               const uint32_t *flags, uint32_t epoch, int32_t &code,
+                                               WsHeader *ws) {
+    const uint32_t h = ld_relaxed_gpu(head);
+    if (h >= ld_acquire_gpu(tail)) return false;
+    if (atomicCAS(head, h, h + 1u) != h) return false;
+    if (!wait_flag_eq(ws, &flags[h], epoch + 1u, PIPE_LIMIT_NS, -21)) return false;
+    code = *reinterpret_cast<const volatile int32_t *>(&items[h]);
+    return true;
+}
+
+__device__ __forceinline__ int32_t push_code(int e, int rb, int dn) { return e | (rb << 9) | (dn << 20); }
+__device__ __forceinline__ void push_decode(int32_t c, int &e, int &rb, int &dn) {
+    e = c & 511; rb = (c >> 9) & 2047; dn = (c >> 20) & 4095;
+}
+
+// ---------------------------------------------------------------- producer (warp 0)
+enum MoeAct : int { ACT_NONE = 0, ACT_DISPATCH = 1, ACT_EXIT = 2 };
+
+struct MoeProdState {
+    PipeState ps;
+    RingState rs;
+    uint32_t cphase = 0;
+    int nrec = 0;
+    bool main_done = false;
+    bool plan_seen = false;
+    uint64_t idle_t0 = 0;
+};
+
+__device__ __forceinline__ void fill_entry(SchedEntry &e, int kind, int a, int b, int c, int nstage, int ticket,
+                                           int slot) {
+    e.kind = kind; e.a = a; e.b = b; e.c = c; e.d = 0; e.nstage = nstage; e.ticket = ticket; e.slot = slot;
+    e.nmma = 0; e.x0 = e.x1 = e.x2 = 0;
+}
+
+__device__ __forceinline__ int trace_open(const MoeParams &p, MoeProdState &st, int kind, int ticket, int64_t tc) {
+    int slot = -1;
+    if (TraceRec *r = trace_rec(p.trace, blockIdx.x, st.nrec)) {
+        r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
+        r->kind = kind; r->ticket = ticket; r->cta = blockIdx.x;
+        slot = st.nrec;
+    }
+    ++st.nrec;
+    return slot;
+}
+
+__device__ __forceinline__ bool wait_plan(const MoeParams &p, MoeProdState &st, uint32_t epoch) {
+    if (st.plan_seen) return true;
+    if (!wait_flag_eq(p.ws, &p.ws->aux[1], epoch + 1u, p.wait_limit_ns, -10)) return false;
+    st.plan_seen = true;
+    return true;
+}
+
+// Waits until every pipeline stage is free (all earlier MMAs have read their
+// operands), so the stage buffers can serve as copy buffers.
+__device__ __forceinline__ bool drain_pipeline(const MoeParams &p, const Smem &sm, const PipeState &ps) {
+    for (int i = 0; i < NSTAGE; ++i) {
+        uint32_t s = ps.stage + i, ph = ps.phase;
+        if (s >= NSTAGE) { s -= NSTAGE; ph ^= 1u; }
+        if (!mbar_wait(&sm.empty[s], ph ^ 1u, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -11);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Locates unit u of rank q: its local expert and row block.
+__device__ __forceinline__ void unit_decode(const MoeParams &p, int q, int u, int &le, int &rb) {
+    const int32_t *us = p.unit_start + q * (p.g.Eq + 1);
+    le = 0;
+    while (le + 1 < p.g.Eq && ldcg_i32(&us[le + 1]) <= u) ++le;
+    rb = u - ldcg_i32(&us[le]);
+}
+
+// Lane 0 of the producer warp: claims and issues one piece of work.  Returns
+// ACT_DISPATCH (with v0 = b, v1 = k, v2 = ticket) when the whole warp must
+// help, ACT_EXIT when this CTA is finished.
+__device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoeProdState &st, uint32_t epoch, int &v0,
+                                       int &v1, int &v2) {
+    const MoeGeom &g = p.g;
+    const int q = blockIdx.x % g.P;
+    uint32_t *qc = p.qctl + 4 * q;
+    if (failed(p.ws)) return ACT_EXIT;
+    // 1) a ready result to push back to its source rank
+    if (st.plan_seen) {
+        int32_t code;
+        if (queue_try_take(&qc[1], &qc[0], p.push_items + q * g.push_cap, p.push_flags + q * g.push_cap, epoch,
+                           code, p.ws)) {
+            int e, rb, dn;
+            push_decode(code, e, rb, dn);
+            SchedEntry en;
+            fill_entry(en, K_PUSH, e, rb, dn, 0, code,
+                       trace_open(p, st, K_PUSH, code, p.trace ? static_cast<int64_t>(globaltimer()) : 0));
+            en.x0 = ldcg_i32(&p.offsets[e]) + rb * BM;
+            const int rows = ldcg_i32(&p.counts[e]) - rb * BM;
+            en.x1 = rows < BM ? rows : BM;
+            ring_push(sm, st.rs, en, p.ws);
+            st.idle_t0 = 0;
+            return ACT_NONE;
+        }
+        if (failed(p.ws)) return ACT_EXIT;
+    }
+    // 2) the next entry of this rank's main rail
+    if (!st.main_done) {
+        const uint32_t t = atomicAdd(&p.ws->tickets[q], 1u);
+        const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+        if (t < static_cast<uint32_t>(g.RB)) {  // ROUTE(b)
+            const int b = static_cast<int>(t);
+            SchedEntry en;
+            fill_entry(en, K_ROUTE, q, b, q * g.RB + b, g.nkb_h, t, trace_open(p, st, K_ROUTE, t, tc));
+            en.nmma = g.E;
+            if (!ring_push(sm, st.rs, en, p.ws)) return ACT_EXIT;
+            const uint32_t bytes = A_STAGE_BYTES + (g.E / 64) * (64 * BK * 2);
+            for (int kb = 0; kb < g.nkb_h; ++kb) {
+                if (!mbar_wait(&sm.empty[st.ps.stage], st.ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                    return ACT_EXIT;
+                }
+                uint8_t *sa = sm.stages + st.ps.stage * STAGE_BYTES;
+                uint8_t *sb = sa + A_STAGE_BYTES;
+                uint64_t *bar = &sm.full[st.ps.stage];
+                mbar_arrive_expect_tx(bar, bytes);
+                tma_load_2d(sa, &p.tmX[q], bar, kb * BK, b * BM);
+                for (int j = 0; j < g.E / 64; ++j) tma_load_2d(sb + j * (64 * BK * 2), &p.tmWr, bar, j * 64, kb * BK);
+                st.ps.advance();
+            }
+            st.idle_t0 = 0;
+            return ACT_NONE;
+        }
+        if (t < static_cast<uint32_t>(g.n_head)) {  // DISPATCH(b, k)
+            if (!wait_plan(p, st, epoch)) return ACT_EXIT;
+            const int i = static_cast<int>(t) - g.RB;
+            v0 = i / g.K;
+            v1 = i % g.K;
+            v2 = static_cast<int>(t);
+            st.idle_t0 = 0;
+            return ACT_DISPATCH;
+        }
+        if (!wait_plan(p, st, epoch)) return ACT_EXIT;
+        const int U = ldcg_i32(&p.unit_start[q * (g.Eq + 1) + g.Eq]);
+        const int G = g.NGU + g.ND;
+        const int tt = static_cast<int>(t) - g.n_head;
+        int kind = 0, u = 0, col = 0;
+        if (U > 0 && tt < U * G) {
+            if (tt < g.NGU) {
+                kind = K_TILE_GU; u = 0; col = tt;
+            } else {
+                const int t2 = tt - g.NGU;
+                const int grp = t2 / G + 1;
+                const int r = t2 % G;
+                if (grp < U) {
+                    if (r < g.NGU) { kind = K_TILE_GU; u = grp; col = r; }
+                    else { kind = K_TILE_D; u = grp - 1; col = r - g.NGU; }
+                } else {
+                    kind = K_TILE_D; u = U - 1; col = r;
+                }
+            }
+        }
+        if (kind == 0) {
+            st.main_done = true;
+        } else {
+            int le, rb;
+            unit_decode(p, q, u, le, rb);
+            const int e = q * g.Eq + le;
+            const int row0 = ldcg_i32(&p.offsets[e]) + rb * BM;
+            const int left = ldcg_i32(&p.counts[e]) - rb * BM;
+            const int rows = left < BM ? left : BM;
+            const int ci = e * g.MAXRB + rb;
+            if (kind == K_TILE_GU) {
+                if (!wait_flag_eq(p.ws, &p.disp_cnt[ci], static_cast<uint32_t>(rows), p.wait_limit_ns, t))
+                    return ACT_EXIT;
+            } else {
+                if (!wait_flag_eq(p.ws, &p.gu_cnt[ci], static_cast<uint32_t>(g.NGU), p.wait_limit_ns, t))
+                    return ACT_EXIT;
+            }
+            const int slot = trace_open(p, st, kind, t, tc);
+            if (p.identity) {
+                // identity experts: no GEMMs; keep the dependency chain and the push
+                if (kind == K_TILE_GU) {
+                    __threadfence();
+                    red_release_add_gpu(&p.gu_cnt[ci], 1u);
+                } else {
+                    const int qe = e / g.Eq;
+                    queue_put(&p.qctl[4 * qe + 0], p.push_items + qe * g.push_cap, p.push_flags + qe * g.push_cap,
+                              g.push_cap, push_code(e, rb, col), epoch, p.ws);
+                }
+                if (TraceRec *r = trace_rec(p.trace, blockIdx.x, slot)) r->t_done = static_cast<int64_t>(globaltimer());
+                st.idle_t0 = 0;
+                return ACT_NONE;
+            }
+            SchedEntry en;
+            fill_entry(en, kind, e, rb, col, kind == K_TILE_GU ? g.nkb_h : g.nkb_i, t, slot);
+            en.x0 = row0;
+            en.x1 = rows;
+            en.d = le;
+            if (!ring_push(sm, st.rs, en, p.ws)) return ACT_EXIT;
+            for (int kb = 0; kb < en.nstage; ++kb) {
+                if (!mbar_wait(&sm.empty[st.ps.stage], st.ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                    return ACT_EXIT;
+                }
+                uint8_t *sa = sm.stages + st.ps.stage * STAGE_BYTES;
+                uint8_t *sb = sa + A_STAGE_BYTES;
+                uint64_t *bar = &sm.full[st.ps.stage];
+                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                if (kind == K_TILE_GU) {
+                    tma_load_2d(sa, &p.tmRecv, bar, kb * BK, row0);
+                    tma_load_3d(sb + 0 * 8192, &p.tmWg[q], bar, col * 128 + 0, kb * BK, le);
+                    tma_load_3d(sb + 1 * 8192, &p.tmWg[q], bar, col * 128 + 64, kb * BK, le);
+                    tma_load_3d(sb + 2 * 8192, &p.tmWu[q], bar, col * 128 + 0, kb * BK, le);
+                    tma_load_3d(sb + 3 * 8192, &p.tmWu[q], bar, col * 128 + 64, kb * BK, le);
+                } else {
+                    tma_load_2d(sa, &p.tmH, bar, kb * BK, row0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tma_load_3d(sb + j * 8192, &p.tmWd[q], bar, col * BN + j * 64, kb * BK, le);
+                }
+                st.ps.advance();
+            }
+            st.idle_t0 = 0;
+            return ACT_NONE;
+        }
+    }
+    // 3) a ready fold of this rank's tokens
+    if (st.plan_seen) {
+        int32_t code;
+        if (queue_try_take(&qc[3], &qc[2], p.fold_items + q * g.fold_cap, p.fold_flags + q * g.fold_cap, epoch, code,
+                           p.ws)) {
+            SchedEntry en;
+            fill_entry(en, K_FOLD, code & 0xFFFF, 0, (code >> 16) & 0xFFFF, 0, code,
+                       trace_open(p, st, K_FOLD, code, p.trace ? static_cast<int64_t>(globaltimer()) : 0));
+            ring_push(sm, st.rs, en, p.ws);
+            st.idle_t0 = 0;
+            return ACT_NONE;
+        }
+        if (failed(p.ws)) return ACT_EXIT;
+    }
+    // 4) finished when the rail and both queues of this rank are drained
+    if (st.main_done && st.plan_seen) {
+        const uint32_t push_total = static_cast<uint32_t>(ldcg_i32(&p.unit_start[q * (g.Eq + 1) + g.Eq])) * g.ND;
+        const uint32_t fold_total = static_cast<uint32_t>(g.fold_cap);
+        if (ld_relaxed_gpu(&qc[1]) >= push_total && ld_relaxed_gpu(&qc[3]) >= fold_total) return ACT_EXIT;
+    }
+    const uint64_t now = globaltimer();
+    if (st.idle_t0 == 0) {
+        st.idle_t0 = now;
+    } else if (now - st.idle_t0 > p.wait_limit_ns) {
+        set_error(p.ws, KOSMOS_ERR_TIMEOUT, -12);
+        return ACT_EXIT;
+    }
+    return ACT_NONE;
+}
+
+// The whole producer warp: slot k of the 128 tokens of block b goes to the
+// receive buffer of its expert's rank.  Lanes compute the destination rows;
+// lane 0 moves the rows with bulk async copies through the stage buffers and
+// then releases the per-(expert, row block) arrival counters.
+__device__ __noinline__ void moe_dispatch(const MoeParams &p, const Smem &sm, MoeProdState &st, uint8_t *pscr,
+                                          int lane, int b, int k, int ticket, uint32_t epoch) {
+    const MoeGeom &g = p.g;
+    const int q = blockIdx.x % g.P;
+    const int gblk = q * g.RB + b;
+    const int64_t left = g.Tq - static_cast<int64_t>(b) * BM;
+    const int nrows = static_cast<int>(left < BM ? left : BM);
+    int32_t *s_pos = reinterpret_cast<int32_t *>(pscr);
+    int32_t *s_ci = s_pos + BM;
+    __syncwarp();  // orders lane 0's acquire of the plan before the other lanes' reads
+    int slot = -1;
+    if (lane == 0) slot = trace_open(p, st, K_DISPATCH, ticket, p.trace ? static_cast<int64_t>(globaltimer()) : 0);
+    for (int r = lane; r < nrows; r += 32) {
+        const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(b) * BM + r;
+        const int e = ldcg_i32(&p.topk_idx[t * g.K + k]);
+        const int pos = ldcg_i32(&p.base[gblk * g.E + e]) + ldcg_i32(&p.rank_in_blk[t * g.K + k]);
+        p.pos_out[t * g.K + k] = pos;
+        p.inv_pos[pos] = static_cast<int32_t>(t * g.K + k);
+        s_pos[r] = pos;
+        s_ci[r] = e * g.MAXRB + (pos - ldcg_i32(&p.offsets[e])) / BM;
+    }
+    __syncwarp();
+    if (lane == 0) {
+        bool ok = drain_pipeline(p, sm, st.ps);
+        const uint32_t rbytes = static_cast<uint32_t>(g.H * 2);
+        const int per = STAGE_BYTES / static_cast<int>(rbytes);
+        const int nch = (nrows + per - 1) / per;
+        const uint8_t *src0 = reinterpret_cast<const uint8_t *>(p.x[q] + static_cast<int64_t>(b) * BM * g.H);
+        uint8_t *recv = reinterpret_cast<uint8_t *>(p.recv);
+        auto issue = [&](int c) {
+            const int bi = c % NSTAGE;
+            const int r0 = c * per;
+            const int n = (nrows - r0) < per ? (nrows - r0) : per;
+            mbar_arrive_expect_tx(&sm.cbar[bi], n * rbytes);
+            for (int i = 0; i < n; ++i)
+                bulk_g2s(sm.stages + bi * STAGE_BYTES + i * rbytes, src0 + static_cast<int64_t>(r0 + i) * rbytes,
+                         rbytes, &sm.cbar[bi]);
+        };
+        for (int c = 0; ok && c < nch && c < NSTAGE; ++c) issue(c);
+        for (int c = 0; ok && c < nch; ++c) {
+            const int bi = c % NSTAGE;
+            if (!mbar_wait(&sm.cbar[bi], (st.cphase >> bi) & 1u, PIPE_LIMIT_NS)) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, ticket);
+                ok = false;
+                break;
+            }
+            st.cphase ^= (1u << bi);
+            const int r0 = c * per;
+            const int n = (nrows - r0) < per ? (nrows - r0) : per;
+            for (int i = 0; i < n; ++i)
+                bulk_s2g(recv + static_cast<int64_t>(s_pos[r0 + i]) * rbytes, sm.stages + bi * STAGE_BYTES + i * rbytes,
+                         rbytes);
+            bulk_commit();
+            if (c >= 1 && c - 1 + NSTAGE < nch) {
+                bulk_wait_read<1>();
+                issue(c - 1 + NSTAGE);
+            }
+        }
+        bulk_wait<0>();
+        fence_proxy_async_global();
+        __threadfence();
+        if (ok)
+            for (int r = 0; r < nrows; ++r) red_release_add_gpu(&p.disp_cnt[s_ci[r]], 1u);
+        if (TraceRec *rec = trace_rec(p.trace, blockIdx.x, slot)) rec->t_done = static_cast<int64_t>(globaltimer());
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ void moe_producer(const MoeParams &p, const Smem &sm, uint8_t *pscr, uint32_t epoch,
+                                             int lane) {
+    MoeProdState st;
+    while (true) {
+        int act = ACT_NONE, v0 = 0, v1 = 0, v2 = 0;
+        if (lane == 0) act = moe_decide(p, sm, st, epoch, v0, v1, v2);
+        act = __shfl_sync(0xFFFFFFFFu, act, 0);
+        v0 = __shfl_sync(0xFFFFFFFFu, v0, 0);
+        v1 = __shfl_sync(0xFFFFFFFFu, v1, 0);
+        v2 = __shfl_sync(0xFFFFFFFFu, v2, 0);
+        if (act == ACT_EXIT) break;
+        if (act == ACT_DISPATCH) moe_dispatch(p, sm, st, pscr, lane, v0, v1, v2, epoch);
+    }
+    if (lane == 0) {
+        SchedEntry done;
+        fill_entry(done, K_DONE, 0, 0, 0, 0, -1, -1);
+        ring_push(sm, st.rs, done, p.ws);
+    }
+}
+
+// ---------------------------------------------------------------- epilogue (warps 2-5)
+// ROUTE epilogue for one block of 128 tokens (one token per thread).
+__device__ __noinline__ void moe_route_epilogue(const MoeParams &p, const SchedEntry &e, uint32_t taddr, int row,
+                                                int et, uint8_t *escr, uint32_t epoch) {
+    const MoeGeom &g = p.g;
+    const int q = e.a, b = e.b, gblk = e.c;
+    const int K = g.K, E = g.E;
+    const int64_t tl = static_cast<int64_t>(b) * BM + row;
+    const bool valid = tl < g.Tq;
+    const int64_t t = static_cast<int64_t>(q) * g.Tq + (valid ? tl : 0);
+    float tv[MOE_MAXK];
+    int ti[MOE_MAXK];
+#pragma unroll
+    for (int s = 0; s < MOE_MAXK; ++s) { tv[s] = -INFINITY; ti[s] = 0x7FFFFFFF; }
+    int cnt = 0;
+    float lmax = -INFINITY;
+    for (int ch = 0; ch < E / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + ch * 32, r);
+        tmem_ld_wait();
+        if (valid) {
+            float4 *dump = reinterpret_cast<float4 *>(p.logits + t * E + ch * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dump[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float l = __uint_as_float(r[j]);
+            lmax = fmaxf(lmax, l);
+            // insert (l, ch*32+j) after every kept entry with value >= l: the list
+            // stays sorted by (value descending, index ascending)
+            bool shifting = false;
+            float cv = l;
+            int ci = ch * 32 + j;
+#pragma unroll
+            for (int s = 0; s < MOE_MAXK; ++s) {
+                if (s < K) {
+                    if (!shifting && (s >= cnt || cv > tv[s])) shifting = true;
+                    if (shifting) {
+                        const float fv = tv[s];
+                        const int fi = ti[s];
+                        tv[s] = cv; ti[s] = ci;
+                        cv = fv; ci = fi;
+                    }
+                }
+            }
+            if (cnt < K) ++cnt;
+        }
+    }
+    // softmax denominator over all experts (ascending expert order)
+    float z = 0.f;
+    for (int ch = 0; ch < E / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + ch * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z += expf(__uint_as_float(r[j]) - lmax);
+    }
+    float pk[MOE_MAXK];
+    float ps = 0.f;
+#pragma unroll
+    for (int s = 0; s < MOE_MAXK; ++s) {
+        pk[s] = (s < K) ? expf(tv[s] - lmax) / z : 0.f;
+        if (s < K) ps += pk[s];
+    }
+    int32_t *s_idx = reinterpret_cast<int32_t *>(escr);            // [128][K]
+    int32_t *s_hist = reinterpret_cast<int32_t *>(escr + 4096);    // [E]
+    for (int i = et; i < E; i += NUM_EPI_THREADS) s_hist[i] = 0;
+#pragma unroll
+    for (int s = 0; s < MOE_MAXK; ++s) {
+        if (s < K) {
+            s_idx[row * K + s] = valid ? ti[s] : -1;
+            if (valid) {
+                p.topk_idx[t * K + s] = ti[s];
+                p.topk_gate[t * K + s] = pk[s] / ps;
+            }
+        }
+    }
+    named_bar_sync(1, NUM_EPI_THREADS);
+    if (valid) {
+#pragma unroll
+        for (int s = 0; s < MOE_MAXK; ++s) {
+            if (s < K) {
+                const int ex = ti[s];
+                int rk = 0;
+                for (int r2 = 0; r2 < row; ++r2)
+                    for (int s2 = 0; s2 < K; ++s2) rk += (s_idx[r2 * K + s2] == ex) ? 1 : 0;
+                p.rank_in_blk[t * K + s] = rk;
+                atomicAdd(&s_hist[ex], 1);
+            }
+        }
+    }
+    named_bar_sync(1, NUM_EPI_THREADS);
+    for (int i = et; i < E; i += NUM_EPI_THREADS) p.blk_counts[gblk * E + i] = s_hist[i];
+    __threadfence();
+    named_bar_sync(1, NUM_EPI_THREADS);
+    int32_t *s_last = reinterpret_cast<int32_t *>(escr + 8188);
+    if (et == 0) *s_last = (atom_add_acqrel_gpu(p.route_done, 1u) == static_cast<uint32_t>(g.NB - 1)) ? 1 : 0;
+    named_bar_sync(1, NUM_EPI_THREADS);
+    if (*s_last == 0) return;
+    // PLAN: every route block has published its counts
+    __threadfence();
+    int32_t *s_cnt = reinterpret_cast<int32_t *>(escr + 5120);
+    int32_t *s_off = reinterpret_cast<int32_t *>(escr + 6144);
+    for (int i = et; i < E; i += NUM_EPI_THREADS) {
+        int c = 0;
+        for (int gb = 0; gb < g.NB; ++gb) c += *reinterpret_cast<volatile int32_t *>(&p.blk_counts[gb * E + i]);
+        s_cnt[i] = c;
+        p.counts[i] = c;
+        p.counts_out[i] = c;
+    }
+    named_bar_sync(1, NUM_EPI_THREADS);
+    if (et == 0) {
+        int run = 0;
+        for (int i = 0; i < E; ++i) { s_off[i] = run; p.offsets[i] = run; run += s_cnt[i]; }
+        s_off[E] = run;
+        p.offsets[E] = run;
+        for (int qq = 0; qq < g.P; ++qq) {
+            int u = 0;
+            for (int j = 0; j < g.Eq; ++j) {
+                p.unit_start[qq * (g.Eq + 1) + j] = u;
+                u += (s_cnt[qq * g.Eq + j] + BM - 1) / BM;
+            }
+            p.unit_start[qq * (g.Eq + 1) + g.Eq] = u;
+        }
+    }
+    named_bar_sync(1, NUM_EPI_THREADS);
+    for (int i = et; i < E; i += NUM_EPI_THREADS) {
+        int run = s_off[i];
+        for (int gb = 0; gb < g.NB; ++gb) {
+            p.base[gb * E + i] = run;
+            run += *reinterpret_cast<volatile int32_t *>(&p.blk_counts[gb * E + i]);
+        }
+    }
+    __threadfence();
+    named_bar_sync(1, NUM_EPI_THREADS);
+    if (et == 0) st_release_gpu(&p.ws->aux[1], epoch + 1u);
+}
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+
+// Copies the dn-th 256-column slice of each row of one unit back to the
+// source slot[t][k] (warp w: rows 32w..32w+31, lane: 16 bytes of the slice),
+// then counts the arrivals per (token block, dn); the arrival that completes a
+// block queues its FOLD on the block's rank.
+__device__ __noinline__ void moe_push(const MoeParams &p, const SchedEntry &e, int ew, int lane, uint32_t epoch) {
+    const MoeGeom &g = p.g;
+    const int dn = e.c;
+    const int row0 = e.x0, rows = e.x1;
+    const __nv_bfloat16 *srcb = p.identity ? p.recv : p.ybuf;
+    const int rbase = ew * 32;
+    const int my = rbase + lane;                       // the row this lane accounts for
+    const int32_t my_sl = (my < rows) ? ldcg_i32(&p.inv_pos[row0 + my]) : -1;
+    const int n = (rows - rbase) < 32 ? (rows - rbase) : 32;
+    for (int i0 = 0; i0 < n; i0 += 8) {
+        int32_t sl[8];
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sl[i] = __shfl_sync(0xFFFFFFFFu, my_sl, (i0 + i) & 31);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i0 + i < n)
+                v[i] = ldcg_u4(srcb + static_cast<int64_t>(row0 + rbase + i0 + i) * g.H + dn * BN + lane * 8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i0 + i < n)
+                *reinterpret_cast<uint4 *>(p.slot + static_cast<int64_t>(sl[i]) * g.H + dn * BN + lane * 8) = v[i];
+    }
+    __threadfence();
+    __syncwarp();
+    // one release-add per distinct token block among this warp's rows
+    int gb = -1;
+    uint32_t target = 0;
+    if (my_sl >= 0) {
+        const int64_t t = my_sl / g.K;
+        const int qs = static_cast<int>(t / g.Tq);
+        const int bq = static_cast<int>((t - static_cast<int64_t>(qs) * g.Tq) / BM);
+        gb = qs * g.RB + bq;
+        const int64_t left = g.Tq - static_cast<int64_t>(bq) * BM;
+        target = static_cast<uint32_t>((left < BM ? left : BM) * g.K);
+    }
+    const uint32_t grp = __match_any_sync(0xFFFFFFFFu, gb);
+    if (gb >= 0 && (__ffs(grp) - 1) == lane) {
+        const uint32_t cnt = __popc(grp);
+        if (atom_add_acqrel_gpu(&p.fold_cnt[gb * g.ND + dn], cnt) + cnt == target) {
+            const int qs = gb / g.RB;
+            queue_put(&p.qctl[4 * qs + 2], p.fold_items + qs * g.fold_cap, p.fold_flags + qs * g.fold_cap, g.fold_cap,
+                      gb | (dn << 16), epoch, p.ws);
+        }
+    }
+    __syncwarp();
+}
+
+__device__ __noinline__ void moe_fold(const MoeParams &p, const SchedEntry &e, int ew, int lane) {
+    const MoeGeom &g = p.g;
+    const int gb = e.a, dn = e.c;
+    const int q = gb / g.RB, b = gb % g.RB;
+    const int K = g.K;
+    for (int i = 0; i < 32; ++i) {
+        const int r = ew * 32 + i;
+        const int64_t tl = static_cast<int64_t>(b) * BM + r;
+        if (tl >= g.Tq) break;
+        const int64_t t = static_cast<int64_t>(q) * g.Tq + tl;
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        uint4 v[MOE_MAXK];
+        float gk[MOE_MAXK];
+#pragma unroll
+        for (int k = 0; k < MOE_MAXK; ++k) {
+            if (k < K) {
+                gk[k] = ldcg_f32(&p.topk_gate[t * K + k]);
+                v[k] = ldcg_u4(p.slot + (t * K + k) * g.H + dn * BN + lane * 8);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < MOE_MAXK; ++k) {
+            if (k < K) {
+                const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(gk[k], __uint_as_float(w[j] << 16)));
+                    acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(gk[k], __uint_as_float(w[j] & 0xFFFF0000u)));
+                }
+            }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4 *>(p.y[q] + tl * g.H + dn * BN + lane * 8) = o;
+    }
+}
+
+__device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm, uint32_t tmem_base, uint8_t *escr,
+                                             int warp, int lane, uint32_t epoch) {
+    const MoeGeom &g = p.g;
+    const int grp = warp & 3;
+    const int row = grp * 32 + lane;
+    const int ew = warp - 2;
+    const int et = ew * 32 + lane;
+    RingState rs;
+    uint32_t acc = 0, acc_phase = 0;
+    while (true) {
+        if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -6);
+            break;
+        }
+        const SchedEntry e = sm.sched[rs.idx];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sempty[rs.idx]);
+        rs.advance();
+        if (e.kind == K_DONE) break;
+        if (is_mma_kind(e.kind)) {
+            if (!mbar_wait(&sm.tfull[acc], acc_phase, PIPE_LIMIT_NS)) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
+            if (e.kind == K_ROUTE) {
+                moe_route_epilogue(p, e, taddr, row, et, escr, epoch);
+            } else if (e.kind == K_TILE_GU) {
+                const bool valid = row < e.x1;
+                __nv_bfloat16 *dst = p.h + static_cast<int64_t>(e.x0 + (valid ? row : 0)) * g.I + e.c * 128;
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t gr[32], ur[32];
+                    tmem_ld_32x32b_x32(taddr + ch * 32, gr);
+                    tmem_ld_32x32b_x32(taddr + 128 + ch * 32, ur);
+                    tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float hv[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                hv[j] = silu_f(__uint_as_float(gr[q4 * 8 + j])) * __uint_as_float(ur[q4 * 8 + j]);
+                            uint4 o;
+                            o.x = pack_bf16x2(hv[0], hv[1]);
+                            o.y = pack_bf16x2(hv[2], hv[3]);
+                            o.z = pack_bf16x2(hv[4], hv[5]);
+                            o.w = pack_bf16x2(hv[6], hv[7]);
+                            *reinterpret_cast<uint4 *>(dst + ch * 32 + q4 * 8) = o;
+                        }
+                    }
+                }
+            } else {  // K_TILE_D
+                const bool valid = row < e.x1;
+                __nv_bfloat16 *dst = p.ybuf + static_cast<int64_t>(e.x0 + (valid ? row : 0)) * g.H + e.c * BN;
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32; ++ch) tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + ch * 32, 32);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (e.kind == K_TILE_GU || e.kind == K_TILE_D) {
+                __threadfence();
+                named_bar_sync(1, NUM_EPI_THREADS);
+                if (et == 0) {
+                    if (e.kind == K_TILE_GU) {
+                        red_release_add_gpu(&p.gu_cnt[e.a * g.MAXRB + e.b], 1u);
+                    } else {
+                        const int qe = e.a / g.Eq;
+                        queue_put(&p.qctl[4 * qe + 0], p.push_items + qe * g.push_cap, p.push_flags + qe * g.push_cap,
+                                  g.push_cap, push_code(e.a, e.b, e.c), epoch, p.ws);
+                    }
+                }
+            }
+        } else if (e.kind == K_PUSH) {
+            moe_push(p, e, ew, lane, epoch);
+        } else if (e.kind == K_FOLD) {
+            moe_fold(p, e, ew, lane);
+        }
+        if (e.slot >= 0 && et == 0) {
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) moe_fwd_kernel(const __grid_constant__ MoeParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem sm = carve_smem(smem_raw);
+    uint8_t *scratch = sm.stages + NSTAGE * STAGE_BYTES + SMEM_CTRL_BYTES;
+    uint8_t *escr = scratch;          // epilogue: 8 KB
+    uint8_t *pscr = scratch + 8192;   // producer: 4 KB
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
+    engine_setup(sm, warp);
+    const uint32_t tmem_base = *sm.tmem_slot;
+    if (warp == 0) {
+        moe_producer(p, sm, pscr, epoch, lane);
+    } else if (warp == 1) {
+        if (lane == 0) mma_loop(sm, tmem_base, p.ws);
+    } else {
+        moe_epilogue(p, sm, tmem_base, escr, warp, lane, epoch);
+    }
+    engine_teardown(sm, warp, tmem_base);
+    // The last CTA returns every counter to zero, then the rail tickets and epoch.
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = (atomicAdd(&p.ws->done_ctas, 1u) == gridDim.x - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        uint4 *c = reinterpret_cast<uint4 *>(p.ctr);
+        const int n16 = p.ctr_bytes / 16;
+        for (int i = threadIdx.x; i < n16; i += blockDim.x) c[i] = make_uint4(0, 0, 0, 0);
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            volatile uint32_t *t = p.ws->tickets;
+            for (int i = 0; i < KOSMOS_MAX_P; ++i) t[i] = 0u;
+            *reinterpret_cast<volatile uint32_t *>(&p.ws->done_ctas) = 0u;
+            __threadfence();
+            *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch) = epoch + 1u;
+            __threadfence();
+        }
+    }
+}
+
+size_t moe_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool trace) {
+    return moe_ws_layout(moe_geom(P, T, H, E, K, I), trace).total;
+}
+
+bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t I, void *ws, void **ptr,
+                    int64_t *bytes) {
+    const MoeGeom g = moe_geom(P, T, H, E, K, I);
+    const MoeWsLayout L = moe_ws_layout(g, what == 6);
+    size_t off = 0, n = 0;
+    switch (what) {
+        case 0: off = L.logits; n = 4ull * g.T * g.E; break;
+        case 1: off = L.recv; n = 2ull * g.T * g.K * g.H; break;
+        case 2: off = L.h; n = 2ull * g.T * g.K * g.I; break;
+        case 3: off = L.ybuf; n = 2ull * g.T * g.K * g.H; break;
+        case 4: off = L.slot; n = 2ull * g.T * g.K * g.H; break;
+        case 5: off = L.offsets; n = 4ull * (g.E + 1); break;
+        case 6: off = L.trace; n = static_cast<size_t>(MAX_CTAS) * TRACE_CAP * sizeof(TraceRec); break;
+        default: return false;
+    }
+    *ptr = static_cast<uint8_t *>(ws) + off;
+    *bytes = static_cast<int64_t>(n);
+    return true;
+}
+
+kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
+    MoeParams p;
+    memset(&p, 0, sizeof(p));
+    p.g = moe_geom(Lc.P, Lc.T, Lc.H, Lc.E, Lc.K, Lc.I);
+    const MoeGeom &g = p.g;
+    const MoeWsLayout L = moe_ws_layout(g, Lc.trace != 0);
+    uint8_t *ws = static_cast<uint8_t *>(Lc.ws);
+    p.ws = reinterpret_cast<WsHeader *>(ws);
+    p.ctr = ws + L.ctr;
+    p.ctr_bytes = static_cast<int>(L.ctr_bytes);
+    p.disp_cnt = reinterpret_cast<uint32_t *>(ws + L.disp_cnt);
+    p.gu_cnt = reinterpret_cast<uint32_t *>(ws + L.gu_cnt);
+    p.fold_cnt = reinterpret_cast<uint32_t *>(ws + L.fold_cnt);
+    p.qctl = reinterpret_cast<uint32_t *>(ws + L.qctl);
+    p.route_done = reinterpret_cast<uint32_t *>(ws + L.route_done);
+    p.blk_counts = reinterpret_cast<int32_t *>(ws + L.blk_counts);
+    p.rank_in_blk = reinterpret_cast<int32_t *>(ws + L.rank_in_blk);
+    p.base = reinterpret_cast<int32_t *>(ws + L.base);
+    p.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    p.counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    p.unit_start = reinterpret_cast<int32_t *>(ws + L.unit_start);
+    p.inv_pos = reinterpret_cast<int32_t *>(ws + L.inv_pos);
+    p.push_items = reinterpret_cast<int32_t *>(ws + L.push_items);
+    p.push_flags = reinterpret_cast<uint32_t *>(ws + L.push_flags);
+    p.fold_items = reinterpret_cast<int32_t *>(ws + L.fold_items);
+    p.fold_flags = reinterpret_cast<uint32_t *>(ws + L.fold_flags);
+    p.logits = reinterpret_cast<float *>(ws + L.logits);
+    p.recv = reinterpret_cast<__nv_bfloat16 *>(ws + L.recv);
+    p.h = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
+    p.ybuf = reinterpret_cast<__nv_bfloat16 *>(ws + L.ybuf);
+    p.slot = reinterpret_cast<__nv_bfloat16 *>(ws + L.slot);
+    p.trace = Lc.trace ? reinterpret_cast<TraceRec *>(ws + L.trace) : nullptr;
+    p.topk_idx = Lc.topk_idx;
+    p.topk_gate = Lc.topk_gate;
+    p.counts_out = Lc.counts;
+    p.pos_out = Lc.pos;
+    p.identity = (Lc.inject & KOSMOS_INJECT_IDENTITY_EXPERTS) ? 1 : 0;
+    p.wait_limit_ns = Lc.wait_limit_ns;
+    p.inject = Lc.inject;
+    const uint64_t H = static_cast<uint64_t>(g.H), I = static_cast<uint64_t>(g.I), E = static_cast<uint64_t>(g.E);
+    const uint64_t Eq = static_cast<uint64_t>(g.Eq), Tq = static_cast<uint64_t>(g.Tq);
+    const uint64_t RC = static_cast<uint64_t>(g.rows_cap);
+    for (int q = 0; q < g.P; ++q) {
+        p.x[q] = static_cast<const __nv_bfloat16 *>(Lc.x[q]);
+        p.y[q] = static_cast<__nv_bfloat16 *>(Lc.y[q]);
+        {
+            const uint64_t dims[2] = {H, Tq};
+            const uint64_t st[1] = {H * 2};
+            const uint32_t box[2] = {BK, BM};
+            if (!encode_tmap(&p.tmX[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(Lc.x[q]), dims, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+                return KOSMOS_ERR_CUDA;
+        }
+        {
+            const uint64_t dims[3] = {I, H, Eq};
+            const uint64_t st[2] = {I * 2, H * I * 2};
+            const uint32_t box[3] = {64, BK, 1};
+            if (!encode_tmap(&p.tmWg[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(Lc.wg[q]), dims, st,
+                             box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !encode_tmap(&p.tmWu[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(Lc.wu[q]), dims, st,
+                             box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return KOSMOS_ERR_CUDA;
+        }
+        {
+            const uint64_t dims[3] = {H, I, Eq};
+            const uint64_t st[2] = {H * 2, H * I * 2};
+            const uint32_t box[3] = {64, BK, 1};
+            if (!encode_tmap(&p.tmWd[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(Lc.wd[q]), dims, st,
+                             box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return KOSMOS_ERR_CUDA;
+        }
+    }
+    {
+        const uint64_t dims[2] = {E, H};
+        const uint64_t st[1] = {E * 2};
+        const uint32_t box[2] = {64, BK};
+        if (!encode_tmap(&p.tmWr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(Lc.wr), dims, st, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[2] = {H, RC};
+        const uint64_t st[1] = {H * 2};
+        const uint32_t box[2] = {BK, BM};
+        if (!encode_tmap(&p.tmRecv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.recv, dims, st, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[2] = {I, RC};
+        const uint64_t st[1] = {I * 2};
+        const uint32_t box[2] = {BK, BM};
+        if (!encode_tmap(&p.tmH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.h, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    return launch_persistent(reinterpret_cast<const void *>(&moe_fwd_kernel), &p, Lc.grid, MOE_SMEM_BYTES, stream);
 }
 
 kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream) {

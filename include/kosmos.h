@@ -90,6 +90,10 @@ enum { KOSMOS_ORDER_BAND = 0, KOSMOS_ORDER_ROW = 1 };
  * never released, so the waiting side's bounded wait runs out). */
 #define KOSMOS_INJECT_DROP_TRANSFER 0x1ull  /* AG: transfer ticket (inject >> 32) never releases its flag */
 #define KOSMOS_INJECT_DROP_PARTIAL  0x2ull  /* RS: rank (inject >> 32) never signals its partial tiles */
+/* MoE debug mode: every expert is the identity map (no expert GEMMs; the
+ * pushed rows are the dispatched token rows), which isolates router,
+ * dispatch, push and fold.  Not a fault: the output is x * sum of gates. */
+#define KOSMOS_INJECT_IDENTITY_EXPERTS 0x4ull
 
 typedef struct kosmos_opts {
     int32_t sched;            /* KOSMOS_SCHED_* */
@@ -181,8 +185,9 @@ KOSMOS_API kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void 
  *   expert_counts : out, [n_experts] int32.
  *   dispatch_pos  : out, [tokens, topk] int32: row of (t, k) in the expert-ordered
  *                   receive buffer (experts ascending, then tokens ascending).
- *   Requirements: P in {1..8}, n_experts % P == 0, tokens % P == 0,
- *   hidden % 256 == 0, inter % 128 == 0, 1 <= topk <= 8, n_experts <= 256.
+ *   Requirements: P in {1..8}, n_experts % P == 0, n_experts % 64 == 0,
+ *   n_experts <= 256, 1 <= topk <= 8, topk <= n_experts, tokens % P == 0,
+ *   hidden % 256 == 0, inter % 128 == 0.  Workspace: kosmos_moe_workspace_bytes.
  */
 KOSMOS_API kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, int P,
                              int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter,
@@ -191,6 +196,23 @@ KOSMOS_API kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void 
                              int32_t *topk_idx, float *topk_gate, int32_t *expert_counts,
                              int32_t *dispatch_pos, void *ws, size_t ws_bytes,
                              const kosmos_opts *opts, void *stream);
+
+/* Workspace size in bytes for kosmos_moe_fwd with these sizes (opts may be
+ * NULL).  Returns 0 for invalid sizes. */
+KOSMOS_API size_t kosmos_moe_workspace_bytes(int P, int64_t tokens, int64_t hidden, int n_experts, int topk,
+                                             int64_t inter, const kosmos_opts *opts);
+
+/* Device views into a MoE workspace after a call (for checks and tools):
+ *   what 0: router logits [tokens, n_experts] fp32 (as the kernel computed them)
+ *        1: receive buffer [tokens*topk, hidden] bf16, expert-ordered rows
+ *        2: SwiGLU activations h [tokens*topk, inter] bf16, same row order
+ *        3: expert outputs [tokens*topk, hidden] bf16, same row order
+ *        4: pushed slots [tokens, topk, hidden] bf16
+ *        5: expert offsets [n_experts + 1] int32
+ *        6: role trace records (only for a workspace sized with opts.trace)
+ * Returns KOSMOS_OK and sets *ptr / *bytes, or KOSMOS_ERR_INVALID_ARG. */
+KOSMOS_API kosmos_status kosmos_moe_debug_view(int what, int P, int64_t tokens, int64_t hidden, int n_experts,
+                                               int topk, int64_t inter, void *ws, void **ptr, int64_t *bytes);
 
 /*
  * MXFP8 quantiser for the MXFP8 all-gather+GEMM operands.  For each block of

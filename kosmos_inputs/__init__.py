@@ -7,9 +7,11 @@ arithmetic (no GEMM, no quantisation, no routing).
 
 Generation recipe (the pages give only "~N(0, var)" and a seed):
   * one ``torch.Generator('cpu')`` seeded with the workload's seed;
-  * tensors are drawn in the order the workload lists them
-    (AG: X_0..X_{P-1}, then W;  RS: X_0..X_{P-1}, then W_0..W_{P-1};
-    MoE: X, W_router, then for each expert e = 0..E-1: gate, up, down);
+  * AG and RS tensors are drawn in the order the workload lists them
+    (AG: X_0..X_{P-1}, then W;  RS: X_0..X_{P-1}, then W_0..W_{P-1});
+  * MoE tensors (X, W_router, then gate, up, down of each expert) each have
+    their own generator seeded from the workload seed and the tensor's index,
+    so the 384 expert matrices can be drawn in parallel;
   * each draw is ``randn(shape, float32) * sigma`` rounded once to bfloat16
     (round-to-nearest-even, torch's conversion).
 
@@ -19,6 +21,7 @@ uint16 view that the oracle consumes.
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass, field
 from typing import Dict, List
 
@@ -110,19 +113,43 @@ def rs_inputs(P: int, m: int, k: int, n: int, seed: int, var_x: float = 1.0,
     return {"x": xs, "w": ws}
 
 
-def moe_inputs(T: int, H: int, E: int, I: int, seed: int) -> Dict[str, object]:
+def _stream_seed(seed: int, stream: int) -> int:
+    return (seed * 1_000_003 + stream) & 0x7FFFFFFFFFFFFFFF
+
+
+def _draw_stream(seed: int, stream: int, shape, var: float) -> torch.Tensor:
+    g = torch.Generator(device="cpu").manual_seed(_stream_seed(seed, stream))
+    return _draw(g, shape, var)
+
+
+def moe_inputs(T: int, H: int, E: int, I: int, seed: int, threads: int = 0) -> Dict[str, object]:
     """X [T, H] ~N(0,1), W_router [H, E] ~N(0, 1/H), then per expert
-    gate [H, I] ~N(0, 1/H), up [H, I] ~N(0, 1/H), down [I, H] ~N(0, 1/I)."""
-    g = torch.Generator(device="cpu").manual_seed(seed)
-    x = _draw(g, (T, H), 1.0)
-    wr = _draw(g, (H, E), 1.0 / H)
+    gate [H, I] ~N(0, 1/H), up [H, I] ~N(0, 1/H), down [I, H] ~N(0, 1/I).
+
+    Each tensor has its own generator, seeded (seed * 1000003 + stream) with
+    stream 0 for X, 1 for W_router and 2 + 3e, 3 + 3e, 4 + 3e for expert e's
+    gate, up and down; the draws run in parallel threads and the values do not
+    depend on the thread count."""
+    from concurrent.futures import ThreadPoolExecutor
+    x = _draw_stream(seed, 0, (T, H), 1.0)
+    wr = _draw_stream(seed, 1, (H, E), 1.0 / H)
     wg = torch.empty(E, H, I, dtype=torch.bfloat16)
     wu = torch.empty(E, H, I, dtype=torch.bfloat16)
     wd = torch.empty(E, I, H, dtype=torch.bfloat16)
-    for e in range(E):
-        wg[e] = _draw(g, (H, I), 1.0 / H)
-        wu[e] = _draw(g, (H, I), 1.0 / H)
-        wd[e] = _draw(g, (I, H), 1.0 / I)
+
+    def one(e):
+        wg[e] = _draw_stream(seed, 2 + 3 * e, (H, I), 1.0 / H)
+        wu[e] = _draw_stream(seed, 3 + 3 * e, (H, I), 1.0 / H)
+        wd[e] = _draw_stream(seed, 4 + 3 * e, (I, H), 1.0 / I)
+
+    n = threads or min(32, os.cpu_count() or 1)
+    prev = torch.get_num_threads()
+    torch.set_num_threads(1)
+    try:
+        with ThreadPoolExecutor(max_workers=n) as ex:
+            list(ex.map(one, range(E)))
+    finally:
+        torch.set_num_threads(prev)
     return {"x": x, "w_router": wr, "w_gate": wg, "w_up": wu, "w_down": wd}
 
 
