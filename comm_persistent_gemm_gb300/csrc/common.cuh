@@ -128,14 +128,16 @@ KOS_HD RsGeom rs_geom(int P, int64_t m, int64_t k, int64_t n) {
     g.n_reduce = g.bands * g.tiles_n;
     return g;
 }
-// Tile rail of one rank.  Band order: band, chunk, column.  Row order: chunk, band, column.
+// Tile rail of one rank.  Band order: band, column, chunk (the P tiles that
+// share one W_r column slice are adjacent, so the slice is read from DRAM once
+// per band).  Row order: chunk, band, column.
 KOS_HD void rs_decode_tile(const RsGeom &g, int order, int t, int &chunk, int &band, int &tcol) {
     if (order == KOSMOS_ORDER_BAND) {
         const int per_band = g.P * g.tiles_n;
         band = t / per_band;
         const int r = t - band * per_band;
-        chunk = r / g.tiles_n;
-        tcol = r - chunk * g.tiles_n;
+        tcol = r / g.P;
+        chunk = r - tcol * g.P;
     } else {
         const int per_chunk = g.bands * g.tiles_n;
         chunk = t / per_chunk;

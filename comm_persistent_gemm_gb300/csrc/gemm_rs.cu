@@ -7,7 +7,7 @@
 //   tile rail    TILE(chunk, band, col): the partial X_r . W_r on one 128x256
 //                tile, rounded to bf16 into rank r's partial buffer, then one
 //                release-increment of that output tile's arrival counter;
-//                band order (band, chunk, col) or the row-order ablation
+//                band order (band, col, chunk) or the row-order ablation
 //                (chunk, band, col) (explainer, "Role switching only works");
 //   reduce rail  REDUCE(band, col) of rank r's own chunk: acquire counter == P,
 //                sum the P partials in rank order 0..P-1 in fp32, round once

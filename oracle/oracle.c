@@ -484,9 +484,11 @@ ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN,
 /* Reduce-scatter rails for one rank r.
  * Tile rail of rank r: TILE(chunk c, band b, column tile j) over the whole
  * [m, n] partial of rank r.
- *   band order (order = 0): band b outermost, then chunk c, then j
+ *   band order (order = 0): band b outermost, then column tile j, then chunk c
  *     [explainer, "Role switching only works": output produced band by band
- *     across every rank's chunk];
+ *     across every rank's chunk; the order inside a band is not given: column
+ *     tile outer, chunk inner keeps the tiles that share one W_r column slice
+ *     adjacent];
  *   row order  (order = 1): chunk c, then band b, then j (global row order).
  * Reduce rail of rank r: REDUCE(c = r, band b, column tile j), b outer, j inner.
  * Bands are R rows of a chunk of m/P rows. */
@@ -499,8 +501,8 @@ ORC_EXPORT int64_t orc_rail_rs(int P, int64_t m, int64_t n, int R, int BN, int o
     int64_t nb = 0, nr = 0;
     if (order == 0) {
         for (int64_t b = 0; b < bands; b++)
-            for (int c = 0; c < P; c++)
-                for (int64_t j = 0; j < tn; j++) {
+            for (int64_t j = 0; j < tn; j++)
+                for (int c = 0; c < P; c++) {
                     if (tile_out) {
                         int32_t *e = tile_out + 4 * nb;
                         e[0] = ORC_TILE; e[1] = c; e[2] = (int32_t)b; e[3] = (int32_t)j;
