@@ -261,6 +261,50 @@ def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak):
             "launches_per_step": 1}
 
 
+def bench_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak):
+    """All-gather + GEMM on MXFP8 operands (E4M3 + E8M0 per 32 K), the shapes
+    of the 8-rank bf16 workload; quantisation on the GPU before timing (the
+    kernel's inputs are the quantised bytes).  Peak: the measured bf16 dense
+    peak x 2 (the nominal fp8 : bf16 dense ratio, 4.5 : 2.25 PFLOP/s)."""
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS["ag_mxfp8_p8"]
+    inp = workload_inputs(w)
+    P, m, k, n = w.P, w.m, w.k, w.n
+
+    def quant(x, along):
+        r, c = x.shape
+        q = torch.empty(r, c, dtype=torch.uint8, device=dev)
+        sc = torch.empty(K.mxfp8_scale_bytes(r, c, along), dtype=torch.uint8, device=dev)
+        K.mxfp8_quantize(x.to(dev), q, sc, along, stream=stream)
+        return q, sc
+
+    qs, ss = zip(*[quant(x, True) for x in inp["x"]])
+    qw, sw = quant(inp["w"], False)
+    del inp
+    xg = torch.empty(P * m, k, dtype=torch.uint8, device=dev)
+    y = torch.empty(P * m, n, dtype=torch.bfloat16, device=dev)
+    flops = w.flops()
+    peak = 2.0 * bf16_peak
+
+    def timed(o):
+        wsb = K.workspace(K.OP_AG_GEMM, P, m, n, k, dtype=K.MXFP8_E4M3, o=o, device=dev)
+        f = lambda: K.ag_gemm(list(qs), qw, xg, y, wsb, o, dtype=K.MXFP8_E4M3, x_scales=list(ss), w_scales=sw,
+                              stream=stream)
+        f()
+        K.check(wsb, "ag_gemm mxfp8")
+        t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
+        K.check(wsb, "ag_gemm mxfp8")
+        return flops / (t * 1e-3) / 1e12, t
+
+    tf, ms = timed(K.opts())
+    fx, _ = timed(K.opts(sched=K.SCHED_FIXED))
+    un, _ = timed(K.opts(sched=K.SCHED_UNFUSED))
+    return {"workload": "ag_mxfp8_p8", "ms": ms, "tflops": tf, "peak": peak,
+            "peak_source": "measured bf16 dense x 2 (nominal fp8/bf16 ratio)", "frac_of_peak": tf / peak,
+            "fixed_split_tflops": fx, "unfused_tflops": un, "vs_fixed_split": tf / fx, "vs_unfused": tf / un}
+
+
 def run_reference(args):
     ws, rank, local = dist_env()
     if ws > 1 and rank != 0:
@@ -409,6 +453,8 @@ def run_kosmos(args):
         also["gemm_rs"] = bench_rs(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
         also["moe_fwd"] = bench_moe(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"], peak)
+        torch.cuda.empty_cache()
+        also["ag_mxfp8"] = bench_mxfp8(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
 
     line = None

@@ -249,6 +249,13 @@ def moe_debug_view(what: int, P: int, tokens: int, hidden: int, n_experts: int, 
     return ws[off:off + nb.value]
 
 
+def mxfp8_scale_bytes(rows: int, cols: int, along_cols: bool) -> int:
+    """Bytes of the MMA-tiled E8M0 scale tensor for an operand [rows, cols]."""
+    srows = rows if along_cols else cols
+    kk = cols if along_cols else rows
+    return -(-srows // 128) * 128 * (kk // 32)
+
+
 def mxfp8_quantize(x, q, scales, along_cols: bool, stream=None):
     _check_cuda(x, q, scales)
     rows, cols = x.shape

@@ -1,0 +1,453 @@
+// ag_mxfp8.cu -- all-gather + GEMM with MXFP8 operands (E4M3 elements, one E8M0
+// scale per 32 consecutive K-elements), one self-scheduling persistent launch
+// (KOSMOS abstract: TP+SP training "1.10-1.25x in MXFP8").
+//
+// Same rails and roles as the bf16 kernel (ag_gemm.cu): movers copy remote
+// shard pieces (elements and their scale blocks) into the gathered buffers and
+// release per-piece flags; builders start on the local shard.  The product uses
+// tcgen05.mma kind::mxf8f6f4.block_scale: per 128-wide K stage the MMA warp
+// copies the stage's scale factors from shared memory into tensor memory with
+// tcgen05.cp, then issues four K=32 MMAs, each selecting its scale byte.
+//
+// Scale layout (MMA-tiled, produced by kosmos_mxfp8_quantize): for an operand
+// with R scale rows (rows of X, columns of W) and K, the scale of (row r,
+// K-block b) is at byte ((r/128)*(K/128) + b/4)*512 + (r%32)*16 + ((r/32)%4)*4
+// + b%4.  One 512-byte atom covers 128 rows x 4 K-blocks; copied with
+// tcgen05.cp 32x128b.warpx4 it lands in four TMEM columns, lane r%32 of every
+// 32-lane group holding rows r%32 + 32c in column c, one byte per K-block.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "engine.cuh"
+#include "launch.h"
+
+namespace kosmos {
+
+constexpr int FBK = 128;                       // K elements (bytes) per stage
+constexpr int F_A_BYTES = BM * FBK;            // 16 KB
+constexpr int F_B_SLAB = 128 * FBK;            // one 128-column slab of B: 16 KB
+constexpr int F_B_BYTES = 2 * F_B_SLAB;        // 32 KB
+constexpr int F_SF_BYTES = 3 * 512;            // SFA atom + two SFB atoms
+constexpr int F_SMEM_BYTES = SMEM_BYTES + NSTAGE * F_SF_BYTES;
+constexpr int F_TMEM_SF = 256;                 // first TMEM column of the scale buffers
+constexpr int F_TMEM_SF_STRIDE = 16;           // columns per stage: SFA 4, SFB 8 (+4 spare)
+
+struct AgF8Params {
+    CUtensorMap tmA_local;  // x_shards[0]: dims {k, m} (bytes), box {128, 128}, 128B swizzle
+    CUtensorMap tmA_gath;   // x_gathered: dims {k, m, P}, box {128, 128, 1}
+    CUtensorMap tmB;        // W: dims {n, k}, box {128, 128}
+    const uint8_t *x_src[KOSMOS_MAX_P];
+    const uint8_t *sx_src[KOSMOS_MAX_P];  // tiled scales of each shard
+    const uint8_t *sw;                    // tiled scales of W
+    uint8_t *x_gath;
+    uint8_t *sx_gath;                     // tiled scales, gathered [P][pieces][k/128][512]
+    __nv_bfloat16 *y;
+    WsHeader *ws;
+    uint32_t *flags;
+    TraceRec *trace;
+    AgGeom g;
+    int nkb;          // k / 128
+    int nb_w;         // 128-column scale blocks of W
+    int sched;
+    int n_comm;
+    uint64_t wait_limit_ns;
+    uint64_t inject;
+};
+
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 32 rows x 16 bytes from shared memory into TMEM lanes 0-31 of four columns,
+// replicated to the four 32-lane groups.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Descriptor of a 32-row x 16-byte matrix stored contiguously (rows 16 bytes
+// apart; 8-row core matrices 128 bytes apart), no swizzle.
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128 >> 4) << 16;  // leading byte offset (one 16-byte column: unused)
+    d |= static_cast<uint64_t>(128 >> 4) << 32;  // stride byte offset between 8-row core matrices
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: A/B E4M3 (format 0),
+// A K-major, B MN-major, scale type E8M0 (bit 23), N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28, B scale byte at bits 4-5, A scale byte at bits 29-30.
+__device__ __forceinline__ uint32_t idesc_mxf8(int M, int N, int sf_id) {
+    return (static_cast<uint32_t>(sf_id) << 4) | (1u << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+}
+
+struct F8Smem {
+    Smem base;
+    uint8_t *sf;  // [NSTAGE][F_SF_BYTES]
+};
+
+__device__ __forceinline__ F8Smem carve_f8(uint8_t *raw) {
+    F8Smem s;
+    s.base = carve_smem(raw);
+    s.sf = s.base.stages + NSTAGE * STAGE_BYTES + SMEM_CTRL_BYTES;
+    return s;
+}
+
+// Copies n bytes with bulk async copies through the stage buffers (the caller
+// owns them), tracking the copy barriers' phases in cphase.
+__device__ __forceinline__ bool bulk_copy_staged(const Smem &sm, const uint8_t *src, uint8_t *dst, int64_t bytes,
+                                                 uint32_t &cphase, WsHeader *ws, int64_t entry) {
+    constexpr int64_t CH = STAGE_BYTES;
+    const int64_t nch = cdiv(bytes, CH);
+    auto cb = [&](int64_t c) -> uint32_t {
+        const int64_t rem = bytes - c * CH;
+        return static_cast<uint32_t>(rem < CH ? rem : CH);
+    };
+    for (int64_t c = 0; c < nch && c < NSTAGE; ++c) {
+        mbar_arrive_expect_tx(&sm.cbar[c], cb(c));
+        bulk_g2s(sm.stages + c * CH, src + c * CH, cb(c), &sm.cbar[c]);
+    }
+    for (int64_t c = 0; c < nch; ++c) {
+        const int b = static_cast<int>(c % NSTAGE);
+        if (!mbar_wait(&sm.cbar[b], (cphase >> b) & 1u, PIPE_LIMIT_NS)) {
+            bulk_wait<0>();
+            set_error(ws, KOSMOS_ERR_DEVICE, entry);
+            return false;
+        }
+        cphase ^= (1u << b);
+        bulk_s2g(dst + c * CH, sm.stages + b * CH, cb(c));
+        bulk_commit();
+        const int64_t refill = c - 1 + NSTAGE;
+        if (c >= 1 && refill < nch) {
+            bulk_wait_read<1>();
+            const int rb = static_cast<int>((c - 1) % NSTAGE);
+            mbar_arrive_expect_tx(&sm.cbar[rb], cb(refill));
+            bulk_g2s(sm.stages + rb * CH, src + refill * CH, cb(refill), &sm.cbar[rb]);
+        }
+    }
+    bulk_wait<0>();
+    return true;
+}
+
+__device__ __noinline__ bool f8_transfer(const AgF8Params &p, const Smem &sm, int t, uint32_t &cphase,
+                                         uint32_t epoch) {
+    int shard, piece;
+    ag_decode_transfer(p.g, t, shard, piece);
+    const int64_t row_bytes = p.g.k;
+    const int64_t row0 = static_cast<int64_t>(piece) * PIECE_ROWS;
+    const int64_t rows = (p.g.m - row0 < PIECE_ROWS) ? (p.g.m - row0) : PIECE_ROWS;
+    if (!bulk_copy_staged(sm, p.x_src[shard] + row0 * row_bytes,
+                          p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes, rows * row_bytes, cphase,
+                          p.ws, t))
+        return false;
+    const int64_t sblk = static_cast<int64_t>(p.nkb) * 512;  // scale bytes of one 128-row block
+    if (!bulk_copy_staged(sm, p.sx_src[shard] + piece * sblk,
+                          p.sx_gath + (static_cast<int64_t>(shard) * p.g.pieces + piece) * sblk, sblk, cphase, p.ws, t))
+        return false;
+    fence_proxy_async_global();
+    __threadfence();
+    const bool drop = (p.inject & KOSMOS_INJECT_DROP_TRANSFER) && static_cast<int64_t>(p.inject >> 32) == t;
+    if (!drop) st_release_gpu(&p.flags[shard * p.g.pieces + piece], epoch + 1u);
+    return true;
+}
+
+__device__ __forceinline__ void f8_producer(const AgF8Params &p, const F8Smem &fs, uint32_t epoch) {
+    const Smem &sm = fs.base;
+    const int cta = blockIdx.x;
+    bool mover = (p.sched != KOSMOS_SCHED_UNFUSED) && cta < p.n_comm;
+    uint32_t cphase = 0;
+    PipeState ps;
+    RingState rs;
+    int nrec = 0;
+    const int64_t sblk = static_cast<int64_t>(p.nkb) * 512;
+    while (true) {
+        if (failed(p.ws)) break;
+        if (mover) {
+            const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
+            if (t < static_cast<uint32_t>(p.g.n_transfer)) {
+                const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+                if (!f8_transfer(p, sm, static_cast<int>(t), cphase, epoch)) break;
+                if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
+                    r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
+                    r->kind = K_TRANSFER; r->ticket = static_cast<int32_t>(t); r->cta = cta;
+                }
+                ++nrec;
+                continue;
+            }
+            if (p.sched == KOSMOS_SCHED_FIXED) break;
+            mover = false;
+        }
+        const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
+        if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
+        int s, i, c;
+        ag_decode_tile(p.g, static_cast<int>(t), s, i, c);
+        const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+        if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0) {
+            if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], epoch + 1u, p.wait_limit_ns, t)) break;
+        }
+        int slot = -1;
+        if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
+            r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
+            r->kind = K_TILE; r->ticket = static_cast<int32_t>(t); r->cta = cta;
+            slot = nrec;
+        }
+        ++nrec;
+        SchedEntry e;
+        e.kind = K_TILE; e.a = s; e.b = i; e.c = c; e.d = 0; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
+        e.slot = slot; e.nmma = 0; e.x0 = e.x1 = e.x2 = 0;
+        if (!ring_push(sm, rs, e, p.ws)) break;
+        const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+        const uint8_t *sfa_base = local ? (p.sx_src[0] + static_cast<int64_t>(i) * sblk)
+                                        : (p.sx_gath + (static_cast<int64_t>(s) * p.g.pieces + i) * sblk);
+        const int nb0 = c * 2, nb1 = c * 2 + 1;
+        const bool has_b1 = nb1 < p.nb_w;
+        const uint32_t bytes = F_A_BYTES + F_B_BYTES + 512u * (has_b1 ? 3u : 2u);
+        bool ok = true;
+        for (int kb = 0; kb < p.nkb; ++kb) {
+            if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                ok = false;
+                break;
+            }
+            uint8_t *sa = sm.stages + ps.stage * STAGE_BYTES;
+            uint8_t *sb = sa + F_A_BYTES;
+            uint8_t *sf = fs.sf + ps.stage * F_SF_BYTES;
+            uint64_t *bar = &sm.full[ps.stage];
+            mbar_arrive_expect_tx(bar, bytes);
+            if (local)
+                tma_load_2d(sa, &p.tmA_local, bar, kb * FBK, i * BM);
+            else
+                tma_load_3d(sa, &p.tmA_gath, bar, kb * FBK, i * BM, s);
+            tma_load_2d(sb, &p.tmB, bar, c * BN, kb * FBK);
+            tma_load_2d(sb + F_B_SLAB, &p.tmB, bar, c * BN + 128, kb * FBK);
+            bulk_g2s(sf, sfa_base + static_cast<int64_t>(kb) * 512, 512, bar);
+            bulk_g2s(sf + 512, p.sw + (static_cast<int64_t>(nb0) * p.nkb + kb) * 512, 512, bar);
+            if (has_b1) bulk_g2s(sf + 1024, p.sw + (static_cast<int64_t>(nb1) * p.nkb + kb) * 512, 512, bar);
+            ps.advance();
+        }
+        if (!ok) break;
+    }
+    SchedEntry done;
+    done.kind = K_DONE; done.a = done.b = done.c = done.d = 0; done.nstage = 0; done.ticket = -1; done.slot = -1;
+    done.nmma = 0; done.x0 = done.x1 = done.x2 = 0;
+    ring_push(sm, rs, done, p.ws);
+}
+
+// One accumulator (TMEM columns 0..255); the scale buffers use 256 + 16*stage.
+__device__ __forceinline__ void f8_mma_loop(const F8Smem &fs, uint32_t tmem_base, WsHeader *ws) {
+    const Smem &sm = fs.base;
+    PipeState ps;
+    RingState rs;
+    uint32_t acc_phase = 0;
+    while (true) {
+        if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
+            set_error(ws, KOSMOS_ERR_DEVICE, -3);
+            break;
+        }
+        const SchedEntry e = sm.sched[rs.idx];
+        mbar_arrive(&sm.sempty[rs.idx]);
+        rs.advance();
+        if (e.kind == K_DONE) break;
+        if (e.kind != K_TILE) {
+            ps.advance(e.nstage);
+            continue;
+        }
+        if (!mbar_wait(&sm.tempty[0], acc_phase ^ 1u, PIPE_LIMIT_NS)) {
+            set_error(ws, KOSMOS_ERR_DEVICE, -4);
+            break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < e.nstage; ++kb) {
+            if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+                set_error(ws, KOSMOS_ERR_DEVICE, -5);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sm.stages + ps.stage * STAGE_BYTES);
+            const uint32_t b_addr = a_addr + F_A_BYTES;
+            const uint32_t sf_addr = smem_u32(fs.sf + ps.stage * F_SF_BYTES);
+            const uint32_t sfa_t = tmem_base + F_TMEM_SF + ps.stage * F_TMEM_SF_STRIDE;
+            const uint32_t sfb_t = sfa_t + 4;
+            tmem_cp_32x128b_x4(sfa_t, sdesc_sf(sf_addr));
+            tmem_cp_32x128b_x4(sfb_t, sdesc_sf(sf_addr + 512));
+            tmem_cp_32x128b_x4(sfb_t + 4, sdesc_sf(sf_addr + 1024));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint64_t ad = sdesc_sw128(a_addr + j * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(b_addr + j * (32 * 128), F_B_SLAB, 1024);
+                mma_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(BM, BN, j), sfa_t, sfb_t, (kb | j) != 0 ? 1u : 0u);
+            }
+            mma_commit(&sm.empty[ps.stage]);
+            ps.advance();
+        }
+        if (!ok) break;
+        mma_commit(&sm.tfull[0]);
+        acc_phase ^= 1u;
+    }
+}
+
+// Drains the accumulator into registers (bf16-packed), releases it, then stores.
+__device__ __forceinline__ void f8_epilogue(const AgF8Params &p, const Smem &sm, uint32_t tmem_base, int warp,
+                                            int lane) {
+    const int grp = warp & 3;
+    const int row = grp * 32 + lane;
+    RingState rs;
+    uint32_t acc_phase = 0;
+    while (true) {
+        if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -6);
+            break;
+        }
+        const SchedEntry e = sm.sched[rs.idx];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sempty[rs.idx]);
+        rs.advance();
+        if (e.kind == K_DONE) break;
+        if (e.kind != K_TILE) continue;
+        if (!mbar_wait(&sm.tfull[0], acc_phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
+            break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16);
+        uint32_t packed[BN / 2];
+#pragma unroll
+        for (int ch = 0; ch < BN / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + ch * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                packed[ch * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[0]);
+        acc_phase ^= 1u;
+        const int s = e.a, i = e.b, c = e.c;
+        const int64_t rloc = static_cast<int64_t>(i) * BM + row;
+        if (rloc < p.g.m) {
+            __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + rloc) * p.g.n;
+#pragma unroll
+            for (int q = 0; q < BN / 8; ++q) {
+                const int64_t col = static_cast<int64_t>(c) * BN + q * 8;
+                if (col < p.g.n)
+                    *reinterpret_cast<uint4 *>(yrow + col) =
+                        make_uint4(packed[q * 4], packed[q * 4 + 1], packed[q * 4 + 2], packed[q * 4 + 3]);
+            }
+        }
+        if (e.slot >= 0 && lane == 0 && grp == 0) {
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) ag_mxfp8_kernel(const __grid_constant__ AgF8Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const F8Smem fs = carve_f8(smem_raw);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
+    engine_setup(fs.base, warp);
+    const uint32_t tmem_base = *fs.base.tmem_slot;
+    if (warp == 0) {
+        if (lane == 0) f8_producer(p, fs, epoch);
+    } else if (warp == 1) {
+        if (lane == 0) f8_mma_loop(fs, tmem_base, p.ws);
+    } else {
+        f8_epilogue(p, fs.base, tmem_base, warp, lane);
+    }
+    engine_teardown(fs.base, warp, tmem_base);
+    if (threadIdx.x == 0) engine_finish(p.ws, epoch, 2);
+}
+
+// Unfused baseline, first launch: gather elements and scale blocks of every shard.
+__global__ void __launch_bounds__(256) ag_f8_gather_copy_kernel(const AgF8Params p) {
+    const int64_t shard_bytes = p.g.m * p.g.k;
+    const int64_t sblk = static_cast<int64_t>(p.nkb) * 512 * p.g.pieces;
+    const int64_t per = shard_bytes / 16, sper = sblk / 16;
+    const int64_t total = (per + sper) * p.g.P;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += stride) {
+        const int64_t s = v / (per + sper);
+        const int64_t o = v - s * (per + sper);
+        if (o < per)
+            reinterpret_cast<uint4 *>(p.x_gath + s * shard_bytes)[o] = reinterpret_cast<const uint4 *>(p.x_src[s])[o];
+        else
+            reinterpret_cast<uint4 *>(p.sx_gath + s * sblk)[o - per] =
+                reinterpret_cast<const uint4 *>(p.sx_src[s])[o - per];
+    }
+}
+
+size_t ag_mxfp8_scale_bytes(int P, int64_t m, int64_t k) {
+    return static_cast<size_t>(P) * static_cast<size_t>(cdiv(m, BM)) * static_cast<size_t>(k / FBK) * 512;
+}
+
+kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream) {
+    AgF8Params p;
+    memset(&p, 0, sizeof(p));
+    p.g = ag_geom(L.P, L.m, L.k, L.n);
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(L.k), static_cast<uint64_t>(L.m)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(L.k)};
+        const uint32_t box[2] = {FBK, BM};
+        if (!encode_tmap(&p.tmA_local, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.x[0]), dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(L.k), static_cast<uint64_t>(L.m), static_cast<uint64_t>(L.P)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(L.k), static_cast<uint64_t>(L.m * L.k)};
+        const uint32_t box[3] = {FBK, BM, 1};
+        if (!encode_tmap(&p.tmA_gath, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, L.x_gathered, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(L.n), static_cast<uint64_t>(L.k)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(L.n)};
+        const uint32_t box[2] = {128, FBK};
+        if (!encode_tmap(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.w), dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    for (int r = 0; r < L.P; ++r) {
+        p.x_src[r] = static_cast<const uint8_t *>(L.x[r]);
+        p.sx_src[r] = static_cast<const uint8_t *>(L.xs[r]);
+    }
+    p.sw = static_cast<const uint8_t *>(L.wsc);
+    p.x_gath = static_cast<uint8_t *>(L.x_gathered);
+    p.y = static_cast<__nv_bfloat16 *>(L.y);
+    const AgWsLayout W = ag_ws_layout(p.g, L.trace != 0);
+    uint8_t *ws = static_cast<uint8_t *>(L.ws);
+    p.ws = reinterpret_cast<WsHeader *>(ws);
+    p.flags = reinterpret_cast<uint32_t *>(ws + W.flags_off);
+    p.trace = L.trace ? reinterpret_cast<TraceRec *>(ws + W.trace_off) : nullptr;
+    p.sx_gath = ws + W.total;  // gathered scale blocks follow the bf16 layout (see kosmos_workspace_bytes)
+    p.nkb = static_cast<int>(L.k / FBK);
+    p.nb_w = static_cast<int>(cdiv(L.n, 128));
+    p.sched = L.sched;
+    p.n_comm = L.n_comm;
+    p.wait_limit_ns = L.wait_limit_ns;
+    p.inject = L.inject;
+    if (L.sched == KOSMOS_SCHED_UNFUSED) {
+        ag_f8_gather_copy_kernel<<<L.grid * 4, 256, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return KOSMOS_ERR_CUDA;
+    }
+    return launch_persistent(reinterpret_cast<const void *>(&ag_mxfp8_kernel), &p, L.grid, F_SMEM_BYTES, stream);
+}
+
+}  // namespace kosmos

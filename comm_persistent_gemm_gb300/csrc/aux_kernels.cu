@@ -26,24 +26,43 @@ __device__ __forceinline__ int mx_block_exp(float blockmax) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
-// One thread per 32-element block.
+// Byte offset of the scale of (scale row r, K-block b) in the MMA-tiled layout:
+// 512-byte atoms of 128 scale rows x 4 K-blocks, atoms ordered by row block,
+// then K; inside an atom row r sits at (r % 32) * 16 + ((r / 32) % 4) * 4.
+__device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t b, int64_t kblocks) {
+    return ((r / 128) * (kblocks / 4) + b / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + (b % 4);
+}
+
+// One thread per 32-element block; scale rows beyond the operand (padding of
+// the last 128-row atom) get the neutral scale 2^0.
 __global__ void mxfp8_quantize_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols, int along_cols,
                                       uint8_t *__restrict__ q, uint8_t *__restrict__ scales) {
-    const int64_t nblk = along_cols ? rows * (cols / 32) : (rows / 32) * cols;
+    const int64_t srows = along_cols ? rows : cols;       // scale rows
+    const int64_t kblocks = along_cols ? cols / 32 : rows / 32;
+    const int64_t srows_pad = cdiv(srows, 128) * 128;
+    const int64_t nblk = srows_pad * kblocks;
     for (int64_t bi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; bi < nblk;
          bi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         int64_t base, step, sidx;
         if (along_cols) {
-            const int64_t r = bi / (cols / 32), kb = bi % (cols / 32);
+            const int64_t r = bi / kblocks, kb = bi % kblocks;
+            if (r >= rows) {
+                scales[sf_tiled_offset(r, kb, kblocks)] = 127;
+                continue;
+            }
             base = r * cols + kb * 32;
             step = 1;
-            sidx = r * (cols / 32) + kb;
+            sidx = sf_tiled_offset(r, kb, kblocks);
         } else {
             // consecutive threads take consecutive columns of the same 32-row block
-            const int64_t kb = bi / cols, c = bi % cols;
+            const int64_t kb = bi / srows_pad, c = bi % srows_pad;
+            if (c >= cols) {
+                scales[sf_tiled_offset(c, kb, kblocks)] = 127;
+                continue;
+            }
             base = kb * 32 * cols + c;
             step = cols;
-            sidx = c * (rows / 32) + kb;
+            sidx = sf_tiled_offset(c, kb, kblocks);
         }
         float mx = 0.f;
         for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(bf16_bits_to_float(x[base + j * step])));
@@ -59,7 +78,7 @@ __global__ void mxfp8_quantize_kernel(const uint16_t *__restrict__ x, int64_t ro
 
 kosmos_status launch_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q, void *scales,
                                     cudaStream_t stream) {
-    const int64_t nblk = along_cols ? rows * (cols / 32) : (rows / 32) * cols;
+    const int64_t nblk = cdiv(along_cols ? rows : cols, 128) * 128 * (along_cols ? cols / 32 : rows / 32);
     int64_t blocks = cdiv(nblk, 256);
     if (blocks > 65535) blocks = 65535;
     if (blocks < 1) blocks = 1;

@@ -138,9 +138,13 @@ int kosmos_num_sms(void) { return device_sms(); }
 size_t kosmos_workspace_bytes(int op, int P, int64_t m, int64_t n, int64_t k, int dtype, const kosmos_opts *opts) {
     const kosmos_opts o = resolve_opts(opts);
     if (P < 1 || P > KOSMOS_MAX_P || m < 1 || n < 1 || k < 1) return 0;
-    (void)dtype;
     if (op == KOSMOS_OP_AG_GEMM) {
-        return ag_ws_layout(ag_geom(P, m, k, n), o.trace != 0).total;
+        size_t total = ag_ws_layout(ag_geom(P, m, k, n), o.trace != 0).total;
+        if (dtype == KOSMOS_MXFP8_E4M3) {
+            if (k % 128) return 0;
+            total += ag_mxfp8_scale_bytes(P, m, k);  // gathered scale blocks
+        }
+        return total;
     }
     if (op == KOSMOS_OP_GEMM_RS) {
         if (m % P) return 0;
@@ -308,7 +312,7 @@ kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, 
 kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q, void *scales,
                                     void *stream) {
     if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || rows < 1 || cols < 1) return KOSMOS_ERR_INVALID_ARG;
-    if (along_cols ? (cols % 32 != 0) : (rows % 32 != 0)) return KOSMOS_ERR_INVALID_ARG;
+    if (along_cols ? (cols % 128 != 0) : (rows % 128 != 0)) return KOSMOS_ERR_INVALID_ARG;
     return launch_mxfp8_quantize(x, rows, cols, along_cols, q, scales, static_cast<cudaStream_t>(stream));
 }
 

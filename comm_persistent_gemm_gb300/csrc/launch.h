@@ -77,6 +77,7 @@ kosmos_status launch_persistent(const void *func, void *params, int grid, int sm
 
 kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream);
 kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream);
+size_t ag_mxfp8_scale_bytes(int P, int64_t m, int64_t k);
 kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream);
 kosmos_status launch_moe_fwd(const MoeLaunch &L, cudaStream_t stream);
 size_t moe_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool trace);

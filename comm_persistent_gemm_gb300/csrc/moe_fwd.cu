@@ -1021,9 +1021,4 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
     return launch_persistent(reinterpret_cast<const void *>(&moe_fwd_kernel), &p, Lc.grid, MOE_SMEM_BYTES, stream);
 }
 
-kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream) {
-    (void)L; (void)stream;
-    return KOSMOS_ERR_UNSUPPORTED;
-}
-
 }  // namespace kosmos

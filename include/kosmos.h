@@ -131,10 +131,16 @@ KOSMOS_API kosmos_status kosmos_workspace_init(void *ws, size_t ws_bytes, void *
  *
  *   x_shards[r]  : P pointers, X_r [m_per_shard, k]; x_shards[0] is the local shard.
  *                  BF16: bf16.  MXFP8: E4M3 bytes.
- *   x_scales[r]  : MXFP8 only: [m_per_shard, k/32] E8M0 bytes; else NULL.
+ *   x_scales[r]  : MXFP8 only: E8M0 scales of X_r (one per row and 32
+ *                  consecutive K-elements) in the MMA-tiled layout below; else NULL.
  *   w            : [k, n] (BF16: bf16; MXFP8: E4M3 bytes).
- *   w_scales     : MXFP8 only: [n, k/32] E8M0, one byte per 32 consecutive
- *                  K-elements of a column; else NULL.
+ *   w_scales     : MXFP8 only: E8M0 scales of W (one per column and 32
+ *                  consecutive K-elements), MMA-tiled with the columns of W as
+ *                  scale rows; else NULL.
+ *   MMA-tiled scale layout: for R scale rows and K, the scale of (row r,
+ *   K-block b = k/32) is at byte ((r/128)*(K/128) + b/4)*512 + (r%32)*16 +
+ *   ((r/32)%4)*4 + b%4; size ceil(R/128)*128*K/32 bytes.  kosmos_mxfp8_quantize
+ *   writes it.  The MXFP8 workspace also holds the gathered scale blocks.
  *   x_gathered   : out, [P*m_per_shard, k], same element type as X: the
  *                  gathered input (kept for the backward pass).
  *   y            : out, [P*m_per_shard, n] bf16, fp32 accumulation, one
@@ -220,10 +226,12 @@ KOSMOS_API kosmos_status kosmos_moe_debug_view(int what, int P, int64_t tokens, 
  * (clamped to [-127, 127]; an all-zero block takes e = 0), scale byte e + 127,
  * element byte = E4M3(x / 2^e) rounded to nearest even.
  *   along_cols = 1: x [rows, cols], blocks along a row (activations X[m, k]);
- *                   scales [rows, cols/32].
+ *                   scale rows = rows, K = cols.
  *   along_cols = 0: x [rows, cols], blocks along a column (weights W[k, n]);
- *                   scales [cols, rows/32].
- *   q keeps x's [rows, cols] layout.  Requirements: the blocked extent % 32 == 0.
+ *                   scale rows = cols, K = rows.
+ *   q keeps x's [rows, cols] layout; scales are written in the MMA-tiled
+ *   layout described at kosmos_ag_gemm (ceil(R/128)*128*K/32 bytes; padding
+ *   rows get the scale byte 127).  Requirements: K % 128 == 0.
  */
 KOSMOS_API kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols,
                                     void *q, void *scales, void *stream);

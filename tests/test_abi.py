@@ -64,7 +64,7 @@ def test_host_validation_rejects_bad_args(K):
     ys = (C.c_void_p * P)(base, base)
     assert lib.kosmos_gemm_rs(xs, xs, P, 63, 64, 64, 0, ys, base, 1 << 20, None, None) == 1
     # quantiser: blocked extent not a multiple of 32
-    assert lib.kosmos_mxfp8_quantize(base, 4, 48, 1, base, base, None) == 1
+    assert lib.kosmos_mxfp8_quantize(base, 4, 96, 1, base, base, None) == 1
 
 
 @pytest.mark.parametrize("P,m,n", [(2, 64, 128), (8, 1024, 3584), (3, 200, 264), (1, 5, 8)])
