@@ -109,6 +109,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def dist_max(value: float, device=None) -> float:
+    """Maximum of a per-rank value over all ranks (the value itself when not
+    running distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank: float, step_ms_max: float, world: int) -> float:
+    """Units per second processed by all ranks, timed by the slowest rank."""
+    return world * work_per_rank / (step_ms_max * 1e-3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -210,6 +227,25 @@ def bench_rs(K, dev, steps, warmup, flush, stream, peak):
             "vs_fixed_split_best": tf / fixed[best], "vs_unfused": tf / (flops / (unf * 1e-3) / 1e12)}
 
 
+def bench_rs_quick(K, dev, steps, warmup, flush, stream):
+    """The band-ordered GEMM + reduce-scatter alone (8 ranks, [8192, 3584] x [3584, 8192])."""
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS["rs_bf16_p8"]
+    inp = workload_inputs(w)
+    P, m, k, n = w.P, w.m, w.k, w.n
+    xs = [x.to(dev) for x in inp["x"]]
+    ws_ = [x.to(dev) for x in inp["w"]]
+    del inp
+    ys = [torch.empty(m // P, n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    o = K.opts()
+    wsb = K.workspace(K.OP_GEMM_RS, P, m, n, k, o=o, device=dev)
+    f = lambda: K.gemm_rs(xs, ws_, ys, wsb, o, stream=stream)
+    t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
+    K.check(wsb, "gemm_rs")
+    return {"workload": "rs_bf16_p8", "ms": t, "tflops": w.flops() / (t * 1e-3) / 1e12}
+
+
 # Algorithmic HBM bytes of one MoE forward step (2048 tokens, hidden 4096,
 # 128 experts top-8, inter 1536, bf16): every expert weight read once
 # (128 x 3 x 4096 x 1536 x 2 = 4.83 GB), router weights, token reads and
@@ -229,10 +265,13 @@ def moe_algorithmic_bytes(T, H, E, K, I):
     return weights + dispatch + gemm_in + h_out + y_out + push + fold + router_in
 
 
-def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak):
+def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0):
+    import dataclasses
     import torch
     from kosmos_inputs import WORKLOADS, workload_inputs
     w = WORKLOADS["moe_fwd_p8"]
+    if experts:  # a smaller expert count for profiler captures (same kernel, fewer weights)
+        w = dataclasses.replace(w, E=experts, name=f"moe_fwd_p8_e{experts}")
     inp = workload_inputs(w)
     P, T, H, E, Kt, I = w.P, w.T, w.H, w.E, w.topk, w.I
     xs = [t.to(dev) for t in torch.chunk(inp["x"], P, 0)]
@@ -254,14 +293,14 @@ def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak):
     K.check(wsb, "moe_fwd")
     byt = moe_algorithmic_bytes(T, H, E, Kt, I)
     gbs = byt / (t * 1e-3) / 1e9
-    return {"workload": "moe_fwd_p8", "ms": t, "tokens_per_s": T / (t * 1e-3),
+    return {"workload": w.name, "ms": t, "tokens_per_s": T / (t * 1e-3),
             "tflops": w.flops() / (t * 1e-3) / 1e12, "frac_of_tensor_peak": w.flops() / (t * 1e-3) / 1e12 / tensor_peak,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
                          "bytes_per_launch": byt},
             "launches_per_step": 1}
 
 
-def bench_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak):
+def bench_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=True):
     """All-gather + GEMM on MXFP8 operands (E4M3 + E8M0 per 32 K), the shapes
     of the 8-rank bf16 workload; quantisation on the GPU before timing (the
     kernel's inputs are the quantised bytes).  Peak: the measured bf16 dense
@@ -298,6 +337,8 @@ def bench_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak):
         return flops / (t * 1e-3) / 1e12, t
 
     tf, ms = timed(K.opts())
+    if not baselines:
+        return {"workload": "ag_mxfp8_p8", "ms": ms, "tflops": tf, "peak": peak, "frac_of_peak": tf / peak}
     fx, _ = timed(K.opts(sched=K.SCHED_FIXED))
     un, _ = timed(K.opts(sched=K.SCHED_UNFUSED))
     return {"workload": "ag_mxfp8_p8", "ms": ms, "tflops": tf, "peak": peak,
@@ -333,8 +374,32 @@ def run_reference(args):
     return 0
 
 
+def run_quick_other(args):
+    """Quick mode for the other workloads: one configuration, timed region only."""
+    import torch
+    import comm_persistent_gemm_gb300 as K
+    K.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)
+    peaks, _ = load_peaks()
+    if args.workload == "rs":
+        r = bench_rs_quick(K, dev, args.steps, args.warmup, flush, stream)
+    elif args.workload == "moe":
+        r = bench_moe(K, dev, args.steps, args.warmup, flush, stream, peaks["hbm_gbs"], peaks["bf16_tflops"],
+                      experts=args.experts)
+    else:
+        r = bench_mxfp8(K, dev, args.steps, args.warmup, flush, stream, peaks["bf16_tflops"], baselines=False)
+    print(json.dumps({"quick": True, "workload": args.workload, **r}))
+    return 0
+
+
 def run_kosmos(args):
     import torch
+    if args.quick and args.workload != "ag":
+        return run_quick_other(args)
     world, rank, local = dist_env()
     if world > 1:
         import torch.distributed as dist
@@ -382,12 +447,8 @@ def run_kosmos(args):
     if world > 1:
         torch.distributed.barrier()
     K.check(ws_self, "ag_gemm")
-    step_ms = statistics.mean(times)
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = world * flops / (step_ms * 1e-3) / 1e12
+    step_ms = dist_max(statistics.mean(times), dev)
+    value = whole_job_rate(flops, step_ms, world) / 1e12
     clocks = clk.summary()
     if args.quick:
         if rank == 0:
@@ -433,12 +494,8 @@ def run_kosmos(args):
 
     et = time_kernel_steps(e2e_step, args.steps, args.warmup, flush, stream)
     K.check(ws_self, "ag_gemm e2e")
-    e2e_ms = statistics.mean(et)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+    e2e_ms = dist_max(statistics.mean(et), dev)
+    e2e = {"value": whole_job_rate(flops, e2e_ms, world) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
 
@@ -484,6 +541,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kosmos", choices=["kosmos", "reference"])
     ap.add_argument("--ag-only", action="store_true", help="skip the GEMM+RS and MoE measurements")
+    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8"],
+                    help="with --quick: which fused operator to time")
+    ap.add_argument("--experts", type=int, default=0, help="with --quick --workload moe: expert count (0 = 128)")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed region of the fused kernel (no baselines, e2e or CPU oracle): "
                          "a short launch list for profilers")

@@ -174,6 +174,20 @@ __device__ __forceinline__ void engine_teardown(const Smem &sm, int warp, uint32
     }
 }
 
+// Waits until every stage of the pipeline is free again (all MMAs issued so far
+// have read their operands), so the stage buffers can serve as copy buffers.
+__device__ __forceinline__ bool drain_stages(const Smem &sm, const PipeState &ps, WsHeader *ws) {
+    for (int i = 0; i < NSTAGE; ++i) {
+        uint32_t s = ps.stage + i, ph = ps.phase;
+        if (s >= NSTAGE) { s -= NSTAGE; ph ^= 1u; }
+        if (!mbar_wait(&sm.empty[s], ph ^ 1u, PIPE_LIMIT_NS)) {
+            set_error(ws, KOSMOS_ERR_DEVICE, -11);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- ring (producer side)
 __device__ __forceinline__ bool ring_push(const Smem &sm, RingState &rs, const SchedEntry &e, WsHeader *ws) {
     if (!mbar_wait(&sm.sempty[rs.idx], rs.phase ^ 1u, PIPE_LIMIT_NS)) {

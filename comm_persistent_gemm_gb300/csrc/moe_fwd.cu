@@ -164,6 +164,10 @@ __device__ __forceinline__ int32_t ldcg_i32(const int32_t *p) { return __ldcg(p)
 __device__ __forceinline__ float ldcg_f32(const float *p) { return __ldcg(p); }
 __device__ __forceinline__ uint4 ldcg_u4(const void *p) { return __ldcg(reinterpret_cast<const uint4 *>(p)); }
 
+__device__ __forceinline__ void red_relaxed_add_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t atom_add_acqrel_gpu(uint32_t *p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -252,12 +256,38 @@ __device__ __forceinline__ bool drain_pipeline(const MoeParams &p, const Smem &s
     return true;
 }
 
-// Locates unit u of rank q: its local expert and row block.
-__device__ __forceinline__ void unit_decode(const MoeParams &p, int q, int u, int &le, int &rb) {
-    const int32_t *us = p.unit_start + q * (p.g.Eq + 1);
-    le = 0;
-    while (le + 1 < p.g.Eq && ldcg_i32(&us[le + 1]) <= u) ++le;
-    rb = u - ldcg_i32(&us[le]);
+// Expert tile rail of rank q, grouped by expert with a lag of one expert:
+//   GU(e0) | GU(e1) D(e0) | GU(e2) D(e1) | ... | D(e_last)
+// GU(e): column block outer, row block inner (the row blocks of one weight
+// slice are adjacent, so the slice is read from DRAM once); D(e) likewise.
+// With us[j] = row blocks of the rank's experts before j, group j starts at
+// 12 us[j] + 16 us[j-1] (NGU = 12, ND = 16 for the 4096/1536 shapes).
+__device__ __forceinline__ void moe_decode_tile(const MoeParams &p, int q, int tt, int &kind, int &le, int &rb,
+                                                int &col) {
+    const MoeGeom &g = p.g;
+    const int32_t *us = p.unit_start + q * (g.Eq + 1);
+    kind = 0;
+    const int U = ldcg_i32(&us[g.Eq]);
+    if (tt < 0 || tt >= U * (g.NGU + g.ND)) return;
+    int prev = 0;  // us[j - 1]
+    for (int j = 0; j <= g.Eq; ++j) {
+        const int usj = ldcg_i32(&us[j]);
+        const int nj = (j < g.Eq) ? ldcg_i32(&us[j + 1]) - usj : 0;     // row blocks of expert j
+        const int np = (j >= 1) ? usj - prev : 0;                        // row blocks of expert j-1
+        const int start = g.NGU * usj + g.ND * prev;
+        const int size = g.NGU * nj + g.ND * np;
+        if (tt < start + size) {
+            const int r = tt - start;
+            if (r < g.NGU * nj) {
+                kind = K_TILE_GU; le = j; col = r / nj; rb = r % nj;
+            } else {
+                const int r2 = r - g.NGU * nj;
+                kind = K_TILE_D; le = j - 1; col = r2 / np; rb = r2 % np;
+            }
+            return;
+        }
+        prev = usj;
+    }
 }
 
 // Lane 0 of the producer warp: claims and issues one piece of work.  Returns
@@ -325,30 +355,12 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
             return ACT_DISPATCH;
         }
         if (!wait_plan(p, st, epoch)) return ACT_EXIT;
-        const int U = ldcg_i32(&p.unit_start[q * (g.Eq + 1) + g.Eq]);
-        const int G = g.NGU + g.ND;
         const int tt = static_cast<int>(t) - g.n_head;
-        int kind = 0, u = 0, col = 0;
-        if (U > 0 && tt < U * G) {
-            if (tt < g.NGU) {
-                kind = K_TILE_GU; u = 0; col = tt;
-            } else {
-                const int t2 = tt - g.NGU;
-                const int grp = t2 / G + 1;
-                const int r = t2 % G;
-                if (grp < U) {
-                    if (r < g.NGU) { kind = K_TILE_GU; u = grp; col = r; }
-                    else { kind = K_TILE_D; u = grp - 1; col = r - g.NGU; }
-                } else {
-                    kind = K_TILE_D; u = U - 1; col = r;
-                }
-            }
-        }
+        int kind = 0, le = 0, rb = 0, col = 0;
+        moe_decode_tile(p, q, tt, kind, le, rb, col);
         if (kind == 0) {
             st.main_done = true;
         } else {
-            int le, rb;
-            unit_decode(p, q, u, le, rb);
             const int e = q * g.Eq + le;
             const int row0 = ldcg_i32(&p.offsets[e]) + rb * BM;
             const int left = ldcg_i32(&p.counts[e]) - rb * BM;
@@ -503,9 +515,9 @@ __device__ __noinline__ void moe_dispatch(const MoeParams &p, const Smem &sm, Mo
         }
         bulk_wait<0>();
         fence_proxy_async_global();
-        __threadfence();
+        __threadfence();  // orders the row copies before the relaxed arrival adds below
         if (ok)
-            for (int r = 0; r < nrows; ++r) red_release_add_gpu(&p.disp_cnt[s_ci[r]], 1u);
+            for (int r = 0; r < nrows; ++r) red_relaxed_add_gpu(&p.disp_cnt[s_ci[r]], 1u);
         if (TraceRec *rec = trace_rec(p.trace, blockIdx.x, slot)) rec->t_done = static_cast<int64_t>(globaltimer());
     }
     __syncwarp();
@@ -598,17 +610,23 @@ __device__ __noinline__ void moe_route_epilogue(const MoeParams &p, const SchedE
         pk[s] = (s < K) ? expf(tv[s] - lmax) / z : 0.f;
         if (s < K) ps += pk[s];
     }
-    int32_t *s_idx = reinterpret_cast<int32_t *>(escr);            // [128][K]
+    // Rank of each slot among the block's tokens routed to the same expert:
+    // a 128-bit membership mask per expert (token r sets bit r), then a
+    // popcount of the bits below this token.
+    uint32_t *s_bits = reinterpret_cast<uint32_t *>(escr);         // [E][4]
     int32_t *s_hist = reinterpret_cast<int32_t *>(escr + 4096);    // [E]
-    for (int i = et; i < E; i += NUM_EPI_THREADS) s_hist[i] = 0;
+    for (int i = et; i < E; i += NUM_EPI_THREADS) {
+        s_hist[i] = 0;
+        s_bits[4 * i + 0] = s_bits[4 * i + 1] = s_bits[4 * i + 2] = s_bits[4 * i + 3] = 0u;
+    }
+    named_bar_sync(1, NUM_EPI_THREADS);
 #pragma unroll
     for (int s = 0; s < MOE_MAXK; ++s) {
-        if (s < K) {
-            s_idx[row * K + s] = valid ? ti[s] : -1;
-            if (valid) {
-                p.topk_idx[t * K + s] = ti[s];
-                p.topk_gate[t * K + s] = pk[s] / ps;
-            }
+        if (s < K && valid) {
+            p.topk_idx[t * K + s] = ti[s];
+            p.topk_gate[t * K + s] = pk[s] / ps;
+            atomicOr(&s_bits[4 * ti[s] + (row >> 5)], 1u << (row & 31));
+            atomicAdd(&s_hist[ti[s]], 1);
         }
     }
     named_bar_sync(1, NUM_EPI_THREADS);
@@ -616,12 +634,11 @@ __device__ __noinline__ void moe_route_epilogue(const MoeParams &p, const SchedE
 #pragma unroll
         for (int s = 0; s < MOE_MAXK; ++s) {
             if (s < K) {
-                const int ex = ti[s];
+                const uint32_t *b4 = s_bits + 4 * ti[s];
                 int rk = 0;
-                for (int r2 = 0; r2 < row; ++r2)
-                    for (int s2 = 0; s2 < K; ++s2) rk += (s_idx[r2 * K + s2] == ex) ? 1 : 0;
+                for (int w = 0; w < (row >> 5); ++w) rk += __popc(b4[w]);
+                rk += __popc(b4[row >> 5] & ((1u << (row & 31)) - 1u));
                 p.rank_in_blk[t * K + s] = rk;
-                atomicAdd(&s_hist[ex], 1);
             }
         }
     }
@@ -687,17 +704,18 @@ __device__ __noinline__ void moe_push(const MoeParams &p, const SchedEntry &e, i
     const int my = rbase + lane;                       // the row this lane accounts for
     const int32_t my_sl = (my < rows) ? ldcg_i32(&p.inv_pos[row0 + my]) : -1;
     const int n = (rows - rbase) < 32 ? (rows - rbase) : 32;
-    for (int i0 = 0; i0 < n; i0 += 8) {
-        int32_t sl[8];
-        uint4 v[8];
+    constexpr int RU = 16;
+    for (int i0 = 0; i0 < n; i0 += RU) {
+        int32_t sl[RU];
+        uint4 v[RU];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sl[i] = __shfl_sync(0xFFFFFFFFu, my_sl, (i0 + i) & 31);
+        for (int i = 0; i < RU; ++i) sl[i] = __shfl_sync(0xFFFFFFFFu, my_sl, (i0 + i) & 31);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < RU; ++i)
             if (i0 + i < n)
                 v[i] = ldcg_u4(srcb + static_cast<int64_t>(row0 + rbase + i0 + i) * g.H + dn * BN + lane * 8);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < RU; ++i)
             if (i0 + i < n)
                 *reinterpret_cast<uint4 *>(p.slot + static_cast<int64_t>(sl[i]) * g.H + dn * BN + lane * 8) = v[i];
     }
@@ -726,45 +744,58 @@ __device__ __noinline__ void moe_push(const MoeParams &p, const SchedEntry &e, i
     __syncwarp();
 }
 
+// out[t] = sum_k gate[t][k] * slot[t][k] (fp32 multiply, then add, k in
+// emission order), one rounding to bf16.  Warp w: tokens 32w..32w+31 of the
+// block, two at a time; lane: 8 of the 256 columns.
 __device__ __noinline__ void moe_fold(const MoeParams &p, const SchedEntry &e, int ew, int lane) {
+    constexpr int TU = 2;
     const MoeGeom &g = p.g;
     const int gb = e.a, dn = e.c;
     const int q = gb / g.RB, b = gb % g.RB;
     const int K = g.K;
-    for (int i = 0; i < 32; ++i) {
-        const int r = ew * 32 + i;
-        const int64_t tl = static_cast<int64_t>(b) * BM + r;
-        if (tl >= g.Tq) break;
-        const int64_t t = static_cast<int64_t>(q) * g.Tq + tl;
-        float acc[8];
+    const int64_t left = g.Tq - static_cast<int64_t>(b) * BM;
+    const int ntok = static_cast<int>(left < BM ? left : BM);
+    for (int i0 = 0; i0 < 32; i0 += TU) {
+        uint4 v[TU][MOE_MAXK];
+        float gk[TU][MOE_MAXK];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-        uint4 v[MOE_MAXK];
-        float gk[MOE_MAXK];
+        for (int u = 0; u < TU; ++u) {
+            const int r = ew * 32 + i0 + u;
+            const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(b) * BM + r;
 #pragma unroll
-        for (int k = 0; k < MOE_MAXK; ++k) {
-            if (k < K) {
-                gk[k] = ldcg_f32(&p.topk_gate[t * K + k]);
-                v[k] = ldcg_u4(p.slot + (t * K + k) * g.H + dn * BN + lane * 8);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < MOE_MAXK; ++k) {
-            if (k < K) {
-                const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(gk[k], __uint_as_float(w[j] << 16)));
-                    acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(gk[k], __uint_as_float(w[j] & 0xFFFF0000u)));
+            for (int k = 0; k < MOE_MAXK; ++k) {
+                if (k < K && r < ntok) {
+                    gk[u][k] = ldcg_f32(&p.topk_gate[t * K + k]);
+                    v[u][k] = ldcg_u4(p.slot + (t * K + k) * g.H + dn * BN + lane * 8);
                 }
             }
         }
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        *reinterpret_cast<uint4 *>(p.y[q] + tl * g.H + dn * BN + lane * 8) = o;
+#pragma unroll
+        for (int u = 0; u < TU; ++u) {
+            const int r = ew * 32 + i0 + u;
+            if (r >= ntok) continue;
+            float acc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+            for (int k = 0; k < MOE_MAXK; ++k) {
+                if (k < K) {
+                    const uint32_t w[4] = {v[u][k].x, v[u][k].y, v[u][k].z, v[u][k].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(gk[u][k], __uint_as_float(w[j] << 16)));
+                        acc[2 * j + 1] =
+                            __fadd_rn(acc[2 * j + 1], __fmul_rn(gk[u][k], __uint_as_float(w[j] & 0xFFFF0000u)));
+                    }
+                }
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4 *>(p.y[q] + (static_cast<int64_t>(b) * BM + r) * g.H + dn * BN + lane * 8) = o;
+        }
     }
 }
 
