@@ -34,7 +34,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # src_sha (otherwise the bench reports traffic = null).
 TRAFFIC_CAPTURE = {"bytes": 828650496, "src_sha": "4da220e81c53f296"}
 KERNEL_SOURCES = ["comm_persistent_gemm_gb300/csrc/ag_gemm.cu", "comm_persistent_gemm_gb300/csrc/engine.cuh",
-                  "comm_persistent_gemm_gb300/csrc/ptx.cuh", "comm_persistent_gemm_gb300/csrc/common.cuh"]
+                  "comm_persistent_gemm_gb300/csrc/engine2.cuh", "comm_persistent_gemm_gb300/csrc/ptx.cuh",
+                  "comm_persistent_gemm_gb300/csrc/common.cuh"]
 
 
 def kernel_src_sha() -> str:
@@ -215,15 +216,17 @@ def bench_rs(K, dev, steps, warmup, flush, stream, peak):
     band = timed(K.opts(order=K.ORDER_BAND))
     row = timed(K.opts(order=K.ORDER_ROW))
     fixed = {}
-    for crew in (1, 2, 4, 6):
+    for crew in (1, 2, 3):  # reducer pairs per rank
         fixed[str(crew)] = flops / (timed(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=crew)) * 1e-3) / 1e12
     unf = timed(K.opts(sched=K.SCHED_UNFUSED))
+    single = timed(K.opts(cta_pair=0))
     tf = flops / (band * 1e-3) / 1e12
     best = max(fixed, key=fixed.get)
     return {"workload": "rs_bf16_p8", "ms": band, "tflops": tf, "frac_of_peak": tf / peak,
             "row_order_ms": row, "row_over_band": row / band,
             "fixed_split_best": {"tflops": fixed[best], "crew_per_rank": int(best), "sweep": fixed},
             "unfused": {"tflops": flops / (unf * 1e-3) / 1e12, "launches_per_step": 2},
+            "self_single_sm_tiles_tflops": flops / (single * 1e-3) / 1e12,
             "vs_fixed_split_best": tf / fixed[best], "vs_unfused": tf / (flops / (unf * 1e-3) / 1e12)}
 
 
@@ -472,6 +475,11 @@ def run_kosmos(args):
     K.check(wsb, "ag_gemm unfused")
     base["unfused"] = {"tflops": flops / (statistics.mean(tt) * 1e-3) / 1e12,
                        "launches_per_step": 2}
+    f, wsb = make(K.opts(cta_pair=0))
+    tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
+    K.check(wsb, "ag_gemm single-SM tiles")
+    base["self_single_sm_tiles"] = {"tflops": flops / (statistics.mean(tt) * 1e-3) / 1e12,
+                                    "note": "same schedule, 128x256 tiles on one SM each (tcgen05 cta_group::1)"}
     sweep = {}
     for nc in sorted({max(1, sms // 16), max(1, sms // 8), max(1, sms // 4)}):
         f, wsb = make(K.opts(n_comm0=nc))
@@ -502,7 +510,7 @@ def run_kosmos(args):
     achieved = flops / (step_ms * 1e-3) / 1e12
     traffic = TRAFFIC_CAPTURE["bytes"] if TRAFFIC_CAPTURE["src_sha"] == kernel_src_sha() else None
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": traffic, "peak_source": f"{src} bf16 dense (burst)", "kernel": "ag_gemm_kernel",
+            "traffic": traffic, "peak_source": f"{src} bf16 dense (burst)", "kernel": "ag_gemm_pair_kernel",
             "flop_per_launch": flops}
 
     also = {}

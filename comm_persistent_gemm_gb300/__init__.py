@@ -46,6 +46,7 @@ class KosmosError(RuntimeError):
 class Opts(C.Structure):
     _fields_ = [("sched", C.c_int32), ("n_comm0", C.c_int32), ("fixed_comm_ctas", C.c_int32),
                 ("order", C.c_int32), ("num_ctas", C.c_int32), ("trace", C.c_int32),
+                ("cta_pair", C.c_int32), ("reserved0", C.c_int32),
                 ("wait_limit_ns", C.c_uint64), ("inject", C.c_uint64)]
 
 
@@ -93,9 +94,9 @@ def lib():
     L.kosmos_trace_info.argtypes = [i32, i32, i64, i64, i64, i32, C.POINTER(Opts), vp, C.POINTER(vp),
                                     C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
     L.kosmos_trace_info.restype = i32
-    L.kosmos_rail_decode.argtypes = [i32, i32, i64, i64, i32, i32, i32, vp, i64]
+    L.kosmos_rail_decode.argtypes = [i32, i32, i64, i64, i32, i32, i32, i32, vp, i64]
     L.kosmos_rail_decode.restype = i64
-    L.kosmos_rail_decode_device.argtypes = [i32, i32, i64, i64, i32, i32, i32, vp, i64, vp]
+    L.kosmos_rail_decode_device.argtypes = [i32, i32, i64, i64, i32, i32, i32, i32, vp, i64, vp]
     L.kosmos_rail_decode_device.restype = i64
     L.kosmos_ag_gemm_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, i32, vp, vp, C.POINTER(Opts), vp]
     L.kosmos_ag_gemm_noalloc.restype = i32
@@ -297,25 +298,26 @@ def trace_records(op: int, P: int, m: int, n: int, k: int, ws, o: Opts):
     return recs[recs["kind"] != 0]
 
 
-def rail_decode(op: int, P: int, m: int, n: int, rail: int, order: int = ORDER_BAND, rank: int = 0):
+def rail_decode(op: int, P: int, m: int, n: int, rail: int, order: int = ORDER_BAND, rank: int = 0,
+                tile_m: int = 256):
     """Host-compiled decode of one rail: int32 array [len, 4]."""
     import numpy as np
-    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, None, 0)
+    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, None, 0)
     if ln < 0:
         raise KosmosError(ERR_INVALID_ARG, "kosmos_rail_decode")
     out = np.zeros((ln, 4), dtype=np.int32)
-    lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, out.ctypes.data, ln)
+    lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, out.ctypes.data, ln)
     return out
 
 
 def rail_decode_device(op: int, P: int, m: int, n: int, rail: int, order: int = ORDER_BAND, rank: int = 0,
-                       stream=None):
+                       tile_m: int = 256, stream=None):
     import torch
-    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, None, 0)
+    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, None, 0)
     if ln < 0:
         raise KosmosError(ERR_INVALID_ARG, "kosmos_rail_decode")
     out = torch.zeros((max(ln, 1), 4), dtype=torch.int32, device="cuda")
-    r = lib().kosmos_rail_decode_device(op, P, m, n, order, rank, rail, out.data_ptr(), ln, _stream(stream))
+    r = lib().kosmos_rail_decode_device(op, P, m, n, order, rank, rail, tile_m, out.data_ptr(), ln, _stream(stream))
     if r < 0:
         raise KosmosError(ERR_CUDA, "kosmos_rail_decode_device")
     torch.cuda.synchronize()

@@ -15,7 +15,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "engine.cuh"
+#include "engine2.cuh"
 #include "launch.h"
 
 namespace kosmos {
@@ -251,6 +251,238 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_kernel(const __grid_co
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
 }
 
+// ============================================================== SM-pair variant
+// Same rails and roles; tiles are 256 x 256 and belong to an SM pair (a
+// cluster of two CTAs).  Transfer pieces stay 128 rows: the leader's half of a
+// tile waits for piece 2i, the peer's half for piece 2i + 1.  Movers are whole
+// pairs (both CTAs copy, then both build).
+
+__device__ __noinline__ bool ag_transfer2(const AgParams &p, const Smem2 &sm, int t, uint32_t &cphase,
+                                          uint32_t epoch) {
+    int shard, piece;
+    ag_decode_transfer(p.g, t, shard, piece);
+    const int64_t row_bytes = p.g.k * 2;
+    const int64_t row0 = static_cast<int64_t>(piece) * PIECE_ROWS;
+    const int64_t rows = (p.g.m - row0 < PIECE_ROWS) ? (p.g.m - row0) : PIECE_ROWS;
+    if (!bulk_copy2(sm, p.x_src[shard] + row0 * row_bytes,
+                    p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes, rows * row_bytes, cphase, p.ws,
+                    t))
+        return false;
+    fence_proxy_async_global();
+    __threadfence();
+    const bool drop = (p.inject & KOSMOS_INJECT_DROP_TRANSFER) && static_cast<int64_t>(p.inject >> 32) == t;
+    if (!drop) st_release_gpu(&p.flags[shard * p.g.pieces + piece], epoch + 1u);
+    return true;
+}
+
+// Mover phase of either CTA of a mover pair; returns false on a device error.
+__device__ __forceinline__ bool ag2_mover_phase(const AgParams &p, const Smem2 &sm, uint32_t &cphase, uint32_t epoch,
+                                                int &nrec) {
+    const uint32_t n_mv =
+        static_cast<uint32_t>(p.sched == KOSMOS_SCHED_FIXED ? p.g.n_transfer : p.g.n_transfer - p.g.pieces);
+    while (!failed(p.ws)) {
+        const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
+        if (t >= n_mv) return true;
+        const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+        if (!ag_transfer2(p, sm, static_cast<int>(t), cphase, epoch)) return false;
+        if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+            r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
+            r->kind = K_TRANSFER; r->ticket = static_cast<int32_t>(t); r->cta = blockIdx.x;
+        }
+        ++nrec;
+    }
+    return false;
+}
+
+// After the tile rail: each CTA copies local-shard pieces into the gathered buffer.
+__device__ __forceinline__ void ag2_local_copies(const AgParams &p, const Smem2 &sm, const PipeState2 &ps,
+                                                 uint32_t &cphase, uint32_t epoch, int &nrec) {
+    if (p.sched != KOSMOS_SCHED_SELF) return;
+    if (!drain_stages2(sm, ps, p.ws)) return;
+    while (!failed(p.ws)) {
+        const uint32_t lt = atomicAdd(&p.ws->tickets[2], 1u);
+        if (lt >= static_cast<uint32_t>(p.g.pieces)) break;
+        const int tr = p.g.n_transfer - p.g.pieces + static_cast<int>(lt);
+        const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+        if (!ag_transfer2(p, sm, tr, cphase, epoch)) break;
+        if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+            r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
+            r->kind = K_TRANSFER; r->ticket = tr; r->cta = blockIdx.x;
+        }
+        ++nrec;
+    }
+}
+
+// Loads this CTA's half of one stage: A rows [row0, row0+128) of shard s and
+// B columns [col0, col0+128), completing on the leader's full barrier.
+__device__ __forceinline__ void ag2_load_half(const AgParams &p, const Smem2 &sm, const PipeState2 &ps, bool local,
+                                              int s, int64_t row0, int64_t col0, int kb, uint32_t leader_full) {
+    uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
+    uint8_t *sb = sa + A2_BYTES;
+    if (local)
+        tma_load_2d_pair(sa, &p.tmA_local, leader_full, kb * BK, static_cast<int32_t>(row0));
+    else
+        tma_load_3d_pair(sa, &p.tmA_gath, leader_full, kb * BK, static_cast<int32_t>(row0), s);
+    tma_load_2d_pair(sb, &p.tmB, leader_full, static_cast<int32_t>(col0), kb * BK);
+    tma_load_2d_pair(sb + 64 * BK * 2, &p.tmB, leader_full, static_cast<int32_t>(col0 + 64), kb * BK);
+}
+
+__device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm, uint32_t epoch, uint32_t rank) {
+    const int pair = blockIdx.x / 2;
+    const bool leader = rank == 0;
+    const bool mover = (p.sched != KOSMOS_SCHED_UNFUSED) && pair < p.n_comm;
+    uint32_t cphase = 0;
+    PipeState2 ps;
+    RingPair rs;
+    int nrec = 0;
+    if (mover) {
+        if (!ag2_mover_phase(p, sm, cphase, epoch, nrec) || p.sched == KOSMOS_SCHED_FIXED) {
+            if (leader) {
+                SchedEntry done;
+                fill_done(done);
+                ring2_push(sm, rs, done, p.ws);
+            } else {
+                SchedEntry e;
+                while (ring2_take(sm, rs, false, e, p.ws, false) && e.kind != K_DONE) {
+                }
+            }
+            return;
+        }
+    }
+    if (leader) {
+        const uint32_t my_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
+        while (true) {
+            if (failed(p.ws)) break;
+            const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
+            if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
+            int s, i2, c;
+            ag_decode_tile(p.g, static_cast<int>(t), s, i2, c);
+            const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+            const int pc = 2 * i2;  // the leader's 128-row piece
+            if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
+                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], epoch + 1u, p.wait_limit_ns, t)) break;
+            }
+            int slot = -1;
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+                r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
+                r->kind = K_TILE; r->ticket = static_cast<int32_t>(t); r->cta = blockIdx.x;
+                slot = nrec;
+            }
+            ++nrec;
+            SchedEntry e;
+            fill_done(e);
+            e.kind = K_TILE; e.a = s; e.b = i2; e.c = c; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
+            e.slot = slot;
+            if (!ring2_push(sm, rs, e, p.ws)) break;
+            const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+            bool ok = true;
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * STAGE2_BYTES);
+                ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM, static_cast<int64_t>(c) * BN,
+                              kb, my_full0 + ps.stage * 8);
+                ps.advance();
+            }
+            if (!ok) break;
+        }
+        SchedEntry done;
+        fill_done(done);
+        ring2_push(sm, rs, done, p.ws);
+    } else {
+        const uint32_t leader_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
+        while (true) {
+            SchedEntry e;
+            if (!ring2_take(sm, rs, false, e, p.ws, false)) break;
+            if (e.kind == K_DONE) break;
+            const int s = e.a, i2 = e.b, c = e.c;
+            const int pc = 2 * i2 + 1;  // the peer's 128-row piece
+            if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
+                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], epoch + 1u, p.wait_limit_ns, e.ticket)) break;
+            }
+            const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+            bool ok = true;
+            for (int kb = 0; kb < e.nstage; ++kb) {
+                if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, e.ticket);
+                    ok = false;
+                    break;
+                }
+                ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM + HBM_ROWS,
+                              static_cast<int64_t>(c) * BN + HBN, kb, leader_full0 + ps.stage * 8);
+                ps.advance();
+            }
+            if (!ok) break;
+        }
+    }
+    ag2_local_copies(p, sm, ps, cphase, epoch, nrec);
+}
+
+__device__ __forceinline__ void ag2_epilogue(const AgParams &p, const Smem2 &sm, uint32_t tmem_base, int warp, int lane,
+                                             uint32_t rank) {
+    const bool leader = rank == 0;
+    const int grp = warp & 3;
+    const int row = grp * 32 + lane;
+    RingPair rs;
+    uint32_t acc = 0, acc_phase = 0;
+    while (true) {
+        SchedEntry e;
+        if (!ring2_take(sm, rs, leader, e, p.ws, true)) break;
+        if (e.kind == K_DONE) break;
+        if (e.kind != K_TILE) continue;
+        if (!mbar_wait(&sm.tfull[acc], acc_phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
+            break;
+        }
+        tc_fence_after();
+        const int s = e.a, i2 = e.b, c = e.c;
+        const int64_t rloc = static_cast<int64_t>(i2) * PBM + rank * HBM_ROWS + row;
+        const bool valid = rloc < p.g.m;
+        __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + (valid ? rloc : 0)) * p.g.n;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+            const int64_t col0 = static_cast<int64_t>(c) * BN + ch * 32;
+            if (col0 >= p.g.n) break;
+            const int64_t left = p.g.n - col0;
+            tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
+        }
+        acc_release(sm, acc, leader, lane);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (leader && e.slot >= 0 && lane == 0 && grp == 0) {
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_pair_kernel(const __grid_constant__ AgParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem2 sm = carve_smem2(smem_raw);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_rank();
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&p.tmA_local);
+        prefetch_tmap(&p.tmA_gath);
+        prefetch_tmap(&p.tmB);
+    }
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
+    engine2_setup(sm, warp);
+    const uint32_t tmem_base = *sm.tmem_slot;
+    if (warp == 0) {
+        if (lane == 0) ag2_producer(p, sm, epoch, rank);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) mma2_loop(sm, tmem_base, p.ws);
+    } else {
+        ag2_epilogue(p, sm, tmem_base, warp, lane, rank);
+    }
+    engine2_teardown(sm, warp, tmem_base);
+    if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
+}
+
 // Unfused baseline, first launch: gather every shard into x_gathered with
 // plain 16-byte vector copies over all SMs.
 __global__ void __launch_bounds__(256) ag_gather_copy_kernel(const AgParams p) {
@@ -267,6 +499,8 @@ __global__ void __launch_bounds__(256) ag_gather_copy_kernel(const AgParams p) {
 }
 
 // ---------------------------------------------------------------- host launcher
+int ag_pair_grid_limit() { return max_pair_ctas(reinterpret_cast<const void *>(&ag_gemm_pair_kernel), SMEM2_BYTES); }
+
 kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     AgParams p;
     memset(&p, 0, sizeof(p));
@@ -310,11 +544,18 @@ kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;
 
+    if (L.pair) {
+        p.g = ag_geom(L.P, L.m, L.k, L.n, PBM);
+        p.n_comm = (L.n_comm + 1) / 2;  // mover pairs
+    }
     if (L.sched == KOSMOS_SCHED_UNFUSED) {
         const int sms = L.grid;
         ag_gather_copy_kernel<<<sms * 4, 256, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return KOSMOS_ERR_CUDA;
     }
+    if (L.pair)
+        return launch_persistent_pairs(reinterpret_cast<const void *>(&ag_gemm_pair_kernel), &p, L.grid, SMEM2_BYTES,
+                                       stream);
     return launch_persistent(reinterpret_cast<const void *>(&ag_gemm_kernel), &p, L.grid, SMEM_BYTES, stream);
 }
 

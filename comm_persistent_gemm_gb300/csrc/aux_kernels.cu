@@ -88,13 +88,13 @@ kosmos_status launch_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, i
     return cudaGetLastError() == cudaSuccess ? KOSMOS_OK : KOSMOS_ERR_CUDA;
 }
 
-__global__ void rail_decode_kernel(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int32_t *out,
-                                   int64_t count) {
+__global__ void rail_decode_kernel(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
+                                   int32_t *out, int64_t count) {
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < count;
          t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         int32_t *e = out + 4 * t;
         if (op == KOSMOS_OP_AG_GEMM) {
-            const AgGeom g = ag_geom(P, m, 64, n);
+            const AgGeom g = ag_geom(P, m, 64, n, tile_m);
             if (rail == 0) {
                 int s, j;
                 ag_decode_transfer(g, static_cast<int>(t), s, j);
@@ -105,7 +105,7 @@ __global__ void rail_decode_kernel(int op, int P, int64_t m, int64_t n, int orde
                 e[0] = K_TILE; e[1] = s; e[2] = i; e[3] = c;
             }
         } else {
-            const RsGeom g = rs_geom(P, m, 64, n);
+            const RsGeom g = rs_geom(P, m, 64, n, tile_m);
             if (rail == 0) {
                 int c, b, j;
                 rs_decode_tile(g, order, static_cast<int>(t), c, b, j);
@@ -119,12 +119,13 @@ __global__ void rail_decode_kernel(int op, int P, int64_t m, int64_t n, int orde
     }
 }
 
-kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int32_t *out,
-                                 int64_t count, cudaStream_t stream) {
+kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
+                                 int32_t *out, int64_t count, cudaStream_t stream) {
     int64_t blocks = cdiv(count, 256);
     if (blocks < 1) blocks = 1;
     if (blocks > 4096) blocks = 4096;
-    rail_decode_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(op, P, m, n, order, rank, rail, out, count);
+    rail_decode_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(op, P, m, n, order, rank, rail, tile_m, out,
+                                                                           count);
     return cudaGetLastError() == cudaSuccess ? KOSMOS_OK : KOSMOS_ERR_CUDA;
 }
 

@@ -79,18 +79,22 @@ KOS_HD int64_t align_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 struct AgGeom {
     int P;
     int64_t m, k, n;
-    int pieces;      // tile rows (= transfer pieces) per shard
+    int pieces;      // 128-row transfer pieces per shard
+    int tile_rows;   // 128 (one SM per tile) or 256 (an SM pair per tile)
+    int tiles_m;     // tile rows per shard
     int tiles_n;
     int n_transfer;  // P * pieces: remote shards first, the local shard's copies last
-    int n_tile;      // P * pieces * tiles_n
+    int n_tile;      // P * tiles_m * tiles_n
 };
-KOS_HD AgGeom ag_geom(int P, int64_t m, int64_t k, int64_t n) {
+KOS_HD AgGeom ag_geom(int P, int64_t m, int64_t k, int64_t n, int tile_rows = BM) {
     AgGeom g;
     g.P = P; g.m = m; g.k = k; g.n = n;
     g.pieces = static_cast<int>(cdiv(m, PIECE_ROWS));
+    g.tile_rows = tile_rows;
+    g.tiles_m = static_cast<int>(cdiv(m, tile_rows));
     g.tiles_n = static_cast<int>(cdiv(n, BN));
     g.n_transfer = P * g.pieces;
-    g.n_tile = P * g.pieces * g.tiles_n;
+    g.n_tile = P * g.tiles_m * g.tiles_n;
     return g;
 }
 // Transfer rail: shards 1..P-1 in the order the tiles consume them, then shard 0.
@@ -101,7 +105,7 @@ KOS_HD void ag_decode_transfer(const AgGeom &g, int t, int &shard, int &piece) {
 }
 // Tile rail: shard-major (local shard 0 first), tile rows, then tile columns.
 KOS_HD void ag_decode_tile(const AgGeom &g, int t, int &shard, int &trow, int &tcol) {
-    const int per_shard = g.pieces * g.tiles_n;
+    const int per_shard = g.tiles_m * g.tiles_n;
     shard = t / per_shard;
     const int r = t - shard * per_shard;
     trow = r / g.tiles_n;
@@ -113,16 +117,18 @@ struct RsGeom {
     int P;
     int64_t m, k, n;
     int64_t mc;       // rows per chunk = m / P
+    int band_rows;    // 128 (one SM per tile) or 256 (an SM pair per tile)
     int bands;        // tile rows per chunk
     int tiles_n;
     int n_tile;       // per rank: P * bands * tiles_n
     int n_reduce;     // per rank: bands * tiles_n
 };
-KOS_HD RsGeom rs_geom(int P, int64_t m, int64_t k, int64_t n) {
+KOS_HD RsGeom rs_geom(int P, int64_t m, int64_t k, int64_t n, int band_rows = BM) {
     RsGeom g;
     g.P = P; g.m = m; g.k = k; g.n = n;
     g.mc = m / P;
-    g.bands = static_cast<int>(cdiv(g.mc, BM));
+    g.band_rows = band_rows;
+    g.bands = static_cast<int>(cdiv(g.mc, band_rows));
     g.tiles_n = static_cast<int>(cdiv(n, BN));
     g.n_tile = P * g.bands * g.tiles_n;
     g.n_reduce = g.bands * g.tiles_n;

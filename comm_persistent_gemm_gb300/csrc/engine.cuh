@@ -32,6 +32,11 @@ struct SchedEntry {
     int32_t x0, x1, x2;  // extra fields (op specific)
 };
 
+__device__ __forceinline__ void fill_done(SchedEntry &e) {
+    e.kind = K_DONE; e.a = e.b = e.c = e.d = 0; e.nstage = 0; e.ticket = -1; e.slot = -1;
+    e.nmma = 0; e.x0 = e.x1 = e.x2 = 0;
+}
+
 __host__ __device__ __forceinline__ bool is_mma_kind(int32_t k) {
     return k == K_TILE || k == K_ROUTE || k == K_TILE_GU || k == K_TILE_D;
 }

@@ -18,7 +18,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "engine.cuh"
+#include "engine2.cuh"
 #include "launch.h"
 
 namespace kosmos {
@@ -266,6 +266,313 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_rs_kernel(const __grid_co
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 2 * KOSMOS_MAX_P);
 }
 
+// ============================================================== SM-pair variant
+// Builder pairs compute 256 x 256 partial tiles (bands of 256 rows); each CTA
+// stores its 128 rows and adds one arrival, so an output tile is complete at
+// 2P arrivals.  When the pair's tile rail runs out (one-way switch), or from
+// the start for reducer pairs, each CTA reduces on its own through a local
+// reduce ring with its own stage barriers.
+
+struct RedRing {
+    uint64_t *rfull;    // [NSTAGE2]
+    uint64_t *rempty;   // [NSTAGE2]
+    uint64_t *rsfull;   // [NSCHED]
+    uint64_t *rsempty;  // [NSCHED] 4 epilogue warps
+    SchedEntry *rsched; // [NSCHED]
+};
+
+__device__ __forceinline__ RedRing carve_red(const Smem2 &sm) {
+    RedRing r;
+    uint64_t *b = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sm.tmem_slot) + 16);
+    r.rfull = b; b += NSTAGE2;
+    r.rempty = b; b += NSTAGE2;
+    r.rsfull = b; b += NSCHED;
+    r.rsempty = b; b += NSCHED;
+    r.rsched = reinterpret_cast<SchedEntry *>(b);
+    return r;
+}
+
+__device__ __forceinline__ bool red_push(const RedRing &rr, RingState &rs, const SchedEntry &e, WsHeader *ws) {
+    if (!mbar_wait(&rr.rsempty[rs.idx], rs.phase ^ 1u, PIPE_LIMIT_NS)) {
+        set_error(ws, KOSMOS_ERR_DEVICE, -2);
+        return false;
+    }
+    rr.rsched[rs.idx] = e;
+    mbar_arrive(&rr.rsfull[rs.idx]);
+    rs.advance();
+    return true;
+}
+
+__device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm, const RedRing &rr, uint32_t crank) {
+    const int P = p.g.P;
+    const int pair = blockIdx.x / 2;
+    const int rank = pair % P;
+    const int lp = pair / P;
+    const bool leader = crank == 0;
+    const bool reducer_pair = (p.mode == RS_REDUCE_ONLY) || (p.mode == RS_FUSED && lp < p.n_red);
+    PipeState2 ps;
+    RingPair rs;
+    int nrec = 0;
+    // ---- tile phase (pair)
+    if (leader) {
+        const uint32_t my_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
+        while (!reducer_pair && !failed(p.ws)) {
+            const uint32_t t = atomicAdd(&p.ws->tickets[rank], 1u);
+            if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
+            int chunk, band, tcol;
+            rs_decode_tile(p.g, p.order, static_cast<int>(t), chunk, band, tcol);
+            int slot = -1;
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+                const int64_t now = static_cast<int64_t>(globaltimer());
+                r->t_claim = now; r->t_ready = now; r->t_done = 0;
+                r->kind = K_TILE; r->ticket = static_cast<int32_t>(t); r->cta = blockIdx.x;
+                slot = nrec;
+            }
+            ++nrec;
+            SchedEntry e;
+            fill_done(e);
+            e.kind = K_TILE; e.a = chunk; e.b = band; e.c = tcol; e.d = rank; e.nstage = p.nkb;
+            e.ticket = static_cast<int32_t>(t); e.slot = slot;
+            if (!ring2_push(sm, rs, e, p.ws)) break;
+            bool ok = true;
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * STAGE2_BYTES);
+                uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
+                uint8_t *sb = sa + A2_BYTES;
+                const uint32_t fb = my_full0 + ps.stage * 8;
+                tma_load_3d_pair(sa, &p.tmX[rank], fb, kb * BK, band * PBM, chunk);
+                tma_load_2d_pair(sb, &p.tmW[rank], fb, tcol * BN, kb * BK);
+                tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[rank], fb, tcol * BN + 64, kb * BK);
+                ps.advance();
+            }
+            if (!ok) break;
+        }
+        SchedEntry done;
+        fill_done(done);
+        ring2_push(sm, rs, done, p.ws);
+    } else {
+        const uint32_t leader_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
+        while (true) {
+            SchedEntry e;
+            if (!ring2_take(sm, rs, false, e, p.ws, false)) break;
+            if (e.kind == K_DONE) break;
+            const int chunk = e.a, band = e.b, tcol = e.c;
+            bool ok = true;
+            for (int kb = 0; kb < e.nstage; ++kb) {
+                if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, e.ticket);
+                    ok = false;
+                    break;
+                }
+                uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
+                uint8_t *sb = sa + A2_BYTES;
+                const uint32_t fb = leader_full0 + ps.stage * 8;
+                tma_load_3d_pair(sa, &p.tmX[rank], fb, kb * BK, band * PBM + HBM_ROWS, chunk);
+                tma_load_2d_pair(sb, &p.tmW[rank], fb, tcol * BN + HBN, kb * BK);
+                tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[rank], fb, tcol * BN + HBN + 64, kb * BK);
+                ps.advance();
+            }
+            if (!ok) break;
+        }
+    }
+    // ---- reduce phase (this CTA alone): one-way switch after the tiles, or a reducer pair
+    RingState rrs;
+    const bool reduce = reducer_pair || (p.mode == RS_FUSED && p.sched == KOSMOS_SCHED_SELF);
+    if (reduce && drain_stages2(sm, ps, p.ws)) {
+        PipeState2 rp;
+        const uint32_t red_bytes = static_cast<uint32_t>(BN * RED_ROWS * 2 * P);
+        while (!failed(p.ws)) {
+            const uint32_t t = atomicAdd(&p.ws->tickets[KOSMOS_MAX_P + rank], 1u);
+            if (t >= static_cast<uint32_t>(p.g.n_reduce)) break;
+            int band, tcol;
+            rs_decode_reduce(p.g, static_cast<int>(t), band, tcol);
+            const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+            if (p.mode == RS_FUSED) {
+                uint32_t *ctr = &p.arrive[(static_cast<int64_t>(rank) * p.g.bands + band) * p.g.tiles_n + tcol];
+                if (!wait_flag_eq(p.ws, ctr, static_cast<uint32_t>(2 * P), p.wait_limit_ns,
+                                  (static_cast<int64_t>(1) << 40) | (static_cast<int64_t>(rank) << 32) | t))
+                    break;
+                st_relaxed_gpu(ctr, 0u);
+            }
+            int slot = -1;
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+                r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
+                r->kind = K_REDUCE; r->ticket = static_cast<int32_t>(t); r->cta = blockIdx.x;
+                slot = nrec;
+            }
+            ++nrec;
+            const int64_t left = p.g.mc - static_cast<int64_t>(band) * PBM;
+            const int64_t rows = left < PBM ? left : PBM;
+            const int nsub = static_cast<int>(cdiv(rows, RED_ROWS));
+            SchedEntry e;
+            fill_done(e);
+            e.kind = K_REDUCE; e.a = rank; e.b = band; e.c = tcol; e.d = rank; e.nstage = nsub;
+            e.ticket = static_cast<int32_t>(t); e.slot = slot;
+            if (!red_push(rr, rrs, e, p.ws)) break;
+            bool ok = true;
+            for (int sidx = 0; sidx < nsub; ++sidx) {
+                if (!mbar_wait(&rr.rempty[rp.stage], rp.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&rr.rfull[rp.stage], red_bytes);
+                tma_load_4d(sm.stages + rp.stage * STAGE2_BYTES, &p.tmPart, &rr.rfull[rp.stage], tcol * BN,
+                            band * PBM + sidx * RED_ROWS, rank, 0);
+                rp.advance();
+            }
+            if (!ok) break;
+        }
+    }
+    SchedEntry done;
+    fill_done(done);
+    red_push(rr, rrs, done, p.ws);
+}
+
+__device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm, const RedRing &rr, uint32_t tmem_base,
+                                             int warp, int lane, uint32_t crank) {
+    const bool leader = crank == 0;
+    const int grp = warp & 3;
+    const int row = grp * 32 + lane;
+    const int et = (warp - 2) * 32 + lane;
+    const int P = p.g.P;
+    RingPair rs;
+    uint32_t acc = 0, acc_phase = 0;
+    // ---- pair tiles
+    while (true) {
+        SchedEntry e;
+        if (!ring2_take(sm, rs, leader, e, p.ws, true)) break;
+        if (e.kind == K_DONE) break;
+        if (e.kind != K_TILE) continue;
+        if (!mbar_wait(&sm.tfull[acc], acc_phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
+            break;
+        }
+        tc_fence_after();
+        const int chunk = e.a, band = e.b, tcol = e.c, rank = e.d;
+        const int64_t rloc = static_cast<int64_t>(band) * PBM + crank * HBM_ROWS + row;
+        const bool valid = rloc < p.g.mc;
+        __nv_bfloat16 *dst = p.part + (static_cast<int64_t>(rank) * p.g.m + static_cast<int64_t>(chunk) * p.g.mc +
+                                       (valid ? rloc : 0)) * p.g.n;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+            const int64_t col0 = static_cast<int64_t>(tcol) * BN + ch * 32;
+            if (col0 >= p.g.n) break;
+            const int64_t left = p.g.n - col0;
+            tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + col0, left < 32 ? static_cast<int>(left) : 32);
+        }
+        acc_release(sm, acc, leader, lane);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (p.mode == RS_FUSED) {
+            __threadfence();
+            named_bar_sync(1, NUM_EPI_THREADS);
+            const bool drop = (p.inject & KOSMOS_INJECT_DROP_PARTIAL) && static_cast<int>(p.inject >> 32) == rank;
+            if (et == 0 && !drop)
+                red_release_add_gpu(&p.arrive[(static_cast<int64_t>(chunk) * p.g.bands + band) * p.g.tiles_n + tcol], 1u);
+        }
+        if (leader && e.slot >= 0 && et == 0) {
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+        }
+    }
+    // ---- this CTA's reductions
+    RingState rrs;
+    PipeState2 rp;
+    const int cg = et & 31;
+    while (true) {
+        if (!mbar_wait(&rr.rsfull[rrs.idx], rrs.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -9);
+            break;
+        }
+        const SchedEntry e = rr.rsched[rrs.idx];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rr.rsempty[rrs.idx]);
+        rrs.advance();
+        if (e.kind == K_DONE) break;
+        const int chunk = e.a, band = e.b, tcol = e.c;
+        const int64_t col = static_cast<int64_t>(tcol) * BN + cg * 8;
+        bool ok = true;
+        for (int sidx = 0; sidx < e.nstage; ++sidx) {
+            if (!mbar_wait(&rr.rfull[rp.stage], rp.phase, PIPE_LIMIT_NS)) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
+                ok = false;
+                break;
+            }
+            const uint8_t *buf = sm.stages + rp.stage * STAGE2_BYTES;
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+                const int r8 = (et >> 5) * 2 + r2;
+                float a[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) a[q] = 0.f;
+                for (int rk = 0; rk < P; ++rk) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(buf + ((rk * RED_ROWS + r8) * BN + cg * 8) * 2);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        a[2 * q] += __uint_as_float(w[q] << 16);
+                        a[2 * q + 1] += __uint_as_float(w[q] & 0xFFFF0000u);
+                    }
+                }
+                const int64_t grow = static_cast<int64_t>(band) * PBM + sidx * RED_ROWS + r8;
+                if (grow < p.g.mc && col < p.g.n) {
+                    uint4 o;
+                    o.x = pack_bf16x2(a[0], a[1]);
+                    o.y = pack_bf16x2(a[2], a[3]);
+                    o.z = pack_bf16x2(a[4], a[5]);
+                    o.w = pack_bf16x2(a[6], a[7]);
+                    *reinterpret_cast<uint4 *>(p.y[chunk] + grow * p.g.n + col) = o;
+                }
+            }
+            named_bar_sync(1, NUM_EPI_THREADS);
+            if (et == 0) mbar_arrive(&rr.rempty[rp.stage]);
+            rp.advance();
+        }
+        if (!ok) break;
+        if (e.slot >= 0 && et == 0) {
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_rs_pair_kernel(const __grid_constant__ RsParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem2 sm = carve_smem2(smem_raw);
+    const RedRing rr = carve_red(sm);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t crank = cluster_rank();
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE2; ++i) {
+            mbar_init(&rr.rfull[i], 1);
+            mbar_init(&rr.rempty[i], 1);
+        }
+        for (int i = 0; i < NSCHED; ++i) {
+            mbar_init(&rr.rsfull[i], 1);
+            mbar_init(&rr.rsempty[i], 4);
+        }
+    }
+    engine2_setup(sm, warp);
+    const uint32_t tmem_base = *sm.tmem_slot;
+    if (warp == 0) {
+        if (lane == 0) rs2_producer(p, sm, rr, crank);
+    } else if (warp == 1) {
+        if (lane == 0 && crank == 0) mma2_loop(sm, tmem_base, p.ws);
+    } else {
+        rs2_epilogue(p, sm, rr, tmem_base, warp, lane, crank);
+    }
+    engine2_teardown(sm, warp, tmem_base);
+    if (threadIdx.x == 0) engine_finish(p.ws, epoch, 2 * KOSMOS_MAX_P);
+}
+
+int rs_pair_grid_limit() { return max_pair_ctas(reinterpret_cast<const void *>(&gemm_rs_pair_kernel), SMEM2_BYTES); }
+
 kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
     RsParams p;
     memset(&p, 0, sizeof(p));
@@ -312,16 +619,23 @@ kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
     p.order = L.order;
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;
+    const void *fn = L.pair ? reinterpret_cast<const void *>(&gemm_rs_pair_kernel)
+                            : reinterpret_cast<const void *>(&gemm_rs_kernel);
+    const int smem = L.pair ? SMEM2_BYTES : SMEM_BYTES;
+    if (L.pair) p.g = rs_geom(L.P, L.m, L.k, L.n, PBM);
+    auto go = [&]() {
+        return L.pair ? launch_persistent_pairs(fn, &p, L.grid, smem, stream)
+                      : launch_persistent(fn, &p, L.grid, smem, stream);
+    };
     if (L.sched == KOSMOS_SCHED_UNFUSED) {
         p.mode = RS_TILES_ONLY;
-        const kosmos_status s1 = launch_persistent(reinterpret_cast<const void *>(&gemm_rs_kernel), &p, L.grid,
-                                                   SMEM_BYTES, stream);
+        const kosmos_status s1 = go();
         if (s1 != KOSMOS_OK) return s1;
         p.mode = RS_REDUCE_ONLY;
-        return launch_persistent(reinterpret_cast<const void *>(&gemm_rs_kernel), &p, L.grid, SMEM_BYTES, stream);
+        return go();
     }
     p.mode = RS_FUSED;
-    return launch_persistent(reinterpret_cast<const void *>(&gemm_rs_kernel), &p, L.grid, SMEM_BYTES, stream);
+    return go();
 }
 
 }  // namespace kosmos

@@ -70,6 +70,70 @@ kosmos_status launch_persistent(const void *func, void *params, int grid, int sm
     return KOSMOS_OK;
 }
 
+kosmos_status launch_persistent_pairs(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream) {
+    if ((grid & 1) != 0 || grid < 2) return KOSMOS_ERR_INVALID_ARG;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+        return KOSMOS_ERR_CUDA;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    void *args[1] = {params};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, func, args);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return KOSMOS_ERR_CUDA;
+    }
+    return KOSMOS_OK;
+}
+
+int max_pair_ctas(const void *func, int smem_bytes) {
+    static const void *cached_func[8] = {};
+    static int cached_dev[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    static int cached_val[8] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    for (int i = 0; i < 8; ++i)
+        if (cached_func[i] == func && cached_dev[i] == dev) return cached_val[i];
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess) return -1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, func, &cfg) != cudaSuccess || clusters < 1) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    for (int i = 0; i < 8; ++i)
+        if (cached_func[i] == nullptr) {
+            cached_func[i] = func;
+            cached_dev[i] = dev;
+            cached_val[i] = 2 * clusters;
+            break;
+        }
+    return 2 * clusters;
+}
+
 }  // namespace kosmos
 
 namespace {
@@ -129,6 +193,8 @@ void kosmos_default_opts(kosmos_opts *opts) {
     opts->order = KOSMOS_ORDER_BAND;
     opts->num_ctas = -1;
     opts->trace = 0;
+    opts->cta_pair = -1;
+    opts->reserved0 = 0;
     opts->wait_limit_ns = 0;
     opts->inject = 0;
 }
@@ -180,9 +246,21 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     if (o.sched < KOSMOS_SCHED_SELF || o.sched > KOSMOS_SCHED_UNFUSED) return KOSMOS_ERR_INVALID_ARG;
     if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_AG_GEMM, P, m_per_shard, n, k, dtype, &o))
         return KOSMOS_ERR_WORKSPACE;
-    const int grid = grid_for(o);
+    int grid = grid_for(o);
     if (grid < 1) return KOSMOS_ERR_CUDA;
-    if (o.sched == KOSMOS_SCHED_FIXED && grid < 2) return KOSMOS_ERR_INVALID_ARG;
+    int pair = (dtype == KOSMOS_BF16 && o.cta_pair != 0) ? 1 : 0;
+    if (pair) {
+        const int lim = ag_pair_grid_limit();
+        int g2 = grid & ~1;
+        if (lim >= 2 && g2 > lim) g2 = lim;
+        if (lim < 2 || g2 < 2) {
+            if (o.cta_pair == 1) return KOSMOS_ERR_UNSUPPORTED;
+            pair = 0;
+        } else {
+            grid = g2;
+        }
+    }
+    if (o.sched == KOSMOS_SCHED_FIXED && grid < (pair ? 4 : 2)) return KOSMOS_ERR_INVALID_ARG;
     AgLaunch L;
     memset(&L, 0, sizeof(L));
     L.P = P; L.m = m_per_shard; L.k = k; L.n = n;
@@ -193,6 +271,8 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     L.w = w; L.wsc = w_scales; L.x_gathered = x_gathered; L.y = y; L.ws = ws;
     L.dtype = dtype; L.sched = o.sched;
     L.n_comm = resolve_comm(o, grid, P, o.sched == KOSMOS_SCHED_FIXED);
+    if (pair && L.n_comm > grid - 2) L.n_comm = grid - 2;  // keep a builder pair
+    L.pair = pair;
     L.trace = o.trace; L.grid = grid; L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == KOSMOS_BF16 ? launch_ag_bf16(L, s) : launch_ag_mxfp8(L, s);
@@ -216,8 +296,22 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
     if (o.order != KOSMOS_ORDER_BAND && o.order != KOSMOS_ORDER_ROW) return KOSMOS_ERR_INVALID_ARG;
     if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_GEMM_RS, P, m, n, k_per_rank, dtype, &o))
         return KOSMOS_ERR_WORKSPACE;
-    const int grid = grid_for(o);
+    int grid = grid_for(o);
     if (grid < 1) return KOSMOS_ERR_CUDA;
+    int pair = o.cta_pair != 0 ? 1 : 0;
+    if (pair) {
+        const int lim = rs_pair_grid_limit();
+        int g2 = grid & ~1;
+        if (lim >= 2 && g2 > lim) g2 = lim;
+        // every emulated rank needs a pair; a fixed reducer crew needs a second one
+        const int need = (o.sched == KOSMOS_SCHED_FIXED) ? 4 * P : 2 * P;
+        if (lim < 2 || g2 < need) {
+            if (o.cta_pair == 1) return KOSMOS_ERR_UNSUPPORTED;
+            pair = 0;
+        } else {
+            grid = g2;
+        }
+    }
     if (grid < P) return KOSMOS_ERR_INVALID_ARG;  // every emulated rank needs a CTA
     RsLaunch L;
     memset(&L, 0, sizeof(L));
@@ -229,8 +323,9 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
     }
     L.ws = ws;
     L.sched = o.sched;
+    L.pair = pair;
     {
-        const int per_rank = grid / P;
+        const int per_rank = pair ? (grid / 2) / P : grid / P;  // pairs (or CTAs) per emulated rank
         int n_red = o.n_comm0 >= 0 ? o.n_comm0 : 1;
         if (o.sched == KOSMOS_SCHED_FIXED && o.fixed_comm_ctas >= 0) n_red = o.fixed_comm_ctas;
         if (n_red < 1) n_red = 1;
@@ -343,11 +438,11 @@ kosmos_status kosmos_trace_info(int op, int P, int64_t m, int64_t n, int64_t k, 
     return KOSMOS_OK;
 }
 
-int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int32_t *out,
-                           int64_t max_entries) {
-    if (P < 1 || P > KOSMOS_MAX_P || m < 1 || n < 1) return -1;
+int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
+                           int32_t *out, int64_t max_entries) {
+    if (P < 1 || P > KOSMOS_MAX_P || m < 1 || n < 1 || (tile_m != 128 && tile_m != 256)) return -1;
     if (op == KOSMOS_OP_AG_GEMM) {
-        const AgGeom g = ag_geom(P, m, 64, n);
+        const AgGeom g = ag_geom(P, m, 64, n, tile_m);
         const int64_t len = rail == 0 ? g.n_transfer : g.n_tile;
         if (out) {
             for (int64_t t = 0; t < len && t < max_entries; ++t) {
@@ -367,7 +462,7 @@ int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int r
     }
     if (op == KOSMOS_OP_GEMM_RS) {
         if (m % P || rank < 0 || rank >= P) return -1;
-        const RsGeom g = rs_geom(P, m, 64, n);
+        const RsGeom g = rs_geom(P, m, 64, n, tile_m);
         const int64_t len = rail == 0 ? g.n_tile : g.n_reduce;
         if (out) {
             for (int64_t t = 0; t < len && t < max_entries; ++t) {
@@ -388,12 +483,13 @@ int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int r
     return -1;
 }
 
-int64_t kosmos_rail_decode_device(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int32_t *out,
-                                  int64_t max_entries, void *stream) {
-    const int64_t len = kosmos_rail_decode(op, P, m, n, order, rank, rail, nullptr, 0);
+int64_t kosmos_rail_decode_device(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
+                                  int32_t *out, int64_t max_entries, void *stream) {
+    const int64_t len = kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, nullptr, 0);
     if (len < 0 || out == nullptr) return len;
     const int64_t cnt = len < max_entries ? len : max_entries;
-    if (launch_rail_decode(op, P, m, n, order, rank, rail, out, cnt, static_cast<cudaStream_t>(stream)) != KOSMOS_OK)
+    if (launch_rail_decode(op, P, m, n, order, rank, rail, tile_m, out, cnt, static_cast<cudaStream_t>(stream)) !=
+        KOSMOS_OK)
         return -1;
     return len;
 }

@@ -25,6 +25,7 @@ struct AgLaunch {
     int n_comm;
     int trace;
     int grid;
+    int pair;       // 1: SM-pair (cta_group::2) tiles, grid = 2 x clusters
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -41,6 +42,7 @@ struct RsLaunch {
     int order;
     int trace;
     int grid;
+    int pair;
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -74,6 +76,11 @@ bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, void *base,
 
 // Cooperative launch of a persistent kernel whose only argument is *params.
 kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream);
+// The same with clusters of two CTAs (SM pairs); grid must be even.
+kosmos_status launch_persistent_pairs(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream);
+// Number of CTAs a pair-kernel grid may have on the current device (2 x the
+// co-resident clusters of two at ~200 KB of shared memory), or -1.
+int max_pair_ctas(const void *func, int smem_bytes);
 
 kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream);
 kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream);
@@ -85,7 +92,9 @@ bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t
                     int64_t *bytes);
 kosmos_status launch_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q,
                                     void *scales, cudaStream_t stream);
-kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail,
+kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
                                  int32_t *out, int64_t count, cudaStream_t stream);
+int ag_pair_grid_limit();
+int rs_pair_grid_limit();
 
 }  // namespace kosmos

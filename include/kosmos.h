@@ -102,6 +102,9 @@ typedef struct kosmos_opts {
     int32_t order;            /* KOSMOS_ORDER_* (GEMM+RS) */
     int32_t num_ctas;         /* -1 = one CTA per SM */
     int32_t trace;            /* nonzero: record a per-entry role trace in the workspace */
+    int32_t cta_pair;         /* bf16 AG / RS tiles: 1 = 256x256 per SM pair (tcgen05 cta_group::2),
+                                 0 = 128x256 per SM; -1 = default (pairs) */
+    int32_t reserved0;
     uint64_t wait_limit_ns;   /* bound on every readiness wait; 0 = 2e9 (2 s) */
     uint64_t inject;          /* KOSMOS_INJECT_* bits | (argument << 32); 0 = none */
 } kosmos_opts;
@@ -294,18 +297,19 @@ KOSMOS_API kosmos_status kosmos_trace_info(int op, int P, int64_t m, int64_t n, 
 
 /* Rail decode, for checking ticket order against an independent rail
  * builder.  Writes 4 int32 {kind, a, b, c} per ticket of one rail:
- *   op AG_GEMM: rail 0 = transfers {1, shard, piece, 0}; rail 1 = tiles
- *               {2, shard, tile_row, tile_col}.  args: m = m_per_shard.
+ *   op AG_GEMM: rail 0 = transfers {1, shard, piece, 0} (128-row pieces);
+ *               rail 1 = tiles {2, shard, tile_row, tile_col}.  args: m = m_per_shard.
  *   op GEMM_RS: rail 0 = tiles of rank `rank` {2, chunk, band, tile_col};
  *               rail 1 = reductions of rank `rank` {3, rank, band, tile_col}.
+ * tile_m = tile (band) height in rows: 128 (one SM per tile) or 256 (SM pairs).
  * out is HOST memory of max_entries*4 int32; returns the rail length or -1.
  * Runs the same decode functions the kernels use, compiled for the host. */
 KOSMOS_API int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail,
-                           int32_t *out, int64_t max_entries);
+                           int tile_m, int32_t *out, int64_t max_entries);
 
 /* Same decode executed by a device kernel (out is DEVICE memory). */
 KOSMOS_API int64_t kosmos_rail_decode_device(int op, int P, int64_t m, int64_t n, int order, int rank,
-                                  int rail, int32_t *out, int64_t max_entries, void *stream);
+                                  int rail, int tile_m, int32_t *out, int64_t max_entries, void *stream);
 
 #ifdef __cplusplus
 }

@@ -448,14 +448,15 @@ static int64_t orc_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
  * Transfer rail: remote shards s = 1..P-1 in the order the multiplication
  * consumes them, each cut into pieces j of R rows; then the local shard's own
  * pieces (copied into the gathered buffer; nothing waits on them).
- * Tile rail: output tiles TILE(shard, tile-row, tile-col), row-major over tile
- * rows with the local shard (s = 0) first, then s = 1, 2, ...
+ * Tile rail: output tiles TILE(shard, tile-row, tile-col) of TR rows and BN
+ * columns, row-major over tile rows with the local shard (s = 0) first, then
+ * s = 1, 2, ...
  * Returns the number of entries written (transfer rail then tile rail), or
  * the count only when out == NULL. */
-ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN,
+ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN, int TR,
                                int32_t *transfer_out, int64_t *n_transfer,
                                int32_t *tile_out, int64_t *n_tile) {
-    int64_t pieces = orc_cdiv(m, R), tn = orc_cdiv(n, BN);
+    int64_t pieces = orc_cdiv(m, R), tn = orc_cdiv(n, BN), tm = orc_cdiv(m, TR);
     int64_t nt = 0, nb = 0;
     for (int s = 1; s <= P; s++) {
         int shard = (s == P) ? 0 : s;
@@ -468,7 +469,7 @@ ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN,
         }
     }
     for (int s = 0; s < P; s++)
-        for (int64_t i = 0; i < pieces; i++)
+        for (int64_t i = 0; i < tm; i++)
             for (int64_t c = 0; c < tn; c++) {
                 if (tile_out) {
                     int32_t *e = tile_out + 4 * nb;

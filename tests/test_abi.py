@@ -27,7 +27,7 @@ def test_exports_every_declared_symbol(K):
 def test_default_opts(K):
     o = K.opts()
     assert o.sched == K.SCHED_SELF and o.n_comm0 == -1 and o.order == K.ORDER_BAND
-    assert o.num_ctas == -1 and o.trace == 0 and o.inject == 0
+    assert o.num_ctas == -1 and o.trace == 0 and o.inject == 0 and o.cta_pair == -1
 
 
 def test_workspace_sizes(K):
@@ -67,17 +67,19 @@ def test_host_validation_rejects_bad_args(K):
     assert lib.kosmos_mxfp8_quantize(base, 4, 96, 1, base, base, None) == 1
 
 
+@pytest.mark.parametrize("tile_m", [128, 256])
 @pytest.mark.parametrize("P,m,n", [(2, 64, 128), (8, 1024, 3584), (3, 200, 264), (1, 5, 8)])
-def test_ag_rail_decode_matches_oracle(K, orc, P, m, n):
-    tr, tl = orc.rail_ag(P, m, n, R=128, BN=256)
-    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=0), tr)
-    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=1), tl)
+def test_ag_rail_decode_matches_oracle(K, orc, P, m, n, tile_m):
+    tr, tl = orc.rail_ag(P, m, n, R=128, BN=256, TR=tile_m)
+    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=0, tile_m=tile_m), tr)
+    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=1, tile_m=tile_m), tl)
 
 
+@pytest.mark.parametrize("tile_m", [128, 256])
 @pytest.mark.parametrize("order", [0, 1])
 @pytest.mark.parametrize("P,m,n", [(8, 8192, 8192), (3, 600, 520), (1, 128, 256)])
-def test_rs_rail_decode_matches_oracle(K, orc, P, m, n, order):
+def test_rs_rail_decode_matches_oracle(K, orc, P, m, n, order, tile_m):
     for r in range(P):
-        tl, rd = orc.rail_rs(P, m, n, rank=r, order=order, R=128, BN=256)
-        assert np.array_equal(K.rail_decode(K.OP_GEMM_RS, P, m, n, rail=0, order=order, rank=r), tl)
-        assert np.array_equal(K.rail_decode(K.OP_GEMM_RS, P, m, n, rail=1, order=order, rank=r), rd)
+        tl, rd = orc.rail_rs(P, m, n, rank=r, order=order, R=tile_m, BN=256)
+        assert np.array_equal(K.rail_decode(K.OP_GEMM_RS, P, m, n, rail=0, order=order, rank=r, tile_m=tile_m), tl)
+        assert np.array_equal(K.rail_decode(K.OP_GEMM_RS, P, m, n, rail=1, order=order, rank=r, tile_m=tile_m), rd)

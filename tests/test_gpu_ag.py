@@ -51,34 +51,49 @@ def _check_full(orc, K, inp, o):
 
 
 SCHEDS = {"self": 0, "fixed": 1, "unfused": 2}
+PAIR = {"pair": 1, "single": 0}
 
 
+@pytest.mark.parametrize("mode", list(PAIR))
 @pytest.mark.parametrize("sched", list(SCHEDS))
-def test_ag_tiny_workload(K, orc, sched):
+def test_ag_tiny_workload(K, orc, sched, mode):
     w = WORKLOADS["ag_tiny_p2"]
     inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
-    _check_full(orc, K, inp, K.opts(sched=SCHEDS[sched]))
+    _check_full(orc, K, inp, K.opts(sched=SCHEDS[sched], cta_pair=PAIR[mode]))
 
 
+@pytest.mark.parametrize("mode", list(PAIR))
 @pytest.mark.parametrize("sched", list(SCHEDS))
 @pytest.mark.parametrize("P,m,k,n", [(3, 200, 192, 264), (1, 130, 128, 256), (4, 128, 320, 512),
-                                     (2, 37, 64, 8)])
-def test_ag_ragged_multi_tile(K, orc, sched, P, m, k, n):
+                                     (2, 37, 64, 8), (2, 300, 128, 520)])
+def test_ag_ragged_multi_tile(K, orc, sched, P, m, k, n, mode):
     inp = ag_inputs(P, m, k, n, seed=1000 + P * m + n, var_w=1.0 / k)
-    _check_full(orc, K, inp, K.opts(sched=SCHEDS[sched]))
+    _check_full(orc, K, inp, K.opts(sched=SCHEDS[sched], cta_pair=PAIR[mode]))
 
 
+@pytest.mark.parametrize("mode", list(PAIR))
 @pytest.mark.parametrize("n_comm0", [1, 8, 40])
-def test_ag_mover_counts(K, orc, n_comm0):
+def test_ag_mover_counts(K, orc, n_comm0, mode):
     inp = ag_inputs(8, 256, 256, 512, seed=77, var_w=1.0 / 256)
-    _check_full(orc, K, inp, K.opts(n_comm0=n_comm0))
+    _check_full(orc, K, inp, K.opts(n_comm0=n_comm0, cta_pair=PAIR[mode]))
 
 
 def test_ag_few_ctas(K, orc):
     """A grid much smaller than the tile count: CTAs loop over many entries."""
     inp = ag_inputs(4, 384, 256, 768, seed=5, var_w=1.0 / 256)
-    _check_full(orc, K, inp, K.opts(num_ctas=6, n_comm0=2))
-    _check_full(orc, K, inp, K.opts(num_ctas=3, sched=1, fixed_comm_ctas=1))
+    _check_full(orc, K, inp, K.opts(num_ctas=6, n_comm0=2, cta_pair=0))
+    _check_full(orc, K, inp, K.opts(num_ctas=3, sched=1, fixed_comm_ctas=1, cta_pair=0))
+    _check_full(orc, K, inp, K.opts(num_ctas=6, n_comm0=2, cta_pair=1))
+    _check_full(orc, K, inp, K.opts(num_ctas=4, sched=1, fixed_comm_ctas=2, cta_pair=1))
+
+
+def test_ag_pair_and_single_agree(K, orc):
+    """Both tile engines on the full 8-rank workload: equal within tolerance."""
+    w = WORKLOADS["ag_bf16_p8"]
+    inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
+    _, _, a, _ = _run(K, inp, K.opts(cta_pair=1))
+    _, _, b, _ = _run(K, inp, K.opts(cta_pair=0))
+    assert rel_err(bf16_tensor_to_f64(a[0]), bf16_tensor_to_f64(b[0])) <= TOL
 
 
 @pytest.mark.parametrize("sched", list(SCHEDS))
@@ -100,17 +115,19 @@ def test_ag_full_size_sampled(K, orc, sched):
 
 def test_ag_rail_decode_device_matches_oracle(K, orc):
     for (P, m, n) in [(8, 1024, 3584), (3, 200, 264)]:
-        tr, tl = orc.rail_ag(P, m, n)
-        assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=0), tr)
-        assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=1), tl)
+        for tm in (128, 256):
+            tr, tl = orc.rail_ag(P, m, n, TR=tm)
+            assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=0, tile_m=tm), tr)
+            assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=1, tile_m=tm), tl)
 
 
-def test_ag_trace_every_entry_once(K, orc):
-    inp = ag_inputs(4, 256, 128, 512, seed=3, var_w=1.0 / 128)
-    o = K.opts(trace=1)
+@pytest.mark.parametrize("mode", list(PAIR))
+def test_ag_trace_every_entry_once(K, orc, mode):
+    inp = ag_inputs(4, 512, 128, 512, seed=3, var_w=1.0 / 128)
+    o = K.opts(trace=1, cta_pair=PAIR[mode])
     xs, xg, outs, ws = _run(K, inp, o)
-    recs = K.trace_records(K.OP_AG_GEMM, 4, 256, 512, 128, ws, o)
-    tr, tl = orc.rail_ag(4, 256, 512)
+    recs = K.trace_records(K.OP_AG_GEMM, 4, 512, 512, 128, ws, o)
+    tr, tl = orc.rail_ag(4, 512, 512, TR=256 if PAIR[mode] else 128)
     tiles = np.sort(recs["ticket"][recs["kind"] == 2])
     transfers = np.sort(recs["ticket"][recs["kind"] == 1])
     assert np.array_equal(tiles, np.arange(len(tl)))

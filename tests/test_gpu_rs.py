@@ -41,15 +41,18 @@ def _run(K, inp, o, reps=1):
 
 
 SCHEDS = {"self": 0, "fixed": 1, "unfused": 2}
+PAIR = {"pair": 1, "single": 0}
 
 
+@pytest.mark.parametrize("mode", list(PAIR))
 @pytest.mark.parametrize("order", [0, 1])
 @pytest.mark.parametrize("sched", list(SCHEDS))
 @pytest.mark.parametrize("P,m,k,n", [(3, 600, 128, 264), (1, 130, 64, 256), (8, 1024, 256, 512),
-                                     (2, 16, 64, 8)])
-def test_rs_small_full_compare(K, orc, P, m, k, n, sched, order):
+                                     (2, 16, 64, 8), (4, 2048, 128, 512)])
+def test_rs_small_full_compare(K, orc, P, m, k, n, sched, order, mode):
     inp = rs_inputs(P, m, k, n, seed=2000 + P * m + n, var_w=1.0 / (P * k))
-    outs, _ = _run(K, inp, K.opts(sched=SCHEDS[sched], order=order), reps=2)
+    cp = PAIR[mode] if mode == "single" else -1  # auto: pairs where the grid allows
+    outs, _ = _run(K, inp, K.opts(sched=SCHEDS[sched], order=order, cta_pair=cp), reps=2)
     ref = orc.gemm_rs([bf16_bits(x) for x in inp["x"]], [bf16_bits(w) for w in inp["w"]])
     got = bf16_tensor_to_f64(outs[0])
     assert not np.isnan(got).any()
@@ -60,14 +63,21 @@ def test_rs_small_full_compare(K, orc, P, m, k, n, sched, order):
 def test_rs_reducer_counts_and_few_ctas(K, orc):
     inp = rs_inputs(4, 512, 128, 512, seed=4, var_w=1.0 / 512)
     ref = orc.gemm_rs([bf16_bits(x) for x in inp["x"]], [bf16_bits(w) for w in inp["w"]])
-    base = None
-    for o in [K.opts(n_comm0=1), K.opts(n_comm0=5), K.opts(num_ctas=8), K.opts(num_ctas=4),
-              K.opts(num_ctas=12, sched=1, fixed_comm_ctas=1)]:
-        outs, _ = _run(K, inp, o)
-        assert rel_err(bf16_tensor_to_f64(outs[0]), ref) <= TOL
-        if base is None:
-            base = outs[0]
-        assert torch.equal(outs[0], base), "result depends on the schedule"
+    groups = {
+        # one tile engine per group: results must not depend on the schedule
+        "pair": [K.opts(n_comm0=1, cta_pair=1), K.opts(n_comm0=5, cta_pair=1), K.opts(num_ctas=8, cta_pair=1),
+                 K.opts(num_ctas=16, cta_pair=1), K.opts(num_ctas=32, sched=1, fixed_comm_ctas=1, cta_pair=1)],
+        "single": [K.opts(cta_pair=0), K.opts(num_ctas=8, cta_pair=0), K.opts(num_ctas=4, cta_pair=0),
+                   K.opts(num_ctas=12, sched=1, fixed_comm_ctas=1, cta_pair=0)],
+    }
+    for name, opts in groups.items():
+        base = None
+        for o in opts:
+            outs, _ = _run(K, inp, o)
+            assert rel_err(bf16_tensor_to_f64(outs[0]), ref) <= TOL
+            if base is None:
+                base = outs[0]
+            assert torch.equal(outs[0], base), f"{name}: result depends on the schedule"
 
 
 def test_rs_full_size_sampled_band_and_row(K, orc):
@@ -79,9 +89,11 @@ def test_rs_full_size_sampled_band_and_row(K, orc):
     band, _ = _run(K, inp, K.opts(order=0), reps=2)
     row, _ = _run(K, inp, K.opts(order=1))
     unf, _ = _run(K, inp, K.opts(sched=2))
+    single, _ = _run(K, inp, K.opts(cta_pair=0))
     assert torch.equal(band[0], band[1])
     assert torch.equal(band[0], row[0])
     assert torch.equal(band[0], unf[0])
+    assert rel_err(bf16_tensor_to_f64(single[0]), bf16_tensor_to_f64(band[0])) <= TOL
     mc = w.m // w.P
     rows = np.unique(np.concatenate([sample_indices(w.m, 12, seed=2), np.arange(w.P) * mc,
                                      np.arange(w.P) * mc + mc - 1]))
@@ -92,22 +104,26 @@ def test_rs_full_size_sampled_band_and_row(K, orc):
 
 def test_rs_rail_decode_device_matches_oracle(K, orc):
     for order in (0, 1):
-        for r in range(8):
-            tl, rd = orc.rail_rs(8, 8192, 8192, rank=r, order=order)
-            assert np.array_equal(K.rail_decode_device(K.OP_GEMM_RS, 8, 8192, 8192, rail=0, order=order, rank=r), tl)
-            assert np.array_equal(K.rail_decode_device(K.OP_GEMM_RS, 8, 8192, 8192, rail=1, order=order, rank=r), rd)
+        for tm in (128, 256):
+            for r in range(8):
+                tl, rd = orc.rail_rs(8, 8192, 8192, rank=r, order=order, R=tm)
+                assert np.array_equal(K.rail_decode_device(K.OP_GEMM_RS, 8, 8192, 8192, rail=0, order=order, rank=r,
+                                                           tile_m=tm), tl)
+                assert np.array_equal(K.rail_decode_device(K.OP_GEMM_RS, 8, 8192, 8192, rail=1, order=order, rank=r,
+                                                           tile_m=tm), rd)
 
 
-def test_rs_trace_every_entry_once(K, orc):
-    P, m, k, n = 4, 512, 128, 512
+@pytest.mark.parametrize("mode", list(PAIR))
+def test_rs_trace_every_entry_once(K, orc, mode):
+    P, m, k, n = 4, 2048, 128, 512
     inp = rs_inputs(P, m, k, n, seed=6, var_w=1.0 / 512)
-    o = K.opts(trace=1)
+    o = K.opts(trace=1, cta_pair=PAIR[mode])
     outs, wsb = _run(K, inp, o)
     recs = K.trace_records(K.OP_GEMM_RS, P, m, n, k, wsb, o)
-    tl, rd = orc.rail_rs(P, m, n, rank=0, order=0)
+    tl, rd = orc.rail_rs(P, m, n, rank=0, order=0, R=256 if PAIR[mode] else 128)
     for kind, per_rank in ((2, len(tl)), (3, len(rd))):
         r = recs[recs["kind"] == kind]
-        rank_of = r["cta"] % P
+        rank_of = (r["cta"] // 2) % P if PAIR[mode] else r["cta"] % P
         for q in range(P):
             assert np.array_equal(np.sort(r["ticket"][rank_of == q]), np.arange(per_rank)), (kind, q)
     red = recs[recs["kind"] == 3]
