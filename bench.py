@@ -434,7 +434,7 @@ def run_kosmos(args):
     sms = K.num_sms()
     peaks, src = load_peaks()
     peak = peaks["bf16_tflops"]
-    o_self = K.opts()
+    o_self = K.opts(num_ctas=args.num_ctas if args.num_ctas > 0 else None)
     f_self, ws_self = make(o_self)
     # warm up + correctness gate of the timed configuration
     f_self()
@@ -552,6 +552,8 @@ def main():
     ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8"],
                     help="with --quick: which fused operator to time")
     ap.add_argument("--experts", type=int, default=0, help="with --quick --workload moe: expert count (0 = 128)")
+    ap.add_argument("--num-ctas", type=int, default=0,
+                    help="with --quick: persistent grid size (0 = one CTA per SM); profilers may need fewer")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed region of the fused kernel (no baselines, e2e or CPU oracle): "
                          "a short launch list for profilers")

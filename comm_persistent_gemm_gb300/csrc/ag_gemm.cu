@@ -99,12 +99,8 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
     while (true) {
         if (failed(p.ws)) break;
         if (mover) {
-            // SELF movers take the remote pieces; the local shard's own copies
-            // (nothing waits on them) are left to builders whose tiles ran out.
-            const uint32_t n_mv = static_cast<uint32_t>(p.sched == KOSMOS_SCHED_FIXED ? p.g.n_transfer
-                                                                                    : p.g.n_transfer - p.g.pieces);
             const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
-            if (t < n_mv) {
+            if (t < static_cast<uint32_t>(p.g.n_transfer)) {
                 const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
                 if (!ag_transfer(p, sm, static_cast<int>(t), cphase, epoch)) break;
                 if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
@@ -118,25 +114,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
             mover = false;                             // one-way switch: mover -> builder
         }
         const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
-        if (t >= static_cast<uint32_t>(p.g.n_tile)) {
-            if (p.sched == KOSMOS_SCHED_SELF) {
-                // tile rail exhausted: copy the local shard's pieces into the gathered buffer
-                if (!drain_stages(sm, ps, p.ws)) break;
-                while (!failed(p.ws)) {
-                    const uint32_t lt = atomicAdd(&p.ws->tickets[2], 1u);
-                    if (lt >= static_cast<uint32_t>(p.g.pieces)) break;
-                    const int tr = p.g.n_transfer - p.g.pieces + static_cast<int>(lt);
-                    const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
-                    if (!ag_transfer(p, sm, tr, cphase, epoch)) break;
-                    if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
-                        r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
-                        r->kind = K_TRANSFER; r->ticket = tr; r->cta = cta;
-                    }
-                    ++nrec;
-                }
-            }
-            break;
-        }
+        if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
         int s, i, c;
         ag_decode_tile(p.g, static_cast<int>(t), s, i, c);
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
@@ -278,11 +256,9 @@ __device__ __noinline__ bool ag_transfer2(const AgParams &p, const Smem2 &sm, in
 // Mover phase of either CTA of a mover pair; returns false on a device error.
 __device__ __forceinline__ bool ag2_mover_phase(const AgParams &p, const Smem2 &sm, uint32_t &cphase, uint32_t epoch,
                                                 int &nrec) {
-    const uint32_t n_mv =
-        static_cast<uint32_t>(p.sched == KOSMOS_SCHED_FIXED ? p.g.n_transfer : p.g.n_transfer - p.g.pieces);
     while (!failed(p.ws)) {
         const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
-        if (t >= n_mv) return true;
+        if (t >= static_cast<uint32_t>(p.g.n_transfer)) return true;
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
         if (!ag_transfer2(p, sm, static_cast<int>(t), cphase, epoch)) return false;
         if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
@@ -292,25 +268,6 @@ __device__ __forceinline__ bool ag2_mover_phase(const AgParams &p, const Smem2 &
         ++nrec;
     }
     return false;
-}
-
-// After the tile rail: each CTA copies local-shard pieces into the gathered buffer.
-__device__ __forceinline__ void ag2_local_copies(const AgParams &p, const Smem2 &sm, const PipeState2 &ps,
-                                                 uint32_t &cphase, uint32_t epoch, int &nrec) {
-    if (p.sched != KOSMOS_SCHED_SELF) return;
-    if (!drain_stages2(sm, ps, p.ws)) return;
-    while (!failed(p.ws)) {
-        const uint32_t lt = atomicAdd(&p.ws->tickets[2], 1u);
-        if (lt >= static_cast<uint32_t>(p.g.pieces)) break;
-        const int tr = p.g.n_transfer - p.g.pieces + static_cast<int>(lt);
-        const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
-        if (!ag_transfer2(p, sm, tr, cphase, epoch)) break;
-        if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
-            r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
-            r->kind = K_TRANSFER; r->ticket = tr; r->cta = blockIdx.x;
-        }
-        ++nrec;
-    }
 }
 
 // Loads this CTA's half of one stage: A rows [row0, row0+128) of shard s and
@@ -418,7 +375,6 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             if (!ok) break;
         }
     }
-    ag2_local_copies(p, sm, ps, cphase, epoch, nrec);
 }
 
 __device__ __forceinline__ void ag2_epilogue(const AgParams &p, const Smem2 &sm, uint32_t tmem_base, int warp, int lane,

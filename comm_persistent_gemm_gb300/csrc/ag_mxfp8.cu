@@ -174,12 +174,8 @@ __device__ __forceinline__ void f8_producer(const AgF8Params &p, const F8Smem &f
     while (true) {
         if (failed(p.ws)) break;
         if (mover) {
-            // SELF movers take the remote pieces; the local shard's own copies
-            // (nothing waits on them) are left to builders whose tiles ran out.
-            const uint32_t n_mv = static_cast<uint32_t>(p.sched == KOSMOS_SCHED_FIXED ? p.g.n_transfer
-                                                                                    : p.g.n_transfer - p.g.pieces);
             const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
-            if (t < n_mv) {
+            if (t < static_cast<uint32_t>(p.g.n_transfer)) {
                 const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
                 if (!f8_transfer(p, sm, static_cast<int>(t), cphase, epoch)) break;
                 if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
@@ -193,25 +189,7 @@ __device__ __forceinline__ void f8_producer(const AgF8Params &p, const F8Smem &f
             mover = false;
         }
         const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
-        if (t >= static_cast<uint32_t>(p.g.n_tile)) {
-            if (p.sched == KOSMOS_SCHED_SELF) {
-                // tile rail exhausted: copy the local shard's pieces into the gathered buffer
-                if (!drain_stages(sm, ps, p.ws)) break;
-                while (!failed(p.ws)) {
-                    const uint32_t lt = atomicAdd(&p.ws->tickets[2], 1u);
-                    if (lt >= static_cast<uint32_t>(p.g.pieces)) break;
-                    const int tr = p.g.n_transfer - p.g.pieces + static_cast<int>(lt);
-                    const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
-                    if (!f8_transfer(p, sm, tr, cphase, epoch)) break;
-                    if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
-                        r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
-                        r->kind = K_TRANSFER; r->ticket = tr; r->cta = cta;
-                    }
-                    ++nrec;
-                }
-            }
-            break;
-        }
+        if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
         int s, i, c;
         ag_decode_tile(p.g, static_cast<int>(t), s, i, c);
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
