@@ -32,7 +32,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one ag_gemm_kernel launch on the 8-rank AG
 # workload, from an ncu capture; valid only while the kernel sources hash to
 # src_sha (otherwise the bench reports traffic = null).
-TRAFFIC_CAPTURE = {"bytes": 828650496, "src_sha": "4da220e81c53f296"}
+TRAFFIC_CAPTURE = {"bytes": 815280128, "src_sha": "efc52f44e16c953d"}
 KERNEL_SOURCES = ["comm_persistent_gemm_gb300/csrc/ag_gemm.cu", "comm_persistent_gemm_gb300/csrc/engine.cuh",
                   "comm_persistent_gemm_gb300/csrc/engine2.cuh", "comm_persistent_gemm_gb300/csrc/ptx.cuh",
                   "comm_persistent_gemm_gb300/csrc/common.cuh"]
@@ -230,6 +230,11 @@ def bench_rs(K, dev, steps, warmup, flush, stream, peak):
             "vs_fixed_split_best": tf / fixed[best], "vs_unfused": tf / (flops / (unf * 1e-3) / 1e12)}
 
 
+# Launch options of the --quick configurations (grid size, plain launch for
+# profilers); the full run always uses the defaults.
+QUICK_OPTS = {}
+
+
 def bench_rs_quick(K, dev, steps, warmup, flush, stream):
     """The band-ordered GEMM + reduce-scatter alone (8 ranks, [8192, 3584] x [3584, 8192])."""
     import torch
@@ -241,7 +246,7 @@ def bench_rs_quick(K, dev, steps, warmup, flush, stream):
     ws_ = [x.to(dev) for x in inp["w"]]
     del inp
     ys = [torch.empty(m // P, n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
-    o = K.opts()
+    o = K.opts(**QUICK_OPTS)
     wsb = K.workspace(K.OP_GEMM_RS, P, m, n, k, o=o, device=dev)
     f = lambda: K.gemm_rs(xs, ws_, ys, wsb, o, stream=stream)
     t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
@@ -289,7 +294,8 @@ def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, exper
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     pos = torch.empty(T, Kt, dtype=torch.int32, device=dev)
     wsb = K.moe_workspace(P, T, H, E, Kt, I, device=dev)
-    f = lambda: K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, wsb, Kt, stream=stream)
+    o = K.opts(**QUICK_OPTS)
+    f = lambda: K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, wsb, Kt, o, stream=stream)
     f()
     K.check(wsb, "moe_fwd")
     t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
@@ -339,7 +345,7 @@ def bench_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=True)
         K.check(wsb, "ag_gemm mxfp8")
         return flops / (t * 1e-3) / 1e12, t
 
-    tf, ms = timed(K.opts())
+    tf, ms = timed(K.opts(**(QUICK_OPTS if not baselines else {})))
     if not baselines:
         return {"workload": "ag_mxfp8_p8", "ms": ms, "tflops": tf, "peak": peak, "frac_of_peak": tf / peak}
     fx, _ = timed(K.opts(sched=K.SCHED_FIXED))
@@ -434,7 +440,7 @@ def run_kosmos(args):
     sms = K.num_sms()
     peaks, src = load_peaks()
     peak = peaks["bf16_tflops"]
-    o_self = K.opts(num_ctas=args.num_ctas if args.num_ctas > 0 else None)
+    o_self = K.opts(**QUICK_OPTS) if args.quick else K.opts()
     f_self, ws_self = make(o_self)
     # warm up + correctness gate of the timed configuration
     f_self()
@@ -553,11 +559,16 @@ def main():
                     help="with --quick: which fused operator to time")
     ap.add_argument("--experts", type=int, default=0, help="with --quick --workload moe: expert count (0 = 128)")
     ap.add_argument("--num-ctas", type=int, default=0,
-                    help="with --quick: persistent grid size (0 = one CTA per SM); profilers may need fewer")
+                    help="with --quick: persistent grid size (0 = one CTA per SM)")
+    ap.add_argument("--plain-launch", action="store_true",
+                    help="with --quick: launch without the cooperative attribute (for profilers)")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed region of the fused kernel (no baselines, e2e or CPU oracle): "
                          "a short launch list for profilers")
     args = ap.parse_args()
+    if args.quick:
+        QUICK_OPTS.update({"num_ctas": args.num_ctas if args.num_ctas > 0 else None,
+                           "plain_launch": 1 if args.plain_launch else None})
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -511,8 +511,9 @@ kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     }
     if (L.pair)
         return launch_persistent_pairs(reinterpret_cast<const void *>(&ag_gemm_pair_kernel), &p, L.grid, SMEM2_BYTES,
-                                       stream);
-    return launch_persistent(reinterpret_cast<const void *>(&ag_gemm_kernel), &p, L.grid, SMEM_BYTES, stream);
+                                       stream, L.plain_launch != 0);
+    return launch_persistent(reinterpret_cast<const void *>(&ag_gemm_kernel), &p, L.grid, SMEM_BYTES, stream,
+                             L.plain_launch != 0);
 }
 
 }  // namespace kosmos

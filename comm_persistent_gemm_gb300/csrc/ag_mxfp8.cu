@@ -447,7 +447,8 @@ kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream) {
         ag_f8_gather_copy_kernel<<<L.grid * 4, 256, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return KOSMOS_ERR_CUDA;
     }
-    return launch_persistent(reinterpret_cast<const void *>(&ag_mxfp8_kernel), &p, L.grid, F_SMEM_BYTES, stream);
+    return launch_persistent(reinterpret_cast<const void *>(&ag_mxfp8_kernel), &p, L.grid, F_SMEM_BYTES, stream,
+                             L.plain_launch != 0);
 }
 
 }  // namespace kosmos

@@ -624,8 +624,8 @@ kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
     const int smem = L.pair ? SMEM2_BYTES : SMEM_BYTES;
     if (L.pair) p.g = rs_geom(L.P, L.m, L.k, L.n, PBM);
     auto go = [&]() {
-        return L.pair ? launch_persistent_pairs(fn, &p, L.grid, smem, stream)
-                      : launch_persistent(fn, &p, L.grid, smem, stream);
+        return L.pair ? launch_persistent_pairs(fn, &p, L.grid, smem, stream, L.plain_launch != 0)
+                      : launch_persistent(fn, &p, L.grid, smem, stream, L.plain_launch != 0);
     };
     if (L.sched == KOSMOS_SCHED_UNFUSED) {
         p.mode = RS_TILES_ONLY;

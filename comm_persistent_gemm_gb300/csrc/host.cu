@@ -47,7 +47,8 @@ bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, void *base,
     return r == CUDA_SUCCESS;
 }
 
-kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream) {
+kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream,
+                                bool plain) {
     if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
         return KOSMOS_ERR_CUDA;
     cudaLaunchConfig_t cfg;
@@ -60,7 +61,7 @@ kosmos_status launch_persistent(const void *func, void *params, int grid, int sm
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = plain ? 0 : 1;
     void *args[1] = {params};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, func, args);
     if (e != cudaSuccess) {
@@ -70,7 +71,8 @@ kosmos_status launch_persistent(const void *func, void *params, int grid, int sm
     return KOSMOS_OK;
 }
 
-kosmos_status launch_persistent_pairs(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream) {
+kosmos_status launch_persistent_pairs(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream,
+                                      bool plain) {
     if ((grid & 1) != 0 || grid < 2) return KOSMOS_ERR_INVALID_ARG;
     if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
         return KOSMOS_ERR_CUDA;
@@ -88,7 +90,7 @@ kosmos_status launch_persistent_pairs(const void *func, void *params, int grid, 
     attr[1].id = cudaLaunchAttributeCooperative;
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = plain ? 1 : 2;
     void *args[1] = {params};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, func, args);
     if (e != cudaSuccess) {
@@ -194,7 +196,7 @@ void kosmos_default_opts(kosmos_opts *opts) {
     opts->num_ctas = -1;
     opts->trace = 0;
     opts->cta_pair = -1;
-    opts->reserved0 = 0;
+    opts->plain_launch = 0;
     opts->wait_limit_ns = 0;
     opts->inject = 0;
 }
@@ -274,6 +276,7 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     if (pair && L.n_comm > grid - 2) L.n_comm = grid - 2;  // keep a builder pair
     L.pair = pair;
     L.trace = o.trace; L.grid = grid; L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
+    L.plain_launch = o.plain_launch;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == KOSMOS_BF16 ? launch_ag_bf16(L, s) : launch_ag_mxfp8(L, s);
 }
@@ -333,7 +336,7 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
         if (n_red < 1 && o.sched == KOSMOS_SCHED_FIXED) return KOSMOS_ERR_INVALID_ARG;
         L.n_comm = n_red;
     }
-    L.order = o.order; L.trace = o.trace; L.grid = grid;
+    L.order = o.order; L.trace = o.trace; L.grid = grid; L.plain_launch = o.plain_launch;
     L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
     return launch_rs_bf16(L, static_cast<cudaStream_t>(stream));
 }
@@ -399,7 +402,7 @@ kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, 
     }
     L.wr = w_router;
     L.topk_idx = topk_idx; L.topk_gate = topk_gate; L.counts = expert_counts; L.pos = dispatch_pos;
-    L.ws = ws; L.sched = o.sched; L.n_comm = 0; L.trace = o.trace; L.grid = grid;
+    L.ws = ws; L.sched = o.sched; L.n_comm = 0; L.trace = o.trace; L.grid = grid; L.plain_launch = o.plain_launch;
     L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
     return launch_moe_fwd(L, static_cast<cudaStream_t>(stream));
 }

@@ -26,6 +26,7 @@ struct AgLaunch {
     int trace;
     int grid;
     int pair;       // 1: SM-pair (cta_group::2) tiles, grid = 2 x clusters
+    int plain_launch;
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -43,6 +44,7 @@ struct RsLaunch {
     int trace;
     int grid;
     int pair;
+    int plain_launch;
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -66,6 +68,7 @@ struct MoeLaunch {
     int n_comm;
     int trace;
     int grid;
+    int plain_launch;
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -74,10 +77,13 @@ struct MoeLaunch {
 bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, void *base, const uint64_t *dims,
                  const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
 
-// Cooperative launch of a persistent kernel whose only argument is *params.
-kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream);
+// Cooperative launch of a persistent kernel whose only argument is *params
+// (plain = true: the same grid without the cooperative attribute).
+kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream,
+                                bool plain = false);
 // The same with clusters of two CTAs (SM pairs); grid must be even.
-kosmos_status launch_persistent_pairs(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream);
+kosmos_status launch_persistent_pairs(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream,
+                                      bool plain = false);
 // Number of CTAs a pair-kernel grid may have on the current device (2 x the
 // co-resident clusters of two at ~200 KB of shared memory), or -1.
 int max_pair_ctas(const void *func, int smem_bytes);

@@ -1049,7 +1049,8 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
         if (!encode_tmap(&p.tmH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.h, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return KOSMOS_ERR_CUDA;
     }
-    return launch_persistent(reinterpret_cast<const void *>(&moe_fwd_kernel), &p, Lc.grid, MOE_SMEM_BYTES, stream);
+    return launch_persistent(reinterpret_cast<const void *>(&moe_fwd_kernel), &p, Lc.grid, MOE_SMEM_BYTES, stream,
+                             Lc.plain_launch != 0);
 }
 
 }  // namespace kosmos

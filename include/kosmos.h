@@ -104,7 +104,12 @@ typedef struct kosmos_opts {
     int32_t trace;            /* nonzero: record a per-entry role trace in the workspace */
     int32_t cta_pair;         /* bf16 AG / RS tiles: 1 = 256x256 per SM pair (tcgen05 cta_group::2),
                                  0 = 128x256 per SM; -1 = default (pairs) */
-    int32_t reserved0;
+    int32_t plain_launch;     /* 0 = cooperative launch (the driver guarantees every CTA is resident);
+                                 1 = the same grid as a plain launch, for profilers that cannot replay
+                                 cooperative cluster launches.  The grid never exceeds the occupancy
+                                 limit, so on an otherwise idle GPU every CTA is resident; if one is
+                                 not, the others' bounded waits run out and the call reports
+                                 KOSMOS_ERR_TIMEOUT. */
     uint64_t wait_limit_ns;   /* bound on every readiness wait; 0 = 2e9 (2 s) */
     uint64_t inject;          /* KOSMOS_INJECT_* bits | (argument << 32); 0 = none */
 } kosmos_opts;
