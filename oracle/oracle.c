@@ -437,7 +437,7 @@ ORC_EXPORT int orc_moe_experts(int64_t T, int64_t H, int E, int K, int64_t I, in
 /* ------------------------------------------------------------------------ */
 /* [explainer, "Role switching only works"]: data is produced in the order its
  * consumers claim it.  Entries are written as 4 int32 fields
- * {kind, a, b, c}; kinds: 1 TRANSFER(shard, piece), 2 TILE, 3 REDUCE.
+ * {kind, a, b, c}; kinds: 1 TRANSFER(shard, piece, part), 2 TILE, 3 REDUCE.
  * Tile and piece heights are R rows; output tiles are BN columns wide. */
 
 enum { ORC_TRANSFER = 1, ORC_TILE = 2, ORC_REDUCE = 3 };
@@ -447,26 +447,34 @@ static int64_t orc_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 /* All-gather rails.
  * Transfer rail: remote shards s = 1..P-1 in the order the multiplication
  * consumes them, each cut into pieces j of R rows; then the local shard's own
- * pieces (copied into the gathered buffer; nothing waits on them).
+ * pieces (copied into the gathered buffer; nothing waits on them).  Each
+ * piece is split into R / PR parts q of PR rows, in row order, so that
+ * several movers can fill the piece the next tile waits for [the pages do
+ * not fix the transfer granularity; a piece counts as arrived once all of
+ * its parts have arrived].  Parts past the shard's last row are still
+ * entries (empty ones).
  * Tile rail: output tiles TILE(shard, tile-row, tile-col) of TR rows and BN
  * columns, row-major over tile rows with the local shard (s = 0) first, then
  * s = 1, 2, ...
  * Returns the number of entries written (transfer rail then tile rail), or
  * the count only when out == NULL. */
-ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN, int TR,
+ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN, int TR, int PR,
                                int32_t *transfer_out, int64_t *n_transfer,
                                int32_t *tile_out, int64_t *n_tile) {
+    if (PR < 1 || R % PR != 0) return -1;
     int64_t pieces = orc_cdiv(m, R), tn = orc_cdiv(n, BN), tm = orc_cdiv(m, TR);
+    int parts = R / PR;
     int64_t nt = 0, nb = 0;
     for (int s = 1; s <= P; s++) {
         int shard = (s == P) ? 0 : s;
-        for (int64_t j = 0; j < pieces; j++) {
-            if (transfer_out) {
-                int32_t *e = transfer_out + 4 * nt;
-                e[0] = ORC_TRANSFER; e[1] = shard; e[2] = (int32_t)j; e[3] = 0;
+        for (int64_t j = 0; j < pieces; j++)
+            for (int q = 0; q < parts; q++) {
+                if (transfer_out) {
+                    int32_t *e = transfer_out + 4 * nt;
+                    e[0] = ORC_TRANSFER; e[1] = shard; e[2] = (int32_t)j; e[3] = q;
+                }
+                nt++;
             }
-            nt++;
-        }
     }
     for (int s = 0; s < P; s++)
         for (int64_t i = 0; i < tm; i++)

@@ -9,14 +9,22 @@ import numpy as np
 import pytest
 
 
+@pytest.mark.parametrize("PR", [32, 128])
 @pytest.mark.parametrize("P,m,n", [(2, 64, 128), (8, 1024, 3584), (3, 320, 200)])
-def test_ag_rail_exactly_once_and_demand_order(orc, P, m, n):
+def test_ag_rail_exactly_once_and_demand_order(orc, P, m, n, PR):
     R, BN = 128, 256
-    tr, tl = orc.rail_ag(P, m, n, R=R, BN=BN)
+    tr_all, tl = orc.rail_ag(P, m, n, R=R, BN=BN, PR=PR)
     pieces = -(-m // R)
+    parts = R // PR
     tn = -(-n // BN)
-    assert len(tr) == P * pieces
-    assert len({tuple(e) for e in tr}) == len(tr)
+    assert len(tr_all) == P * pieces * parts
+    assert len({tuple(e) for e in tr_all}) == len(tr_all)
+    assert set(tr_all[:, 3].tolist()) == set(range(parts))
+    # the parts of one piece are adjacent and in row order; dropping the part
+    # field leaves the piece rail
+    assert np.array_equal(tr_all[:, 3], np.tile(np.arange(parts), P * pieces))
+    tr = tr_all[::parts]
+    assert np.array_equal(np.repeat(tr[:, 1:3], parts, axis=0), tr_all[:, 1:3])
     assert len(tl) == P * pieces * tn
     assert len({tuple(e) for e in tl}) == len(tl)
     assert np.all(tr[:, 0] == 1) and np.all(tl[:, 0] == 2)
@@ -63,3 +71,8 @@ def test_rs_rails(orc, order):
 def test_rs_rail_rejects_indivisible(orc):
     with pytest.raises(ValueError):
         orc.rail_rs(3, 100, 256, rank=0, order=0)
+
+
+def test_ag_rail_rejects_uneven_parts(orc):
+    with pytest.raises(ValueError):
+        orc.rail_ag(2, 64, 128, R=128, PR=48)
