@@ -70,7 +70,7 @@ def lib():
         L.orc_moe_experts.argtypes = [i64, i64, C.c_int, C.c_int, i64, C.c_int, P, P, P,
                                       P, P, P, C.c_int, P, i64, P]
         L.orc_rail_ag.restype = i64
-        L.orc_rail_ag.argtypes = [C.c_int, i64, i64, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P, P]
+        L.orc_rail_ag.argtypes = [C.c_int, i64, i64, C.c_int, C.c_int, C.c_int, C.c_int, i64, P, P, P, P]
         L.orc_rail_rs.restype = i64
         L.orc_rail_rs.argtypes = [C.c_int, i64, i64, C.c_int, C.c_int, C.c_int, C.c_int,
                                   P, P, P, P]
@@ -271,17 +271,18 @@ def moe_experts(x_bits: np.ndarray, idx: np.ndarray, gate: np.ndarray,
 
 # -- rails ------------------------------------------------------------------
 
-def rail_ag(P: int, m: int, n: int, R: int = 128, BN: int = 256, TR: Optional[int] = None, PR: int = 32):
+def rail_ag(P: int, m: int, n: int, R: int = 128, BN: int = 256, TR: Optional[int] = None, PR: int = 32,
+            XS: int = 0):
     """Transfer rail (pieces of R rows in parts of PR rows) and tile rail
-    (tiles of TR rows, BN columns)."""
+    (tiles of TR rows, BN columns; the last XS tiles as column halves)."""
     TR = R if TR is None else TR
     nt = C.c_int64()
     nb = C.c_int64()
-    if lib().orc_rail_ag(P, m, n, R, BN, TR, PR, None, C.byref(nt), None, C.byref(nb)) < 0:
-        raise ValueError("R must be a multiple of PR")
+    if lib().orc_rail_ag(P, m, n, R, BN, TR, PR, XS, None, C.byref(nt), None, C.byref(nb)) < 0:
+        raise ValueError("inconsistent rail arguments")
     tr = np.zeros((nt.value, 4), dtype=np.int32)
     tl = np.zeros((nb.value, 4), dtype=np.int32)
-    lib().orc_rail_ag(P, m, n, R, BN, TR, PR, _ptr(tr), C.byref(nt), _ptr(tl), C.byref(nb))
+    lib().orc_rail_ag(P, m, n, R, BN, TR, PR, XS, _ptr(tr), C.byref(nt), _ptr(tl), C.byref(nb))
     return tr, tl
 
 

@@ -437,10 +437,11 @@ ORC_EXPORT int orc_moe_experts(int64_t T, int64_t H, int E, int K, int64_t I, in
 /* ------------------------------------------------------------------------ */
 /* [explainer, "Role switching only works"]: data is produced in the order its
  * consumers claim it.  Entries are written as 4 int32 fields
- * {kind, a, b, c}; kinds: 1 TRANSFER(shard, piece, part), 2 TILE, 3 REDUCE.
+ * {kind, a, b, c}; kinds: 1 TRANSFER(shard, piece, part), 2 TILE, 3 REDUCE,
+ * 10 TILE_HALF (a tile's column half).
  * Tile and piece heights are R rows; output tiles are BN columns wide. */
 
-enum { ORC_TRANSFER = 1, ORC_TILE = 2, ORC_REDUCE = 3 };
+enum { ORC_TRANSFER = 1, ORC_TILE = 2, ORC_REDUCE = 3, ORC_TILE_HALF = 10 };
 
 static int64_t orc_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -455,15 +456,22 @@ static int64_t orc_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
  * entries (empty ones).
  * Tile rail: output tiles TILE(shard, tile-row, tile-col) of TR rows and BN
  * columns, row-major over tile rows with the local shard (s = 0) first, then
- * s = 1, 2, ...
+ * s = 1, 2, ...  The last XS tiles of that order are each replaced by their
+ * two column halves, TILE_HALF(shard, tile-row, half-col) covering columns
+ * [half-col * BN/2, (half-col + 1) * BN/2), left half first [the pages give
+ * no tile shapes; halving the final wave's tiles shortens the tail, where
+ * CTAs that drew one tile more than others would otherwise finish a whole
+ * tile later].
  * Returns the number of entries written (transfer rail then tile rail), or
- * the count only when out == NULL. */
-ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN, int TR, int PR,
+ * the count only when out == NULL; -1 for inconsistent arguments. */
+ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN, int TR, int PR, int64_t XS,
                                int32_t *transfer_out, int64_t *n_transfer,
                                int32_t *tile_out, int64_t *n_tile) {
-    if (PR < 1 || R % PR != 0) return -1;
+    if (PR < 1 || R % PR != 0 || XS < 0 || BN % 2 != 0) return -1;
     int64_t pieces = orc_cdiv(m, R), tn = orc_cdiv(n, BN), tm = orc_cdiv(m, TR);
     int parts = R / PR;
+    int64_t n_full = (int64_t)P * tm * tn;
+    if (XS > n_full) XS = n_full;
     int64_t nt = 0, nb = 0;
     for (int s = 1; s <= P; s++) {
         int shard = (s == P) ? 0 : s;
@@ -476,14 +484,25 @@ ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN, int T
                 nt++;
             }
     }
+    int64_t f = 0; /* position of the tile in the unsplit order */
     for (int s = 0; s < P; s++)
         for (int64_t i = 0; i < tm; i++)
-            for (int64_t c = 0; c < tn; c++) {
-                if (tile_out) {
-                    int32_t *e = tile_out + 4 * nb;
-                    e[0] = ORC_TILE; e[1] = s; e[2] = (int32_t)i; e[3] = (int32_t)c;
+            for (int64_t c = 0; c < tn; c++, f++) {
+                if (f < n_full - XS) {
+                    if (tile_out) {
+                        int32_t *e = tile_out + 4 * nb;
+                        e[0] = ORC_TILE; e[1] = s; e[2] = (int32_t)i; e[3] = (int32_t)c;
+                    }
+                    nb++;
+                } else {
+                    for (int h = 0; h < 2; h++) {
+                        if (tile_out) {
+                            int32_t *e = tile_out + 4 * nb;
+                            e[0] = ORC_TILE_HALF; e[1] = s; e[2] = (int32_t)i; e[3] = (int32_t)(2 * c + h);
+                        }
+                        nb++;
+                    }
                 }
-                nb++;
             }
     if (n_transfer) *n_transfer = nt;
     if (n_tile) *n_tile = nb;
