@@ -27,12 +27,12 @@ INJECT_DROP_PARTIAL = 0x2
 INJECT_IDENTITY_EXPERTS = 0x4
 MOE_VIEW_LOGITS, MOE_VIEW_RECV, MOE_VIEW_H, MOE_VIEW_Y, MOE_VIEW_SLOT, MOE_VIEW_OFFSETS, MOE_VIEW_TRACE = range(7)
 KIND_NAMES = {1: "TRANSFER", 2: "TILE", 3: "REDUCE", 4: "ROUTE", 5: "DISPATCH", 6: "TILE_GU", 7: "TILE_D",
-              8: "PUSH", 9: "FOLD"}
+              8: "PUSH", 9: "FOLD", 10: "TILE_HALF"}
 
 EXPORTS = ["kosmos_default_opts", "kosmos_num_sms", "kosmos_workspace_bytes", "kosmos_workspace_init",
            "kosmos_ag_gemm", "kosmos_gemm_rs", "kosmos_moe_fwd", "kosmos_mxfp8_quantize", "kosmos_status_sync",
            "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device", "kosmos_ag_gemm_noalloc",
-           "kosmos_moe_workspace_bytes", "kosmos_moe_debug_view"]
+           "kosmos_moe_workspace_bytes", "kosmos_moe_debug_view", "kosmos_ag_tile_plan"]
 
 
 class KosmosError(RuntimeError):
@@ -47,7 +47,7 @@ class Opts(C.Structure):
     _fields_ = [("sched", C.c_int32), ("n_comm0", C.c_int32), ("fixed_comm_ctas", C.c_int32),
                 ("order", C.c_int32), ("num_ctas", C.c_int32), ("trace", C.c_int32),
                 ("cta_pair", C.c_int32), ("plain_launch", C.c_int32),
-                ("wait_limit_ns", C.c_uint64), ("inject", C.c_uint64)]
+                ("wait_limit_ns", C.c_uint64), ("inject", C.c_uint64), ("tail_split", C.c_int64)]
 
 
 class TraceRec(C.Structure):
@@ -94,9 +94,9 @@ def lib():
     L.kosmos_trace_info.argtypes = [i32, i32, i64, i64, i64, i32, C.POINTER(Opts), vp, C.POINTER(vp),
                                     C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
     L.kosmos_trace_info.restype = i32
-    L.kosmos_rail_decode.argtypes = [i32, i32, i64, i64, i32, i32, i32, i32, vp, i64]
+    L.kosmos_rail_decode.argtypes = [i32, i32, i64, i64, i32, i32, i32, i32, i64, vp, i64]
     L.kosmos_rail_decode.restype = i64
-    L.kosmos_rail_decode_device.argtypes = [i32, i32, i64, i64, i32, i32, i32, i32, vp, i64, vp]
+    L.kosmos_rail_decode_device.argtypes = [i32, i32, i64, i64, i32, i32, i32, i32, i64, vp, i64, vp]
     L.kosmos_rail_decode_device.restype = i64
     L.kosmos_ag_gemm_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, i32, vp, vp, C.POINTER(Opts), vp]
     L.kosmos_ag_gemm_noalloc.restype = i32
@@ -104,6 +104,8 @@ def lib():
     L.kosmos_moe_workspace_bytes.restype = C.c_size_t
     L.kosmos_moe_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, vp, C.POINTER(vp), C.POINTER(i64)]
     L.kosmos_moe_debug_view.restype = i32
+    L.kosmos_ag_tile_plan.argtypes = [i32, i64, i64, i32, C.POINTER(Opts), C.POINTER(i64), C.POINTER(C.c_int32)]
+    L.kosmos_ag_tile_plan.restype = i32
     _lib = L
     return L
 
@@ -298,26 +300,38 @@ def trace_records(op: int, P: int, m: int, n: int, k: int, ws, o: Opts):
     return recs[recs["kind"] != 0]
 
 
+def ag_tile_plan(P: int, m_per_shard: int, n: int, o: Optional[Opts] = None, dtype: int = BF16):
+    """(tail_split, tile_m) that ag_gemm uses for these sizes and options on
+    the current device: the arguments of its tile rail's decode."""
+    sp = C.c_int64()
+    tm = C.c_int32()
+    if lib().kosmos_ag_tile_plan(P, m_per_shard, n, dtype, C.byref(o) if o is not None else None, C.byref(sp),
+                                 C.byref(tm)) != 0:
+        raise KosmosError(ERR_INVALID_ARG, "kosmos_ag_tile_plan")
+    return sp.value, tm.value
+
+
 def rail_decode(op: int, P: int, m: int, n: int, rail: int, order: int = ORDER_BAND, rank: int = 0,
-                tile_m: int = 256):
+                tile_m: int = 256, split: int = 0):
     """Host-compiled decode of one rail: int32 array [len, 4]."""
     import numpy as np
-    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, None, 0)
+    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, split, None, 0)
     if ln < 0:
         raise KosmosError(ERR_INVALID_ARG, "kosmos_rail_decode")
     out = np.zeros((ln, 4), dtype=np.int32)
-    lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, out.ctypes.data, ln)
+    lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, split, out.ctypes.data, ln)
     return out
 
 
 def rail_decode_device(op: int, P: int, m: int, n: int, rail: int, order: int = ORDER_BAND, rank: int = 0,
-                       tile_m: int = 256, stream=None):
+                       tile_m: int = 256, split: int = 0, stream=None):
     import torch
-    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, None, 0)
+    ln = lib().kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, split, None, 0)
     if ln < 0:
         raise KosmosError(ERR_INVALID_ARG, "kosmos_rail_decode")
     out = torch.zeros((max(ln, 1), 4), dtype=torch.int32, device="cuda")
-    r = lib().kosmos_rail_decode_device(op, P, m, n, order, rank, rail, tile_m, out.data_ptr(), ln, _stream(stream))
+    r = lib().kosmos_rail_decode_device(op, P, m, n, order, rank, rail, tile_m, split, out.data_ptr(), ln,
+                                        _stream(stream))
     if r < 0:
         raise KosmosError(ERR_CUDA, "kosmos_rail_decode_device")
     torch.cuda.synchronize()

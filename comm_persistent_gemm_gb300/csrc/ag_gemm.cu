@@ -39,54 +39,43 @@ struct AgParams {
     uint64_t inject;
 };
 
-// Mover: copy one piece (<= 128 rows of one shard, contiguous in both the
-// shard and the gathered buffer) through the four stage buffers with bulk
-// async copies, then release the piece's flag with value epoch + 1.
-__device__ __noinline__ bool ag_transfer(const AgParams &p, const Smem &sm, int t, uint32_t &cphase,
-                                         uint32_t epoch) {
-    int shard, piece;
-    ag_decode_transfer(p.g, t, shard, piece);
+// Mover side of the all-gather: claims transfer entries (one part of one
+// piece: <= 32 rows of one shard, contiguous in both the shard and the
+// gathered buffer) and streams them through the stage buffers; each landed
+// part adds one arrival to its piece's flag.
+__device__ __forceinline__ bool ag_claim_transfer(const AgParams &p, MoveEntry &e) {
+    if (failed(p.ws)) return false;
+    const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
+    if (t >= static_cast<uint32_t>(p.g.n_transfer)) return false;
+    int shard, piece, part;
+    ag_decode_transfer(p.g, static_cast<int>(t), shard, piece, part);
+    int64_t row0, rows;
+    ag_part_rows(p.g, piece, part, row0, rows);
     const int64_t row_bytes = p.g.k * 2;
-    const int64_t row0 = static_cast<int64_t>(piece) * PIECE_ROWS;
-    const int64_t rows = (p.g.m - row0 < PIECE_ROWS) ? (p.g.m - row0) : PIECE_ROWS;
-    const int64_t bytes = rows * row_bytes;
-    const uint8_t *src = p.x_src[shard] + row0 * row_bytes;
-    uint8_t *dst = p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes;
-    constexpr int64_t CH = STAGE_BYTES;
-    const int64_t nch = cdiv(bytes, CH);
-    auto chunk_bytes = [&](int64_t c) -> uint32_t {
-        const int64_t rem = bytes - c * CH;
-        return static_cast<uint32_t>(rem < CH ? rem : CH);
-    };
-    for (int64_t c = 0; c < nch && c < NSTAGE; ++c) {
-        mbar_arrive_expect_tx(&sm.cbar[c], chunk_bytes(c));
-        bulk_g2s(sm.stages + c * CH, src + c * CH, chunk_bytes(c), &sm.cbar[c]);
-    }
-    for (int64_t c = 0; c < nch; ++c) {
-        const int b = static_cast<int>(c % NSTAGE);
-        if (!mbar_wait(&sm.cbar[b], (cphase >> b) & 1u, PIPE_LIMIT_NS)) {
-            bulk_wait<0>();
-            set_error(p.ws, KOSMOS_ERR_DEVICE, t);
-            return false;
-        }
-        cphase ^= (1u << b);
-        bulk_s2g(dst + c * CH, sm.stages + b * CH, chunk_bytes(c));
-        bulk_commit();
-        // refill the buffer of the previous chunk once its store has read it
-        const int64_t refill = c - 1 + NSTAGE;
-        if (c >= 1 && refill < nch) {
-            bulk_wait_read<1>();
-            const int rb = static_cast<int>((c - 1) % NSTAGE);
-            mbar_arrive_expect_tx(&sm.cbar[rb], chunk_bytes(refill));
-            bulk_g2s(sm.stages + rb * CH, src + refill * CH, chunk_bytes(refill), &sm.cbar[rb]);
-        }
-    }
-    bulk_wait<0>();
-    fence_proxy_async_global();
-    __threadfence();
+    e.src[0] = p.x_src[shard] + row0 * row_bytes;
+    e.dst[0] = p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes;
+    e.bytes[0] = rows * row_bytes;
+    e.src[1] = nullptr; e.dst[1] = nullptr; e.bytes[1] = 0;
     const bool drop = (p.inject & KOSMOS_INJECT_DROP_TRANSFER) && static_cast<int64_t>(p.inject >> 32) == t;
-    if (!drop) st_release_gpu(&p.flags[shard * p.g.pieces + piece], epoch + 1u);
+    e.flag = drop ? nullptr : &p.flags[shard * p.g.pieces + piece];
+    e.ticket = static_cast<int32_t>(t);
+    e.t_claim = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
     return true;
+}
+
+// Runs this CTA's mover role until the transfer rail is exhausted; false after a device error.
+template <int NS, int CH>
+__device__ __forceinline__ bool ag_mover_phase(const AgParams &p, uint8_t *stages, uint64_t *cbar, uint32_t &cphase,
+                                               int &nrec) {
+    auto claim = [&](MoveEntry &e) { return ag_claim_transfer(p, e); };
+    auto done = [&](int32_t ticket, int64_t t_claim) {
+        if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+            r->t_claim = t_claim; r->t_ready = t_claim; r->t_done = static_cast<int64_t>(globaltimer());
+            r->kind = K_TRANSFER; r->ticket = ticket; r->cta = blockIdx.x;
+        }
+        ++nrec;
+    };
+    return stream_mover<NS, CH, 2>(stages, cbar, cphase, p.ws, claim, done) && !failed(p.ws);
 }
 
 __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, uint32_t epoch) {
@@ -99,27 +88,19 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
     while (true) {
         if (failed(p.ws)) break;
         if (mover) {
-            const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
-            if (t < static_cast<uint32_t>(p.g.n_transfer)) {
-                const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
-                if (!ag_transfer(p, sm, static_cast<int>(t), cphase, epoch)) break;
-                if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
-                    r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
-                    r->kind = K_TRANSFER; r->ticket = static_cast<int32_t>(t); r->cta = cta;
-                }
-                ++nrec;
-                continue;
-            }
+            if (!ag_mover_phase<NSTAGE, STAGE_BYTES>(p, sm.stages, sm.cbar, cphase, nrec)) break;
             if (p.sched == KOSMOS_SCHED_FIXED) break;  // a fixed crew never builds
             mover = false;                             // one-way switch: mover -> builder
         }
         const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
         if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
         int s, i, c;
-        ag_decode_tile(p.g, static_cast<int>(t), s, i, c);
+        const int width = ag_decode_tile(p.g, static_cast<int>(t), s, i, c) == K_TILE ? BN : BN / 2;
+        const int col0 = c * width;
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
         if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0) {
-            if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], epoch + 1u, p.wait_limit_ns, t)) break;
+            if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], ag_piece_ready(p.g, epoch), p.wait_limit_ns, t))
+                break;
         }
         int slot = -1;
         if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
@@ -129,10 +110,12 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
         }
         ++nrec;
         SchedEntry e;
-        e.kind = K_TILE; e.a = s; e.b = i; e.c = c; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
-        e.slot = slot; e.d = 0; e.nmma = 0; e.x0 = e.x1 = e.x2 = 0;
+        e.kind = K_TILE; e.a = s; e.b = i; e.c = col0; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
+        e.slot = slot; e.d = 0; e.nmma = width; e.x0 = e.x1 = e.x2 = 0;
         if (!ring_push(sm, rs, e, p.ws)) break;
         const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+        const int nslab = width / 64;
+        const uint32_t stage_tx = A_STAGE_BYTES + nslab * (64 * BK * 2);
         bool ok = true;
         for (int kb = 0; kb < p.nkb; ++kb) {
             if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
@@ -143,14 +126,13 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
             uint8_t *sa = sm.stages + ps.stage * STAGE_BYTES;
             uint8_t *sb = sa + A_STAGE_BYTES;
             uint64_t *bar = &sm.full[ps.stage];
-            mbar_arrive_expect_tx(bar, STAGE_BYTES);
+            mbar_arrive_expect_tx(bar, stage_tx);
             if (local)
                 tma_load_2d(sa, &p.tmA_local, bar, kb * BK, i * BM);
             else
                 tma_load_3d(sa, &p.tmA_gath, bar, kb * BK, i * BM, s);
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(sb + j * (64 * BK * 2), &p.tmB, bar, c * BN + j * 64, kb * BK);
+            for (int j = 0; j < nslab; ++j)
+                tma_load_2d(sb + j * (64 * BK * 2), &p.tmB, bar, col0 + j * 64, kb * BK);
             ps.advance();
         }
         if (!ok) break;
@@ -183,14 +165,15 @@ __device__ __forceinline__ void ag_epilogue(const AgParams &p, const Smem &sm, u
             break;
         }
         tc_fence_after();
-        const int s = e.a, i = e.b, c = e.c;
+        const int s = e.a, i = e.b;
+        const int width = e.nmma > 0 ? e.nmma : BN;
         const int64_t rloc = static_cast<int64_t>(i) * BM + row;
         const bool valid = rloc < p.g.m;
         __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + (valid ? rloc : 0)) * p.g.n;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-            const int64_t col0 = static_cast<int64_t>(c) * BN + ch * 32;
+        for (int ch = 0; ch < width / 32; ++ch) {
+            const int64_t col0 = static_cast<int64_t>(e.c) + ch * 32;
             if (col0 >= p.g.n) break;
             const int64_t left = p.g.n - col0;
             tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
@@ -235,45 +218,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_kernel(const __grid_co
 // tile waits for piece 2i, the peer's half for piece 2i + 1.  Movers are whole
 // pairs (both CTAs copy, then both build).
 
-__device__ __noinline__ bool ag_transfer2(const AgParams &p, const Smem2 &sm, int t, uint32_t &cphase,
-                                          uint32_t epoch) {
-    int shard, piece;
-    ag_decode_transfer(p.g, t, shard, piece);
-    const int64_t row_bytes = p.g.k * 2;
-    const int64_t row0 = static_cast<int64_t>(piece) * PIECE_ROWS;
-    const int64_t rows = (p.g.m - row0 < PIECE_ROWS) ? (p.g.m - row0) : PIECE_ROWS;
-    if (!bulk_copy2(sm, p.x_src[shard] + row0 * row_bytes,
-                    p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes, rows * row_bytes, cphase, p.ws,
-                    t))
-        return false;
-    fence_proxy_async_global();
-    __threadfence();
-    const bool drop = (p.inject & KOSMOS_INJECT_DROP_TRANSFER) && static_cast<int64_t>(p.inject >> 32) == t;
-    if (!drop) st_release_gpu(&p.flags[shard * p.g.pieces + piece], epoch + 1u);
-    return true;
-}
-
-// Mover phase of either CTA of a mover pair; returns false on a device error.
-__device__ __forceinline__ bool ag2_mover_phase(const AgParams &p, const Smem2 &sm, uint32_t &cphase, uint32_t epoch,
-                                                int &nrec) {
-    while (!failed(p.ws)) {
-        const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
-        if (t >= static_cast<uint32_t>(p.g.n_transfer)) return true;
-        const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
-        if (!ag_transfer2(p, sm, static_cast<int>(t), cphase, epoch)) return false;
-        if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
-            r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
-            r->kind = K_TRANSFER; r->ticket = static_cast<int32_t>(t); r->cta = blockIdx.x;
-        }
-        ++nrec;
-    }
-    return false;
-}
-
 // Loads this CTA's half of one stage: A rows [row0, row0+128) of shard s and
-// B columns [col0, col0+128), completing on the leader's full barrier.
+// nslab 64-column slabs of B from column col0 (two for a 256-wide tile, one
+// for a column half), completing on the leader's full barrier.
 __device__ __forceinline__ void ag2_load_half(const AgParams &p, const Smem2 &sm, const PipeState2 &ps, bool local,
-                                              int s, int64_t row0, int64_t col0, int kb, uint32_t leader_full) {
+                                              int s, int64_t row0, int64_t col0, int nslab, int kb,
+                                              uint32_t leader_full) {
     uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
     uint8_t *sb = sa + A2_BYTES;
     if (local)
@@ -281,7 +231,7 @@ __device__ __forceinline__ void ag2_load_half(const AgParams &p, const Smem2 &sm
     else
         tma_load_3d_pair(sa, &p.tmA_gath, leader_full, kb * BK, static_cast<int32_t>(row0), s);
     tma_load_2d_pair(sb, &p.tmB, leader_full, static_cast<int32_t>(col0), kb * BK);
-    tma_load_2d_pair(sb + 64 * BK * 2, &p.tmB, leader_full, static_cast<int32_t>(col0 + 64), kb * BK);
+    if (nslab > 1) tma_load_2d_pair(sb + 64 * BK * 2, &p.tmB, leader_full, static_cast<int32_t>(col0 + 64), kb * BK);
 }
 
 __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm, uint32_t epoch, uint32_t rank) {
@@ -293,7 +243,8 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
     RingPair rs;
     int nrec = 0;
     if (mover) {
-        if (!ag2_mover_phase(p, sm, cphase, epoch, nrec) || p.sched == KOSMOS_SCHED_FIXED) {
+        if (!ag_mover_phase<NSTAGE2, STAGE2_BYTES>(p, sm.stages, sm.cbar, cphase, nrec) ||
+            p.sched == KOSMOS_SCHED_FIXED) {
             if (leader) {
                 SchedEntry done;
                 fill_done(done);
@@ -313,11 +264,14 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
             if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
             int s, i2, c;
-            ag_decode_tile(p.g, static_cast<int>(t), s, i2, c);
+            const int width = ag_decode_tile(p.g, static_cast<int>(t), s, i2, c) == K_TILE ? BN : BN / 2;
+            const int col0 = c * width;
             const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
             const int pc = 2 * i2;  // the leader's 128-row piece
             if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
-                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], epoch + 1u, p.wait_limit_ns, t)) break;
+                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch), p.wait_limit_ns,
+                                  t))
+                    break;
             }
             int slot = -1;
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
@@ -328,9 +282,10 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             ++nrec;
             SchedEntry e;
             fill_done(e);
-            e.kind = K_TILE; e.a = s; e.b = i2; e.c = c; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
-            e.slot = slot;
+            e.kind = K_TILE; e.a = s; e.b = i2; e.c = col0; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
+            e.slot = slot; e.nmma = width;
             if (!ring2_push(sm, rs, e, p.ws)) break;
+            const int nslab = width / 128;  // B slabs per CTA: each CTA holds half of the tile's columns
             const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
             bool ok = true;
             for (int kb = 0; kb < p.nkb; ++kb) {
@@ -339,9 +294,9 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * STAGE2_BYTES);
-                ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM, static_cast<int64_t>(c) * BN,
-                              kb, my_full0 + ps.stage * 8);
+                mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * (A2_BYTES + nslab * (64 * BK * 2)));
+                ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM, col0, nslab, kb,
+                              my_full0 + ps.stage * 8);
                 ps.advance();
             }
             if (!ok) break;
@@ -355,10 +310,13 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             SchedEntry e;
             if (!ring2_take(sm, rs, false, e, p.ws, false)) break;
             if (e.kind == K_DONE) break;
-            const int s = e.a, i2 = e.b, c = e.c;
+            const int s = e.a, i2 = e.b;
+            const int width = e.nmma > 0 ? e.nmma : BN;
             const int pc = 2 * i2 + 1;  // the peer's 128-row piece
             if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
-                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], epoch + 1u, p.wait_limit_ns, e.ticket)) break;
+                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch), p.wait_limit_ns,
+                                  e.ticket))
+                    break;
             }
             const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
             bool ok = true;
@@ -369,7 +327,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
                     break;
                 }
                 ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM + HBM_ROWS,
-                              static_cast<int64_t>(c) * BN + HBN, kb, leader_full0 + ps.stage * 8);
+                              static_cast<int64_t>(e.c) + width / 2, width / 128, kb, leader_full0 + ps.stage * 8);
                 ps.advance();
             }
             if (!ok) break;
@@ -394,14 +352,15 @@ __device__ __forceinline__ void ag2_epilogue(const AgParams &p, const Smem2 &sm,
             break;
         }
         tc_fence_after();
-        const int s = e.a, i2 = e.b, c = e.c;
+        const int s = e.a, i2 = e.b;
+        const int width = e.nmma > 0 ? e.nmma : BN;
         const int64_t rloc = static_cast<int64_t>(i2) * PBM + rank * HBM_ROWS + row;
         const bool valid = rloc < p.g.m;
         __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + (valid ? rloc : 0)) * p.g.n;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-            const int64_t col0 = static_cast<int64_t>(c) * BN + ch * 32;
+        for (int ch = 0; ch < width / 32; ++ch) {
+            const int64_t col0 = static_cast<int64_t>(e.c) + ch * 32;
             if (col0 >= p.g.n) break;
             const int64_t left = p.g.n - col0;
             tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
@@ -460,7 +419,7 @@ int ag_pair_grid_limit() { return max_pair_ctas(reinterpret_cast<const void *>(&
 kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     AgParams p;
     memset(&p, 0, sizeof(p));
-    p.g = ag_geom(L.P, L.m, L.k, L.n);
+    p.g = ag_geom(L.P, L.m, L.k, L.n, L.pair ? PBM : BM, L.n_split);
     // tensor maps
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(L.k), static_cast<uint64_t>(L.m)};
@@ -500,10 +459,7 @@ kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;
 
-    if (L.pair) {
-        p.g = ag_geom(L.P, L.m, L.k, L.n, PBM);
-        p.n_comm = (L.n_comm + 1) / 2;  // mover pairs
-    }
+    if (L.pair) p.n_comm = (L.n_comm + 1) / 2;  // mover pairs
     if (L.sched == KOSMOS_SCHED_UNFUSED) {
         const int sms = L.grid;
         ag_gather_copy_kernel<<<sms * 4, 256, 0, stream>>>(p);

@@ -104,61 +104,29 @@ __device__ __forceinline__ F8Smem carve_f8(uint8_t *raw) {
     return s;
 }
 
-// Copies n bytes with bulk async copies through the stage buffers (the caller
-// owns them), tracking the copy barriers' phases in cphase.
-__device__ __forceinline__ bool bulk_copy_staged(const Smem &sm, const uint8_t *src, uint8_t *dst, int64_t bytes,
-                                                 uint32_t &cphase, WsHeader *ws, int64_t entry) {
-    constexpr int64_t CH = STAGE_BYTES;
-    const int64_t nch = cdiv(bytes, CH);
-    auto cb = [&](int64_t c) -> uint32_t {
-        const int64_t rem = bytes - c * CH;
-        return static_cast<uint32_t>(rem < CH ? rem : CH);
-    };
-    for (int64_t c = 0; c < nch && c < NSTAGE; ++c) {
-        mbar_arrive_expect_tx(&sm.cbar[c], cb(c));
-        bulk_g2s(sm.stages + c * CH, src + c * CH, cb(c), &sm.cbar[c]);
-    }
-    for (int64_t c = 0; c < nch; ++c) {
-        const int b = static_cast<int>(c % NSTAGE);
-        if (!mbar_wait(&sm.cbar[b], (cphase >> b) & 1u, PIPE_LIMIT_NS)) {
-            bulk_wait<0>();
-            set_error(ws, KOSMOS_ERR_DEVICE, entry);
-            return false;
-        }
-        cphase ^= (1u << b);
-        bulk_s2g(dst + c * CH, sm.stages + b * CH, cb(c));
-        bulk_commit();
-        const int64_t refill = c - 1 + NSTAGE;
-        if (c >= 1 && refill < nch) {
-            bulk_wait_read<1>();
-            const int rb = static_cast<int>((c - 1) % NSTAGE);
-            mbar_arrive_expect_tx(&sm.cbar[rb], cb(refill));
-            bulk_g2s(sm.stages + rb * CH, src + refill * CH, cb(refill), &sm.cbar[rb]);
-        }
-    }
-    bulk_wait<0>();
-    return true;
-}
-
-__device__ __noinline__ bool f8_transfer(const AgF8Params &p, const Smem &sm, int t, uint32_t &cphase,
-                                         uint32_t epoch) {
-    int shard, piece;
-    ag_decode_transfer(p.g, t, shard, piece);
+// Transfer entry of the MXFP8 all-gather: one part (<= 32 rows of E4M3
+// bytes) of one piece; part 0 also carries the piece's scale block (the
+// E8M0 scales are tiled per 128 rows).
+__device__ __forceinline__ bool f8_claim_transfer(const AgF8Params &p, MoveEntry &e) {
+    if (failed(p.ws)) return false;
+    const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
+    if (t >= static_cast<uint32_t>(p.g.n_transfer)) return false;
+    int shard, piece, part;
+    ag_decode_transfer(p.g, static_cast<int>(t), shard, piece, part);
+    int64_t row0, rows;
+    ag_part_rows(p.g, piece, part, row0, rows);
     const int64_t row_bytes = p.g.k;
-    const int64_t row0 = static_cast<int64_t>(piece) * PIECE_ROWS;
-    const int64_t rows = (p.g.m - row0 < PIECE_ROWS) ? (p.g.m - row0) : PIECE_ROWS;
-    if (!bulk_copy_staged(sm, p.x_src[shard] + row0 * row_bytes,
-                          p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes, rows * row_bytes, cphase,
-                          p.ws, t))
-        return false;
+    e.src[0] = p.x_src[shard] + row0 * row_bytes;
+    e.dst[0] = p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes;
+    e.bytes[0] = rows * row_bytes;
     const int64_t sblk = static_cast<int64_t>(p.nkb) * 512;  // scale bytes of one 128-row block
-    if (!bulk_copy_staged(sm, p.sx_src[shard] + piece * sblk,
-                          p.sx_gath + (static_cast<int64_t>(shard) * p.g.pieces + piece) * sblk, sblk, cphase, p.ws, t))
-        return false;
-    fence_proxy_async_global();
-    __threadfence();
+    e.src[1] = p.sx_src[shard] + piece * sblk;
+    e.dst[1] = p.sx_gath + (static_cast<int64_t>(shard) * p.g.pieces + piece) * sblk;
+    e.bytes[1] = part == 0 ? sblk : 0;
     const bool drop = (p.inject & KOSMOS_INJECT_DROP_TRANSFER) && static_cast<int64_t>(p.inject >> 32) == t;
-    if (!drop) st_release_gpu(&p.flags[shard * p.g.pieces + piece], epoch + 1u);
+    e.flag = drop ? nullptr : &p.flags[shard * p.g.pieces + piece];
+    e.ticket = static_cast<int32_t>(t);
+    e.t_claim = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
     return true;
 }
 
@@ -174,17 +142,16 @@ __device__ __forceinline__ void f8_producer(const AgF8Params &p, const F8Smem &f
     while (true) {
         if (failed(p.ws)) break;
         if (mover) {
-            const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
-            if (t < static_cast<uint32_t>(p.g.n_transfer)) {
-                const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
-                if (!f8_transfer(p, sm, static_cast<int>(t), cphase, epoch)) break;
+            auto claim = [&](MoveEntry &e) { return f8_claim_transfer(p, e); };
+            auto done = [&](int32_t ticket, int64_t t_claim) {
                 if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
-                    r->t_claim = tc; r->t_ready = tc; r->t_done = static_cast<int64_t>(globaltimer());
-                    r->kind = K_TRANSFER; r->ticket = static_cast<int32_t>(t); r->cta = cta;
+                    r->t_claim = t_claim; r->t_ready = t_claim; r->t_done = static_cast<int64_t>(globaltimer());
+                    r->kind = K_TRANSFER; r->ticket = ticket; r->cta = cta;
                 }
                 ++nrec;
-                continue;
-            }
+            };
+            if (!stream_mover<NSTAGE, STAGE_BYTES, 2>(sm.stages, sm.cbar, cphase, p.ws, claim, done) || failed(p.ws))
+                break;
             if (p.sched == KOSMOS_SCHED_FIXED) break;
             mover = false;
         }
@@ -194,7 +161,8 @@ __device__ __forceinline__ void f8_producer(const AgF8Params &p, const F8Smem &f
         ag_decode_tile(p.g, static_cast<int>(t), s, i, c);
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
         if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0) {
-            if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], epoch + 1u, p.wait_limit_ns, t)) break;
+            if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], ag_piece_ready(p.g, epoch), p.wait_limit_ns, t))
+                break;
         }
         int slot = -1;
         if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {

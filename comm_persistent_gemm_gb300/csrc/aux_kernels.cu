@@ -89,20 +89,20 @@ kosmos_status launch_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, i
 }
 
 __global__ void rail_decode_kernel(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
-                                   int32_t *out, int64_t count) {
+                                   int64_t split, int32_t *out, int64_t count) {
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < count;
          t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         int32_t *e = out + 4 * t;
         if (op == KOSMOS_OP_AG_GEMM) {
-            const AgGeom g = ag_geom(P, m, 64, n, tile_m);
+            const AgGeom g = ag_geom(P, m, 64, n, tile_m, split);
             if (rail == 0) {
-                int s, j;
-                ag_decode_transfer(g, static_cast<int>(t), s, j);
-                e[0] = K_TRANSFER; e[1] = s; e[2] = j; e[3] = 0;
+                int s, j, q;
+                ag_decode_transfer(g, static_cast<int>(t), s, j, q);
+                e[0] = K_TRANSFER; e[1] = s; e[2] = j; e[3] = q;
             } else {
                 int s, i, c;
-                ag_decode_tile(g, static_cast<int>(t), s, i, c);
-                e[0] = K_TILE; e[1] = s; e[2] = i; e[3] = c;
+                const int kind = ag_decode_tile(g, static_cast<int>(t), s, i, c);
+                e[0] = kind; e[1] = s; e[2] = i; e[3] = c;
             }
         } else {
             const RsGeom g = rs_geom(P, m, 64, n, tile_m);
@@ -120,12 +120,12 @@ __global__ void rail_decode_kernel(int op, int P, int64_t m, int64_t n, int orde
 }
 
 kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
-                                 int32_t *out, int64_t count, cudaStream_t stream) {
+                                 int64_t split, int32_t *out, int64_t count, cudaStream_t stream) {
     int64_t blocks = cdiv(count, 256);
     if (blocks < 1) blocks = 1;
     if (blocks > 4096) blocks = 4096;
-    rail_decode_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(op, P, m, n, order, rank, rail, tile_m, out,
-                                                                           count);
+    rail_decode_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(op, P, m, n, order, rank, rail, tile_m, split,
+                                                                           out, count);
     return cudaGetLastError() == cudaSuccess ? KOSMOS_OK : KOSMOS_ERR_CUDA;
 }
 

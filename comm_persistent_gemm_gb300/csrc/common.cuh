@@ -28,7 +28,10 @@ constexpr int NSTAGE = 4;          // shared-memory pipeline depth
 constexpr int A_STAGE_BYTES = BM * BK * 2;
 constexpr int B_STAGE_BYTES = BK * BN * 2;
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int PIECE_ROWS = BM;     // all-gather transfer piece height (one tile row)
+constexpr int PBM = 256;           // tile rows of an SM pair (tcgen05 cta_group::2, M = 256)
+constexpr int PIECE_ROWS = BM;     // all-gather piece height (one tile row): the unit a tile waits for
+constexpr int PART_ROWS = 32;      // all-gather transfer entry height: a piece arrives in PIECE_PARTS parts
+constexpr int PIECE_PARTS = PIECE_ROWS / PART_ROWS;
 constexpr int NSCHED = 4;          // depth of the in-CTA entry ring
 constexpr int NUM_THREADS = 192;   // warp 0 scheduler/producer, warp 1 MMA, warps 2-5 epilogue
 constexpr int NUM_EPI_THREADS = 128;
@@ -48,6 +51,7 @@ enum EntryKind : int32_t {
     K_TILE_D = 7,
     K_PUSH = 8,
     K_FOLD = 9,
+    K_TILE_HALF = 10,  // rail decode only: a tile's column half (the kernels run it as a K_TILE of BN/2 columns)
     K_DONE = 15
 };
 
@@ -79,37 +83,71 @@ KOS_HD int64_t align_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 struct AgGeom {
     int P;
     int64_t m, k, n;
-    int pieces;      // 128-row transfer pieces per shard
+    int pieces;      // 128-row pieces per shard (one readiness flag each)
+    int parts;       // transfer entries per piece (PART_ROWS rows each)
     int tile_rows;   // 128 (one SM per tile) or 256 (an SM pair per tile)
     int tiles_m;     // tile rows per shard
     int tiles_n;
-    int n_transfer;  // P * pieces: remote shards first, the local shard's copies last
-    int n_tile;      // P * tiles_m * tiles_n
+    int n_transfer;  // P * pieces * parts: remote shards first, the local shard's copies last
+    int n_full;      // P * tiles_m * tiles_n whole tiles
+    int n_split;     // the last n_split of them run as two column halves each
+    int n_tile;      // tile rail length: n_full + n_split
 };
-KOS_HD AgGeom ag_geom(int P, int64_t m, int64_t k, int64_t n, int tile_rows = BM) {
+KOS_HD AgGeom ag_geom(int P, int64_t m, int64_t k, int64_t n, int tile_rows = BM, int64_t n_split = 0) {
     AgGeom g;
     g.P = P; g.m = m; g.k = k; g.n = n;
     g.pieces = static_cast<int>(cdiv(m, PIECE_ROWS));
+    g.parts = PIECE_PARTS;
     g.tile_rows = tile_rows;
     g.tiles_m = static_cast<int>(cdiv(m, tile_rows));
     g.tiles_n = static_cast<int>(cdiv(n, BN));
-    g.n_transfer = P * g.pieces;
-    g.n_tile = P * g.tiles_m * g.tiles_n;
+    g.n_transfer = P * g.pieces * g.parts;
+    g.n_full = P * g.tiles_m * g.tiles_n;
+    g.n_split = static_cast<int>(n_split < 0 ? 0 : (n_split > g.n_full ? g.n_full : n_split));
+    g.n_tile = g.n_full + g.n_split;
     return g;
 }
-// Transfer rail: shards 1..P-1 in the order the tiles consume them, then shard 0.
-KOS_HD void ag_decode_transfer(const AgGeom &g, int t, int &shard, int &piece) {
-    const int sidx = t / g.pieces;
-    piece = t - sidx * g.pieces;
+// Transfer rail: shards 1..P-1 in the order the tiles consume them, then
+// shard 0; inside a shard, pieces in row order, each as `parts` row-ordered
+// parts.  A piece's flag reaches (epoch + 1) * parts when all its parts have
+// landed.
+KOS_HD void ag_decode_transfer(const AgGeom &g, int t, int &shard, int &piece, int &part) {
+    const int per_shard = g.pieces * g.parts;
+    const int sidx = t / per_shard;
+    const int r = t - sidx * per_shard;
+    piece = r / g.parts;
+    part = r - piece * g.parts;
     shard = (sidx + 1 < g.P) ? sidx + 1 : 0;
 }
-// Tile rail: shard-major (local shard 0 first), tile rows, then tile columns.
-KOS_HD void ag_decode_tile(const AgGeom &g, int t, int &shard, int &trow, int &tcol) {
+// Rows [row0, row0 + rows) of a shard carried by transfer part (piece, part); rows may be 0.
+KOS_HD void ag_part_rows(const AgGeom &g, int piece, int part, int64_t &row0, int64_t &rows) {
+    row0 = static_cast<int64_t>(piece) * PIECE_ROWS + static_cast<int64_t>(part) * PART_ROWS;
+    const int64_t left = g.m - row0;
+    rows = left <= 0 ? 0 : (left < PART_ROWS ? left : PART_ROWS);
+}
+KOS_HD uint32_t ag_piece_ready(const AgGeom &g, uint32_t epoch) {
+    return (epoch + 1u) * static_cast<uint32_t>(g.parts);
+}
+// Tile rail: shard-major (local shard 0 first), tile rows, then tile columns;
+// the last n_split tiles of that order appear as their two column halves,
+// left half first.  Returns K_TILE (tcol counts BN columns) or K_TILE_HALF
+// (tcol counts BN / 2 columns).
+KOS_HD int ag_decode_tile(const AgGeom &g, int t, int &shard, int &trow, int &tcol) {
+    const int keep = g.n_full - g.n_split;
+    int f = t, half = -1;
+    if (t >= keep) {
+        const int h = t - keep;
+        f = keep + h / 2;
+        half = h - (h / 2) * 2;
+    }
     const int per_shard = g.tiles_m * g.tiles_n;
-    shard = t / per_shard;
-    const int r = t - shard * per_shard;
+    shard = f / per_shard;
+    const int r = f - shard * per_shard;
     trow = r / g.tiles_n;
     tcol = r - trow * g.tiles_n;
+    if (half < 0) return K_TILE;
+    tcol = 2 * tcol + half;
+    return K_TILE_HALF;
 }
 
 // ---------------------------------------------------------------- RS geometry / rails

@@ -125,6 +125,153 @@ __device__ __forceinline__ bool wait_flag_eq(WsHeader *ws, const uint32_t *flag,
     return true;
 }
 
+// ---------------------------------------------------------------- streaming mover
+// One transfer entry: up to two contiguous segments, copied global -> shared
+// -> global with bulk async copies, then one release-add on *flag.
+struct MoveEntry {
+    const uint8_t *src[2];
+    uint8_t *dst[2];
+    int64_t bytes[2];
+    uint32_t *flag;  // nullptr: no release (a transfer dropped by fault injection)
+    int32_t ticket;
+    int64_t t_claim;
+};
+
+struct MoveChunk {
+    uint8_t *dst;
+    uint32_t *flag;
+    int64_t t_claim;
+    int32_t ticket;
+    uint32_t bytes;
+    int32_t last;  // the entry's final chunk
+};
+
+// Publishes a transfer whose stores have completed: order the async-proxy
+// writes before the generic release, then add one arrival to its flag.
+template <class Done>
+__device__ __forceinline__ void move_release(const MoveChunk &c, Done &done) {
+    fence_proxy_async_global();
+    __threadfence();
+    if (c.flag) red_release_add_gpu(c.flag, 1u);
+    done(c.ticket, c.t_claim);
+}
+
+// Single-thread mover loop over consecutive transfer entries.  Chunks of CH
+// bytes flow through NS stage buffers (stage b completes on cbar[b]); loads of
+// the next entry are issued while the current one drains, so the pipeline
+// does not empty between entries.  An entry is released once its last store
+// is DEFER bulk groups old (cp.async.bulk.wait_group DEFER).
+//   claim(MoveEntry &) -> bool : claim and describe the next entry; false when
+//                                the rail is exhausted.
+//   done(ticket, t_claim)      : called after each release (role trace).
+// Returns false after a device error (a copy that never landed).
+template <int NS, int CH, int DEFER, class Claim, class Done>
+__device__ __noinline__ bool stream_mover(uint8_t *stages, uint64_t *cbar, uint32_t &cphase, WsHeader *ws,
+                                          Claim &claim, Done &done) {
+    static_assert(NS >= 2 && DEFER >= 0 && DEFER < 4, "stream_mover parameters");
+    MoveChunk meta[NS];
+    MoveChunk pend[4];  // entries whose last store is in flight, oldest first
+    int64_t pend_at[4];
+    int npend = 0;
+    MoveEntry cur;
+    int seg = 0;
+    int64_t off = 0;
+    bool have = false, more = true;
+
+    auto next_chunk = [&](MoveChunk &out, const uint8_t *&src) -> bool {
+        while (true) {
+            if (!have) {
+                if (!more || !claim(cur)) {
+                    more = false;
+                    return false;
+                }
+                seg = 0;
+                off = 0;
+                have = true;
+                if (cur.bytes[0] + cur.bytes[1] == 0) {  // an empty part: nothing to copy
+                    MoveChunk e;
+                    e.flag = cur.flag; e.ticket = cur.ticket; e.t_claim = cur.t_claim;
+                    move_release(e, done);
+                    have = false;
+                    continue;
+                }
+            }
+            if (off >= cur.bytes[seg]) {
+                if (++seg >= 2) {
+                    have = false;
+                } else {
+                    off = 0;
+                }
+                continue;
+            }
+            const int64_t rem = cur.bytes[seg] - off;
+            const uint32_t nb = static_cast<uint32_t>(rem < CH ? rem : CH);
+            src = cur.src[seg] + off;
+            out.dst = cur.dst[seg] + off;
+            out.bytes = nb;
+            out.flag = cur.flag;
+            out.ticket = cur.ticket;
+            out.t_claim = cur.t_claim;
+            off += nb;
+            out.last = (off >= cur.bytes[seg]) && (seg == 1 || cur.bytes[1] == 0);
+            if (out.last) have = false;
+            return true;
+        }
+    };
+
+    int64_t issued = 0, stored = 0;
+    for (int b = 0; b < NS; ++b) {
+        const uint8_t *src;
+        if (!next_chunk(meta[b], src)) break;
+        mbar_arrive_expect_tx(&cbar[b], meta[b].bytes);
+        bulk_g2s(stages + b * CH, src, meta[b].bytes, &cbar[b]);
+        ++issued;
+    }
+    while (stored < issued) {
+        const int b = static_cast<int>(stored % NS);
+        if (!mbar_wait(&cbar[b], (cphase >> b) & 1u, PIPE_LIMIT_NS)) {
+            bulk_wait<0>();
+            set_error(ws, KOSMOS_ERR_DEVICE, meta[b].ticket);
+            return false;
+        }
+        cphase ^= (1u << b);
+        bulk_s2g(meta[b].dst, stages + b * CH, meta[b].bytes);
+        bulk_commit();
+        if (meta[b].last) {
+            pend[npend] = meta[b];
+            pend_at[npend] = stored;
+            ++npend;
+        }
+        if (npend > 0 && pend_at[0] + DEFER <= stored) {
+            bulk_wait<DEFER>();
+            int k = 0;
+            while (k < npend && pend_at[k] + DEFER <= stored) move_release(pend[k++], done);
+            for (int j = k; j < npend; ++j) {
+                pend[j - k] = pend[j];
+                pend_at[j - k] = pend_at[j];
+            }
+            npend -= k;
+        }
+        // refill the previous chunk's stage once its store has read it
+        if (stored >= 1) {
+            MoveChunk nc;
+            const uint8_t *src;
+            if (next_chunk(nc, src)) {
+                bulk_wait_read<1>();
+                const int rb = static_cast<int>((stored - 1) % NS);
+                meta[rb] = nc;
+                mbar_arrive_expect_tx(&cbar[rb], nc.bytes);
+                bulk_g2s(stages + rb * CH, src, nc.bytes, &cbar[rb]);
+                ++issued;
+            }
+        }
+        ++stored;
+    }
+    bulk_wait<0>();
+    for (int k = 0; k < npend; ++k) move_release(pend[k], done);
+    return true;
+}
+
 // ---------------------------------------------------------------- setup / teardown
 __device__ __forceinline__ void engine_setup(const Smem &sm, int warp) {
     if (threadIdx.x == 0) {
@@ -177,20 +324,6 @@ __device__ __forceinline__ void engine_teardown(const Smem &sm, int warp, uint32
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
-}
-
-// Waits until every stage of the pipeline is free again (all MMAs issued so far
-// have read their operands), so the stage buffers can serve as copy buffers.
-__device__ __forceinline__ bool drain_stages(const Smem &sm, const PipeState &ps, WsHeader *ws) {
-    for (int i = 0; i < NSTAGE; ++i) {
-        uint32_t s = ps.stage + i, ph = ps.phase;
-        if (s >= NSTAGE) { s -= NSTAGE; ph ^= 1u; }
-        if (!mbar_wait(&sm.empty[s], ph ^ 1u, PIPE_LIMIT_NS)) {
-            set_error(ws, KOSMOS_ERR_DEVICE, -11);
-            return false;
-        }
-    }
-    return true;
 }
 
 // ---------------------------------------------------------------- ring (producer side)

@@ -19,15 +19,15 @@
 
 namespace kosmos {
 
-constexpr int PBM = 256;                        // pair tile rows
 constexpr int HBM_ROWS = 128;                   // rows per CTA
 constexpr int HBN = 128;                        // B columns per CTA
-constexpr int NSTAGE2 = 6;
+constexpr int NSTAGE2 = 7;                      // 224 KB of stages: loads are latency-bound below ~7
 constexpr int A2_BYTES = HBM_ROWS * BK * 2;     // 16 KB
 constexpr int B2_BYTES = BK * HBN * 2;          // 16 KB (two 64-column slabs)
 constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
 constexpr int SMEM2_CTRL = 2048;
 constexpr int SMEM2_BYTES = NSTAGE2 * STAGE2_BYTES + SMEM2_CTRL + 1024;
+static_assert(SMEM2_BYTES <= 232448, "pair engine exceeds 227 KB of shared memory per CTA");
 
 // ---------------------------------------------------------------- cluster helpers
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -270,6 +270,8 @@ __device__ __forceinline__ void mma2_loop(const Smem2 &sm, uint32_t tmem_base, W
             ps.advance(e.nstage);
             continue;
         }
+        // N of this entry's MMA (both CTAs' columns): a multiple of 32 in [32, 256] (0 selects BN)
+        const uint32_t idesc = (e.nmma > 0 && e.nmma < BN) ? idesc_bf16_f32(PBM, e.nmma, false, true) : IDESC;
         if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, PIPE_LIMIT_NS)) {
             set_error(ws, KOSMOS_ERR_DEVICE, -4);
             break;
@@ -290,7 +292,7 @@ __device__ __forceinline__ void mma2_loop(const Smem2 &sm, uint32_t tmem_base, W
             for (int k = 0; k < BK / UMMA_K; ++k) {
                 const uint64_t ad = sdesc_sw128(a_addr + k * (UMMA_K * 2), 16, 1024);
                 const uint64_t bd = sdesc_sw128(b_addr + k * (UMMA_K * 128), 64 * 128, 1024);
-                mma2_bf16_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                mma2_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
             mma2_commit_both(&sm.empty[ps.stage]);
             ps.advance();
@@ -325,41 +327,6 @@ __device__ __forceinline__ bool drain_stages2(const Smem2 &sm, const PipeState2 
             return false;
         }
     }
-    return true;
-}
-
-// Bulk async copy of `bytes` through the NSTAGE2 stage buffers (the caller owns them).
-__device__ __forceinline__ bool bulk_copy2(const Smem2 &sm, const uint8_t *src, uint8_t *dst, int64_t bytes,
-                                           uint32_t &cphase, WsHeader *ws, int64_t entry) {
-    constexpr int64_t CH = STAGE2_BYTES;
-    const int64_t nch = cdiv(bytes, CH);
-    auto cb = [&](int64_t c) -> uint32_t {
-        const int64_t rem = bytes - c * CH;
-        return static_cast<uint32_t>(rem < CH ? rem : CH);
-    };
-    for (int64_t c = 0; c < nch && c < NSTAGE2; ++c) {
-        mbar_arrive_expect_tx(&sm.cbar[c], cb(c));
-        bulk_g2s(sm.stages + c * CH, src + c * CH, cb(c), &sm.cbar[c]);
-    }
-    for (int64_t c = 0; c < nch; ++c) {
-        const int b = static_cast<int>(c % NSTAGE2);
-        if (!mbar_wait(&sm.cbar[b], (cphase >> b) & 1u, PIPE_LIMIT_NS)) {
-            bulk_wait<0>();
-            set_error(ws, KOSMOS_ERR_DEVICE, entry);
-            return false;
-        }
-        cphase ^= (1u << b);
-        bulk_s2g(dst + c * CH, sm.stages + b * CH, cb(c));
-        bulk_commit();
-        const int64_t refill = c - 1 + NSTAGE2;
-        if (c >= 1 && refill < nch) {
-            bulk_wait_read<1>();
-            const int rb = static_cast<int>((c - 1) % NSTAGE2);
-            mbar_arrive_expect_tx(&sm.cbar[rb], cb(refill));
-            bulk_g2s(sm.stages + rb * CH, src + refill * CH, cb(refill), &sm.cbar[rb]);
-        }
-    }
-    bulk_wait<0>();
     return true;
 }
 

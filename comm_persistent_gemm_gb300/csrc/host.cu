@@ -182,6 +182,52 @@ int resolve_comm(const kosmos_opts &o, int grid, int P, bool fixed) {
     return n;
 }
 
+// Launch shape of one all-gather + GEMM call: grid, tile engine, initial
+// movers (CTAs) and the tile-rail split.
+struct AgPlan {
+    int grid;
+    int pair;
+    int n_comm;
+    int64_t n_split;
+};
+
+kosmos_status ag_plan(int P, int64_t m, int64_t n, int dtype, const kosmos_opts &o, AgPlan &pl) {
+    int grid = grid_for(o);
+    if (grid < 1) return KOSMOS_ERR_CUDA;
+    int pair = (dtype == KOSMOS_BF16 && o.cta_pair != 0) ? 1 : 0;
+    if (pair) {
+        const int lim = ag_pair_grid_limit();
+        int g2 = grid & ~1;
+        if (lim >= 2 && g2 > lim) g2 = lim;
+        if (lim < 2 || g2 < 2) {
+            if (o.cta_pair == 1) return KOSMOS_ERR_UNSUPPORTED;
+            pair = 0;
+        } else {
+            grid = g2;
+        }
+    }
+    if (o.sched == KOSMOS_SCHED_FIXED && grid < (pair ? 4 : 2)) return KOSMOS_ERR_INVALID_ARG;
+    int n_comm = resolve_comm(o, grid, P, o.sched == KOSMOS_SCHED_FIXED);
+    if (pair && n_comm > grid - 2) n_comm = grid - 2;  // keep a builder pair
+    int64_t split = 0;
+    if (dtype == KOSMOS_BF16) {
+        if (o.tail_split >= 0) {
+            split = o.tail_split;
+        } else {  // one wave: every tile engine that builds
+            split = pair ? grid / 2 : grid;
+            if (o.sched == KOSMOS_SCHED_FIXED) split -= pair ? (n_comm + 1) / 2 : n_comm;
+        }
+        const int64_t n_full = ag_geom(P, m, 64, n, pair ? PBM : BM).n_full;
+        if (split > n_full) split = n_full;
+        if (split < 0) split = 0;
+    }
+    pl.grid = grid;
+    pl.pair = pair;
+    pl.n_comm = n_comm;
+    pl.n_split = split;
+    return KOSMOS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -197,6 +243,7 @@ void kosmos_default_opts(kosmos_opts *opts) {
     opts->trace = 0;
     opts->cta_pair = -1;
     opts->plain_launch = 0;
+    opts->tail_split = 0;
     opts->wait_limit_ns = 0;
     opts->inject = 0;
 }
@@ -248,21 +295,9 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     if (o.sched < KOSMOS_SCHED_SELF || o.sched > KOSMOS_SCHED_UNFUSED) return KOSMOS_ERR_INVALID_ARG;
     if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_AG_GEMM, P, m_per_shard, n, k, dtype, &o))
         return KOSMOS_ERR_WORKSPACE;
-    int grid = grid_for(o);
-    if (grid < 1) return KOSMOS_ERR_CUDA;
-    int pair = (dtype == KOSMOS_BF16 && o.cta_pair != 0) ? 1 : 0;
-    if (pair) {
-        const int lim = ag_pair_grid_limit();
-        int g2 = grid & ~1;
-        if (lim >= 2 && g2 > lim) g2 = lim;
-        if (lim < 2 || g2 < 2) {
-            if (o.cta_pair == 1) return KOSMOS_ERR_UNSUPPORTED;
-            pair = 0;
-        } else {
-            grid = g2;
-        }
-    }
-    if (o.sched == KOSMOS_SCHED_FIXED && grid < (pair ? 4 : 2)) return KOSMOS_ERR_INVALID_ARG;
+    AgPlan pl;
+    const kosmos_status ps = ag_plan(P, m_per_shard, n, dtype, o, pl);
+    if (ps != KOSMOS_OK) return ps;
     AgLaunch L;
     memset(&L, 0, sizeof(L));
     L.P = P; L.m = m_per_shard; L.k = k; L.n = n;
@@ -272,13 +307,25 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     }
     L.w = w; L.wsc = w_scales; L.x_gathered = x_gathered; L.y = y; L.ws = ws;
     L.dtype = dtype; L.sched = o.sched;
-    L.n_comm = resolve_comm(o, grid, P, o.sched == KOSMOS_SCHED_FIXED);
-    if (pair && L.n_comm > grid - 2) L.n_comm = grid - 2;  // keep a builder pair
-    L.pair = pair;
-    L.trace = o.trace; L.grid = grid; L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
+    L.n_comm = pl.n_comm;
+    L.pair = pl.pair;
+    L.n_split = pl.n_split;
+    L.trace = o.trace; L.grid = pl.grid; L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
     L.plain_launch = o.plain_launch;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == KOSMOS_BF16 ? launch_ag_bf16(L, s) : launch_ag_mxfp8(L, s);
+}
+
+int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t n, int dtype, const kosmos_opts *opts,
+                        int64_t *tail_split, int *tile_m) {
+    if (P < 1 || P > KOSMOS_MAX_P || m_per_shard < 1 || n < 8) return -1;
+    if (dtype != KOSMOS_BF16 && dtype != KOSMOS_MXFP8_E4M3) return -1;
+    const kosmos_opts o = resolve_opts(opts);
+    AgPlan pl;
+    if (ag_plan(P, m_per_shard, n, dtype, o, pl) != KOSMOS_OK) return -1;
+    if (tail_split) *tail_split = pl.n_split;
+    if (tile_m) *tile_m = pl.pair ? PBM : BM;
+    return 0;
 }
 
 kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_shards, int P, int64_t m,
@@ -442,22 +489,22 @@ kosmos_status kosmos_trace_info(int op, int P, int64_t m, int64_t n, int64_t k, 
 }
 
 int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
-                           int32_t *out, int64_t max_entries) {
-    if (P < 1 || P > KOSMOS_MAX_P || m < 1 || n < 1 || (tile_m != 128 && tile_m != 256)) return -1;
+                           int64_t split, int32_t *out, int64_t max_entries) {
+    if (P < 1 || P > KOSMOS_MAX_P || m < 1 || n < 1 || (tile_m != 128 && tile_m != 256) || split < 0) return -1;
     if (op == KOSMOS_OP_AG_GEMM) {
-        const AgGeom g = ag_geom(P, m, 64, n, tile_m);
+        const AgGeom g = ag_geom(P, m, 64, n, tile_m, split);
         const int64_t len = rail == 0 ? g.n_transfer : g.n_tile;
         if (out) {
             for (int64_t t = 0; t < len && t < max_entries; ++t) {
                 int32_t *e = out + 4 * t;
                 if (rail == 0) {
-                    int s, j;
-                    ag_decode_transfer(g, static_cast<int>(t), s, j);
-                    e[0] = K_TRANSFER; e[1] = s; e[2] = j; e[3] = 0;
+                    int s, j, q;
+                    ag_decode_transfer(g, static_cast<int>(t), s, j, q);
+                    e[0] = K_TRANSFER; e[1] = s; e[2] = j; e[3] = q;
                 } else {
                     int s, i, c;
-                    ag_decode_tile(g, static_cast<int>(t), s, i, c);
-                    e[0] = K_TILE; e[1] = s; e[2] = i; e[3] = c;
+                    const int kind = ag_decode_tile(g, static_cast<int>(t), s, i, c);
+                    e[0] = kind; e[1] = s; e[2] = i; e[3] = c;
                 }
             }
         }
@@ -487,12 +534,12 @@ int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int r
 }
 
 int64_t kosmos_rail_decode_device(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
-                                  int32_t *out, int64_t max_entries, void *stream) {
-    const int64_t len = kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, nullptr, 0);
+                                  int64_t split, int32_t *out, int64_t max_entries, void *stream) {
+    const int64_t len = kosmos_rail_decode(op, P, m, n, order, rank, rail, tile_m, split, nullptr, 0);
     if (len < 0 || out == nullptr) return len;
     const int64_t cnt = len < max_entries ? len : max_entries;
-    if (launch_rail_decode(op, P, m, n, order, rank, rail, tile_m, out, cnt, static_cast<cudaStream_t>(stream)) !=
-        KOSMOS_OK)
+    if (launch_rail_decode(op, P, m, n, order, rank, rail, tile_m, split, out, cnt,
+                           static_cast<cudaStream_t>(stream)) != KOSMOS_OK)
         return -1;
     return len;
 }

@@ -27,6 +27,7 @@ struct AgLaunch {
     int grid;
     int pair;       // 1: SM-pair (cta_group::2) tiles, grid = 2 x clusters
     int plain_launch;
+    int64_t n_split;  // trailing tiles of the tile rail run as column halves
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -99,6 +100,7 @@ bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t
 kosmos_status launch_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q,
                                     void *scales, cudaStream_t stream);
 kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail, int tile_m,
+                                 int64_t split,
                                  int32_t *out, int64_t count, cudaStream_t stream);
 int ag_pair_grid_limit();
 int rs_pair_grid_limit();

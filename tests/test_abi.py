@@ -67,12 +67,13 @@ def test_host_validation_rejects_bad_args(K):
     assert lib.kosmos_mxfp8_quantize(base, 4, 96, 1, base, base, None) == 1
 
 
+@pytest.mark.parametrize("split", [0, 3, 76, 10**6])
 @pytest.mark.parametrize("tile_m", [128, 256])
 @pytest.mark.parametrize("P,m,n", [(2, 64, 128), (8, 1024, 3584), (3, 200, 264), (1, 5, 8)])
-def test_ag_rail_decode_matches_oracle(K, orc, P, m, n, tile_m):
-    tr, tl = orc.rail_ag(P, m, n, R=128, BN=256, TR=tile_m)
-    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=0, tile_m=tile_m), tr)
-    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=1, tile_m=tile_m), tl)
+def test_ag_rail_decode_matches_oracle(K, orc, P, m, n, tile_m, split):
+    tr, tl = orc.rail_ag(P, m, n, R=128, BN=256, TR=tile_m, PR=32, XS=split)
+    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=0, tile_m=tile_m, split=split), tr)
+    assert np.array_equal(K.rail_decode(K.OP_AG_GEMM, P, m, n, rail=1, tile_m=tile_m, split=split), tl)
 
 
 @pytest.mark.parametrize("tile_m", [128, 256])

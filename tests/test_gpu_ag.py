@@ -78,6 +78,39 @@ def test_ag_mover_counts(K, orc, n_comm0, mode):
     _check_full(orc, K, inp, K.opts(n_comm0=n_comm0, cta_pair=PAIR[mode]))
 
 
+@pytest.mark.parametrize("mode", list(PAIR))
+@pytest.mark.parametrize("split", [-1, 3, 10**6])
+@pytest.mark.parametrize("P,m,k,n", [(3, 200, 192, 264), (2, 300, 128, 520), (4, 128, 320, 512)])
+def test_ag_tail_split(K, orc, P, m, k, n, split, mode):
+    """Tiles run as column halves (none, the last 3, all of them): same
+    results, and bit-identical to the unsplit rail (each output element keeps
+    its K order)."""
+    inp = ag_inputs(P, m, k, n, seed=4000 + P * m + n, var_w=1.0 / k)
+    o = K.opts(cta_pair=PAIR[mode], tail_split=split)
+    _check_full(orc, K, inp, o)
+    _, _, a, _ = _run(K, inp, o)
+    _, _, b, _ = _run(K, inp, K.opts(cta_pair=PAIR[mode], tail_split=0))
+    assert torch.equal(a[0], b[0])
+
+
+def test_ag_tile_plan_split(K):
+    """No split by default; tail_split = -1 is one wave: every tile engine that builds."""
+    sms = K.num_sms()
+    assert K.ag_tile_plan(8, 1024, 3584, K.opts()) == (0, 256)
+    sp, tm = K.ag_tile_plan(8, 1024, 3584, K.opts(tail_split=-1))
+    assert tm == 256 and 1 <= sp <= sms // 2  # one per co-resident SM pair
+    if sms == 152:
+        assert sp == 76
+    assert K.ag_tile_plan(8, 1024, 3584, K.opts(tail_split=10**6))[0] == 8 * 4 * 14  # clamped to the tiles
+    assert K.ag_tile_plan(8, 1024, 3584, K.opts(tail_split=5))[0] == 5
+    sp1, tm1 = K.ag_tile_plan(8, 1024, 3584, K.opts(cta_pair=0, tail_split=-1))
+    assert tm1 == 128 and sp1 == min(sms, 8 * 8 * 14)
+    sp2, _ = K.ag_tile_plan(8, 1024, 3584, K.opts(cta_pair=0, sched=K.SCHED_FIXED, fixed_comm_ctas=10,
+                                                   tail_split=-1))
+    assert sp2 == sms - 10
+    assert K.ag_tile_plan(8, 1024, 3584, K.opts(tail_split=-1), dtype=K.MXFP8_E4M3)[0] == 0
+
+
 def test_ag_few_ctas(K, orc):
     """A grid much smaller than the tile count: CTAs loop over many entries."""
     inp = ag_inputs(4, 384, 256, 768, seed=5, var_w=1.0 / 256)
@@ -116,9 +149,10 @@ def test_ag_full_size_sampled(K, orc, sched):
 def test_ag_rail_decode_device_matches_oracle(K, orc):
     for (P, m, n) in [(8, 1024, 3584), (3, 200, 264)]:
         for tm in (128, 256):
-            tr, tl = orc.rail_ag(P, m, n, TR=tm)
-            assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=0, tile_m=tm), tr)
-            assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=1, tile_m=tm), tl)
+            for split in (0, 76, 10**6):
+                tr, tl = orc.rail_ag(P, m, n, TR=tm, XS=split)
+                assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=0, tile_m=tm, split=split), tr)
+                assert np.array_equal(K.rail_decode_device(K.OP_AG_GEMM, P, m, n, rail=1, tile_m=tm, split=split), tl)
 
 
 @pytest.mark.parametrize("mode", list(PAIR))
@@ -127,7 +161,9 @@ def test_ag_trace_every_entry_once(K, orc, mode):
     o = K.opts(trace=1, cta_pair=PAIR[mode])
     xs, xg, outs, ws = _run(K, inp, o)
     recs = K.trace_records(K.OP_AG_GEMM, 4, 512, 512, 128, ws, o)
-    tr, tl = orc.rail_ag(4, 512, 512, TR=256 if PAIR[mode] else 128)
+    split, tm = K.ag_tile_plan(4, 512, 512, o)
+    assert tm == (256 if PAIR[mode] else 128)
+    tr, tl = orc.rail_ag(4, 512, 512, TR=tm, XS=split)
     tiles = np.sort(recs["ticket"][recs["kind"] == 2])
     transfers = np.sort(recs["ticket"][recs["kind"] == 1])
     assert np.array_equal(tiles, np.arange(len(tl)))
@@ -151,8 +187,10 @@ def test_ag_dropped_transfer_times_out_then_recovers(K, orc):
     K.ag_gemm(xs, w, xg, y, ws, o)
     st, entry = K.status_sync(ws)
     assert st == K.ERR_TIMEOUT
-    # transfer 0 is shard 1 piece 0, consumed by tile tickets 1 (shard 1, row 0, col 0)
-    assert entry == 1
+    # transfer 0 is part 0 of shard 1's piece 0; the first tile of shard 1 waits for it
+    split, tm = K.ag_tile_plan(P, m, n, o)
+    _, tl = orc.rail_ag(P, m, n, TR=tm, XS=split)
+    assert entry == int(np.flatnonzero(tl[:, 1] == 1)[0])
     K.workspace_init(ws)
     K.ag_gemm(xs, w, xg, y, ws, K.opts())
     K.check(ws)
