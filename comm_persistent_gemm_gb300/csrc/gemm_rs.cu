@@ -306,10 +306,11 @@ __device__ __forceinline__ bool red_push(const RedRing &rr, RingState &rs, const
 __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm, const RedRing &rr, uint32_t crank) {
     const int P = p.g.P;
     const int pair = blockIdx.x / 2;
-    const int rank = pair % P;
-    const int lp = pair / P;
     const bool leader = crank == 0;
-    const bool reducer_pair = (p.mode == RS_REDUCE_ONLY) || (p.mode == RS_FUSED && lp < p.n_red);
+    // the first n_red pairs reduce from the start, each of their CTAs for rank (CTA index mod P);
+    // builder pairs build for rank (pair index mod P) and reduce for it after the switch
+    const bool reducer_pair = (p.mode == RS_REDUCE_ONLY) || (p.mode == RS_FUSED && pair < p.n_red);
+    const int rank = (reducer_pair && p.mode == RS_FUSED) ? static_cast<int>(blockIdx.x) % P : pair % P;
     PipeState2 ps;
     RingPair rs;
     int nrec = 0;
@@ -615,7 +616,7 @@ kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
     }
     p.nkb = static_cast<int>(L.k / BK);
     p.sched = L.sched;
-    p.n_red = L.n_comm;
+    p.n_red = L.pair ? (L.n_comm * L.P + 1) / 2 : L.n_comm;  // pair kernel: reducer pairs
     p.order = L.order;
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;

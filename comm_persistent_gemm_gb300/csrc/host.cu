@@ -353,8 +353,9 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
         const int lim = rs_pair_grid_limit();
         int g2 = grid & ~1;
         if (lim >= 2 && g2 > lim) g2 = lim;
-        // every emulated rank needs a pair; a fixed reducer crew needs a second one
-        const int need = (o.sched == KOSMOS_SCHED_FIXED) ? 4 * P : 2 * P;
+        // every emulated rank needs a builder pair; a fixed reducer crew needs at least one
+        // reducer CTA per rank on top (two ranks per reducer pair)
+        const int need = (o.sched == KOSMOS_SCHED_FIXED) ? 2 * P + 2 * ((P + 1) / 2) : 2 * P;
         if (lim < 2 || g2 < need) {
             if (o.cta_pair == 1) return KOSMOS_ERR_UNSUPPORTED;
             pair = 0;
@@ -375,11 +376,12 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
     L.sched = o.sched;
     L.pair = pair;
     {
-        const int per_rank = pair ? (grid / 2) / P : grid / P;  // pairs (or CTAs) per emulated rank
+        // reducer CTAs per emulated rank; SM pairs host two ranks' reducers each
+        const int max_red = pair ? (2 * (grid / 2 - P)) / P : grid / P - 1;  // keep a builder on every rank
         int n_red = o.n_comm0 >= 0 ? o.n_comm0 : 1;
         if (o.sched == KOSMOS_SCHED_FIXED && o.fixed_comm_ctas >= 0) n_red = o.fixed_comm_ctas;
         if (n_red < 1) n_red = 1;
-        if (n_red > per_rank - 1) n_red = per_rank - 1;  // keep a builder on every rank
+        if (n_red > max_red) n_red = max_red;
         if (n_red < 1 && o.sched == KOSMOS_SCHED_FIXED) return KOSMOS_ERR_INVALID_ARG;
         L.n_comm = n_red;
     }
