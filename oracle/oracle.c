@@ -438,7 +438,7 @@ ORC_EXPORT int orc_moe_experts(int64_t T, int64_t H, int E, int K, int64_t I, in
 /* [explainer, "Role switching only works"]: data is produced in the order its
  * consumers claim it.  Entries are written as 4 int32 fields
  * {kind, a, b, c}; kinds: 1 TRANSFER(shard, piece, part), 2 TILE, 3 REDUCE,
- * 10 TILE_HALF (a tile's column half).
+ * 10 TILE_HALF (one half of a tile's K range).
  * Tile and piece heights are R rows; output tiles are BN columns wide. */
 
 enum { ORC_TRANSFER = 1, ORC_TILE = 2, ORC_REDUCE = 3, ORC_TILE_HALF = 10 };
@@ -456,12 +456,14 @@ static int64_t orc_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
  * entries (empty ones).
  * Tile rail: output tiles TILE(shard, tile-row, tile-col) of TR rows and BN
  * columns, row-major over tile rows with the local shard (s = 0) first, then
- * s = 1, 2, ...  The last XS tiles of that order are each replaced by their
- * two column halves, TILE_HALF(shard, tile-row, half-col) covering columns
- * [half-col * BN/2, (half-col + 1) * BN/2), left half first [the pages give
- * no tile shapes; halving the final wave's tiles shortens the tail, where
- * CTAs that drew one tile more than others would otherwise finish a whole
- * tile later].
+ * s = 1, 2, ...  The last XS tiles of that order are each replaced by two
+ * entries TILE_HALF(shard, tile-row, 2 * tile-col + h) that compute the
+ * tile over the first (h = 0) and the second (h = 1) half of the K blocks;
+ * the output of the tile is the sum of the two [the pages give no tile
+ * shapes; halving the final wave's tiles shortens the tail, where CTAs that
+ * drew one tile more than others would otherwise finish a whole tile
+ * later.  Halving K keeps the operand bytes per multiply-add of a whole
+ * tile, which halving the columns would not].
  * Returns the number of entries written (transfer rail then tile rail), or
  * the count only when out == NULL; -1 for inconsistent arguments. */
 ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN, int TR, int PR, int64_t XS,

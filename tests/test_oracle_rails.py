@@ -81,8 +81,9 @@ def test_ag_rail_rejects_uneven_parts(orc):
 @pytest.mark.parametrize("P,m,n,TR,XS", [(8, 1024, 3584, 256, 76), (3, 320, 200, 128, 5), (2, 64, 128, 128, 99),
                                          (4, 512, 520, 256, 0)])
 def test_ag_rail_tail_halves_cover_every_output_once(orc, P, m, n, TR, XS):
-    """The split rail covers every output element exactly once, keeps the
-    unsplit prefix, and replaces only the last XS tiles (left half first)."""
+    """The split rail keeps the unsplit prefix, replaces only the last XS
+    tiles by their two K halves (adjacent, first half first), and covers
+    every (output element, K half) exactly once."""
     BN = 256
     _, full = orc.rail_ag(P, m, n, TR=TR, BN=BN)
     _, tl = orc.rail_ag(P, m, n, TR=TR, BN=BN, XS=XS)
@@ -93,10 +94,13 @@ def test_ag_rail_tail_halves_cover_every_output_once(orc, P, m, n, TR, XS):
     halves = tl[keep:]
     assert np.all(halves[:, 0] == 10)
     assert np.array_equal(halves[0::2, 1:3], full[keep:, 1:3])
+    assert np.array_equal(halves[1::2, 1:3], full[keep:, 1:3])
     assert np.array_equal(halves[0::2, 3], 2 * full[keep:, 3])
     assert np.array_equal(halves[1::2, 3], 2 * full[keep:, 3] + 1)
-    cover = np.zeros((P, -(-m // TR) * TR, -(-n // BN) * BN), dtype=np.int32)
+    cover = np.zeros((P, -(-m // TR) * TR, -(-n // BN) * BN, 2), dtype=np.int32)
     for kind, s, i, c in tl:
-        w = BN if kind == 2 else BN // 2
-        cover[s, i * TR:(i + 1) * TR, c * w:(c + 1) * w] += 1
+        if kind == 2:
+            cover[s, i * TR:(i + 1) * TR, c * BN:(c + 1) * BN, :] += 1
+        else:
+            cover[s, i * TR:(i + 1) * TR, (c // 2) * BN:(c // 2 + 1) * BN, c % 2] += 1
     assert np.all(cover == 1)
