@@ -104,7 +104,7 @@ def lib():
     L.kosmos_moe_workspace_bytes.restype = C.c_size_t
     L.kosmos_moe_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, vp, C.POINTER(vp), C.POINTER(i64)]
     L.kosmos_moe_debug_view.restype = i32
-    L.kosmos_ag_tile_plan.argtypes = [i32, i64, i64, i32, C.POINTER(Opts), C.POINTER(i64), C.POINTER(C.c_int32)]
+    L.kosmos_ag_tile_plan.argtypes = [i32, i64, i64, i64, i32, C.POINTER(Opts), C.POINTER(i64), C.POINTER(C.c_int32)]
     L.kosmos_ag_tile_plan.restype = i32
     _lib = L
     return L
@@ -300,12 +300,12 @@ def trace_records(op: int, P: int, m: int, n: int, k: int, ws, o: Opts):
     return recs[recs["kind"] != 0]
 
 
-def ag_tile_plan(P: int, m_per_shard: int, n: int, o: Optional[Opts] = None, dtype: int = BF16):
+def ag_tile_plan(P: int, m_per_shard: int, k: int, n: int, o: Optional[Opts] = None, dtype: int = BF16):
     """(tail_split, tile_m) that ag_gemm uses for these sizes and options on
     the current device: the arguments of its tile rail's decode."""
     sp = C.c_int64()
     tm = C.c_int32()
-    if lib().kosmos_ag_tile_plan(P, m_per_shard, n, dtype, C.byref(o) if o is not None else None, C.byref(sp),
+    if lib().kosmos_ag_tile_plan(P, m_per_shard, k, n, dtype, C.byref(o) if o is not None else None, C.byref(sp),
                                  C.byref(tm)) != 0:
         raise KosmosError(ERR_INVALID_ARG, "kosmos_ag_tile_plan")
     return sp.value, tm.value

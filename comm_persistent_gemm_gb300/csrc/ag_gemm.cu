@@ -29,6 +29,8 @@ struct AgParams {
     __nv_bfloat16 *y;
     WsHeader *ws;
     uint32_t *flags;
+    uint32_t *ksync;  // K-split slots: [slot][cta of the engine][counter, flag]
+    float4 *kpart;    // K-split slots: [slot][cta of the engine] fp32 partials
     TraceRec *trace;
     AgGeom g;
     int nkb;
@@ -38,6 +40,29 @@ struct AgParams {
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
+
+// Tile-rail entry -> what the engine runs: output columns [col0, col0 + BN)
+// and K blocks [kb0, kb0 + nk); slot >= 0 marks one K half of a split tile.
+struct AgTileWork {
+    int s, i, col0, kb0, nk, slot;
+};
+__device__ __forceinline__ AgTileWork ag_tile_work(const AgParams &p, int t) {
+    AgTileWork w;
+    int c;
+    const int kind = ag_decode_tile(p.g, t, w.s, w.i, c);
+    w.kb0 = 0;
+    w.nk = p.nkb;
+    w.slot = -1;
+    if (kind == K_TILE_HALF) {
+        const int h = c & 1;
+        c >>= 1;
+        w.kb0 = h ? p.nkb / 2 : 0;
+        w.nk = h ? p.nkb - p.nkb / 2 : p.nkb / 2;
+        w.slot = (t - (p.g.n_full - p.g.n_split)) >> 1;
+    }
+    w.col0 = c * BN;
+    return w;
+}
 
 // Mover side of the all-gather: claims transfer entries (one part of one
 // piece: <= 32 rows of one shard, contiguous in both the shard and the
@@ -94,9 +119,8 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
         }
         const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
         if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
-        int s, i, c;
-        const int width = ag_decode_tile(p.g, static_cast<int>(t), s, i, c) == K_TILE ? BN : BN / 2;
-        const int col0 = c * width;
+        const AgTileWork w = ag_tile_work(p, static_cast<int>(t));
+        const int s = w.s, i = w.i;
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
         if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0) {
             if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], ag_piece_ready(p.g, epoch), p.wait_limit_ns, t))
@@ -110,14 +134,14 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
         }
         ++nrec;
         SchedEntry e;
-        e.kind = K_TILE; e.a = s; e.b = i; e.c = col0; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
-        e.slot = slot; e.d = 0; e.nmma = width; e.x0 = e.x1 = e.x2 = 0;
+        fill_done(e);
+        e.kind = K_TILE; e.a = s; e.b = i; e.c = w.col0; e.d = w.kb0; e.nstage = w.nk;
+        e.ticket = static_cast<int32_t>(t); e.slot = slot; e.x1 = w.slot;
         if (!ring_push(sm, rs, e, p.ws)) break;
         const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
-        const int nslab = width / 64;
-        const uint32_t stage_tx = A_STAGE_BYTES + nslab * (64 * BK * 2);
         bool ok = true;
-        for (int kb = 0; kb < p.nkb; ++kb) {
+        for (int kk = 0; kk < w.nk; ++kk) {
+            const int kb = w.kb0 + kk;
             if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
                 set_error(p.ws, KOSMOS_ERR_DEVICE, t);
                 ok = false;
@@ -126,13 +150,14 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
             uint8_t *sa = sm.stages + ps.stage * STAGE_BYTES;
             uint8_t *sb = sa + A_STAGE_BYTES;
             uint64_t *bar = &sm.full[ps.stage];
-            mbar_arrive_expect_tx(bar, stage_tx);
+            mbar_arrive_expect_tx(bar, STAGE_BYTES);
             if (local)
                 tma_load_2d(sa, &p.tmA_local, bar, kb * BK, i * BM);
             else
                 tma_load_3d(sa, &p.tmA_gath, bar, kb * BK, i * BM, s);
-            for (int j = 0; j < nslab; ++j)
-                tma_load_2d(sb + j * (64 * BK * 2), &p.tmB, bar, col0 + j * 64, kb * BK);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sb + j * (64 * BK * 2), &p.tmB, bar, w.col0 + j * 64, kb * BK);
             ps.advance();
         }
         if (!ok) break;
@@ -144,7 +169,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
 }
 
 __device__ __forceinline__ void ag_epilogue(const AgParams &p, const Smem &sm, uint32_t tmem_base, int warp,
-                                            int lane) {
+                                            int lane, uint32_t epoch) {
     const int grp = warp & 3;  // TMEM lane group this warp may access
     const int row = grp * 32 + lane;
     RingState rs;
@@ -166,17 +191,22 @@ __device__ __forceinline__ void ag_epilogue(const AgParams &p, const Smem &sm, u
         }
         tc_fence_after();
         const int s = e.a, i = e.b;
-        const int width = e.nmma > 0 ? e.nmma : BN;
         const int64_t rloc = static_cast<int64_t>(i) * BM + row;
         const bool valid = rloc < p.g.m;
         __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + (valid ? rloc : 0)) * p.g.n;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
+        if (e.x1 >= 0) {  // one K half of a split tile
+            const int64_t cs = static_cast<int64_t>(e.x1) * 2;  // slot, CTA 0 of the engine
+            khalf_epilogue(taddr, valid, yrow, e.c, p.g.n, p.kpart + cs * (BM * BN / 4), &p.ksync[cs * 2],
+                           &p.ksync[cs * 2 + 1], epoch, p.ws, p.wait_limit_ns, e.ticket, row, sm.tmem_slot + 1);
+        } else {
 #pragma unroll 1
-        for (int ch = 0; ch < width / 32; ++ch) {
-            const int64_t col0 = static_cast<int64_t>(e.c) + ch * 32;
-            if (col0 >= p.g.n) break;
-            const int64_t left = p.g.n - col0;
-            tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                const int64_t col0 = static_cast<int64_t>(e.c) + ch * 32;
+                if (col0 >= p.g.n) break;
+                const int64_t left = p.g.n - col0;
+                tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
+            }
         }
         tc_fence_before();
         __syncwarp();
@@ -206,7 +236,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_kernel(const __grid_co
     } else if (warp == 1) {
         if (lane == 0) mma_loop(sm, tmem_base, p.ws);
     } else {
-        ag_epilogue(p, sm, tmem_base, warp, lane);
+        ag_epilogue(p, sm, tmem_base, warp, lane, epoch);
     }
     engine_teardown(sm, warp, tmem_base);
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
@@ -219,11 +249,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_kernel(const __grid_co
 // pairs (both CTAs copy, then both build).
 
 // Loads this CTA's half of one stage: A rows [row0, row0+128) of shard s and
-// nslab 64-column slabs of B from column col0 (two for a 256-wide tile, one
-// for a column half), completing on the leader's full barrier.
+// B columns [col0, col0+128) of K block kb, completing on the leader's full barrier.
 __device__ __forceinline__ void ag2_load_half(const AgParams &p, const Smem2 &sm, const PipeState2 &ps, bool local,
-                                              int s, int64_t row0, int64_t col0, int nslab, int kb,
-                                              uint32_t leader_full) {
+                                              int s, int64_t row0, int64_t col0, int kb, uint32_t leader_full) {
     uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
     uint8_t *sb = sa + A2_BYTES;
     if (local)
@@ -231,7 +259,7 @@ __device__ __forceinline__ void ag2_load_half(const AgParams &p, const Smem2 &sm
     else
         tma_load_3d_pair(sa, &p.tmA_gath, leader_full, kb * BK, static_cast<int32_t>(row0), s);
     tma_load_2d_pair(sb, &p.tmB, leader_full, static_cast<int32_t>(col0), kb * BK);
-    if (nslab > 1) tma_load_2d_pair(sb + 64 * BK * 2, &p.tmB, leader_full, static_cast<int32_t>(col0 + 64), kb * BK);
+    tma_load_2d_pair(sb + 64 * BK * 2, &p.tmB, leader_full, static_cast<int32_t>(col0 + 64), kb * BK);
 }
 
 __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm, uint32_t epoch, uint32_t rank) {
@@ -263,9 +291,8 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             if (failed(p.ws)) break;
             const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
             if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
-            int s, i2, c;
-            const int width = ag_decode_tile(p.g, static_cast<int>(t), s, i2, c) == K_TILE ? BN : BN / 2;
-            const int col0 = c * width;
+            const AgTileWork w = ag_tile_work(p, static_cast<int>(t));
+            const int s = w.s, i2 = w.i;
             const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
             const int pc = 2 * i2;  // the leader's 128-row piece
             if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
@@ -282,20 +309,19 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             ++nrec;
             SchedEntry e;
             fill_done(e);
-            e.kind = K_TILE; e.a = s; e.b = i2; e.c = col0; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
-            e.slot = slot; e.nmma = width;
+            e.kind = K_TILE; e.a = s; e.b = i2; e.c = w.col0; e.d = w.kb0; e.nstage = w.nk;
+            e.ticket = static_cast<int32_t>(t); e.slot = slot; e.x1 = w.slot;
             if (!ring2_push(sm, rs, e, p.ws)) break;
-            const int nslab = width / 128;  // B slabs per CTA: each CTA holds half of the tile's columns
             const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
             bool ok = true;
-            for (int kb = 0; kb < p.nkb; ++kb) {
+            for (int kk = 0; kk < w.nk; ++kk) {
                 if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
                     set_error(p.ws, KOSMOS_ERR_DEVICE, t);
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * (A2_BYTES + nslab * (64 * BK * 2)));
-                ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM, col0, nslab, kb,
+                mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * STAGE2_BYTES);
+                ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM, w.col0, w.kb0 + kk,
                               my_full0 + ps.stage * 8);
                 ps.advance();
             }
@@ -311,7 +337,6 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             if (!ring2_take(sm, rs, false, e, p.ws, false)) break;
             if (e.kind == K_DONE) break;
             const int s = e.a, i2 = e.b;
-            const int width = e.nmma > 0 ? e.nmma : BN;
             const int pc = 2 * i2 + 1;  // the peer's 128-row piece
             if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
                 if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch), p.wait_limit_ns,
@@ -327,7 +352,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
                     break;
                 }
                 ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM + HBM_ROWS,
-                              static_cast<int64_t>(e.c) + width / 2, width / 128, kb, leader_full0 + ps.stage * 8);
+                              static_cast<int64_t>(e.c) + HBN, e.d + kb, leader_full0 + ps.stage * 8);
                 ps.advance();
             }
             if (!ok) break;
@@ -336,7 +361,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
 }
 
 __device__ __forceinline__ void ag2_epilogue(const AgParams &p, const Smem2 &sm, uint32_t tmem_base, int warp, int lane,
-                                             uint32_t rank) {
+                                             uint32_t rank, uint32_t epoch) {
     const bool leader = rank == 0;
     const int grp = warp & 3;
     const int row = grp * 32 + lane;
@@ -353,17 +378,22 @@ __device__ __forceinline__ void ag2_epilogue(const AgParams &p, const Smem2 &sm,
         }
         tc_fence_after();
         const int s = e.a, i2 = e.b;
-        const int width = e.nmma > 0 ? e.nmma : BN;
         const int64_t rloc = static_cast<int64_t>(i2) * PBM + rank * HBM_ROWS + row;
         const bool valid = rloc < p.g.m;
         __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + (valid ? rloc : 0)) * p.g.n;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
+        if (e.x1 >= 0) {  // one K half of a split tile: this CTA's 128 rows
+            const int64_t cs = static_cast<int64_t>(e.x1) * 2 + rank;
+            khalf_epilogue(taddr, valid, yrow, e.c, p.g.n, p.kpart + cs * (BM * BN / 4), &p.ksync[cs * 2],
+                           &p.ksync[cs * 2 + 1], epoch, p.ws, p.wait_limit_ns, e.ticket, row, sm.tmem_slot + 1);
+        } else {
 #pragma unroll 1
-        for (int ch = 0; ch < width / 32; ++ch) {
-            const int64_t col0 = static_cast<int64_t>(e.c) + ch * 32;
-            if (col0 >= p.g.n) break;
-            const int64_t left = p.g.n - col0;
-            tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                const int64_t col0 = static_cast<int64_t>(e.c) + ch * 32;
+                if (col0 >= p.g.n) break;
+                const int64_t left = p.g.n - col0;
+                tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
+            }
         }
         acc_release(sm, acc, leader, lane);
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
@@ -392,7 +422,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_pair_kernel(const __gr
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) mma2_loop(sm, tmem_base, p.ws);
     } else {
-        ag2_epilogue(p, sm, tmem_base, warp, lane, rank);
+        ag2_epilogue(p, sm, tmem_base, warp, lane, rank, epoch);
     }
     engine2_teardown(sm, warp, tmem_base);
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
@@ -448,10 +478,12 @@ kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     for (int r = 0; r < L.P; ++r) p.x_src[r] = static_cast<const uint8_t *>(L.x[r]);
     p.x_gath = static_cast<uint8_t *>(L.x_gathered);
     p.y = static_cast<__nv_bfloat16 *>(L.y);
-    const AgWsLayout W = ag_ws_layout(p.g, L.trace != 0);
+    const AgWsLayout W = ag_ws_layout(p.g, L.trace != 0, L.n_slots);
     uint8_t *ws = static_cast<uint8_t *>(L.ws);
     p.ws = reinterpret_cast<WsHeader *>(ws);
     p.flags = reinterpret_cast<uint32_t *>(ws + W.flags_off);
+    p.ksync = reinterpret_cast<uint32_t *>(ws + W.ksync_off);
+    p.kpart = reinterpret_cast<float4 *>(ws + W.kpart_off);
     p.trace = L.trace ? reinterpret_cast<TraceRec *>(ws + W.trace_off) : nullptr;
     p.nkb = static_cast<int>(L.k / BK);
     p.sched = L.sched;

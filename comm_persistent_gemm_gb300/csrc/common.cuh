@@ -197,13 +197,22 @@ KOS_HD void rs_decode_reduce(const RsGeom &g, int t, int &band, int &tcol) {
 }
 
 // ---------------------------------------------------------------- workspace layouts
+// K-split tail tiles: each split tile owns a slot with, per CTA of the tile
+// engine (two for an SM pair), an arrival counter, a ready flag and an fp32
+// partial of 128 rows x 256 columns, stored as [64 column quads][128 rows] of float4.
+constexpr int MAX_SPLIT_SLOTS = 256;
+constexpr size_t KPART_CTA_BYTES = static_cast<size_t>(BM) * BN * 4;
 struct AgWsLayout {
-    size_t flags_off, trace_off, total;
+    size_t flags_off, ksync_off, kpart_off, trace_off, total;
 };
-inline AgWsLayout ag_ws_layout(const AgGeom &g, bool trace) {
+inline AgWsLayout ag_ws_layout(const AgGeom &g, bool trace, int n_slots = 0) {
     AgWsLayout L;
     L.flags_off = 256;
     size_t off = L.flags_off + static_cast<size_t>(align_up(static_cast<int64_t>(g.P) * g.pieces * 4, 256));
+    L.ksync_off = off;
+    off += static_cast<size_t>(align_up(static_cast<int64_t>(n_slots) * 2 * 2 * 4, 256));
+    L.kpart_off = off;
+    off += static_cast<size_t>(n_slots) * 2 * KPART_CTA_BYTES;
     L.trace_off = off;
     if (trace) off += static_cast<size_t>(MAX_CTAS) * TRACE_CAP * sizeof(TraceRec);
     L.total = off;

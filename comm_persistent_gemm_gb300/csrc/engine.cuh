@@ -424,6 +424,82 @@ __device__ __forceinline__ void tmem_row_chunk_to_bf16(uint32_t taddr, bool row_
     }
 }
 
+// Epilogue of one CTA's 128 x 256 accumulator for a tile computed as two K
+// halves by two entries (possibly on two engines).  The first of the two to
+// arrive stores its fp32 partial in the slot and releases the slot's flag;
+// the second waits for the flag, adds the partial to its own accumulator
+// (fp32 addition is commutative, so the result does not depend on which half
+// finished first), writes Y and returns the slot's counter to zero.  Called
+// by all 128 epilogue threads; thread `row` owns accumulator row `row`;
+// xword points to two shared-memory words.  Returns false after a device error.
+__device__ __forceinline__ bool khalf_epilogue(uint32_t taddr, bool row_valid, __nv_bfloat16 *yrow, int64_t col0,
+                                               int64_t n, float4 *part, uint32_t *cnt, uint32_t *flag,
+                                               uint32_t epoch, WsHeader *ws, uint64_t limit_ns, int64_t entry,
+                                               int row, uint32_t *xword) {
+    const bool lead = row == 0;
+    if (lead) xword[0] = atomicAdd(cnt, 1u);
+    named_bar_sync(1, NUM_EPI_THREADS);
+    const uint32_t order = *reinterpret_cast<volatile uint32_t *>(&xword[0]);
+    if (order == 0) {
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + ch * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                part[(ch * 8 + v) * BM + row] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                            __uint_as_float(r[4 * v + 2]),
+                                                            __uint_as_float(r[4 * v + 3]));
+        }
+        __threadfence();
+        named_bar_sync(1, NUM_EPI_THREADS);
+        if (lead) st_release_gpu(flag, epoch + 1u);
+        return true;
+    }
+    if (lead) {
+        const bool ok = wait_flag_eq(ws, flag, epoch + 1u, limit_ns, entry);
+        st_relaxed_gpu(cnt, 0u);
+        xword[1] = ok ? 1u : 0u;
+    }
+    named_bar_sync(1, NUM_EPI_THREADS);
+    if (*reinterpret_cast<volatile uint32_t *>(&xword[1]) == 0u) return false;
+    // 64 columns (16 float4 of the partner's partial) per pass; the next
+    // pass's loads are in flight while this one is combined
+    float4 pv[2][16];
+#pragma unroll
+    for (int v = 0; v < 16; ++v) pv[0][v] = __ldcg(&part[v * BM + row]);
+#pragma unroll
+    for (int ps = 0; ps < BN / 64; ++ps) {
+        if (ps + 1 < BN / 64) {
+#pragma unroll
+            for (int v = 0; v < 16; ++v) pv[(ps + 1) & 1][v] = __ldcg(&part[((ps + 1) * 16 + v) * BM + row]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int ch = ps * 2 + cc;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + ch * 32, r);
+            tmem_ld_wait();
+            const int64_t c0 = col0 + ch * 32;
+            if (!row_valid || c0 >= n) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (c0 + q * 8 >= n) break;
+                const float4 a = pv[ps & 1][cc * 8 + 2 * q];
+                const float4 b = pv[ps & 1][cc * 8 + 2 * q + 1];
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(r[q * 8 + 0]) + a.x, __uint_as_float(r[q * 8 + 1]) + a.y);
+                v.y = pack_bf16x2(__uint_as_float(r[q * 8 + 2]) + a.z, __uint_as_float(r[q * 8 + 3]) + a.w);
+                v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]) + b.x, __uint_as_float(r[q * 8 + 5]) + b.y);
+                v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]) + b.z, __uint_as_float(r[q * 8 + 7]) + b.w);
+                *reinterpret_cast<uint4 *>(yrow + c0 + q * 8) = v;
+            }
+        }
+    }
+    return true;
+}
+
 __device__ __forceinline__ TraceRec *trace_rec(TraceRec *base, int cta, int slot) {
     return (base != nullptr && slot >= 0 && slot < TRACE_CAP) ? base + static_cast<int64_t>(cta) * TRACE_CAP + slot
                                                               : nullptr;

@@ -182,6 +182,18 @@ int resolve_comm(const kosmos_opts &o, int grid, int P, bool fixed) {
     return n;
 }
 
+}  // namespace
+
+int kosmos::ag_split_slots(int P, int64_t m, int64_t n, int dtype, const kosmos_opts &o) {
+    if (dtype != KOSMOS_BF16 || o.tail_split == 0) return 0;
+    int64_t s = ag_geom(P, m, 64, n, BM).n_full;  // 128-row tiles: the most tiles either engine has
+    if (s > MAX_SPLIT_SLOTS) s = MAX_SPLIT_SLOTS;
+    if (o.tail_split > 0 && o.tail_split < s) s = o.tail_split;
+    return static_cast<int>(s);
+}
+
+namespace {
+
 // Launch shape of one all-gather + GEMM call: grid, tile engine, initial
 // movers (CTAs) and the tile-rail split.
 struct AgPlan {
@@ -191,7 +203,7 @@ struct AgPlan {
     int64_t n_split;
 };
 
-kosmos_status ag_plan(int P, int64_t m, int64_t n, int dtype, const kosmos_opts &o, AgPlan &pl) {
+kosmos_status ag_plan(int P, int64_t m, int64_t k, int64_t n, int dtype, const kosmos_opts &o, AgPlan &pl) {
     int grid = grid_for(o);
     if (grid < 1) return KOSMOS_ERR_CUDA;
     int pair = (dtype == KOSMOS_BF16 && o.cta_pair != 0) ? 1 : 0;
@@ -210,7 +222,7 @@ kosmos_status ag_plan(int P, int64_t m, int64_t n, int dtype, const kosmos_opts 
     int n_comm = resolve_comm(o, grid, P, o.sched == KOSMOS_SCHED_FIXED);
     if (pair && n_comm > grid - 2) n_comm = grid - 2;  // keep a builder pair
     int64_t split = 0;
-    if (dtype == KOSMOS_BF16) {
+    if (dtype == KOSMOS_BF16 && k >= 2 * BK) {  // both K halves need at least one K block
         if (o.tail_split >= 0) {
             split = o.tail_split;
         } else {  // one wave: every tile engine that builds
@@ -219,6 +231,7 @@ kosmos_status ag_plan(int P, int64_t m, int64_t n, int dtype, const kosmos_opts 
         }
         const int64_t n_full = ag_geom(P, m, 64, n, pair ? PBM : BM).n_full;
         if (split > n_full) split = n_full;
+        if (split > ag_split_slots(P, m, n, dtype, o)) split = ag_split_slots(P, m, n, dtype, o);
         if (split < 0) split = 0;
     }
     pl.grid = grid;
@@ -254,7 +267,7 @@ size_t kosmos_workspace_bytes(int op, int P, int64_t m, int64_t n, int64_t k, in
     const kosmos_opts o = resolve_opts(opts);
     if (P < 1 || P > KOSMOS_MAX_P || m < 1 || n < 1 || k < 1) return 0;
     if (op == KOSMOS_OP_AG_GEMM) {
-        size_t total = ag_ws_layout(ag_geom(P, m, k, n), o.trace != 0).total;
+        size_t total = ag_ws_layout(ag_geom(P, m, k, n), o.trace != 0, ag_split_slots(P, m, n, dtype, o)).total;
         if (dtype == KOSMOS_MXFP8_E4M3) {
             if (k % 128) return 0;
             total += ag_mxfp8_scale_bytes(P, m, k);  // gathered scale blocks
@@ -296,7 +309,7 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_AG_GEMM, P, m_per_shard, n, k, dtype, &o))
         return KOSMOS_ERR_WORKSPACE;
     AgPlan pl;
-    const kosmos_status ps = ag_plan(P, m_per_shard, n, dtype, o, pl);
+    const kosmos_status ps = ag_plan(P, m_per_shard, k, n, dtype, o, pl);
     if (ps != KOSMOS_OK) return ps;
     AgLaunch L;
     memset(&L, 0, sizeof(L));
@@ -310,19 +323,20 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     L.n_comm = pl.n_comm;
     L.pair = pl.pair;
     L.n_split = pl.n_split;
+    L.n_slots = ag_split_slots(P, m_per_shard, n, dtype, o);
     L.trace = o.trace; L.grid = pl.grid; L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
     L.plain_launch = o.plain_launch;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == KOSMOS_BF16 ? launch_ag_bf16(L, s) : launch_ag_mxfp8(L, s);
 }
 
-int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t n, int dtype, const kosmos_opts *opts,
+int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t k, int64_t n, int dtype, const kosmos_opts *opts,
                         int64_t *tail_split, int *tile_m) {
-    if (P < 1 || P > KOSMOS_MAX_P || m_per_shard < 1 || n < 8) return -1;
+    if (P < 1 || P > KOSMOS_MAX_P || m_per_shard < 1 || n < 8 || k < BK) return -1;
     if (dtype != KOSMOS_BF16 && dtype != KOSMOS_MXFP8_E4M3) return -1;
     const kosmos_opts o = resolve_opts(opts);
     AgPlan pl;
-    if (ag_plan(P, m_per_shard, n, dtype, o, pl) != KOSMOS_OK) return -1;
+    if (ag_plan(P, m_per_shard, k, n, dtype, o, pl) != KOSMOS_OK) return -1;
     if (tail_split) *tail_split = pl.n_split;
     if (tile_m) *tile_m = pl.pair ? PBM : BM;
     return 0;
@@ -477,9 +491,8 @@ kosmos_status kosmos_trace_info(int op, int P, int64_t m, int64_t n, int64_t k, 
     const kosmos_opts o = resolve_opts(opts);
     if (!o.trace || ws == nullptr) return KOSMOS_ERR_INVALID_ARG;
     size_t off = 0;
-    (void)dtype;
     if (op == KOSMOS_OP_AG_GEMM)
-        off = ag_ws_layout(ag_geom(P, m, k, n), true).trace_off;
+        off = ag_ws_layout(ag_geom(P, m, k, n), true, ag_split_slots(P, m, n, dtype, o)).trace_off;
     else if (op == KOSMOS_OP_GEMM_RS)
         off = rs_ws_layout(rs_geom(P, m, k, n), true).trace_off;
     else

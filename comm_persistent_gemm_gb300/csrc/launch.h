@@ -27,7 +27,8 @@ struct AgLaunch {
     int grid;
     int pair;       // 1: SM-pair (cta_group::2) tiles, grid = 2 x clusters
     int plain_launch;
-    int64_t n_split;  // trailing tiles of the tile rail run as column halves
+    int64_t n_split;  // trailing tiles of the tile rail run as two K halves
+    int n_slots;      // K-split slots in the workspace (>= n_split)
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -90,6 +91,8 @@ kosmos_status launch_persistent_pairs(const void *func, void *params, int grid, 
 int max_pair_ctas(const void *func, int smem_bytes);
 
 kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream);
+// K-split slots a workspace holds for these sizes and options (0 without a tail split).
+int ag_split_slots(int P, int64_t m, int64_t n, int dtype, const kosmos_opts &o);
 kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream);
 size_t ag_mxfp8_scale_bytes(int P, int64_t m, int64_t k);
 kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream);

@@ -60,6 +60,7 @@ extern "C" KOSMOS_API kosmos_status kosmos_ag_gemm_noalloc(const void *const *x_
     kosmos_default_opts(&o);
     if (opts) o = *opts;
     if (o.trace) return KOSMOS_ERR_UNSUPPORTED;  // the trace ring does not fit the static scratch
+    o.tail_split = 0;                            // nor do the K-split partials
     const size_t need = kosmos_workspace_bytes(KOSMOS_OP_AG_GEMM, P, m_per_shard, n, k, dtype, &o);
     if (need == 0) return KOSMOS_ERR_INVALID_ARG;
     if (need > static_cast<size_t>(KOSMOS_STATIC_WS_BYTES)) return KOSMOS_ERR_WORKSPACE;

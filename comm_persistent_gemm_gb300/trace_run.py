@@ -85,6 +85,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", required=True)
     ap.add_argument("--only", default="ag,rs,moe")
+    ap.add_argument("--tail-split", type=int, default=None, help="all-gather: kosmos_opts.tail_split")
     a = ap.parse_args(argv)
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     if root not in sys.path:
@@ -97,8 +98,10 @@ def main(argv=None):
     runs = []
     only = set(a.only.split(","))
     if "ag" in only:
-        runs += [("ag_self", _trace_ag, K.opts(trace=1)),
-                 ("ag_fixed19", _trace_ag, K.opts(trace=1, sched=K.SCHED_FIXED, fixed_comm_ctas=-(-sms // 8)))]
+        ts = a.tail_split
+        runs += [("ag_self", _trace_ag, K.opts(trace=1, tail_split=ts)),
+                 ("ag_fixed19", _trace_ag, K.opts(trace=1, sched=K.SCHED_FIXED, fixed_comm_ctas=-(-sms // 8),
+                                                  tail_split=ts))]
     if "rs" in only:
         runs += [("rs_band", _trace_rs, K.opts(trace=1)), ("rs_row", _trace_rs, K.opts(trace=1, order=K.ORDER_ROW))]
     if "moe" in only:

@@ -112,9 +112,11 @@ typedef struct kosmos_opts {
                                  KOSMOS_ERR_TIMEOUT. */
     uint64_t wait_limit_ns;   /* bound on every readiness wait; 0 = 2e9 (2 s) */
     uint64_t inject;          /* KOSMOS_INJECT_* bits | (argument << 32); 0 = none */
-    int64_t tail_split;       /* bf16 AG: the last tail_split tiles of the tile rail run as two column
-                                 halves each; 0 = none (default); -1 = one wave (the number of tile
-                                 engines, i.e. SM pairs or SMs, that build) */
+    int64_t tail_split;       /* bf16 AG: the last tail_split tiles of the tile rail run as two K halves
+                                 each (two entries whose fp32 partials are added through the
+                                 workspace); 0 = none; -1 = one wave (the number of tile engines,
+                                 i.e. SM pairs or SMs, that build).  At most 256; needs k >= 128.
+                                 The workspace holds 256 KB per split tile. */
 } kosmos_opts;
 
 /* Fills *opts with the defaults (SELF, band order, all SMs, no trace). */
@@ -165,12 +167,12 @@ KOSMOS_API kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void 
                              void *x_gathered, void *y, void *ws, size_t ws_bytes,
                              const kosmos_opts *opts, void *stream);
 
-/* The tile-rail split (number of trailing tiles run as column halves) and
+/* The tile-rail split (number of trailing tiles run as two K halves) and
  * the tile height (256: SM pairs, 128: one SM per tile) that kosmos_ag_gemm
  * would use for these sizes and options on the current device; the values
  * to pass to kosmos_rail_decode.  Returns 0, or -1 for invalid arguments. */
-KOSMOS_API int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t n, int dtype, const kosmos_opts *opts,
-                                   int64_t *tail_split, int *tile_m);
+KOSMOS_API int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t k, int64_t n, int dtype,
+                                   const kosmos_opts *opts, int64_t *tail_split, int *tile_m);
 
 /*
  * GEMM + reduce-scatter  (explainer, "Start with the problem": scatter and
@@ -317,8 +319,8 @@ KOSMOS_API kosmos_status kosmos_trace_info(int op, int P, int64_t m, int64_t n, 
  *   op GEMM_RS: rail 0 = tiles of rank `rank` {2, chunk, band, tile_col};
  *               rail 1 = reductions of rank `rank` {3, rank, band, tile_col}.
  * tile_m = tile (band) height in rows: 128 (one SM per tile) or 256 (SM pairs).
- * split = AG tile rail only: trailing tiles run as column halves (entries
- * {10, shard, tile-row, half-column}); ignored for GEMM+RS.
+ * split = AG tile rail only: trailing tiles run as two K halves (entries
+ * {10, shard, tile-row, 2 * tile-col + half}); ignored for GEMM+RS.
  * out is HOST memory of max_entries*4 int32; returns the rail length or -1.
  * Runs the same decode functions the kernels use, compiled for the host. */
 KOSMOS_API int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int rank, int rail,

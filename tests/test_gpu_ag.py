@@ -82,33 +82,53 @@ def test_ag_mover_counts(K, orc, n_comm0, mode):
 @pytest.mark.parametrize("split", [-1, 3, 10**6])
 @pytest.mark.parametrize("P,m,k,n", [(3, 200, 192, 264), (2, 300, 128, 520), (4, 128, 320, 512)])
 def test_ag_tail_split(K, orc, P, m, k, n, split, mode):
-    """Tiles run as column halves (none, the last 3, all of them): same
-    results, and bit-identical to the unsplit rail (each output element keeps
-    its K order)."""
+    """The last tiles run as two K halves (one wave, the last 3, all of
+    them): results within tolerance of the oracle and of the unsplit rail,
+    bit-identical on reruns (the two fp32 halves are added once, in either
+    order: the sum is the same)."""
     inp = ag_inputs(P, m, k, n, seed=4000 + P * m + n, var_w=1.0 / k)
     o = K.opts(cta_pair=PAIR[mode], tail_split=split)
+    assert K.ag_tile_plan(P, m, k, n, o)[0] > 0
     _check_full(orc, K, inp, o)
     _, _, a, _ = _run(K, inp, o)
     _, _, b, _ = _run(K, inp, K.opts(cta_pair=PAIR[mode], tail_split=0))
-    assert torch.equal(a[0], b[0])
+    assert rel_err(bf16_tensor_to_f64(a[0]), bf16_tensor_to_f64(b[0])) <= TOL
+
+
+@pytest.mark.parametrize("mode", list(PAIR))
+def test_ag_tail_split_full_size(K, orc, mode):
+    """One wave of K-split tiles on the 8-rank workload: sampled rows against
+    the oracle (the split tiles are the last ones: the last shard's rows)."""
+    w = WORKLOADS["ag_bf16_p8"]
+    inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
+    o = K.opts(cta_pair=PAIR[mode], tail_split=-1)
+    xs, xg, outs, _ = _run(K, inp, o, reps=2)
+    rows = np.unique(np.concatenate([sample_indices(w.P * w.m, 16, seed=5),
+                                     (w.P - 1) * w.m + np.arange(0, w.m, 97), [w.P * w.m - 1]]))
+    ref = orc.ag_gemm([bf16_bits(x) for x in inp["x"]], bf16_bits(inp["w"]), rows=rows)
+    got = bf16_tensor_to_f64(outs[0][torch.from_numpy(rows).cuda()])
+    assert rel_err(got, ref) <= TOL, rel_err(got, ref)
+    assert torch.equal(outs[0], outs[1])
 
 
 def test_ag_tile_plan_split(K):
     """No split by default; tail_split = -1 is one wave: every tile engine that builds."""
     sms = K.num_sms()
-    assert K.ag_tile_plan(8, 1024, 3584, K.opts()) == (0, 256)
-    sp, tm = K.ag_tile_plan(8, 1024, 3584, K.opts(tail_split=-1))
+    assert K.ag_tile_plan(8, 1024, 8192, 3584, K.opts(tail_split=0)) == (0, 256)
+    assert K.ag_tile_plan(8, 1024, 64, 3584, K.opts(tail_split=-1))[0] == 0  # one K block: nothing to split
+    sp, tm = K.ag_tile_plan(8, 1024, 8192, 3584, K.opts(tail_split=-1))
     assert tm == 256 and 1 <= sp <= sms // 2  # one per co-resident SM pair
     if sms == 152:
         assert sp == 76
-    assert K.ag_tile_plan(8, 1024, 3584, K.opts(tail_split=10**6))[0] == 8 * 4 * 14  # clamped to the tiles
-    assert K.ag_tile_plan(8, 1024, 3584, K.opts(tail_split=5))[0] == 5
-    sp1, tm1 = K.ag_tile_plan(8, 1024, 3584, K.opts(cta_pair=0, tail_split=-1))
-    assert tm1 == 128 and sp1 == min(sms, 8 * 8 * 14)
-    sp2, _ = K.ag_tile_plan(8, 1024, 3584, K.opts(cta_pair=0, sched=K.SCHED_FIXED, fixed_comm_ctas=10,
-                                                   tail_split=-1))
+    assert K.ag_tile_plan(8, 1024, 8192, 3584, K.opts(tail_split=10**6))[0] == 256  # the slot limit
+    assert K.ag_tile_plan(2, 256, 8192, 512, K.opts(tail_split=10**6))[0] == 2 * 1 * 2  # clamped to the tiles
+    assert K.ag_tile_plan(8, 1024, 8192, 3584, K.opts(tail_split=5))[0] == 5
+    sp1, tm1 = K.ag_tile_plan(8, 1024, 8192, 3584, K.opts(cta_pair=0, tail_split=-1))
+    assert tm1 == 128 and sp1 == min(sms, 8 * 8 * 14, 256)
+    sp2, _ = K.ag_tile_plan(8, 1024, 8192, 3584, K.opts(cta_pair=0, sched=K.SCHED_FIXED, fixed_comm_ctas=10,
+                                                         tail_split=-1))
     assert sp2 == sms - 10
-    assert K.ag_tile_plan(8, 1024, 3584, K.opts(tail_split=-1), dtype=K.MXFP8_E4M3)[0] == 0
+    assert K.ag_tile_plan(8, 1024, 8192, 3584, K.opts(tail_split=-1), dtype=K.MXFP8_E4M3)[0] == 0
 
 
 def test_ag_few_ctas(K, orc):
@@ -161,7 +181,7 @@ def test_ag_trace_every_entry_once(K, orc, mode):
     o = K.opts(trace=1, cta_pair=PAIR[mode])
     xs, xg, outs, ws = _run(K, inp, o)
     recs = K.trace_records(K.OP_AG_GEMM, 4, 512, 512, 128, ws, o)
-    split, tm = K.ag_tile_plan(4, 512, 512, o)
+    split, tm = K.ag_tile_plan(4, 512, 128, 512, o)
     assert tm == (256 if PAIR[mode] else 128)
     tr, tl = orc.rail_ag(4, 512, 512, TR=tm, XS=split)
     tiles = np.sort(recs["ticket"][recs["kind"] == 2])
@@ -188,7 +208,7 @@ def test_ag_dropped_transfer_times_out_then_recovers(K, orc):
     st, entry = K.status_sync(ws)
     assert st == K.ERR_TIMEOUT
     # transfer 0 is part 0 of shard 1's piece 0; the first tile of shard 1 waits for it
-    split, tm = K.ag_tile_plan(P, m, n, o)
+    split, tm = K.ag_tile_plan(P, m, k, n, o)
     _, tl = orc.rail_ag(P, m, n, TR=tm, XS=split)
     assert entry == int(np.flatnonzero(tl[:, 1] == 1)[0])
     K.workspace_init(ws)
