@@ -511,44 +511,49 @@ ORC_EXPORT int64_t orc_rail_ag(int P, int64_t m, int64_t n, int R, int BN, int T
     return nt + nb;
 }
 
-/* Reduce-scatter rails for one rank r.
- * Tile rail of rank r: TILE(chunk c, band b, column tile j) over the whole
- * [m, n] partial of rank r.
- *   band order (order = 0): band b outermost, then column tile j, then chunk c
- *     [explainer, "Role switching only works": output produced band by band
- *     across every rank's chunk; the order inside a band is not given: column
- *     tile outer, chunk inner keeps the tiles that share one W_r column slice
- *     adjacent];
- *   row order  (order = 1): chunk c, then band b, then j (global row order).
+/* Reduce-scatter rails.
+ * Tile rail (one rail for all emulated ranks): TILE(rank q, chunk c, band b,
+ * column tile j) = rows [c*m/P + b*R, +R) x columns [j*BN, +BN) of rank q's
+ * partial X_q . W_q, written as {2, q*P + c, b, j}.
+ *   band order (order = 0): band b outermost, then rank q, then column tile j,
+ *     then chunk c [explainer, "Role switching only works": every rank
+ *     produces its output band by band across all chunks; the order inside a
+ *     band is not given: one rank at a time, column tile outer and chunk
+ *     inner keeps the tiles that read one W_q column slice adjacent and one
+ *     band of X_q in use, so the operands of the tiles in flight fit in L2;
+ *     with all ranks of one GPU interleaved tile by tile they did not];
+ *   row order  (order = 1): chunk c, then band b, then rank q, then j (global
+ *     row order).
  * Reduce rail of rank r: REDUCE(c = r, band b, column tile j), b outer, j inner.
  * Bands are R rows of a chunk of m/P rows. */
 ORC_EXPORT int64_t orc_rail_rs(int P, int64_t m, int64_t n, int R, int BN, int order, int rank,
                                int32_t *tile_out, int64_t *n_tile,
                                int32_t *reduce_out, int64_t *n_reduce) {
-    (void)rank;
     if (m % P) return -1;
     int64_t mc = m / P, bands = orc_cdiv(mc, R), tn = orc_cdiv(n, BN);
     int64_t nb = 0, nr = 0;
     if (order == 0) {
         for (int64_t b = 0; b < bands; b++)
-            for (int64_t j = 0; j < tn; j++)
-                for (int c = 0; c < P; c++) {
-                    if (tile_out) {
-                        int32_t *e = tile_out + 4 * nb;
-                        e[0] = ORC_TILE; e[1] = c; e[2] = (int32_t)b; e[3] = (int32_t)j;
+            for (int q = 0; q < P; q++)
+                for (int64_t j = 0; j < tn; j++)
+                    for (int c = 0; c < P; c++) {
+                        if (tile_out) {
+                            int32_t *e = tile_out + 4 * nb;
+                            e[0] = ORC_TILE; e[1] = q * P + c; e[2] = (int32_t)b; e[3] = (int32_t)j;
+                        }
+                        nb++;
                     }
-                    nb++;
-                }
     } else {
         for (int c = 0; c < P; c++)
             for (int64_t b = 0; b < bands; b++)
-                for (int64_t j = 0; j < tn; j++) {
-                    if (tile_out) {
-                        int32_t *e = tile_out + 4 * nb;
-                        e[0] = ORC_TILE; e[1] = c; e[2] = (int32_t)b; e[3] = (int32_t)j;
+                for (int q = 0; q < P; q++)
+                    for (int64_t j = 0; j < tn; j++) {
+                        if (tile_out) {
+                            int32_t *e = tile_out + 4 * nb;
+                            e[0] = ORC_TILE; e[1] = q * P + c; e[2] = (int32_t)b; e[3] = (int32_t)j;
+                        }
+                        nb++;
                     }
-                    nb++;
-                }
     }
     for (int64_t b = 0; b < bands; b++)
         for (int64_t j = 0; j < tn; j++) {

@@ -3,8 +3,8 @@ order follows consumer demand (the explainer's queue-order paragraph):
   * AG: remote transfers are ordered by the first tile that consumes them, the
     local shard's tiles come first, and no tile's input is transferred after a
     later tile's input;
-  * RS band order: every rank finishes band b of every chunk before band b+1;
-    row order finishes chunk c before chunk c+1."""
+  * RS band order: band b of every rank and chunk before band b+1, one rank
+    at a time inside a band; row order finishes chunk c before chunk c+1."""
 import numpy as np
 import pytest
 
@@ -41,31 +41,38 @@ def test_ag_rail_exactly_once_and_demand_order(orc, P, m, n, PR):
     assert all(int(s) == 0 for (_, s, _, _) in tr[len(remote):])
 
 
+@pytest.mark.parametrize("P,m,n", [(8, 8192, 8192), (3, 768, 520)])
 @pytest.mark.parametrize("order", [0, 1])
-def test_rs_rails(orc, order):
-    P, m, n = 8, 8192, 8192
+def test_rs_rails(orc, order, P, m, n):
     R, BN = 128, 256
-    bands = (m // P) // R
-    tn = n // BN
-    done_band = []
+    bands = -(-(m // P) // R)
+    tn = -(-n // BN)
+    tl = None
     for r in range(P):
-        tl, rd = orc.rail_rs(P, m, n, rank=r, order=order, R=R, BN=BN)
-        assert len(tl) == P * bands * tn and len({tuple(e) for e in tl}) == len(tl)
+        t_r, rd = orc.rail_rs(P, m, n, rank=r, order=order, R=R, BN=BN)
+        if tl is None:
+            tl = t_r
+        assert np.array_equal(t_r, tl)  # one tile rail for every rank
         assert len(rd) == bands * tn and len({tuple(e) for e in rd}) == len(rd)
         assert np.all(rd[:, 1] == r)
-        # reducer rail follows the order in which its chunk's tiles complete
-        pos = {(int(c), int(b), int(j)): t for t, (_, c, b, j) in enumerate(tl)}
-        mine = [pos[(r, int(b), int(j))] for (_, _, b, j) in rd]
-        assert mine == sorted(mine)
-        if order == 0:
-            # band-major: all chunks' band b before any band b+1
-            assert list(tl[:, 2]) == sorted(tl[:, 2])
-            done_band.append(pos[(r, 0, tn - 1)])
-        else:
-            assert list(tl[:, 1]) == sorted(tl[:, 1])
+        # the reduce rail follows the order in which its chunk's tiles complete:
+        # the last of the P partials of (chunk r, b, j) moves forward along it
+        pos = {(int(a), int(b), int(j)): t for t, (_, a, b, j) in enumerate(tl)}
+        last = [max(pos[(q * P + r, int(b), int(j))] for q in range(P)) for (_, _, b, j) in rd]
+        assert last == sorted(last)
+    q, c = tl[:, 1] // P, tl[:, 1] % P
+    assert len(tl) == P * P * bands * tn and len({tuple(e) for e in tl}) == len(tl)
+    assert set(q.tolist()) == set(range(P)) and set(c.tolist()) == set(range(P))
     if order == 0:
-        # every rank's first band completes within the first P*tn tickets
-        assert max(done_band) < P * tn
+        # band-major; inside a band one rank at a time; chunk innermost
+        key = tl[:, 2] * P + q
+        assert list(key) == sorted(key)
+        assert np.array_equal(c, np.tile(np.arange(P), len(tl) // P))
+        # every chunk's band 0 is complete after the first P*P*tn tickets
+        assert np.all(tl[: P * P * tn, 2] == 0)
+    else:
+        key = (c * bands + tl[:, 2]) * P + q
+        assert list(key) == sorted(key)
 
 
 def test_rs_rail_rejects_indivisible(orc):
