@@ -107,9 +107,9 @@ __global__ void rail_decode_kernel(int op, int P, int64_t m, int64_t n, int orde
         } else {
             const RsGeom g = rs_geom(P, m, 64, n, tile_m);
             if (rail == 0) {
-                int c, b, j;
-                rs_decode_tile(g, order, static_cast<int>(t), c, b, j);
-                e[0] = K_TILE; e[1] = c; e[2] = b; e[3] = j;
+                int q, c, b, j;
+                rs_decode_tile(g, order, static_cast<int>(t), q, c, b, j);
+                e[0] = K_TILE; e[1] = q * P + c; e[2] = b; e[3] = j;
             } else {
                 int b, j;
                 rs_decode_reduce(g, static_cast<int>(t), b, j);

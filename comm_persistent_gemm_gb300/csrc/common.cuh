@@ -158,7 +158,7 @@ struct RsGeom {
     int band_rows;    // 128 (one SM per tile) or 256 (an SM pair per tile)
     int bands;        // tile rows per chunk
     int tiles_n;
-    int n_tile;       // per rank: P * bands * tiles_n
+    int n_tile;       // one rail for all ranks: P * P * bands * tiles_n
     int n_reduce;     // per rank: bands * tiles_n
 };
 KOS_HD RsGeom rs_geom(int P, int64_t m, int64_t k, int64_t n, int band_rows = BM) {
@@ -168,26 +168,35 @@ KOS_HD RsGeom rs_geom(int P, int64_t m, int64_t k, int64_t n, int band_rows = BM
     g.band_rows = band_rows;
     g.bands = static_cast<int>(cdiv(g.mc, band_rows));
     g.tiles_n = static_cast<int>(cdiv(n, BN));
-    g.n_tile = P * g.bands * g.tiles_n;
+    g.n_tile = P * P * g.bands * g.tiles_n;
     g.n_reduce = g.bands * g.tiles_n;
     return g;
 }
-// Tile rail of one rank.  Band order: band, column, chunk (the P tiles that
-// share one W_r column slice are adjacent, so the slice is read from DRAM once
-// per band).  Row order: chunk, band, column.
-KOS_HD void rs_decode_tile(const RsGeom &g, int order, int t, int &chunk, int &band, int &tcol) {
+// Tile rail shared by all ranks: TILE(rank, chunk, band, column) of the
+// rank's partial.  Band order: band, rank, column, chunk (one rank's band at a
+// time, the P tiles that share one W_rank column slice adjacent: the tiles in
+// flight read one band of X_rank and a few W_rank slices, which stay in L2).
+// Row order: chunk, band, rank, column.
+KOS_HD void rs_decode_tile(const RsGeom &g, int order, int t, int &rank, int &chunk, int &band, int &tcol) {
     if (order == KOSMOS_ORDER_BAND) {
-        const int per_band = g.P * g.tiles_n;
+        const int per_rank = g.P * g.tiles_n;
+        const int per_band = g.P * per_rank;
         band = t / per_band;
-        const int r = t - band * per_band;
+        int r = t - band * per_band;
+        rank = r / per_rank;
+        r -= rank * per_rank;
         tcol = r / g.P;
         chunk = r - tcol * g.P;
     } else {
-        const int per_chunk = g.bands * g.tiles_n;
+        const int per_rank = g.tiles_n;
+        const int per_band = g.P * per_rank;
+        const int per_chunk = g.bands * per_band;
         chunk = t / per_chunk;
-        const int r = t - chunk * per_chunk;
-        band = r / g.tiles_n;
-        tcol = r - band * g.tiles_n;
+        int r = t - chunk * per_chunk;
+        band = r / per_band;
+        r -= band * per_band;
+        rank = r / per_rank;
+        tcol = r - rank * per_rank;
     }
 }
 // Reduce rail of rank r (its own chunk): band, then column.

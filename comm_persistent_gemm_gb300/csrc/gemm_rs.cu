@@ -2,19 +2,19 @@
 //
 // Y = sum_r X_r . W_r, scattered as P row chunks (KOSMOS explainer, paragraph
 // "Start with the problem": scatter and add the partial results).  All P
-// emulated ranks run in one launch: CTA c plays rank c mod P.  Per rank r two
-// rails:
-//   tile rail    TILE(chunk, band, col): the partial X_r . W_r on one 128x256
-//                tile, rounded to bf16 into rank r's partial buffer, then one
-//                release-increment of that output tile's arrival counter;
-//                band order (band, col, chunk) or the row-order ablation
-//                (chunk, band, col) (explainer, "Role switching only works");
-//   reduce rail  REDUCE(band, col) of rank r's own chunk: acquire counter == P,
-//                sum the P partials in rank order 0..P-1 in fp32, round once
-//                to bf16 into y_chunks[r].
-// Builders whose tile rail runs out join their rank's reduction (one-way,
-// explainer "KOSMOS removes the manager"); n_comm CTAs per rank reduce from
-// the start.
+// emulated ranks run in one launch.  Rails:
+//   tile rail    TILE(rank q, chunk, band, col), one rail for all ranks: the
+//                partial X_q . W_q on one tile, rounded to bf16 into rank q's
+//                partial buffer, then one release-increment of that output
+//                tile's arrival counter; band order (band, rank, col, chunk)
+//                or the row-order ablation (chunk, band, rank, col)
+//                (explainer, "Role switching only works");
+//   reduce rail  REDUCE(band, col) of rank r's own chunk, one per rank:
+//                acquire counter == P arrivals, sum the P partials in rank
+//                order 0..P-1 in fp32, round once to bf16 into y_chunks[r].
+// CTA c reduces for rank c mod P.  Builders whose tile rail runs out join
+// that rank's reduction (one-way, explainer "KOSMOS removes the manager");
+// n_comm CTAs per rank reduce from the start.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,10 +58,10 @@ __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
     while (true) {
         if (failed(p.ws)) break;
         if (!reducer) {
-            const uint32_t t = atomicAdd(&p.ws->tickets[rank], 1u);
+            const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
             if (t < static_cast<uint32_t>(p.g.n_tile)) {
-                int chunk, band, tcol;
-                rs_decode_tile(p.g, p.order, static_cast<int>(t), chunk, band, tcol);
+                int q, chunk, band, tcol;
+                rs_decode_tile(p.g, p.order, static_cast<int>(t), q, chunk, band, tcol);
                 int slot = -1;
                 if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
                     const int64_t now = static_cast<int64_t>(globaltimer());
@@ -71,7 +71,7 @@ __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
                 }
                 ++nrec;
                 SchedEntry e;
-                e.kind = K_TILE; e.a = chunk; e.b = band; e.c = tcol; e.d = rank; e.nstage = p.nkb;
+                e.kind = K_TILE; e.a = chunk; e.b = band; e.c = tcol; e.d = q; e.nstage = p.nkb;
                 e.ticket = static_cast<int32_t>(t); e.slot = slot; e.nmma = 0; e.x0 = e.x1 = e.x2 = 0;
                 if (!ring_push(sm, rs, e, p.ws)) break;
                 bool ok = true;
@@ -85,10 +85,10 @@ __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
                     uint8_t *sb = sa + A_STAGE_BYTES;
                     uint64_t *bar = &sm.full[ps.stage];
                     mbar_arrive_expect_tx(bar, STAGE_BYTES);
-                    tma_load_3d(sa, &p.tmX[rank], bar, kb * BK, band * BM, chunk);
+                    tma_load_3d(sa, &p.tmX[q], bar, kb * BK, band * BM, chunk);
 #pragma unroll
                     for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(sb + j * (64 * BK * 2), &p.tmW[rank], bar, tcol * BN + j * 64, kb * BK);
+                        tma_load_2d(sb + j * (64 * BK * 2), &p.tmW[q], bar, tcol * BN + j * 64, kb * BK);
                     ps.advance();
                 }
                 if (!ok) break;
@@ -308,7 +308,7 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
     const int pair = blockIdx.x / 2;
     const bool leader = crank == 0;
     // the first n_red pairs reduce from the start, each of their CTAs for rank (CTA index mod P);
-    // builder pairs build for rank (pair index mod P) and reduce for it after the switch
+    // builder pairs build tiles of any rank and reduce for rank (pair index mod P) after the switch
     const bool reducer_pair = (p.mode == RS_REDUCE_ONLY) || (p.mode == RS_FUSED && pair < p.n_red);
     const int rank = (reducer_pair && p.mode == RS_FUSED) ? static_cast<int>(blockIdx.x) % P : pair % P;
     PipeState2 ps;
@@ -318,10 +318,10 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
     if (leader) {
         const uint32_t my_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
         while (!reducer_pair && !failed(p.ws)) {
-            const uint32_t t = atomicAdd(&p.ws->tickets[rank], 1u);
+            const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
             if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
-            int chunk, band, tcol;
-            rs_decode_tile(p.g, p.order, static_cast<int>(t), chunk, band, tcol);
+            int q, chunk, band, tcol;
+            rs_decode_tile(p.g, p.order, static_cast<int>(t), q, chunk, band, tcol);
             int slot = -1;
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
                 const int64_t now = static_cast<int64_t>(globaltimer());
@@ -332,7 +332,7 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
             ++nrec;
             SchedEntry e;
             fill_done(e);
-            e.kind = K_TILE; e.a = chunk; e.b = band; e.c = tcol; e.d = rank; e.nstage = p.nkb;
+            e.kind = K_TILE; e.a = chunk; e.b = band; e.c = tcol; e.d = q; e.nstage = p.nkb;
             e.ticket = static_cast<int32_t>(t); e.slot = slot;
             if (!ring2_push(sm, rs, e, p.ws)) break;
             bool ok = true;
@@ -346,9 +346,9 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
                 uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
                 uint8_t *sb = sa + A2_BYTES;
                 const uint32_t fb = my_full0 + ps.stage * 8;
-                tma_load_3d_pair(sa, &p.tmX[rank], fb, kb * BK, band * PBM, chunk);
-                tma_load_2d_pair(sb, &p.tmW[rank], fb, tcol * BN, kb * BK);
-                tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[rank], fb, tcol * BN + 64, kb * BK);
+                tma_load_3d_pair(sa, &p.tmX[q], fb, kb * BK, band * PBM, chunk);
+                tma_load_2d_pair(sb, &p.tmW[q], fb, tcol * BN, kb * BK);
+                tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[q], fb, tcol * BN + 64, kb * BK);
                 ps.advance();
             }
             if (!ok) break;
@@ -362,7 +362,7 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
             SchedEntry e;
             if (!ring2_take(sm, rs, false, e, p.ws, false)) break;
             if (e.kind == K_DONE) break;
-            const int chunk = e.a, band = e.b, tcol = e.c;
+            const int chunk = e.a, band = e.b, tcol = e.c, q = e.d;
             bool ok = true;
             for (int kb = 0; kb < e.nstage; ++kb) {
                 if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
@@ -373,9 +373,9 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
                 uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
                 uint8_t *sb = sa + A2_BYTES;
                 const uint32_t fb = leader_full0 + ps.stage * 8;
-                tma_load_3d_pair(sa, &p.tmX[rank], fb, kb * BK, band * PBM + HBM_ROWS, chunk);
-                tma_load_2d_pair(sb, &p.tmW[rank], fb, tcol * BN + HBN, kb * BK);
-                tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[rank], fb, tcol * BN + HBN + 64, kb * BK);
+                tma_load_3d_pair(sa, &p.tmX[q], fb, kb * BK, band * PBM + HBM_ROWS, chunk);
+                tma_load_2d_pair(sb, &p.tmW[q], fb, tcol * BN + HBN, kb * BK);
+                tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[q], fb, tcol * BN + HBN + 64, kb * BK);
                 ps.advance();
             }
             if (!ok) break;

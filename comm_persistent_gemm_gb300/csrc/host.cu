@@ -533,9 +533,9 @@ int64_t kosmos_rail_decode(int op, int P, int64_t m, int64_t n, int order, int r
             for (int64_t t = 0; t < len && t < max_entries; ++t) {
                 int32_t *e = out + 4 * t;
                 if (rail == 0) {
-                    int c, b, j;
-                    rs_decode_tile(g, order, static_cast<int>(t), c, b, j);
-                    e[0] = K_TILE; e[1] = c; e[2] = b; e[3] = j;
+                    int q, c, b, j;
+                    rs_decode_tile(g, order, static_cast<int>(t), q, c, b, j);
+                    e[0] = K_TILE; e[1] = q * P + c; e[2] = b; e[3] = j;
                 } else {
                     int b, j;
                     rs_decode_reduce(g, static_cast<int>(t), b, j);

@@ -314,9 +314,11 @@ KOSMOS_API kosmos_status kosmos_trace_info(int op, int P, int64_t m, int64_t n, 
 
 /* Rail decode, for checking ticket order against an independent rail
  * builder.  Writes 4 int32 {kind, a, b, c} per ticket of one rail:
- *   op AG_GEMM: rail 0 = transfers {1, shard, piece, 0} (128-row pieces);
- *               rail 1 = tiles {2, shard, tile_row, tile_col}.  args: m = m_per_shard.
- *   op GEMM_RS: rail 0 = tiles of rank `rank` {2, chunk, band, tile_col};
+ *   op AG_GEMM: rail 0 = transfers {1, shard, piece, part} (128-row pieces in
+ *               32-row parts); rail 1 = tiles {2, shard, tile_row, tile_col}.
+ *               args: m = m_per_shard.
+ *   op GEMM_RS: rail 0 = the tile rail shared by all ranks
+ *               {2, q * P + chunk, band, tile_col} (rank q's partial);
  *               rail 1 = reductions of rank `rank` {3, rank, band, tile_col}.
  * tile_m = tile (band) height in rows: 128 (one SM per tile) or 256 (SM pairs).
  * split = AG tile rail only: trailing tiles run as two K halves (entries

@@ -122,14 +122,15 @@ def test_rs_trace_every_entry_once(K, orc, mode):
     recs = K.trace_records(K.OP_GEMM_RS, P, m, n, k, wsb, o)
     tl, rd = orc.rail_rs(P, m, n, rank=0, order=0, R=256 if PAIR[mode] else 128)
     red_pairs = (P + 1) // 2  # one reducer CTA per rank from the start, two ranks per pair
-    for kind, per_rank in ((2, len(tl)), (3, len(rd))):
-        r = recs[recs["kind"] == kind]
-        if PAIR[mode]:
-            rank_of = np.where(r["cta"] < 2 * red_pairs, r["cta"] % P, (r["cta"] // 2) % P)
-        else:
-            rank_of = r["cta"] % P
-        for q in range(P):
-            assert np.array_equal(np.sort(r["ticket"][rank_of == q]), np.arange(per_rank)), (kind, q)
+    # one tile rail for all ranks: every ticket exactly once
+    assert np.array_equal(np.sort(recs["ticket"][recs["kind"] == 2]), np.arange(len(tl)))
+    r = recs[recs["kind"] == 3]
+    if PAIR[mode]:
+        rank_of = np.where(r["cta"] < 2 * red_pairs, r["cta"] % P, (r["cta"] // 2) % P)
+    else:
+        rank_of = r["cta"] % P
+    for q in range(P):
+        assert np.array_equal(np.sort(r["ticket"][rank_of == q]), np.arange(len(rd))), q
     red = recs[recs["kind"] == 3]
     assert np.all(red["t_done"] >= red["t_ready"])
 
