@@ -248,18 +248,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_kernel(const __grid_co
 // tile waits for piece 2i, the peer's half for piece 2i + 1.  Movers are whole
 // pairs (both CTAs copy, then both build).
 
+constexpr bool AG_KEEP_W_IN_L2 = true;
+
 // Loads this CTA's half of one stage: A rows [row0, row0+128) of shard s and
-// B columns [col0, col0+128) of K block kb, completing on the leader's full barrier.
+// B columns [col0, col0+128) of K block kb, completing on the leader's full
+// barrier.  W is read by every tile row: its loads ask L2 to keep it (wpol).
 __device__ __forceinline__ void ag2_load_half(const AgParams &p, const Smem2 &sm, const PipeState2 &ps, bool local,
-                                              int s, int64_t row0, int64_t col0, int kb, uint32_t leader_full) {
+                                              int s, int64_t row0, int64_t col0, int kb, uint32_t leader_full,
+                                              uint64_t wpol) {
     uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
     uint8_t *sb = sa + A2_BYTES;
     if (local)
         tma_load_2d_pair(sa, &p.tmA_local, leader_full, kb * BK, static_cast<int32_t>(row0));
     else
         tma_load_3d_pair(sa, &p.tmA_gath, leader_full, kb * BK, static_cast<int32_t>(row0), s);
-    tma_load_2d_pair(sb, &p.tmB, leader_full, static_cast<int32_t>(col0), kb * BK);
-    tma_load_2d_pair(sb + 64 * BK * 2, &p.tmB, leader_full, static_cast<int32_t>(col0 + 64), kb * BK);
+    if (AG_KEEP_W_IN_L2) {
+        tma_load_2d_pair_hint(sb, &p.tmB, leader_full, static_cast<int32_t>(col0), kb * BK, wpol);
+        tma_load_2d_pair_hint(sb + 64 * BK * 2, &p.tmB, leader_full, static_cast<int32_t>(col0 + 64), kb * BK, wpol);
+    } else {
+        tma_load_2d_pair(sb, &p.tmB, leader_full, static_cast<int32_t>(col0), kb * BK);
+        tma_load_2d_pair(sb + 64 * BK * 2, &p.tmB, leader_full, static_cast<int32_t>(col0 + 64), kb * BK);
+    }
 }
 
 __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm, uint32_t epoch, uint32_t rank) {
@@ -270,6 +279,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
     PipeState2 ps;
     RingPair rs;
     int nrec = 0;
+    const uint64_t wpol = AG_KEEP_W_IN_L2 ? l2_policy_evict_last() : 0;
     if (mover) {
         if (!ag_mover_phase<NSTAGE2, STAGE2_BYTES>(p, sm.stages, sm.cbar, cphase, nrec) ||
             p.sched == KOSMOS_SCHED_FIXED) {
@@ -322,7 +332,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
                 }
                 mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * STAGE2_BYTES);
                 ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM, w.col0, w.kb0 + kk,
-                              my_full0 + ps.stage * 8);
+                              my_full0 + ps.stage * 8, wpol);
                 ps.advance();
             }
             if (!ok) break;
@@ -352,7 +362,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
                     break;
                 }
                 ag2_load_half(p, sm, ps, local, s, static_cast<int64_t>(i2) * PBM + HBM_ROWS,
-                              static_cast<int64_t>(e.c) + HBN, e.d + kb, leader_full0 + ps.stage * 8);
+                              static_cast<int64_t>(e.c) + HBN, e.d + kb, leader_full0 + ps.stage * 8, wpol);
                 ps.advance();
             }
             if (!ok) break;

@@ -219,12 +219,14 @@ __device__ __noinline__ bool stream_mover(uint8_t *stages, uint64_t *cbar, uint3
         }
     };
 
+    // sources are read once: let them leave L2 first
+    const uint64_t pol = l2_policy_evict_first();
     int64_t issued = 0, stored = 0;
     for (int b = 0; b < NS; ++b) {
         const uint8_t *src;
         if (!next_chunk(meta[b], src)) break;
         mbar_arrive_expect_tx(&cbar[b], meta[b].bytes);
-        bulk_g2s(stages + b * CH, src, meta[b].bytes, &cbar[b]);
+        bulk_g2s_hint(stages + b * CH, src, meta[b].bytes, &cbar[b], pol);
         ++issued;
     }
     while (stored < issued) {
@@ -261,7 +263,7 @@ __device__ __noinline__ bool stream_mover(uint8_t *stages, uint64_t *cbar, uint3
                 const int rb = static_cast<int>((stored - 1) % NS);
                 meta[rb] = nc;
                 mbar_arrive_expect_tx(&cbar[rb], nc.bytes);
-                bulk_g2s(stages + rb * CH, src, nc.bytes, &cbar[rb]);
+                bulk_g2s_hint(stages + rb * CH, src, nc.bytes, &cbar[rb], pol);
                 ++issued;
             }
         }
