@@ -135,6 +135,7 @@ struct MoeParams {
     CUtensorMap tmWg[KOSMOS_MAX_P];  // w_gate[q]: dims {I, H, Eq}, box {64, 64, 1}
     CUtensorMap tmWu[KOSMOS_MAX_P];  // w_up[q]:   dims {I, H, Eq}, box {64, 64, 1}
     CUtensorMap tmWd[KOSMOS_MAX_P];  // w_down[q]: dims {H, I, Eq}, box {64, 64, 1}
+    CUtensorMap tmSlot;              // slot buffer: dims {H, T*K}, box {256, fold_tps*K}, no swizzle
     const __nv_bfloat16 *x[KOSMOS_MAX_P];
     __nv_bfloat16 *y[KOSMOS_MAX_P];
     int32_t *topk_idx;
@@ -153,6 +154,8 @@ struct MoeParams {
     __nv_bfloat16 *recv, *h, *ybuf, *slot;
     TraceRec *trace;
     MoeGeom g;
+    int fold_tps;                    // FOLD: tokens per pipeline stage (64 / K)
+    int pad;
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -426,10 +429,30 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
         int32_t code;
         if (queue_try_take(&qc[3], &qc[2], p.fold_items + q * g.fold_cap, p.fold_flags + q * g.fold_cap, epoch, code,
                            p.ws)) {
+            // the block's K slot rows of every token, column tile dn, through the
+            // stage ring: fold_tps tokens (fold_tps * K rows x 256 columns) per stage
+            const int gb = code & 0xFFFF, dn = (code >> 16) & 0xFFFF;
+            const int qs = gb / g.RB, bq = gb % g.RB;
+            const int64_t left = g.Tq - static_cast<int64_t>(bq) * BM;
+            const int ntok = static_cast<int>(left < BM ? left : BM);
+            const int nst = (ntok + p.fold_tps - 1) / p.fold_tps;
+            const int64_t row0 = (static_cast<int64_t>(qs) * g.Tq + static_cast<int64_t>(bq) * BM) * g.K;
             SchedEntry en;
-            fill_entry(en, K_FOLD, code & 0xFFFF, 0, (code >> 16) & 0xFFFF, 0, code,
+            fill_entry(en, K_FOLD, gb, 0, dn, nst, code,
                        trace_open(p, st, K_FOLD, code, p.trace ? static_cast<int64_t>(globaltimer()) : 0));
-            ring_push(sm, st.rs, en, p.ws);
+            if (!ring_push(sm, st.rs, en, p.ws)) return ACT_EXIT;
+            const uint32_t bytes = static_cast<uint32_t>(BN * 2 * p.fold_tps * g.K);
+            for (int s = 0; s < nst; ++s) {
+                if (!mbar_wait(&sm.empty[st.ps.stage], st.ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, code);
+                    return ACT_EXIT;
+                }
+                uint64_t *bar = &sm.full[st.ps.stage];
+                mbar_arrive_expect_tx(bar, bytes);
+                tma_load_2d(sm.stages + st.ps.stage * STAGE_BYTES, &p.tmSlot, bar, dn * BN,
+                            static_cast<int32_t>(row0 + static_cast<int64_t>(s) * p.fold_tps * g.K));
+                st.ps.advance();
+            }
             st.idle_t0 = 0;
             return ACT_NONE;
         }
@@ -544,6 +567,28 @@ __device__ __forceinline__ void moe_producer(const MoeParams &p, const Smem &sm,
 }
 
 // ---------------------------------------------------------------- epilogue (warps 2-5)
+// Exclusive prefix sum of n values by one warp (lane l takes a run of
+// consecutive values); with div > 0 each value v counts as ceil(v / div).
+// Returns the total.
+__device__ __forceinline__ int warp_excl_scan(const int32_t *in, int32_t *out, int n, int lane, int div) {
+    const int per = (n + 31) / 32;
+    const int i0 = lane * per;
+    int loc = 0;
+    for (int i = i0; i < i0 + per && i < n; ++i) loc += div > 0 ? (in[i] + div - 1) / div : in[i];
+    int incl = loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    int run = incl - loc;
+    for (int i = i0; i < i0 + per && i < n; ++i) {
+        out[i] = run;
+        run += div > 0 ? (in[i] + div - 1) / div : in[i];
+    }
+    return __shfl_sync(0xFFFFFFFFu, incl, 31);
+}
+
 // ROUTE epilogue for one block of 128 tokens (one token per thread).
 __device__ __noinline__ void moe_route_epilogue(const MoeParams &p, const SchedEntry &e, uint32_t taddr, int row,
                                                 int et, uint8_t *escr, uint32_t epoch) {
@@ -553,49 +598,51 @@ __device__ __noinline__ void moe_route_epilogue(const MoeParams &p, const SchedE
     const int64_t tl = static_cast<int64_t>(b) * BM + row;
     const bool valid = tl < g.Tq;
     const int64_t t = static_cast<int64_t>(q) * g.Tq + (valid ? tl : 0);
+    // Top-k by k rounds of selection: round s takes the largest logit not
+    // taken yet, ties to the lower expert (the scan runs in ascending expert
+    // order and only a strictly larger value replaces the best so far).
+    // Round 0 also writes the logits out.  The logits are re-read from TMEM
+    // in every round, which keeps the code and the registers small.
     float tv[MOE_MAXK];
     int ti[MOE_MAXK];
+    uint32_t taken[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // one bit per expert (E <= 256)
+#pragma unroll 1
+    for (int s = 0; s < K; ++s) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll 1
+        for (int ch = 0; ch < E / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + ch * 32, r);
+            tmem_ld_wait();
+            if (s == 0 && valid) {
+                float4 *dump = reinterpret_cast<float4 *>(p.logits + t * E + ch * 32);
 #pragma unroll
-    for (int s = 0; s < MOE_MAXK; ++s) { tv[s] = -INFINITY; ti[s] = 0x7FFFFFFF; }
-    int cnt = 0;
-    float lmax = -INFINITY;
-    for (int ch = 0; ch < E / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + ch * 32, r);
-        tmem_ld_wait();
-        if (valid) {
-            float4 *dump = reinterpret_cast<float4 *>(p.logits + t * E + ch * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                dump[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float l = __uint_as_float(r[j]);
-            lmax = fmaxf(lmax, l);
-            // insert (l, ch*32+j) after every kept entry with value >= l: the list
-            // stays sorted by (value descending, index ascending)
-            bool shifting = false;
-            float cv = l;
-            int ci = ch * 32 + j;
-#pragma unroll
-            for (int s = 0; s < MOE_MAXK; ++s) {
-                if (s < K) {
-                    if (!shifting && (s >= cnt || cv > tv[s])) shifting = true;
-                    if (shifting) {
-                        const float fv = tv[s];
-                        const int fi = ti[s];
-                        tv[s] = cv; ti[s] = ci;
-                        cv = fv; ci = fi;
-                    }
-                }
+                for (int j = 0; j < 8; ++j)
+                    dump[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
             }
-            if (cnt < K) ++cnt;
+            uint32_t tk = 0u;
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                if (w == ch) tk = taken[w];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float l = __uint_as_float(r[j]);
+                if (!((tk >> j) & 1u) && l > bv) { bv = l; bi = ch * 32 + j; }
+            }
         }
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            if (w == (bi >> 5)) taken[w] |= 1u << (bi & 31);
+#pragma unroll
+        for (int u = 0; u < MOE_MAXK; ++u)
+            if (u == s) { tv[u] = bv; ti[u] = bi; }
     }
+    const float lmax = tv[0];
     // softmax denominator over all experts (ascending expert order)
     float z = 0.f;
+#pragma unroll 1
     for (int ch = 0; ch < E / 32; ++ch) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + ch * 32, r);
@@ -656,32 +703,37 @@ __device__ __noinline__ void moe_route_epilogue(const MoeParams &p, const SchedE
     int32_t *s_off = reinterpret_cast<int32_t *>(escr + 6144);
     for (int i = et; i < E; i += NUM_EPI_THREADS) {
         int c = 0;
-        for (int gb = 0; gb < g.NB; ++gb) c += *reinterpret_cast<volatile int32_t *>(&p.blk_counts[gb * E + i]);
+#pragma unroll 8
+        for (int gb = 0; gb < g.NB; ++gb) c += ldcg_i32(&p.blk_counts[gb * E + i]);
         s_cnt[i] = c;
         p.counts[i] = c;
         p.counts_out[i] = c;
     }
     named_bar_sync(1, NUM_EPI_THREADS);
-    if (et == 0) {
-        int run = 0;
-        for (int i = 0; i < E; ++i) { s_off[i] = run; p.offsets[i] = run; run += s_cnt[i]; }
-        s_off[E] = run;
-        p.offsets[E] = run;
-        for (int qq = 0; qq < g.P; ++qq) {
-            int u = 0;
-            for (int j = 0; j < g.Eq; ++j) {
-                p.unit_start[qq * (g.Eq + 1) + j] = u;
-                u += (s_cnt[qq * g.Eq + j] + BM - 1) / BM;
-            }
-            p.unit_start[qq * (g.Eq + 1) + g.Eq] = u;
+    // exclusive prefix sums by warp scans (a serial loop interleaving shared
+    // and global accesses cost tens of microseconds here): warp 0 scans the
+    // expert counts into the receive offsets, warps 1.. scan each rank's
+    // row-block units
+    int32_t *s_us = reinterpret_cast<int32_t *>(escr);  // [P][Eq + 1] <= 264 words, over s_bits (done with)
+    const int ew = et / 32, lane = et % 32;
+    if (ew == 0) {
+        const int total = warp_excl_scan(s_cnt, s_off, E, lane, 0);
+        if (lane == 0) s_off[E] = total;
+    } else {
+        for (int qq = ew - 1; qq < g.P; qq += NUM_EPI_THREADS / 32 - 1) {
+            const int total = warp_excl_scan(s_cnt + qq * g.Eq, s_us + qq * (g.Eq + 1), g.Eq, lane, BM);
+            if (lane == 0) s_us[qq * (g.Eq + 1) + g.Eq] = total;
         }
     }
     named_bar_sync(1, NUM_EPI_THREADS);
+    for (int i = et; i <= E; i += NUM_EPI_THREADS) p.offsets[i] = s_off[i];
+    for (int i = et; i < g.P * (g.Eq + 1); i += NUM_EPI_THREADS) p.unit_start[i] = s_us[i];
     for (int i = et; i < E; i += NUM_EPI_THREADS) {
         int run = s_off[i];
+#pragma unroll 8
         for (int gb = 0; gb < g.NB; ++gb) {
             p.base[gb * E + i] = run;
-            run += *reinterpret_cast<volatile int32_t *>(&p.blk_counts[gb * E + i]);
+            run += ldcg_i32(&p.blk_counts[gb * E + i]);
         }
     }
     __threadfence();
@@ -745,58 +797,68 @@ __device__ __noinline__ void moe_push(const MoeParams &p, const SchedEntry &e, i
 }
 
 // out[t] = sum_k gate[t][k] * slot[t][k] (fp32 multiply, then add, k in
-// emission order), one rounding to bf16.  Warp w: tokens 32w..32w+31 of the
-// block, two at a time; lane: 8 of the 256 columns.
-__device__ __noinline__ void moe_fold(const MoeParams &p, const SchedEntry &e, int ew, int lane) {
-    constexpr int TU = 2;
+// emission order), one rounding to bf16.  The slot rows arrive through the
+// stage ring, fold_tps tokens per stage; thread et takes token et / 16 (and
+// every 8th after it) and 16 of the 256 columns.  Returns false after a
+// device error.
+__device__ __noinline__ bool moe_fold(const MoeParams &p, const Smem &sm, PipeState &ps, const SchedEntry &e, int et,
+                                      uint8_t *escr) {
     const MoeGeom &g = p.g;
     const int gb = e.a, dn = e.c;
     const int q = gb / g.RB, b = gb % g.RB;
     const int K = g.K;
     const int64_t left = g.Tq - static_cast<int64_t>(b) * BM;
     const int ntok = static_cast<int>(left < BM ? left : BM);
-    for (int i0 = 0; i0 < 32; i0 += TU) {
-        uint4 v[TU][MOE_MAXK];
-        float gk[TU][MOE_MAXK];
-#pragma unroll
-        for (int u = 0; u < TU; ++u) {
-            const int r = ew * 32 + i0 + u;
-            const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(b) * BM + r;
-#pragma unroll
-            for (int k = 0; k < MOE_MAXK; ++k) {
-                if (k < K && r < ntok) {
-                    gk[u][k] = ldcg_f32(&p.topk_gate[t * K + k]);
-                    v[u][k] = ldcg_u4(p.slot + (t * K + k) * g.H + dn * BN + lane * 8);
-                }
-            }
+    const int64_t t0 = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(b) * BM;
+    // the block's gates, once
+    float *s_gate = reinterpret_cast<float *>(escr);  // [BM * K] <= 4 KB
+    for (int i = et; i < ntok * K; i += NUM_EPI_THREADS) s_gate[i] = ldcg_f32(&p.topk_gate[t0 * K + i]);
+    named_bar_sync(1, NUM_EPI_THREADS);
+    const int c0 = (et & 15) * 16;
+    for (int s = 0; s < e.nstage; ++s) {
+        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -9);
+            return false;
         }
+        const uint8_t *buf = sm.stages + ps.stage * STAGE_BYTES;
+        for (int u = et >> 4; u < p.fold_tps; u += NUM_EPI_THREADS / 16) {
+            const int r = s * p.fold_tps + u;  // token within the block
+            if (r >= ntok) break;
+            float acc[16];
 #pragma unroll
-        for (int u = 0; u < TU; ++u) {
-            const int r = ew * 32 + i0 + u;
-            if (r >= ntok) continue;
-            float acc[8];
+            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+            for (int k = 0; k < K; ++k) {
+                const float gk = s_gate[r * K + k];
+                const uint4 *src = reinterpret_cast<const uint4 *>(buf + ((u * K + k) * BN + c0) * 2);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-#pragma unroll
-            for (int k = 0; k < MOE_MAXK; ++k) {
-                if (k < K) {
-                    const uint32_t w[4] = {v[u][k].x, v[u][k].y, v[u][k].z, v[u][k].w};
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 v = src[h];
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(gk[u][k], __uint_as_float(w[j] << 16)));
-                        acc[2 * j + 1] =
-                            __fadd_rn(acc[2 * j + 1], __fmul_rn(gk[u][k], __uint_as_float(w[j] & 0xFFFF0000u)));
+                        acc[h * 8 + 2 * j] = __fadd_rn(acc[h * 8 + 2 * j], __fmul_rn(gk, __uint_as_float(w[j] << 16)));
+                        acc[h * 8 + 2 * j + 1] =
+                            __fadd_rn(acc[h * 8 + 2 * j + 1], __fmul_rn(gk, __uint_as_float(w[j] & 0xFFFF0000u)));
                     }
                 }
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            *reinterpret_cast<uint4 *>(p.y[q] + (static_cast<int64_t>(b) * BM + r) * g.H + dn * BN + lane * 8) = o;
+            uint4 o[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                o[h].x = pack_bf16x2(acc[h * 8 + 0], acc[h * 8 + 1]);
+                o[h].y = pack_bf16x2(acc[h * 8 + 2], acc[h * 8 + 3]);
+                o[h].z = pack_bf16x2(acc[h * 8 + 4], acc[h * 8 + 5]);
+                o[h].w = pack_bf16x2(acc[h * 8 + 6], acc[h * 8 + 7]);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(p.y[q] + (static_cast<int64_t>(b) * BM + r) * g.H + dn * BN + c0);
+            dst[0] = o[0];
+            dst[1] = o[1];
         }
+        named_bar_sync(1, NUM_EPI_THREADS);
+        if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
+        ps.advance();
     }
+    return true;
 }
 
 __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm, uint32_t tmem_base, uint8_t *escr,
@@ -807,6 +869,7 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
     const int ew = warp - 2;
     const int et = ew * 32 + lane;
     RingState rs;
+    PipeState ps;  // stages of the ring: MMA entries are skipped, FOLD stages consumed here
     uint32_t acc = 0, acc_phase = 0;
     while (true) {
         if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
@@ -819,6 +882,7 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
         rs.advance();
         if (e.kind == K_DONE) break;
         if (is_mma_kind(e.kind)) {
+            ps.advance(e.nstage);
             if (!mbar_wait(&sm.tfull[acc], acc_phase, PIPE_LIMIT_NS)) {
                 set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
                 break;
@@ -878,7 +942,7 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
         } else if (e.kind == K_PUSH) {
             moe_push(p, e, ew, lane, epoch);
         } else if (e.kind == K_FOLD) {
-            moe_fold(p, e, ew, lane);
+            if (!moe_fold(p, sm, ps, e, et, escr)) break;
         }
         if (e.slot >= 0 && et == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
@@ -1047,6 +1111,16 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
         const uint64_t st[1] = {I * 2};
         const uint32_t box[2] = {BK, BM};
         if (!encode_tmap(&p.tmH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.h, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return KOSMOS_ERR_CUDA;
+    }
+    {
+        // FOLD: fold_tps tokens x K slot rows x 256 columns per stage (<= 32 KB)
+        p.fold_tps = 64 / g.K;
+        const uint64_t dims[2] = {static_cast<uint64_t>(g.H), static_cast<uint64_t>(g.T * g.K)};
+        const uint64_t st[1] = {static_cast<uint64_t>(g.H) * 2};
+        const uint32_t box[2] = {BN, static_cast<uint32_t>(p.fold_tps * g.K)};
+        if (!encode_tmap(&p.tmSlot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.slot, dims, st, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
             return KOSMOS_ERR_CUDA;
     }
     return launch_persistent(reinterpret_cast<const void *>(&moe_fwd_kernel), &p, Lc.grid, MOE_SMEM_BYTES, stream,
