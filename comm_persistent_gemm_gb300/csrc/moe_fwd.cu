@@ -18,7 +18,7 @@
 //                   expert-ordered receive buffer; per (expert, row block)
 //                   arrival counters are released.
 //   TILE_GU / TILE_D  per unit u = (expert, 128-row block), consumer-ordered
-//                   with a lag of one unit: GU(u0) | GU(u1) D(u0) | ... | D(uN-1).
+//                   with a lag of two experts: GU(e0) | GU(e1) | GU(e2) D(e0) | ...
 //                   GU: [rows x H] . [W_gate | W_up] (128 + 128 columns) with a
 //                   SwiGLU epilogue h = silu(gate) * up; D: [rows x I] . W_down.
 // Ready queues of rank q (the combine step, two-way role switching; explainer
@@ -209,7 +209,7 @@ __device__ __forceinline__ void push_decode(int32_t c, int &e, int &rb, int &dn)
 }
 
 // ---------------------------------------------------------------- producer (warp 0)
-enum MoeAct : int { ACT_NONE = 0, ACT_DISPATCH = 1, ACT_EXIT = 2 };
+enum MoeAct : int { ACT_NONE = 0, ACT_DISPATCH = 1, ACT_EXIT = 2, ACT_PLAN = 3 };
 
 struct MoeProdState {
     PipeState ps;
@@ -219,6 +219,11 @@ struct MoeProdState {
     bool main_done = false;
     bool plan_seen = false;
     uint64_t idle_t0 = 0;
+    // this rank's plan, copied to shared memory once it is published:
+    // us[Eq + 1] row-block prefix, off[Eq] receive offsets, cnt[Eq] row counts
+    int32_t *us = nullptr, *off = nullptr, *cnt = nullptr;
+    int64_t pending = -1;  // a claimed main-rail ticket waiting for the plan table
+    int64_t ahead = -1;    // the next main-rail ticket, claimed early so its latency overlaps the current entry
 };
 
 __device__ __forceinline__ void fill_entry(SchedEntry &e, int kind, int a, int b, int c, int nstage, int ticket,
@@ -238,11 +243,19 @@ __device__ __forceinline__ int trace_open(const MoeParams &p, MoeProdState &st, 
     return slot;
 }
 
-__device__ __forceinline__ bool wait_plan(const MoeParams &p, MoeProdState &st, uint32_t epoch) {
-    if (st.plan_seen) return true;
-    if (!wait_flag_eq(p.ws, &p.ws->aux[1], epoch + 1u, p.wait_limit_ns, -10)) return false;
+// The whole producer warp, once the plan is published (lane 0 acquired its
+// flag): copies this rank's plan into the shared-memory table.
+__device__ __forceinline__ void load_plan_table(const MoeParams &p, MoeProdState &st, int lane) {
+    const MoeGeom &g = p.g;
+    const int q = blockIdx.x % g.P;
+    __syncwarp();  // orders lane 0's acquire of the plan before the other lanes' reads
+    for (int j = lane; j <= g.Eq; j += 32) st.us[j] = ldcg_i32(&p.unit_start[q * (g.Eq + 1) + j]);
+    for (int j = lane; j < g.Eq; j += 32) {
+        st.off[j] = ldcg_i32(&p.offsets[q * g.Eq + j]);
+        st.cnt[j] = ldcg_i32(&p.counts[q * g.Eq + j]);
+    }
+    __syncwarp();
     st.plan_seen = true;
-    return true;
 }
 
 // Waits until every pipeline stage is free (all earlier MMAs have read their
@@ -259,37 +272,35 @@ __device__ __forceinline__ bool drain_pipeline(const MoeParams &p, const Smem &s
     return true;
 }
 
-// Expert tile rail of rank q, grouped by expert with a lag of one expert:
-//   GU(e0) | GU(e1) D(e0) | GU(e2) D(e1) | ... | D(e_last)
-// GU(e): column block outer, row block inner (the row blocks of one weight
-// slice are adjacent, so the slice is read from DRAM once); D(e) likewise.
-// With us[j] = row blocks of the rank's experts before j, group j starts at
-// 12 us[j] + 16 us[j-1] (NGU = 12, ND = 16 for the 4096/1536 shapes).
-__device__ __forceinline__ void moe_decode_tile(const MoeParams &p, int q, int tt, int &kind, int &le, int &rb,
-                                                int &col) {
+// Expert tile rail of rank q, grouped by expert with a lag of MOE_LAG experts:
+//   GU(e0) | GU(e1) | GU(e2) D(e0) | GU(e3) D(e1) | ... | D(e_last)
+// so that a D tile, which needs every GU column block of its rows, is claimed
+// well after them.  GU(e): column block outer, row block inner (the row
+// blocks of one weight slice are adjacent, so the slice is read from DRAM
+// once); D(e) likewise.  With U(j) = row blocks of the rank's experts before
+// expert j (clamped to [0, Eq]), group j starts at NGU U(j) + ND U(j - LAG).
+constexpr int MOE_LAG = 2;
+__device__ __forceinline__ void moe_decode_tile(const MoeParams &p, const int32_t *us, int tt, int &kind, int &le,
+                                                int &rb, int &col) {
     const MoeGeom &g = p.g;
-    const int32_t *us = p.unit_start + q * (g.Eq + 1);
+    auto U = [&](int j) { return j <= 0 ? 0 : us[j < g.Eq ? j : g.Eq]; };
     kind = 0;
-    const int U = ldcg_i32(&us[g.Eq]);
-    if (tt < 0 || tt >= U * (g.NGU + g.ND)) return;
-    int prev = 0;  // us[j - 1]
-    for (int j = 0; j <= g.Eq; ++j) {
-        const int usj = ldcg_i32(&us[j]);
-        const int nj = (j < g.Eq) ? ldcg_i32(&us[j + 1]) - usj : 0;     // row blocks of expert j
-        const int np = (j >= 1) ? usj - prev : 0;                        // row blocks of expert j-1
-        const int start = g.NGU * usj + g.ND * prev;
-        const int size = g.NGU * nj + g.ND * np;
-        if (tt < start + size) {
+    const int total = U(g.Eq);
+    if (tt < 0 || tt >= total * (g.NGU + g.ND)) return;
+    for (int j = 0; j < g.Eq + MOE_LAG; ++j) {
+        const int ngu = j < g.Eq ? U(j + 1) - U(j) : 0;                        // row blocks of expert j
+        const int nd = j >= MOE_LAG ? U(j - MOE_LAG + 1) - U(j - MOE_LAG) : 0;  // of expert j - LAG
+        const int start = g.NGU * U(j) + g.ND * U(j - MOE_LAG);
+        if (tt < start + g.NGU * ngu + g.ND * nd) {
             const int r = tt - start;
-            if (r < g.NGU * nj) {
-                kind = K_TILE_GU; le = j; col = r / nj; rb = r % nj;
+            if (r < g.NGU * ngu) {
+                kind = K_TILE_GU; le = j; col = r / ngu; rb = r % ngu;
             } else {
-                const int r2 = r - g.NGU * nj;
-                kind = K_TILE_D; le = j - 1; col = r2 / np; rb = r2 % np;
+                const int r2 = r - g.NGU * ngu;
+                kind = K_TILE_D; le = j - MOE_LAG; col = r2 / nd; rb = r2 % nd;
             }
             return;
         }
-        prev = usj;
     }
 }
 
@@ -312,8 +323,8 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
             SchedEntry en;
             fill_entry(en, K_PUSH, e, rb, dn, 0, code,
                        trace_open(p, st, K_PUSH, code, p.trace ? static_cast<int64_t>(globaltimer()) : 0));
-            en.x0 = ldcg_i32(&p.offsets[e]) + rb * BM;
-            const int rows = ldcg_i32(&p.counts[e]) - rb * BM;
+            en.x0 = st.off[e - q * g.Eq] + rb * BM;
+            const int rows = st.cnt[e - q * g.Eq] - rb * BM;
             en.x1 = rows < BM ? rows : BM;
             ring_push(sm, st.rs, en, p.ws);
             st.idle_t0 = 0;
@@ -323,7 +334,16 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
     }
     // 2) the next entry of this rank's main rail
     if (!st.main_done) {
-        const uint32_t t = atomicAdd(&p.ws->tickets[q], 1u);
+        uint32_t t;
+        if (st.pending >= 0) {
+            t = static_cast<uint32_t>(st.pending);
+        } else if (st.ahead >= 0) {
+            t = static_cast<uint32_t>(st.ahead);
+        } else {
+            t = atomicAdd(&p.ws->tickets[q], 1u);
+        }
+        st.pending = -1;
+        st.ahead = -1;
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
         if (t < static_cast<uint32_t>(g.RB)) {  // ROUTE(b)
             const int b = static_cast<int>(t);
@@ -348,8 +368,12 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
             st.idle_t0 = 0;
             return ACT_NONE;
         }
+        if (!st.plan_seen) {  // every later entry needs the plan: wait for it, then the warp loads the table
+            if (!wait_flag_eq(p.ws, &p.ws->aux[1], epoch + 1u, p.wait_limit_ns, -10)) return ACT_EXIT;
+            st.pending = t;
+            return ACT_PLAN;
+        }
         if (t < static_cast<uint32_t>(g.n_head)) {  // DISPATCH(b, k)
-            if (!wait_plan(p, st, epoch)) return ACT_EXIT;
             const int i = static_cast<int>(t) - g.RB;
             v0 = i / g.K;
             v1 = i % g.K;
@@ -357,16 +381,18 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
             st.idle_t0 = 0;
             return ACT_DISPATCH;
         }
-        if (!wait_plan(p, st, epoch)) return ACT_EXIT;
         const int tt = static_cast<int>(t) - g.n_head;
         int kind = 0, le = 0, rb = 0, col = 0;
-        moe_decode_tile(p, q, tt, kind, le, rb, col);
+        moe_decode_tile(p, st.us, tt, kind, le, rb, col);
         if (kind == 0) {
             st.main_done = true;
         } else {
+            // claim the next tile ticket now; its value is first needed after this
+            // entry's loads are issued, so the atomic's round trip overlaps them
+            const uint32_t nxt = atomicAdd(&p.ws->tickets[q], 1u);
             const int e = q * g.Eq + le;
-            const int row0 = ldcg_i32(&p.offsets[e]) + rb * BM;
-            const int left = ldcg_i32(&p.counts[e]) - rb * BM;
+            const int row0 = st.off[le] + rb * BM;
+            const int left = st.cnt[le] - rb * BM;
             const int rows = left < BM ? left : BM;
             const int ci = e * g.MAXRB + rb;
             if (kind == K_TILE_GU) {
@@ -389,6 +415,7 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
                 }
                 if (TraceRec *r = trace_rec(p.trace, blockIdx.x, slot)) r->t_done = static_cast<int64_t>(globaltimer());
                 st.idle_t0 = 0;
+                st.ahead = nxt;
                 return ACT_NONE;
             }
             SchedEntry en;
@@ -421,6 +448,7 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
                 st.ps.advance();
             }
             st.idle_t0 = 0;
+            st.ahead = nxt;
             return ACT_NONE;
         }
     }
@@ -460,7 +488,7 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
     }
     // 4) finished when the rail and both queues of this rank are drained
     if (st.main_done && st.plan_seen) {
-        const uint32_t push_total = static_cast<uint32_t>(ldcg_i32(&p.unit_start[q * (g.Eq + 1) + g.Eq])) * g.ND;
+        const uint32_t push_total = static_cast<uint32_t>(st.us[g.Eq]) * g.ND;
         const uint32_t fold_total = static_cast<uint32_t>(g.fold_cap);
         if (ld_relaxed_gpu(&qc[1]) >= push_total && ld_relaxed_gpu(&qc[3]) >= fold_total) return ACT_EXIT;
     }
@@ -549,6 +577,10 @@ __device__ __noinline__ void moe_dispatch(const MoeParams &p, const Smem &sm, Mo
 __device__ __forceinline__ void moe_producer(const MoeParams &p, const Smem &sm, uint8_t *pscr, uint32_t epoch,
                                              int lane) {
     MoeProdState st;
+    // producer scratch: [0, 1 KB) dispatch rows, then the plan table (3 Eq + 1 words <= 3 KB)
+    st.us = reinterpret_cast<int32_t *>(pscr + 1024);
+    st.off = st.us + p.g.Eq + 1;
+    st.cnt = st.off + p.g.Eq;
     while (true) {
         int act = ACT_NONE, v0 = 0, v1 = 0, v2 = 0;
         if (lane == 0) act = moe_decide(p, sm, st, epoch, v0, v1, v2);
@@ -557,6 +589,7 @@ __device__ __forceinline__ void moe_producer(const MoeParams &p, const Smem &sm,
         v1 = __shfl_sync(0xFFFFFFFFu, v1, 0);
         v2 = __shfl_sync(0xFFFFFFFFu, v2, 0);
         if (act == ACT_EXIT) break;
+        if (act == ACT_PLAN) load_plan_table(p, st, lane);
         if (act == ACT_DISPATCH) moe_dispatch(p, sm, st, pscr, lane, v0, v1, v2, epoch);
     }
     if (lane == 0) {
