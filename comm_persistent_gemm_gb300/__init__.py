@@ -280,7 +280,7 @@ def check(ws, what: str = "kosmos", stream=None):
         raise KosmosError(st, what, ent)
 
 
-def trace_records(op: int, P: int, m: int, n: int, k: int, ws, o: Opts):
+def trace_records(op: int, P: int, m: int, n: int, k: int, ws, o: Opts, dtype: int = BF16):
     """Copies the role trace out of the workspace: list of dicts, one per
     recorded entry (CTA ring order)."""
     import numpy as np
@@ -288,7 +288,7 @@ def trace_records(op: int, P: int, m: int, n: int, k: int, ws, o: Opts):
     ptr = C.c_void_p()
     cap = C.c_int32()
     nct = C.c_int32()
-    rc = lib().kosmos_trace_info(op, P, m, n, k, BF16, C.byref(o), ws.data_ptr(), C.byref(ptr), C.byref(cap),
+    rc = lib().kosmos_trace_info(op, P, m, n, k, dtype, C.byref(o), ws.data_ptr(), C.byref(ptr), C.byref(cap),
                                  C.byref(nct))
     _raise(rc, "kosmos_trace_info")
     off = ptr.value - ws.data_ptr()

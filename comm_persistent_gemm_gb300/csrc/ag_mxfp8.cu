@@ -20,7 +20,7 @@
 
 #include <cstring>
 
-#include "engine.cuh"
+#include "engine2.cuh"
 #include "launch.h"
 
 namespace kosmos {
@@ -38,6 +38,10 @@ struct AgF8Params {
     CUtensorMap tmA_local;  // x_shards[0]: dims {k, m} (bytes), box {128, 128}, 128B swizzle
     CUtensorMap tmA_gath;   // x_gathered: dims {k, m, P}, box {128, 128, 1}
     CUtensorMap tmB;        // W: dims {n, k}, box {128, 128}
+    // SM-pair kernel only: the tiled scales as rows of 16 bytes, one 512-byte atom per box
+    CUtensorMap tmSA_local; // x_scales[0]: dims {16, pieces * nkb * 32}, box {16, 32}
+    CUtensorMap tmSA_gath;  // gathered scales: dims {16, P * pieces * nkb * 32}, box {16, 32}
+    CUtensorMap tmSW;       // W scales: dims {16, nb_w * nkb * 32}, box {16, 32}
     const uint8_t *x_src[KOSMOS_MAX_P];
     const uint8_t *sx_src[KOSMOS_MAX_P];  // tiled scales of each shard
     const uint8_t *sw;                    // tiled scales of W
@@ -342,6 +346,326 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_mxfp8_kernel(const __grid_c
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
 }
 
+// ============================================================== SM-pair variant
+// Tiles of 256 x 256 on an SM pair (tcgen05.mma.cta_group::2, block-scaled).
+// Each CTA stages its 128 rows of A, its 128 columns of B, the scale atom of
+// its rows (SFA) and the scale atoms of all 256 columns (SFB); the leader's
+// tcgen05.cp.cta_group::2 copies every CTA's atoms into that CTA's tensor
+// memory, where the pair MMA reads SFA of the CTA's rows and SFB of the whole
+// tile (the placement was checked on the GB300 against exact results).
+constexpr int F2_NSTAGE = 6;
+constexpr int F2_A_BYTES = HBM_ROWS * FBK;             // 16 KB
+constexpr int F2_B_BYTES = HBN * FBK;                  // 16 KB
+constexpr int F2_STAGE = F2_A_BYTES + F2_B_BYTES;
+constexpr int F2_SF = 3 * 512;                         // SFA atom + two SFB atoms
+constexpr int F2_SMEM_BYTES = F2_NSTAGE * (F2_STAGE + F2_SF) + SMEM2_CTRL + 1024;
+static_assert(F2_SMEM_BYTES <= 232448, "MXFP8 pair engine exceeds 227 KB of shared memory per CTA");
+using PipeF2 = PipeStateN<F2_NSTAGE>;
+
+struct F2Smem {
+    Smem2 base;
+    uint8_t *sf;  // [F2_NSTAGE][F2_SF]
+};
+
+__device__ __forceinline__ F2Smem carve_f2(uint8_t *raw) {
+    const uintptr_t b0 = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
+    uint8_t *p = reinterpret_cast<uint8_t *>(b0);
+    F2Smem f;
+    Smem2 &s = f.base;
+    s.stages = p;
+    p += F2_NSTAGE * F2_STAGE;
+    f.sf = p;
+    p += F2_NSTAGE * F2_SF;
+    uint64_t *b = reinterpret_cast<uint64_t *>(p);
+    s.full = b; b += F2_NSTAGE;
+    s.empty = b; b += F2_NSTAGE;
+    s.cbar = b; b += F2_NSTAGE;
+    s.tfull = b; b += 2;
+    s.tempty = b; b += 2;
+    s.sfull = b; b += NSCHED;
+    s.sempty = b; b += NSCHED;
+    s.pempty = b; b += NSCHED;
+    s.sched = reinterpret_cast<SchedEntry *>(b);
+    s.tmem_slot = reinterpret_cast<uint32_t *>(s.sched + NSCHED);
+    return f;
+}
+
+__device__ __forceinline__ void mma2_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+// Issued by the leader: each CTA of the pair copies its own shared-memory
+// atom into its own tensor memory.
+__device__ __forceinline__ void tmem_cp2_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// This CTA's half of one K stage of tile (s, i2, c): A rows of piece pc, B
+// columns [col0, col0 + 128), the piece's scale atom and the tile's two W
+// scale atoms; everything completes on the leader's full barrier.
+__device__ __forceinline__ void f2_load_half(const AgF8Params &p, const F2Smem &fs, uint32_t stage, bool local, int s,
+                                             int pc, int64_t col0, int tile_c, int kb, uint32_t leader_full) {
+    uint8_t *sa = fs.base.stages + stage * F2_STAGE;
+    uint8_t *sb = sa + F2_A_BYTES;
+    uint8_t *sf = fs.sf + stage * F2_SF;
+    const int32_t row0 = pc * BM;
+    if (local) {
+        tma_load_2d_pair(sa, &p.tmA_local, leader_full, kb * FBK, row0);
+        tma_load_2d_pair(sf, &p.tmSA_local, leader_full, 0, (pc * p.nkb + kb) * 32);
+    } else {
+        tma_load_3d_pair(sa, &p.tmA_gath, leader_full, kb * FBK, row0, s);
+        tma_load_2d_pair(sf, &p.tmSA_gath, leader_full, 0, ((s * p.g.pieces + pc) * p.nkb + kb) * 32);
+    }
+    tma_load_2d_pair(sb, &p.tmB, leader_full, static_cast<int32_t>(col0), kb * FBK);
+    tma_load_2d_pair(sf + 512, &p.tmSW, leader_full, 0, ((2 * tile_c) * p.nkb + kb) * 32);
+    tma_load_2d_pair(sf + 1024, &p.tmSW, leader_full, 0, ((2 * tile_c + 1) * p.nkb + kb) * 32);
+}
+
+__device__ __forceinline__ void f2_producer(const AgF8Params &p, const F2Smem &fs, uint32_t epoch, uint32_t rank) {
+    const Smem2 &sm = fs.base;
+    const int pair = blockIdx.x / 2;
+    const bool leader = rank == 0;
+    const bool mover = (p.sched != KOSMOS_SCHED_UNFUSED) && pair < p.n_comm;
+    uint32_t cphase = 0;
+    PipeF2 ps;
+    RingPair rs;
+    int nrec = 0;
+    if (mover) {
+        auto claim = [&](MoveEntry &e) { return f8_claim_transfer(p, e); };
+        auto done = [&](int32_t ticket, int64_t t_claim) {
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+                r->t_claim = t_claim; r->t_ready = t_claim; r->t_done = static_cast<int64_t>(globaltimer());
+                r->kind = K_TRANSFER; r->ticket = ticket; r->cta = blockIdx.x;
+            }
+            ++nrec;
+        };
+        if (!stream_mover<F2_NSTAGE, F2_STAGE, 2>(sm.stages, sm.cbar, cphase, p.ws, claim, done) || failed(p.ws) ||
+            p.sched == KOSMOS_SCHED_FIXED) {
+            if (leader) {
+                SchedEntry d;
+                fill_done(d);
+                ring2_push(sm, rs, d, p.ws);
+            } else {
+                SchedEntry e;
+                while (ring2_take(sm, rs, false, e, p.ws, false) && e.kind != K_DONE) {
+                }
+            }
+            return;
+        }
+    }
+    const uint32_t leader_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
+    if (leader) {
+        while (true) {
+            if (failed(p.ws)) break;
+            const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
+            if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
+            int s, i2, c;
+            ag_decode_tile(p.g, static_cast<int>(t), s, i2, c);
+            const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+            const int pc = 2 * i2;  // the leader's 128-row piece
+            if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
+                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch), p.wait_limit_ns,
+                                  t))
+                    break;
+            }
+            int slot = -1;
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+                r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
+                r->kind = K_TILE; r->ticket = static_cast<int32_t>(t); r->cta = blockIdx.x;
+                slot = nrec;
+            }
+            ++nrec;
+            SchedEntry e;
+            fill_done(e);
+            e.kind = K_TILE; e.a = s; e.b = i2; e.c = c; e.nstage = p.nkb; e.ticket = static_cast<int32_t>(t);
+            e.slot = slot;
+            if (!ring2_push(sm, rs, e, p.ws)) break;
+            const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+            bool ok = true;
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * (F2_STAGE + F2_SF));
+                f2_load_half(p, fs, ps.stage, local, s, pc, static_cast<int64_t>(c) * BN, c, kb,
+                             leader_full0 + ps.stage * 8);
+                ps.advance();
+            }
+            if (!ok) break;
+        }
+        SchedEntry d;
+        fill_done(d);
+        ring2_push(sm, rs, d, p.ws);
+    } else {
+        while (true) {
+            SchedEntry e;
+            if (!ring2_take(sm, rs, false, e, p.ws, false)) break;
+            if (e.kind == K_DONE) break;
+            const int s = e.a, i2 = e.b, c = e.c;
+            const int pc = 2 * i2 + 1;  // the peer's 128-row piece
+            if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
+                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch), p.wait_limit_ns,
+                                  e.ticket))
+                    break;
+            }
+            const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+            bool ok = true;
+            for (int kb = 0; kb < e.nstage; ++kb) {
+                if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, e.ticket);
+                    ok = false;
+                    break;
+                }
+                f2_load_half(p, fs, ps.stage, local, s, pc, static_cast<int64_t>(c) * BN + HBN, c, kb,
+                             leader_full0 + ps.stage * 8);
+                ps.advance();
+            }
+            if (!ok) break;
+        }
+    }
+}
+
+// Leader only: per stage, copy the pair's scale atoms into tensor memory, then
+// four K = 32 block-scaled MMAs into the single accumulator (columns 0-255).
+__device__ __forceinline__ void f2_mma_loop(const F2Smem &fs, uint32_t tmem_base, WsHeader *ws) {
+    const Smem2 &sm = fs.base;
+    PipeF2 ps;
+    RingPair rs;
+    uint32_t acc_phase = 0;
+    while (true) {
+        SchedEntry e;
+        if (!ring2_take(sm, rs, true, e, ws, false)) break;
+        if (e.kind == K_DONE) break;
+        if (e.kind != K_TILE) {
+            ps.advance(e.nstage);
+            continue;
+        }
+        if (!mbar_wait(&sm.tempty[0], acc_phase ^ 1u, PIPE_LIMIT_NS)) {
+            set_error(ws, KOSMOS_ERR_DEVICE, -4);
+            break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < e.nstage; ++kb) {
+            if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+                set_error(ws, KOSMOS_ERR_DEVICE, -5);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sm.stages + ps.stage * F2_STAGE);
+            const uint32_t b_addr = a_addr + F2_A_BYTES;
+            const uint32_t sf_addr = smem_u32(fs.sf + ps.stage * F2_SF);
+            const uint32_t sfa_t = tmem_base + F_TMEM_SF + ps.stage * F_TMEM_SF_STRIDE;
+            const uint32_t sfb_t = sfa_t + 4;
+            tmem_cp2_32x128b_x4(sfa_t, sdesc_sf(sf_addr));
+            tmem_cp2_32x128b_x4(sfb_t, sdesc_sf(sf_addr + 512));
+            tmem_cp2_32x128b_x4(sfb_t + 4, sdesc_sf(sf_addr + 1024));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint64_t ad = sdesc_sw128(a_addr + j * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(b_addr + j * (32 * 128), F2_B_BYTES, 1024);
+                mma2_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(PBM, BN, j), sfa_t, sfb_t, (kb | j) != 0 ? 1u : 0u);
+            }
+            mma2_commit_both(&sm.empty[ps.stage]);
+            ps.advance();
+        }
+        if (!ok) break;
+        mma2_commit_both(&sm.tfull[0]);
+        acc_phase ^= 1u;
+    }
+}
+
+// Both CTAs: drain this CTA's 128 rows into registers (bf16-packed), release
+// the accumulator (local or remote arrive), then store.
+__device__ __forceinline__ void f2_epilogue(const AgF8Params &p, const Smem2 &sm, uint32_t tmem_base, int warp, int lane,
+                                            uint32_t rank) {
+    const bool leader = rank == 0;
+    const int grp = warp & 3;
+    const int row = grp * 32 + lane;
+    RingPair rs;
+    uint32_t acc_phase = 0;
+    while (true) {
+        SchedEntry e;
+        if (!ring2_take(sm, rs, leader, e, p.ws, true)) break;
+        if (e.kind == K_DONE) break;
+        if (e.kind != K_TILE) continue;
+        if (!mbar_wait(&sm.tfull[0], acc_phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
+            break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16);
+        uint32_t packed[BN / 2];
+#pragma unroll
+        for (int ch = 0; ch < BN / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + ch * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                packed[ch * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+        }
+        acc_release(sm, 0, leader, lane);
+        acc_phase ^= 1u;
+        const int s = e.a, i2 = e.b, c = e.c;
+        const int64_t rloc = static_cast<int64_t>(i2) * PBM + rank * HBM_ROWS + row;
+        if (rloc < p.g.m) {
+            __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + rloc) * p.g.n;
+#pragma unroll
+            for (int q = 0; q < BN / 8; ++q) {
+                const int64_t col = static_cast<int64_t>(c) * BN + q * 8;
+                if (col < p.g.n)
+                    *reinterpret_cast<uint4 *>(yrow + col) =
+                        make_uint4(packed[q * 4], packed[q * 4 + 1], packed[q * 4 + 2], packed[q * 4 + 3]);
+            }
+        }
+        if (leader && e.slot >= 0 && lane == 0 && grp == 0) {
+            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) ag_mxfp8_pair_kernel(const __grid_constant__ AgF8Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const F2Smem fs = carve_f2(smem_raw);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_rank();
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&p.tmA_local);
+        prefetch_tmap(&p.tmA_gath);
+        prefetch_tmap(&p.tmB);
+        prefetch_tmap(&p.tmSA_local);
+        prefetch_tmap(&p.tmSA_gath);
+        prefetch_tmap(&p.tmSW);
+    }
+    const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
+    engine2_setup(fs.base, warp, F2_NSTAGE);
+    const uint32_t tmem_base = *fs.base.tmem_slot;
+    if (warp == 0) {
+        if (lane == 0) f2_producer(p, fs, epoch, rank);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) f2_mma_loop(fs, tmem_base, p.ws);
+    } else {
+        f2_epilogue(p, fs.base, tmem_base, warp, lane, rank);
+    }
+    engine2_teardown(fs.base, warp, tmem_base);
+    if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
+}
+
+int ag_mxfp8_pair_grid_limit() {
+    return max_pair_ctas(reinterpret_cast<const void *>(&ag_mxfp8_pair_kernel), F2_SMEM_BYTES);
+}
+
 // Unfused baseline, first launch: gather elements and scale blocks of every shard.
 __global__ void __launch_bounds__(256) ag_f8_gather_copy_kernel(const AgF8Params p) {
     const int64_t shard_bytes = p.g.m * p.g.k;
@@ -411,10 +735,37 @@ kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream) {
     p.n_comm = L.n_comm;
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;
+    if (L.pair) {
+        p.g = ag_geom(L.P, L.m, L.k, L.n, PBM);
+        p.n_comm = (L.n_comm + 1) / 2;  // mover pairs
+        const uint32_t box[2] = {16, 32};
+        const uint64_t st[1] = {16};
+        {
+            const uint64_t dims[2] = {16, static_cast<uint64_t>(p.g.pieces) * p.nkb * 32};
+            if (!encode_tmap(&p.tmSA_local, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.xs[0]), dims, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+                return KOSMOS_ERR_CUDA;
+        }
+        {
+            const uint64_t dims[2] = {16, static_cast<uint64_t>(L.P) * p.g.pieces * p.nkb * 32};
+            if (!encode_tmap(&p.tmSA_gath, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.sx_gath, dims, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+                return KOSMOS_ERR_CUDA;
+        }
+        {
+            const uint64_t dims[2] = {16, static_cast<uint64_t>(p.nb_w) * p.nkb * 32};
+            if (!encode_tmap(&p.tmSW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.wsc), dims, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+                return KOSMOS_ERR_CUDA;
+        }
+    }
     if (L.sched == KOSMOS_SCHED_UNFUSED) {
         ag_f8_gather_copy_kernel<<<L.grid * 4, 256, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return KOSMOS_ERR_CUDA;
     }
+    if (L.pair)
+        return launch_persistent_pairs(reinterpret_cast<const void *>(&ag_mxfp8_pair_kernel), &p, L.grid,
+                                       F2_SMEM_BYTES, stream, L.plain_launch != 0);
     return launch_persistent(reinterpret_cast<const void *>(&ag_mxfp8_kernel), &p, L.grid, F_SMEM_BYTES, stream,
                              L.plain_launch != 0);
 }

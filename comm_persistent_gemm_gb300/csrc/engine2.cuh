@@ -160,19 +160,21 @@ __device__ __forceinline__ Smem2 carve_smem2(uint8_t *raw) {
     return s;
 }
 
-struct PipeState2 {
+template <int NS>
+struct PipeStateN {
     uint32_t stage = 0, phase = 0;
     __device__ __forceinline__ void advance() {
-        if (++stage == NSTAGE2) { stage = 0; phase ^= 1; }
+        if (++stage == NS) { stage = 0; phase ^= 1; }
     }
     __device__ __forceinline__ void advance(int n) {
         for (int i = 0; i < n; ++i) advance();
     }
 };
+using PipeState2 = PipeStateN<NSTAGE2>;
 
-__device__ __forceinline__ void engine2_setup(const Smem2 &sm, int warp) {
+__device__ __forceinline__ void engine2_setup(const Smem2 &sm, int warp, int nstage = NSTAGE2) {
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSTAGE2; ++i) {
+        for (int i = 0; i < nstage; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], 1);
             mbar_init(&sm.cbar[i], 1);

@@ -206,9 +206,9 @@ struct AgPlan {
 kosmos_status ag_plan(int P, int64_t m, int64_t k, int64_t n, int dtype, const kosmos_opts &o, AgPlan &pl) {
     int grid = grid_for(o);
     if (grid < 1) return KOSMOS_ERR_CUDA;
-    int pair = (dtype == KOSMOS_BF16 && o.cta_pair != 0) ? 1 : 0;
+    int pair = o.cta_pair != 0 ? 1 : 0;
     if (pair) {
-        const int lim = ag_pair_grid_limit();
+        const int lim = dtype == KOSMOS_BF16 ? ag_pair_grid_limit() : ag_mxfp8_pair_grid_limit();
         int g2 = grid & ~1;
         if (lim >= 2 && g2 > lim) g2 = lim;
         if (lim < 2 || g2 < 2) {

@@ -106,6 +106,7 @@ kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order,
                                  int64_t split,
                                  int32_t *out, int64_t count, cudaStream_t stream);
 int ag_pair_grid_limit();
+int ag_mxfp8_pair_grid_limit();
 int rs_pair_grid_limit();
 
 }  // namespace kosmos

@@ -1,7 +1,7 @@
 """Runs one traced launch of each fused operator on the full-size synthetic
 workloads and writes Chrome traces plus the role time accounting.
 
-    python -m comm_persistent_gemm_gb300.trace_run --out DIR [--only ag,rs,moe]
+    python -m comm_persistent_gemm_gb300.trace_run --out DIR [--only ag,rs,moe,mxfp8]
 
 Output: DIR/<name>.trace.json (chrome://tracing / Perfetto) and one JSON line
 per traced launch on stdout with the summary of trace.summarize().
@@ -33,6 +33,34 @@ def _trace_ag(K, out, name, o):
     K.ag_gemm(xs, W, xg, y, ws, o)
     K.check(ws, name)
     return K.trace_records(K.OP_AG_GEMM, w.P, w.m, w.n, w.k, ws, o)
+
+
+def _trace_mxfp8(K, out, name, o):
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS["ag_mxfp8_p8"]
+    inp = workload_inputs(w)
+
+    def quant(x, along):
+        r, c = x.shape
+        q = torch.empty(r, c, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(K.mxfp8_scale_bytes(r, c, along), dtype=torch.uint8, device="cuda")
+        K.mxfp8_quantize(x.cuda(), q, sc, along)
+        return q, sc
+
+    qs, ss = zip(*[quant(x, True) for x in inp["x"]])
+    qw, sw = quant(inp["w"], False)
+    xg = torch.empty(w.P * w.m, w.k, dtype=torch.uint8, device="cuda")
+    y = torch.empty(w.P * w.m, w.n, dtype=torch.bfloat16, device="cuda")
+    ws = K.workspace(K.OP_AG_GEMM, w.P, w.m, w.n, w.k, dtype=K.MXFP8_E4M3, o=o)
+    run = lambda: K.ag_gemm(list(qs), qw, xg, y, ws, o, dtype=K.MXFP8_E4M3, x_scales=list(ss), w_scales=sw)
+    for _ in range(3):
+        run()
+    K.check(ws, name)
+    ws.zero_()
+    run()
+    K.check(ws, name)
+    return K.trace_records(K.OP_AG_GEMM, w.P, w.m, w.n, w.k, ws, o, dtype=K.MXFP8_E4M3)
 
 
 def _trace_rs(K, out, name, o):
@@ -102,6 +130,8 @@ def main(argv=None):
         runs += [("ag_self", _trace_ag, K.opts(trace=1, tail_split=ts)),
                  ("ag_fixed19", _trace_ag, K.opts(trace=1, sched=K.SCHED_FIXED, fixed_comm_ctas=-(-sms // 8),
                                                   tail_split=ts))]
+    if "mxfp8" in only:
+        runs += [("ag_mxfp8_self", _trace_mxfp8, K.opts(trace=1))]
     if "rs" in only:
         runs += [("rs_band", _trace_rs, K.opts(trace=1)), ("rs_row", _trace_rs, K.opts(trace=1, order=K.ORDER_ROW))]
     if "moe" in only:

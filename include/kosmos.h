@@ -102,7 +102,7 @@ typedef struct kosmos_opts {
     int32_t order;            /* KOSMOS_ORDER_* (GEMM+RS) */
     int32_t num_ctas;         /* -1 = one CTA per SM */
     int32_t trace;            /* nonzero: record a per-entry role trace in the workspace */
-    int32_t cta_pair;         /* bf16 AG / RS tiles: 1 = 256x256 per SM pair (tcgen05 cta_group::2),
+    int32_t cta_pair;         /* AG (bf16, MXFP8) / RS tiles: 1 = 256x256 per SM pair (tcgen05 cta_group::2),
                                  0 = 128x256 per SM; -1 = default (pairs) */
     int32_t plain_launch;     /* 0 = cooperative launch (the driver guarantees every CTA is resident);
                                  1 = the same grid as a plain launch, for profilers that cannot replay

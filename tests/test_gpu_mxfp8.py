@@ -94,13 +94,16 @@ def oracle_f8(orc, inp, rows=None):
 
 
 SCHEDS = {"self": 0, "fixed": 1, "unfused": 2}
+PAIR = {"pair": 1, "single": 0}
 
 
+@pytest.mark.parametrize("mode", list(PAIR))
 @pytest.mark.parametrize("sched", list(SCHEDS))
-@pytest.mark.parametrize("P,m,k,n", [(2, 64, 128, 128), (3, 200, 256, 272), (1, 128, 384, 256), (4, 130, 128, 512)])
-def test_ag_mxfp8_small(K, orc, sched, P, m, k, n):
+@pytest.mark.parametrize("P,m,k,n", [(2, 64, 128, 128), (3, 200, 256, 272), (1, 128, 384, 256), (4, 130, 128, 512),
+                                     (2, 300, 256, 400)])
+def test_ag_mxfp8_small(K, orc, sched, P, m, k, n, mode):
     inp = ag_inputs(P, m, k, n, seed=500 + P * m + n, var_w=1.0 / k)
-    qs, xg, outs = run_f8(K, inp, K.opts(sched=SCHEDS[sched]), reps=2)
+    qs, xg, outs = run_f8(K, inp, K.opts(sched=SCHEDS[sched], cta_pair=PAIR[mode]), reps=2)
     ref = oracle_f8(orc, inp)
     got = bf16_tensor_to_f64(outs[0])
     assert not np.isnan(got).any()
@@ -109,10 +112,11 @@ def test_ag_mxfp8_small(K, orc, sched, P, m, k, n):
     assert torch.equal(xg, torch.cat(qs, 0))
 
 
-def test_ag_mxfp8_full_size_sampled(K, orc):
+@pytest.mark.parametrize("mode", list(PAIR))
+def test_ag_mxfp8_full_size_sampled(K, orc, mode):
     w = WORKLOADS["ag_mxfp8_p8"]
     inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
-    qs, xg, outs = run_f8(K, inp, K.opts(), reps=2)
+    qs, xg, outs = run_f8(K, inp, K.opts(cta_pair=PAIR[mode]), reps=2)
     rows = np.unique(np.concatenate([sample_indices(w.P * w.m, 16, seed=3), np.arange(w.P) * w.m,
                                      np.arange(w.P) * w.m + w.m - 1]))
     ref = oracle_f8(orc, inp, rows=rows)
@@ -120,3 +124,23 @@ def test_ag_mxfp8_full_size_sampled(K, orc):
     assert rel_err(got, ref) <= TOL, rel_err(got, ref)
     assert torch.equal(outs[0], outs[1])
     assert torch.equal(xg, torch.cat(qs, 0))
+
+
+def test_ag_mxfp8_pair_and_single_agree(K):
+    """Both tile engines on the full 8-rank MXFP8 workload: the same sums in
+    another order, equal within tolerance."""
+    w = WORKLOADS["ag_mxfp8_p8"]
+    inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
+    _, _, a = run_f8(K, inp, K.opts(cta_pair=1))
+    _, _, b = run_f8(K, inp, K.opts(cta_pair=0))
+    assert rel_err(bf16_tensor_to_f64(a[0]), bf16_tensor_to_f64(b[0])) <= TOL
+
+
+@pytest.mark.parametrize("n_comm0", [1, 40])
+def test_ag_mxfp8_pair_mover_counts_and_few_ctas(K, orc, n_comm0):
+    inp = ag_inputs(4, 256, 256, 512, seed=88, var_w=1.0 / 256)
+    ref = oracle_f8(orc, inp)
+    for o in (K.opts(cta_pair=1, n_comm0=n_comm0), K.opts(cta_pair=1, num_ctas=6, n_comm0=2),
+              K.opts(cta_pair=1, num_ctas=4, sched=1, fixed_comm_ctas=2)):
+        _, _, outs = run_f8(K, inp, o)
+        assert rel_err(bf16_tensor_to_f64(outs[0]), ref) <= TOL
