@@ -32,7 +32,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one ag_gemm_kernel launch on the 8-rank AG
 # workload, from an ncu capture; valid only while the kernel sources hash to
 # src_sha (otherwise the bench reports traffic = null).
-TRAFFIC_CAPTURE = {"bytes": 815280128, "src_sha": "efc52f44e16c953d"}
+TRAFFIC_CAPTURE = {"bytes": 836141824, "src_sha": "884ccf99a95d520b"}
 KERNEL_SOURCES = ["comm_persistent_gemm_gb300/csrc/ag_gemm.cu", "comm_persistent_gemm_gb300/csrc/engine.cuh",
                   "comm_persistent_gemm_gb300/csrc/engine2.cuh", "comm_persistent_gemm_gb300/csrc/ptx.cuh",
                   "comm_persistent_gemm_gb300/csrc/common.cuh"]
