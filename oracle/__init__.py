@@ -60,6 +60,8 @@ def lib():
         L.orc_ag_gemm_mxfp8.argtypes = [C.c_int, i64, i64, i64, P, P, P, P, P, i64, P]
         L.orc_gemm_rs.restype = C.c_int
         L.orc_gemm_rs.argtypes = [C.c_int, i64, i64, i64, P, P, P, i64, P]
+        L.orc_gemm_rs_mxfp8.restype = C.c_int
+        L.orc_gemm_rs_mxfp8.argtypes = [C.c_int, i64, i64, i64, P, P, P, P, P, i64, P]
         L.orc_topk_f32.restype = C.c_int
         L.orc_topk_f32.argtypes = [i64, C.c_int, C.c_int, P, P]
         L.orc_moe_dispatch_tables.restype = C.c_int
@@ -196,6 +198,26 @@ def gemm_rs(x_bits: List[np.ndarray], w_bits: List[np.ndarray],
     rc = lib().orc_gemm_rs(P, m, k, n, _ptr_array(xs), _ptr_array(ws), rp, nrows, _ptr(y))
     if rc:
         raise ValueError("orc_gemm_rs failed")
+    return y
+
+
+def gemm_rs_mxfp8(qx: List[np.ndarray], sx: List[np.ndarray], qw: List[np.ndarray], sw: List[np.ndarray],
+                  rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """Rows of Y = sum_r dequant(X_r) dequant(W_r); scales row-major [rows, k/32]
+    for X_r and [n, k/32] for W_r (as mxfp8_quantize returns them)."""
+    P = len(qx)
+    m, k = qx[0].shape
+    n = qw[0].shape[1]
+    nrows = m if rows is None else len(rows)
+    y = np.empty((nrows, n), dtype=np.float64)
+    arrs = [[np.ascontiguousarray(a) for a in lst] for lst in (qx, sx, qw, sw)]
+    rp = None
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        rp = _ptr(rows)
+    rc = lib().orc_gemm_rs_mxfp8(P, m, k, n, *[_ptr_array(a) for a in arrs], rp, nrows, _ptr(y))
+    if rc:
+        raise ValueError("orc_gemm_rs_mxfp8 failed")
     return y
 
 

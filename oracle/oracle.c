@@ -257,6 +257,51 @@ ORC_EXPORT int orc_gemm_rs(int P, int64_t m, int64_t k, int64_t n,
     return bad ? 1 : 0;
 }
 
+/* MXFP8 GEMM + reduce-scatter [abstract: the MXFP8 results cover the whole
+ * TP+SP layer; same definition as orc_gemm_rs]: Y = sum_r dequant(X_r) .
+ * dequant(W_r), each element e4m3 x 2^(scale - 127) exactly in fp64; X_r
+ * scales [m, k/32] (one per row and 32 K), W_r scales [n, k/32] (one per
+ * column and 32 K), row-major.  Ranks summed in order 0..P-1 per row. */
+ORC_EXPORT int orc_gemm_rs_mxfp8(int P, int64_t m, int64_t k, int64_t n,
+                                 const uint8_t *const *qx, const uint8_t *const *sx,
+                                 const uint8_t *const *qw, const uint8_t *const *sw,
+                                 const int64_t *rows, int64_t nrows, double *y) {
+    if (k % 32) return 1;
+    if (!rows) nrows = m;
+    int64_t kb = k / 32;
+    double *wd = (double *)malloc(sizeof(double) * (size_t)(P * k * n));
+    if (!wd) return 2;
+    for (int r = 0; r < P; r++)
+        for (int64_t kk = 0; kk < k; kk++)
+            for (int64_t j = 0; j < n; j++)
+                wd[(int64_t)r * k * n + kk * n + j] =
+                    ldexp(orc_e4m3_to_f64(qw[r][kk * n + j]), (int)sw[r][j * kb + kk / 32] - 127);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *part = (double *)malloc(sizeof(double) * (size_t)n);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < nrows; t++) {
+            int64_t g = rows ? rows[t] : t;
+            if (g < 0 || g >= m || !part) { bad = 1; continue; }
+            double *acc = y + t * n;
+            for (int64_t j = 0; j < n; j++) acc[j] = 0.0;
+            for (int r = 0; r < P; r++) {
+                for (int64_t j = 0; j < n; j++) part[j] = 0.0;
+                for (int64_t kk = 0; kk < k; kk++) {
+                    double a = ldexp(orc_e4m3_to_f64(qx[r][g * k + kk]), (int)sx[r][g * kb + kk / 32] - 127);
+                    const double *wrow = wd + (int64_t)r * k * n + kk * n;
+                    for (int64_t j = 0; j < n; j++) part[j] += a * wrow[j];
+                }
+                for (int64_t j = 0; j < n; j++) acc[j] += part[j];
+            }
+        }
+        free(part);
+    }
+    free(wd);
+    return bad ? 1 : 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* MoE expert layer (forward)                                                */
 /* ------------------------------------------------------------------------ */

@@ -122,3 +122,31 @@ def test_mxfp8_gemm_vs_dequantised_numpy(orc):
     # a transposed scale layout would blow this up)
     ref = np.concatenate([_f64(x) for x in inp["x"]]) @ _f64(inp["w"])
     assert np.max(np.abs(y - ref)) <= 0.1 * np.max(np.abs(ref))
+
+
+def test_mxfp8_rs_vs_dequantised_numpy_and_bf16_path(orc):
+    """MXFP8 RS = sum_r of the dequantised products (numpy, torch's E4M3
+    decode); equals the bf16 RS oracle on the dequantised values (exactly
+    representable in bf16); a rank-order or scale-layout mistake fails."""
+    P, m, k, n = 3, 12, 64, 16
+    inp = rs_inputs(P, m, k, n, seed=32, var_w=1.0 / (P * k))
+    qx, sx = zip(*[orc.mxfp8_quantize(bf16_bits(x), along_cols=True) for x in inp["x"]])
+    qw, sw = zip(*[orc.mxfp8_quantize(bf16_bits(w), along_cols=False) for w in inp["w"]])
+    y = orc.gemm_rs_mxfp8(list(qx), list(sx), list(qw), list(sw))
+
+    def deq(q, s, along_cols):
+        v = torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy()
+        e = s.astype(np.int64) - 127
+        sc = np.repeat(e, 32, axis=1) if along_cols else np.repeat(e, 32, axis=1).T
+        return np.ldexp(v, sc)
+
+    Xd = [deq(q, s, True) for q, s in zip(qx, sx)]
+    Wd = [deq(q, s, False) for q, s in zip(qw, sw)]
+    np.testing.assert_allclose(y, sum(a @ b for a, b in zip(Xd, Wd)), rtol=1e-12, atol=1e-12)
+    # the dequantised operands are bf16 values: the bf16 oracle gives the same sums
+    to_bits = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert all(np.array_equal(torch.from_numpy(a).to(torch.bfloat16).double().numpy(), a) for a in Xd + Wd)
+    y2 = orc.gemm_rs([to_bits(a) for a in Xd], [to_bits(b) for b in Wd])
+    np.testing.assert_allclose(y, y2, rtol=1e-13, atol=1e-13)
+    rows = np.array([0, 5, 11])
+    np.testing.assert_array_equal(orc.gemm_rs_mxfp8(list(qx), list(sx), list(qw), list(sw), rows=rows), y[rows])
