@@ -355,6 +355,54 @@ def bench_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=True)
             "fixed_split_tflops": fx, "unfused_tflops": un, "vs_fixed_split": tf / fx, "vs_unfused": tf / un}
 
 
+def bench_rs_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=True):
+    """GEMM + reduce-scatter on MXFP8 operands, the shapes of the 8-rank bf16
+    workload (X_r [8192, 3584], W_r [3584, 8192]); band order, with the
+    row-order ablation and the unfused baseline.  Peak as for the MXFP8
+    all-gather: the measured bf16 dense peak x 2."""
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS["rs_mxfp8_p8"]
+    inp = workload_inputs(w)
+    P, m, k, n = w.P, w.m, w.k, w.n
+
+    def quant(x, along):
+        r, c = x.shape
+        q = torch.empty(r, c, dtype=torch.uint8, device=dev)
+        sc = torch.empty(K.mxfp8_scale_bytes(r, c, along), dtype=torch.uint8, device=dev)
+        K.mxfp8_quantize(x.to(dev), q, sc, along, stream=stream)
+        return q, sc
+
+    qx, sx = zip(*[quant(x, True) for x in inp["x"]])
+    qw, sw = zip(*[quant(x, False) for x in inp["w"]])
+    del inp
+    ys = [torch.empty(m // P, n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    flops = w.flops()
+    peak = 2.0 * bf16_peak
+
+    def timed(o):
+        wsb = K.workspace(K.OP_GEMM_RS, P, m, n, k, dtype=K.MXFP8_E4M3, o=o, device=dev)
+        f = lambda: K.gemm_rs(list(qx), list(qw), ys, wsb, o, stream=stream, dtype=K.MXFP8_E4M3,
+                              x_scales=list(sx), w_scales=list(sw))
+        f()
+        K.check(wsb, "gemm_rs mxfp8")
+        t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
+        K.check(wsb, "gemm_rs mxfp8")
+        return flops / (t * 1e-3) / 1e12, t
+
+    tf, ms = timed(K.opts(**(QUICK_OPTS if not baselines else {})))
+    r = {"workload": "rs_mxfp8_p8", "ms": ms, "tflops": tf, "peak": peak, "frac_of_peak": tf / peak}
+    if not baselines:
+        return r
+    row, row_ms = timed(K.opts(order=K.ORDER_ROW))
+    fx, _ = timed(K.opts(sched=K.SCHED_FIXED))
+    un, _ = timed(K.opts(sched=K.SCHED_UNFUSED))
+    r.update({"peak_source": "measured bf16 dense x 2 (nominal fp8/bf16 ratio)", "row_order_ms": row_ms,
+              "row_over_band": row_ms / ms, "fixed_split_tflops": fx, "unfused_tflops": un,
+              "vs_fixed_split": tf / fx, "vs_unfused": tf / un})
+    return r
+
+
 def run_reference(args):
     ws, rank, local = dist_env()
     if ws > 1 and rank != 0:
@@ -399,6 +447,8 @@ def run_quick_other(args):
     elif args.workload == "moe":
         r = bench_moe(K, dev, args.steps, args.warmup, flush, stream, peaks["hbm_gbs"], peaks["bf16_tflops"],
                       experts=args.experts)
+    elif args.workload == "rs_mxfp8":
+        r = bench_rs_mxfp8(K, dev, args.steps, args.warmup, flush, stream, peaks["bf16_tflops"], baselines=False)
     else:
         r = bench_mxfp8(K, dev, args.steps, args.warmup, flush, stream, peaks["bf16_tflops"], baselines=False)
     print(json.dumps({"quick": True, "workload": args.workload, **r}))
@@ -527,6 +577,8 @@ def run_kosmos(args):
         torch.cuda.empty_cache()
         also["ag_mxfp8"] = bench_mxfp8(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
+        also["rs_mxfp8"] = bench_rs_mxfp8(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
+        torch.cuda.empty_cache()
 
     line = None
     if rank == 0:
@@ -555,7 +607,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kosmos", choices=["kosmos", "reference"])
     ap.add_argument("--ag-only", action="store_true", help="skip the GEMM+RS and MoE measurements")
-    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8"],
+    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8", "rs_mxfp8"],
                     help="with --quick: which fused operator to time")
     ap.add_argument("--experts", type=int, default=0, help="with --quick --workload moe: expert count (0 = 128)")
     ap.add_argument("--num-ctas", type=int, default=0,

@@ -82,7 +82,7 @@ def lib():
     L.kosmos_ag_gemm.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, i32, vp, vp, vp, C.c_size_t,
                                  C.POINTER(Opts), vp]
     L.kosmos_ag_gemm.restype = i32
-    L.kosmos_gemm_rs.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, C.c_size_t, C.POINTER(Opts), vp]
+    L.kosmos_gemm_rs.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, vp, vp, C.c_size_t, C.POINTER(Opts), vp]
     L.kosmos_gemm_rs.restype = i32
     L.kosmos_moe_fwd.argtypes = [vp, vp, i32, i64, i64, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                  C.c_size_t, C.POINTER(Opts), vp]
@@ -203,13 +203,16 @@ def ag_gemm_noalloc(x_shards: List, w, x_gathered, y, o: Optional[Opts] = None, 
     _raise(rc, "kosmos_ag_gemm_noalloc")
 
 
-def gemm_rs(x_shards: List, w_shards: List, y_chunks: List, ws, o: Optional[Opts] = None, stream=None):
-    """y_chunks[c] = rows [c*m/P, (c+1)*m/P) of sum_r x_shards[r] @ w_shards[r]."""
-    _check_cuda(*x_shards, *w_shards, *y_chunks, ws)
+def gemm_rs(x_shards: List, w_shards: List, y_chunks: List, ws, o: Optional[Opts] = None, stream=None,
+            dtype: int = BF16, x_scales: Optional[List] = None, w_scales: Optional[List] = None):
+    """y_chunks[c] = rows [c*m/P, (c+1)*m/P) of sum_r x_shards[r] @ w_shards[r]
+    (MXFP8: E4M3 bytes with MMA-tiled E8M0 scales)."""
+    _check_cuda(*x_shards, *w_shards, *y_chunks, ws, *(x_scales or []), *(w_scales or []))
     P = len(x_shards)
     m, k = x_shards[0].shape
     n = w_shards[0].shape[1]
-    rc = lib().kosmos_gemm_rs(_ptrs(x_shards), _ptrs(w_shards), P, m, k, n, BF16, _ptrs(y_chunks),
+    rc = lib().kosmos_gemm_rs(_ptrs(x_shards), _ptrs(x_scales) if x_scales else None, _ptrs(w_shards),
+                              _ptrs(w_scales) if w_scales else None, P, m, k, n, dtype, _ptrs(y_chunks),
                               ws.data_ptr(), ws.numel(), C.byref(o) if o is not None else None, _stream(stream))
     _raise(rc, "kosmos_gemm_rs")
 

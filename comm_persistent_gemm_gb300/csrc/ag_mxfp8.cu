@@ -20,19 +20,16 @@
 
 #include <cstring>
 
-#include "engine2.cuh"
+#include "mxfp8.cuh"
 #include "launch.h"
 
 namespace kosmos {
 
-constexpr int FBK = 128;                       // K elements (bytes) per stage
 constexpr int F_A_BYTES = BM * FBK;            // 16 KB
 constexpr int F_B_SLAB = 128 * FBK;            // one 128-column slab of B: 16 KB
 constexpr int F_B_BYTES = 2 * F_B_SLAB;        // 32 KB
 constexpr int F_SF_BYTES = 3 * 512;            // SFA atom + two SFB atoms
 constexpr int F_SMEM_BYTES = SMEM_BYTES + NSTAGE * F_SF_BYTES;
-constexpr int F_TMEM_SF = 256;                 // first TMEM column of the scale buffers
-constexpr int F_TMEM_SF_STRIDE = 16;           // columns per stage: SFA 4, SFB 8 (+4 spare)
 
 struct AgF8Params {
     CUtensorMap tmA_local;  // x_shards[0]: dims {k, m} (bytes), box {128, 128}, 128B swizzle
@@ -75,25 +72,6 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uin
 // replicated to the four 32-lane groups.
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// Descriptor of a 32-row x 16-byte matrix stored contiguously (rows 16 bytes
-// apart; 8-row core matrices 128 bytes apart), no swizzle.
-__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(128 >> 4) << 16;  // leading byte offset (one 16-byte column: unused)
-    d |= static_cast<uint64_t>(128 >> 4) << 32;  // stride byte offset between 8-row core matrices
-    d |= static_cast<uint64_t>(1) << 46;
-    return d;
-}
-
-// Instruction descriptor, kind::mxf8f6f4 block-scaled: A/B E4M3 (format 0),
-// A K-major, B MN-major, scale type E8M0 (bit 23), N >> 3 at bits 17-22,
-// M >> 4 at bits 24-28, B scale byte at bits 4-5, A scale byte at bits 29-30.
-__device__ __forceinline__ uint32_t idesc_mxf8(int M, int N, int sf_id) {
-    return (static_cast<uint32_t>(sf_id) << 4) | (1u << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
 }
 
 struct F8Smem {
@@ -352,59 +330,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_mxfp8_kernel(const __grid_c
 // its rows (SFA) and the scale atoms of all 256 columns (SFB); the leader's
 // tcgen05.cp.cta_group::2 copies every CTA's atoms into that CTA's tensor
 // memory, where the pair MMA reads SFA of the CTA's rows and SFB of the whole
-// tile (the placement was checked on the GB300 against exact results).
-constexpr int F2_NSTAGE = 6;
-constexpr int F2_A_BYTES = HBM_ROWS * FBK;             // 16 KB
-constexpr int F2_B_BYTES = HBN * FBK;                  // 16 KB
-constexpr int F2_STAGE = F2_A_BYTES + F2_B_BYTES;
-constexpr int F2_SF = 3 * 512;                         // SFA atom + two SFB atoms
-constexpr int F2_SMEM_BYTES = F2_NSTAGE * (F2_STAGE + F2_SF) + SMEM2_CTRL + 1024;
-static_assert(F2_SMEM_BYTES <= 232448, "MXFP8 pair engine exceeds 227 KB of shared memory per CTA");
-using PipeF2 = PipeStateN<F2_NSTAGE>;
-
-struct F2Smem {
-    Smem2 base;
-    uint8_t *sf;  // [F2_NSTAGE][F2_SF]
-};
-
-__device__ __forceinline__ F2Smem carve_f2(uint8_t *raw) {
-    const uintptr_t b0 = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
-    uint8_t *p = reinterpret_cast<uint8_t *>(b0);
-    F2Smem f;
-    Smem2 &s = f.base;
-    s.stages = p;
-    p += F2_NSTAGE * F2_STAGE;
-    f.sf = p;
-    p += F2_NSTAGE * F2_SF;
-    uint64_t *b = reinterpret_cast<uint64_t *>(p);
-    s.full = b; b += F2_NSTAGE;
-    s.empty = b; b += F2_NSTAGE;
-    s.cbar = b; b += F2_NSTAGE;
-    s.tfull = b; b += 2;
-    s.tempty = b; b += 2;
-    s.sfull = b; b += NSCHED;
-    s.sempty = b; b += NSCHED;
-    s.pempty = b; b += NSCHED;
-    s.sched = reinterpret_cast<SchedEntry *>(b);
-    s.tmem_slot = reinterpret_cast<uint32_t *>(s.sched + NSCHED);
-    return f;
-}
-
-__device__ __forceinline__ void mma2_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-// Issued by the leader: each CTA of the pair copies its own shared-memory
-// atom into its own tensor memory.
-__device__ __forceinline__ void tmem_cp2_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
+// tile (the placement was checked on the GB300 against exact results); the
+// stage layout and MMA loop are in mxfp8.cuh.
 
 // This CTA's half of one K stage of tile (s, i2, c): A rows of piece pc, B
 // columns [col0, col0 + 128), the piece's scale atom and the tile's two W
@@ -530,57 +457,6 @@ __device__ __forceinline__ void f2_producer(const AgF8Params &p, const F2Smem &f
             }
             if (!ok) break;
         }
-    }
-}
-
-// Leader only: per stage, copy the pair's scale atoms into tensor memory, then
-// four K = 32 block-scaled MMAs into the single accumulator (columns 0-255).
-__device__ __forceinline__ void f2_mma_loop(const F2Smem &fs, uint32_t tmem_base, WsHeader *ws) {
-    const Smem2 &sm = fs.base;
-    PipeF2 ps;
-    RingPair rs;
-    uint32_t acc_phase = 0;
-    while (true) {
-        SchedEntry e;
-        if (!ring2_take(sm, rs, true, e, ws, false)) break;
-        if (e.kind == K_DONE) break;
-        if (e.kind != K_TILE) {
-            ps.advance(e.nstage);
-            continue;
-        }
-        if (!mbar_wait(&sm.tempty[0], acc_phase ^ 1u, PIPE_LIMIT_NS)) {
-            set_error(ws, KOSMOS_ERR_DEVICE, -4);
-            break;
-        }
-        tc_fence_after();
-        bool ok = true;
-        for (int kb = 0; kb < e.nstage; ++kb) {
-            if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
-                set_error(ws, KOSMOS_ERR_DEVICE, -5);
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t a_addr = smem_u32(sm.stages + ps.stage * F2_STAGE);
-            const uint32_t b_addr = a_addr + F2_A_BYTES;
-            const uint32_t sf_addr = smem_u32(fs.sf + ps.stage * F2_SF);
-            const uint32_t sfa_t = tmem_base + F_TMEM_SF + ps.stage * F_TMEM_SF_STRIDE;
-            const uint32_t sfb_t = sfa_t + 4;
-            tmem_cp2_32x128b_x4(sfa_t, sdesc_sf(sf_addr));
-            tmem_cp2_32x128b_x4(sfb_t, sdesc_sf(sf_addr + 512));
-            tmem_cp2_32x128b_x4(sfb_t + 4, sdesc_sf(sf_addr + 1024));
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint64_t ad = sdesc_sw128(a_addr + j * 32, 16, 1024);
-                const uint64_t bd = sdesc_sw128(b_addr + j * (32 * 128), F2_B_BYTES, 1024);
-                mma2_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(PBM, BN, j), sfa_t, sfb_t, (kb | j) != 0 ? 1u : 0u);
-            }
-            mma2_commit_both(&sm.empty[ps.stage]);
-            ps.advance();
-        }
-        if (!ok) break;
-        mma2_commit_both(&sm.tfull[0]);
-        acc_phase ^= 1u;
     }
 }
 

@@ -328,10 +328,11 @@ __device__ __forceinline__ void acc_release(const Smem2 &sm, uint32_t acc, bool 
 
 // Waits until every stage is free again (both CTAs' stages are released by the
 // leader's multicast commits), so the stage buffers can serve as copy buffers.
-__device__ __forceinline__ bool drain_stages2(const Smem2 &sm, const PipeState2 &ps, WsHeader *ws) {
-    for (int i = 0; i < NSTAGE2; ++i) {
+template <int NS>
+__device__ __forceinline__ bool drain_stages2(const Smem2 &sm, const PipeStateN<NS> &ps, WsHeader *ws) {
+    for (int i = 0; i < NS; ++i) {
         uint32_t s = ps.stage + i, ph = ps.phase;
-        if (s >= NSTAGE2) { s -= NSTAGE2; ph ^= 1u; }
+        if (s >= NS) { s -= NS; ph ^= 1u; }
         if (!mbar_wait(&sm.empty[s], ph ^ 1u, PIPE_LIMIT_NS)) {
             set_error(ws, KOSMOS_ERR_DEVICE, -11);
             return false;

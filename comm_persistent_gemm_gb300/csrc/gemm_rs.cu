@@ -18,7 +18,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "engine2.cuh"
+#include "mxfp8.cuh"
 #include "launch.h"
 
 namespace kosmos {
@@ -29,13 +29,17 @@ struct RsParams {
     CUtensorMap tmX[KOSMOS_MAX_P];  // X_r viewed [P chunks][mc][k]: dims {k, mc, P}, box {64, 128, 1}, 128B swizzle
     CUtensorMap tmW[KOSMOS_MAX_P];  // W_r: dims {n, k}, box {64, 64}, 128B swizzle
     CUtensorMap tmPart;             // partials [rank][chunk][mc][n]: dims {n, mc, P, P}, box {256, 8, 1, P}
+    // MXFP8 (SM pairs): tmX/tmW hold E4M3 bytes (boxes {128, 128, 1} / {128, 128}) and these the
+    // tiled scales as rows of 16 bytes, one 512-byte atom per box {16, 32}
+    CUtensorMap tmSX[KOSMOS_MAX_P]; // X_r scales: dims {16, (m / 128) * nkb * 32}
+    CUtensorMap tmSW[KOSMOS_MAX_P]; // W_r scales: dims {16, ceil(n / 128) * nkb * 32}
     __nv_bfloat16 *part;            // [P ranks][m][n]
     __nv_bfloat16 *y[KOSMOS_MAX_P]; // chunk c: [mc][n]
     WsHeader *ws;
     uint32_t *arrive;               // [chunk][band][col] arrival counters
     TraceRec *trace;
     RsGeom g;
-    int nkb;
+    int nkb;                        // K stages: k / 64 (bf16) or k / 128 (MXFP8)
     int sched;
     int n_red;
     int order;
@@ -303,7 +307,45 @@ __device__ __forceinline__ bool red_push(const RedRing &rr, RingState &rs, const
     return true;
 }
 
-__device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm, const RedRing &rr, uint32_t crank) {
+// Stage geometry of the two pair engines: bf16 (7 stages, two accumulators)
+// and MXFP8 (6 stages + scale atoms, one accumulator); both stages are 32 KB,
+// which the reduce phase reuses.
+template <bool MX>
+struct RsPairCfg {
+    static constexpr int NS = MX ? F2_NSTAGE : NSTAGE2;
+    static constexpr int SMEM = MX ? F2_SMEM_BYTES : SMEM2_BYTES;
+    static constexpr int NACC = MX ? 1 : 2;
+};
+static_assert(F2_STAGE == STAGE2_BYTES, "both pair engines reuse 32 KB stages for the reduce phase");
+
+// One CTA's half of one K stage of tile (q, chunk, band, tcol): A rows
+// [row0, row0 + 128) of chunk `chunk` of X_q, B columns [col0, col0 + 128) of
+// W_q; MXFP8 adds the rows' scale atom and the tile's two W scale atoms.
+template <bool MX>
+__device__ __forceinline__ void rs2_load_half(const RsParams &p, const Smem2 &sm, uint8_t *sf, uint32_t stage, int q,
+                                              int chunk, int row0, int col0, int tile_c, int kb, uint32_t fb) {
+    uint8_t *sa = sm.stages + stage * STAGE2_BYTES;
+    if (MX) {
+        uint8_t *sb = sa + F2_A_BYTES;
+        uint8_t *sfs = sf + stage * F2_SF;
+        const int rb = static_cast<int>((static_cast<int64_t>(chunk) * p.g.mc + row0) / BM);  // 128-row scale block
+        tma_load_3d_pair(sa, &p.tmX[q], fb, kb * FBK, row0, chunk);
+        tma_load_2d_pair(sb, &p.tmW[q], fb, col0, kb * FBK);
+        tma_load_2d_pair(sfs, &p.tmSX[q], fb, 0, (rb * p.nkb + kb) * 32);
+        tma_load_2d_pair(sfs + 512, &p.tmSW[q], fb, 0, ((2 * tile_c) * p.nkb + kb) * 32);
+        tma_load_2d_pair(sfs + 1024, &p.tmSW[q], fb, 0, ((2 * tile_c + 1) * p.nkb + kb) * 32);
+    } else {
+        uint8_t *sb = sa + A2_BYTES;
+        tma_load_3d_pair(sa, &p.tmX[q], fb, kb * BK, row0, chunk);
+        tma_load_2d_pair(sb, &p.tmW[q], fb, col0, kb * BK);
+        tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[q], fb, col0 + 64, kb * BK);
+    }
+}
+
+template <bool MX>
+__device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm, uint8_t *sf, const RedRing &rr,
+                                             uint32_t crank) {
+    using Cfg = RsPairCfg<MX>;
     const int P = p.g.P;
     const int pair = blockIdx.x / 2;
     const bool leader = crank == 0;
@@ -311,7 +353,7 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
     // builder pairs build tiles of any rank and reduce for rank (pair index mod P) after the switch
     const bool reducer_pair = (p.mode == RS_REDUCE_ONLY) || (p.mode == RS_FUSED && pair < p.n_red);
     const int rank = (reducer_pair && p.mode == RS_FUSED) ? static_cast<int>(blockIdx.x) % P : pair % P;
-    PipeState2 ps;
+    PipeStateN<Cfg::NS> ps;
     RingPair rs;
     int nrec = 0;
     // ---- tile phase (pair)
@@ -342,13 +384,9 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&sm.full[ps.stage], 2 * STAGE2_BYTES);
-                uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
-                uint8_t *sb = sa + A2_BYTES;
-                const uint32_t fb = my_full0 + ps.stage * 8;
-                tma_load_3d_pair(sa, &p.tmX[q], fb, kb * BK, band * PBM, chunk);
-                tma_load_2d_pair(sb, &p.tmW[q], fb, tcol * BN, kb * BK);
-                tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[q], fb, tcol * BN + 64, kb * BK);
+                mbar_arrive_expect_tx(&sm.full[ps.stage], MX ? 2 * (F2_STAGE + F2_SF) : 2 * STAGE2_BYTES);
+                rs2_load_half<MX>(p, sm, sf, ps.stage, q, chunk, band * PBM, tcol * BN, tcol, kb,
+                                  my_full0 + ps.stage * 8);
                 ps.advance();
             }
             if (!ok) break;
@@ -370,12 +408,8 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
                     ok = false;
                     break;
                 }
-                uint8_t *sa = sm.stages + ps.stage * STAGE2_BYTES;
-                uint8_t *sb = sa + A2_BYTES;
-                const uint32_t fb = leader_full0 + ps.stage * 8;
-                tma_load_3d_pair(sa, &p.tmX[q], fb, kb * BK, band * PBM + HBM_ROWS, chunk);
-                tma_load_2d_pair(sb, &p.tmW[q], fb, tcol * BN + HBN, kb * BK);
-                tma_load_2d_pair(sb + 64 * BK * 2, &p.tmW[q], fb, tcol * BN + HBN + 64, kb * BK);
+                rs2_load_half<MX>(p, sm, sf, ps.stage, q, chunk, band * PBM + HBM_ROWS, tcol * BN + HBN, tcol, kb,
+                                  leader_full0 + ps.stage * 8);
                 ps.advance();
             }
             if (!ok) break;
@@ -385,7 +419,7 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
     RingState rrs;
     const bool reduce = reducer_pair || (p.mode == RS_FUSED && p.sched == KOSMOS_SCHED_SELF);
     if (reduce && drain_stages2(sm, ps, p.ws)) {
-        PipeState2 rp;
+        PipeStateN<Cfg::NS> rp;
         const uint32_t red_bytes = static_cast<uint32_t>(BN * RED_ROWS * 2 * P);
         while (!failed(p.ws)) {
             const uint32_t t = atomicAdd(&p.ws->tickets[KOSMOS_MAX_P + rank], 1u);
@@ -435,8 +469,10 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
     red_push(rr, rrs, done, p.ws);
 }
 
+template <bool MX>
 __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm, const RedRing &rr, uint32_t tmem_base,
                                              int warp, int lane, uint32_t crank) {
+    using Cfg = RsPairCfg<MX>;
     const bool leader = crank == 0;
     const int grp = warp & 3;
     const int row = grp * 32 + lane;
@@ -469,7 +505,7 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
             tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + col0, left < 32 ? static_cast<int>(left) : 32);
         }
         acc_release(sm, acc, leader, lane);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
         if (p.mode == RS_FUSED) {
             __threadfence();
             named_bar_sync(1, NUM_EPI_THREADS);
@@ -483,7 +519,7 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
     }
     // ---- this CTA's reductions
     RingState rrs;
-    PipeState2 rp;
+    PipeStateN<Cfg::NS> rp;
     const int cg = et & 31;
     while (true) {
         if (!mbar_wait(&rr.rsfull[rrs.idx], rrs.phase, PIPE_LIMIT_NS)) {
@@ -541,16 +577,25 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
     }
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_rs_pair_kernel(const __grid_constant__ RsParams p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const Smem2 sm = carve_smem2(smem_raw);
+template <bool MX>
+__device__ __forceinline__ void rs_pair_body(const RsParams &p, uint8_t *smem_raw) {
+    using Cfg = RsPairCfg<MX>;
+    Smem2 sm;
+    uint8_t *sf = nullptr;
+    if (MX) {
+        const F2Smem fs = carve_f2(smem_raw);
+        sm = fs.base;
+        sf = fs.sf;
+    } else {
+        sm = carve_smem2(smem_raw);
+    }
     const RedRing rr = carve_red(sm);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint32_t crank = cluster_rank();
     const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSTAGE2; ++i) {
+        for (int i = 0; i < Cfg::NS; ++i) {
             mbar_init(&rr.rfull[i], 1);
             mbar_init(&rr.rempty[i], 1);
         }
@@ -559,41 +604,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_rs_pair_kernel(const __gr
             mbar_init(&rr.rsempty[i], 4);
         }
     }
-    engine2_setup(sm, warp);
+    engine2_setup(sm, warp, Cfg::NS);
     const uint32_t tmem_base = *sm.tmem_slot;
     if (warp == 0) {
-        if (lane == 0) rs2_producer(p, sm, rr, crank);
+        if (lane == 0) rs2_producer<MX>(p, sm, sf, rr, crank);
     } else if (warp == 1) {
-        if (lane == 0 && crank == 0) mma2_loop(sm, tmem_base, p.ws);
+        if (lane == 0 && crank == 0) {
+            if (MX) {
+                F2Smem fs;
+                fs.base = sm;
+                fs.sf = sf;
+                f2_mma_loop(fs, tmem_base, p.ws);
+            } else {
+                mma2_loop(sm, tmem_base, p.ws);
+            }
+        }
     } else {
-        rs2_epilogue(p, sm, rr, tmem_base, warp, lane, crank);
+        rs2_epilogue<MX>(p, sm, rr, tmem_base, warp, lane, crank);
     }
     engine2_teardown(sm, warp, tmem_base);
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 2 * KOSMOS_MAX_P);
 }
 
-int rs_pair_grid_limit() { return max_pair_ctas(reinterpret_cast<const void *>(&gemm_rs_pair_kernel), SMEM2_BYTES); }
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_rs_pair_kernel(const __grid_constant__ RsParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    rs_pair_body<false>(p, smem_raw);
+}
+
+// MXFP8 operands (E4M3 + E8M0 per 32 K), block-scaled pair MMAs; bf16 partials.
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_rs_mx_pair_kernel(const __grid_constant__ RsParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    rs_pair_body<true>(p, smem_raw);
+}
+
+int rs_pair_grid_limit(bool mx) {
+    return mx ? max_pair_ctas(reinterpret_cast<const void *>(&gemm_rs_mx_pair_kernel), F2_SMEM_BYTES)
+              : max_pair_ctas(reinterpret_cast<const void *>(&gemm_rs_pair_kernel), SMEM2_BYTES);
+}
 
 kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
     RsParams p;
     memset(&p, 0, sizeof(p));
     p.g = rs_geom(L.P, L.m, L.k, L.n);
     const int64_t mc = p.g.mc;
+    const bool mx = L.dtype == KOSMOS_MXFP8_E4M3;
+    const uint64_t esz = mx ? 1 : 2;  // element bytes
+    const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int kstage = mx ? FBK : BK;  // K elements per stage
     for (int r = 0; r < L.P; ++r) {
         {
             const uint64_t dims[3] = {static_cast<uint64_t>(L.k), static_cast<uint64_t>(mc), static_cast<uint64_t>(L.P)};
-            const uint64_t strides[2] = {static_cast<uint64_t>(L.k) * 2, static_cast<uint64_t>(mc * L.k) * 2};
-            const uint32_t box[3] = {BK, BM, 1};
-            if (!encode_tmap(&p.tmX[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(L.x[r]), dims, strides,
-                             box, CU_TENSOR_MAP_SWIZZLE_128B))
+            const uint64_t strides[2] = {static_cast<uint64_t>(L.k) * esz, static_cast<uint64_t>(mc * L.k) * esz};
+            const uint32_t box[3] = {static_cast<uint32_t>(kstage), BM, 1};
+            if (!encode_tmap(&p.tmX[r], dt, 3, const_cast<void *>(L.x[r]), dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
                 return KOSMOS_ERR_CUDA;
         }
         {
             const uint64_t dims[2] = {static_cast<uint64_t>(L.n), static_cast<uint64_t>(L.k)};
-            const uint64_t strides[1] = {static_cast<uint64_t>(L.n) * 2};
-            const uint32_t box[2] = {64, BK};
-            if (!encode_tmap(&p.tmW[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(L.w[r]), dims, strides,
-                             box, CU_TENSOR_MAP_SWIZZLE_128B))
+            const uint64_t strides[1] = {static_cast<uint64_t>(L.n) * esz};
+            const uint32_t box[2] = {mx ? 128u : 64u, static_cast<uint32_t>(kstage)};
+            if (!encode_tmap(&p.tmW[r], dt, 2, const_cast<void *>(L.w[r]), dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+                return KOSMOS_ERR_CUDA;
+        }
+        if (mx) {
+            const uint64_t nkb = static_cast<uint64_t>(L.k / FBK);
+            const uint64_t st[1] = {16};
+            const uint32_t box[2] = {16, 32};
+            const uint64_t dx[2] = {16, static_cast<uint64_t>(L.m / BM) * nkb * 32};
+            if (!encode_tmap(&p.tmSX[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.xs[r]), dx, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+                return KOSMOS_ERR_CUDA;
+            const uint64_t dw[2] = {16, static_cast<uint64_t>(cdiv(L.n, 128)) * nkb * 32};
+            if (!encode_tmap(&p.tmSW[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.ws_[r]), dw, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
                 return KOSMOS_ERR_CUDA;
         }
         p.y[r] = static_cast<__nv_bfloat16 *>(L.y[r]);
@@ -614,15 +699,17 @@ kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return KOSMOS_ERR_CUDA;
     }
-    p.nkb = static_cast<int>(L.k / BK);
+    p.nkb = static_cast<int>(L.k / kstage);
     p.sched = L.sched;
     p.n_red = L.pair ? (L.n_comm * L.P + 1) / 2 : L.n_comm;  // pair kernel: reducer pairs
     p.order = L.order;
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;
-    const void *fn = L.pair ? reinterpret_cast<const void *>(&gemm_rs_pair_kernel)
-                            : reinterpret_cast<const void *>(&gemm_rs_kernel);
-    const int smem = L.pair ? SMEM2_BYTES : SMEM_BYTES;
+    const void *fn = mx       ? reinterpret_cast<const void *>(&gemm_rs_mx_pair_kernel)
+                     : L.pair ? reinterpret_cast<const void *>(&gemm_rs_pair_kernel)
+                              : reinterpret_cast<const void *>(&gemm_rs_kernel);
+    const int smem = mx ? F2_SMEM_BYTES : (L.pair ? SMEM2_BYTES : SMEM_BYTES);
+    if (mx && !L.pair) return KOSMOS_ERR_UNSUPPORTED;
     if (L.pair) p.g = rs_geom(L.P, L.m, L.k, L.n, PBM);
     auto go = [&]() {
         return L.pair ? launch_persistent_pairs(fn, &p, L.grid, smem, stream, L.plain_launch != 0)

@@ -342,18 +342,25 @@ int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t k, int64_t n, int dt
     return 0;
 }
 
-kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_shards, int P, int64_t m,
-                             int64_t k_per_rank, int64_t n, int dtype, void *const *y_chunks, void *ws,
-                             size_t ws_bytes, const kosmos_opts *opts, void *stream) {
+kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *x_scales, const void *const *w_shards,
+                             const void *const *w_scales, int P, int64_t m, int64_t k_per_rank, int64_t n, int dtype,
+                             void *const *y_chunks, void *ws, size_t ws_bytes, const kosmos_opts *opts,
+                             void *stream) {
     if (P < 1 || P > KOSMOS_MAX_P || x_shards == nullptr || w_shards == nullptr || y_chunks == nullptr)
         return KOSMOS_ERR_INVALID_ARG;
     if (m < P || m % P != 0 || k_per_rank < BK || k_per_rank % BK != 0 || n < 8 || n % 8 != 0)
         return KOSMOS_ERR_INVALID_ARG;
     if (m > (1ll << 30) || k_per_rank > (1ll << 24) || n > (1ll << 24)) return KOSMOS_ERR_INVALID_ARG;
-    if (dtype != KOSMOS_BF16) return dtype == KOSMOS_MXFP8_E4M3 ? KOSMOS_ERR_UNSUPPORTED : KOSMOS_ERR_INVALID_ARG;
-    for (int r = 0; r < P; ++r)
+    if (dtype != KOSMOS_BF16 && dtype != KOSMOS_MXFP8_E4M3) return KOSMOS_ERR_INVALID_ARG;
+    const bool mx = dtype == KOSMOS_MXFP8_E4M3;
+    if (mx && ((m / P) % 128 != 0 || k_per_rank % 128 != 0 || n % 16 != 0 || x_scales == nullptr ||
+               w_scales == nullptr))
+        return KOSMOS_ERR_INVALID_ARG;
+    for (int r = 0; r < P; ++r) {
         if (!aligned16(x_shards[r]) || !aligned16(w_shards[r]) || !aligned16(y_chunks[r]))
             return KOSMOS_ERR_INVALID_ARG;
+        if (mx && (!aligned16(x_scales[r]) || !aligned16(w_scales[r]))) return KOSMOS_ERR_INVALID_ARG;
+    }
     if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
     const kosmos_opts o = resolve_opts(opts);
     if (o.sched < KOSMOS_SCHED_SELF || o.sched > KOSMOS_SCHED_UNFUSED) return KOSMOS_ERR_INVALID_ARG;
@@ -363,15 +370,16 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
     int grid = grid_for(o);
     if (grid < 1) return KOSMOS_ERR_CUDA;
     int pair = o.cta_pair != 0 ? 1 : 0;
+    if (mx && !pair) return KOSMOS_ERR_UNSUPPORTED;  // MXFP8 runs on SM pairs only
     if (pair) {
-        const int lim = rs_pair_grid_limit();
+        const int lim = rs_pair_grid_limit(mx);
         int g2 = grid & ~1;
         if (lim >= 2 && g2 > lim) g2 = lim;
         // every emulated rank needs a builder pair; a fixed reducer crew needs at least one
         // reducer CTA per rank on top (two ranks per reducer pair)
         const int need = (o.sched == KOSMOS_SCHED_FIXED) ? 2 * P + 2 * ((P + 1) / 2) : 2 * P;
         if (lim < 2 || g2 < need) {
-            if (o.cta_pair == 1) return KOSMOS_ERR_UNSUPPORTED;
+            if (o.cta_pair == 1 || mx) return KOSMOS_ERR_UNSUPPORTED;
             pair = 0;
         } else {
             grid = g2;
@@ -385,8 +393,11 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_s
         L.x[r] = x_shards[r];
         L.w[r] = w_shards[r];
         L.y[r] = y_chunks[r];
+        L.xs[r] = mx ? x_scales[r] : nullptr;
+        L.ws_[r] = mx ? w_scales[r] : nullptr;
     }
     L.ws = ws;
+    L.dtype = dtype;
     L.sched = o.sched;
     L.pair = pair;
     {

@@ -38,8 +38,11 @@ struct RsLaunch {
     int64_t m, k, n;
     const void *x[KOSMOS_MAX_P];
     const void *w[KOSMOS_MAX_P];
+    const void *xs[KOSMOS_MAX_P];   // MXFP8 scales of X_r
+    const void *ws_[KOSMOS_MAX_P];  // MXFP8 scales of W_r
     void *y[KOSMOS_MAX_P];
     void *ws;
+    int dtype;
     int sched;
     int n_comm;
     int order;
@@ -107,6 +110,6 @@ kosmos_status launch_rail_decode(int op, int P, int64_t m, int64_t n, int order,
                                  int32_t *out, int64_t count, cudaStream_t stream);
 int ag_pair_grid_limit();
 int ag_mxfp8_pair_grid_limit();
-int rs_pair_grid_limit();
+int rs_pair_grid_limit(bool mx = false);
 
 }  // namespace kosmos

@@ -181,15 +181,21 @@ KOSMOS_API int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t k, int64_
  *
  *   Y = sum_{r=0..P-1} X_r . W_r,  chunk c = rows [c*m/P, (c+1)*m/P) of Y
  *
- *   x_shards[r]  : X_r [m, k_per_rank] bf16
- *   w_shards[r]  : W_r [k_per_rank, n] bf16
- *   y_chunks[c]  : out, [m/P, n] bf16: each rank's partial rounded once to
- *                  bf16, the P partials summed in fp32 in rank order 0..P-1,
- *                  the sum rounded once to bf16.
+ *   x_shards[r]  : X_r [m, k_per_rank]; BF16: bf16; MXFP8: E4M3 bytes.
+ *   x_scales[r]  : MXFP8 only: E8M0 scales of X_r (one per row and 32 K),
+ *                  MMA-tiled as for kosmos_ag_gemm; else NULL.
+ *   w_shards[r]  : W_r [k_per_rank, n]; BF16: bf16; MXFP8: E4M3 bytes.
+ *   w_scales[r]  : MXFP8 only: E8M0 scales of W_r (one per column and 32 K),
+ *                  MMA-tiled with the columns as scale rows; else NULL.
+ *   y_chunks[c]  : out, [m/P, n] bf16: each rank's partial (fp32 accumulation)
+ *                  rounded once to bf16, the P partials summed in fp32 in rank
+ *                  order 0..P-1, the sum rounded once to bf16.
  *   Requirements: 1 <= P <= 8, m % P == 0, k_per_rank % 64 == 0, n % 8 == 0;
- *   BF16 only.
+ *   MXFP8: SM-pair tiles only (cta_pair != 0), (m/P) % 128 == 0,
+ *   k_per_rank % 128 == 0, n % 16 == 0.
  */
-KOSMOS_API kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *w_shards, int P,
+KOSMOS_API kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *x_scales,
+                             const void *const *w_shards, const void *const *w_scales, int P,
                              int64_t m, int64_t k_per_rank, int64_t n, int dtype,
                              void *const *y_chunks, void *ws, size_t ws_bytes,
                              const kosmos_opts *opts, void *stream);

@@ -76,6 +76,9 @@ WORKLOADS: Dict[str, Workload] = {
     "ag_mxfp8_p8": Workload("ag_mxfp8_p8", "ag", seed=3, P=8, m=1024, k=8192, n=3584, dtype="mxfp8",
                             var_x=1.0, var_w=1.0 / 8192,
                             note="AG-GEMM MXFP8 (E4M3 + E8M0 per 32 K), shapes of ag_bf16_p8"),
+    "rs_mxfp8_p8": Workload("rs_mxfp8_p8", "rs", seed=5, P=8, m=8192, k=3584, n=8192, dtype="mxfp8",
+                            var_x=1.0, var_w=1.0 / 28672,
+                            note="GEMM+RS MXFP8 (E4M3 + E8M0 per 32 K), shapes of rs_bf16_p8"),
     "moe_fwd_p8": Workload("moe_fwd_p8", "moe", seed=4, P=8, T=2048, H=4096, E=128, topk=8, I=1536,
                            var_x=1.0, var_w=1.0,
                            note="MoE forward, 2048 tokens, hidden 4096, 128 experts top-8, 8 EP ranks x 16, I=1536"),

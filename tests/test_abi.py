@@ -62,7 +62,9 @@ def test_host_validation_rejects_bad_args(K):
     assert lib.kosmos_ag_gemm(xs, None, P, 64, 128, 128, base, None, 0, base, base, base, 16, None, None) == 3
     # RS: m not divisible by P
     ys = (C.c_void_p * P)(base, base)
-    assert lib.kosmos_gemm_rs(xs, xs, P, 63, 64, 64, 0, ys, base, 1 << 20, None, None) == 1
+    assert lib.kosmos_gemm_rs(xs, None, xs, None, P, 63, 64, 64, 0, ys, base, 1 << 20, None, None) == 1
+    # RS MXFP8 without scales
+    assert lib.kosmos_gemm_rs(xs, None, xs, None, P, 256, 128, 64, 1, ys, base, 1 << 20, None, None) == 1
     # quantiser: blocked extent not a multiple of 32
     assert lib.kosmos_mxfp8_quantize(base, 4, 96, 1, base, base, None) == 1
 
