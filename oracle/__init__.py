@@ -68,6 +68,9 @@ def lib():
         L.orc_moe_dispatch_tables.argtypes = [i64, C.c_int, C.c_int, P, P, P, P]
         L.orc_moe_route.restype = C.c_int
         L.orc_moe_route.argtypes = [i64, i64, C.c_int, C.c_int, P, P, P, P, P, P, P, P]
+        L.orc_moe_experts_mxfp8.restype = C.c_int
+        L.orc_moe_experts_mxfp8.argtypes = [i64, i64, C.c_int, C.c_int, i64, C.c_int, P, P, P, P,
+                                            P, P, P, P, P, P, P, i64, P]
         L.orc_moe_experts.restype = C.c_int
         L.orc_moe_experts.argtypes = [i64, i64, C.c_int, C.c_int, i64, C.c_int, P, P, P,
                                       P, P, P, C.c_int, P, i64, P]
@@ -288,6 +291,36 @@ def moe_experts(x_bits: np.ndarray, idx: np.ndarray, gate: np.ndarray,
                                1 if identity else 0, tp, ntok, _ptr(out))
     if rc:
         raise ValueError("orc_moe_experts failed")
+    return out
+
+
+def moe_experts_mxfp8(xq: np.ndarray, xs: np.ndarray, idx: np.ndarray, gate: np.ndarray,
+                      wg: List[tuple], wu: List[tuple], wd: List[tuple],
+                      tokens: Optional[np.ndarray] = None) -> np.ndarray:
+    """MXFP8 experts.  xq [T, H] E4M3 codes, xs [T, H/32] scale bytes (as
+    mxfp8_quantize(x, along_cols=True) returns them); wg/wu/wd: one
+    (codes, scales) pair per EP rank, codes [E/P, H, I] (down: [E/P, I, H]),
+    scales [E/P, I, H/32] (down: [E/P, H, I/32]) -- each expert quantised
+    along its K dimension."""
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    xs = np.ascontiguousarray(xs, dtype=np.uint8)
+    T, H = xq.shape
+    K = idx.shape[1]
+    P = len(wg)
+    Eq, _, I = wg[0][0].shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    gate = np.ascontiguousarray(gate, dtype=np.float64)
+    arrs = [[np.ascontiguousarray(w[j], dtype=np.uint8) for w in lst] for lst in (wg, wu, wd) for j in (0, 1)]
+    ntok = T if tokens is None else len(tokens)
+    out = np.empty((ntok, H), dtype=np.float64)
+    tp = None
+    if tokens is not None:
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        tp = _ptr(tokens)
+    rc = lib().orc_moe_experts_mxfp8(T, H, Eq * P, K, I, P, _ptr(xq), _ptr(xs), _ptr(idx), _ptr(gate),
+                                     *[_ptr_array(a) for a in arrs], tp, ntok, _ptr(out))
+    if rc:
+        raise ValueError("orc_moe_experts_mxfp8 failed")
     return out
 
 

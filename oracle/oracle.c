@@ -477,6 +477,87 @@ ORC_EXPORT int orc_moe_experts(int64_t T, int64_t H, int E, int K, int64_t I, in
     return bad ? 1 : 0;
 }
 
+/* MXFP8 experts [abstract: the MXFP8 results; reading: an MXFP8 expert layer
+ * quantises what enters each expert GEMM].  The same layer as orc_moe_experts
+ * with every GEMM operand in MXFP8:
+ *   x_t      : e4m3 codes xq[t][h] x 2^(xs[t][h/32] - 127)   (the token rows,
+ *              quantised once along the hidden dimension);
+ *   W_g[e], W_u[e] [H, I]: codes x 2^(scale[i][h/32] - 127);
+ *   W_d[e] [I, H]       : codes x 2^(scale[h][i/32] - 127);
+ *   g, u = x_t W_g, x_t W_u (fp64 sums of exact products); h = silu(g) * u;
+ *   h quantised along I in blocks of 32 by the same rule as the inputs
+ *   (e = smallest integer with blockmax <= 448 * 2^e, codes = E4M3 RNE of
+ *   h / 2^e), then y = dequant(h) W_d and out[t] = sum_k gate * y in k order.
+ * Weight scales per EP rank q: Eq experts' row-major blocks one after the
+ * other ([Eq][I][H/32] for gate and up, [Eq][H][I/32] for down). */
+ORC_EXPORT int orc_moe_experts_mxfp8(int64_t T, int64_t H, int E, int K, int64_t I, int P,
+                                     const uint8_t *xq, const uint8_t *xs, const int32_t *idx,
+                                     const double *gate,
+                                     const uint8_t *const *wgq, const uint8_t *const *wgs,
+                                     const uint8_t *const *wuq, const uint8_t *const *wus,
+                                     const uint8_t *const *wdq, const uint8_t *const *wds,
+                                     const int64_t *tokens, int64_t ntok, double *out) {
+    if (E % P || H % 32 || I % 32) return 1;
+    int Eq = E / P;
+    if (!tokens) ntok = T;
+    double code[256], pw[256];
+    for (int c = 0; c < 256; c++) { code[c] = orc_e4m3_to_f64((uint8_t)c); pw[c] = ldexp(1.0, c - 127); }
+    const int64_t HB = H / 32, IB = I / 32;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *u = (double *)malloc(sizeof(double) * (size_t)I);
+        double *hd = (double *)malloc(sizeof(double) * (size_t)I);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t s = 0; s < ntok; s++) {
+            int64_t t = tokens ? tokens[s] : s;
+            if (t < 0 || t >= T) { bad = 1; continue; }
+            double *o = out + s * H;
+            for (int64_t h = 0; h < H; h++) {
+                xt[h] = code[xq[t * H + h]] * pw[xs[t * HB + h / 32]];
+                o[h] = 0.0;
+            }
+            for (int kk = 0; kk < K; kk++) {
+                int e = idx[t * K + kk];
+                int q = e / Eq, le = e % Eq;
+                const uint8_t *Qg = wgq[q] + (int64_t)le * H * I, *Sg = wgs[q] + (int64_t)le * I * HB;
+                const uint8_t *Qu = wuq[q] + (int64_t)le * H * I, *Su = wus[q] + (int64_t)le * I * HB;
+                const uint8_t *Qd = wdq[q] + (int64_t)le * I * H, *Sd = wds[q] + (int64_t)le * H * IB;
+                for (int64_t i = 0; i < I; i++) { g[i] = 0.0; u[i] = 0.0; }
+                for (int64_t h = 0; h < H; h++) {
+                    double a = xt[h];
+                    for (int64_t i = 0; i < I; i++) {
+                        g[i] += a * (code[Qg[h * I + i]] * pw[Sg[i * HB + h / 32]]);
+                        u[i] += a * (code[Qu[h * I + i]] * pw[Su[i * HB + h / 32]]);
+                    }
+                }
+                for (int64_t b = 0; b < IB; b++) {
+                    double hv[32], mx = 0.0;
+                    for (int j = 0; j < 32; j++) {
+                        hv[j] = orc_silu(g[b * 32 + j]) * u[b * 32 + j];
+                        if (fabs(hv[j]) > mx) mx = fabs(hv[j]);
+                    }
+                    int ex = orc_mx_scale_exp(mx);
+                    for (int j = 0; j < 32; j++)
+                        hd[b * 32 + j] = ldexp(orc_e4m3_to_f64(orc_f64_to_e4m3(ldexp(hv[j], -ex))), ex);
+                }
+                for (int64_t hh = 0; hh < H; hh++) y[hh] = 0.0;
+                for (int64_t i = 0; i < I; i++) {
+                    double hv = hd[i];
+                    for (int64_t hh = 0; hh < H; hh++) y[hh] += hv * (code[Qd[i * H + hh]] * pw[Sd[hh * IB + i / 32]]);
+                }
+                double gk = gate[t * K + kk];
+                for (int64_t hh = 0; hh < H; hh++) o[hh] += gk * y[hh];
+            }
+        }
+        free(xt); free(g); free(u); free(hd); free(y);
+    }
+    return bad ? 1 : 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Work rails ("the order of the rail is the schedule")                      */
 /* ------------------------------------------------------------------------ */

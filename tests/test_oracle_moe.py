@@ -142,3 +142,97 @@ def test_experts_vs_numpy_per_token(orc):
             h = torch.nn.functional.silu(X[t] @ inp["w_gate"][e].double()) * (X[t] @ inp["w_up"][e].double())
             acc += r["gate"][t, kk] * (h @ inp["w_down"][e].double())
         np.testing.assert_allclose(out[s], acc.numpy(), rtol=1e-11, atol=1e-12)
+
+
+# -- MXFP8 experts ---------------------------------------------------------
+
+def _quant_experts(orc, w, P):
+    """Per EP rank: (codes [E/P, K, N], scales [E/P, N, K/32]), each expert
+    quantised along its K (row) dimension."""
+    E = w.shape[0]
+    out = []
+    for q in range(P):
+        qs = [orc.mxfp8_quantize(bf16_bits(w[e]), along_cols=False) for e in range(q * (E // P), (q + 1) * (E // P))]
+        out.append((np.stack([a for a, _ in qs]), np.stack([b for _, b in qs])))
+    return out
+
+
+def _deq_rows(codes, scales):
+    """codes [R, C] with one scale per row and 32 columns (scales [R, C/32])."""
+    v = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+    return v * np.exp2(np.repeat(scales.astype(np.float64) - 127.0, 32, axis=1))
+
+
+def _mx_round_blocks(h):
+    """MXFP8 rounding of a vector in blocks of 32, restated with numpy and
+    torch's E4M3 cast: 2^e with e the smallest integer such that
+    blockmax <= 448 * 2^e, elements rounded to E4M3 at that scale."""
+    out = np.empty_like(h)
+    for b in range(0, len(h), 32):
+        blk = h[b:b + 32]
+        mx = np.abs(blk).max()
+        if mx == 0.0:
+            out[b:b + 32] = 0.0
+            continue
+        e = int(np.ceil(np.log2(mx / 448.0)))
+        while mx > 448.0 * 2.0 ** e:
+            e += 1
+        while mx <= 448.0 * 2.0 ** (e - 1):
+            e -= 1
+        v = torch.from_numpy(blk / 2.0 ** e).to(torch.float8_e4m3fn).double().numpy()
+        out[b:b + 32] = v * 2.0 ** e
+    return out
+
+
+def test_mxfp8_experts_vs_numpy(orc):
+    """Every step restated: E4M3 decode by torch's float8 type, scales as
+    powers of two, h rounded to MXFP8 per 32 intermediate columns."""
+    T, H, E, I, K, P = 10, 64, 4, 96, 2, 2
+    inp = moe_inputs(T=T, H=H, E=E, I=I, seed=21)
+    x = bf16_bits(inp["x"])
+    r = orc.moe_route(x, bf16_bits(inp["w_router"]), K)
+    xq, xs = orc.mxfp8_quantize(x, along_cols=True)
+    wg, wu, wd = (_quant_experts(orc, inp[n], P) for n in ("w_gate", "w_up", "w_down"))
+    tokens = np.array([0, 3, 9], dtype=np.int64)
+    out = orc.moe_experts_mxfp8(xq, xs, r["idx"], r["gate"], wg, wu, wd, tokens=tokens)
+    X = _deq_rows(xq, xs)
+    Eq = E // P
+
+    def wdeq(pack, e):
+        codes, scales = pack[e // Eq][0][e % Eq], pack[e // Eq][1][e % Eq]
+        return _deq_rows(codes.T, scales).T  # scales run along the K rows of [K, N]
+
+    for s, t in enumerate(tokens):
+        acc = np.zeros(H)
+        for kk in range(K):
+            e = int(r["idx"][t, kk])
+            g = X[t] @ wdeq(wg, e)
+            u = X[t] @ wdeq(wu, e)
+            h = _mx_round_blocks(g / (1.0 + np.exp(-g)) * u)
+            acc += r["gate"][t, kk] * (h @ wdeq(wd, e))
+        np.testing.assert_allclose(out[s], acc, rtol=1e-10, atol=1e-12)
+
+
+def test_mxfp8_experts_close_to_bf16_layer_on_dequantised_inputs(orc):
+    """The dequantised E4M3 x 2^e operands are exact bf16 values, so the bf16
+    layer on them differs from the MXFP8 layer only by the rounding of h
+    (at most 1/16 of each element)."""
+    T, H, E, I, K, P = 16, 64, 8, 64, 3, 2
+    inp = moe_inputs(T=T, H=H, E=E, I=I, seed=22)
+    x = bf16_bits(inp["x"])
+    r = orc.moe_route(x, bf16_bits(inp["w_router"]), K)
+    xq, xs = orc.mxfp8_quantize(x, along_cols=True)
+    packs = [_quant_experts(orc, inp[n], P) for n in ("w_gate", "w_up", "w_down")]
+    mx = orc.moe_experts_mxfp8(xq, xs, r["idx"], r["gate"], *packs)
+
+    def to_bf16_bits(a):
+        t = torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16)
+        assert np.array_equal(t.double().numpy(), a), "dequantised value not exact in bf16"
+        return t.view(torch.int16).numpy().view(np.uint16)
+
+    xb = to_bf16_bits(_deq_rows(xq, xs))
+    wb = [[to_bf16_bits(np.stack([_deq_rows(c.T, s).T for c, s in zip(codes, scales)])) for codes, scales in pack]
+          for pack in packs]
+    ref = orc.moe_experts(xb, r["idx"], r["gate"], wb[0], wb[1], wb[2], E=E)
+    err = np.abs(mx - ref).max() / np.abs(ref).max()
+    assert 1e-4 < err < 0.06, err  # h rounding is visible, and bounded
