@@ -273,34 +273,76 @@ def moe_algorithmic_bytes(T, H, E, K, I):
     return weights + dispatch + gemm_in + h_out + y_out + push + fold + router_in
 
 
-def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0):
+# MXFP8 layer: weights, tokens and h in E4M3 with one E8M0 byte per 32
+# (router, expert outputs, slots and the fold stay bf16); adds the in-launch
+# quantisation of the tokens (read bf16, write E4M3 + scales).
+def moe_algorithmic_bytes_mxfp8(T, H, E, K, I):
+    rows = T * K
+    f8 = lambda n: n + n // 32  # E4M3 bytes plus their scales
+    weights = f8(E * 3 * H * I) + H * E * 2
+    quant = T * H * 2 + f8(T * H)
+    dispatch = 2 * f8(rows * H)
+    gemm_in = f8(rows * H) + f8(rows * I)
+    h_out = f8(rows * I)
+    y_out = rows * H * 2
+    push = 2 * rows * H * 2
+    fold = rows * H * 2 + T * H * 2
+    router_in = T * H * 2
+    return weights + quant + dispatch + gemm_in + h_out + y_out + push + fold + router_in
+
+
+def _quant_experts_gpu(K, w, P, dev, stream):
+    """E4M3 codes per rank and the experts' tiled scales one after the other."""
+    import torch
+    E, Kd, N = w.shape
+    codes, scales = [], []
+    nb = K.mxfp8_scale_bytes(Kd, N, False)
+    for q in range(P):
+        c = torch.empty(E // P, Kd, N, dtype=torch.uint8, device=dev)
+        s = torch.empty((E // P) * nb, dtype=torch.uint8, device=dev)
+        for j in range(E // P):
+            K.mxfp8_quantize(w[q * (E // P) + j].to(dev), c[j], s[j * nb:(j + 1) * nb], False, stream=stream)
+        codes.append(c)
+        scales.append(s)
+    return codes, scales
+
+
+def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0, mx=False):
     import dataclasses
     import torch
     from kosmos_inputs import WORKLOADS, workload_inputs
     w = WORKLOADS["moe_fwd_p8"]
     if experts:  # a smaller expert count for profiler captures (same kernel, fewer weights)
         w = dataclasses.replace(w, E=experts, name=f"moe_fwd_p8_e{experts}")
+    if mx:
+        w = dataclasses.replace(w, name=w.name.replace("moe_fwd", "moe_fwd_mxfp8"), dtype="mxfp8")
     inp = workload_inputs(w)
     P, T, H, E, Kt, I = w.P, w.T, w.H, w.E, w.topk, w.I
     xs = [t.to(dev) for t in torch.chunk(inp["x"], P, 0)]
     wr = inp["w_router"].to(dev)
-    wg = [t.to(dev) for t in _split_experts(inp["w_gate"], P)]
-    wu = [t.to(dev) for t in _split_experts(inp["w_up"], P)]
-    wd = [t.to(dev) for t in _split_experts(inp["w_down"], P)]
+    kw = {}
+    if mx:
+        (wg, sg), (wu, su), (wd, sd) = (_quant_experts_gpu(K, inp[n], P, dev, stream)
+                                        for n in ("w_gate", "w_up", "w_down"))
+        kw = {"dtype": K.MXFP8_E4M3, "w_gate_scales": sg, "w_up_scales": su, "w_down_scales": sd}
+    else:
+        wg = [t.to(dev) for t in _split_experts(inp["w_gate"], P)]
+        wu = [t.to(dev) for t in _split_experts(inp["w_up"], P)]
+        wd = [t.to(dev) for t in _split_experts(inp["w_down"], P)]
     del inp
     ys = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
     idx = torch.empty(T, Kt, dtype=torch.int32, device=dev)
     gate = torch.empty(T, Kt, dtype=torch.float32, device=dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     pos = torch.empty(T, Kt, dtype=torch.int32, device=dev)
-    wsb = K.moe_workspace(P, T, H, E, Kt, I, device=dev)
+    wsb = K.moe_workspace(P, T, H, E, Kt, I, device=dev, dtype=K.MXFP8_E4M3 if mx else K.BF16)
     o = K.opts(**QUICK_OPTS)
-    f = lambda: K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, wsb, Kt, o, stream=stream)
+    f = lambda: K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, wsb, Kt, o, stream=stream, **kw)
     f()
     K.check(wsb, "moe_fwd")
     t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
     K.check(wsb, "moe_fwd")
-    byt = moe_algorithmic_bytes(T, H, E, Kt, I)
+    byt = (moe_algorithmic_bytes_mxfp8 if mx else moe_algorithmic_bytes)(T, H, E, Kt, I)
     gbs = byt / (t * 1e-3) / 1e9
     return {"workload": w.name, "ms": t, "tokens_per_s": T / (t * 1e-3),
             "tflops": w.flops() / (t * 1e-3) / 1e12, "frac_of_tensor_peak": w.flops() / (t * 1e-3) / 1e12 / tensor_peak,
@@ -447,6 +489,9 @@ def run_quick_other(args):
     elif args.workload == "moe":
         r = bench_moe(K, dev, args.steps, args.warmup, flush, stream, peaks["hbm_gbs"], peaks["bf16_tflops"],
                       experts=args.experts)
+    elif args.workload == "moe_mxfp8":
+        r = bench_moe(K, dev, args.steps, args.warmup, flush, stream, peaks["hbm_gbs"], 2 * peaks["bf16_tflops"],
+                      experts=args.experts, mx=True)
     elif args.workload == "rs_mxfp8":
         r = bench_rs_mxfp8(K, dev, args.steps, args.warmup, flush, stream, peaks["bf16_tflops"], baselines=False)
     else:
@@ -579,6 +624,9 @@ def run_kosmos(args):
         torch.cuda.empty_cache()
         also["rs_mxfp8"] = bench_rs_mxfp8(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
+        also["moe_fwd_mxfp8"] = bench_moe(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"],
+                                          2 * peak, mx=True)
+        torch.cuda.empty_cache()
 
     line = None
     if rank == 0:
@@ -607,7 +655,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kosmos", choices=["kosmos", "reference"])
     ap.add_argument("--ag-only", action="store_true", help="skip the GEMM+RS and MoE measurements")
-    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8", "rs_mxfp8"],
+    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8", "rs_mxfp8", "moe_mxfp8"],
                     help="with --quick: which fused operator to time")
     ap.add_argument("--experts", type=int, default=0, help="with --quick --workload moe: expert count (0 = 128)")
     ap.add_argument("--num-ctas", type=int, default=0,

@@ -26,8 +26,9 @@ INJECT_DROP_TRANSFER = 0x1
 INJECT_DROP_PARTIAL = 0x2
 INJECT_IDENTITY_EXPERTS = 0x4
 MOE_VIEW_LOGITS, MOE_VIEW_RECV, MOE_VIEW_H, MOE_VIEW_Y, MOE_VIEW_SLOT, MOE_VIEW_OFFSETS, MOE_VIEW_TRACE = range(7)
+MOE_VIEW_RECV_SCALES, MOE_VIEW_XQ, MOE_VIEW_XS = 7, 8, 9  # MXFP8 only
 KIND_NAMES = {1: "TRANSFER", 2: "TILE", 3: "REDUCE", 4: "ROUTE", 5: "DISPATCH", 6: "TILE_GU", 7: "TILE_D",
-              8: "PUSH", 9: "FOLD", 10: "TILE_HALF"}
+              8: "PUSH", 9: "FOLD", 10: "TILE_HALF", 11: "QUANT"}
 
 EXPORTS = ["kosmos_default_opts", "kosmos_num_sms", "kosmos_workspace_bytes", "kosmos_workspace_init",
            "kosmos_ag_gemm", "kosmos_gemm_rs", "kosmos_moe_fwd", "kosmos_mxfp8_quantize", "kosmos_status_sync",
@@ -84,8 +85,8 @@ def lib():
     L.kosmos_ag_gemm.restype = i32
     L.kosmos_gemm_rs.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, vp, vp, C.c_size_t, C.POINTER(Opts), vp]
     L.kosmos_gemm_rs.restype = i32
-    L.kosmos_moe_fwd.argtypes = [vp, vp, i32, i64, i64, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                 C.c_size_t, C.POINTER(Opts), vp]
+    L.kosmos_moe_fwd.argtypes = [vp, vp, i32, i64, i64, i32, i32, i64, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp,
+                                 vp, vp, C.c_size_t, C.POINTER(Opts), vp]
     L.kosmos_moe_fwd.restype = i32
     L.kosmos_mxfp8_quantize.argtypes = [vp, i64, i64, i32, vp, vp, vp]
     L.kosmos_mxfp8_quantize.restype = i32
@@ -100,9 +101,9 @@ def lib():
     L.kosmos_rail_decode_device.restype = i64
     L.kosmos_ag_gemm_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, i32, vp, vp, C.POINTER(Opts), vp]
     L.kosmos_ag_gemm_noalloc.restype = i32
-    L.kosmos_moe_workspace_bytes.argtypes = [i32, i64, i64, i32, i32, i64, C.POINTER(Opts)]
+    L.kosmos_moe_workspace_bytes.argtypes = [i32, i64, i64, i32, i32, i64, i32, C.POINTER(Opts)]
     L.kosmos_moe_workspace_bytes.restype = C.c_size_t
-    L.kosmos_moe_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, vp, C.POINTER(vp), C.POINTER(i64)]
+    L.kosmos_moe_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, i32, vp, C.POINTER(vp), C.POINTER(i64)]
     L.kosmos_moe_debug_view.restype = i32
     L.kosmos_ag_tile_plan.argtypes = [i32, i64, i64, i64, i32, C.POINTER(Opts), C.POINTER(i64), C.POINTER(C.c_int32)]
     L.kosmos_ag_tile_plan.restype = i32
@@ -218,37 +219,49 @@ def gemm_rs(x_shards: List, w_shards: List, y_chunks: List, ws, o: Optional[Opts
 
 
 def moe_fwd(x_shards: List, w_router, w_gate: List, w_up: List, w_down: List, y_shards: List, topk_idx,
-            topk_gate, expert_counts, dispatch_pos, ws, topk: int, o: Optional[Opts] = None, stream=None):
+            topk_gate, expert_counts, dispatch_pos, ws, topk: int, o: Optional[Opts] = None, stream=None,
+            dtype: int = BF16, w_gate_scales: Optional[List] = None, w_up_scales: Optional[List] = None,
+            w_down_scales: Optional[List] = None):
+    """One MoE layer forward.  MXFP8: w_gate / w_up / w_down hold E4M3 bytes
+    ([E/P, hidden, inter], [E/P, inter, hidden] per rank) and *_scales their
+    MMA-tiled E8M0 scales, expert after expert (each expert quantised along
+    its K dimension as mxfp8_quantize(w[e], along_cols=False) does)."""
     _check_cuda(*x_shards, w_router, *w_gate, *w_up, *w_down, *y_shards, topk_idx, topk_gate, expert_counts,
-                dispatch_pos, ws)
+                dispatch_pos, ws, *(w_gate_scales or []), *(w_up_scales or []), *(w_down_scales or []))
     P = len(x_shards)
     tokens = x_shards[0].shape[0] * P
     hidden = x_shards[0].shape[1]
     E = w_router.shape[1]
     inter = w_gate[0].shape[2]
+    mx = dtype == MXFP8_E4M3
+    if mx and (w_gate_scales is None or w_up_scales is None or w_down_scales is None):
+        raise KosmosError(ERR_INVALID_ARG, "moe_fwd: MXFP8 needs the weight scales")
     rc = lib().kosmos_moe_fwd(_ptrs(x_shards), w_router.data_ptr(), P, tokens, hidden, E, topk, inter,
-                              _ptrs(w_gate), _ptrs(w_up), _ptrs(w_down), _ptrs(y_shards), topk_idx.data_ptr(),
+                              _ptrs(w_gate), _ptrs(w_gate_scales) if mx else None, _ptrs(w_up),
+                              _ptrs(w_up_scales) if mx else None, _ptrs(w_down),
+                              _ptrs(w_down_scales) if mx else None, dtype, _ptrs(y_shards), topk_idx.data_ptr(),
                               topk_gate.data_ptr(), expert_counts.data_ptr(), dispatch_pos.data_ptr(),
                               ws.data_ptr(), ws.numel(), C.byref(o) if o is not None else None, _stream(stream))
     _raise(rc, "kosmos_moe_fwd")
 
 
 def moe_workspace(P: int, tokens: int, hidden: int, n_experts: int, topk: int, inter: int,
-                  o: Optional[Opts] = None, device=None):
+                  o: Optional[Opts] = None, device=None, dtype: int = BF16):
     """A zeroed workspace tensor (uint8) for kosmos_moe_fwd."""
     import torch
-    nbytes = int(lib().kosmos_moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter,
+    nbytes = int(lib().kosmos_moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, dtype,
                                                   C.byref(o) if o is not None else None))
     if nbytes == 0:
         raise KosmosError(ERR_INVALID_ARG, "kosmos_moe_workspace_bytes")
     return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
 
 
-def moe_debug_view(what: int, P: int, tokens: int, hidden: int, n_experts: int, topk: int, inter: int, ws):
+def moe_debug_view(what: int, P: int, tokens: int, hidden: int, n_experts: int, topk: int, inter: int, ws,
+                   dtype: int = BF16):
     """A uint8 view (torch tensor slice of ws) of one internal MoE buffer."""
     ptr = C.c_void_p()
     nb = C.c_int64()
-    rc = lib().kosmos_moe_debug_view(what, P, tokens, hidden, n_experts, topk, inter, ws.data_ptr(),
+    rc = lib().kosmos_moe_debug_view(what, P, tokens, hidden, n_experts, topk, inter, dtype, ws.data_ptr(),
                                      C.byref(ptr), C.byref(nb))
     _raise(rc, "kosmos_moe_debug_view")
     off = ptr.value - ws.data_ptr()

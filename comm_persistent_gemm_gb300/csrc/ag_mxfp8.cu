@@ -57,23 +57,6 @@ struct AgF8Params {
     uint64_t inject;
 };
 
-__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-// 32 rows x 16 bytes from shared memory into TMEM lanes 0-31 of four columns,
-// replicated to the four 32-lane groups.
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 struct F8Smem {
     Smem base;
     uint8_t *sf;  // [NSTAGE][F_SF_BYTES]
@@ -230,16 +213,7 @@ __device__ __forceinline__ void f8_mma_loop(const F8Smem &fs, uint32_t tmem_base
             const uint32_t b_addr = a_addr + F_A_BYTES;
             const uint32_t sf_addr = smem_u32(fs.sf + ps.stage * F_SF_BYTES);
             const uint32_t sfa_t = tmem_base + F_TMEM_SF + ps.stage * F_TMEM_SF_STRIDE;
-            const uint32_t sfb_t = sfa_t + 4;
-            tmem_cp_32x128b_x4(sfa_t, sdesc_sf(sf_addr));
-            tmem_cp_32x128b_x4(sfb_t, sdesc_sf(sf_addr + 512));
-            tmem_cp_32x128b_x4(sfb_t + 4, sdesc_sf(sf_addr + 1024));
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint64_t ad = sdesc_sw128(a_addr + j * 32, 16, 1024);
-                const uint64_t bd = sdesc_sw128(b_addr + j * (32 * 128), F_B_SLAB, 1024);
-                mma_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(BM, BN, j), sfa_t, sfb_t, (kb | j) != 0 ? 1u : 0u);
-            }
+            mx_stage_mma(tmem_base, a_addr, b_addr, F_B_SLAB, sf_addr, sfa_t, kb == 0);
             mma_commit(&sm.empty[ps.stage]);
             ps.advance();
         }

@@ -3,35 +3,12 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
-#include "common.cuh"
+#include "mxfp8.cuh"
 #include "launch.h"
 
 namespace kosmos {
 
-// Shared exponent of one block: the smallest integer e with
-// blockmax <= 448 * 2^e, clamped to [-127, 127]; 0 for an all-zero block.
-// blockmax is a bf16 value, hence an exact float: write it as f * 2^E with
-// f in [1, 2); 448 = 1.75 * 2^8, so e = E - 8 when f <= 1.75 and E - 7 otherwise.
-__device__ __forceinline__ int mx_block_exp(float blockmax) {
-    const uint32_t b = __float_as_uint(blockmax);
-    const int ex = static_cast<int>((b >> 23) & 0xFF);
-    const uint32_t man = b & 0x7FFFFFu;
-    if (ex == 0) return man == 0 ? 0 : -127;  // zero, or below 2^-126: clamped
-    const int E = ex - 127;
-    int e = (man <= 0x600000u) ? E - 8 : E - 7;
-    if (e < -127) e = -127;
-    if (e > 127) e = 127;
-    return e;
-}
-
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
-
-// Byte offset of the scale of (scale row r, K-block b) in the MMA-tiled layout:
-// 512-byte atoms of 128 scale rows x 4 K-blocks, atoms ordered by row block,
-// then K; inside an atom row r sits at (r % 32) * 16 + ((r / 32) % 4) * 4.
-__device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t b, int64_t kblocks) {
-    return ((r / 128) * (kblocks / 4) + b / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + (b % 4);
-}
 
 // One thread per 32-element block; scale rows beyond the operand (padding of
 // the last 128-row atom) get the neutral scale 2^0.

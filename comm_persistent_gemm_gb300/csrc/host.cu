@@ -426,40 +426,52 @@ static bool moe_sizes_ok(int P, int64_t tokens, int64_t hidden, int n_experts, i
 }
 
 size_t kosmos_moe_workspace_bytes(int P, int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter,
-                                  const kosmos_opts *opts) {
+                                  int dtype, const kosmos_opts *opts) {
     const kosmos_opts o = resolve_opts(opts);
     if (!moe_sizes_ok(P, tokens, hidden, n_experts, topk, inter)) return 0;
-    return moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, o.trace != 0);
+    if (dtype != KOSMOS_BF16 && dtype != KOSMOS_MXFP8_E4M3) return 0;
+    return moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, dtype == KOSMOS_MXFP8_E4M3, o.trace != 0);
 }
 
 kosmos_status kosmos_moe_debug_view(int what, int P, int64_t tokens, int64_t hidden, int n_experts, int topk,
-                                    int64_t inter, void *ws, void **ptr, int64_t *bytes) {
+                                    int64_t inter, int dtype, void *ws, void **ptr, int64_t *bytes) {
     if (!moe_sizes_ok(P, tokens, hidden, n_experts, topk, inter) || ws == nullptr || ptr == nullptr ||
-        bytes == nullptr)
+        bytes == nullptr || (dtype != KOSMOS_BF16 && dtype != KOSMOS_MXFP8_E4M3))
         return KOSMOS_ERR_INVALID_ARG;
-    return moe_debug_view(what, P, tokens, hidden, n_experts, topk, inter, ws, ptr, bytes) ? KOSMOS_OK
-                                                                                          : KOSMOS_ERR_INVALID_ARG;
+    return moe_debug_view(what, P, tokens, hidden, n_experts, topk, inter, dtype == KOSMOS_MXFP8_E4M3, ws, ptr, bytes)
+               ? KOSMOS_OK
+               : KOSMOS_ERR_INVALID_ARG;
 }
 
 kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, int P, int64_t tokens, int64_t hidden,
                              int n_experts, int topk, int64_t inter, const void *const *w_gate,
-                             const void *const *w_up, const void *const *w_down, void *const *y_shards,
-                             int32_t *topk_idx, float *topk_gate, int32_t *expert_counts, int32_t *dispatch_pos,
-                             void *ws, size_t ws_bytes, const kosmos_opts *opts, void *stream) {
+                             const void *const *w_gate_scales, const void *const *w_up,
+                             const void *const *w_up_scales, const void *const *w_down,
+                             const void *const *w_down_scales, int dtype, void *const *y_shards, int32_t *topk_idx,
+                             float *topk_gate, int32_t *expert_counts, int32_t *dispatch_pos, void *ws,
+                             size_t ws_bytes, const kosmos_opts *opts, void *stream) {
     if (!moe_sizes_ok(P, tokens, hidden, n_experts, topk, inter)) return KOSMOS_ERR_INVALID_ARG;
     if (x_shards == nullptr || w_gate == nullptr || w_up == nullptr || w_down == nullptr || y_shards == nullptr)
         return KOSMOS_ERR_INVALID_ARG;
-    for (int q = 0; q < P; ++q)
+    if (dtype != KOSMOS_BF16 && dtype != KOSMOS_MXFP8_E4M3) return KOSMOS_ERR_INVALID_ARG;
+    const bool mx = dtype == KOSMOS_MXFP8_E4M3;
+    if (mx && (w_gate_scales == nullptr || w_up_scales == nullptr || w_down_scales == nullptr))
+        return KOSMOS_ERR_INVALID_ARG;
+    for (int q = 0; q < P; ++q) {
         if (!aligned16(x_shards[q]) || !aligned16(w_gate[q]) || !aligned16(w_up[q]) || !aligned16(w_down[q]) ||
             !aligned16(y_shards[q]))
             return KOSMOS_ERR_INVALID_ARG;
+        if (mx && (!aligned16(w_gate_scales[q]) || !aligned16(w_up_scales[q]) || !aligned16(w_down_scales[q])))
+            return KOSMOS_ERR_INVALID_ARG;
+    }
     if (!aligned16(w_router) || !aligned16(topk_idx) || !aligned16(topk_gate) || !aligned16(expert_counts) ||
         !aligned16(dispatch_pos))
         return KOSMOS_ERR_INVALID_ARG;
     if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
     const kosmos_opts o = resolve_opts(opts);
     if (o.sched != KOSMOS_SCHED_SELF) return KOSMOS_ERR_UNSUPPORTED;
-    if (ws_bytes < kosmos_moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, &o))
+    if (mx && (o.inject & KOSMOS_INJECT_IDENTITY_EXPERTS)) return KOSMOS_ERR_UNSUPPORTED;
+    if (ws_bytes < kosmos_moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, dtype, &o))
         return KOSMOS_ERR_WORKSPACE;
     const int grid = grid_for(o);
     if (grid < 1) return KOSMOS_ERR_CUDA;
@@ -472,8 +484,12 @@ kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, 
         L.wg[q] = w_gate[q];
         L.wu[q] = w_up[q];
         L.wd[q] = w_down[q];
+        L.wgs[q] = mx ? w_gate_scales[q] : nullptr;
+        L.wus[q] = mx ? w_up_scales[q] : nullptr;
+        L.wds[q] = mx ? w_down_scales[q] : nullptr;
         L.y[q] = y_shards[q];
     }
+    L.dtype = dtype;
     L.wr = w_router;
     L.topk_idx = topk_idx; L.topk_gate = topk_gate; L.counts = expert_counts; L.pos = dispatch_pos;
     L.ws = ws; L.sched = o.sched; L.n_comm = 0; L.trace = o.trace; L.grid = grid; L.plain_launch = o.plain_launch;

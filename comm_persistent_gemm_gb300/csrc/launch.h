@@ -63,6 +63,10 @@ struct MoeLaunch {
     const void *wg[KOSMOS_MAX_P];
     const void *wu[KOSMOS_MAX_P];
     const void *wd[KOSMOS_MAX_P];
+    const void *wgs[KOSMOS_MAX_P];  // MXFP8: tiled scales of the gate / up / down weights
+    const void *wus[KOSMOS_MAX_P];
+    const void *wds[KOSMOS_MAX_P];
+    int dtype;
     void *y[KOSMOS_MAX_P];
     int32_t *topk_idx;
     float *topk_gate;
@@ -100,8 +104,8 @@ kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream);
 size_t ag_mxfp8_scale_bytes(int P, int64_t m, int64_t k);
 kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream);
 kosmos_status launch_moe_fwd(const MoeLaunch &L, cudaStream_t stream);
-size_t moe_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool trace);
-bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t I, void *ws, void **ptr,
+size_t moe_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool mx, bool trace);
+bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t I, bool mx, void *ws, void **ptr,
                     int64_t *bytes);
 kosmos_status launch_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q,
                                     void *scales, cudaStream_t stream);

@@ -31,21 +31,35 @@
 //                   fp32, k in emission order, one rounding to bf16.
 // A CTA takes a ready PUSH first, else its next main-rail entry, else a ready
 // FOLD, and exits when its rank's rail and queues are drained.
+//
+// MXFP8 variant (E4M3 elements, one E8M0 scale per 32 K-elements, on every
+// operand of the expert GEMMs): between ROUTE and DISPATCH the rail holds
+//   QUANT(j)        16 token rows of the rank quantised along the hidden
+//                   dimension (bf16 rows staged through the pipeline; scales
+//                   row-major); DISPATCH then moves E4M3 rows and their scales;
+// each expert's receive rows start on a 128-row boundary (the scale atoms of
+// the block-scaled MMA cover 128 aligned rows); the GU epilogue quantises h
+// along the intermediate dimension for TILE_D.  The router stays bf16.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
 
-#include "engine.cuh"
+#include "mxfp8.cuh"
 #include "launch.h"
 
 namespace kosmos {
 
 constexpr int MOE_MAXK = 8;
 constexpr int MOE_SCRATCH = 12288;          // epilogue 8 KB + producer 4 KB
-constexpr int MOE_SMEM_BYTES = SMEM_BYTES + MOE_SCRATCH;
+constexpr int MOE_SF_BYTES = 3 * 512;       // MXFP8: per stage, SFA atom + two SFB atoms
+constexpr int MOE_SMEM_BYTES = SMEM_BYTES + MOE_SCRATCH + NSTAGE * MOE_SF_BYTES;
+static_assert(MOE_SMEM_BYTES <= 232448, "MoE kernel exceeds 227 KB of shared memory per CTA");
+constexpr int MOE_QR = 16;                  // MXFP8: token rows per QUANT entry
+constexpr int K_QUANT = 11;                 // rail kind of a QUANT entry
 
 struct MoeGeom {
+    bool mx;         // MXFP8 expert GEMMs
     int P, E, Eq, K;
     int64_t T, Tq, H, I;
     int RB;          // route blocks per rank
@@ -56,13 +70,16 @@ struct MoeGeom {
     int64_t rows_cap;
     int push_cap;    // per rank
     int fold_cap;    // per rank
-    int n_head;      // RB + RB*K main-rail entries before the tiles
-    int nkb_h;       // H / 64
-    int nkb_i;       // I / 64
+    int NQ;          // QUANT entries per rank (MXFP8; else 0)
+    int n_head;      // RB + NQ + RB*K main-rail entries before the tiles
+    int nkb_r;       // router K blocks: H / 64
+    int nkb_h;       // GU K stages: H / 64 (bf16) or H / 128 (MXFP8)
+    int nkb_i;       // D K stages: I / 64 or I / 128
 };
 
-inline MoeGeom moe_geom(int P, int64_t T, int64_t H, int E, int K, int64_t I) {
+inline MoeGeom moe_geom(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool mx) {
     MoeGeom g;
+    g.mx = mx;
     g.P = P; g.E = E; g.Eq = E / P; g.K = K;
     g.T = T; g.Tq = T / P; g.H = H; g.I = I;
     g.RB = static_cast<int>(cdiv(g.Tq, BM));
@@ -70,20 +87,25 @@ inline MoeGeom moe_geom(int P, int64_t T, int64_t H, int E, int K, int64_t I) {
     g.NGU = static_cast<int>(I / 128);
     g.ND = static_cast<int>(H / BN);
     g.MAXRB = static_cast<int>(cdiv(T, BM));
-    g.rows_cap = T * K + BM;
+    // MXFP8: every expert's rows start on a 128-row boundary (at most E * 127
+    // padding rows), and the buffer is whole 128-row scale atoms
+    g.rows_cap = mx ? align_up(T * K + static_cast<int64_t>(E + 1) * BM, BM) : T * K + BM;
     g.push_cap = static_cast<int>((g.Eq + cdiv(T * K, BM)) * g.ND);
     g.fold_cap = g.RB * g.ND;
-    g.n_head = g.RB + g.RB * K;
-    g.nkb_h = static_cast<int>(H / BK);
-    g.nkb_i = static_cast<int>(I / BK);
+    g.NQ = mx ? static_cast<int>(cdiv(g.Tq, MOE_QR)) : 0;
+    g.n_head = g.RB + g.NQ + g.RB * K;
+    const int kst = mx ? FBK : BK;
+    g.nkb_r = static_cast<int>(H / BK);
+    g.nkb_h = static_cast<int>(H / kst);
+    g.nkb_i = static_cast<int>(I / kst);
     return g;
 }
 
 struct MoeWsLayout {
-    size_t ctr, ctr_bytes, disp_cnt, gu_cnt, fold_cnt, qctl, route_done;
-    size_t blk_counts, rank_in_blk, base, offsets, counts, unit_start, inv_pos;
+    size_t ctr, ctr_bytes, disp_cnt, gu_cnt, fold_cnt, quant_cnt, qctl, route_done;
+    size_t blk_counts, rank_in_blk, base, offsets, offl, counts, unit_start, inv_pos;
     size_t push_items, push_flags, fold_items, fold_flags;
-    size_t logits, recv, h, ybuf, slot, trace, total;
+    size_t logits, xq, xs, recv, recv_sf, h, h_sf, ybuf, slot, trace, total;
 };
 
 inline MoeWsLayout moe_ws_layout(const MoeGeom &g, bool trace) {
@@ -100,6 +122,7 @@ inline MoeWsLayout moe_ws_layout(const MoeGeom &g, bool trace) {
     L.disp_cnt = c; c += 4ull * g.E * g.MAXRB;
     L.gu_cnt = c; c += 4ull * g.E * g.MAXRB;
     L.fold_cnt = c; c += 4ull * g.NB * g.ND;
+    L.quant_cnt = c; c += 4ull * g.NB;
     L.qctl = c; c += 4ull * 4 * g.P;
     L.route_done = c; c += 4;
     L.ctr_bytes = static_cast<size_t>(align_up(static_cast<int64_t>(c - L.ctr), 16));
@@ -109,16 +132,22 @@ inline MoeWsLayout moe_ws_layout(const MoeGeom &g, bool trace) {
     L.rank_in_blk = take(4ull * g.T * g.K);
     L.base = take(4ull * g.NB * g.E);
     L.offsets = take(4ull * (g.E + 1));
+    L.offl = take(4ull * (g.E + 1));
     L.counts = take(4ull * g.E);
     L.unit_start = take(4ull * g.P * (g.Eq + 1));
-    L.inv_pos = take(4ull * g.T * g.K);
+    L.inv_pos = take(4ull * g.rows_cap);
     L.push_items = take(4ull * g.P * g.push_cap);
     L.push_flags = take(4ull * g.P * g.push_cap);
     L.fold_items = take(4ull * g.P * g.fold_cap);
     L.fold_flags = take(4ull * g.P * g.fold_cap);
     L.logits = take(4ull * g.T * g.E);
-    L.recv = take(2ull * g.rows_cap * g.H);
-    L.h = take(2ull * g.rows_cap * g.I);
+    const size_t esz = g.mx ? 1 : 2;
+    L.xq = g.mx ? take(static_cast<size_t>(g.T * g.H)) : 0;
+    L.xs = g.mx ? take(static_cast<size_t>(g.T * g.H / 32)) : 0;
+    L.recv = take(esz * g.rows_cap * g.H);
+    L.recv_sf = g.mx ? take(static_cast<size_t>(g.rows_cap * g.H / 32)) : 0;
+    L.h = take(esz * g.rows_cap * g.I);
+    L.h_sf = g.mx ? take(static_cast<size_t>(g.rows_cap * g.I / 32)) : 0;
     L.ybuf = take(2ull * g.rows_cap * g.H);
     L.slot = take(2ull * g.T * g.K * g.H);
     L.trace = off;
@@ -136,6 +165,14 @@ struct MoeParams {
     CUtensorMap tmWu[KOSMOS_MAX_P];  // w_up[q]:   dims {I, H, Eq}, box {64, 64, 1}
     CUtensorMap tmWd[KOSMOS_MAX_P];  // w_down[q]: dims {H, I, Eq}, box {64, 64, 1}
     CUtensorMap tmSlot;              // slot buffer: dims {H, T*K}, box {256, fold_tps*K}, no swizzle
+    // MXFP8 (the maps above then hold E4M3 bytes: tmRecv, tmH box {128, 128};
+    // tmWg, tmWu, tmWd box {128, 128, 1}): tiled scales as rows of 16 bytes,
+    // one 512-byte atom per box {16, 32}
+    CUtensorMap tmSRecv;             // receive-row scales, K = H
+    CUtensorMap tmSH;                // h scales, K = I
+    CUtensorMap tmSWg[KOSMOS_MAX_P]; // per expert: I/128 column atoms x H/128 K atoms
+    CUtensorMap tmSWu[KOSMOS_MAX_P];
+    CUtensorMap tmSWd[KOSMOS_MAX_P]; // per expert: H/128 column atoms x I/128 K atoms
     const __nv_bfloat16 *x[KOSMOS_MAX_P];
     __nv_bfloat16 *y[KOSMOS_MAX_P];
     int32_t *topk_idx;
@@ -148,6 +185,10 @@ struct MoeParams {
     int identity;
     uint32_t *disp_cnt, *gu_cnt, *fold_cnt, *qctl, *route_done;
     int32_t *blk_counts, *rank_in_blk, *base, *offsets, *counts, *unit_start, *inv_pos;
+    int32_t *offl;                   // receive offsets without padding (dispatch_pos is reported in these)
+    uint32_t *quant_cnt;             // MXFP8: quantised rows per route block
+    uint8_t *xq, *xs;                // MXFP8: quantised tokens [T, H], scales [T, H/32] row-major
+    uint8_t *recv8, *recv_sf, *h8, *h_sf;
     int32_t *push_items, *fold_items;
     uint32_t *push_flags, *fold_flags;
     float *logits;
@@ -222,6 +263,7 @@ struct MoeProdState {
     // this rank's plan, copied to shared memory once it is published:
     // us[Eq + 1] row-block prefix, off[Eq] receive offsets, cnt[Eq] row counts
     int32_t *us = nullptr, *off = nullptr, *cnt = nullptr;
+    uint8_t *sf = nullptr;  // MXFP8: per-stage scale atoms
     int64_t pending = -1;  // a claimed main-rail ticket waiting for the plan table
     int64_t ahead = -1;    // the next main-rail ticket, claimed early so its latency overlaps the current entry
 };
@@ -348,11 +390,11 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
         if (t < static_cast<uint32_t>(g.RB)) {  // ROUTE(b)
             const int b = static_cast<int>(t);
             SchedEntry en;
-            fill_entry(en, K_ROUTE, q, b, q * g.RB + b, g.nkb_h, t, trace_open(p, st, K_ROUTE, t, tc));
+            fill_entry(en, K_ROUTE, q, b, q * g.RB + b, g.nkb_r, t, trace_open(p, st, K_ROUTE, t, tc));
             en.nmma = g.E;
             if (!ring_push(sm, st.rs, en, p.ws)) return ACT_EXIT;
             const uint32_t bytes = A_STAGE_BYTES + (g.E / 64) * (64 * BK * 2);
-            for (int kb = 0; kb < g.nkb_h; ++kb) {
+            for (int kb = 0; kb < g.nkb_r; ++kb) {
                 if (!mbar_wait(&sm.empty[st.ps.stage], st.ps.phase ^ 1u, PIPE_LIMIT_NS)) {
                     set_error(p.ws, KOSMOS_ERR_DEVICE, t);
                     return ACT_EXIT;
@@ -368,13 +410,39 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
             st.idle_t0 = 0;
             return ACT_NONE;
         }
+        if (t < static_cast<uint32_t>(g.RB + g.NQ)) {  // QUANT(j): bf16 token rows through the stages
+            const int j = static_cast<int>(t) - g.RB;
+            const int64_t r0 = static_cast<int64_t>(j) * MOE_QR;
+            const int rows = static_cast<int>((g.Tq - r0) < MOE_QR ? (g.Tq - r0) : MOE_QR);
+            const uint32_t rbytes = static_cast<uint32_t>(g.H * 2);
+            const int rps = STAGE_BYTES / static_cast<int>(rbytes);
+            SchedEntry en;
+            fill_entry(en, K_QUANT, q, j, rows, (rows + rps - 1) / rps, t, trace_open(p, st, K_QUANT, t, tc));
+            if (!ring_push(sm, st.rs, en, p.ws)) return ACT_EXIT;
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(p.x[q] + r0 * g.H);
+            for (int s0 = 0; s0 < rows; s0 += rps) {
+                if (!mbar_wait(&sm.empty[st.ps.stage], st.ps.phase ^ 1u, PIPE_LIMIT_NS)) {
+                    set_error(p.ws, KOSMOS_ERR_DEVICE, t);
+                    return ACT_EXIT;
+                }
+                const int n = (rows - s0) < rps ? (rows - s0) : rps;
+                uint64_t *bar = &sm.full[st.ps.stage];
+                mbar_arrive_expect_tx(bar, n * rbytes);
+                for (int i = 0; i < n; ++i)
+                    bulk_g2s(sm.stages + st.ps.stage * STAGE_BYTES + i * rbytes, src + (s0 + i) * static_cast<int64_t>(rbytes),
+                             rbytes, bar);
+                st.ps.advance();
+            }
+            st.idle_t0 = 0;
+            return ACT_NONE;
+        }
         if (!st.plan_seen) {  // every later entry needs the plan: wait for it, then the warp loads the table
             if (!wait_flag_eq(p.ws, &p.ws->aux[1], epoch + 1u, p.wait_limit_ns, -10)) return ACT_EXIT;
             st.pending = t;
             return ACT_PLAN;
         }
         if (t < static_cast<uint32_t>(g.n_head)) {  // DISPATCH(b, k)
-            const int i = static_cast<int>(t) - g.RB;
+            const int i = static_cast<int>(t) - g.RB - g.NQ;
             v0 = i / g.K;
             v1 = i % g.K;
             v2 = static_cast<int>(t);
@@ -432,6 +500,30 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
                 uint8_t *sa = sm.stages + st.ps.stage * STAGE_BYTES;
                 uint8_t *sb = sa + A_STAGE_BYTES;
                 uint64_t *bar = &sm.full[st.ps.stage];
+                if (g.mx) {
+                    // A 128 rows x 128 bytes, B two 128-column slabs of 16 KB, three scale atoms
+                    uint8_t *sfs = st.sf + st.ps.stage * MOE_SF_BYTES;
+                    mbar_arrive_expect_tx(bar, STAGE_BYTES + MOE_SF_BYTES);
+                    if (kind == K_TILE_GU) {
+                        const int wa = (le * g.NGU + col) * g.nkb_h + kb;  // weight atom (gate and up alike)
+                        tma_load_2d(sa, &p.tmRecv, bar, kb * FBK, row0);
+                        tma_load_3d(sb, &p.tmWg[q], bar, col * 128, kb * FBK, le);
+                        tma_load_3d(sb + 16384, &p.tmWu[q], bar, col * 128, kb * FBK, le);
+                        tma_load_2d(sfs, &p.tmSRecv, bar, 0, ((row0 / BM) * g.nkb_h + kb) * 32);
+                        tma_load_2d(sfs + 512, &p.tmSWg[q], bar, 0, wa * 32);
+                        tma_load_2d(sfs + 1024, &p.tmSWu[q], bar, 0, wa * 32);
+                    } else {
+                        const int wa = (le * 2 * g.ND + 2 * col) * g.nkb_i + kb;  // down atoms of columns 2col, 2col+1
+                        tma_load_2d(sa, &p.tmH, bar, kb * FBK, row0);
+                        tma_load_3d(sb, &p.tmWd[q], bar, col * BN, kb * FBK, le);
+                        tma_load_3d(sb + 16384, &p.tmWd[q], bar, col * BN + 128, kb * FBK, le);
+                        tma_load_2d(sfs, &p.tmSH, bar, 0, ((row0 / BM) * g.nkb_i + kb) * 32);
+                        tma_load_2d(sfs + 512, &p.tmSWd[q], bar, 0, wa * 32);
+                        tma_load_2d(sfs + 1024, &p.tmSWd[q], bar, 0, (wa + g.nkb_i) * 32);
+                    }
+                    st.ps.advance();
+                    continue;
+                }
                 mbar_arrive_expect_tx(bar, STAGE_BYTES);
                 if (kind == K_TILE_GU) {
                     tma_load_2d(sa, &p.tmRecv, bar, kb * BK, row0);
@@ -505,7 +597,10 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
 // The whole producer warp: slot k of the 128 tokens of block b goes to the
 // receive buffer of its expert's rank.  Lanes compute the destination rows;
 // lane 0 moves the rows with bulk async copies through the stage buffers and
-// then releases the per-(expert, row block) arrival counters.
+// then releases the per-(expert, row block) arrival counters.  MXFP8: the
+// rows are the block's quantised rows (once its QUANT entries are done), and
+// the lanes first copy each row's scale words (4 K-blocks each) into the
+// tiled scale atoms of the destination row.
 __device__ __noinline__ void moe_dispatch(const MoeParams &p, const Smem &sm, MoeProdState &st, uint8_t *pscr,
                                           int lane, int b, int k, int ticket, uint32_t epoch) {
     const MoeGeom &g = p.g;
@@ -518,23 +613,55 @@ __device__ __noinline__ void moe_dispatch(const MoeParams &p, const Smem &sm, Mo
     __syncwarp();  // orders lane 0's acquire of the plan before the other lanes' reads
     int slot = -1;
     if (lane == 0) slot = trace_open(p, st, K_DISPATCH, ticket, p.trace ? static_cast<int64_t>(globaltimer()) : 0);
+    const int64_t tok0 = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(b) * BM;
     for (int r = lane; r < nrows; r += 32) {
-        const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(b) * BM + r;
+        const int64_t t = tok0 + r;
         const int e = ldcg_i32(&p.topk_idx[t * g.K + k]);
         const int pos = ldcg_i32(&p.base[gblk * g.E + e]) + ldcg_i32(&p.rank_in_blk[t * g.K + k]);
-        p.pos_out[t * g.K + k] = pos;
+        const int oe = ldcg_i32(&p.offsets[e]);
+        p.pos_out[t * g.K + k] = g.mx ? pos - oe + ldcg_i32(&p.offl[e]) : pos;  // reported without padding
         p.inv_pos[pos] = static_cast<int32_t>(t * g.K + k);
         s_pos[r] = pos;
-        s_ci[r] = e * g.MAXRB + (pos - ldcg_i32(&p.offsets[e])) / BM;
+        s_ci[r] = e * g.MAXRB + (pos - oe) / BM;
+    }
+    bool qok = true;
+    if (g.mx) {
+        if (lane == 0) qok = wait_flag_eq(p.ws, &p.quant_cnt[gblk], static_cast<uint32_t>(nrows), p.wait_limit_ns, ticket);
+        qok = __shfl_sync(0xFFFFFFFFu, qok ? 1 : 0, 0) != 0;
+        __syncwarp();
+        if (qok) {
+            const int W = static_cast<int>(g.H / 128);  // scale words per row
+            const int nw = nrows * W;
+            const uint32_t *xs = reinterpret_cast<const uint32_t *>(p.xs);
+            constexpr int U = 16;
+            for (int i0 = 0; i0 < nw; i0 += 32 * U) {
+                uint32_t v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = i0 + u * 32 + lane;
+                    if (i < nw) v[u] = __ldcg(xs + (tok0 + i / W) * W + i % W);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = i0 + u * 32 + lane;
+                    if (i < nw) {
+                        const int64_t pos = s_pos[i / W];
+                        *reinterpret_cast<uint32_t *>(p.recv_sf + sf_tiled_offset(pos, 4 * (i % W), 4 * W)) = v[u];
+                    }
+                }
+            }
+            __threadfence();
+        }
     }
     __syncwarp();
     if (lane == 0) {
-        bool ok = drain_pipeline(p, sm, st.ps);
-        const uint32_t rbytes = static_cast<uint32_t>(g.H * 2);
+        bool ok = qok && drain_pipeline(p, sm, st.ps);
+        const uint32_t rbytes = static_cast<uint32_t>(g.mx ? g.H : g.H * 2);
         const int per = STAGE_BYTES / static_cast<int>(rbytes);
         const int nch = (nrows + per - 1) / per;
-        const uint8_t *src0 = reinterpret_cast<const uint8_t *>(p.x[q] + static_cast<int64_t>(b) * BM * g.H);
-        uint8_t *recv = reinterpret_cast<uint8_t *>(p.recv);
+        const uint8_t *src0 = g.mx ? p.xq + tok0 * g.H
+                                   : reinterpret_cast<const uint8_t *>(p.x[q] + static_cast<int64_t>(b) * BM * g.H);
+        uint8_t *recv = g.mx ? p.recv8 : reinterpret_cast<uint8_t *>(p.recv);
         auto issue = [&](int c) {
             const int bi = c % NSTAGE;
             const int r0 = c * per;
@@ -574,9 +701,10 @@ __device__ __noinline__ void moe_dispatch(const MoeParams &p, const Smem &sm, Mo
     __syncwarp();
 }
 
-__device__ __forceinline__ void moe_producer(const MoeParams &p, const Smem &sm, uint8_t *pscr, uint32_t epoch,
-                                             int lane) {
+__device__ __forceinline__ void moe_producer(const MoeParams &p, const Smem &sm, uint8_t *pscr, uint8_t *sf,
+                                             uint32_t epoch, int lane) {
     MoeProdState st;
+    st.sf = sf;
     // producer scratch: [0, 1 KB) dispatch rows, then the plan table (3 Eq + 1 words <= 3 KB)
     st.us = reinterpret_cast<int32_t *>(pscr + 1024);
     st.off = st.us + p.g.Eq + 1;
@@ -747,11 +875,23 @@ __device__ __noinline__ void moe_route_epilogue(const MoeParams &p, const SchedE
     // and global accesses cost tens of microseconds here): warp 0 scans the
     // expert counts into the receive offsets, warps 1.. scan each rank's
     // row-block units
-    int32_t *s_us = reinterpret_cast<int32_t *>(escr);  // [P][Eq + 1] <= 264 words, over s_bits (done with)
+    int32_t *s_us = reinterpret_cast<int32_t *>(escr);           // [P][Eq + 1] <= 264 words, over s_bits (done with)
+    int32_t *s_offl = reinterpret_cast<int32_t *>(escr + 2048);  // [E + 1], MXFP8 only, over s_bits
     const int ew = et / 32, lane = et % 32;
     if (ew == 0) {
-        const int total = warp_excl_scan(s_cnt, s_off, E, lane, 0);
-        if (lane == 0) s_off[E] = total;
+        if (g.mx) {
+            // receive offsets without padding (reported), and with every expert
+            // starting on a 128-row boundary (the layout of the buffers)
+            const int tl = warp_excl_scan(s_cnt, s_offl, E, lane, 0);
+            if (lane == 0) s_offl[E] = tl;
+            const int tu = warp_excl_scan(s_cnt, s_off, E, lane, BM);
+            __syncwarp();
+            for (int i = lane; i < E; i += 32) s_off[i] *= BM;
+            if (lane == 0) s_off[E] = tu * BM;
+        } else {
+            const int total = warp_excl_scan(s_cnt, s_off, E, lane, 0);
+            if (lane == 0) s_off[E] = total;
+        }
     } else {
         for (int qq = ew - 1; qq < g.P; qq += NUM_EPI_THREADS / 32 - 1) {
             const int total = warp_excl_scan(s_cnt + qq * g.Eq, s_us + qq * (g.Eq + 1), g.Eq, lane, BM);
@@ -759,7 +899,10 @@ __device__ __noinline__ void moe_route_epilogue(const MoeParams &p, const SchedE
         }
     }
     named_bar_sync(1, NUM_EPI_THREADS);
-    for (int i = et; i <= E; i += NUM_EPI_THREADS) p.offsets[i] = s_off[i];
+    for (int i = et; i <= E; i += NUM_EPI_THREADS) {
+        p.offsets[i] = s_off[i];
+        p.offl[i] = g.mx ? s_offl[i] : s_off[i];
+    }
     for (int i = et; i < g.P * (g.Eq + 1); i += NUM_EPI_THREADS) p.unit_start[i] = s_us[i];
     for (int i = et; i < E; i += NUM_EPI_THREADS) {
         int run = s_off[i];
@@ -894,6 +1037,56 @@ __device__ __noinline__ bool moe_fold(const MoeParams &p, const Smem &sm, PipeSt
     return true;
 }
 
+// QUANT(j): the entry's bf16 token rows arrive through the stage ring; each
+// thread quantises 32-element blocks (E4M3 bytes to xq, the E8M0 byte to the
+// row-major xs), then the block's quantised-row counter is released.
+__device__ __noinline__ bool moe_quant(const MoeParams &p, const Smem &sm, PipeState &ps, const SchedEntry &e,
+                                       int et) {
+    const MoeGeom &g = p.g;
+    const int q = e.a, j = e.b, rows = e.c;
+    const int64_t t0 = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(j) * MOE_QR;
+    const int rbytes = static_cast<int>(g.H * 2);
+    const int rps = STAGE_BYTES / rbytes;
+    const int HB = static_cast<int>(g.H / 32);
+    for (int s = 0; s < e.nstage; ++s) {
+        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -13);
+            return false;
+        }
+        const uint8_t *buf = sm.stages + ps.stage * STAGE_BYTES;
+        const int n = (rows - s * rps) < rps ? (rows - s * rps) : rps;
+        for (int bi = et; bi < n * HB; bi += NUM_EPI_THREADS) {
+            const int r = bi / HB, kb = bi % HB;
+            const uint4 *src = reinterpret_cast<const uint4 *>(buf + r * rbytes + kb * 64);
+            float v[32];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint4 w4 = src[h];
+                const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[h * 8 + 2 * i] = __uint_as_float(w[i] << 16);
+                    v[h * 8 + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+            }
+            uint32_t o[8];
+            const uint32_t sc = mx_quant32(v, o);
+            const int64_t t = t0 + static_cast<int64_t>(s) * rps + r;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.xq + t * g.H + kb * 32);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            p.xs[t * HB + kb] = static_cast<uint8_t>(sc);
+        }
+        named_bar_sync(1, NUM_EPI_THREADS);
+        if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
+        ps.advance();
+    }
+    __threadfence();
+    named_bar_sync(1, NUM_EPI_THREADS);
+    if (et == 0) red_release_add_gpu(&p.quant_cnt[q * g.RB + (j * MOE_QR) / BM], static_cast<uint32_t>(rows));
+    return true;
+}
+
 __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm, uint32_t tmem_base, uint8_t *escr,
                                              int warp, int lane, uint32_t epoch) {
     const MoeGeom &g = p.g;
@@ -902,8 +1095,9 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
     const int ew = warp - 2;
     const int et = ew * 32 + lane;
     RingState rs;
-    PipeState ps;  // stages of the ring: MMA entries are skipped, FOLD stages consumed here
+    PipeState ps;  // stages of the ring: MMA entries are skipped, FOLD and QUANT stages consumed here
     uint32_t acc = 0, acc_phase = 0;
+    const uint32_t nacc = g.mx ? 1u : 2u;  // MXFP8: the scale atoms take the second accumulator's columns
     while (true) {
         if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
             set_error(p.ws, KOSMOS_ERR_DEVICE, -6);
@@ -924,6 +1118,31 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
             if (e.kind == K_ROUTE) {
                 moe_route_epilogue(p, e, taddr, row, et, escr, epoch);
+            } else if (e.kind == K_TILE_GU && g.mx) {
+                // h = silu(gate) * up per 32 columns, quantised: E4M3 bytes to h8,
+                // the four E8M0 bytes of this row (K-blocks 4c .. 4c+3) as one word
+                const bool valid = row < e.x1;
+                const int64_t r = e.x0 + row;  // e.x0 is a multiple of 128
+                uint8_t *dst = p.h8 + r * g.I + e.c * 128;
+                uint32_t sw = 0;
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t gr[32], ur[32];
+                    tmem_ld_32x32b_x32(taddr + ch * 32, gr);
+                    tmem_ld_32x32b_x32(taddr + 128 + ch * 32, ur);
+                    tmem_ld_wait();
+                    float hv[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) hv[j] = silu_f(__uint_as_float(gr[j])) * __uint_as_float(ur[j]);
+                    uint32_t o[8];
+                    sw |= mx_quant32(hv, o) << (8 * ch);
+                    if (valid) {
+                        uint4 *d = reinterpret_cast<uint4 *>(dst + ch * 32);
+                        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+                if (valid) *reinterpret_cast<uint32_t *>(p.h_sf + sf_tiled_offset(r, 4 * e.c, g.I / 32)) = sw;
             } else if (e.kind == K_TILE_GU) {
                 const bool valid = row < e.x1;
                 __nv_bfloat16 *dst = p.h + static_cast<int64_t>(e.x0 + (valid ? row : 0)) * g.I + e.c * 128;
@@ -958,7 +1177,7 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.tempty[acc]);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
             if (e.kind == K_TILE_GU || e.kind == K_TILE_D) {
                 __threadfence();
                 named_bar_sync(1, NUM_EPI_THREADS);
@@ -976,10 +1195,75 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
             moe_push(p, e, ew, lane, epoch);
         } else if (e.kind == K_FOLD) {
             if (!moe_fold(p, sm, ps, e, et, escr)) break;
+        } else if (e.kind == K_QUANT) {
+            if (!moe_quant(p, sm, ps, e, et)) break;
         }
         if (e.slot >= 0 && et == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
         }
+    }
+}
+
+// MMA warp (one thread): ROUTE entries as bf16 MMAs with N = E; GU / D tiles
+// as bf16 MMAs into two alternating accumulators, or (MXFP8) as block-scaled
+// MMAs into one accumulator with the stage's scale atoms copied to tensor
+// memory columns 256 + 16 * stage.
+__device__ __forceinline__ void moe_mma_loop(const MoeParams &p, const Smem &sm, const uint8_t *sf,
+                                             uint32_t tmem_base) {
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, true);
+    const bool mx = p.g.mx;
+    const uint32_t nacc = mx ? 1u : 2u;
+    PipeState ps;
+    RingState rs;
+    uint32_t acc = 0, acc_phase = 0;
+    while (true) {
+        if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -3);
+            break;
+        }
+        const SchedEntry e = sm.sched[rs.idx];
+        mbar_arrive(&sm.sempty[rs.idx]);
+        rs.advance();
+        if (e.kind == K_DONE) break;
+        if (!is_mma_kind(e.kind)) {
+            ps.advance(e.nstage);
+            continue;
+        }
+        const uint32_t idesc = (e.nmma > 0 && e.nmma < BN) ? idesc_bf16_f32(BM, e.nmma, false, true) : IDESC;
+        const bool blk = mx && e.kind != K_ROUTE;
+        if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -4);
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < e.nstage; ++kb) {
+            if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, -5);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sm.stages + ps.stage * STAGE_BYTES);
+            const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+            if (blk) {
+                mx_stage_mma(d_tmem, a_addr, b_addr, 16384, smem_u32(sf + ps.stage * MOE_SF_BYTES),
+                             tmem_base + F_TMEM_SF + ps.stage * F_TMEM_SF_STRIDE, kb == 0);
+            } else {
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; ++k) {
+                    const uint64_t ad = sdesc_sw128(a_addr + k * (UMMA_K * 2), 16, 1024);
+                    const uint64_t bd = sdesc_sw128(b_addr + k * (UMMA_K * 128), 64 * 128, 1024);
+                    mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                }
+            }
+            mma_commit(&sm.empty[ps.stage]);
+            ps.advance();
+        }
+        if (!ok) break;
+        mma_commit(&sm.tfull[acc]);
+        if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
     }
 }
 
@@ -989,15 +1273,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_fwd_kernel(const __grid_co
     uint8_t *scratch = sm.stages + NSTAGE * STAGE_BYTES + SMEM_CTRL_BYTES;
     uint8_t *escr = scratch;          // epilogue: 8 KB
     uint8_t *pscr = scratch + 8192;   // producer: 4 KB
+    uint8_t *sf = scratch + MOE_SCRATCH;  // MXFP8 scale atoms: NSTAGE x 1.5 KB
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
     engine_setup(sm, warp);
     const uint32_t tmem_base = *sm.tmem_slot;
     if (warp == 0) {
-        moe_producer(p, sm, pscr, epoch, lane);
+        moe_producer(p, sm, pscr, sf, epoch, lane);
     } else if (warp == 1) {
-        if (lane == 0) mma_loop(sm, tmem_base, p.ws);
+        if (lane == 0) moe_mma_loop(p, sm, sf, tmem_base);
     } else {
         moe_epilogue(p, sm, tmem_base, escr, warp, lane, epoch);
     }
@@ -1027,23 +1312,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_fwd_kernel(const __grid_co
     }
 }
 
-size_t moe_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool trace) {
-    return moe_ws_layout(moe_geom(P, T, H, E, K, I), trace).total;
+size_t moe_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool mx, bool trace) {
+    return moe_ws_layout(moe_geom(P, T, H, E, K, I, mx), trace).total;
 }
 
-bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t I, void *ws, void **ptr,
+bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t I, bool mx, void *ws, void **ptr,
                     int64_t *bytes) {
-    const MoeGeom g = moe_geom(P, T, H, E, K, I);
+    const MoeGeom g = moe_geom(P, T, H, E, K, I, mx);
     const MoeWsLayout L = moe_ws_layout(g, what == 6);
+    const size_t esz = mx ? 1 : 2;
+    const size_t rows = mx ? static_cast<size_t>(g.rows_cap) : static_cast<size_t>(g.T * g.K);
     size_t off = 0, n = 0;
     switch (what) {
         case 0: off = L.logits; n = 4ull * g.T * g.E; break;
-        case 1: off = L.recv; n = 2ull * g.T * g.K * g.H; break;
-        case 2: off = L.h; n = 2ull * g.T * g.K * g.I; break;
-        case 3: off = L.ybuf; n = 2ull * g.T * g.K * g.H; break;
+        case 1: off = L.recv; n = esz * rows * g.H; break;
+        case 2: off = L.h; n = esz * rows * g.I; break;
+        case 3: off = L.ybuf; n = 2ull * rows * g.H; break;
         case 4: off = L.slot; n = 2ull * g.T * g.K * g.H; break;
         case 5: off = L.offsets; n = 4ull * (g.E + 1); break;
         case 6: off = L.trace; n = static_cast<size_t>(MAX_CTAS) * TRACE_CAP * sizeof(TraceRec); break;
+        case 7: if (!mx) return false; off = L.recv_sf; n = static_cast<size_t>(g.rows_cap * g.H / 32); break;
+        case 8: if (!mx) return false; off = L.xq; n = static_cast<size_t>(g.T * g.H); break;
+        case 9: if (!mx) return false; off = L.xs; n = static_cast<size_t>(g.T * g.H / 32); break;
         default: return false;
     }
     *ptr = static_cast<uint8_t *>(ws) + off;
@@ -1054,7 +1344,8 @@ bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t
 kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
     MoeParams p;
     memset(&p, 0, sizeof(p));
-    p.g = moe_geom(Lc.P, Lc.T, Lc.H, Lc.E, Lc.K, Lc.I);
+    const bool mx = Lc.dtype == KOSMOS_MXFP8_E4M3;
+    p.g = moe_geom(Lc.P, Lc.T, Lc.H, Lc.E, Lc.K, Lc.I, mx);
     const MoeGeom &g = p.g;
     const MoeWsLayout L = moe_ws_layout(g, Lc.trace != 0);
     uint8_t *ws = static_cast<uint8_t *>(Lc.ws);
@@ -1070,6 +1361,16 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
     p.rank_in_blk = reinterpret_cast<int32_t *>(ws + L.rank_in_blk);
     p.base = reinterpret_cast<int32_t *>(ws + L.base);
     p.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    p.offl = reinterpret_cast<int32_t *>(ws + L.offl);
+    p.quant_cnt = reinterpret_cast<uint32_t *>(ws + L.quant_cnt);
+    if (mx) {
+        p.xq = ws + L.xq;
+        p.xs = ws + L.xs;
+        p.recv8 = ws + L.recv;
+        p.recv_sf = ws + L.recv_sf;
+        p.h8 = ws + L.h;
+        p.h_sf = ws + L.h_sf;
+    }
     p.counts = reinterpret_cast<int32_t *>(ws + L.counts);
     p.unit_start = reinterpret_cast<int32_t *>(ws + L.unit_start);
     p.inv_pos = reinterpret_cast<int32_t *>(ws + L.inv_pos);
@@ -1104,22 +1405,39 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
                              CU_TENSOR_MAP_SWIZZLE_128B))
                 return KOSMOS_ERR_CUDA;
         }
+        // weights: bf16 boxes of 64 columns x 64 K, or E4M3 boxes of 128 x 128
+        const CUtensorMapDataType wdt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const uint64_t esz = mx ? 1 : 2;
+        const uint32_t bw = mx ? 128u : 64u, bk = mx ? static_cast<uint32_t>(FBK) : static_cast<uint32_t>(BK);
         {
             const uint64_t dims[3] = {I, H, Eq};
-            const uint64_t st[2] = {I * 2, H * I * 2};
-            const uint32_t box[3] = {64, BK, 1};
-            if (!encode_tmap(&p.tmWg[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(Lc.wg[q]), dims, st,
-                             box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-                !encode_tmap(&p.tmWu[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(Lc.wu[q]), dims, st,
-                             box, CU_TENSOR_MAP_SWIZZLE_128B))
+            const uint64_t st[2] = {I * esz, H * I * esz};
+            const uint32_t box[3] = {bw, bk, 1};
+            if (!encode_tmap(&p.tmWg[q], wdt, 3, const_cast<void *>(Lc.wg[q]), dims, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !encode_tmap(&p.tmWu[q], wdt, 3, const_cast<void *>(Lc.wu[q]), dims, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
                 return KOSMOS_ERR_CUDA;
         }
         {
             const uint64_t dims[3] = {H, I, Eq};
-            const uint64_t st[2] = {H * 2, H * I * 2};
-            const uint32_t box[3] = {64, BK, 1};
-            if (!encode_tmap(&p.tmWd[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(Lc.wd[q]), dims, st,
-                             box, CU_TENSOR_MAP_SWIZZLE_128B))
+            const uint64_t st[2] = {H * esz, H * I * esz};
+            const uint32_t box[3] = {bw, bk, 1};
+            if (!encode_tmap(&p.tmWd[q], wdt, 3, const_cast<void *>(Lc.wd[q]), dims, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+                return KOSMOS_ERR_CUDA;
+        }
+        if (mx) {
+            // tiled weight scales, experts one after the other: I*H/32 bytes each
+            const uint64_t st[1] = {16};
+            const uint32_t box[2] = {16, 32};
+            const uint64_t dims[2] = {16, Eq * I * H / 32 / 16};
+            if (!encode_tmap(&p.tmSWg[q], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Lc.wgs[q]), dims, st,
+                             box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                !encode_tmap(&p.tmSWu[q], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Lc.wus[q]), dims, st,
+                             box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                !encode_tmap(&p.tmSWd[q], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Lc.wds[q]), dims, st,
+                             box, CU_TENSOR_MAP_SWIZZLE_NONE))
                 return KOSMOS_ERR_CUDA;
         }
     }
@@ -1132,19 +1450,26 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
             return KOSMOS_ERR_CUDA;
     }
     {
-        const uint64_t dims[2] = {H, RC};
-        const uint64_t st[1] = {H * 2};
-        const uint32_t box[2] = {BK, BM};
-        if (!encode_tmap(&p.tmRecv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.recv, dims, st, box,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
+        // receive rows and h: bf16 boxes of 64 K x 128 rows, or E4M3 boxes of 128 x 128
+        const CUtensorMapDataType adt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const uint64_t esz = mx ? 1 : 2;
+        const uint32_t bk = mx ? static_cast<uint32_t>(FBK) : static_cast<uint32_t>(BK);
+        const uint64_t dr[2] = {H, RC}, sr[1] = {H * esz};
+        const uint64_t dh[2] = {I, RC}, sh[1] = {I * esz};
+        const uint32_t box[2] = {bk, BM};
+        if (!encode_tmap(&p.tmRecv, adt, 2, p.recv, dr, sr, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&p.tmH, adt, 2, p.h, dh, sh, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return KOSMOS_ERR_CUDA;
-    }
-    {
-        const uint64_t dims[2] = {I, RC};
-        const uint64_t st[1] = {I * 2};
-        const uint32_t box[2] = {BK, BM};
-        if (!encode_tmap(&p.tmH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.h, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return KOSMOS_ERR_CUDA;
+        if (mx) {
+            const uint64_t st[1] = {16};
+            const uint32_t sbox[2] = {16, 32};
+            const uint64_t dsr[2] = {16, RC * H / 32 / 16}, dsh[2] = {16, RC * I / 32 / 16};
+            if (!encode_tmap(&p.tmSRecv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.recv_sf, dsr, st, sbox,
+                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                !encode_tmap(&p.tmSH, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.h_sf, dsh, st, sbox,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+                return KOSMOS_ERR_CUDA;
+        }
     }
     {
         // FOLD: fold_tps tokens x K slot rows x 256 columns per stage (<= 32 KB)

@@ -11,6 +11,8 @@
 // tcgen05.cp 32x128b.warpx4 it lands in four TMEM columns, lane r%32 of every
 // 32-lane group holding rows r%32 + 32c in column c, one byte per K-block.
 #pragma once
+#include <cuda_fp8.h>
+
 #include "engine2.cuh"
 
 namespace kosmos {
@@ -37,6 +39,87 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
 __device__ __forceinline__ uint32_t idesc_mxf8(int M, int N, int sf_id) {
     return (static_cast<uint32_t>(sf_id) << 4) | (1u << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
            (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+}
+
+// ---------------------------------------------------------------- codec
+// Shared exponent of one block: the smallest integer e with
+// blockmax <= 448 * 2^e, clamped to [-127, 127]; 0 for an all-zero block.
+// Write blockmax (a finite float) as f * 2^E with f in [1, 2); 448 = 1.75 * 2^8,
+// so e = E - 8 when f <= 1.75 and E - 7 otherwise.
+__device__ __forceinline__ int mx_block_exp(float blockmax) {
+    const uint32_t b = __float_as_uint(blockmax);
+    const int ex = static_cast<int>((b >> 23) & 0xFF);
+    const uint32_t man = b & 0x7FFFFFu;
+    if (ex == 0) return man == 0 ? 0 : -127;  // zero, or below 2^-126: clamped
+    const int E = ex - 127;
+    int e = (man <= 0x600000u) ? E - 8 : E - 7;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+// Byte offset of the scale of (scale row r, K-block b) in the MMA-tiled layout:
+// 512-byte atoms of 128 scale rows x 4 K-blocks, atoms ordered by row block,
+// then K; inside an atom row r sits at (r % 32) * 16 + ((r / 32) % 4) * 4.
+__host__ __device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t b, int64_t kblocks) {
+    return ((r / 128) * (kblocks / 4) + b / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + (b % 4);
+}
+
+// One MXFP8 block of 32 values: the E4M3 bytes of v / 2^e (round to nearest
+// even, saturating; exact scaling by a power of two) packed four to a word in
+// element order, and the E8M0 byte e + 127 as the return value.
+__device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&w)[8]) {
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(v[j]));
+    const int e = mx_block_exp(mx);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e (e <= 126 for finite input)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            word |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[4 * i + j] * inv, __NV_SATFINITE, __NV_E4M3))
+                    << (8 * j);
+        w[i] = word;
+    }
+    return static_cast<uint32_t>(e + 127);
+}
+
+// ---------------------------------------------------------------- single-SM pieces
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 32 rows x 16 bytes from shared memory into TMEM lanes 0-31 of four columns,
+// replicated to the four 32-lane groups.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// One 128-wide K stage of a 128 x 256 block-scaled tile on one SM: copy the
+// stage's three scale atoms (SFA, SFB columns 0-127, SFB 128-255) into tensor
+// memory at sfa_t, then four K = 32 MMAs.  A: 128 rows x 128 bytes, B: two
+// 128-column slabs of b_slab bytes, both with the 128-byte swizzle.
+__device__ __forceinline__ void mx_stage_mma(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t b_slab,
+                                             uint32_t sf_addr, uint32_t sfa_t, bool first) {
+    const uint32_t sfb_t = sfa_t + 4;
+    tmem_cp_32x128b_x4(sfa_t, sdesc_sf(sf_addr));
+    tmem_cp_32x128b_x4(sfb_t, sdesc_sf(sf_addr + 512));
+    tmem_cp_32x128b_x4(sfb_t + 4, sdesc_sf(sf_addr + 1024));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint64_t ad = sdesc_sw128(a_addr + j * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(b_addr + j * (32 * 128), b_slab, 1024);
+        mma_mxf8_ss(d_tmem, ad, bd, idesc_mxf8(BM, BN, j), sfa_t, sfb_t, (!first || j != 0) ? 1u : 0u);
+    }
 }
 
 // ---------------------------------------------------------------- SM-pair engine

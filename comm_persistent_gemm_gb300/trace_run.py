@@ -1,7 +1,7 @@
 """Runs one traced launch of each fused operator on the full-size synthetic
 workloads and writes Chrome traces plus the role time accounting.
 
-    python -m comm_persistent_gemm_gb300.trace_run --out DIR [--only ag,rs,moe,mxfp8]
+    python -m comm_persistent_gemm_gb300.trace_run --out DIR [--only ag,rs,moe,mxfp8,moe_mxfp8]
 
 Output: DIR/<name>.trace.json (chrome://tracing / Perfetto) and one JSON line
 per traced launch on stdout with the summary of trace.summarize().
@@ -81,7 +81,22 @@ def _trace_rs(K, out, name, o):
     return K.trace_records(K.OP_GEMM_RS, w.P, w.m, w.n, w.k, ws, o)
 
 
-def _trace_moe(K, out, name, o):
+def _quant_experts(K, w, P):
+    import torch
+    E, Kd, N = w.shape
+    nb = K.mxfp8_scale_bytes(Kd, N, False)
+    codes, scales = [], []
+    for q in range(P):
+        c = torch.empty(E // P, Kd, N, dtype=torch.uint8, device="cuda")
+        s = torch.empty((E // P) * nb, dtype=torch.uint8, device="cuda")
+        for j in range(E // P):
+            K.mxfp8_quantize(w[q * (E // P) + j].cuda(), c[j], s[j * nb:(j + 1) * nb], False)
+        codes.append(c)
+        scales.append(s)
+    return codes, scales
+
+
+def _trace_moe(K, out, name, o, mx=False):
     import torch
     from kosmos_inputs import WORKLOADS, workload_inputs
     from .trace import TRACE_DTYPE
@@ -90,21 +105,27 @@ def _trace_moe(K, out, name, o):
     P, T, H, E, Kt, I = w.P, w.T, w.H, w.E, w.topk, w.I
     xs = [t.cuda() for t in torch.chunk(inp["x"], P, 0)]
     wr = inp["w_router"].cuda()
-    sp = lambda t: [t[q * (E // P):(q + 1) * (E // P)].contiguous().cuda() for q in range(P)]
-    wg, wu, wd = sp(inp["w_gate"]), sp(inp["w_up"]), sp(inp["w_down"])
+    kw = {}
+    if mx:
+        (wg, sg), (wu, su), (wd, sd) = (_quant_experts(K, inp[n], P) for n in ("w_gate", "w_up", "w_down"))
+        kw = {"dtype": K.MXFP8_E4M3, "w_gate_scales": sg, "w_up_scales": su, "w_down_scales": sd}
+    else:
+        sp = lambda t: [t[q * (E // P):(q + 1) * (E // P)].contiguous().cuda() for q in range(P)]
+        wg, wu, wd = sp(inp["w_gate"]), sp(inp["w_up"]), sp(inp["w_down"])
     ys = [torch.empty(T // P, H, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
     idx = torch.empty(T, Kt, dtype=torch.int32, device="cuda")
     gate = torch.empty(T, Kt, dtype=torch.float32, device="cuda")
     cnt = torch.empty(E, dtype=torch.int32, device="cuda")
     pos = torch.empty(T, Kt, dtype=torch.int32, device="cuda")
-    ws = K.moe_workspace(P, T, H, E, Kt, I, o)
+    dt = K.MXFP8_E4M3 if mx else K.BF16
+    ws = K.moe_workspace(P, T, H, E, Kt, I, o, dtype=dt)
     for _ in range(2):
-        K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, cnt, pos, ws, Kt, o)
+        K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, cnt, pos, ws, Kt, o, **kw)
     K.check(ws, name)
     ws.zero_()
-    K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, cnt, pos, ws, Kt, o)
+    K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, cnt, pos, ws, Kt, o, **kw)
     K.check(ws, name)
-    raw = K.moe_debug_view(K.MOE_VIEW_TRACE, P, T, H, E, Kt, I, ws).cpu().numpy()
+    raw = K.moe_debug_view(K.MOE_VIEW_TRACE, P, T, H, E, Kt, I, ws, dtype=dt).cpu().numpy()
     recs = raw.view(TRACE_DTYPE)
     return recs[recs["kind"] != 0]
 
@@ -136,6 +157,8 @@ def main(argv=None):
         runs += [("rs_band", _trace_rs, K.opts(trace=1)), ("rs_row", _trace_rs, K.opts(trace=1, order=K.ORDER_ROW))]
     if "moe" in only:
         runs += [("moe_fwd", _trace_moe, K.opts(trace=1))]
+    if "moe_mxfp8" in only:
+        runs += [("moe_fwd_mxfp8", lambda *a: _trace_moe(*a, mx=True), K.opts(trace=1))]
     for name, fn, o in runs:
         recs = fn(K, a.out, name, o)
         s = summarize(recs, n_ctas=sms)

@@ -208,43 +208,67 @@ KOSMOS_API kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void 
  *
  *   x_shards[q]   : EP rank q's tokens [tokens/P, hidden] bf16 (token t lives on
  *                   rank t / (tokens/P)).
- *   w_router      : [hidden, n_experts] bf16.
- *   w_gate[q], w_up[q] : rank q's experts [n_experts/P, hidden, inter] bf16.
- *   w_down[q]     : [n_experts/P, inter, hidden] bf16.
+ *   w_router      : [hidden, n_experts] bf16 (the router is bf16 for both dtypes).
+ *   w_gate[q], w_up[q] : rank q's experts [n_experts/P, hidden, inter]; BF16: bf16,
+ *                   MXFP8: E4M3 bytes.
+ *   w_down[q]     : [n_experts/P, inter, hidden]; bf16 or E4M3 bytes.
+ *   w_*_scales[q] : MXFP8 only (else NULL): the E8M0 scales of rank q's experts,
+ *                   one after the other, each expert's matrix quantised along its
+ *                   K dimension (hidden for gate/up, inter for down; one scale per
+ *                   column and 32 K) and MMA-tiled with the columns as scale rows
+ *                   (kosmos_mxfp8_quantize with along_cols = 0 per expert):
+ *                   inter*hidden/32 bytes per expert.
+ *   dtype         : KOSMOS_BF16 or KOSMOS_MXFP8_E4M3.  MXFP8 quantises the token
+ *                   rows (along hidden) and the SwiGLU activations h (along
+ *                   inter) inside the launch with the rule of kosmos_mxfp8_quantize
+ *                   (h from its fp32 value); the expert GEMMs are block-scaled
+ *                   with fp32 accumulation.
  *   y_shards[q]   : out, [tokens/P, hidden] bf16.
  *   topk_idx      : out, [tokens, topk] int32, descending router score, ties to the lower index.
  *   topk_gate     : out, [tokens, topk] fp32, softmax probabilities renormalised over the top-k.
  *   expert_counts : out, [n_experts] int32.
  *   dispatch_pos  : out, [tokens, topk] int32: row of (t, k) in the expert-ordered
- *                   receive buffer (experts ascending, then tokens ascending).
+ *                   receive buffer (experts ascending, then tokens ascending),
+ *                   counted without padding (MXFP8 stores each expert's rows
+ *                   from a 128-row boundary: physical row = dispatch_pos -
+ *                   unpadded offset of the expert + padded offset).
  *   Requirements: P in {1..8}, n_experts % P == 0, n_experts % 64 == 0,
  *   n_experts <= 256, 1 <= topk <= 8, topk <= n_experts, tokens % P == 0,
- *   hidden % 256 == 0, inter % 128 == 0.  Workspace: kosmos_moe_workspace_bytes.
+ *   hidden % 256 == 0, inter % 128 == 0.  MXFP8: no identity-expert
+ *   injection (KOSMOS_ERR_UNSUPPORTED).  Workspace: kosmos_moe_workspace_bytes.
  */
 KOSMOS_API kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, int P,
                              int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter,
-                             const void *const *w_gate, const void *const *w_up,
-                             const void *const *w_down, void *const *y_shards,
+                             const void *const *w_gate, const void *const *w_gate_scales,
+                             const void *const *w_up, const void *const *w_up_scales,
+                             const void *const *w_down, const void *const *w_down_scales, int dtype,
+                             void *const *y_shards,
                              int32_t *topk_idx, float *topk_gate, int32_t *expert_counts,
                              int32_t *dispatch_pos, void *ws, size_t ws_bytes,
                              const kosmos_opts *opts, void *stream);
 
-/* Workspace size in bytes for kosmos_moe_fwd with these sizes (opts may be
- * NULL).  Returns 0 for invalid sizes. */
+/* Workspace size in bytes for kosmos_moe_fwd with these sizes and dtype (opts
+ * may be NULL).  Returns 0 for invalid sizes or dtype. */
 KOSMOS_API size_t kosmos_moe_workspace_bytes(int P, int64_t tokens, int64_t hidden, int n_experts, int topk,
-                                             int64_t inter, const kosmos_opts *opts);
+                                             int64_t inter, int dtype, const kosmos_opts *opts);
 
-/* Device views into a MoE workspace after a call (for checks and tools):
+/* Device views into a MoE workspace after a call (for checks and tools).
+ * R = tokens*topk rows (BF16) or the padded row capacity (MXFP8: each expert's
+ * rows from a 128-row boundary, row order as in the receive buffer):
  *   what 0: router logits [tokens, n_experts] fp32 (as the kernel computed them)
- *        1: receive buffer [tokens*topk, hidden] bf16, expert-ordered rows
- *        2: SwiGLU activations h [tokens*topk, inter] bf16, same row order
- *        3: expert outputs [tokens*topk, hidden] bf16, same row order
+ *        1: receive buffer [R, hidden], bf16 or E4M3 bytes, expert-ordered rows
+ *        2: SwiGLU activations h [R, inter], bf16 or E4M3 bytes, same row order
+ *        3: expert outputs [R, hidden] bf16, same row order
  *        4: pushed slots [tokens, topk, hidden] bf16
- *        5: expert offsets [n_experts + 1] int32
+ *        5: expert offsets [n_experts + 1] int32 (MXFP8: padded)
  *        6: role trace records (only for a workspace sized with opts.trace)
+ *        7: MXFP8: receive-row scales, MMA-tiled (K = hidden)
+ *        8: MXFP8: quantised tokens [tokens, hidden] E4M3 bytes
+ *        9: MXFP8: their scales [tokens, hidden/32], row-major
  * Returns KOSMOS_OK and sets *ptr / *bytes, or KOSMOS_ERR_INVALID_ARG. */
 KOSMOS_API kosmos_status kosmos_moe_debug_view(int what, int P, int64_t tokens, int64_t hidden, int n_experts,
-                                               int topk, int64_t inter, void *ws, void **ptr, int64_t *bytes);
+                                               int topk, int64_t inter, int dtype, void *ws, void **ptr,
+                                               int64_t *bytes);
 
 /*
  * MXFP8 quantiser for the MXFP8 all-gather+GEMM operands.  For each block of

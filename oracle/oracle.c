@@ -108,6 +108,7 @@ ORC_EXPORT int orc_mxfp8_quantize(int64_t rows, int64_t cols, const uint16_t *x,
                                   int along_cols, uint8_t *q, uint8_t *scales) {
     if (along_cols) {
         if (cols % 32) return 1;
+#pragma omp parallel for schedule(static)
         for (int64_t i = 0; i < rows; i++)
             for (int64_t b = 0; b < cols / 32; b++) {
                 double mx = 0.0;
@@ -124,6 +125,7 @@ ORC_EXPORT int orc_mxfp8_quantize(int64_t rows, int64_t cols, const uint16_t *x,
             }
     } else {
         if (rows % 32) return 1;
+#pragma omp parallel for schedule(static)
         for (int64_t c = 0; c < cols; c++)
             for (int64_t b = 0; b < rows / 32; b++) {
                 double mx = 0.0;

@@ -24,6 +24,43 @@ def test_exports_every_declared_symbol(K):
     assert sorted(K.EXPORTS) == names
 
 
+def _header_prototypes():
+    """name -> list of parameter declarations, from include/kosmos.h."""
+    import os
+    import re
+    from _helpers import ROOT
+    src = open(os.path.join(ROOT, "include", "kosmos.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"KOSMOS_API\s+[\w\s\*]+?\b(kosmos_\w+)\s*\(([^)]*)\)\s*;", src):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip()]
+        out[m.group(1)] = [] if params == ["void"] else params
+    return out
+
+
+def test_binding_argument_lists_match_the_header(K):
+    """Every ctypes prototype has the header's parameter count, and 64-bit
+    integer / size / pointer parameters line up with the header's types."""
+    protos = _header_prototypes()
+    assert sorted(protos) == sorted(K.EXPORTS)
+    L = K.lib()
+    for name, params in protos.items():
+        argt = getattr(L, name).argtypes
+        if argt is None:
+            assert params == [], name
+            continue
+        assert len(argt) == len(params), (name, len(argt), len(params))
+        for a, decl in zip(argt, params):
+            if "*" in decl:
+                assert a is C.c_void_p or issubclass(a, C._Pointer) or a is C.c_char_p, (name, decl, a)
+            elif "int64_t" in decl:
+                assert a is C.c_int64, (name, decl, a)
+            elif "size_t" in decl:
+                assert a is C.c_size_t, (name, decl, a)
+            elif decl.split()[0] in ("int", "int32_t"):
+                assert a in (C.c_int, C.c_int32), (name, decl, a)
+
+
 def test_default_opts(K):
     o = K.opts()
     assert o.sched == K.SCHED_SELF and o.n_comm0 == -1 and o.order == K.ORDER_BAND
