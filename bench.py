@@ -445,6 +445,81 @@ def bench_rs_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=Tr
     return r
 
 
+# One GPU's per-direction NVLink 5 bandwidth: the emulated link of the
+# attention-shape measurements (kosmos_opts.link_gbs).
+LINK_GBS = 900
+
+
+def bench_attn(K, dev, steps, warmup, flush, stream, peak):
+    """Attention block of the layer: QKV all-gather + GEMM (8 ranks, X_r
+    1024x8192, W 8192x1280) and output-projection GEMM + reduce-scatter
+    (X_r 8192x1024, W_r 1024x8192), each with the copies free (one HBM) and
+    through an emulated 900 GB/s link; self-scheduling, fixed crew and
+    unfused."""
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    out = {"link_gbs": LINK_GBS}
+    w = WORKLOADS["ag_qkv_p8"]
+    inp = workload_inputs(w)
+    P, m, k, n = w.P, w.m, w.k, w.n
+    xs = [x.to(dev) for x in inp["x"]]
+    W = inp["w"].to(dev)
+    del inp
+    xg = torch.empty(P * m, k, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(P * m, n, dtype=torch.bfloat16, device=dev)
+
+    def t_ag(**kw):
+        o = K.opts(**kw)
+        wsb = K.workspace(K.OP_AG_GEMM, P, m, n, k, o=o, device=dev)
+        f = lambda: K.ag_gemm(xs, W, xg, y, wsb, o, stream=stream)
+        f()
+        K.check(wsb, "ag_gemm")
+        t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
+        K.check(wsb, "ag_gemm")
+        return w.flops() / (t * 1e-3) / 1e12
+
+    res = {}
+    for cap in (0, LINK_GBS):
+        tag = "link" if cap else "free"
+        fixed = {str(c): t_ag(sched=K.SCHED_FIXED, fixed_comm_ctas=c, link_gbs=cap) for c in (20, 40, 60)}
+        res[tag] = {"self": t_ag(link_gbs=cap), "fixed_best": max(fixed.values()), "fixed_sweep": fixed,
+                    "unfused": t_ag(sched=K.SCHED_UNFUSED, link_gbs=cap)}
+    out["ag_qkv_p8"] = {"tflops": res, "frac_of_peak_free": res["free"]["self"] / peak,
+                        "link_bound_us": (P - 1) * m * k * 2 / LINK_GBS / 1e3,
+                        "gemm_at_peak_us": w.flops() / (peak * 1e12) * 1e6}
+    del xs, W, xg, y
+    torch.cuda.empty_cache()
+    w = WORKLOADS["rs_oproj_p8"]
+    inp = workload_inputs(w)
+    P, m, k, n = w.P, w.m, w.k, w.n
+    xs = [x.to(dev) for x in inp["x"]]
+    ws_ = [x.to(dev) for x in inp["w"]]
+    del inp
+    ys = [torch.empty(m // P, n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+
+    def t_rs(**kw):
+        o = K.opts(**kw)
+        wsb = K.workspace(K.OP_GEMM_RS, P, m, n, k, o=o, device=dev)
+        f = lambda: K.gemm_rs(xs, ws_, ys, wsb, o, stream=stream)
+        f()
+        K.check(wsb, "gemm_rs")
+        t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
+        K.check(wsb, "gemm_rs")
+        return w.flops() / (t * 1e-3) / 1e12
+
+    res = {}
+    for cap in (0, LINK_GBS):
+        tag = "link" if cap else "free"
+        fixed = {str(c): t_rs(sched=K.SCHED_FIXED, fixed_comm_ctas=c, link_gbs=cap) for c in (1, 2, 4)}
+        res[tag] = {"band": t_rs(link_gbs=cap), "row": t_rs(order=K.ORDER_ROW, link_gbs=cap),
+                    "fixed_best": max(fixed.values()), "fixed_sweep_per_rank": fixed,
+                    "unfused": t_rs(sched=K.SCHED_UNFUSED, link_gbs=cap)}
+    out["rs_oproj_p8"] = {"tflops": res, "frac_of_peak_free": res["free"]["band"] / peak,
+                          "link_bound_us": (P - 1) * m * n * 2 / LINK_GBS / 1e3,
+                          "gemm_at_peak_us": w.flops() / (peak * 1e12) * 1e6}
+    return out
+
+
 def run_reference(args):
     ws, rank, local = dist_env()
     if ws > 1 and rank != 0:
@@ -489,6 +564,8 @@ def run_quick_other(args):
     elif args.workload == "moe":
         r = bench_moe(K, dev, args.steps, args.warmup, flush, stream, peaks["hbm_gbs"], peaks["bf16_tflops"],
                       experts=args.experts)
+    elif args.workload == "attn":
+        r = bench_attn(K, dev, args.steps, args.warmup, flush, stream, peaks["bf16_tflops"])
     elif args.workload == "moe_mxfp8":
         r = bench_moe(K, dev, args.steps, args.warmup, flush, stream, peaks["hbm_gbs"], 2 * peaks["bf16_tflops"],
                       experts=args.experts, mx=True)
@@ -627,6 +704,8 @@ def run_kosmos(args):
         also["moe_fwd_mxfp8"] = bench_moe(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"],
                                           2 * peak, mx=True)
         torch.cuda.empty_cache()
+        also["attention"] = bench_attn(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
+        torch.cuda.empty_cache()
 
     line = None
     if rank == 0:
@@ -655,7 +734,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kosmos", choices=["kosmos", "reference"])
     ap.add_argument("--ag-only", action="store_true", help="skip the GEMM+RS and MoE measurements")
-    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8", "rs_mxfp8", "moe_mxfp8"],
+    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8", "rs_mxfp8", "moe_mxfp8", "attn"],
                     help="with --quick: which fused operator to time")
     ap.add_argument("--experts", type=int, default=0, help="with --quick --workload moe: expert count (0 = 128)")
     ap.add_argument("--num-ctas", type=int, default=0,

@@ -48,7 +48,8 @@ class Opts(C.Structure):
     _fields_ = [("sched", C.c_int32), ("n_comm0", C.c_int32), ("fixed_comm_ctas", C.c_int32),
                 ("order", C.c_int32), ("num_ctas", C.c_int32), ("trace", C.c_int32),
                 ("cta_pair", C.c_int32), ("plain_launch", C.c_int32),
-                ("wait_limit_ns", C.c_uint64), ("inject", C.c_uint64), ("tail_split", C.c_int64)]
+                ("wait_limit_ns", C.c_uint64), ("inject", C.c_uint64), ("tail_split", C.c_int64),
+                ("link_gbs", C.c_int64)]
 
 
 class TraceRec(C.Structure):

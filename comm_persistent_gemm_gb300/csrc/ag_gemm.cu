@@ -39,6 +39,7 @@ struct AgParams {
     int pad;
     uint64_t wait_limit_ns;
     uint64_t inject;
+    int64_t link_gbs;  // emulated link for the remote pieces; 0 = uncapped
 };
 
 // Tile-rail entry -> what the engine runs: output columns [col0, col0 + BN)
@@ -85,6 +86,8 @@ __device__ __forceinline__ bool ag_claim_transfer(const AgParams &p, MoveEntry &
     e.flag = drop ? nullptr : &p.flags[shard * p.g.pieces + piece];
     e.ticket = static_cast<int32_t>(t);
     e.t_claim = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+    // a remote piece crosses the emulated link; the local shard's own copy does not
+    e.deadline = (p.link_gbs > 0 && shard != 0) ? link_reserve(p.ws, static_cast<uint64_t>(e.bytes[0]), p.link_gbs) : 0;
     return true;
 }
 
@@ -451,6 +454,7 @@ __global__ void __launch_bounds__(256) ag_gather_copy_kernel(const AgParams p) {
         const uint4 x = reinterpret_cast<const uint4 *>(p.x_src[s])[o];
         reinterpret_cast<uint4 *>(p.x_gath + s * shard_bytes)[o] = x;
     }
+    if (p.link_gbs > 0) ag_copy_link_pace(p.ws, per, total, p.link_gbs);
 }
 
 // ---------------------------------------------------------------- host launcher
@@ -500,6 +504,7 @@ kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     p.n_comm = L.n_comm;
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;
+    p.link_gbs = L.link_gbs;
 
     if (L.pair) p.n_comm = (L.n_comm + 1) / 2;  // mover pairs
     if (L.sched == KOSMOS_SCHED_UNFUSED) {

@@ -55,6 +55,7 @@ struct AgF8Params {
     int n_comm;
     uint64_t wait_limit_ns;
     uint64_t inject;
+    int64_t link_gbs;  // emulated link for the remote pieces; 0 = uncapped
 };
 
 struct F8Smem {
@@ -92,6 +93,9 @@ __device__ __forceinline__ bool f8_claim_transfer(const AgF8Params &p, MoveEntry
     e.flag = drop ? nullptr : &p.flags[shard * p.g.pieces + piece];
     e.ticket = static_cast<int32_t>(t);
     e.t_claim = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
+    e.deadline = (p.link_gbs > 0 && shard != 0)
+                     ? link_reserve(p.ws, static_cast<uint64_t>(e.bytes[0] + e.bytes[1]), p.link_gbs)
+                     : 0;
     return true;
 }
 
@@ -532,6 +536,7 @@ __global__ void __launch_bounds__(256) ag_f8_gather_copy_kernel(const AgF8Params
             reinterpret_cast<uint4 *>(p.sx_gath + s * sblk)[o - per] =
                 reinterpret_cast<const uint4 *>(p.sx_src[s])[o - per];
     }
+    if (p.link_gbs > 0) ag_copy_link_pace(p.ws, per + sper, total, p.link_gbs);
 }
 
 size_t ag_mxfp8_scale_bytes(int P, int64_t m, int64_t k) {
@@ -585,6 +590,7 @@ kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream) {
     p.n_comm = L.n_comm;
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;
+    p.link_gbs = L.link_gbs;
     if (L.pair) {
         p.g = ag_geom(L.P, L.m, L.k, L.n, PBM);
         p.n_comm = (L.n_comm + 1) / 2;  // mover pairs

@@ -67,6 +67,8 @@ struct WsHeader {
     int64_t fail_entry;    // ticket (or encoded entry) that failed, -1 none
     uint32_t tickets[40];  // rail counters
     uint32_t aux[4];
+    uint64_t link_t0;      // emulated link: globaltimer of the launch's first reservation (0 = none yet)
+    uint64_t link_bytes;   // emulated link: bytes reserved so far in this launch
 };
 static_assert(sizeof(WsHeader) <= 256, "header must fit its 256-byte slot");
 

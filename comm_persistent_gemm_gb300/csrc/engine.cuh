@@ -135,6 +135,7 @@ struct MoveEntry {
     uint32_t *flag;  // nullptr: no release (a transfer dropped by fault injection)
     int32_t ticket;
     int64_t t_claim;
+    uint64_t deadline = 0;  // emulated link: release no earlier than this globaltimer value (0 = none)
 };
 
 struct MoveChunk {
@@ -144,12 +145,46 @@ struct MoveChunk {
     int32_t ticket;
     uint32_t bytes;
     int32_t last;  // the entry's final chunk
+    uint64_t deadline;
 };
+
+// ---------------------------------------------------------------- emulated link
+// A pipe of gbs bytes per ns that never idles once the launch first uses it:
+// the transfer that brings the reserved total to B bytes is delivered at
+// t0 + B / gbs, t0 = the launch's first reservation.  While the link is
+// backlogged (the case the cap exists for) this is a first-come-first-served
+// server; when it would idle, later transfers catch up on the unused time.
+// One atomic add per transfer (a compare-and-swap server serialised the
+// reservations of 150 CTAs and cost more than the link itself).
+__device__ __forceinline__ uint64_t link_reserve(WsHeader *ws, uint64_t bytes, int64_t gbs) {
+    unsigned long long *t0p = reinterpret_cast<unsigned long long *>(&ws->link_t0);
+    unsigned long long t0 = *reinterpret_cast<volatile unsigned long long *>(t0p);
+    if (t0 == 0) {
+        const unsigned long long now = globaltimer();
+        const unsigned long long seen = atomicCAS(t0p, 0ull, now);
+        t0 = seen == 0 ? now : seen;
+    }
+    const unsigned long long c =
+        atomicAdd(reinterpret_cast<unsigned long long *>(&ws->link_bytes), static_cast<unsigned long long>(bytes));
+    return t0 + (c + bytes) / static_cast<uint64_t>(gbs);
+}
+
+// Spins until globaltimer reaches deadline (at most 4 s: the host bounds the
+// total link time of a call well below that).
+__device__ __forceinline__ void link_wait(uint64_t deadline) {
+    if (deadline == 0) return;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        const uint64_t now = globaltimer();
+        if (now >= deadline || now - t0 > PIPE_LIMIT_NS) return;
+    }
+}
 
 // Publishes a transfer whose stores have completed: order the async-proxy
 // writes before the generic release, then add one arrival to its flag.
 template <class Done>
 __device__ __forceinline__ void move_release(const MoveChunk &c, Done &done) {
+    link_wait(c.deadline);
     fence_proxy_async_global();
     __threadfence();
     if (c.flag) red_release_add_gpu(c.flag, 1u);
@@ -190,7 +225,7 @@ __device__ __noinline__ bool stream_mover(uint8_t *stages, uint64_t *cbar, uint3
                 have = true;
                 if (cur.bytes[0] + cur.bytes[1] == 0) {  // an empty part: nothing to copy
                     MoveChunk e;
-                    e.flag = cur.flag; e.ticket = cur.ticket; e.t_claim = cur.t_claim;
+                    e.flag = cur.flag; e.ticket = cur.ticket; e.t_claim = cur.t_claim; e.deadline = cur.deadline;
                     move_release(e, done);
                     have = false;
                     continue;
@@ -212,6 +247,7 @@ __device__ __noinline__ bool stream_mover(uint8_t *stages, uint64_t *cbar, uint3
             out.flag = cur.flag;
             out.ticket = cur.ticket;
             out.t_claim = cur.t_claim;
+            out.deadline = cur.deadline;
             off += nb;
             out.last = (off >= cur.bytes[seg]) && (seg == 1 || cur.bytes[1] == 0);
             if (out.last) have = false;
@@ -274,6 +310,24 @@ __device__ __noinline__ bool stream_mover(uint8_t *stages, uint64_t *cbar, uint3
     return true;
 }
 
+// Unfused all-gather copy kernels (grid-stride over 16-byte words, the first
+// `local` words being the local shard's): once a block has copied its words,
+// it reserves the link for the remote ones and waits until they would have
+// crossed it.
+__device__ __forceinline__ void ag_copy_link_pace(WsHeader *ws, int64_t local, int64_t total, int64_t gbs) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t mine = 0;  // remote words of this thread
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += stride)
+        mine += v >= local ? 1 : 0;
+    __shared__ unsigned long long s_words;
+    if (threadIdx.x == 0) s_words = 0;
+    __syncthreads();
+    atomicAdd(&s_words, static_cast<unsigned long long>(mine));
+    __syncthreads();
+    if (threadIdx.x == 0 && s_words > 0) link_wait(link_reserve(ws, s_words * 16ull, gbs));
+    __syncthreads();
+}
+
 // ---------------------------------------------------------------- setup / teardown
 __device__ __forceinline__ void engine_setup(const Smem &sm, int warp) {
     if (threadIdx.x == 0) {
@@ -311,6 +365,8 @@ __device__ __forceinline__ void engine_finish(WsHeader *ws, uint32_t epoch, int 
         __threadfence();
         volatile uint32_t *t = ws->tickets;
         for (int i = 0; i < n_tickets; ++i) t[i] = 0u;
+        *reinterpret_cast<volatile uint64_t *>(&ws->link_t0) = 0ull;
+        *reinterpret_cast<volatile uint64_t *>(&ws->link_bytes) = 0ull;
         *reinterpret_cast<volatile uint32_t *>(&ws->done_ctas) = 0u;
         __threadfence();
         *reinterpret_cast<volatile uint32_t *>(&ws->epoch) = epoch + 1u;

@@ -47,7 +47,17 @@ struct RsParams {
     int pad;
     uint64_t wait_limit_ns;
     uint64_t inject;
+    int64_t link_gbs;               // emulated link for other ranks' partial tiles; 0 = uncapped
 };
+
+// Bytes of partial tile (band, tcol) rows [r0, r0 + nr) that exist.
+__device__ __forceinline__ uint64_t rs_tile_bytes(const RsParams &p, int64_t r0, int64_t nr, int tcol) {
+    int64_t rows = p.g.mc - r0;
+    rows = rows < 0 ? 0 : (rows > nr ? nr : rows);
+    int64_t cols = p.g.n - static_cast<int64_t>(tcol) * BN;
+    cols = cols > BN ? BN : cols;
+    return static_cast<uint64_t>(rows * cols * 2);
+}
 
 __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
     const int cta = blockIdx.x;
@@ -112,6 +122,10 @@ __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
                               (static_cast<int64_t>(1) << 40) | (static_cast<int64_t>(rank) << 32) | t))
                 break;
             st_relaxed_gpu(ctr, 0u);  // sole consumer: return the counter to zero for the next call
+        } else if (p.link_gbs > 0 && P > 1) {
+            // unfused: the other ranks' partials of this tile cross the link now
+            link_wait(link_reserve(p.ws, (P - 1) * rs_tile_bytes(p, static_cast<int64_t>(band) * BM, BM, tcol),
+                                   p.link_gbs));
         }
         int slot = -1;
         if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
@@ -194,8 +208,12 @@ __device__ __forceinline__ void rs_epilogue(const RsParams &p, const Smem &sm, u
                 __threadfence();
                 named_bar_sync(1, NUM_EPI_THREADS);
                 const bool drop = (p.inject & KOSMOS_INJECT_DROP_PARTIAL) && static_cast<int>(p.inject >> 32) == rank;
-                if (et == 0 && !drop)
+                if (et == 0 && !drop) {
+                    if (p.link_gbs > 0 && rank != chunk)  // another rank's partial crosses the link
+                        link_wait(link_reserve(p.ws, rs_tile_bytes(p, static_cast<int64_t>(band) * BM, BM, tcol),
+                                               p.link_gbs));
                     red_release_add_gpu(&p.arrive[(static_cast<int64_t>(chunk) * p.g.bands + band) * p.g.tiles_n + tcol], 1u);
+                }
             }
             if (e.slot >= 0 && et == 0) {
                 if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
@@ -433,6 +451,9 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
                                   (static_cast<int64_t>(1) << 40) | (static_cast<int64_t>(rank) << 32) | t))
                     break;
                 st_relaxed_gpu(ctr, 0u);
+            } else if (p.link_gbs > 0 && P > 1) {
+                link_wait(link_reserve(p.ws, (P - 1) * rs_tile_bytes(p, static_cast<int64_t>(band) * PBM, PBM, tcol),
+                                       p.link_gbs));
             }
             int slot = -1;
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
@@ -510,8 +531,13 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
             __threadfence();
             named_bar_sync(1, NUM_EPI_THREADS);
             const bool drop = (p.inject & KOSMOS_INJECT_DROP_PARTIAL) && static_cast<int>(p.inject >> 32) == rank;
-            if (et == 0 && !drop)
+            if (et == 0 && !drop) {
+                if (p.link_gbs > 0 && rank != chunk)  // this CTA's half of another rank's partial
+                    link_wait(link_reserve(
+                        p.ws, rs_tile_bytes(p, static_cast<int64_t>(band) * PBM + crank * HBM_ROWS, HBM_ROWS, tcol),
+                        p.link_gbs));
                 red_release_add_gpu(&p.arrive[(static_cast<int64_t>(chunk) * p.g.bands + band) * p.g.tiles_n + tcol], 1u);
+            }
         }
         if (leader && e.slot >= 0 && et == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
@@ -705,6 +731,7 @@ kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
     p.order = L.order;
     p.wait_limit_ns = L.wait_limit_ns;
     p.inject = L.inject;
+    p.link_gbs = L.link_gbs;
     const void *fn = mx       ? reinterpret_cast<const void *>(&gemm_rs_mx_pair_kernel)
                      : L.pair ? reinterpret_cast<const void *>(&gemm_rs_pair_kernel)
                               : reinterpret_cast<const void *>(&gemm_rs_kernel);

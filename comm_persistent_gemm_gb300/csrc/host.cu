@@ -156,6 +156,14 @@ int device_sms() {
 
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The emulated link: 0 (off) or 1..1e6 GB/s, and the call's whole link
+// traffic must cross it within half the wait bound (every wait stays bounded).
+static bool link_ok(const kosmos_opts &o, uint64_t link_bytes) {
+    if (o.link_gbs == 0) return true;
+    if (o.link_gbs < 1 || o.link_gbs > 1000000) return false;
+    return link_bytes / static_cast<uint64_t>(o.link_gbs) < o.wait_limit_ns / 2;
+}
+
 kosmos_opts resolve_opts(const kosmos_opts *o) {
     kosmos_opts r;
     kosmos_default_opts(&r);
@@ -257,6 +265,7 @@ void kosmos_default_opts(kosmos_opts *opts) {
     opts->cta_pair = -1;
     opts->plain_launch = 0;
     opts->tail_split = 0;
+    opts->link_gbs = 0;
     opts->wait_limit_ns = 0;
     opts->inject = 0;
 }
@@ -306,6 +315,9 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
     const kosmos_opts o = resolve_opts(opts);
     if (o.sched < KOSMOS_SCHED_SELF || o.sched > KOSMOS_SCHED_UNFUSED) return KOSMOS_ERR_INVALID_ARG;
+    if (!link_ok(o, static_cast<uint64_t>(P - 1) * static_cast<uint64_t>(m_per_shard) * static_cast<uint64_t>(k) *
+                        (dtype == KOSMOS_BF16 ? 2u : 1u)))
+        return KOSMOS_ERR_INVALID_ARG;
     if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_AG_GEMM, P, m_per_shard, n, k, dtype, &o))
         return KOSMOS_ERR_WORKSPACE;
     AgPlan pl;
@@ -326,6 +338,7 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     L.n_slots = ag_split_slots(P, m_per_shard, n, dtype, o);
     L.trace = o.trace; L.grid = pl.grid; L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
     L.plain_launch = o.plain_launch;
+    L.link_gbs = o.link_gbs;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == KOSMOS_BF16 ? launch_ag_bf16(L, s) : launch_ag_mxfp8(L, s);
 }
@@ -365,6 +378,8 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *x_s
     const kosmos_opts o = resolve_opts(opts);
     if (o.sched < KOSMOS_SCHED_SELF || o.sched > KOSMOS_SCHED_UNFUSED) return KOSMOS_ERR_INVALID_ARG;
     if (o.order != KOSMOS_ORDER_BAND && o.order != KOSMOS_ORDER_ROW) return KOSMOS_ERR_INVALID_ARG;
+    if (!link_ok(o, static_cast<uint64_t>(P - 1) * static_cast<uint64_t>(m) * static_cast<uint64_t>(n) * 2u))
+        return KOSMOS_ERR_INVALID_ARG;
     if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_GEMM_RS, P, m, n, k_per_rank, dtype, &o))
         return KOSMOS_ERR_WORKSPACE;
     int grid = grid_for(o);
@@ -411,6 +426,7 @@ kosmos_status kosmos_gemm_rs(const void *const *x_shards, const void *const *x_s
         L.n_comm = n_red;
     }
     L.order = o.order; L.trace = o.trace; L.grid = grid; L.plain_launch = o.plain_launch;
+    L.link_gbs = o.link_gbs;
     L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
     return launch_rs_bf16(L, static_cast<cudaStream_t>(stream));
 }
@@ -470,6 +486,7 @@ kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, 
     if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
     const kosmos_opts o = resolve_opts(opts);
     if (o.sched != KOSMOS_SCHED_SELF) return KOSMOS_ERR_UNSUPPORTED;
+    if (o.link_gbs != 0) return KOSMOS_ERR_UNSUPPORTED;
     if (mx && (o.inject & KOSMOS_INJECT_IDENTITY_EXPERTS)) return KOSMOS_ERR_UNSUPPORTED;
     if (ws_bytes < kosmos_moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, dtype, &o))
         return KOSMOS_ERR_WORKSPACE;

@@ -31,6 +31,7 @@ struct AgLaunch {
     int n_slots;      // K-split slots in the workspace (>= n_split)
     uint64_t wait_limit_ns;
     uint64_t inject;
+    int64_t link_gbs;
 };
 
 struct RsLaunch {
@@ -52,6 +53,7 @@ struct RsLaunch {
     int plain_launch;
     uint64_t wait_limit_ns;
     uint64_t inject;
+    int64_t link_gbs;
 };
 
 struct MoeLaunch {

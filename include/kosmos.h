@@ -117,6 +117,12 @@ typedef struct kosmos_opts {
                                  workspace); 0 = none; -1 = one wave (the number of tile engines,
                                  i.e. SM pairs or SMs, that build).  At most 256; needs k >= 128.
                                  The workspace holds 256 KB per split tile. */
+    int64_t link_gbs;         /* emulated link bandwidth in GB/s (1e9 bytes/s) for the bytes that would
+                                 cross GPU-to-GPU links (all-gather: remote shard pieces; GEMM+RS: the
+                                 partial tiles of other ranks).  One link for the emulated traffic: a
+                                 transfer is released no earlier than a pipe of this rate, busy from
+                                 the launch's first link transfer on, would have delivered it.
+                                 0 = uncapped; else 1..1000000.  MoE: must be 0. */
 } kosmos_opts;
 
 /* Fills *opts with the defaults (SELF, band order, all SMs, no trace). */

@@ -79,6 +79,16 @@ WORKLOADS: Dict[str, Workload] = {
     "rs_mxfp8_p8": Workload("rs_mxfp8_p8", "rs", seed=5, P=8, m=8192, k=3584, n=8192, dtype="mxfp8",
                             var_x=1.0, var_w=1.0 / 28672,
                             note="GEMM+RS MXFP8 (E4M3 + E8M0 per 32 K), shapes of rs_bf16_p8"),
+    # attention block of the same layer (hidden 8192, 64 query heads and 8
+    # key/value heads of 128): QKV projection as an all-gather + GEMM
+    # (8192 + 2 * 1024 columns over 8 ranks = 1280 each) and the output
+    # projection as a GEMM + reduce-scatter (8192 / 8 = 1024 K per rank)
+    "ag_qkv_p8": Workload("ag_qkv_p8", "ag", seed=6, P=8, m=1024, k=8192, n=1280,
+                          var_x=1.0, var_w=1.0 / 8192,
+                          note="QKV AG-GEMM BF16, P=8, X_r 1024x8192, W_qkv 8192x1280 (rank 0's column shard)"),
+    "rs_oproj_p8": Workload("rs_oproj_p8", "rs", seed=7, P=8, m=8192, k=1024, n=8192,
+                            var_x=1.0, var_w=1.0 / 8192,
+                            note="out-proj GEMM+RS BF16, P=8, X_r 8192x1024, W_r 1024x8192, chunks 1024x8192"),
     "moe_fwd_p8": Workload("moe_fwd_p8", "moe", seed=4, P=8, T=2048, H=4096, E=128, topk=8, I=1536,
                            var_x=1.0, var_w=1.0,
                            note="MoE forward, 2048 tokens, hidden 4096, 128 experts top-8, 8 EP ranks x 16, I=1536"),

@@ -104,6 +104,15 @@ def test_host_validation_rejects_bad_args(K):
     assert lib.kosmos_gemm_rs(xs, None, xs, None, P, 256, 128, 64, 1, ys, base, 1 << 20, None, None) == 1
     # quantiser: blocked extent not a multiple of 32
     assert lib.kosmos_mxfp8_quantize(base, 4, 96, 1, base, base, None) == 1
+    # emulated link: out of range, or more link time than half the wait bound
+    for gbs in (-1, 2000000):
+        o = K.opts(link_gbs=gbs)
+        assert lib.kosmos_ag_gemm(xs, None, P, 64, 128, 128, base, None, 0, base, base, base, 1 << 20,
+                                  C.byref(o), None) == 1
+        assert lib.kosmos_gemm_rs(xs, None, xs, None, P, 256, 64, 64, 0, ys, base, 1 << 20, C.byref(o), None) == 1
+    o = K.opts(link_gbs=1, wait_limit_ns=1000)  # 16 KB over 1 GB/s = 16 us > 0.5 us
+    assert lib.kosmos_ag_gemm(xs, None, P, 64, 128, 128, base, None, 0, base, base, base, 1 << 20,
+                              C.byref(o), None) == 1
 
 
 @pytest.mark.parametrize("split", [0, 3, 76, 10**6])
