@@ -71,6 +71,15 @@ def lib():
         L.orc_moe_experts_mxfp8.restype = C.c_int
         L.orc_moe_experts_mxfp8.argtypes = [i64, i64, C.c_int, C.c_int, i64, C.c_int, P, P, P, P,
                                             P, P, P, P, P, P, P, i64, P]
+        L.orc_moe_bwd_tokens.restype = C.c_int
+        L.orc_moe_bwd_tokens.argtypes = [i64, i64, C.c_int, C.c_int, i64, C.c_int, P, P, P, P, P, P, P, P, P,
+                                         P, i64, P, P, P]
+        L.orc_moe_bwd_experts.restype = C.c_int
+        L.orc_moe_bwd_experts.argtypes = [i64, i64, C.c_int, C.c_int, i64, C.c_int, P, P, P, P, P, P, P, P,
+                                          C.c_int, P, P, P]
+        L.orc_moe_bwd_router_weight.restype = C.c_int
+        L.orc_moe_bwd_router_weight.argtypes = [i64, i64, C.c_int, C.c_int, i64, C.c_int, P, P, P, P, P, P,
+                                                P, P, P, P]
         L.orc_moe_experts.restype = C.c_int
         L.orc_moe_experts.argtypes = [i64, i64, C.c_int, C.c_int, i64, C.c_int, P, P, P,
                                       P, P, P, C.c_int, P, i64, P]
@@ -322,6 +331,90 @@ def moe_experts_mxfp8(xq: np.ndarray, xs: np.ndarray, idx: np.ndarray, gate: np.
     if rc:
         raise ValueError("orc_moe_experts_mxfp8 failed")
     return out
+
+
+def moe_bwd_tokens(x_bits, wr_bits, route, dout_bits, wg_bits, wu_bits, wd_bits, tokens=None):
+    """dx (expert and router paths), dgate and dl of the selected tokens
+    (all when tokens is None).  route: orc.moe_route's output."""
+    x = _u16(x_bits)
+    T, H = x.shape
+    wr = _u16(wr_bits)
+    E = wr.shape[1]
+    idx = np.ascontiguousarray(route["idx"], dtype=np.int32)
+    K = idx.shape[1]
+    gate = np.ascontiguousarray(route["gate"], dtype=np.float64)
+    logits = np.ascontiguousarray(route["logits"], dtype=np.float64)
+    dout = _u16(dout_bits)
+    wg = [_u16(a) for a in wg_bits]
+    wu = [_u16(a) for a in wu_bits]
+    wd = [_u16(a) for a in wd_bits]
+    P = len(wg)
+    I = wg[0].shape[2]
+    ntok = T if tokens is None else len(tokens)
+    tp = None
+    if tokens is not None:
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        tp = _ptr(tokens)
+    dx = np.empty((ntok, H))
+    dgate = np.empty((ntok, K))
+    dl = np.empty((ntok, E))
+    rc = lib().orc_moe_bwd_tokens(T, H, E, K, I, P, _ptr(x), _ptr(wr), _ptr(logits), _ptr(idx), _ptr(gate),
+                                  _ptr(dout), _ptr_array(wg), _ptr_array(wu), _ptr_array(wd), tp, ntok,
+                                  _ptr(dx), _ptr(dgate), _ptr(dl))
+    if rc:
+        raise ValueError("orc_moe_bwd_tokens failed")
+    return {"dx": dx, "dgate": dgate, "dl": dl}
+
+
+def moe_bwd_experts(x_bits, route, dout_bits, wg_bits, wu_bits, wd_bits, experts):
+    """(dWg, dWu, dWd) of the selected experts: [n, H, I], [n, H, I], [n, I, H]."""
+    x = _u16(x_bits)
+    T, H = x.shape
+    idx = np.ascontiguousarray(route["idx"], dtype=np.int32)
+    K = idx.shape[1]
+    gate = np.ascontiguousarray(route["gate"], dtype=np.float64)
+    dout = _u16(dout_bits)
+    wg = [_u16(a) for a in wg_bits]
+    wu = [_u16(a) for a in wu_bits]
+    wd = [_u16(a) for a in wd_bits]
+    P = len(wg)
+    Eq, _, I = wg[0].shape
+    ex = np.ascontiguousarray(experts, dtype=np.int32)
+    n = len(ex)
+    dwg = np.empty((n, H, I))
+    dwu = np.empty((n, H, I))
+    dwd = np.empty((n, I, H))
+    rc = lib().orc_moe_bwd_experts(T, H, Eq * P, K, I, P, _ptr(x), _ptr(idx), _ptr(gate), _ptr(dout),
+                                   _ptr_array(wg), _ptr_array(wu), _ptr_array(wd), _ptr(ex), n,
+                                   _ptr(dwg), _ptr(dwu), _ptr(dwd))
+    if rc:
+        raise ValueError("orc_moe_bwd_experts failed")
+    return dwg, dwu, dwd
+
+
+def moe_bwd_router_weight(x_bits, wr_bits, route, dout_bits, wg_bits, wu_bits, wd_bits):
+    """dWr [H, E] over every token."""
+    x = _u16(x_bits)
+    T, H = x.shape
+    wr = _u16(wr_bits)
+    E = wr.shape[1]
+    idx = np.ascontiguousarray(route["idx"], dtype=np.int32)
+    K = idx.shape[1]
+    gate = np.ascontiguousarray(route["gate"], dtype=np.float64)
+    logits = np.ascontiguousarray(route["logits"], dtype=np.float64)
+    dout = _u16(dout_bits)
+    wg = [_u16(a) for a in wg_bits]
+    wu = [_u16(a) for a in wu_bits]
+    wd = [_u16(a) for a in wd_bits]
+    P = len(wg)
+    I = wg[0].shape[2]
+    dwr = np.empty((H, E))
+    rc = lib().orc_moe_bwd_router_weight(T, H, E, K, I, P, _ptr(x), _ptr(wr), _ptr(logits), _ptr(idx),
+                                         _ptr(gate), _ptr(dout), _ptr_array(wg), _ptr_array(wu), _ptr_array(wd),
+                                         _ptr(dwr))
+    if rc:
+        raise ValueError("orc_moe_bwd_router_weight failed")
+    return dwr
 
 
 # -- rails ------------------------------------------------------------------

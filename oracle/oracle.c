@@ -561,6 +561,225 @@ ORC_EXPORT int orc_moe_experts_mxfp8(int64_t T, int64_t H, int E, int K, int64_t
 }
 
 /* ------------------------------------------------------------------------ */
+/* MoE expert layer (backward)                                               */
+/* ------------------------------------------------------------------------ */
+/* [abstract: "one launch per direction"; reading: the gradients of the
+ * forward layer above with the routing (top-K indices) held fixed].  Forward:
+ *   l_t = x_t Wr, p_t = softmax(l_t), S_t = sum_{k<K} p_t[e_k],
+ *   gate_{t,k} = p_t[e_k] / S_t, g = x_t Wg[e], u = x_t Wu[e],
+ *   h = silu(g) * u, y_{t,k} = h Wd[e], out_t = sum_k gate_{t,k} y_{t,k}.
+ * Given dout_t = dL/dout_t:
+ *   dgate_{t,k} = <dout_t, y_{t,k}>,  dy_{t,k} = gate_{t,k} dout_t,
+ *   dh = dy Wd[e]^T,  dg = dh * u * silu'(g),  du = dh * silu(g),
+ *   silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + exp(-g)),
+ *   dp_j = (dgate_{k(j)} - sum_k dgate_k gate_k) / S for j = e_{k(j)} in the
+ *   top-K set, 0 elsewhere;  dl = p * (dp - <p, dp>),
+ *   dx_t = sum_k (dg Wg[e]^T + du Wu[e]^T) + dl_t Wr^T,
+ *   dWg[e] = sum over slots routed to e of x_t^T dg, dWu[e] likewise with du,
+ *   dWd[e] = sum of h^T dy,  dWr = sum_t x_t^T dl_t.
+ * All in fp64 from the bf16 inputs; logits from orc_moe_route (fp64). */
+
+typedef struct {
+    int64_t H, I;
+    const uint16_t *Wg, *Wu, *Wd;
+} orc_expert_w;
+
+/* One slot: forward g, u, h, y and backward dg, du for a token row xt
+ * (fp64) and upstream dy_row = gate * dout (fp64). */
+static void orc_slot_fwd_bwd(const orc_expert_w *w, const double *xt, const double *dyv, double *g, double *u,
+                             double *hh, double *y, double *dh, double *dg, double *du) {
+    int64_t H = w->H, I = w->I;
+    for (int64_t i = 0; i < I; i++) { g[i] = 0.0; u[i] = 0.0; }
+    for (int64_t h = 0; h < H; h++) {
+        double a = xt[h];
+        for (int64_t i = 0; i < I; i++) {
+            g[i] += a * orc_bf16_to_f64(w->Wg[h * I + i]);
+            u[i] += a * orc_bf16_to_f64(w->Wu[h * I + i]);
+        }
+    }
+    for (int64_t i = 0; i < I; i++) hh[i] = orc_silu(g[i]) * u[i];
+    if (y) {
+        for (int64_t c = 0; c < H; c++) y[c] = 0.0;
+        for (int64_t i = 0; i < I; i++)
+            for (int64_t c = 0; c < H; c++) y[c] += hh[i] * orc_bf16_to_f64(w->Wd[i * H + c]);
+    }
+    for (int64_t i = 0; i < I; i++) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < H; c++) acc += dyv[c] * orc_bf16_to_f64(w->Wd[i * H + c]);
+        dh[i] = acc;
+        double sg = 1.0 / (1.0 + exp(-g[i]));
+        dg[i] = dh[i] * u[i] * sg * (1.0 + g[i] * (1.0 - sg));
+        du[i] = dh[i] * orc_silu(g[i]);
+    }
+}
+
+static orc_expert_w orc_expert(int e, int Eq, int64_t H, int64_t I, const uint16_t *const *wg,
+                               const uint16_t *const *wu, const uint16_t *const *wd) {
+    orc_expert_w w;
+    int q = e / Eq, le = e % Eq;
+    w.H = H; w.I = I;
+    w.Wg = wg[q] + (int64_t)le * H * I;
+    w.Wu = wu[q] + (int64_t)le * H * I;
+    w.Wd = wd[q] + (int64_t)le * I * H;
+    return w;
+}
+
+/* Router backward of one token from its dgate: dl[E] (see above). */
+static void orc_router_bwd(int E, int K, const double *l, const int32_t *idx, const double *dgate, double *dl) {
+    double mx = l[0];
+    for (int e = 1; e < E; e++) if (l[e] > mx) mx = l[e];
+    double z = 0.0;
+    for (int e = 0; e < E; e++) { dl[e] = exp(l[e] - mx); z += dl[e]; }
+    for (int e = 0; e < E; e++) dl[e] /= z;  /* p */
+    double S = 0.0;
+    for (int k = 0; k < K; k++) S += dl[idx[k]];
+    double sdg = 0.0;
+    for (int k = 0; k < K; k++) sdg += dgate[k] * dl[idx[k]] / S;
+    /* dp is nonzero on the top-K set only */
+    double pdp = 0.0;
+    for (int k = 0; k < K; k++) pdp += dl[idx[k]] * (dgate[k] - sdg) / S;
+    double *p = dl;  /* overwritten in place below: keep dp of the top-K in a small table */
+    double dpk[64];
+    for (int k = 0; k < K; k++) dpk[k] = (dgate[k] - sdg) / S;
+    for (int e = 0; e < E; e++) {
+        double dp = 0.0;
+        for (int k = 0; k < K; k++) if (idx[k] == e) dp = dpk[k];
+        p[e] = p[e] * (dp - pdp);
+    }
+}
+
+/* dx of selected tokens (the expert and router paths), with dgate [ntok, K]
+ * and dl [ntok, E] of those tokens.  logits: [T, E] fp64 from orc_moe_route. */
+ORC_EXPORT int orc_moe_bwd_tokens(int64_t T, int64_t H, int E, int K, int64_t I, int P,
+                                  const uint16_t *x, const uint16_t *wr, const double *logits,
+                                  const int32_t *idx, const double *gate, const uint16_t *dout,
+                                  const uint16_t *const *wg, const uint16_t *const *wu,
+                                  const uint16_t *const *wd, const int64_t *tokens, int64_t ntok,
+                                  double *dx, double *dgate_out, double *dl_out) {
+    if (E % P || K > 64) return 1;
+    int Eq = E / P;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dv = (double *)malloc(sizeof(double) * (size_t)H);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *u = (double *)malloc(sizeof(double) * (size_t)I);
+        double *hh = (double *)malloc(sizeof(double) * (size_t)I);
+        double *dh = (double *)malloc(sizeof(double) * (size_t)I);
+        double *dg = (double *)malloc(sizeof(double) * (size_t)I);
+        double *du = (double *)malloc(sizeof(double) * (size_t)I);
+        double *dl = (double *)malloc(sizeof(double) * (size_t)E);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t s = 0; s < ntok; s++) {
+            int64_t t = tokens ? tokens[s] : s;
+            if (t < 0 || t >= T) { bad = 1; continue; }
+            double *o = dx + s * H;
+            double dgt[64];
+            for (int64_t c = 0; c < H; c++) { xt[c] = orc_bf16_to_f64(x[t * H + c]); o[c] = 0.0; }
+            for (int k = 0; k < K; k++) {
+                int e = idx[t * K + k];
+                orc_expert_w w = orc_expert(e, Eq, H, I, wg, wu, wd);
+                double gk = gate[t * K + k];
+                for (int64_t c = 0; c < H; c++) dv[c] = gk * orc_bf16_to_f64(dout[t * H + c]);
+                orc_slot_fwd_bwd(&w, xt, dv, g, u, hh, y, dh, dg, du);
+                double acc = 0.0;
+                for (int64_t c = 0; c < H; c++) acc += orc_bf16_to_f64(dout[t * H + c]) * y[c];
+                dgt[k] = acc;
+                for (int64_t c = 0; c < H; c++) {
+                    double a = 0.0;
+                    for (int64_t i = 0; i < I; i++)
+                        a += dg[i] * orc_bf16_to_f64(w.Wg[c * I + i]) + du[i] * orc_bf16_to_f64(w.Wu[c * I + i]);
+                    o[c] += a;
+                }
+            }
+            orc_router_bwd(E, K, logits + t * E, idx + t * K, dgt, dl);
+            for (int64_t c = 0; c < H; c++) {
+                double a = 0.0;
+                for (int e = 0; e < E; e++) a += dl[e] * orc_bf16_to_f64(wr[c * E + e]);
+                o[c] += a;
+            }
+            if (dgate_out) for (int k = 0; k < K; k++) dgate_out[s * K + k] = dgt[k];
+            if (dl_out) for (int e = 0; e < E; e++) dl_out[s * E + e] = dl[e];
+        }
+        free(xt); free(dv); free(y); free(g); free(u); free(hh); free(dh); free(dg); free(du); free(dl);
+    }
+    return bad ? 1 : 0;
+}
+
+/* Weight gradients of selected experts: dwg, dwu [nexp, H, I], dwd [nexp, I, H];
+ * sums over the slots routed to each expert in (token, k) order. */
+ORC_EXPORT int orc_moe_bwd_experts(int64_t T, int64_t H, int E, int K, int64_t I, int P,
+                                   const uint16_t *x, const int32_t *idx, const double *gate,
+                                   const uint16_t *dout, const uint16_t *const *wg,
+                                   const uint16_t *const *wu, const uint16_t *const *wd,
+                                   const int32_t *experts, int nexp, double *dwg, double *dwu, double *dwd) {
+    if (E % P) return 1;
+    int Eq = E / P;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dv = (double *)malloc(sizeof(double) * (size_t)H);
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *u = (double *)malloc(sizeof(double) * (size_t)I);
+        double *hh = (double *)malloc(sizeof(double) * (size_t)I);
+        double *dh = (double *)malloc(sizeof(double) * (size_t)I);
+        double *dg = (double *)malloc(sizeof(double) * (size_t)I);
+        double *du = (double *)malloc(sizeof(double) * (size_t)I);
+#pragma omp for schedule(dynamic, 1)
+        for (int n = 0; n < nexp; n++) {
+            int e = experts[n];
+            if (e < 0 || e >= E) { bad = 1; continue; }
+            orc_expert_w w = orc_expert(e, Eq, H, I, wg, wu, wd);
+            double *Dg = dwg + (int64_t)n * H * I, *Du = dwu + (int64_t)n * H * I, *Dd = dwd + (int64_t)n * I * H;
+            for (int64_t j = 0; j < H * I; j++) { Dg[j] = 0.0; Du[j] = 0.0; Dd[j] = 0.0; }
+            for (int64_t t = 0; t < T; t++)
+                for (int k = 0; k < K; k++) {
+                    if (idx[t * K + k] != e) continue;
+                    for (int64_t c = 0; c < H; c++) {
+                        xt[c] = orc_bf16_to_f64(x[t * H + c]);
+                        dv[c] = gate[t * K + k] * orc_bf16_to_f64(dout[t * H + c]);
+                    }
+                    orc_slot_fwd_bwd(&w, xt, dv, g, u, hh, NULL, dh, dg, du);
+                    for (int64_t c = 0; c < H; c++)
+                        for (int64_t i = 0; i < I; i++) {
+                            Dg[c * I + i] += xt[c] * dg[i];
+                            Du[c * I + i] += xt[c] * du[i];
+                        }
+                    for (int64_t i = 0; i < I; i++)
+                        for (int64_t c = 0; c < H; c++) Dd[i * H + c] += hh[i] * dv[c];
+                }
+        }
+        free(xt); free(dv); free(g); free(u); free(hh); free(dh); free(dg); free(du);
+    }
+    return bad ? 1 : 0;
+}
+
+/* dWr [H, E] = sum over all tokens of x_t^T dl_t (token order). */
+ORC_EXPORT int orc_moe_bwd_router_weight(int64_t T, int64_t H, int E, int K, int64_t I, int P,
+                                         const uint16_t *x, const uint16_t *wr, const double *logits,
+                                         const int32_t *idx, const double *gate, const uint16_t *dout,
+                                         const uint16_t *const *wg, const uint16_t *const *wu,
+                                         const uint16_t *const *wd, double *dwr) {
+    double *dx = (double *)malloc(sizeof(double) * (size_t)(T * H));
+    double *dl = (double *)malloc(sizeof(double) * (size_t)(T * E));
+    if (!dx || !dl) { free(dx); free(dl); return 2; }
+    int rc = orc_moe_bwd_tokens(T, H, E, K, I, P, x, wr, logits, idx, gate, dout, wg, wu, wd, NULL, T, dx, NULL, dl);
+    if (!rc) {
+        for (int64_t j = 0; j < H * E; j++) dwr[j] = 0.0;
+        for (int64_t t = 0; t < T; t++)
+            for (int64_t c = 0; c < H; c++) {
+                double a = orc_bf16_to_f64(x[t * H + c]);
+                for (int e = 0; e < E; e++) dwr[c * E + e] += a * dl[t * E + e];
+            }
+    }
+    free(dx); free(dl);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Work rails ("the order of the rail is the schedule")                      */
 /* ------------------------------------------------------------------------ */
 /* [explainer, "Role switching only works"]: data is produced in the order its

@@ -236,3 +236,79 @@ def test_mxfp8_experts_close_to_bf16_layer_on_dequantised_inputs(orc):
     ref = orc.moe_experts(xb, r["idx"], r["gate"], wb[0], wb[1], wb[2], E=E)
     err = np.abs(mx - ref).max() / np.abs(ref).max()
     assert 1e-4 < err < 0.06, err  # h rounding is visible, and bounded
+
+
+# -- backward --------------------------------------------------------------
+
+def _torch_layer(x, wr, wg, wu, wd, idx, K):
+    """The forward layer restated in torch fp64 with the top-K indices held
+    fixed (the routing decision is not differentiated)."""
+    logits = x @ wr
+    p = torch.softmax(logits, dim=1)
+    sel = torch.gather(p, 1, idx)
+    gate = sel / sel.sum(dim=1, keepdim=True)
+    out = torch.zeros_like(x)
+    for k in range(K):
+        e = idx[:, k]
+        g = torch.einsum("th,thi->ti", x, wg[e])
+        u = torch.einsum("th,thi->ti", x, wu[e])
+        y = torch.einsum("ti,tih->th", torch.nn.functional.silu(g) * u, wd[e])
+        out = out + gate[:, k:k + 1] * y
+    return out
+
+
+def _bwd_case(T=12, H=32, E=8, I=16, K=3, P=2, seed=51):
+    inp = moe_inputs(T=T, H=H, E=E, I=I, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    dout = (torch.randn(T, H, generator=g)).to(torch.bfloat16)
+    return inp, dout, K, P
+
+
+def test_moe_bwd_vs_torch_autograd(orc):
+    inp, dout, K, P = _bwd_case()
+    E = inp["w_router"].shape[1]
+    x = bf16_bits(inp["x"])
+    r = orc.moe_route(x, bf16_bits(inp["w_router"]), K)
+    wg, wu, wd = (_split_ranks(inp[n], P) for n in ("w_gate", "w_up", "w_down"))
+    tok = orc.moe_bwd_tokens(x, bf16_bits(inp["w_router"]), r, bf16_bits(dout), wg, wu, wd)
+    dwg, dwu, dwd = orc.moe_bwd_experts(x, r, bf16_bits(dout), wg, wu, wd, np.arange(E))
+    dwr = orc.moe_bwd_router_weight(x, bf16_bits(inp["w_router"]), r, bf16_bits(dout), wg, wu, wd)
+    leaves = {n: inp[n].double().clone().requires_grad_(True) for n in ("x", "w_router", "w_gate", "w_up", "w_down")}
+    idx = torch.from_numpy(r["idx"].astype(np.int64))
+    out = _torch_layer(leaves["x"], leaves["w_router"], leaves["w_gate"], leaves["w_up"], leaves["w_down"], idx, K)
+    (out * dout.double()).sum().backward()
+    np.testing.assert_allclose(tok["dx"], leaves["x"].grad.numpy(), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(dwr, leaves["w_router"].grad.numpy(), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(dwg, leaves["w_gate"].grad.numpy(), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(dwu, leaves["w_up"].grad.numpy(), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(dwd, leaves["w_down"].grad.numpy(), rtol=1e-9, atol=1e-12)
+
+
+def test_moe_bwd_finite_differences(orc):
+    """Central differences of <dout, out(x + eps v)> with the routing fixed
+    match <dx, v>; likewise for one expert's W_down and the router."""
+    inp, dout, K, P = _bwd_case(T=10, H=24, E=8, I=16, K=2, seed=52)
+    x = bf16_bits(inp["x"])
+    r = orc.moe_route(x, bf16_bits(inp["w_router"]), K)
+    wg, wu, wd = (_split_ranks(inp[n], P) for n in ("w_gate", "w_up", "w_down"))
+    tok = orc.moe_bwd_tokens(x, bf16_bits(inp["w_router"]), r, bf16_bits(dout), wg, wu, wd)
+    dwr = orc.moe_bwd_router_weight(x, bf16_bits(inp["w_router"]), r, bf16_bits(dout), wg, wu, wd)
+    e0 = int(r["idx"][0, 0])
+    _, _, dwd = orc.moe_bwd_experts(x, r, bf16_bits(dout), wg, wu, wd, [e0])
+    idx = torch.from_numpy(r["idx"].astype(np.int64))
+    base = {n: inp[n].double() for n in ("x", "w_router", "w_gate", "w_up", "w_down")}
+    D = dout.double()
+    L = lambda t: float((_torch_layer(t["x"], t["w_router"], t["w_gate"], t["w_up"], t["w_down"], idx, K) * D).sum())
+    g = torch.Generator().manual_seed(9)
+    eps = 1e-6
+    for name, grad in (("x", tok["dx"]), ("w_router", dwr)):
+        v = torch.randn(base[name].shape, generator=g, dtype=torch.float64)
+        plus = dict(base); plus[name] = base[name] + eps * v
+        minus = dict(base); minus[name] = base[name] - eps * v
+        fd = (L(plus) - L(minus)) / (2 * eps)
+        assert abs(fd - float((torch.from_numpy(grad) * v).sum())) <= 1e-6 * max(1.0, abs(fd)), name
+    v = torch.randn(base["w_down"].shape[1:], generator=g, dtype=torch.float64)
+    plus = dict(base); plus["w_down"] = base["w_down"].clone(); plus["w_down"][e0] += eps * v
+    minus = dict(base); minus["w_down"] = base["w_down"].clone(); minus["w_down"][e0] -= eps * v
+    fd = (L(plus) - L(minus)) / (2 * eps)
+    assert abs(fd - float((torch.from_numpy(dwd[0]) * v).sum())) <= 1e-6 * max(1.0, abs(fd))
