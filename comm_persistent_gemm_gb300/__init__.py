@@ -28,12 +28,14 @@ INJECT_IDENTITY_EXPERTS = 0x4
 MOE_VIEW_LOGITS, MOE_VIEW_RECV, MOE_VIEW_H, MOE_VIEW_Y, MOE_VIEW_SLOT, MOE_VIEW_OFFSETS, MOE_VIEW_TRACE = range(7)
 MOE_VIEW_RECV_SCALES, MOE_VIEW_XQ, MOE_VIEW_XS = 7, 8, 9  # MXFP8 only
 KIND_NAMES = {1: "TRANSFER", 2: "TILE", 3: "REDUCE", 4: "ROUTE", 5: "DISPATCH", 6: "TILE_GU", 7: "TILE_D",
-              8: "PUSH", 9: "FOLD", 10: "TILE_HALF", 11: "QUANT"}
+              8: "PUSH", 9: "FOLD", 10: "TILE_HALF", 11: "QUANT", 16: "ZPAD", 17: "GRADIN", 18: "RBWD",
+              19: "RDX", 20: "DH", 21: "DGU", 22: "DWD", 23: "DWGU", 24: "DWR"}
 
 EXPORTS = ["kosmos_default_opts", "kosmos_num_sms", "kosmos_workspace_bytes", "kosmos_workspace_init",
            "kosmos_ag_gemm", "kosmos_gemm_rs", "kosmos_moe_fwd", "kosmos_mxfp8_quantize", "kosmos_status_sync",
            "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device", "kosmos_ag_gemm_noalloc",
-           "kosmos_moe_workspace_bytes", "kosmos_moe_debug_view", "kosmos_ag_tile_plan"]
+           "kosmos_moe_workspace_bytes", "kosmos_moe_debug_view", "kosmos_ag_tile_plan", "kosmos_moe_bwd",
+           "kosmos_moe_bwd_workspace_bytes", "kosmos_moe_bwd_debug_view"]
 
 
 class KosmosError(RuntimeError):
@@ -107,6 +109,13 @@ def lib():
     L.kosmos_moe_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, i32, vp, C.POINTER(vp), C.POINTER(i64)]
     L.kosmos_moe_debug_view.restype = i32
     L.kosmos_ag_tile_plan.argtypes = [i32, i64, i64, i64, i32, C.POINTER(Opts), C.POINTER(i64), C.POINTER(C.c_int32)]
+    L.kosmos_moe_bwd.argtypes = [vp, vp, i32, i64, i64, i32, i32, i64, vp, vp, vp, vp, vp, vp, C.c_size_t, vp, vp, vp,
+                                 vp, vp, vp, vp, C.c_size_t, C.POINTER(Opts), vp]
+    L.kosmos_moe_bwd.restype = i32
+    L.kosmos_moe_bwd_workspace_bytes.argtypes = [i32, i64, i64, i32, i32, i64, C.POINTER(Opts)]
+    L.kosmos_moe_bwd_workspace_bytes.restype = C.c_size_t
+    L.kosmos_moe_bwd_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, vp, C.POINTER(vp), C.POINTER(i64)]
+    L.kosmos_moe_bwd_debug_view.restype = i32
     L.kosmos_ag_tile_plan.restype = i32
     _lib = L
     return L
@@ -265,6 +274,51 @@ def moe_debug_view(what: int, P: int, tokens: int, hidden: int, n_experts: int, 
     rc = lib().kosmos_moe_debug_view(what, P, tokens, hidden, n_experts, topk, inter, dtype, ws.data_ptr(),
                                      C.byref(ptr), C.byref(nb))
     _raise(rc, "kosmos_moe_debug_view")
+    off = ptr.value - ws.data_ptr()
+    return ws[off:off + nb.value]
+
+
+def moe_bwd(x_shards: List, w_router, w_gate: List, w_up: List, w_down: List, topk_idx, topk_gate, fwd_ws,
+            dy_shards: List, dx_shards: List, dw_router, dw_gate: List, dw_up: List, dw_down: List, ws,
+            o: Optional[Opts] = None, stream=None):
+    """Backward of a bf16 moe_fwd call whose workspace fwd_ws is passed
+    unchanged: dx, dW_router (fp32), dW_gate / dW_up / dW_down (bf16)."""
+    _check_cuda(*x_shards, w_router, *w_gate, *w_up, *w_down, topk_idx, topk_gate, fwd_ws, *dy_shards, *dx_shards,
+                dw_router, *dw_gate, *dw_up, *dw_down, ws)
+    P = len(x_shards)
+    tokens = x_shards[0].shape[0] * P
+    hidden = x_shards[0].shape[1]
+    E = w_router.shape[1]
+    topk = topk_idx.shape[1]
+    inter = w_gate[0].shape[2]
+    rc = lib().kosmos_moe_bwd(_ptrs(x_shards), w_router.data_ptr(), P, tokens, hidden, E, topk, inter, _ptrs(w_gate),
+                              _ptrs(w_up), _ptrs(w_down), topk_idx.data_ptr(), topk_gate.data_ptr(), fwd_ws.data_ptr(),
+                              fwd_ws.numel(), _ptrs(dy_shards), _ptrs(dx_shards), dw_router.data_ptr(),
+                              _ptrs(dw_gate), _ptrs(dw_up), _ptrs(dw_down), ws.data_ptr(), ws.numel(),
+                              C.byref(o) if o is not None else None, _stream(stream))
+    _raise(rc, "kosmos_moe_bwd")
+
+
+def moe_bwd_workspace(P: int, tokens: int, hidden: int, n_experts: int, topk: int, inter: int,
+                      o: Optional[Opts] = None, device=None):
+    import torch
+    nbytes = int(lib().kosmos_moe_bwd_workspace_bytes(P, tokens, hidden, n_experts, topk, inter,
+                                                      C.byref(o) if o is not None else None))
+    if nbytes == 0:
+        raise KosmosError(ERR_INVALID_ARG, "kosmos_moe_bwd_workspace_bytes")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+MOE_BWD_VIEW_DY, MOE_BWD_VIEW_DG, MOE_BWD_VIEW_DU, MOE_BWD_VIEW_DXB, MOE_BWD_VIEW_DSLOT = range(5)
+MOE_BWD_VIEW_DGATE, MOE_BWD_VIEW_DL, MOE_BWD_VIEW_DXR, MOE_BWD_VIEW_TRACE = 5, 6, 7, 8
+
+
+def moe_bwd_debug_view(what: int, P: int, tokens: int, hidden: int, n_experts: int, topk: int, inter: int, ws):
+    """A uint8 view (torch tensor slice of ws) of one internal backward buffer."""
+    ptr = C.c_void_p()
+    nb = C.c_int64()
+    _raise(lib().kosmos_moe_bwd_debug_view(what, P, tokens, hidden, n_experts, topk, inter, ws.data_ptr(),
+                                           C.byref(ptr), C.byref(nb)), "kosmos_moe_bwd_debug_view")
     off = ptr.value - ws.data_ptr()
     return ws[off:off + nb.value]
 

@@ -13,7 +13,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkosmos.so")
-SOURCES = ["host.cu", "ag_gemm.cu", "gemm_rs.cu", "moe_fwd.cu", "aux_kernels.cu", "static_ws.cu", "ag_mxfp8.cu"]
+SOURCES = ["host.cu", "ag_gemm.cu", "gemm_rs.cu", "moe_fwd.cu", "moe_bwd.cu", "aux_kernels.cu", "static_ws.cu",
+           "ag_mxfp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

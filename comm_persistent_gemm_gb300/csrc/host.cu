@@ -514,6 +514,77 @@ kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, 
     return launch_moe_fwd(L, static_cast<cudaStream_t>(stream));
 }
 
+static bool moe_bwd_sizes_ok(int P, int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter) {
+    if (!moe_sizes_ok(P, tokens, hidden, n_experts, topk, inter)) return false;
+    return inter % 256 == 0 && (tokens / P) % 64 == 0;
+}
+
+size_t kosmos_moe_bwd_workspace_bytes(int P, int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter,
+                                      const kosmos_opts *opts) {
+    const kosmos_opts o = resolve_opts(opts);
+    if (!moe_bwd_sizes_ok(P, tokens, hidden, n_experts, topk, inter)) return 0;
+    return moe_bwd_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, o.trace != 0);
+}
+
+kosmos_status kosmos_moe_bwd_debug_view(int what, int P, int64_t tokens, int64_t hidden, int n_experts, int topk,
+                                        int64_t inter, void *ws, void **ptr, int64_t *bytes) {
+    if (!moe_bwd_sizes_ok(P, tokens, hidden, n_experts, topk, inter) || ws == nullptr || ptr == nullptr ||
+        bytes == nullptr)
+        return KOSMOS_ERR_INVALID_ARG;
+    return moe_bwd_debug_view(what, P, tokens, hidden, n_experts, topk, inter, ws, ptr, bytes)
+               ? KOSMOS_OK
+               : KOSMOS_ERR_INVALID_ARG;
+}
+
+kosmos_status kosmos_moe_bwd(const void *const *x_shards, const void *w_router, int P, int64_t tokens, int64_t hidden,
+                             int n_experts, int topk, int64_t inter, const void *const *w_gate,
+                             const void *const *w_up, const void *const *w_down, const int32_t *topk_idx,
+                             const float *topk_gate, const void *fwd_ws, size_t fwd_ws_bytes,
+                             const void *const *dy_shards, void *const *dx_shards, float *dw_router,
+                             void *const *dw_gate, void *const *dw_up, void *const *dw_down, void *ws,
+                             size_t ws_bytes, const kosmos_opts *opts, void *stream) {
+    if (!moe_bwd_sizes_ok(P, tokens, hidden, n_experts, topk, inter)) return KOSMOS_ERR_INVALID_ARG;
+    if (x_shards == nullptr || w_gate == nullptr || w_up == nullptr || w_down == nullptr || dy_shards == nullptr ||
+        dx_shards == nullptr || dw_gate == nullptr || dw_up == nullptr || dw_down == nullptr)
+        return KOSMOS_ERR_INVALID_ARG;
+    for (int q = 0; q < P; ++q)
+        if (!aligned16(x_shards[q]) || !aligned16(w_gate[q]) || !aligned16(w_up[q]) || !aligned16(w_down[q]) ||
+            !aligned16(dy_shards[q]) || !aligned16(dx_shards[q]) || !aligned16(dw_gate[q]) || !aligned16(dw_up[q]) ||
+            !aligned16(dw_down[q]))
+            return KOSMOS_ERR_INVALID_ARG;
+    if (!aligned16(w_router) || !aligned16(topk_idx) || !aligned16(topk_gate) || !aligned16(dw_router) ||
+        !aligned16(fwd_ws))
+        return KOSMOS_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
+    const kosmos_opts o = resolve_opts(opts);
+    if (o.sched != KOSMOS_SCHED_SELF || o.link_gbs != 0 || o.inject != 0) return KOSMOS_ERR_UNSUPPORTED;
+    if (fwd_ws_bytes < moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, false, false))
+        return KOSMOS_ERR_WORKSPACE;
+    if (ws_bytes < kosmos_moe_bwd_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, &o))
+        return KOSMOS_ERR_WORKSPACE;
+    const int grid = grid_for(o);
+    if (grid < 1) return KOSMOS_ERR_CUDA;
+    if (grid < P) return KOSMOS_ERR_INVALID_ARG;
+    MoeBwdLaunch L;
+    memset(&L, 0, sizeof(L));
+    L.P = P; L.T = tokens; L.H = hidden; L.I = inter; L.E = n_experts; L.K = topk;
+    for (int q = 0; q < P; ++q) {
+        L.x[q] = x_shards[q];
+        L.wg[q] = w_gate[q];
+        L.wu[q] = w_up[q];
+        L.wd[q] = w_down[q];
+        L.dout[q] = dy_shards[q];
+        L.dx[q] = dx_shards[q];
+        L.dwg[q] = dw_gate[q];
+        L.dwu[q] = dw_up[q];
+        L.dwd[q] = dw_down[q];
+    }
+    L.wr = w_router;
+    L.topk_idx = topk_idx; L.topk_gate = topk_gate; L.fwd_ws = fwd_ws; L.dwr = dw_router;
+    L.ws = ws; L.trace = o.trace; L.grid = grid; L.plain_launch = o.plain_launch; L.wait_limit_ns = o.wait_limit_ns;
+    return launch_moe_bwd(L, static_cast<cudaStream_t>(stream));
+}
+
 kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int along_cols, void *q, void *scales,
                                     void *stream) {
     if (!aligned16(x) || !aligned16(q) || !aligned16(scales) || rows < 1 || cols < 1) return KOSMOS_ERR_INVALID_ARG;

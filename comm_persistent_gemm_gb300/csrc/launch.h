@@ -106,6 +106,35 @@ kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream);
 size_t ag_mxfp8_scale_bytes(int P, int64_t m, int64_t k);
 kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream);
 kosmos_status launch_moe_fwd(const MoeLaunch &L, cudaStream_t stream);
+
+struct MoeBwdLaunch {
+    int P;
+    int64_t T, H, I;
+    int E, K;
+    const void *x[KOSMOS_MAX_P];
+    const void *wr;
+    const void *wg[KOSMOS_MAX_P];
+    const void *wu[KOSMOS_MAX_P];
+    const void *wd[KOSMOS_MAX_P];
+    const int32_t *topk_idx;
+    const float *topk_gate;
+    const void *fwd_ws;
+    const void *dout[KOSMOS_MAX_P];
+    void *dx[KOSMOS_MAX_P];
+    float *dwr;
+    void *dwg[KOSMOS_MAX_P];
+    void *dwu[KOSMOS_MAX_P];
+    void *dwd[KOSMOS_MAX_P];
+    void *ws;
+    int trace;
+    int grid;
+    int plain_launch;
+    uint64_t wait_limit_ns;
+};
+kosmos_status launch_moe_bwd(const MoeBwdLaunch &L, cudaStream_t stream);
+size_t moe_bwd_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool trace);
+bool moe_bwd_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t I, void *ws, void **ptr,
+                        int64_t *bytes);
 size_t moe_workspace_bytes(int P, int64_t T, int64_t H, int E, int K, int64_t I, bool mx, bool trace);
 bool moe_debug_view(int what, int P, int64_t T, int64_t H, int E, int K, int64_t I, bool mx, void *ws, void **ptr,
                     int64_t *bytes);

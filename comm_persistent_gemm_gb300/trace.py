@@ -15,7 +15,8 @@ from typing import Dict, Iterable, List, Optional
 import numpy as np
 
 KIND_NAMES = {1: "TRANSFER", 2: "TILE", 3: "REDUCE", 4: "ROUTE", 5: "DISPATCH", 6: "TILE_GU", 7: "TILE_D",
-              8: "PUSH", 9: "FOLD"}
+              8: "PUSH", 9: "FOLD", 10: "TILE_HALF", 11: "QUANT", 16: "ZPAD", 17: "GRADIN", 18: "RBWD",
+              19: "RDX", 20: "DH", 21: "DGU", 22: "DWD", 23: "DWGU", 24: "DWR"}
 TRACE_DTYPE = np.dtype([("t_claim", "<i8"), ("t_ready", "<i8"), ("t_done", "<i8"), ("kind", "<i4"),
                         ("ticket", "<i4"), ("cta", "<i4"), ("pad", "<i4")])
 

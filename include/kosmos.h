@@ -277,6 +277,59 @@ KOSMOS_API kosmos_status kosmos_moe_debug_view(int what, int P, int64_t tokens, 
                                                int64_t *bytes);
 
 /*
+ * MoE expert layer backward in one launch  (abstract: "one launch per
+ * direction").  Gradients of a BF16 kosmos_moe_fwd call with its top-K
+ * routing held fixed (L = <dout, out>):
+ *   dgate[t][k] = <dout_t, y[t][k]>, dy[t][k] = gate[t][k] dout_t,
+ *   dh = dy W_down^T, dg = dh * u * silu'(g), du = dh * silu(g),
+ *   dx_t = sum_k (dg W_gate^T + du W_up^T) + dl_t W_router^T,
+ *   dl = softmax backward of the renormalised top-K gates,
+ *   dW_gate[e] = x^T dg, dW_up[e] = x^T du, dW_down[e] = h^T dy (sums over
+ *   the slots routed to e), dW_router = x^T dl (all tokens).
+ *   Arguments as for kosmos_moe_fwd, plus:
+ *   topk_idx, topk_gate : the forward's outputs.
+ *   fwd_ws        : the forward's workspace, untouched since that call (it
+ *                   holds the saved context: expert-ordered token rows, g, u,
+ *                   h, the per-slot outputs, logits, dispatch tables).
+ *   dy_shards[q]  : dout of rank q's tokens [tokens/P, hidden] bf16.
+ *   dx_shards[q]  : out, [tokens/P, hidden] bf16: the expert and router parts
+ *                   summed in fp32 (slots in k order, then the router part),
+ *                   one rounding.
+ *   dw_router     : out, [hidden, n_experts] fp32.
+ *   dw_gate[q], dw_up[q] : out, [n_experts/P, hidden, inter] bf16;
+ *   dw_down[q]    : out, [n_experts/P, inter, hidden] bf16 (fp32 sums over
+ *                   each expert's rows, one rounding).
+ *   Intermediates dy, dg, du, dl and the slot gradients are bf16.
+ *   Requirements: those of kosmos_moe_fwd, inter % 256 == 0 and
+ *   (tokens/P) % 64 == 0; SELF schedule, no link cap, no injection.
+ *   Workspace: kosmos_moe_bwd_workspace_bytes.
+ */
+KOSMOS_API kosmos_status kosmos_moe_bwd(const void *const *x_shards, const void *w_router, int P,
+                             int64_t tokens, int64_t hidden, int n_experts, int topk, int64_t inter,
+                             const void *const *w_gate, const void *const *w_up,
+                             const void *const *w_down, const int32_t *topk_idx,
+                             const float *topk_gate, const void *fwd_ws, size_t fwd_ws_bytes,
+                             const void *const *dy_shards, void *const *dx_shards, float *dw_router,
+                             void *const *dw_gate, void *const *dw_up, void *const *dw_down,
+                             void *ws, size_t ws_bytes, const kosmos_opts *opts, void *stream);
+
+/* Workspace size in bytes for kosmos_moe_bwd (opts may be NULL); 0 for invalid sizes. */
+KOSMOS_API size_t kosmos_moe_bwd_workspace_bytes(int P, int64_t tokens, int64_t hidden, int n_experts, int topk,
+                                                 int64_t inter, const kosmos_opts *opts);
+
+/* Device views into a backward workspace after a call (R = the padded row
+ * capacity: each expert's rows from a 16-row boundary, experts ascending):
+ *   what 0: dy [R, hidden] bf16   1: dg [R, inter] bf16   2: du [R, inter] bf16
+ *        3: dx of the expert rows [R, hidden] bf16   4: dx slots [tokens, topk, hidden] bf16
+ *        5: dgate [tokens, topk] fp32   6: dl [tokens, n_experts] bf16
+ *        7: dx of the router path [tokens, hidden] fp32
+ *        8: role trace records (only for a workspace sized with opts.trace)
+ * Returns KOSMOS_OK and sets *ptr / *bytes, or KOSMOS_ERR_INVALID_ARG. */
+KOSMOS_API kosmos_status kosmos_moe_bwd_debug_view(int what, int P, int64_t tokens, int64_t hidden, int n_experts,
+                                                   int topk, int64_t inter, void *ws, void **ptr,
+                                                   int64_t *bytes);
+
+/*
  * MXFP8 quantiser for the MXFP8 all-gather+GEMM operands.  For each block of
  * 32 consecutive K-elements: e = smallest integer with blockmax <= 448 * 2^e
  * (clamped to [-127, 127]; an all-zero block takes e = 0), scale byte e + 127,

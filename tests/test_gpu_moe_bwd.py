@@ -1,0 +1,182 @@
+"""GPU parity of the one-launch MoE backward against the oracle's fp64
+gradients of the forward layer (top-K routing held fixed).
+
+Compared where the routing is the oracle's (tokens whose top-K decision has
+a margin, and experts whose slot sets match): dx on tokens, dW_gate / dW_up /
+dW_down on experts, dW_router on the whole layer (small cases), each within
+max|got - ref| <= 1e-2 * max|ref|; reruns bit-identical."""
+import numpy as np
+import pytest
+import torch
+
+from _helpers import bf16_tensor_to_f64, kosmos, rel_err
+from kosmos_inputs import WORKLOADS, bf16_bits, moe_inputs, sample_indices
+from test_gpu_moe import _split, check_routing
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return kosmos()
+
+
+def dout_for(T, H, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(T, H, generator=g).to(torch.bfloat16)
+
+
+def run_fwd_bwd(K, inp, dout, P, topk, reps=1, o=None):
+    T, H = inp["x"].shape
+    E = inp["w_router"].shape[1]
+    I = inp["w_gate"].shape[2]
+    dev = "cuda"
+    xs = [t.to(dev) for t in torch.chunk(inp["x"], P, 0)]
+    wr = inp["w_router"].to(dev)
+    wg = [t.to(dev) for t in _split(inp["w_gate"], P)]
+    wu = [t.to(dev) for t in _split(inp["w_up"], P)]
+    wd = [t.to(dev) for t in _split(inp["w_down"], P)]
+    ys = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    idx = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    gate = torch.empty(T, topk, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    pos = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    fws = K.moe_workspace(P, T, H, E, topk, I)
+    K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, fws, topk)
+    K.check(fws, "moe_fwd")
+    dys = [t.to(dev) for t in torch.chunk(dout, P, 0)]
+    dxs = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    dwr = torch.empty(H, E, dtype=torch.float32, device=dev)
+    dwg = [torch.empty_like(w) for w in wg]
+    dwu = [torch.empty_like(w) for w in wu]
+    dwd = [torch.empty_like(w) for w in wd]
+    bws = K.moe_bwd_workspace(P, T, H, E, topk, I, o)
+    outs = []
+    for _ in range(reps):
+        for t in dxs + dwg + dwu + dwd + [dwr]:
+            t.fill_(float("nan"))
+        K.moe_bwd(xs, wr, wg, wu, wd, idx, gate, fws, dys, dxs, dwr, dwg, dwu, dwd, bws, o)
+        K.check(bws, "moe_bwd")
+        outs.append({"dx": torch.cat(dxs, 0).clone(), "dwr": dwr.clone(), "dwg": torch.cat(dwg, 0).clone(),
+                     "dwu": torch.cat(dwu, 0).clone(), "dwd": torch.cat(dwd, 0).clone()})
+    logits = K.moe_debug_view(K.MOE_VIEW_LOGITS, P, T, H, E, topk, I, fws).view(torch.float32).view(T, E)
+    fwd = {"idx": idx.cpu().numpy(), "gate": gate.cpu().numpy(), "counts": counts.cpu().numpy(),
+           "pos": pos.cpu().numpy(), "logits": logits.cpu().numpy()}
+    return outs, fwd, bws
+
+
+def oracle_args(inp, P):
+    return ([bf16_bits(w) for w in _split(inp["w_gate"], P)], [bf16_bits(w) for w in _split(inp["w_up"], P)],
+            [bf16_bits(w) for w in _split(inp["w_down"], P)])
+
+
+def same_slots(kern_idx, ref_idx, e):
+    return np.array_equal(np.argwhere(kern_idx == e), np.argwhere(ref_idx == e))
+
+
+@pytest.mark.parametrize("P,T,H,E,topk,I", [(2, 256, 256, 64, 4, 256), (4, 512, 512, 64, 8, 512),
+                                            (1, 128, 256, 64, 2, 256), (8, 1024, 256, 128, 8, 256)])
+def test_moe_bwd_small_full_compare(K, orc, P, T, H, E, topk, I):
+    inp = moe_inputs(T, H, E, I, seed=900 + T + E + topk)
+    dout = dout_for(T, H, seed=T + H)
+    outs, fwd, _ = run_fwd_bwd(K, inp, dout, P, topk, reps=2)
+    route = orc.moe_route(bf16_bits(inp["x"]), bf16_bits(inp["w_router"]), topk)
+    clear = check_routing(fwd, route, topk)
+    wg, wu, wd = oracle_args(inp, P)
+    x, wr, d = bf16_bits(inp["x"]), bf16_bits(inp["w_router"]), bf16_bits(dout)
+    ref = orc.moe_bwd_tokens(x, wr, route, d, wg, wu, wd)
+    got = outs[0]
+    for key in ("dx", "dwr", "dwg", "dwu", "dwd"):
+        assert not torch.isnan(got[key]).any(), key
+        assert torch.equal(outs[0][key], outs[1][key]), f"{key}: reruns differ"
+    gx = bf16_tensor_to_f64(got["dx"])
+    assert rel_err(gx[clear], ref["dx"][clear]) <= TOL, rel_err(gx[clear], ref["dx"][clear])
+    experts = [e for e in range(E) if same_slots(fwd["idx"], route["idx"], e)]
+    assert len(experts) >= E // 2
+    rg, ru, rd = orc.moe_bwd_experts(x, route, d, wg, wu, wd, experts)
+    sel = torch.tensor(experts)
+    for key, r in (("dwg", rg), ("dwu", ru), ("dwd", rd)):
+        gk = bf16_tensor_to_f64(got[key][sel])
+        assert rel_err(gk, r) <= TOL, (key, rel_err(gk, r))
+    if clear.all():
+        rwr = orc.moe_bwd_router_weight(x, wr, route, d, wg, wu, wd)
+        assert rel_err(got["dwr"].cpu().double().numpy(), rwr) <= TOL, rel_err(got["dwr"].cpu().double().numpy(), rwr)
+
+
+def test_moe_bwd_empty_expert_and_ragged_blocks(K, orc):
+    """An expert no token selects gets zero weight gradients; token blocks of
+    192 rows (a ragged second block)."""
+    P, T, H, E, topk, I = 2, 384, 256, 64, 4, 256
+    inp = moe_inputs(T, H, E, I, seed=13)
+    wr = inp["w_router"].float() * 50.0
+    wr[:, 7] = 0.0
+    inp["w_router"] = wr.to(torch.bfloat16)
+    dout = dout_for(T, H, seed=3)
+    outs, fwd, _ = run_fwd_bwd(K, inp, dout, P, topk)
+    assert fwd["counts"][7] == 0
+    got = outs[0]
+    for key in ("dwg", "dwu", "dwd"):
+        assert torch.count_nonzero(got[key][7]) == 0, key
+    route = orc.moe_route(bf16_bits(inp["x"]), bf16_bits(inp["w_router"]), topk)
+    clear = check_routing(fwd, route, topk)
+    wg, wu, wd = oracle_args(inp, P)
+    ref = orc.moe_bwd_tokens(bf16_bits(inp["x"]), bf16_bits(inp["w_router"]), route, bf16_bits(dout), wg, wu, wd)
+    gx = bf16_tensor_to_f64(got["dx"])
+    assert rel_err(gx[clear], ref["dx"][clear]) <= TOL
+
+
+def test_moe_bwd_trace_every_entry_once(K, orc):
+    P, T, H, E, topk, I = 4, 512, 512, 64, 4, 256
+    inp = moe_inputs(T, H, E, I, seed=23)
+    o = K.opts(trace=1)
+    outs, fwd, bws = run_fwd_bwd(K, inp, dout_for(T, H, 4), P, topk, o=o)
+    raw = K.moe_bwd_debug_view(K.MOE_BWD_VIEW_TRACE, P, T, H, E, topk, I, bws).cpu().numpy()
+    dt = np.dtype([("t_claim", "<i8"), ("t_ready", "<i8"), ("t_done", "<i8"), ("kind", "<i4"),
+                   ("ticket", "<i4"), ("cta", "<i4"), ("pad", "<i4")])
+    recs = raw.view(dt)
+    recs = recs[recs["kind"] != 0]
+    counts = fwd["counts"]
+    Eq = E // P
+    units = [int(sum((counts[q * Eq + j] + 127) // 128 for j in range(Eq))) for q in range(P)]
+    RB = (T // P + 127) // 128
+    NIC, NHC, NWI, NWH = I // 256, H // 256, I // 128, H // 128
+    head = 1 + RB * topk + RB + RB * NHC
+    for q in range(P):
+        mine = recs[(recs["cta"] % P) == q]
+        main = np.sort(mine["ticket"][np.isin(mine["kind"], list(range(16, 25)))])
+        ndwr = len(range(q, NWH, P))
+        n = head + (NIC + NHC) * units[q] + (NWI * NHC + NWH * NWI) * Eq + ndwr
+        assert np.array_equal(main, np.arange(n)), q
+    kinds = recs["kind"]
+    assert (kinds == 8).sum() == sum(units) * NHC        # one push per DGU tile
+    assert (kinds == 9).sum() == P * RB * NHC            # one fold per (token block, column tile)
+
+
+def test_moe_bwd_full_size_sampled(K, orc):
+    """2048 tokens, hidden 4096, 128 experts top-8 over 8 EP ranks, inter
+    1536: dx on sampled tokens, weight gradients of two experts, bit-identical
+    rerun."""
+    w = WORKLOADS["moe_fwd_p8"]
+    inp = moe_inputs(w.T, w.H, w.E, w.I, w.seed)
+    dout = dout_for(w.T, w.H, seed=77)
+    outs, fwd, _ = run_fwd_bwd(K, inp, dout, w.P, w.topk, reps=2)
+    for key in ("dx", "dwr", "dwg", "dwu", "dwd"):
+        assert torch.equal(outs[0][key], outs[1][key]), key
+    route = orc.moe_route(bf16_bits(inp["x"]), bf16_bits(inp["w_router"]), w.topk)
+    clear = check_routing(fwd, route, w.topk)
+    wg, wu, wd = oracle_args(inp, w.P)
+    x, d = bf16_bits(inp["x"]), bf16_bits(dout)
+    tokens = sample_indices(w.T, 4, seed=6)
+    tokens = tokens[clear[tokens]]
+    ref = orc.moe_bwd_tokens(x, bf16_bits(inp["w_router"]), route, d, wg, wu, wd, tokens=tokens)
+    got = bf16_tensor_to_f64(outs[0]["dx"][torch.from_numpy(tokens).cuda()])
+    assert rel_err(got, ref["dx"]) <= TOL, rel_err(got, ref["dx"])
+    experts = [e for e in (3, w.E - 1) if same_slots(fwd["idx"], route["idx"], e)]
+    rg, ru, rd = orc.moe_bwd_experts(x, route, d, wg, wu, wd, experts)
+    sel = torch.tensor(experts)
+    for key, r in (("dwg", rg), ("dwu", ru), ("dwd", rd)):
+        gk = bf16_tensor_to_f64(outs[0][key][sel])
+        assert rel_err(gk, r) <= TOL, (key, rel_err(gk, r))
