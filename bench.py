@@ -307,6 +307,73 @@ def _quant_experts_gpu(K, w, P, dev, stream):
     return codes, scales
 
 
+# Algorithmic HBM bytes of one MoE backward step (bf16): every expert weight
+# read once and every weight gradient written once (2 x 4.83 GB at the
+# benchmark shapes), plus the token-side and expert-side activations each
+# read or written once: dout and the saved per-slot outputs, dy, g / u and
+# dg / du, h and x for the weight gradients, dx of the expert rows, the slot
+# push and fold, the router part.
+def moe_bwd_algorithmic_bytes(T, H, E, K, I):
+    rows = T * K
+    w = E * 3 * H * I * 2
+    token = T * H * 2 + rows * H * 2 + rows * H * 2 + rows * 4          # dout, y slots, dy, dgate
+    dh = rows * H * 2 + 2 * rows * I * 2 + 2 * rows * I * 2             # dy, g/u, dg/du
+    dgu = 2 * rows * I * 2 + rows * H * 2                               # dg/du, dx rows
+    wgrad_in = rows * I * 2 + rows * H * 2 + rows * H * 2 + 2 * rows * I * 2  # h, dy, x, dg/du
+    push_fold = 2 * rows * H * 2 + rows * H * 2 + T * H * 4 + T * H * 2
+    router = T * E * 4 + T * E * 2 + H * E * 2 + T * H * 4 + T * H * 2 + H * E * 4
+    return 2 * w + token + dh + dgu + wgrad_in + push_fold + router
+
+
+def bench_moe_bwd(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0):
+    """MoE layer backward (2048 tokens, hidden 4096, 128 experts top-8, 8 EP
+    ranks, inter 1536) in one launch; the forward runs once untimed to fill
+    the saved context."""
+    import dataclasses
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS["moe_fwd_p8"]
+    if experts:  # a smaller expert count for profiler captures
+        w = dataclasses.replace(w, E=experts, name=f"moe_fwd_p8_e{experts}")
+    inp = workload_inputs(w)
+    P, T, H, E, Kt, I = w.P, w.T, w.H, w.E, w.topk, w.I
+    xs = [t.to(dev) for t in torch.chunk(inp["x"], P, 0)]
+    wr = inp["w_router"].to(dev)
+    wg = [t.to(dev) for t in _split_experts(inp["w_gate"], P)]
+    wu = [t.to(dev) for t in _split_experts(inp["w_up"], P)]
+    wd = [t.to(dev) for t in _split_experts(inp["w_down"], P)]
+    del inp
+    ys = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    idx = torch.empty(T, Kt, dtype=torch.int32, device=dev)
+    gate = torch.empty(T, Kt, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    pos = torch.empty(T, Kt, dtype=torch.int32, device=dev)
+    fws = K.moe_workspace(P, T, H, E, Kt, I, device=dev)
+    K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, fws, Kt, stream=stream)
+    K.check(fws, "moe_fwd")
+    g = torch.Generator(device="cpu").manual_seed(11)
+    dys = [t.to(dev) for t in torch.chunk(torch.randn(T, H, generator=g).to(torch.bfloat16), P, 0)]
+    dxs = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    dwr = torch.empty(H, E, dtype=torch.float32, device=dev)
+    dwg = [torch.empty_like(t) for t in wg]
+    dwu = [torch.empty_like(t) for t in wu]
+    dwd = [torch.empty_like(t) for t in wd]
+    bws = K.moe_bwd_workspace(P, T, H, E, Kt, I, device=dev)
+    f = lambda: K.moe_bwd(xs, wr, wg, wu, wd, idx, gate, fws, dys, dxs, dwr, dwg, dwu, dwd, bws, stream=stream)
+    f()
+    K.check(bws, "moe_bwd")
+    t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
+    K.check(bws, "moe_bwd")
+    byt = moe_bwd_algorithmic_bytes(T, H, E, Kt, I)
+    flops = 12.0 * T * Kt * H * I + 4.0 * T * E * H
+    gbs = byt / (t * 1e-3) / 1e9
+    return {"workload": w.name.replace("moe_fwd", "moe_bwd"), "ms": t, "tokens_per_s": T / (t * 1e-3), "tflops": flops / (t * 1e-3) / 1e12,
+            "frac_of_tensor_peak": flops / (t * 1e-3) / 1e12 / tensor_peak,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "bytes_per_launch": byt},
+            "launches_per_step": 1}
+
+
 def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0, mx=False):
     import dataclasses
     import torch
@@ -564,6 +631,9 @@ def run_quick_other(args):
     elif args.workload == "moe":
         r = bench_moe(K, dev, args.steps, args.warmup, flush, stream, peaks["hbm_gbs"], peaks["bf16_tflops"],
                       experts=args.experts)
+    elif args.workload == "moe_bwd":
+        r = bench_moe_bwd(K, dev, args.steps, args.warmup, flush, stream, peaks["hbm_gbs"], peaks["bf16_tflops"],
+                          experts=args.experts)
     elif args.workload == "attn":
         r = bench_attn(K, dev, args.steps, args.warmup, flush, stream, peaks["bf16_tflops"])
     elif args.workload == "moe_mxfp8":
@@ -706,6 +776,8 @@ def run_kosmos(args):
         torch.cuda.empty_cache()
         also["attention"] = bench_attn(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
+        also["moe_bwd"] = bench_moe_bwd(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"], peak)
+        torch.cuda.empty_cache()
 
     line = None
     if rank == 0:
@@ -734,7 +806,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kosmos", choices=["kosmos", "reference"])
     ap.add_argument("--ag-only", action="store_true", help="skip the GEMM+RS and MoE measurements")
-    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8", "rs_mxfp8", "moe_mxfp8", "attn"],
+    ap.add_argument("--workload", default="ag", choices=["ag", "rs", "moe", "mxfp8", "rs_mxfp8", "moe_mxfp8", "attn", "moe_bwd"],
                     help="with --quick: which fused operator to time")
     ap.add_argument("--experts", type=int, default=0, help="with --quick --workload moe: expert count (0 = 128)")
     ap.add_argument("--num-ctas", type=int, default=0,

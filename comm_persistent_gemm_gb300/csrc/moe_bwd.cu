@@ -46,6 +46,12 @@ __device__ __forceinline__ bool bwd_is_mma(int k) {
     return k == KB_RDX || k == KB_DH || k == KB_DGU || k == KB_DWD || k == KB_DWGU || k == KB_DWR;
 }
 constexpr int BWD_LAG = 2;
+// shared memory: the engine's stages and control, the per-CTA tables, and
+// per epilogue warp two 2 KB staging buffers for the weight-gradient stores
+constexpr int BWD_TABLE_BYTES = 5120;
+constexpr int BWD_STAGE_OUT = 2048;
+constexpr int BWD_SMEM_BYTES = SMEM_BYTES + BWD_TABLE_BYTES + 4 * 2 * BWD_STAGE_OUT;
+static_assert(BWD_SMEM_BYTES <= 232448, "MoE backward exceeds 227 KB of shared memory per CTA");
 
 struct BwdGeom {
     MoeGeom f;
@@ -141,6 +147,10 @@ struct BwdParams {
     CUtensorMap tmWgT[KOSMOS_MAX_P]; // W_gate[q] [Eq, H, I] as K-major B of DGU: dims {I, H, Eq}, box {64, 256, 1}
     CUtensorMap tmWuT[KOSMOS_MAX_P];
     CUtensorMap tmXs[KOSMOS_MAX_P];  // x_shards[q] [Tq, H]: MN-major A of DWR, box {64, 64}
+    // weight-gradient outputs, stored from shared memory in 32 x 32 blocks (no swizzle)
+    CUtensorMap tmDwg[KOSMOS_MAX_P]; // dims {I, H, Eq}
+    CUtensorMap tmDwu[KOSMOS_MAX_P];
+    CUtensorMap tmDwd[KOSMOS_MAX_P]; // dims {H, I, Eq}
     // forward context
     const int32_t *counts, *offl, *unit_start, *base, *rank_in_blk, *inv_pos;
     const float *logits;
@@ -209,13 +219,17 @@ __device__ __forceinline__ void bwd_load_tables(const BwdParams &p, const BwdTab
 //   (j < Eq), DGU(j-1): NHC x u_{j-1}, DWGU(j-2): W2 (0 <= j-2 < Eq)
 // with u_j the row blocks of expert j and U(j) their prefix.
 __device__ __forceinline__ void bwd_decode_tile(const BwdGeom &b, const int32_t *us, int tt, int &kind, int &le,
-                                                int &x, int &y) {
+                                                int &x, int &y, int &hint) {
     const MoeGeom &g = b.f;
     auto U = [&](int j) { return j <= 0 ? 0 : us[j < g.Eq ? j : g.Eq]; };
     auto clampEq = [&](int v) { return v < 0 ? 0 : (v > g.Eq ? g.Eq : v); };
+    auto gstart = [&](int j) { return b.NIC * U(j) + b.W1 * clampEq(j) + b.NHC * U(j - 1) + b.W2 * clampEq(j - 2); };
     kind = 0;
     if (tt < 0) return;
-    for (int j = 0; j < g.Eq + BWD_LAG; ++j) {
+    // a CTA's tickets increase: start from the group of its previous tile
+    int j0 = (hint > 0 && hint < g.Eq + BWD_LAG && gstart(hint) <= tt) ? hint : 0;
+    for (int j = j0; j < g.Eq + BWD_LAG; ++j) {
+        hint = j;
         const int uj = j < g.Eq ? U(j + 1) - U(j) : 0;
         const int n_dh = b.NIC * uj;
         const int n_dwd = j < g.Eq ? b.W1 : 0;
@@ -255,6 +269,9 @@ struct BwdProdState {
     bool main_done = false;
     uint64_t idle_t0 = 0;
     int64_t ahead = -1;
+    int hint = 0;      // tile-rail group of the previous tile
+    uint32_t polls = 0;  // decide calls: the push queue is polled on every fourth while the rail lasts
+    int ready_dwd = -1, ready_dwgu = -1;  // the expert whose inputs were last confirmed complete
 };
 
 __device__ __forceinline__ int bwd_trace_open(const BwdParams &p, BwdProdState &st, int kind, int ticket) {
@@ -292,8 +309,10 @@ __device__ __noinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdP
     const int q = blockIdx.x % g.P;
     uint32_t *qc = p.qctl + 4 * q;
     if (failed(p.ws)) return false;
-    // 1) a ready PUSH
-    {
+    // 1) a ready PUSH (polled on every fourth call while rail entries remain:
+    //    each poll is a round trip to L2, and the short weight-gradient
+    //    tiles would otherwise wait on it)
+    if (st.main_done || (st.polls++ & 3u) == 0) {
         int32_t code;
         if (queue_try_take(&qc[1], &qc[0], p.push_items + q * b.push_cap, p.push_flags + q * b.push_cap, epoch, code,
                            p.ws)) {
@@ -397,7 +416,7 @@ __device__ __noinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdP
             }
         } else {
             int kind = 0, le = 0, x = 0, y = 0;
-            bwd_decode_tile(b, tb.us, tt, kind, le, x, y);
+            bwd_decode_tile(b, tb.us, tt, kind, le, x, y, st.hint);
             if (kind == 0) {
                 set_error(p.ws, KOSMOS_ERR_DEVICE, -30);
                 return false;
@@ -448,17 +467,21 @@ __device__ __noinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdP
                 // weight gradients over the expert's rows: the K loop covers
                 // the 16-row-padded rows; the last stage issues only its
                 // K steps of 16
-                for (int u = 0; u < units; ++u) {
-                    const int ci = e * g.MAXRB + u;
-                    if (kind == KB_DWD) {
-                        int real, r16;
-                        unit_rows(tb, le, u, real, r16);
-                        if (!wait_flag_eq(p.ws, &p.dy_cnt[ci], static_cast<uint32_t>(r16), p.wait_limit_ns, t))
-                            return false;
-                    } else {
-                        if (!wait_flag_eq(p.ws, &p.dh_cnt[ci], static_cast<uint32_t>(b.NIC), p.wait_limit_ns, t))
-                            return false;
+                int &ready = kind == KB_DWD ? st.ready_dwd : st.ready_dwgu;
+                if (ready != e) {
+                    for (int u = 0; u < units; ++u) {
+                        const int ci = e * g.MAXRB + u;
+                        if (kind == KB_DWD) {
+                            int real, r16;
+                            unit_rows(tb, le, u, real, r16);
+                            if (!wait_flag_eq(p.ws, &p.dy_cnt[ci], static_cast<uint32_t>(r16), p.wait_limit_ns, t))
+                                return false;
+                        } else {
+                            if (!wait_flag_eq(p.ws, &p.dh_cnt[ci], static_cast<uint32_t>(b.NIC), p.wait_limit_ns, t))
+                                return false;
+                        }
                     }
+                    ready = e;
                 }
                 const int nst = (c16 + BK - 1) / BK;
                 const int last = (c16 - (nst - 1) * BK) / 16;  // 1..4 when nst > 0
@@ -907,8 +930,30 @@ __device__ __noinline__ bool bwd_fold(const BwdParams &p, const Smem &sm, PipeSt
 
 __device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + expf(-a)); }
 
+// One 32 x 32 block of this warp's rows (a weight-gradient tile) stored
+// through the warp's staging buffers: the lanes write their rows' 64 bytes,
+// lane 0 issues the tiled bulk store; a buffer is rewritten once the store
+// issued two blocks earlier has read it.
+__device__ __forceinline__ void bwd_store_block(uint8_t *stg, int &sb, int lane, const float (&v)[32],
+                                                const CUtensorMap *m, int32_t c0, int32_t c1, int32_t c2) {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    uint4 *row = reinterpret_cast<uint4 *>(stg + sb * BWD_STAGE_OUT + lane * 64);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+        row[q4] = make_uint4(pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]), pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
+                             pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]), pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(m, stg + sb * BWD_STAGE_OUT, c0, c1, c2);
+        bulk_commit();
+    }
+    sb ^= 1;
+}
+
 __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm, const BwdTables &tb,
-                                             uint32_t tmem_base, int warp, int lane, uint32_t epoch) {
+                                             uint32_t tmem_base, uint8_t *stg, int warp, int lane, uint32_t epoch) {
     const BwdGeom &b = p.b;
     const MoeGeom &g = b.f;
     const int grp = warp & 3;
@@ -918,6 +963,7 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
     RingState rs;
     PipeState ps;
     uint32_t acc = 0, acc_phase = 0;
+    int sb = 0;  // staging buffer of this warp's next block store
     while (true) {
         if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
             set_error(p.ws, KOSMOS_ERR_DEVICE, -6);
@@ -983,25 +1029,26 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
                     acc_chunk(taddr + ch * 32, false, v);
                     if (row < real) store_bf16x32(p.dxb + prow * g.H + static_cast<int64_t>(e.c) * 256 + ch * 32, v);
                 }
-            } else if (e.kind == KB_DWD) {
-                // dW_down[e] rows (inter) x * 128 + row, columns (hidden) y * 256 ..
+            } else if (e.kind == KB_DWD || e.kind == KB_DWGU) {
+                // DWD: dW_down[e] rows (inter) x * 128 + row, columns (hidden) y * 256 ..
+                // DWGU: columns 0-127 dW_gate[e] (hidden row x * 128 + row, inter y * 128 ..), 128-255 dW_up
+                // The next chunk's tensor-memory load is in flight while this one is stored.
                 const int q = e.a / g.Eq;
-                __nv_bfloat16 *dst = p.dwd[q] + (static_cast<int64_t>(e.d) * g.I + e.b * 128 + row) * g.H + e.c * 256;
-#pragma unroll 1
+                uint32_t r[2][32];
+                tmem_ld_32x32b_x32(taddr, r[0]);
+                tmem_ld_wait_regs(r[0]);
+#pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
+                    if (ch + 1 < 8) tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, r[(ch + 1) & 1]);
                     float v[32];
-                    acc_chunk(taddr + ch * 32, zero, v);
-                    store_bf16x32(dst + ch * 32, v);
-                }
-            } else if (e.kind == KB_DWGU) {
-                // columns 0-127: dW_gate[e] (hidden row x * 128 + row, inter y * 128 ..); 128-255: dW_up
-                const int q = e.a / g.Eq;
-                const int64_t off = (static_cast<int64_t>(e.d) * g.H + e.b * 128 + row) * g.I + e.c * 128;
-#pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
-                    float v[32];
-                    acc_chunk(taddr + ch * 32, zero, v);
-                    store_bf16x32((ch < 4 ? p.dwg[q] : p.dwu[q]) + off + (ch & 3) * 32, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = zero ? 0.f : __uint_as_float(r[ch & 1][j]);
+                    if (e.kind == KB_DWD)
+                        bwd_store_block(stg, sb, lane, v, &p.tmDwd[q], e.c * 256 + ch * 32, e.b * 128 + grp * 32, e.d);
+                    else
+                        bwd_store_block(stg, sb, lane, v, ch < 4 ? &p.tmDwg[q] : &p.tmDwu[q],
+                                        e.c * 128 + (ch & 3) * 32, e.b * 128 + grp * 32, e.d);
+                    if (ch + 1 < 8) tmem_ld_wait_regs(r[(ch + 1) & 1]);
                 }
             } else if (e.kind == KB_RDX) {
                 const int q = e.a, bb = e.b;
@@ -1063,6 +1110,8 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
         }
     }
+    if (lane == 0) bulk_wait<0>();  // this warp's block stores have landed
+    __syncwarp();
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1) moe_bwd_kernel(const __grid_constant__ BwdParams p) {
@@ -1086,7 +1135,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_bwd_kernel(const __grid_co
     } else if (warp == 1) {
         if (lane == 0) bwd_mma_loop(p, sm, tmem_base);
     } else {
-        bwd_epilogue(p, sm, tb, tmem_base, warp, lane, epoch);
+        bwd_epilogue(p, sm, tb, tmem_base, scratch + BWD_TABLE_BYTES + (warp - 2) * 2 * BWD_STAGE_OUT, warp, lane,
+                     epoch);
     }
     engine_teardown(sm, warp, tmem_base);
     __shared__ int s_last;
@@ -1218,6 +1268,14 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         p.dwd[q] = static_cast<__nv_bfloat16 *>(Lc.dwd[q]);
         ok = map3(&p.tmWdT[q], Lc.wd[q], H, I, Eq, BK, 256) && map3(&p.tmWgT[q], Lc.wg[q], I, H, Eq, BK, 256) &&
              map3(&p.tmWuT[q], Lc.wu[q], I, H, Eq, BK, 256) && map2(&p.tmXs[q], Lc.x[q], H, Tq, 64, BK);
+        auto out3 = [&](CUtensorMap *m, void *ptr, uint64_t d0, uint64_t d1) {
+            const uint64_t dims[3] = {d0, d1, Eq};
+            const uint64_t st[2] = {d0 * 2, d0 * d1 * 2};
+            const uint32_t box[3] = {32, 32, 1};
+            return encode_tmap(m, BF, 3, ptr, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+        };
+        ok = ok && out3(&p.tmDwg[q], Lc.dwg[q], I, H) && out3(&p.tmDwu[q], Lc.dwu[q], I, H) &&
+             out3(&p.tmDwd[q], Lc.dwd[q], H, I);
     }
     if (ok) {
         const uint64_t dims[2] = {H, TK};
@@ -1226,7 +1284,7 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         ok = encode_tmap(&p.tmDslot, BF, 2, p.dslot, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (!ok) return KOSMOS_ERR_CUDA;
-    return launch_persistent(reinterpret_cast<const void *>(&moe_bwd_kernel), &p, Lc.grid, MOE_SMEM_BYTES, stream,
+    return launch_persistent(reinterpret_cast<const void *>(&moe_bwd_kernel), &p, Lc.grid, BWD_SMEM_BYTES, stream,
                              Lc.plain_launch != 0);
 }
 

@@ -1,7 +1,7 @@
 """Runs one traced launch of each fused operator on the full-size synthetic
 workloads and writes Chrome traces plus the role time accounting.
 
-    python -m comm_persistent_gemm_gb300.trace_run --out DIR [--only ag,rs,moe,mxfp8,moe_mxfp8]
+    python -m comm_persistent_gemm_gb300.trace_run --out DIR [--only ag,rs,moe,mxfp8,moe_mxfp8,moe_bwd]
 
 Output: DIR/<name>.trace.json (chrome://tracing / Perfetto) and one JSON line
 per traced launch on stdout with the summary of trace.summarize().
@@ -130,6 +130,43 @@ def _trace_moe(K, out, name, o, mx=False):
     return recs[recs["kind"] != 0]
 
 
+def _trace_moe_bwd(K, out, name, o):
+    import torch
+    from kosmos_inputs import WORKLOADS, workload_inputs
+    from .trace import TRACE_DTYPE
+    w = WORKLOADS["moe_fwd_p8"]
+    inp = workload_inputs(w)
+    P, T, H, E, Kt, I = w.P, w.T, w.H, w.E, w.topk, w.I
+    xs = [t.cuda() for t in torch.chunk(inp["x"], P, 0)]
+    wr = inp["w_router"].cuda()
+    sp = lambda t: [t[q * (E // P):(q + 1) * (E // P)].contiguous().cuda() for q in range(P)]
+    wg, wu, wd = sp(inp["w_gate"]), sp(inp["w_up"]), sp(inp["w_down"])
+    ys = [torch.empty(T // P, H, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    idx = torch.empty(T, Kt, dtype=torch.int32, device="cuda")
+    gate = torch.empty(T, Kt, dtype=torch.float32, device="cuda")
+    cnt = torch.empty(E, dtype=torch.int32, device="cuda")
+    pos = torch.empty(T, Kt, dtype=torch.int32, device="cuda")
+    fws = K.moe_workspace(P, T, H, E, Kt, I)
+    K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, cnt, pos, fws, Kt)
+    K.check(fws, "moe_fwd")
+    g = torch.Generator().manual_seed(11)
+    dys = [t.cuda() for t in torch.chunk(torch.randn(T, H, generator=g).to(torch.bfloat16), P, 0)]
+    dxs = [torch.empty(T // P, H, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    dwr = torch.empty(H, E, dtype=torch.float32, device="cuda")
+    dwg, dwu, dwd = [torch.empty_like(t) for t in wg], [torch.empty_like(t) for t in wu], [torch.empty_like(t) for t in wd]
+    bws = K.moe_bwd_workspace(P, T, H, E, Kt, I, o)
+    run = lambda: K.moe_bwd(xs, wr, wg, wu, wd, idx, gate, fws, dys, dxs, dwr, dwg, dwu, dwd, bws, o)
+    for _ in range(2):
+        run()
+    K.check(bws, name)
+    bws.zero_()
+    run()
+    K.check(bws, name)
+    raw = K.moe_bwd_debug_view(K.MOE_BWD_VIEW_TRACE, P, T, H, E, Kt, I, bws).cpu().numpy()
+    recs = raw.view(TRACE_DTYPE)
+    return recs[recs["kind"] != 0]
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", required=True)
@@ -157,6 +194,8 @@ def main(argv=None):
         runs += [("rs_band", _trace_rs, K.opts(trace=1)), ("rs_row", _trace_rs, K.opts(trace=1, order=K.ORDER_ROW))]
     if "moe" in only:
         runs += [("moe_fwd", _trace_moe, K.opts(trace=1))]
+    if "moe_bwd" in only:
+        runs += [("moe_bwd", _trace_moe_bwd, K.opts(trace=1))]
     if "moe_mxfp8" in only:
         runs += [("moe_fwd_mxfp8", lambda *a: _trace_moe(*a, mx=True), K.opts(trace=1))]
     for name, fn, o in runs:
