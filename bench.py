@@ -29,10 +29,10 @@ WORKLOAD = "ag_bf16_p8"
 METRIC = "Fused AG/RS-GEMM TFLOP/s & % BF16 tensor peak on 1 GB300; MoE layer tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one ag_gemm_kernel launch on the 8-rank AG
+# DRAM bytes (read + write) of one ag_gemm_pair_kernel launch on the 8-rank AG
 # workload, from an ncu capture; valid only while the kernel sources hash to
 # src_sha (otherwise the bench reports traffic = null).
-TRAFFIC_CAPTURE = {"bytes": 836141824, "src_sha": "884ccf99a95d520b"}
+TRAFFIC_CAPTURE = {"bytes": 804534784, "src_sha": "b113c72395edb0ec"}
 KERNEL_SOURCES = ["comm_persistent_gemm_gb300/csrc/ag_gemm.cu", "comm_persistent_gemm_gb300/csrc/engine.cuh",
                   "comm_persistent_gemm_gb300/csrc/engine2.cuh", "comm_persistent_gemm_gb300/csrc/ptx.cuh",
                   "comm_persistent_gemm_gb300/csrc/common.cuh"]
