@@ -35,7 +35,7 @@ EXPORTS = ["kosmos_default_opts", "kosmos_num_sms", "kosmos_workspace_bytes", "k
            "kosmos_ag_gemm", "kosmos_gemm_rs", "kosmos_moe_fwd", "kosmos_mxfp8_quantize", "kosmos_status_sync",
            "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device", "kosmos_ag_gemm_noalloc",
            "kosmos_moe_workspace_bytes", "kosmos_moe_debug_view", "kosmos_ag_tile_plan", "kosmos_moe_bwd",
-           "kosmos_moe_bwd_workspace_bytes", "kosmos_moe_bwd_debug_view"]
+           "kosmos_moe_bwd_workspace_bytes", "kosmos_moe_bwd_debug_view", "kosmos_ag_gemm_host"]
 
 
 class KosmosError(RuntimeError):
@@ -112,6 +112,9 @@ def lib():
     L.kosmos_moe_bwd.argtypes = [vp, vp, i32, i64, i64, i32, i32, i64, vp, vp, vp, vp, vp, vp, C.c_size_t, vp, vp, vp,
                                  vp, vp, vp, vp, C.c_size_t, C.POINTER(Opts), vp]
     L.kosmos_moe_bwd.restype = i32
+    L.kosmos_ag_gemm_host.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp, C.c_size_t, C.POINTER(Opts), vp,
+                                      vp, vp]
+    L.kosmos_ag_gemm_host.restype = i32
     L.kosmos_moe_bwd_workspace_bytes.argtypes = [i32, i64, i64, i32, i32, i64, C.POINTER(Opts)]
     L.kosmos_moe_bwd_workspace_bytes.restype = C.c_size_t
     L.kosmos_moe_bwd_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, vp, C.POINTER(vp), C.POINTER(i64)]
@@ -196,6 +199,26 @@ def ag_gemm(x_shards: List, w, x_gathered, y, ws, o: Optional[Opts] = None, dtyp
                               x_gathered.data_ptr(), y.data_ptr(), ws.data_ptr(), ws.numel(),
                               C.byref(o) if o is not None else None, _stream(stream))
     _raise(rc, "kosmos_ag_gemm")
+
+
+def ag_gemm_host(x_host: List, x_dev: List, w, x_gathered, y_dev, y_host, ws, o: Optional[Opts] = None,
+                 stream=None, h2d_stream=None, d2h_stream=None):
+    """ag_gemm from pinned host shards to a pinned host output; the copies run
+    on h2d_stream / d2h_stream and overlap the kernel on `stream`."""
+    _check_cuda(*x_dev, w, x_gathered, y_dev, ws)
+    for t in list(x_host) + [y_host]:
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous pinned CPU tensors")
+    if h2d_stream is None or d2h_stream is None:
+        raise ValueError("ag_gemm_host needs two copy streams")
+    P = len(x_host)
+    m, k = x_host[0].shape
+    n = w.shape[1]
+    rc = lib().kosmos_ag_gemm_host(_ptrs(x_host), _ptrs(x_dev), P, m, k, n, w.data_ptr(), x_gathered.data_ptr(),
+                                   y_dev.data_ptr(), y_host.data_ptr(), ws.data_ptr(), ws.numel(),
+                                   C.byref(o) if o is not None else None, _stream(stream), _stream(h2d_stream),
+                                   _stream(d2h_stream))
+    _raise(rc, "kosmos_ag_gemm_host")
 
 
 def ag_gemm_noalloc(x_shards: List, w, x_gathered, y, o: Optional[Opts] = None, dtype: int = BF16,

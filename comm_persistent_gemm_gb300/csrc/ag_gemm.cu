@@ -40,7 +40,26 @@ struct AgParams {
     uint64_t wait_limit_ns;
     uint64_t inject;
     int64_t link_gbs;  // emulated link for the remote pieces; 0 = uncapped
+    // host-input flow (null otherwise): ext_ready[s] becomes 1 once shard s has
+    // been copied to its device buffer (by a copy stream); ydone[s] counts the
+    // output tiles of shard s written (per CTA of a tile engine)
+    const uint32_t *ext_ready;
+    uint32_t *ydone;
 };
+
+// Host-input flow: waits until shard s is on the device.
+__device__ __forceinline__ bool ag_ext_wait(const AgParams &p, int s, int64_t entry) {
+    return p.ext_ready == nullptr ||
+           wait_flag_eq(p.ws, const_cast<uint32_t *>(&p.ext_ready[s]), 1u, p.wait_limit_ns, entry);
+}
+
+// Host-input flow: one output tile of shard s written by this CTA's epilogue warps.
+__device__ __forceinline__ void ag_ydone(const AgParams &p, int s, int grp, int lane) {
+    if (p.ydone == nullptr) return;
+    __threadfence();
+    named_bar_sync(1, NUM_EPI_THREADS);
+    if (grp == 0 && lane == 0) red_release_add_gpu(&p.ydone[s], 1u);
+}
 
 // Tile-rail entry -> what the engine runs: output columns [col0, col0 + BN)
 // and K blocks [kb0, kb0 + nk); slot >= 0 marks one K half of a split tile.
@@ -75,6 +94,7 @@ __device__ __forceinline__ bool ag_claim_transfer(const AgParams &p, MoveEntry &
     if (t >= static_cast<uint32_t>(p.g.n_transfer)) return false;
     int shard, piece, part;
     ag_decode_transfer(p.g, static_cast<int>(t), shard, piece, part);
+    if (!ag_ext_wait(p, shard, t)) return false;
     int64_t row0, rows;
     ag_part_rows(p.g, piece, part, row0, rows);
     const int64_t row_bytes = p.g.k * 2;
@@ -113,6 +133,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
     PipeState ps;
     RingState rs;
     int nrec = 0;
+    bool local_in = false;  // host-input flow: shard 0 seen on the device
     while (true) {
         if (failed(p.ws)) break;
         if (mover) {
@@ -128,6 +149,10 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
         if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0) {
             if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], ag_piece_ready(p.g, epoch), p.wait_limit_ns, t))
                 break;
+        }
+        if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0 && !local_in) {
+            if (!ag_ext_wait(p, 0, t)) break;
+            local_in = true;
         }
         int slot = -1;
         if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
@@ -215,6 +240,7 @@ __device__ __forceinline__ void ag_epilogue(const AgParams &p, const Smem &sm, u
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tempty[acc]);
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        ag_ydone(p, s, grp, lane);
         if (e.slot >= 0 && lane == 0 && grp == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
         }
@@ -242,6 +268,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_kernel(const __grid_co
         ag_epilogue(p, sm, tmem_base, warp, lane, epoch);
     }
     engine_teardown(sm, warp, tmem_base);
+    if (threadIdx.x == 0 && p.ydone != nullptr && failed(p.ws))  // release the host's output waits
+        for (int s = 0; s < p.g.P; ++s) st_release_gpu(&p.ydone[s], AG_YDONE_RELEASE);
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
 }
 
@@ -300,6 +328,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
     }
     if (leader) {
         const uint32_t my_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
+        bool local_in = false;  // host-input flow: shard 0 seen on the device
         while (true) {
             if (failed(p.ws)) break;
             const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
@@ -312,6 +341,10 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
                 if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch), p.wait_limit_ns,
                                   t))
                     break;
+            }
+            if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0 && !local_in) {
+                if (!ag_ext_wait(p, 0, t)) break;
+                local_in = true;
             }
             int slot = -1;
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
@@ -410,6 +443,7 @@ __device__ __forceinline__ void ag2_epilogue(const AgParams &p, const Smem2 &sm,
         }
         acc_release(sm, acc, leader, lane);
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        ag_ydone(p, s, grp, lane);
         if (leader && e.slot >= 0 && lane == 0 && grp == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
         }
@@ -438,12 +472,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_pair_kernel(const __gr
         ag2_epilogue(p, sm, tmem_base, warp, lane, rank, epoch);
     }
     engine2_teardown(sm, warp, tmem_base);
+    if (threadIdx.x == 0 && p.ydone != nullptr && failed(p.ws))  // release the host's output waits
+        for (int s = 0; s < p.g.P; ++s) st_release_gpu(&p.ydone[s], AG_YDONE_RELEASE);
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
 }
 
 // Unfused baseline, first launch: gather every shard into x_gathered with
 // plain 16-byte vector copies over all SMs.
 __global__ void __launch_bounds__(256) ag_gather_copy_kernel(const AgParams p) {
+    if (p.ext_ready != nullptr) {  // host-input flow: every shard must be on the device
+        if (threadIdx.x == 0)
+            for (int s = 0; s < p.g.P; ++s) ag_ext_wait(p, s, -40);
+        __syncthreads();
+        if (failed(p.ws)) return;
+    }
     const int64_t shard_bytes = p.g.m * p.g.k * 2;
     const int64_t per = shard_bytes / 16;
     const int64_t total = per * p.g.P;
@@ -499,6 +541,10 @@ kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     p.ksync = reinterpret_cast<uint32_t *>(ws + W.ksync_off);
     p.kpart = reinterpret_cast<float4 *>(ws + W.kpart_off);
     p.trace = L.trace ? reinterpret_cast<TraceRec *>(ws + W.trace_off) : nullptr;
+    if (L.host_flow) {
+        p.ext_ready = reinterpret_cast<const uint32_t *>(ws + W.ext_off);
+        p.ydone = reinterpret_cast<uint32_t *>(ws + W.ext_off) + KOSMOS_MAX_P;
+    }
     p.nkb = static_cast<int>(L.k / BK);
     p.sched = L.sched;
     p.n_comm = L.n_comm;

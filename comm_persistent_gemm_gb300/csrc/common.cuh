@@ -214,8 +214,13 @@ KOS_HD void rs_decode_reduce(const RsGeom &g, int t, int &band, int &tcol) {
 constexpr int MAX_SPLIT_SLOTS = 256;
 constexpr size_t KPART_CTA_BYTES = static_cast<size_t>(BM) * BN * 4;
 struct AgWsLayout {
-    size_t flags_off, ksync_off, kpart_off, trace_off, total;
+    size_t flags_off, ksync_off, kpart_off, trace_off, ext_off, total;
 };
+constexpr int AG_EXT_BYTES = 256;  // host-input flow: P shard-arrival words, then P output-done counters
+// Written to the output-done counters when a launch fails or never starts: a
+// stream wait "value >= target" compares (int32_t)(word - target) >= 0, so the
+// release value must stay below 2^31 above any target.
+constexpr uint32_t AG_YDONE_RELEASE = 0x40000000u;
 inline AgWsLayout ag_ws_layout(const AgGeom &g, bool trace, int n_slots = 0) {
     AgWsLayout L;
     L.flags_off = 256;
@@ -226,6 +231,8 @@ inline AgWsLayout ag_ws_layout(const AgGeom &g, bool trace, int n_slots = 0) {
     off += static_cast<size_t>(n_slots) * 2 * KPART_CTA_BYTES;
     L.trace_off = off;
     if (trace) off += static_cast<size_t>(MAX_CTAS) * TRACE_CAP * sizeof(TraceRec);
+    L.ext_off = off;
+    off += AG_EXT_BYTES;
     L.total = off;
     return L;
 }

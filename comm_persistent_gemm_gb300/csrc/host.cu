@@ -30,6 +30,22 @@ static PFN_encodeTiled_t get_encode_fn() {
     return fn;
 }
 
+// Stream memory operations (write / wait on a 32-bit word in device memory).
+typedef CUresult (*PFN_streamValue32_t)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+static PFN_streamValue32_t get_stream_value_fn(bool wait) {
+    static PFN_streamValue32_t fw = nullptr, fr = nullptr;
+    PFN_streamValue32_t &fn = wait ? fr : fw;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion(wait ? "cuStreamWaitValue32" : "cuStreamWriteValue32", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_streamValue32_t>(p);
+    }
+    return fn;
+}
+
 bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, void *base, const uint64_t *dims,
                  const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle) {
     PFN_encodeTiled_t fn = get_encode_fn();
@@ -341,6 +357,77 @@ kosmos_status kosmos_ag_gemm(const void *const *x_shards, const void *const *x_s
     L.link_gbs = o.link_gbs;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == KOSMOS_BF16 ? launch_ag_bf16(L, s) : launch_ag_mxfp8(L, s);
+}
+
+kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev, int P, int64_t m_per_shard,
+                                  int64_t k, int64_t n, const void *w, void *x_gathered, void *y_dev, void *y_host,
+                                  void *ws, size_t ws_bytes, const kosmos_opts *opts, void *stream, void *h2d_stream,
+                                  void *d2h_stream) {
+    if (P < 1 || P > KOSMOS_MAX_P || x_host == nullptr || x_dev == nullptr || y_host == nullptr) return KOSMOS_ERR_INVALID_ARG;
+    if (m_per_shard < 1 || k < BK || k % BK != 0 || n < 8 || n % 8 != 0) return KOSMOS_ERR_INVALID_ARG;
+    if (m_per_shard > (1ll << 30) || k > (1ll << 24) || n > (1ll << 24)) return KOSMOS_ERR_INVALID_ARG;
+    if (h2d_stream == nullptr || d2h_stream == nullptr || h2d_stream == stream || d2h_stream == stream)
+        return KOSMOS_ERR_INVALID_ARG;
+    for (int r = 0; r < P; ++r)
+        if (x_host[r] == nullptr || !aligned16(x_dev[r])) return KOSMOS_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(x_gathered) || !aligned16(y_dev)) return KOSMOS_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
+    kosmos_opts o = resolve_opts(opts);
+    o.tail_split = 0;  // every tile writes its output once: the per-shard output counts stay exact
+    if (o.sched < KOSMOS_SCHED_SELF || o.sched > KOSMOS_SCHED_UNFUSED) return KOSMOS_ERR_INVALID_ARG;
+    if (!link_ok(o, static_cast<uint64_t>(P - 1) * static_cast<uint64_t>(m_per_shard) * static_cast<uint64_t>(k) * 2u))
+        return KOSMOS_ERR_INVALID_ARG;
+    if (ws_bytes < kosmos_workspace_bytes(KOSMOS_OP_AG_GEMM, P, m_per_shard, n, k, KOSMOS_BF16, &o))
+        return KOSMOS_ERR_WORKSPACE;
+    PFN_streamValue32_t wr = get_stream_value_fn(false), wt = get_stream_value_fn(true);
+    if (wr == nullptr || wt == nullptr) return KOSMOS_ERR_CUDA;
+    AgPlan pl;
+    const kosmos_status ps = ag_plan(P, m_per_shard, k, n, KOSMOS_BF16, o, pl);
+    if (ps != KOSMOS_OK) return ps;
+    AgLaunch L;
+    memset(&L, 0, sizeof(L));
+    L.P = P; L.m = m_per_shard; L.k = k; L.n = n;
+    for (int r = 0; r < P; ++r) L.x[r] = x_dev[r];
+    L.w = w; L.x_gathered = x_gathered; L.y = y_dev; L.ws = ws;
+    L.dtype = KOSMOS_BF16; L.sched = o.sched; L.n_comm = pl.n_comm; L.pair = pl.pair; L.n_split = 0; L.n_slots = 0;
+    L.trace = o.trace; L.grid = pl.grid; L.wait_limit_ns = o.wait_limit_ns; L.inject = o.inject;
+    L.plain_launch = o.plain_launch; L.link_gbs = o.link_gbs; L.host_flow = 1;
+    const AgWsLayout W = ag_ws_layout(ag_geom(P, m_per_shard, k, n), o.trace != 0, 0);
+    uint8_t *ext = static_cast<uint8_t *>(ws) + W.ext_off;
+    const CUdeviceptr ready = reinterpret_cast<CUdeviceptr>(ext);
+    const CUdeviceptr done = ready + 4 * KOSMOS_MAX_P;
+    // output tiles of one shard, counted per CTA of a tile engine
+    const uint32_t target = static_cast<uint32_t>(cdiv(m_per_shard, pl.pair ? PBM : BM) * cdiv(n, BN) *
+                                                  (pl.pair ? 2 : 1));
+    cudaStream_t s = static_cast<cudaStream_t>(stream), h = static_cast<cudaStream_t>(h2d_stream),
+                 d = static_cast<cudaStream_t>(d2h_stream);
+    cudaEvent_t ev[4];
+    for (int i = 0; i < 4; ++i)
+        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return KOSMOS_ERR_CUDA;
+    bool ok = cudaEventRecord(ev[0], s) == cudaSuccess && cudaStreamWaitEvent(h, ev[0], 0) == cudaSuccess &&
+              cudaMemsetAsync(ext, 0, 8 * KOSMOS_MAX_P, h) == cudaSuccess && cudaEventRecord(ev[1], h) == cudaSuccess &&
+              cudaStreamWaitEvent(s, ev[1], 0) == cudaSuccess && cudaStreamWaitEvent(d, ev[1], 0) == cudaSuccess;
+    // shard r to the device, then its arrival word (the local shard first)
+    const size_t xb = static_cast<size_t>(m_per_shard * k * 2), yb = static_cast<size_t>(m_per_shard * n * 2);
+    for (int r = 0; ok && r < P; ++r)
+        ok = cudaMemcpyAsync(x_dev[r], x_host[r], xb, cudaMemcpyHostToDevice, h) == cudaSuccess &&
+             wr(reinterpret_cast<CUstream>(h), ready + 4 * r, 1u, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+    kosmos_status st = ok ? launch_ag_bf16(L, s) : KOSMOS_ERR_CUDA;
+    if (st != KOSMOS_OK) {
+        // no kernel: release the output waits below so that no stream blocks
+        for (int r = 0; r < P; ++r)
+            wr(reinterpret_cast<CUstream>(h), done + 4 * r, AG_YDONE_RELEASE, CU_STREAM_WRITE_VALUE_DEFAULT);
+    }
+    // shard r's output rows back to the host once all its tiles are written
+    for (int r = 0; ok && r < P; ++r)
+        ok = wt(reinterpret_cast<CUstream>(d), done + 4 * r, target, CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS &&
+             cudaMemcpyAsync(static_cast<uint8_t *>(y_host) + r * yb, static_cast<uint8_t *>(y_dev) + r * yb, yb,
+                             cudaMemcpyDeviceToHost, d) == cudaSuccess;
+    ok = ok && cudaEventRecord(ev[2], h) == cudaSuccess && cudaEventRecord(ev[3], d) == cudaSuccess &&
+         cudaStreamWaitEvent(s, ev[2], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev[3], 0) == cudaSuccess;
+    for (int i = 0; i < 4; ++i) cudaEventDestroy(ev[i]);
+    if (st != KOSMOS_OK) return st;
+    return ok ? KOSMOS_OK : KOSMOS_ERR_CUDA;
 }
 
 int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t k, int64_t n, int dtype, const kosmos_opts *opts,

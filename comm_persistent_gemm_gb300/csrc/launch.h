@@ -32,6 +32,7 @@ struct AgLaunch {
     uint64_t wait_limit_ns;
     uint64_t inject;
     int64_t link_gbs;
+    int host_flow;    // bf16: shards arrive through copy streams (arrival and output-done words in the workspace)
 };
 
 struct RsLaunch {
