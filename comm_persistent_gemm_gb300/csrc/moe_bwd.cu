@@ -152,6 +152,7 @@ struct BwdParams {
     CUtensorMap tmDwu[KOSMOS_MAX_P];
     CUtensorMap tmDwd[KOSMOS_MAX_P]; // dims {H, I, Eq}
     // forward context
+    const WsHeader *fwd_hdr;
     const int32_t *counts, *offl, *unit_start, *base, *rank_in_blk, *inv_pos;
     const float *logits;
     const __nv_bfloat16 *yslot, *gsave, *usave;
@@ -1127,6 +1128,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_bwd_kernel(const __grid_co
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
+    if (threadIdx.x == 0) {
+        // the forward's context must come from a complete bf16 forward call
+        const volatile WsHeader *fh = p.fwd_hdr;
+        if (fh->status != KOSMOS_OK || fh->aux[2] != MOE_BF16_CTX) set_error(p.ws, KOSMOS_ERR_INVALID_ARG, -50);
+    }
     if (warp == 0) bwd_load_tables(p, tb, lane);  // before the setup barrier: every warp reads them after it
     engine_setup(sm, warp);
     const uint32_t tmem_base = *sm.tmem_slot;
@@ -1200,6 +1206,7 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
     const MoeWsLayout F = moe_ws_layout(g, false);
     const uint8_t *fw = static_cast<const uint8_t *>(Lc.fwd_ws);
     uint8_t *ws = static_cast<uint8_t *>(Lc.ws);
+    p.fwd_hdr = reinterpret_cast<const WsHeader *>(fw);
     p.counts = reinterpret_cast<const int32_t *>(fw + F.counts);
     p.offl = reinterpret_cast<const int32_t *>(fw + F.offsets);
     p.unit_start = reinterpret_cast<const int32_t *>(fw + F.unit_start);

@@ -15,6 +15,9 @@ constexpr int MOE_SF_BYTES = 3 * 512;       // MXFP8: per stage, SFA atom + two 
 constexpr int MOE_SMEM_BYTES = SMEM_BYTES + MOE_SCRATCH + NSTAGE * MOE_SF_BYTES;
 static_assert(MOE_SMEM_BYTES <= 232448, "MoE kernel exceeds 227 KB of shared memory per CTA");
 constexpr int MOE_QR = 16;                  // MXFP8: token rows per QUANT entry
+// aux[2] of a forward workspace after a complete bf16 forward: its saved
+// context (g, u, h, slots, logits, tables) is what the backward reads
+constexpr uint32_t MOE_BF16_CTX = 0x4B4D4642u;
 constexpr int K_QUANT = 11;                 // rail kind of a QUANT entry
 
 struct MoeGeom {

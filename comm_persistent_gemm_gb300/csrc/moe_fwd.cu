@@ -1137,6 +1137,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_fwd_kernel(const __grid_co
         if (threadIdx.x == 0) {
             volatile uint32_t *t = p.ws->tickets;
             for (int i = 0; i < KOSMOS_MAX_P; ++i) t[i] = 0u;
+            *reinterpret_cast<volatile uint32_t *>(&p.ws->aux[2]) = p.g.mx ? 0u : MOE_BF16_CTX;
             *reinterpret_cast<volatile uint32_t *>(&p.ws->done_ctas) = 0u;
             __threadfence();
             *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch) = epoch + 1u;

@@ -147,3 +147,41 @@ def test_moe_rejects_link_cap(K):
     with pytest.raises(K.KosmosError):
         K.moe_fwd(xs, inp["w_router"].to(dev), sp(inp["w_gate"]), sp(inp["w_up"]), sp(inp["w_down"]), ys, z,
                   z.float(), z[:, 0].clone(), z, ws, topk, o)
+
+
+@pytest.mark.parametrize("pair", [1, 0])
+def test_ag_mxfp8_link_cap(K, orc, pair):
+    """MXFP8 all-gather + GEMM through the emulated link: same bytes as
+    without it, and at least the link time of the remote pieces and their
+    scale blocks."""
+    P, m, k, n = 4, 256, 512, 512
+    inp = ag_inputs(P, m, k, n, seed=33, var_w=1.0 / k)
+
+    def quant(x, along):
+        r, c = x.shape
+        q = torch.empty(r, c, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(K.mxfp8_scale_bytes(r, c, along), dtype=torch.uint8, device="cuda")
+        K.mxfp8_quantize(x.cuda(), q, sc, along)
+        return q, sc
+
+    qs, ss = zip(*[quant(x, True) for x in inp["x"]])
+    qw, sw = quant(inp["w"], False)
+    xg = torch.zeros(P * m, k, dtype=torch.uint8, device="cuda")
+
+    def run(o):
+        y = torch.full((P * m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ws = K.workspace(K.OP_AG_GEMM, P, m, n, k, dtype=K.MXFP8_E4M3, o=o)
+        f = lambda: K.ag_gemm(list(qs), qw, xg, y, ws, o, dtype=K.MXFP8_E4M3, x_scales=list(ss), w_scales=sw)
+        f()
+        K.check(ws, "ag mxfp8")
+        us = _timed(f)
+        K.check(ws, "ag mxfp8")
+        return y, us
+
+    y0, _ = run(K.opts(cta_pair=pair))
+    gbs = 10
+    y1, us = run(K.opts(cta_pair=pair, link_gbs=gbs))
+    assert torch.equal(y0, y1)
+    assert not torch.isnan(y1).any()
+    link_us = (P - 1) * m * k / gbs / 1e3
+    assert us >= 0.97 * link_us, (us, link_us)

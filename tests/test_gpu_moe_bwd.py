@@ -180,3 +180,43 @@ def test_moe_bwd_full_size_sampled(K, orc):
     for key, r in (("dwg", rg), ("dwu", ru), ("dwd", rd)):
         gk = bf16_tensor_to_f64(outs[0][key][sel])
         assert rel_err(gk, r) <= TOL, (key, rel_err(gk, r))
+
+
+def test_moe_bwd_refuses_a_context_that_is_not_a_complete_bf16_forward(K):
+    """A forward workspace that no bf16 forward has completed on (a fresh one,
+    or one an MXFP8 forward used): the backward reports INVALID_ARG."""
+    P, T, H, E, topk, I = 2, 256, 256, 64, 2, 256
+    inp = moe_inputs(T, H, E, I, seed=5)
+    dev = "cuda"
+    xs = [t.to(dev) for t in torch.chunk(inp["x"], P, 0)]
+    wr = inp["w_router"].to(dev)
+    wg = [t.to(dev) for t in _split(inp["w_gate"], P)]
+    wu = [t.to(dev) for t in _split(inp["w_up"], P)]
+    wd = [t.to(dev) for t in _split(inp["w_down"], P)]
+    idx = torch.zeros(T, topk, dtype=torch.int32, device=dev)
+    gate = torch.zeros(T, topk, dtype=torch.float32, device=dev)
+    dys = [torch.zeros(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    dxs = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    dwr = torch.empty(H, E, dtype=torch.float32, device=dev)
+    dwg, dwu, dwd = [torch.empty_like(w) for w in wg], [torch.empty_like(w) for w in wu], [torch.empty_like(w) for w in wd]
+    fresh = K.moe_workspace(P, T, H, E, topk, I)
+    bws = K.moe_bwd_workspace(P, T, H, E, topk, I)
+    K.moe_bwd(xs, wr, wg, wu, wd, idx, gate, fresh, dys, dxs, dwr, dwg, dwu, dwd, bws)
+    st, _ = K.status_sync(bws)
+    assert st == K.ERR_INVALID_ARG
+    # an MXFP8 forward's workspace (sized for bf16 so that the size check passes)
+    K.workspace_init(bws)
+    from test_gpu_moe_mxfp8 import gpu_quant_experts
+    (qg, sg), (qu, su), (qd, sd) = (gpu_quant_experts(K, inp[n], P) for n in ("w_gate", "w_up", "w_down"))
+    fws = K.moe_workspace(P, T, H, E, topk, I, dtype=K.MXFP8_E4M3)
+    if fws.numel() < fresh.numel():
+        fws = torch.cat([fws, torch.zeros(fresh.numel() - fws.numel(), dtype=torch.uint8, device=dev)])
+    ys = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    cnt = torch.empty(E, dtype=torch.int32, device=dev)
+    pos = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    K.moe_fwd(xs, wr, qg, qu, qd, ys, idx, gate, cnt, pos, fws, topk, dtype=K.MXFP8_E4M3, w_gate_scales=sg,
+              w_up_scales=su, w_down_scales=sd)
+    K.check(fws, "moe_fwd mxfp8")
+    K.moe_bwd(xs, wr, wg, wu, wd, idx, gate, fws, dys, dxs, dwr, dwg, dwu, dwd, bws)
+    st, _ = K.status_sync(bws)
+    assert st == K.ERR_INVALID_ARG
