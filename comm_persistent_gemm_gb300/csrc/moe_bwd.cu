@@ -46,6 +46,7 @@ __device__ __forceinline__ bool bwd_is_mma(int k) {
     return k == KB_RDX || k == KB_DH || k == KB_DGU || k == KB_DWD || k == KB_DWGU || k == KB_DWR;
 }
 constexpr int BWD_LAG = 2;
+constexpr int BWD_CLAIM = 4;  // expert-tile tickets per claim
 // shared memory: the engine's stages and control, the per-CTA tables, and
 // per epilogue warp two 2 KB staging buffers for the weight-gradient stores
 constexpr int BWD_TABLE_BYTES = 5120;
@@ -269,7 +270,10 @@ struct BwdProdState {
     int nrec = 0;
     bool main_done = false;
     uint64_t idle_t0 = 0;
-    int64_t ahead = -1;
+    // tickets of the expert-tile region are claimed BWD_CLAIM at a time (one
+    // atomic round trip per group: the weight-gradient tiles are short)
+    uint32_t bnext = 0, bend = 0;
+    bool in_tiles = false;
     int hint = 0;      // tile-rail group of the previous tile
     uint32_t polls = 0;  // decide calls: the push queue is polled on every fourth while the rail lasts
     int ready_dwd = -1, ready_dwgu = -1;  // the expert whose inputs were last confirmed complete
@@ -334,8 +338,16 @@ __device__ __noinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdP
     }
     // 2) the next entry of this rank's rail
     if (!st.main_done) {
-        const uint32_t t = st.ahead >= 0 ? static_cast<uint32_t>(st.ahead) : atomicAdd(&p.ws->tickets[q], 1u);
-        st.ahead = -1;
+        uint32_t t;
+        if (st.bnext < st.bend) {
+            t = st.bnext++;
+        } else {
+            const uint32_t grp = st.in_tiles ? static_cast<uint32_t>(BWD_CLAIM) : 1u;
+            t = atomicAdd(&p.ws->tickets[q], grp);
+            st.bnext = t + 1;
+            st.bend = t + grp;
+        }
+        if (t >= static_cast<uint32_t>(b.n_head)) st.in_tiles = true;
         const int nh = b.n_head;
         const int RB = g.RB, K = g.K;
         if (t == 0) {  // ZPAD
@@ -422,7 +434,6 @@ __device__ __noinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdP
                 set_error(p.ws, KOSMOS_ERR_DEVICE, -30);
                 return false;
             }
-            const uint32_t nxt = atomicAdd(&p.ws->tickets[q], 1u);
             const int e = q * g.Eq + le;
             const int c = tb.cnt[le];
             const int c16 = (c + 15) / 16 * 16;
@@ -513,7 +524,7 @@ __device__ __noinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdP
                     st.ps.advance();
                 }
             }
-            st.ahead = nxt;
+
             st.idle_t0 = 0;
             return true;
         }
