@@ -47,6 +47,12 @@ __device__ __forceinline__ bool bwd_is_mma(int k) {
 }
 constexpr int BWD_LAG = 2;
 constexpr int BWD_CLAIM = 4;  // expert-tile tickets per claim
+// A DH tile's SwiGLU inputs g and u reach its epilogue through three more
+// pipeline stages after its K loop: per 32-column chunk of the tile, the
+// 128 rows of g then of u (8 KB each, 64-byte swizzled), three chunks to a
+// stage (3 + 3 + 2 of the tile's 8).
+constexpr int DH_EPI_STAGES = 3;
+constexpr int DH_CH_BYTES = 2 * BM * 32 * 2;
 // shared memory: the engine's stages and control, the per-CTA tables, and
 // per epilogue warp two 2 KB staging buffers for the weight-gradient stores
 constexpr int BWD_TABLE_BYTES = 5120;
@@ -139,6 +145,7 @@ struct BwdParams {
     CUtensorMap tmDgA, tmDuA;        // dg, du [rows16, I]: A of DGU, box {64, 128}
     CUtensorMap tmDgB, tmDuB;        // dg, du as B of DWGU: box {64, 64}
     CUtensorMap tmH;                 // forward h [T*K, I]: MN-major A of DWD, box {64, 64}
+    CUtensorMap tmGs, tmUs;          // forward g, u [T*K, I]: DH epilogue chunks, box {32, 128}, 64-byte swizzle
     CUtensorMap tmX;                 // forward receive rows [T*K, H]: MN-major A of DWGU, box {64, 64}
     CUtensorMap tmDlA;               // dl [T, E]: A of RDX, box {64, 128}
     CUtensorMap tmDlB;               // dl as B of DWR: box {64, 64}
@@ -276,6 +283,7 @@ struct BwdProdState {
     bool in_tiles = false;
     int hint = 0;      // tile-rail group of the previous tile
     uint32_t polls = 0;  // decide calls: the push queue is polled on every fourth while the rail lasts
+    uint32_t calls = 0;
     int ready_dwd = -1, ready_dwgu = -1;  // the expert whose inputs were last confirmed complete
 };
 
@@ -306,14 +314,18 @@ __device__ __forceinline__ bool bwd_wait_stage(const BwdParams &p, const Smem &s
 }
 
 // Lane 0 of the producer warp: one piece of work per call.  Returns false
-// when this CTA is finished.
-__device__ __noinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdProdState &st, const BwdTables &tb,
+// when this CTA is finished.  Inlined into the producer loop so that its
+// state stays in registers: as a called function the state lived in local
+// memory, and the short weight-gradient tiles waited on those round trips.
+__device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdProdState &st, const BwdTables &tb,
                                         uint32_t epoch) {
     const BwdGeom &b = p.b;
     const MoeGeom &g = b.f;
     const int q = blockIdx.x % g.P;
     uint32_t *qc = p.qctl + 4 * q;
-    if (failed(p.ws)) return false;
+    // the status word is a round trip to L2: read on every eighth call (the
+    // waits below read it as well)
+    if ((st.calls++ & 7u) == 0 && failed(p.ws)) return false;
     // 1) a ready PUSH (polled on every fourth call while rail entries remain:
     //    each poll is a round trip to L2, and the short weight-gradient
     //    tiles would otherwise wait on it)
@@ -472,6 +484,19 @@ __device__ __noinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, BwdP
                         const int kk = kb < half ? kb : kb - half;
                         tma_load_2d(sa, kb < half ? &p.tmDgA : &p.tmDuA, bar, kk * BK, en.x0);
                         tma_load_3d(sb, kb < half ? &p.tmWgT[q] : &p.tmWuT[q], bar, kk * BK, col * 256, le);
+                    }
+                    st.ps.advance();
+                }
+                for (int s = 0; kind == KB_DH && s < DH_EPI_STAGES; ++s) {  // the epilogue's g / u chunks
+                    if (!bwd_wait_stage(p, sm, st.ps, t)) return false;
+                    uint8_t *sa = sm.stages + st.ps.stage * STAGE_BYTES;
+                    uint64_t *bar = &sm.full[st.ps.stage];
+                    const int c0 = s * 3, nch = 8 - c0 < 3 ? 8 - c0 : 3;
+                    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nch * DH_CH_BYTES));
+                    for (int j = 0; j < nch; ++j) {
+                        const int32_t xc = col * 256 + (c0 + j) * 32;
+                        tma_load_2d(sa + j * DH_CH_BYTES, &p.tmGs, bar, xc, en.x2);
+                        tma_load_2d(sa + j * DH_CH_BYTES + DH_CH_BYTES / 2, &p.tmUs, bar, xc, en.x2);
                     }
                     st.ps.advance();
                 }
@@ -637,6 +662,7 @@ __device__ __forceinline__ void bwd_mma_loop(const BwdParams &p, const Smem &sm,
             ps.advance();
         }
         if (!ok) break;
+        if (e.kind == KB_DH) ps.advance(DH_EPI_STAGES);  // consumed by the epilogue
         if (e.nstage == 0) {
             mbar_arrive(&sm.tfull[acc]);  // nothing to multiply: the epilogue writes zeros
         } else {
@@ -940,20 +966,26 @@ __device__ __noinline__ bool bwd_fold(const BwdParams &p, const Smem &sm, PipeSt
     return true;
 }
 
-__device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + expf(-a)); }
+// fp32 sigmoid through the fast exponential and the approximate division (a
+// few ulp; the results are rounded to bf16)
+__device__ __forceinline__ float sigmoid_f(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
 
 // One 32 x 32 block of this warp's rows (a weight-gradient tile) stored
 // through the warp's staging buffers: the lanes write their rows' 64 bytes,
 // lane 0 issues the tiled bulk store; a buffer is rewritten once the store
-// issued two blocks earlier has read it.
+// issued two blocks earlier has read it.  The buffers hold the 64-byte
+// swizzled layout of the store's tensor map (16-byte piece c of row r at
+// c ^ ((r >> 1) & 3)), so that the 32 lanes' row writes spread over all
+// banks instead of queueing on eight.
 __device__ __forceinline__ void bwd_store_block(uint8_t *stg, int &sb, int lane, const float (&v)[32],
                                                 const CUtensorMap *m, int32_t c0, int32_t c1, int32_t c2) {
     if (lane == 0) bulk_wait_read<1>();
     __syncwarp();
     uint4 *row = reinterpret_cast<uint4 *>(stg + sb * BWD_STAGE_OUT + lane * 64);
+    const int sw = (lane >> 1) & 3;
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4)
-        row[q4] = make_uint4(pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]), pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
+        row[q4 ^ sw] = make_uint4(pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]), pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
                              pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]), pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
     fence_proxy_async_smem();
     __syncwarp();
@@ -988,6 +1020,13 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
         if (e.kind == K_DONE) break;
         if (bwd_is_mma(e.kind)) {
             ps.advance(e.nstage);
+            if (e.kind == KB_DH && row < (e.x1 & 0xFFFF)) {
+                // the SwiGLU inputs of this thread's row come from HBM: start
+                // them towards L2 while the tile's K loop (the whole of H) runs
+                const int64_t off = (static_cast<int64_t>(e.x2) + row) * g.I + static_cast<int64_t>(e.c) * 256;
+                bulk_prefetch_l2(p.gsave + off, 512);
+                bulk_prefetch_l2(p.usave + off, 512);
+            }
             if (!mbar_wait(&sm.tfull[acc], acc_phase, PIPE_LIMIT_NS)) {
                 set_error(p.ws, KOSMOS_ERR_DEVICE, -7);
                 break;
@@ -999,39 +1038,63 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
                 const int real = e.x1 & 0xFFFF, r16 = e.x1 >> 16;
                 const bool is_real = row < real, in16 = row < r16;
                 const int64_t prow = static_cast<int64_t>(e.x0) + row;
-                const int64_t frow = static_cast<int64_t>(e.x2) + (is_real ? row : 0);
+                const int sw = (row >> 1) & 3;  // 64-byte swizzle of this row's 16-byte pieces
+                bool ok = true;
 #pragma unroll 1
                 for (int ch = 0; ch < 8; ++ch) {
+                    const int j = ch % 3;
+                    if (j == 0 && !mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+                        set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *cs = sm.stages + ps.stage * STAGE_BYTES + j * DH_CH_BYTES + row * 64;
                     float dh[32];
                     acc_chunk(taddr + ch * 32, false, dh);
-                    const int64_t col = static_cast<int64_t>(e.c) * 256 + ch * 32;
-                    float dgv[32], duv[32];
+                    uint32_t dgp[16], dup[16];  // bf16 pairs of dg, du
                     if (is_real) {
-                        const uint4 *gs = reinterpret_cast<const uint4 *>(p.gsave + frow * g.I + col);
-                        const uint4 *us = reinterpret_cast<const uint4 *>(p.usave + frow * g.I + col);
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
-                            const uint4 gv = ldcg_u4(gs + q4), uv = ldcg_u4(us + q4);
+                            const uint4 gv = *reinterpret_cast<const uint4 *>(cs + (q4 ^ sw) * 16);
+                            const uint4 uv = *reinterpret_cast<const uint4 *>(cs + DH_CH_BYTES / 2 + (q4 ^ sw) * 16);
                             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const float gg = (j & 1) ? bf_hi(gw[j >> 1]) : bf_lo(gw[j >> 1]);
-                                const float uu = (j & 1) ? bf_hi(uw[j >> 1]) : bf_lo(uw[j >> 1]);
-                                const float sg = sigmoid_f(gg);
-                                const float d = dh[q4 * 8 + j];
-                                dgv[q4 * 8 + j] = d * uu * (sg * (1.0f + gg * (1.0f - sg)));
-                                duv[q4 * 8 + j] = d * (gg * sg);
+                            for (int w = 0; w < 4; ++w) {
+                                float dgo[2], duo[2];
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const float gg = h ? bf_hi(gw[w]) : bf_lo(gw[w]);
+                                    const float uu = h ? bf_hi(uw[w]) : bf_lo(uw[w]);
+                                    const float sg = sigmoid_f(gg);
+                                    const float d = dh[q4 * 8 + 2 * w + h];
+                                    dgo[h] = d * uu * (sg * (1.0f + gg * (1.0f - sg)));
+                                    duo[h] = d * (gg * sg);
+                                }
+                                dgp[q4 * 4 + w] = pack_bf16x2(dgo[0], dgo[1]);
+                                dup[q4 * 4 + w] = pack_bf16x2(duo[0], duo[1]);
                             }
                         }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) { dgv[j] = 0.f; duv[j] = 0.f; }
+                        for (int w = 0; w < 16; ++w) { dgp[w] = 0u; dup[w] = 0u; }
+                    }
+                    if (j == 2 || ch == 7) {  // every epilogue warp has read its rows of the stage
+                        named_bar_sync(1, NUM_EPI_THREADS);
+                        if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
+                        ps.advance();
                     }
                     if (in16) {
-                        store_bf16x32(p.dg + prow * g.I + col, dgv);
-                        store_bf16x32(p.du + prow * g.I + col, duv);
+                        const int64_t col = static_cast<int64_t>(e.c) * 256 + ch * 32;
+                        uint4 *dgd = reinterpret_cast<uint4 *>(p.dg + prow * g.I + col);
+                        uint4 *dud = reinterpret_cast<uint4 *>(p.du + prow * g.I + col);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            dgd[q4] = make_uint4(dgp[q4 * 4], dgp[q4 * 4 + 1], dgp[q4 * 4 + 2], dgp[q4 * 4 + 3]);
+                            dud[q4] = make_uint4(dup[q4 * 4], dup[q4 * 4 + 1], dup[q4 * 4 + 2], dup[q4 * 4 + 3]);
+                        }
                     }
                 }
+                if (!ok) break;
             } else if (e.kind == KB_DGU) {
                 const int real = e.x1 & 0xFFFF;
                 const int64_t prow = static_cast<int64_t>(e.x0) + row;
@@ -1266,6 +1329,12 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         const uint32_t box[2] = {b0, b1};
         return encode_tmap(m, BF, 2, const_cast<void *>(ptr), dims, st, box, SW);
     };
+    auto mapgu = [&](CUtensorMap *m, const void *ptr) {
+        const uint64_t dims[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(TK)};
+        const uint64_t st[1] = {static_cast<uint64_t>(I) * 2};
+        const uint32_t box[2] = {32, BM};
+        return encode_tmap(m, BF, 2, const_cast<void *>(ptr), dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    };
     auto map3 = [&](CUtensorMap *m, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
         const uint64_t dims[3] = {d0, d1, d2};
         const uint64_t st[2] = {d0 * 2, d0 * d1 * 2};
@@ -1276,6 +1345,7 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
               map2(&p.tmDgA, p.dg, I, R16, BK, BM) && map2(&p.tmDuA, p.du, I, R16, BK, BM) &&
               map2(&p.tmDgB, p.dg, I, R16, 64, BK) && map2(&p.tmDuB, p.du, I, R16, 64, BK) &&
               map2(&p.tmH, fw + F.h, I, TK, 64, BK) && map2(&p.tmX, fw + F.recv, H, TK, 64, BK) &&
+              mapgu(&p.tmGs, fw + F.gsave) && mapgu(&p.tmUs, fw + F.usave) &&
               map2(&p.tmDlA, p.dl, E, T, BK, BM) && map2(&p.tmDlB, p.dl, E, T, 64, BK) &&
               map2(&p.tmWrT, Lc.wr, E, H, BK, 256);
     for (int q = 0; ok && q < g.P; ++q) {
@@ -1290,7 +1360,7 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
             const uint64_t dims[3] = {d0, d1, Eq};
             const uint64_t st[2] = {d0 * 2, d0 * d1 * 2};
             const uint32_t box[3] = {32, 32, 1};
-            return encode_tmap(m, BF, 3, ptr, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+            return encode_tmap(m, BF, 3, ptr, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
         };
         ok = ok && out3(&p.tmDwg[q], Lc.dwg[q], I, H) && out3(&p.tmDwu[q], Lc.dwu[q], I, H) &&
              out3(&p.tmDwd[q], Lc.dwd[q], H, I);
