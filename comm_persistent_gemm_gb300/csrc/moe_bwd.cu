@@ -46,7 +46,7 @@ __device__ __forceinline__ bool bwd_is_mma(int k) {
     return k == KB_RDX || k == KB_DH || k == KB_DGU || k == KB_DWD || k == KB_DWGU || k == KB_DWR;
 }
 constexpr int BWD_LAG = 2;
-constexpr int BWD_CLAIM = 4;  // expert-tile tickets per claim
+constexpr int BWD_GROUP = 4;  // weight-gradient tiles per rail ticket (at most)
 // A DH tile's SwiGLU inputs g and u reach its epilogue through three more
 // pipeline stages after its K loop: per 32-column chunk of the tile, the
 // 128 rows of g then of u (8 KB each, 64-byte swizzled), three chunks to a
@@ -68,6 +68,8 @@ struct BwdGeom {
     int NWH;        // H / 128
     int W1;         // DWD tiles per expert: NWI * NHC
     int W2;         // DWGU tiles per expert: NWH * NWI
+    int G1, G2;     // DWD / DWGU tiles per rail ticket (4, 2 or 1: divides W1 / W2)
+    int T1, T2;     // DWD / DWGU tickets per expert: W1 / G1, W2 / G2
     int64_t rows16; // rows of the 16-row-padded expert-ordered buffers
     int push_cap, fold_cap;
     int n_head;     // 1 + RB*K + RB + RB*NHC
@@ -84,6 +86,10 @@ inline BwdGeom bwd_geom(int P, int64_t T, int64_t H, int E, int K, int64_t I) {
     b.NWH = static_cast<int>(H / 128);
     b.W1 = b.NWI * b.NHC;
     b.W2 = b.NWH * b.NWI;
+    b.G1 = b.W1 % BWD_GROUP == 0 ? BWD_GROUP : (b.W1 % 2 == 0 ? 2 : 1);
+    b.G2 = b.W2 % BWD_GROUP == 0 ? BWD_GROUP : (b.W2 % 2 == 0 ? 2 : 1);
+    b.T1 = b.W1 / b.G1;
+    b.T2 = b.W2 / b.G2;
     b.rows16 = align_up(T * K + static_cast<int64_t>(E) * 16, BM) + BM;
     b.push_cap = static_cast<int>((b.f.Eq + cdiv(T * K, BM)) * b.NHC);
     b.fold_cap = b.f.RB * b.NHC;
@@ -224,16 +230,23 @@ __device__ __forceinline__ void bwd_load_tables(const BwdParams &p, const BwdTab
 }
 
 // Expert-tile rail of rank q (tt = ticket - n_head).  Group j holds
-//   DH(j): NIC x u_j (column block outer, row block inner), DWD(j): W1
-//   (j < Eq), DGU(j-1): NHC x u_{j-1}, DWGU(j-2): W2 (0 <= j-2 < Eq)
-// with u_j the row blocks of expert j and U(j) their prefix.
+//   DH(j): NIC x u_j (column block outer, row block inner), DWD(j): T1
+//   (j < Eq), DGU(j-1): NHC x u_{j-1}, DWGU(j-2): T2 (0 <= j-2 < Eq)
+// with u_j the row blocks of expert j and U(j) their prefix.  A DH or DGU
+// ticket is one tile; a DWD / DWGU ticket is G1 / G2 consecutive tiles
+// (cnt), taken by one CTA: these tiles are short, and one atomic claim per
+// group saves round trips.  The long data-gradient tiles are claimed one by
+// one, so that the tiles of an expert's row blocks that read the same weight
+// block run side by side on different CTAs and the weights come from HBM
+// once.
 __device__ __forceinline__ void bwd_decode_tile(const BwdGeom &b, const int32_t *us, int tt, int &kind, int &le,
-                                                int &x, int &y, int &hint) {
+                                                int &x, int &y, int &cnt, int &hint) {
     const MoeGeom &g = b.f;
     auto U = [&](int j) { return j <= 0 ? 0 : us[j < g.Eq ? j : g.Eq]; };
     auto clampEq = [&](int v) { return v < 0 ? 0 : (v > g.Eq ? g.Eq : v); };
-    auto gstart = [&](int j) { return b.NIC * U(j) + b.W1 * clampEq(j) + b.NHC * U(j - 1) + b.W2 * clampEq(j - 2); };
+    auto gstart = [&](int j) { return b.NIC * U(j) + b.T1 * clampEq(j) + b.NHC * U(j - 1) + b.T2 * clampEq(j - 2); };
     kind = 0;
+    cnt = 1;
     if (tt < 0) return;
     // a CTA's tickets increase: start from the group of its previous tile
     int j0 = (hint > 0 && hint < g.Eq + BWD_LAG && gstart(hint) <= tt) ? hint : 0;
@@ -241,25 +254,33 @@ __device__ __forceinline__ void bwd_decode_tile(const BwdGeom &b, const int32_t 
         hint = j;
         const int uj = j < g.Eq ? U(j + 1) - U(j) : 0;
         const int n_dh = b.NIC * uj;
-        const int n_dwd = j < g.Eq ? b.W1 : 0;
+        const int n_dwd = j < g.Eq ? b.T1 : 0;
         const int uj1 = (j >= 1 && j - 1 < g.Eq) ? U(j) - U(j - 1) : 0;
         const int n_dgu = b.NHC * uj1;
-        const int n_dwgu = (j >= 2 && j - 2 < g.Eq) ? b.W2 : 0;
-        const int start = b.NIC * U(j) + b.W1 * clampEq(j) + b.NHC * U(j - 1) + b.W2 * clampEq(j - 2);
+        const int n_dwgu = (j >= 2 && j - 2 < g.Eq) ? b.T2 : 0;
+        const int start = gstart(j);
         int r = tt - start;
         if (r < 0) return;
         if (r < n_dh) { kind = KB_DH; le = j; x = r / uj; y = r % uj; return; }  // x = ic, y = rb
         r -= n_dh;
-        if (r < n_dwd) { kind = KB_DWD; le = j; x = r / b.NHC; y = r % b.NHC; return; }  // x = ib, y = hc
+        if (r < n_dwd) {  // first tile of the group: x = ib, y = hc
+            const int t0 = r * b.G1;
+            kind = KB_DWD; le = j; x = t0 / b.NHC; y = t0 % b.NHC; cnt = b.G1;
+            return;
+        }
         r -= n_dwd;
         if (r < n_dgu) { kind = KB_DGU; le = j - 1; x = r / uj1; y = r % uj1; return; }  // x = hc, y = rb
         r -= n_dgu;
-        if (r < n_dwgu) { kind = KB_DWGU; le = j - 2; x = r / b.NWI; y = r % b.NWI; return; }  // x = hb, y = ib
+        if (r < n_dwgu) {  // first tile of the group: x = hb, y = ib
+            const int t0 = r * b.G2;
+            kind = KB_DWGU; le = j - 2; x = t0 / b.NWI; y = t0 % b.NWI; cnt = b.G2;
+            return;
+        }
     }
 }
 
-__device__ __forceinline__ int bwd_expert_tiles(const BwdGeom &b, const int32_t *us) {
-    return (b.NIC + b.NHC) * us[b.f.Eq] + (b.W1 + b.W2) * b.f.Eq;
+__device__ __forceinline__ int bwd_expert_tickets(const BwdGeom &b, const int32_t *us) {
+    return (b.NIC + b.NHC) * us[b.f.Eq] + (b.T1 + b.T2) * b.f.Eq;
 }
 
 // Rows of unit (expert j of this rank, row block rb): real rows and rows
@@ -277,10 +298,6 @@ struct BwdProdState {
     int nrec = 0;
     bool main_done = false;
     uint64_t idle_t0 = 0;
-    // tickets of the expert-tile region are claimed BWD_CLAIM at a time (one
-    // atomic round trip per group: the weight-gradient tiles are short)
-    uint32_t bnext = 0, bend = 0;
-    bool in_tiles = false;
     int hint = 0;      // tile-rail group of the previous tile
     uint32_t polls = 0;  // decide calls: the push queue is polled on every fourth while the rail lasts
     uint32_t calls = 0;
@@ -350,16 +367,7 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
     }
     // 2) the next entry of this rank's rail
     if (!st.main_done) {
-        uint32_t t;
-        if (st.bnext < st.bend) {
-            t = st.bnext++;
-        } else {
-            const uint32_t grp = st.in_tiles ? static_cast<uint32_t>(BWD_CLAIM) : 1u;
-            t = atomicAdd(&p.ws->tickets[q], grp);
-            st.bnext = t + 1;
-            st.bend = t + grp;
-        }
-        if (t >= static_cast<uint32_t>(b.n_head)) st.in_tiles = true;
+        const uint32_t t = atomicAdd(&p.ws->tickets[q], 1u);
         const int nh = b.n_head;
         const int RB = g.RB, K = g.K;
         if (t == 0) {  // ZPAD
@@ -407,7 +415,7 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
             st.idle_t0 = 0;
             return true;
         }
-        const int ntile = bwd_expert_tiles(b, tb.us);
+        const int ntile = bwd_expert_tickets(b, tb.us);
         const int tt = static_cast<int>(t) - nh;
         if (tt >= ntile) {  // DWR tiles of this rank, then done
             const int hb = q + (tt - ntile) * g.P;
@@ -440,8 +448,8 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
                 return true;
             }
         } else {
-            int kind = 0, le = 0, x = 0, y = 0;
-            bwd_decode_tile(b, tb.us, tt, kind, le, x, y, st.hint);
+            int kind = 0, le = 0, x = 0, y = 0, cnt = 1;
+            bwd_decode_tile(b, tb.us, tt, kind, le, x, y, cnt, st.hint);
             if (kind == 0) {
                 set_error(p.ws, KOSMOS_ERR_DEVICE, -30);
                 return false;
@@ -522,31 +530,35 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
                 }
                 const int nst = (c16 + BK - 1) / BK;
                 const int last = (c16 - (nst - 1) * BK) / 16;  // 1..4 when nst > 0
-                fill_entry(en, kind, e, x, y, nst, t, bwd_trace_open(p, st, kind, t));
-                en.d = le;
-                en.x1 = last & 3;
-                if (!ring_push(sm, st.rs, en, p.ws)) return false;
                 const int32_t rl = tb.offl[le], rp = tb.offp[e];
-                for (int kb = 0; kb < nst; ++kb) {
-                    if (!bwd_wait_stage(p, sm, st.ps, t)) return false;
-                    uint8_t *sa = sm.stages + st.ps.stage * STAGE_BYTES;
-                    uint8_t *sb = sa + A_STAGE_BYTES;
-                    uint64_t *bar = &sm.full[st.ps.stage];
-                    mbar_arrive_expect_tx(bar, STAGE_BYTES);
-                    if (kind == KB_DWD) {  // A = h^T (I block x), B = dy (256 columns y)
-                        tma_load_2d(sa, &p.tmH, bar, x * 128, rl + kb * BK);
-                        tma_load_2d(sa + 8192, &p.tmH, bar, x * 128 + 64, rl + kb * BK);
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_2d(sb + j * 8192, &p.tmDyB, bar, y * 256 + j * 64, rp + kb * BK);
-                    } else {  // A = x^T (hidden block x), B = [dg | du] (inter block y)
-                        tma_load_2d(sa, &p.tmX, bar, x * 128, rl + kb * BK);
-                        tma_load_2d(sa + 8192, &p.tmX, bar, x * 128 + 64, rl + kb * BK);
-                        tma_load_2d(sb, &p.tmDgB, bar, y * 128, rp + kb * BK);
-                        tma_load_2d(sb + 8192, &p.tmDgB, bar, y * 128 + 64, rp + kb * BK);
-                        tma_load_2d(sb + 16384, &p.tmDuB, bar, y * 128, rp + kb * BK);
-                        tma_load_2d(sb + 24576, &p.tmDuB, bar, y * 128 + 64, rp + kb * BK);
+                const int ny = kind == KB_DWD ? b.NHC : b.NWI;  // tiles of the group: y fastest
+                for (int gi = 0; gi < cnt; ++gi) {
+                    const int xi = x + (y + gi) / ny, yi = (y + gi) % ny;
+                    fill_entry(en, kind, e, xi, yi, nst, t, bwd_trace_open(p, st, kind, t));
+                    en.d = le;
+                    en.x1 = last & 3;
+                    if (!ring_push(sm, st.rs, en, p.ws)) return false;
+                    for (int kb = 0; kb < nst; ++kb) {
+                        if (!bwd_wait_stage(p, sm, st.ps, t)) return false;
+                        uint8_t *sa = sm.stages + st.ps.stage * STAGE_BYTES;
+                        uint8_t *sb = sa + A_STAGE_BYTES;
+                        uint64_t *bar = &sm.full[st.ps.stage];
+                        mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                        if (kind == KB_DWD) {  // A = h^T (I block xi), B = dy (256 columns yi)
+                            tma_load_2d(sa, &p.tmH, bar, xi * 128, rl + kb * BK);
+                            tma_load_2d(sa + 8192, &p.tmH, bar, xi * 128 + 64, rl + kb * BK);
+                            for (int j = 0; j < 4; ++j)
+                                tma_load_2d(sb + j * 8192, &p.tmDyB, bar, yi * 256 + j * 64, rp + kb * BK);
+                        } else {  // A = x^T (hidden block xi), B = [dg | du] (inter block yi)
+                            tma_load_2d(sa, &p.tmX, bar, xi * 128, rl + kb * BK);
+                            tma_load_2d(sa + 8192, &p.tmX, bar, xi * 128 + 64, rl + kb * BK);
+                            tma_load_2d(sb, &p.tmDgB, bar, yi * 128, rp + kb * BK);
+                            tma_load_2d(sb + 8192, &p.tmDgB, bar, yi * 128 + 64, rp + kb * BK);
+                            tma_load_2d(sb + 16384, &p.tmDuB, bar, yi * 128, rp + kb * BK);
+                            tma_load_2d(sb + 24576, &p.tmDuB, bar, yi * 128 + 64, rp + kb * BK);
+                        }
+                        st.ps.advance();
                     }
-                    st.ps.advance();
                 }
             }
 

@@ -144,12 +144,20 @@ def test_moe_bwd_trace_every_entry_once(K, orc):
     RB = (T // P + 127) // 128
     NIC, NHC, NWI, NWH = I // 256, H // 256, I // 128, H // 128
     head = 1 + RB * topk + RB + RB * NHC
+    # a DWD / DWGU ticket covers a group of 4 (else 2, else 1) tiles
+    W1, W2 = NWI * NHC, NWH * NWI
+    grp = lambda w: 4 if w % 4 == 0 else (2 if w % 2 == 0 else 1)
     for q in range(P):
         mine = recs[(recs["cta"] % P) == q]
         main = np.sort(mine["ticket"][np.isin(mine["kind"], list(range(16, 25)))])
         ndwr = len(range(q, NWH, P))
-        n = head + (NIC + NHC) * units[q] + (NWI * NHC + NWH * NWI) * Eq + ndwr
-        assert np.array_equal(main, np.arange(n)), q
+        n_tickets = head + (NIC + NHC) * units[q] + (W1 // grp(W1) + W2 // grp(W2)) * Eq + ndwr
+        n_entries = head + (NIC + NHC) * units[q] + (W1 + W2) * Eq + ndwr
+        assert np.array_equal(np.unique(main), np.arange(n_tickets)), q
+        assert len(main) == n_entries, q
+        wg = mine[np.isin(mine["kind"], [22, 23])]
+        _, per_ticket = np.unique(wg["ticket"], return_counts=True)
+        assert set(per_ticket.tolist()) <= {grp(W1), grp(W2)}, q
     kinds = recs["kind"]
     assert (kinds == 8).sum() == sum(units) * NHC        # one push per DGU tile
     assert (kinds == 9).sum() == P * RB * NHC            # one fold per (token block, column tile)
