@@ -54,7 +54,7 @@ constexpr int BWD_GROUP = 4;  // weight-gradient tiles per rail ticket (at most)
 constexpr int DH_EPI_STAGES = 3;
 constexpr int DH_CH_BYTES = 2 * BM * 32 * 2;
 // shared memory: the engine's stages and control, the per-CTA tables, and
-// per epilogue warp two 2 KB staging buffers for the weight-gradient stores
+// per epilogue warp a 4 KB staging box for the weight-gradient stores
 constexpr int BWD_TABLE_BYTES = 5120;
 constexpr int BWD_STAGE_OUT = 2048;
 constexpr int BWD_SMEM_BYTES = SMEM_BYTES + BWD_TABLE_BYTES + 4 * 2 * BWD_STAGE_OUT;
@@ -982,30 +982,21 @@ __device__ __noinline__ bool bwd_fold(const BwdParams &p, const Smem &sm, PipeSt
 // few ulp; the results are rounded to bf16)
 __device__ __forceinline__ float sigmoid_f(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
 
-// One 32 x 32 block of this warp's rows (a weight-gradient tile) stored
-// through the warp's staging buffers: the lanes write their rows' 64 bytes,
-// lane 0 issues the tiled bulk store; a buffer is rewritten once the store
-// issued two blocks earlier has read it.  The buffers hold the 64-byte
-// swizzled layout of the store's tensor map (16-byte piece c of row r at
-// c ^ ((r >> 1) & 3)), so that the 32 lanes' row writes spread over all
-// banks instead of queueing on eight.
-__device__ __forceinline__ void bwd_store_block(uint8_t *stg, int &sb, int lane, const float (&v)[32],
-                                                const CUtensorMap *m, int32_t c0, int32_t c1, int32_t c2) {
-    if (lane == 0) bulk_wait_read<1>();
-    __syncwarp();
-    uint4 *row = reinterpret_cast<uint4 *>(stg + sb * BWD_STAGE_OUT + lane * 64);
-    const int sw = (lane >> 1) & 3;
+// 32 fp32 accumulator columns of this thread's row as bf16 into pieces
+// p0 .. p0 + 3 (16 bytes each) of its 128-byte row of a staging box in the
+// 128-byte swizzled layout of the store's tensor map (piece p of row r at
+// p ^ (r & 7)): the 32 lanes' row writes spread over all banks.
+__device__ __forceinline__ void bwd_stage_cols(uint8_t *box, int lane, const uint32_t (&r)[32], int p0) {
+    uint4 *row = reinterpret_cast<uint4 *>(box + lane * 128);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-        row[q4 ^ sw] = make_uint4(pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]), pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
-                             pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]), pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-        tma_store_3d(m, stg + sb * BWD_STAGE_OUT, c0, c1, c2);
-        bulk_commit();
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t *w = r + q4 * 8;
+        row[(p0 + q4) ^ (lane & 7)] =
+            make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                       pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                       pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                       pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
     }
-    sb ^= 1;
 }
 
 __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm, const BwdTables &tb,
@@ -1019,7 +1010,6 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
     RingState rs;
     PipeState ps;
     uint32_t acc = 0, acc_phase = 0;
-    int sb = 0;  // staging buffer of this warp's next block store
     while (true) {
         if (!mbar_wait(&sm.sfull[rs.idx], rs.phase, PIPE_LIMIT_NS)) {
             set_error(p.ws, KOSMOS_ERR_DEVICE, -6);
@@ -1119,41 +1109,40 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
             } else if (e.kind == KB_DWD || e.kind == KB_DWGU) {
                 // DWD: dW_down[e] rows (inter) x * 128 + row, columns (hidden) y * 256 ..
                 // DWGU: columns 0-127 dW_gate[e] (hidden row x * 128 + row, inter y * 128 ..), 128-255 dW_up
-                // The next chunk's tensor-memory load is in flight while this
-                // one is stored.  The loop body holds two chunks and is not
-                // unrolled further (fully unrolled, the eight chunks' code
-                // made the whole layer 5 % slower).
+                // Per iteration 64 columns (two tensor-memory loads) go out as
+                // one 32 x 64 box through the warp's 4 KB staging buffer: the
+                // tensor-copy unit also serves the operand loads of the next
+                // tiles, and its cost goes with the number of boxes and rows.
                 const int q = e.a / g.Eq;
+                const int32_t r0 = e.b * 128 + grp * 32;
                 uint32_t ra[32], rb[32];
                 tmem_ld_32x32b_x32(taddr, ra);
-                tmem_ld_wait_regs(ra);
+                tmem_ld_32x32b_x32(taddr + 32, rb);
 #pragma unroll 1
-                for (int ch = 0; ch < 8; ch += 2) {
-                    tmem_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
-                    {
-                        float v[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = zero ? 0.f : __uint_as_float(ra[j]);
-                        if (e.kind == KB_DWD)
-                            bwd_store_block(stg, sb, lane, v, &p.tmDwd[q], e.c * 256 + ch * 32, e.b * 128 + grp * 32, e.d);
-                        else
-                            bwd_store_block(stg, sb, lane, v, ch < 4 ? &p.tmDwg[q] : &p.tmDwu[q],
-                                            e.c * 128 + (ch & 3) * 32, e.b * 128 + grp * 32, e.d);
-                    }
+                for (int pr = 0; pr < 4; ++pr) {
+                    tmem_ld_wait_regs(ra);
                     tmem_ld_wait_regs(rb);
-                    if (ch + 2 < 8) tmem_ld_32x32b_x32(taddr + (ch + 2) * 32, ra);
-                    {
-                        float v[32];
+                    if (zero) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = zero ? 0.f : __uint_as_float(rb[j]);
-                        if (e.kind == KB_DWD)
-                            bwd_store_block(stg, sb, lane, v, &p.tmDwd[q], e.c * 256 + (ch + 1) * 32,
-                                            e.b * 128 + grp * 32, e.d);
-                        else
-                            bwd_store_block(stg, sb, lane, v, ch < 4 ? &p.tmDwg[q] : &p.tmDwu[q],
-                                            e.c * 128 + ((ch + 1) & 3) * 32, e.b * 128 + grp * 32, e.d);
+                        for (int j = 0; j < 32; ++j) { ra[j] = 0u; rb[j] = 0u; }
                     }
-                    if (ch + 2 < 8) tmem_ld_wait_regs(ra);
+                    if (lane == 0) bulk_wait_read<0>();  // the previous box has been read
+                    __syncwarp();
+                    bwd_stage_cols(stg, lane, ra, 0);
+                    bwd_stage_cols(stg, lane, rb, 4);
+                    if (pr + 1 < 4) {  // the next 64 columns load while this box is stored
+                        tmem_ld_32x32b_x32(taddr + pr * 64 + 64, ra);
+                        tmem_ld_32x32b_x32(taddr + pr * 64 + 96, rb);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (e.kind == KB_DWD)
+                            tma_store_3d(&p.tmDwd[q], stg, e.c * 256 + pr * 64, r0, e.d);
+                        else  // columns 0-127 dW_gate, 128-255 dW_up
+                            tma_store_3d(pr < 2 ? &p.tmDwg[q] : &p.tmDwu[q], stg, e.c * 128 + (pr & 1) * 64, r0, e.d);
+                        bulk_commit();
+                    }
                 }
             } else if (e.kind == KB_RDX) {
                 const int q = e.a, bb = e.b;
@@ -1389,8 +1378,8 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         auto out3 = [&](CUtensorMap *m, void *ptr, uint64_t d0, uint64_t d1) {
             const uint64_t dims[3] = {d0, d1, Eq};
             const uint64_t st[2] = {d0 * 2, d0 * d1 * 2};
-            const uint32_t box[3] = {32, 32, 1};
-            return encode_tmap(m, BF, 3, ptr, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
+            const uint32_t box[3] = {64, 32, 1};
+            return encode_tmap(m, BF, 3, ptr, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
         };
         ok = ok && out3(&p.tmDwg[q], Lc.dwg[q], I, H) && out3(&p.tmDwu[q], Lc.dwu[q], I, H) &&
              out3(&p.tmDwd[q], Lc.dwd[q], H, I);
