@@ -97,7 +97,7 @@ inline BwdGeom bwd_geom(int P, int64_t T, int64_t H, int E, int K, int64_t I) {
     b.nkb_h = static_cast<int>(H / BK);
     b.nkb_gu = static_cast<int>(2 * I / BK);
     b.nkb_e = E / BK;
-    b.fold_tps = 64 / K;
+    b.fold_tps = 64 / K < 16 ? 64 / K : 16;  // a stage: tps x K slot rows (bf16) + tps router rows (fp32)
     return b;
 }
 
@@ -157,6 +157,7 @@ struct BwdParams {
     CUtensorMap tmDlB;               // dl as B of DWR: box {64, 64}
     CUtensorMap tmWrT;               // W_router [H, E] as K-major B of RDX: dims {E, H}, box {64, 256}
     CUtensorMap tmDslot;             // dx slots [T*K, H]: FOLD, box {256, fold_tps*K}, no swizzle
+    CUtensorMap tmDxr;               // dx router part [T, H] fp32: FOLD, box {256, fold_tps}, no swizzle
     CUtensorMap tmWdT[KOSMOS_MAX_P]; // W_down[q] [Eq, I, H] as K-major B of DH: dims {H, I, Eq}, box {64, 256, 1}
     CUtensorMap tmWgT[KOSMOS_MAX_P]; // W_gate[q] [Eq, H, I] as K-major B of DGU: dims {I, H, Eq}, box {64, 256, 1}
     CUtensorMap tmWuT[KOSMOS_MAX_P];
@@ -580,13 +581,17 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
             SchedEntry en;
             fill_entry(en, K_FOLD, gb, 0, hc, nst, code, bwd_trace_open(p, st, K_FOLD, code));
             if (!ring_push(sm, st.rs, en, p.ws)) return false;
-            const uint32_t bytes = static_cast<uint32_t>(256 * 2 * b.fold_tps * g.K);
+            const uint32_t slot_bytes = static_cast<uint32_t>(256 * 2 * b.fold_tps * g.K);
+            const uint32_t bytes = slot_bytes + static_cast<uint32_t>(256 * 4 * b.fold_tps);
             for (int s = 0; s < nst; ++s) {
                 if (!bwd_wait_stage(p, sm, st.ps, code)) return false;
                 uint64_t *bar = &sm.full[st.ps.stage];
+                uint8_t *sa = sm.stages + st.ps.stage * STAGE_BYTES;
                 mbar_arrive_expect_tx(bar, bytes);
-                tma_load_2d(sm.stages + st.ps.stage * STAGE_BYTES, &p.tmDslot, bar, hc * 256,
+                tma_load_2d(sa, &p.tmDslot, bar, hc * 256,
                             static_cast<int32_t>(row0 + static_cast<int64_t>(s) * b.fold_tps * g.K));
+                tma_load_2d(sa + slot_bytes, &p.tmDxr, bar, hc * 256,
+                            static_cast<int32_t>(row0 / g.K + static_cast<int64_t>(s) * b.fold_tps));
                 st.ps.advance();
             }
             st.idle_t0 = 0;
@@ -912,9 +917,9 @@ __device__ __noinline__ void bwd_push(const BwdParams &p, const SchedEntry &e, i
 }
 
 // FOLD(gb, hc): dx[t] = sum_k slot[t][k] (fp32, k order) + dx_router[t], one
-// rounding to bf16.  Slot rows arrive through the stage ring, fold_tps tokens
-// per stage; thread et takes token et / 16 (and every 8th after it) and 16 of
-// the 256 columns.
+// rounding to bf16.  Slot rows and the tokens' router rows arrive through the
+// stage ring, fold_tps tokens per stage; thread et takes token et / 16 (and
+// every 8th after it) and 16 of the 256 columns.
 __device__ __noinline__ bool bwd_fold(const BwdParams &p, const Smem &sm, PipeState &ps, const SchedEntry &e, int et) {
     const MoeGeom &g = p.b.f;
     const int gb = e.a, hc = e.c;
@@ -923,7 +928,6 @@ __device__ __noinline__ bool bwd_fold(const BwdParams &p, const Smem &sm, PipeSt
     const int tps = p.b.fold_tps;
     const int64_t left = g.Tq - static_cast<int64_t>(bq) * BM;
     const int ntok = static_cast<int>(left < BM ? left : BM);
-    const int64_t t0 = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bq) * BM;
     const int c0 = (et & 15) * 16;
     for (int s = 0; s < e.nstage; ++s) {
         if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
@@ -950,10 +954,11 @@ __device__ __noinline__ bool bwd_fold(const BwdParams &p, const Smem &sm, PipeSt
                     }
                 }
             }
-            const float4 *xr = reinterpret_cast<const float4 *>(p.dxr + (t0 + r) * g.H + hc * 256 + c0);
+            // the router part came with the stage (fp32 rows after the slot rows)
+            const float4 *xr = reinterpret_cast<const float4 *>(buf + 512 * tps * K + (u * 256 + c0) * 4);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float4 a = __ldcg(xr + j);
+                const float4 a = xr[j];
                 acc[4 * j + 0] = __fadd_rn(acc[4 * j + 0], a.x);
                 acc[4 * j + 1] = __fadd_rn(acc[4 * j + 1], a.y);
                 acc[4 * j + 2] = __fadd_rn(acc[4 * j + 2], a.z);
@@ -1389,6 +1394,13 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         const uint64_t st[1] = {H * 2};
         const uint32_t box[2] = {256, static_cast<uint32_t>(b.fold_tps * g.K)};
         ok = encode_tmap(&p.tmDslot, BF, 2, p.dslot, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (ok) {
+        const uint64_t dims[2] = {H, static_cast<uint64_t>(g.T)};
+        const uint64_t st[1] = {H * 4};
+        const uint32_t box[2] = {256, static_cast<uint32_t>(b.fold_tps)};
+        ok = encode_tmap(&p.tmDxr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.dxr, dims, st, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (!ok) return KOSMOS_ERR_CUDA;
     return launch_persistent(reinterpret_cast<const void *>(&moe_bwd_kernel), &p, Lc.grid, BWD_SMEM_BYTES, stream,
