@@ -158,6 +158,7 @@ struct BwdParams {
     CUtensorMap tmWrT;               // W_router [H, E] as K-major B of RDX: dims {E, H}, box {64, 256}
     CUtensorMap tmDslot;             // dx slots [T*K, H]: FOLD, box {256, fold_tps*K}, no swizzle
     CUtensorMap tmDxr;               // dx router part [T, H] fp32: FOLD, box {256, fold_tps}, no swizzle
+    CUtensorMap tmDxbP;              // dx_e rows [rows16, H]: PUSH, box {256, 64}, no swizzle
     CUtensorMap tmWdT[KOSMOS_MAX_P]; // W_down[q] [Eq, I, H] as K-major B of DH: dims {H, I, Eq}, box {64, 256, 1}
     CUtensorMap tmWgT[KOSMOS_MAX_P]; // W_gate[q] [Eq, H, I] as K-major B of DGU: dims {I, H, Eq}, box {64, 256, 1}
     CUtensorMap tmWuT[KOSMOS_MAX_P];
@@ -354,13 +355,22 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
             int e, rb, hc;
             push_decode(code, e, rb, hc);
             SchedEntry en;
-            fill_entry(en, K_PUSH, e, rb, hc, 0, code, bwd_trace_open(p, st, K_PUSH, code));
             int real, r16;
             unit_rows(tb, e - q * g.Eq, rb, real, r16);
+            // the unit's dx_e rows come by TMA, 64 rows (32 KB) per stage
+            const int nst = (real + 63) / 64;
+            fill_entry(en, K_PUSH, e, rb, hc, nst, code, bwd_trace_open(p, st, K_PUSH, code));
             en.x0 = tb.offp[e] + rb * BM;
             en.x1 = real;
             en.x2 = tb.offl[e - q * g.Eq] + rb * BM;  // logical receive row of the unit's first row
-            ring_push(sm, st.rs, en, p.ws);
+            if (!ring_push(sm, st.rs, en, p.ws)) return false;
+            for (int s = 0; s < nst; ++s) {
+                if (!bwd_wait_stage(p, sm, st.ps, code)) return false;
+                uint64_t *bar = &sm.full[st.ps.stage];
+                mbar_arrive_expect_tx(bar, 64 * 512);
+                tma_load_2d(sm.stages + st.ps.stage * STAGE_BYTES, &p.tmDxbP, bar, hc * 256, en.x0 + s * 64);
+                st.ps.advance();
+            }
             st.idle_t0 = 0;
             return true;
         }
@@ -878,29 +888,33 @@ __device__ __forceinline__ void bwd_fold_arrive(const BwdParams &p, int gb, int 
 }
 
 // PUSH(e, rb, hc): the 256-column slice of each of the unit's rows of dx_e
-// goes to its token slot (warp w: rows 32w..32w+31, lane: 16 bytes).
-__device__ __noinline__ void bwd_push(const BwdParams &p, const SchedEntry &e, int ew, int lane, uint32_t epoch) {
+// goes to its token slot.
+__device__ __noinline__ bool bwd_push(const BwdParams &p, const Smem &sm, PipeState &ps, const SchedEntry &e, int et,
+                                      int lane, uint32_t epoch) {
     const MoeGeom &g = p.b.f;
     const int hc = e.c;
-    const int prow0 = e.x0, rows = e.x1, lrow0 = e.x2;
-    const int rbase = ew * 32;
-    const int my = rbase + lane;
-    const int32_t my_sl = (my < rows) ? ldcg_i32(&p.inv_pos[lrow0 + my]) : -1;
-    const int n = (rows - rbase) < 32 ? (rows - rbase) : 32;
-    constexpr int RU = 16;
-    for (int i0 = 0; i0 < n; i0 += RU) {
-        int32_t sl[RU];
-        uint4 v[RU];
-#pragma unroll
-        for (int i = 0; i < RU; ++i) sl[i] = __shfl_sync(0xFFFFFFFFu, my_sl, (i0 + i) & 31);
-#pragma unroll
-        for (int i = 0; i < RU; ++i)
-            if (i0 + i < n)
-                v[i] = ldcg_u4(p.dxb + static_cast<int64_t>(prow0 + rbase + i0 + i) * g.H + hc * 256 + lane * 8);
-#pragma unroll
-        for (int i = 0; i < RU; ++i)
-            if (i0 + i < n)
-                *reinterpret_cast<uint4 *>(p.dslot + static_cast<int64_t>(sl[i]) * g.H + hc * 256 + lane * 8) = v[i];
+    const int rows = e.x1, lrow0 = e.x2;
+    const int32_t my_sl = (et < rows) ? ldcg_i32(&p.inv_pos[lrow0 + et]) : -1;  // this thread's row
+    // the rows arrive by TMA, 64 to a stage; thread et sends row et with one
+    // 512-byte bulk copy to its token slot
+    for (int s = 0; s < e.nstage; ++s) {
+        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -33);
+            return false;
+        }
+        if ((et >> 6) == s && my_sl >= 0) {
+            bulk_s2g(p.dslot + static_cast<int64_t>(my_sl) * g.H + hc * 256,
+                     sm.stages + ps.stage * STAGE_BYTES + (et & 63) * 512, 512);
+            bulk_commit();
+            bulk_wait_read<0>();
+        }
+        named_bar_sync(1, NUM_EPI_THREADS);
+        if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
+        ps.advance();
+    }
+    if (my_sl >= 0) {
+        bulk_wait<0>();  // the row has landed; order it before the release below
+        fence_proxy_async_global();
     }
     __threadfence();
     __syncwarp();
@@ -914,6 +928,7 @@ __device__ __noinline__ void bwd_push(const BwdParams &p, const SchedEntry &e, i
     const uint32_t grp = __match_any_sync(0xFFFFFFFFu, gb);
     if (gb >= 0 && (__ffs(grp) - 1) == lane) bwd_fold_arrive(p, gb, hc, __popc(grp), epoch);
     __syncwarp();
+    return true;
 }
 
 // FOLD(gb, hc): dx[t] = sum_k slot[t][k] (fp32, k order) + dx_router[t], one
@@ -1201,7 +1216,7 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
         } else if (e.kind == KB_RBWD) {
             bwd_rbwd(p, e, et);
         } else if (e.kind == K_PUSH) {
-            bwd_push(p, e, ew, lane, epoch);
+            if (!bwd_push(p, sm, ps, e, et, lane, epoch)) break;
         } else if (e.kind == K_FOLD) {
             if (!bwd_fold(p, sm, ps, e, et)) break;
         }
@@ -1394,6 +1409,12 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         const uint64_t st[1] = {H * 2};
         const uint32_t box[2] = {256, static_cast<uint32_t>(b.fold_tps * g.K)};
         ok = encode_tmap(&p.tmDslot, BF, 2, p.dslot, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (ok) {
+        const uint64_t dims[2] = {H, R16};
+        const uint64_t st[1] = {H * 2};
+        const uint32_t box[2] = {256, 64};
+        ok = encode_tmap(&p.tmDxbP, BF, 2, p.dxb, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (ok) {
         const uint64_t dims[2] = {H, static_cast<uint64_t>(g.T)};
