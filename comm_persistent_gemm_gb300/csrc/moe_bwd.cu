@@ -163,6 +163,8 @@ struct BwdParams {
     CUtensorMap tmWgT[KOSMOS_MAX_P]; // W_gate[q] [Eq, H, I] as K-major B of DGU: dims {I, H, Eq}, box {64, 256, 1}
     CUtensorMap tmWuT[KOSMOS_MAX_P];
     CUtensorMap tmXs[KOSMOS_MAX_P];  // x_shards[q] [Tq, H]: MN-major A of DWR, box {64, 64}
+    CUtensorMap tmDout[KOSMOS_MAX_P];  // dout[q] [Tq, H]: GRADIN, box {256, 32}, no swizzle
+    CUtensorMap tmYslot;             // forward slot outputs [T, K, H]: GRADIN, box {256, 1, 32}, no swizzle
     // weight-gradient outputs, stored from shared memory in 32 x 32 blocks (no swizzle)
     CUtensorMap tmDwg[KOSMOS_MAX_P]; // dims {I, H, Eq}
     CUtensorMap tmDwu[KOSMOS_MAX_P];
@@ -390,9 +392,25 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
         }
         if (t < static_cast<uint32_t>(1 + RB * K)) {  // GRADIN(b, k)
             const int i = static_cast<int>(t) - 1;
+            const int bb = i / K, kk = i % K;
+            const int64_t left = g.Tq - static_cast<int64_t>(bb) * BM;
+            const int ntok = static_cast<int>(left < BM ? left : BM);
+            // per stage 32 tokens x 256 columns of dout and of the slot
+            // outputs (16 KB each), token groups outer
+            const int nch = b.NHC, nst = (ntok + 31) / 32 * nch;
             SchedEntry en;
-            fill_entry(en, KB_GRADIN, q, i / K, i % K, 0, t, bwd_trace_open(p, st, KB_GRADIN, t));
-            ring_push(sm, st.rs, en, p.ws);
+            fill_entry(en, KB_GRADIN, q, bb, kk, nst, t, bwd_trace_open(p, st, KB_GRADIN, t));
+            if (!ring_push(sm, st.rs, en, p.ws)) return false;
+            for (int s = 0; s < nst; ++s) {
+                const int r0 = bb * BM + (s / nch) * 32, c0 = (s % nch) * 256;
+                if (!bwd_wait_stage(p, sm, st.ps, t)) return false;
+                uint8_t *sa = sm.stages + st.ps.stage * STAGE_BYTES;
+                uint64_t *bar = &sm.full[st.ps.stage];
+                mbar_arrive_expect_tx(bar, 2 * 32 * 512);
+                tma_load_2d(sa, &p.tmDout[q], bar, c0, r0);
+                tma_load_3d(sa + 32 * 512, &p.tmYslot, bar, c0, kk, static_cast<int32_t>(q * g.Tq + r0));
+                st.ps.advance();
+            }
             st.idle_t0 = 0;
             return true;
         }
@@ -747,67 +765,97 @@ __device__ __noinline__ void bwd_zpad(const BwdParams &p, const BwdTables &tb, i
     }
 }
 
-// GRADIN(b, k): warp w takes tokens w, w+4, ...; lane l owns 16-byte words
-// l, l+32, ... of the row.  dgate in fp32 (lanes' partial sums added by a
-// butterfly), dy = bf16(gate * dout).
-__device__ __noinline__ void bwd_gradin(const BwdParams &p, const BwdTables &tb, const SchedEntry &e, int ew,
-                                        int lane, int et) {
+// GRADIN(b, k): the combine's backward for slot k of the block's tokens,
+// dgate = <dout, y_slot> in fp32 and dy = bf16(gate * dout) to the token's
+// expert-ordered row.  dout and the slot outputs arrive by TMA, 32 tokens x
+// 256 columns per stage; thread et takes token et / 4 of the group and
+// columns (et % 4) * 64 .. + 63, writes its dy values over its dout in the
+// stage, and the token's dy segment leaves with one 512-byte bulk copy.  The
+// 16-byte pieces are visited in a lane-rotated order so that the lanes of a
+// quarter-warp (two tokens, four segments each) hit distinct banks.
+__device__ __noinline__ bool bwd_gradin(const BwdParams &p, const Smem &sm, PipeState &ps, const BwdTables &tb,
+                                        const SchedEntry &e, int lane, int et) {
     const MoeGeom &g = p.b.f;
     const int q = e.a, bb = e.b, k = e.c;
     const int gblk = q * g.RB + bb;
     const int64_t left = g.Tq - static_cast<int64_t>(bb) * BM;
     const int ntok = static_cast<int>(left < BM ? left : BM);
-    const int H8 = static_cast<int>(g.H / 8);
-    for (int r = ew; r < ntok; r += 4) {
-        const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bb) * BM + r;
-        const int ex = __ldg(&p.topk_idx[t * g.K + k]);
-        const float gk = __ldg(&p.topk_gate[t * g.K + k]);
-        const int pos = ldcg_i32(&p.base[gblk * g.E + ex]) + ldcg_i32(&p.rank_in_blk[t * g.K + k]);
-        const int64_t prow = static_cast<int64_t>(pos) - __ldg(&p.offl[ex]) + tb.offp[ex];
-        const uint4 *dsrc = reinterpret_cast<const uint4 *>(p.dout[q] + (static_cast<int64_t>(bb) * BM + r) * g.H);
-        const uint4 *ysrc = reinterpret_cast<const uint4 *>(p.yslot + (t * g.K + k) * g.H);
-        uint4 *ddst = reinterpret_cast<uint4 *>(p.dy + prow * g.H);
-        float dot = 0.f;
-        for (int w0 = 0; w0 < H8; w0 += 32 * 4) {
-            uint4 dv[4], yv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int w = w0 + u * 32 + lane;
-                if (w < H8) { dv[u] = __ldg(dsrc + w); yv[u] = ldcg_u4(ysrc + w); }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int w = w0 + u * 32 + lane;
-                if (w < H8) {
-                    const uint32_t dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
-                    const uint32_t yw[4] = {yv[u].x, yv[u].y, yv[u].z, yv[u].w};
-                    uint32_t ow[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        dot = __fmaf_rn(bf_lo(dw[j]), bf_lo(yw[j]), dot);
-                        dot = __fmaf_rn(bf_hi(dw[j]), bf_hi(yw[j]), dot);
-                        ow[j] = pack_bf16x2(gk * bf_lo(dw[j]), gk * bf_hi(dw[j]));
-                    }
-                    ddst[w] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                }
+    const int nch = p.b.NHC;
+    const int seg = et & 3, tl = et >> 2;
+    float dot = 0.f, gk = 0.f;
+    int64_t t = 0, prow = 0;
+    bool real = false, sent = false;
+    for (int s = 0; s < e.nstage; ++s) {
+        const int cc = s % nch;
+        if (cc == 0) {  // a new group of 32 tokens
+            const int r = (s / nch) * 32 + tl;
+            real = r < ntok;
+            dot = 0.f;
+            if (real) {
+                t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bb) * BM + r;
+                const int ex = __ldg(&p.topk_idx[t * g.K + k]);
+                gk = __ldg(&p.topk_gate[t * g.K + k]);
+                const int pos = ldcg_i32(&p.base[gblk * g.E + ex]) + ldcg_i32(&p.rank_in_blk[t * g.K + k]);
+                prow = static_cast<int64_t>(pos) - __ldg(&p.offl[ex]) + tb.offp[ex];
             }
         }
+        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -34);
+            return false;
+        }
+        uint8_t *drow = sm.stages + ps.stage * STAGE_BYTES + tl * 512;
+        const uint8_t *yrow = drow + 32 * 512;
+        if (real) {
 #pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, d);
-        if (lane == 0) p.dgate[t * g.K + k] = dot;
+            for (int i = 0; i < 8; ++i) {
+                const int off = seg * 128 + ((i + lane) & 7) * 16;
+                const uint4 dv = *reinterpret_cast<const uint4 *>(drow + off);
+                const uint4 yv = *reinterpret_cast<const uint4 *>(yrow + off);
+                const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w}, yw[4] = {yv.x, yv.y, yv.z, yv.w};
+                uint32_t ow[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    dot = __fmaf_rn(bf_lo(dw[j]), bf_lo(yw[j]), dot);
+                    dot = __fmaf_rn(bf_hi(dw[j]), bf_hi(yw[j]), dot);
+                    ow[j] = pack_bf16x2(gk * bf_lo(dw[j]), gk * bf_hi(dw[j]));
+                }
+                *reinterpret_cast<uint4 *>(drow + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+        }
+        fence_proxy_async_smem();  // the dy values in the stage, for the bulk copy
+        __syncwarp();              // the token's four threads are lanes of one warp
+        if (seg == 0 && real) {
+            bulk_s2g(p.dy + prow * g.H + cc * 256, drow, 512);
+            bulk_commit();
+            bulk_wait_read<0>();
+            sent = true;
+        }
+        named_bar_sync(1, NUM_EPI_THREADS);
+        if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
+        ps.advance();
+        if (cc == nch - 1) {  // the token's dot product: its four threads' parts
+            dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 1);
+            dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 2);
+            if (seg == 0 && real) p.dgate[t * g.K + k] = dot;
+        }
+    }
+    if (sent) {
+        bulk_wait<0>();  // this thread's dy segments have landed
+        fence_proxy_async_global();
     }
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
     // one arrival per row on its unit; then the block's slot-k count
     if (et < ntok) {
-        const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bb) * BM + et;
-        const int ex = __ldg(&p.topk_idx[t * g.K + k]);
-        const int pos = ldcg_i32(&p.base[gblk * g.E + ex]) + ldcg_i32(&p.rank_in_blk[t * g.K + k]);
+        const int64_t tt = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bb) * BM + et;
+        const int ex = __ldg(&p.topk_idx[tt * g.K + k]);
+        const int pos = ldcg_i32(&p.base[gblk * g.E + ex]) + ldcg_i32(&p.rank_in_blk[tt * g.K + k]);
         const int rb = (pos - __ldg(&p.offl[ex])) / BM;
         red_relaxed_add_gpu(&p.dy_cnt[ex * g.MAXRB + rb], 1u);
     }
     named_bar_sync(1, NUM_EPI_THREADS);
     if (et == 0) red_release_add_gpu(&p.dgate_cnt[gblk], 1u);
+    return true;
 }
 
 // RBWD(b): one token per thread.  p = softmax(l) (fp32, the forward's
@@ -1212,7 +1260,7 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
         } else if (e.kind == KB_ZPAD) {
             bwd_zpad(p, tb, e.a, et);
         } else if (e.kind == KB_GRADIN) {
-            bwd_gradin(p, tb, e, ew, lane, et);
+            if (!bwd_gradin(p, sm, ps, tb, e, lane, et)) break;
         } else if (e.kind == KB_RBWD) {
             bwd_rbwd(p, e, et);
         } else if (e.kind == K_PUSH) {
@@ -1393,7 +1441,14 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         p.dwg[q] = static_cast<__nv_bfloat16 *>(Lc.dwg[q]);
         p.dwu[q] = static_cast<__nv_bfloat16 *>(Lc.dwu[q]);
         p.dwd[q] = static_cast<__nv_bfloat16 *>(Lc.dwd[q]);
-        ok = map3(&p.tmWdT[q], Lc.wd[q], H, I, Eq, BK, 256) && map3(&p.tmWgT[q], Lc.wg[q], I, H, Eq, BK, 256) &&
+        {
+            const uint64_t dims[2] = {H, static_cast<uint64_t>(g.Tq)};
+            const uint64_t st[1] = {H * 2};
+            const uint32_t box[2] = {256, 32};
+            ok = encode_tmap(&p.tmDout[q], BF, 2, const_cast<void *>(Lc.dout[q]), dims, st, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE);
+        }
+        ok = ok && map3(&p.tmWdT[q], Lc.wd[q], H, I, Eq, BK, 256) && map3(&p.tmWgT[q], Lc.wg[q], I, H, Eq, BK, 256) &&
              map3(&p.tmWuT[q], Lc.wu[q], I, H, Eq, BK, 256) && map2(&p.tmXs[q], Lc.x[q], H, Tq, 64, BK);
         auto out3 = [&](CUtensorMap *m, void *ptr, uint64_t d0, uint64_t d1) {
             const uint64_t dims[3] = {d0, d1, Eq};
@@ -1409,6 +1464,13 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         const uint64_t st[1] = {H * 2};
         const uint32_t box[2] = {256, static_cast<uint32_t>(b.fold_tps * g.K)};
         ok = encode_tmap(&p.tmDslot, BF, 2, p.dslot, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (ok) {
+        const uint64_t dims[3] = {H, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.T)};
+        const uint64_t st[2] = {H * 2, H * 2 * static_cast<uint64_t>(g.K)};
+        const uint32_t box[3] = {256, 1, 32};
+        ok = encode_tmap(&p.tmYslot, BF, 3, const_cast<__nv_bfloat16 *>(p.yslot), dims, st, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (ok) {
         const uint64_t dims[2] = {H, R16};
