@@ -54,7 +54,7 @@ constexpr int BWD_GROUP = 4;  // weight-gradient tiles per rail ticket (at most)
 constexpr int DH_EPI_STAGES = 3;
 constexpr int DH_CH_BYTES = 2 * BM * 32 * 2;
 // shared memory: the engine's stages and control, the per-CTA tables, and
-// per epilogue warp a 4 KB staging box for the weight-gradient stores
+// per epilogue warp a 4 KB staging buffer for the dW and the dg / du stores
 constexpr int BWD_TABLE_BYTES = 5120;
 constexpr int BWD_STAGE_OUT = 2048;
 constexpr int BWD_SMEM_BYTES = SMEM_BYTES + BWD_TABLE_BYTES + 4 * 2 * BWD_STAGE_OUT;
@@ -152,6 +152,7 @@ struct BwdParams {
     CUtensorMap tmDgB, tmDuB;        // dg, du as B of DWGU: box {64, 64}
     CUtensorMap tmH;                 // forward h [T*K, I]: MN-major A of DWD, box {64, 64}
     CUtensorMap tmGs, tmUs;          // forward g, u [T*K, I]: DH epilogue chunks, box {32, 128}, 64-byte swizzle
+    CUtensorMap tmDgS, tmDuS;        // dg, du [rows16, I] (3-d, depth 1): DH epilogue stores, box {32, 16, 1}, 64-byte swizzle
     CUtensorMap tmX;                 // forward receive rows [T*K, H]: MN-major A of DWGU, box {64, 64}
     CUtensorMap tmDlA;               // dl [T, E]: A of RDX, box {64, 128}
     CUtensorMap tmDlB;               // dl as B of DWR: box {64, 64}
@@ -1106,8 +1107,7 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
             const bool zero = e.nstage == 0;
             if (e.kind == KB_DH) {
                 const int real = e.x1 & 0xFFFF, r16 = e.x1 >> 16;
-                const bool is_real = row < real, in16 = row < r16;
-                const int64_t prow = static_cast<int64_t>(e.x0) + row;
+                const bool is_real = row < real;
                 const int sw = (row >> 1) & 3;  // 64-byte swizzle of this row's 16-byte pieces
                 bool ok = true;
 #pragma unroll 1
@@ -1153,17 +1153,42 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
                         if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
                         ps.advance();
                     }
-                    if (in16) {
-                        const int64_t col = static_cast<int64_t>(e.c) * 256 + ch * 32;
-                        uint4 *dgd = reinterpret_cast<uint4 *>(p.dg + prow * g.I + col);
-                        uint4 *dud = reinterpret_cast<uint4 *>(p.du + prow * g.I + col);
+                    // dg and du leave through the warp's staging buffer as 16-row
+                    // boxes (64-byte swizzle: piece c of row r at c ^ ((r >> 1) & 3));
+                    // boxes past the unit's 16-row-padded end are not stored,
+                    // those rows belong to the next expert
+                    if (lane == 0) bulk_wait_read<0>();
+                    __syncwarp();
+                    {
+                        uint4 *gr = reinterpret_cast<uint4 *>(stg + lane * 64);
+                        uint4 *ur = reinterpret_cast<uint4 *>(stg + 2048 + lane * 64);
+                        const int swz = (lane >> 1) & 3;
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
-                            dgd[q4] = make_uint4(dgp[q4 * 4], dgp[q4 * 4 + 1], dgp[q4 * 4 + 2], dgp[q4 * 4 + 3]);
-                            dud[q4] = make_uint4(dup[q4 * 4], dup[q4 * 4 + 1], dup[q4 * 4 + 2], dup[q4 * 4 + 3]);
+                            gr[q4 ^ swz] = make_uint4(dgp[q4 * 4], dgp[q4 * 4 + 1], dgp[q4 * 4 + 2], dgp[q4 * 4 + 3]);
+                            ur[q4 ^ swz] = make_uint4(dup[q4 * 4], dup[q4 * 4 + 1], dup[q4 * 4 + 2], dup[q4 * 4 + 3]);
                         }
                     }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int32_t col = e.c * 256 + ch * 32;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (grp * 32 + h * 16 < r16) {
+                                const int32_t r0 = e.x0 + grp * 32 + h * 16;
+                                tma_store_3d(&p.tmDgS, stg + h * 1024, col, r0, 0);
+                                tma_store_3d(&p.tmDuS, stg + 2048 + h * 1024, col, r0, 0);
+                            }
+                        }
+                        bulk_commit();
+                    }
                 }
+                if (lane == 0) {  // the boxes have landed; ordered before the release below
+                    bulk_wait<0>();
+                    fence_proxy_async_global();
+                }
+                __syncwarp();
                 if (!ok) break;
             } else if (e.kind == KB_DGU) {
                 const int real = e.x1 & 0xFFFF;
@@ -1471,6 +1496,13 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         const uint32_t box[3] = {256, 1, 32};
         ok = encode_tmap(&p.tmYslot, BF, 3, const_cast<__nv_bfloat16 *>(p.yslot), dims, st, box,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (ok) {
+        const uint64_t dims[3] = {I, R16, 1};
+        const uint64_t st[2] = {I * 2, I * 2 * R16};
+        const uint32_t box[3] = {32, 16, 1};
+        ok = encode_tmap(&p.tmDgS, BF, 3, p.dg, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_tmap(&p.tmDuS, BF, 3, p.du, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
     }
     if (ok) {
         const uint64_t dims[2] = {H, R16};
