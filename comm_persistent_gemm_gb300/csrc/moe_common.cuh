@@ -198,6 +198,9 @@ __device__ __forceinline__ int warp_excl_scan(const int32_t *in, int32_t *out, i
     return __shfl_sync(0xFFFFFFFFu, incl, 31);
 }
 
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+// fp32 silu through the fast exponential and the approximate division (a
+// few ulp; h is rounded to bf16 or quantised to E4M3 after it): the
+// correctly rounded division took a large share of the SwiGLU epilogue
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 }  // namespace kosmos
