@@ -12,7 +12,9 @@ namespace kosmos {
 constexpr int MOE_MAXK = 8;
 constexpr int MOE_SCRATCH = 12288;          // epilogue 8 KB + producer 4 KB
 constexpr int MOE_SF_BYTES = 3 * 512;       // MXFP8: per stage, SFA atom + two SFB atoms
-constexpr int MOE_SMEM_BYTES = SMEM_BYTES + MOE_SCRATCH + NSTAGE * MOE_SF_BYTES;
+constexpr int MOE_STG_BYTES = 2048;         // per epilogue warp: one 32 x 32 bf16 box of a D tile
+constexpr int MOE_SMEM_BYTES = SMEM_BYTES + MOE_SCRATCH + NSTAGE * MOE_SF_BYTES + 4 * MOE_STG_BYTES;
+static_assert(MOE_SMEM_BYTES <= 232448, "MoE forward exceeds 227 KB of shared memory per CTA");
 static_assert(MOE_SMEM_BYTES <= 232448, "MoE kernel exceeds 227 KB of shared memory per CTA");
 constexpr int MOE_QR = 16;                  // MXFP8: token rows per QUANT entry
 // aux[2] of a forward workspace after a complete bf16 forward: its saved

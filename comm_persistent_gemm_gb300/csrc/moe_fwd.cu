@@ -55,6 +55,7 @@ struct MoeParams {
     CUtensorMap tmWr;                // w_router: dims {E, H}, box {64, 64}
     CUtensorMap tmRecv;              // receive buffer: dims {H, rows_cap}, box {64, 128}
     CUtensorMap tmH;                 // SwiGLU output: dims {I, rows_cap}, box {64, 128}
+    CUtensorMap tmYbuf;              // D output rows: dims {H, rows_cap, 1}, box {32, 32, 1}, 64-byte swizzle
     CUtensorMap tmWg[KOSMOS_MAX_P];  // w_gate[q]: dims {I, H, Eq}, box {64, 64, 1}
     CUtensorMap tmWu[KOSMOS_MAX_P];  // w_up[q]:   dims {I, H, Eq}, box {64, 64, 1}
     CUtensorMap tmWd[KOSMOS_MAX_P];  // w_down[q]: dims {H, I, Eq}, box {64, 64, 1}
@@ -907,6 +908,7 @@ __device__ __noinline__ bool moe_quant(const MoeParams &p, const Smem &sm, PipeS
 }
 
 __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm, uint32_t tmem_base, uint8_t *escr,
+                                             uint8_t *stg,
                                              int warp, int lane, uint32_t epoch) {
     const MoeGeom &g = p.g;
     const int grp = warp & 3;
@@ -1001,11 +1003,45 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
                         }
                     }
                 }
-            } else {  // K_TILE_D
+            } else if (!g.mx && grp * 32 + 32 > e.x1) {  // K_TILE_D, bf16, a warp with rows past the
+                // unit's end: plain stores of its real rows (in the bf16 layout the
+                // next rows belong to the next expert; MXFP8 pads every expert to
+                // whole 128-row blocks, never read)
                 const bool valid = row < e.x1;
                 __nv_bfloat16 *dst = p.ybuf + static_cast<int64_t>(e.x0 + (valid ? row : 0)) * g.H + e.c * BN;
 #pragma unroll 1
                 for (int ch = 0; ch < BN / 32; ++ch) tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + ch * 32, 32);
+            } else {  // K_TILE_D: 32 x 32 boxes through the warp's staging buffer
+                // (64-byte swizzle: piece c of row r at c ^ ((r >> 1) & 3))
+                const int swz = (lane >> 1) & 3;
+                uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                    tmem_ld_wait();
+                    if (lane == 0) bulk_wait_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint32_t *w = r + q4 * 8;
+                        srow[q4 ^ swz] = make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                                    pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                                    pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                                    pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&p.tmYbuf, stg, e.c * BN + ch * 32, e.x0 + grp * 32, 0);
+                        bulk_commit();
+                    }
+                }
+                if (lane == 0) {  // landed, and ordered before the PUSH release below
+                    bulk_wait<0>();
+                    fence_proxy_async_global();
+                }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -1107,6 +1143,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_fwd_kernel(const __grid_co
     uint8_t *escr = scratch;          // epilogue: 8 KB
     uint8_t *pscr = scratch + 8192;   // producer: 4 KB
     uint8_t *sf = scratch + MOE_SCRATCH;  // MXFP8 scale atoms: NSTAGE x 1.5 KB
+    uint8_t *stg = sf + NSTAGE * MOE_SF_BYTES;  // epilogue warps' D-tile store boxes: 4 x 2 KB
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint32_t epoch = *reinterpret_cast<volatile uint32_t *>(&p.ws->epoch);
@@ -1117,7 +1154,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_fwd_kernel(const __grid_co
     } else if (warp == 1) {
         if (lane == 0) moe_mma_loop(p, sm, sf, tmem_base);
     } else {
-        moe_epilogue(p, sm, tmem_base, escr, warp, lane, epoch);
+        moe_epilogue(p, sm, tmem_base, escr, stg + (warp - 2) * MOE_STG_BYTES, warp, lane, epoch);
     }
     engine_teardown(sm, warp, tmem_base);
     // The last CTA returns every counter to zero, then the rail tickets and epoch.
@@ -1308,6 +1345,14 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
                              CU_TENSOR_MAP_SWIZZLE_NONE))
                 return KOSMOS_ERR_CUDA;
         }
+    }
+    {
+        // D tile output rows (ybuf), stored as 32 x 32 boxes
+        const uint64_t dy[3] = {H, RC, 1}, sy[2] = {H * 2, H * 2 * RC};
+        const uint32_t ybox[3] = {32, 32, 1};
+        if (!encode_tmap(&p.tmYbuf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.ybuf, dy, sy, ybox,
+                         CU_TENSOR_MAP_SWIZZLE_64B))
+            return KOSMOS_ERR_CUDA;
     }
     {
         // FOLD: fold_tps tokens x K slot rows x 256 columns per stage (<= 32 KB)
