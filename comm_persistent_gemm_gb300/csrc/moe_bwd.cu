@@ -160,6 +160,7 @@ struct BwdParams {
     CUtensorMap tmDslot;             // dx slots [T*K, H]: FOLD, box {256, fold_tps*K}, no swizzle
     CUtensorMap tmDxr;               // dx router part [T, H] fp32: FOLD, box {256, fold_tps}, no swizzle
     CUtensorMap tmDxbP;              // dx_e rows [rows16, H]: PUSH, box {256, 64}, no swizzle
+    CUtensorMap tmDxbS;              // dx_e rows (3-d, depth 1): DGU epilogue stores, box {32, 16, 1}, 64-byte swizzle
     CUtensorMap tmWdT[KOSMOS_MAX_P]; // W_down[q] [Eq, I, H] as K-major B of DH: dims {H, I, Eq}, box {64, 256, 1}
     CUtensorMap tmWgT[KOSMOS_MAX_P]; // W_gate[q] [Eq, H, I] as K-major B of DGU: dims {I, H, Eq}, box {64, 256, 1}
     CUtensorMap tmWuT[KOSMOS_MAX_P];
@@ -731,18 +732,6 @@ __device__ __forceinline__ void acc_chunk(uint32_t taddr, bool zero, float (&v)[
     for (int j = 0; j < 32; ++j) v[j] = zero ? 0.f : __uint_as_float(r[j]);
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&v)[32]) {
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-        uint4 o;
-        o.x = pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]);
-        o.y = pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]);
-        o.z = pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]);
-        o.w = pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]);
-        reinterpret_cast<uint4 *>(dst)[q4] = o;
-    }
-}
-
 // ZPAD: zero the padding rows [cnt, ceil16(cnt)) of each of rank q's experts
 // in dy, then count them as arrived rows of the expert's last unit.
 __device__ __noinline__ void bwd_zpad(const BwdParams &p, const BwdTables &tb, int q, int et) {
@@ -1191,14 +1180,49 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
                 __syncwarp();
                 if (!ok) break;
             } else if (e.kind == KB_DGU) {
-                const int real = e.x1 & 0xFFFF;
-                const int64_t prow = static_cast<int64_t>(e.x0) + row;
+                // dx_e rows as 16-row TMA boxes through the two halves of the
+                // warp's staging buffer (64-byte swizzle); boxes past the unit's
+                // 16-row-padded end are not stored (the next expert's rows), the
+                // padding rows below it are never read
+                const int r16 = e.x1 >> 16;
+                const int swz = (lane >> 1) & 3;
 #pragma unroll 1
                 for (int ch = 0; ch < 8; ++ch) {
-                    float v[32];
-                    acc_chunk(taddr + ch * 32, false, v);
-                    if (row < real) store_bf16x32(p.dxb + prow * g.H + static_cast<int64_t>(e.c) * 256 + ch * 32, v);
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                    tmem_ld_wait();
+                    uint8_t *buf = stg + (ch & 1) * 2048;
+                    if (lane == 0) {
+                        if (ch == 0)
+                            bulk_wait_read<0>();  // the previous entry's boxes may span both halves
+                        else
+                            bulk_wait_read<1>();
+                    }
+                    __syncwarp();
+                    uint4 *srow = reinterpret_cast<uint4 *>(buf + lane * 64);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint32_t *w = r + q4 * 8;
+                        srow[q4 ^ swz] = make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                                    pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                                    pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                                    pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (grp * 32 + h * 16 < r16)
+                                tma_store_3d(&p.tmDxbS, buf + h * 1024, e.c * 256 + ch * 32, e.x0 + grp * 32 + h * 16, 0);
+                        bulk_commit();
+                    }
                 }
+                if (lane == 0) {  // landed, and ordered before the PUSH release below
+                    bulk_wait<0>();
+                    fence_proxy_async_global();
+                }
+                __syncwarp();
             } else if (e.kind == KB_DWD || e.kind == KB_DWGU) {
                 // DWD: dW_down[e] rows (inter) x * 128 + row, columns (hidden) y * 256 ..
                 // DWGU: columns 0-127 dW_gate[e] (hidden row x * 128 + row, inter y * 128 ..), 128-255 dW_up
@@ -1503,6 +1527,12 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         const uint32_t box[3] = {32, 16, 1};
         ok = encode_tmap(&p.tmDgS, BF, 3, p.dg, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B) &&
              encode_tmap(&p.tmDuS, BF, 3, p.du, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+    if (ok) {
+        const uint64_t dims[3] = {H, R16, 1};
+        const uint64_t st[2] = {H * 2, H * 2 * R16};
+        const uint32_t box[3] = {32, 16, 1};
+        ok = encode_tmap(&p.tmDxbS, BF, 3, p.dxb, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
     }
     if (ok) {
         const uint64_t dims[2] = {H, R16};
