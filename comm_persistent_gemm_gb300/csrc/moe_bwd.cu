@@ -858,11 +858,34 @@ __device__ __noinline__ void bwd_rbwd(const BwdParams &p, const SchedEntry &e, i
     const int ntok = static_cast<int>(left < BM ? left : BM);
     if (et < ntok) {
         const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bb) * BM + et;
+        // the token's logits are read 32 at a time (eight 16-byte loads in
+        // flight; one at a time they cost a memory latency each), the sums
+        // still run in ascending expert order
         const float *l = p.logits + t * g.E;
+        const float4 *l4 = reinterpret_cast<const float4 *>(l);
         float mx = -INFINITY;
-        for (int j = 0; j < g.E; ++j) mx = fmaxf(mx, __ldcg(l + j));
+#pragma unroll 1
+        for (int c = 0; c < g.E / 32; ++c) {
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(l4 + c * 8 + i);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx = fmaxf(fmaxf(fmaxf(fmaxf(mx, v[i].x), v[i].y), v[i].z), v[i].w);
+        }
         float z = 0.f;
-        for (int j = 0; j < g.E; ++j) z += expf(__ldcg(l + j) - mx);
+#pragma unroll 1
+        for (int c = 0; c < g.E / 32; ++c) {
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(l4 + c * 8 + i);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                z += expf(v[i].x - mx);
+                z += expf(v[i].y - mx);
+                z += expf(v[i].z - mx);
+                z += expf(v[i].w - mx);
+            }
+        }
         int ix[MOE_MAXK];
         float pk[MOE_MAXK], dgk[MOE_MAXK];
         float S = 0.f;
@@ -888,19 +911,30 @@ __device__ __noinline__ void bwd_rbwd(const BwdParams &p, const SchedEntry &e, i
                 pdp += pk[k] * dpk[k];
             }
         }
+        // dl_j = p_j (dp_j - <p, dp>) with dp_j = 0 off the top-K: every
+        // expert is written as -p_j <p, dp> first, then the K selected ones
+        // are rewritten with their dp
         __nv_bfloat16 *out = p.dl + t * g.E;
-        for (int j = 0; j < g.E; j += 2) {
-            float v[2];
+        const float inv_z = 1.0f / z;
+#pragma unroll 1
+        for (int c = 0; c < g.E / 32; ++c) {
+            float lv[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float dp = 0.f;
-#pragma unroll
-                for (int k = 0; k < MOE_MAXK; ++k)
-                    if (k < g.K && ix[k] == j + h) dp = dpk[k];
-                v[h] = (expf(__ldcg(l + j + h) - mx) / z) * (dp - pdp);
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = __ldcg(l4 + c * 8 + i);
+                lv[4 * i] = v.x; lv[4 * i + 1] = v.y; lv[4 * i + 2] = v.z; lv[4 * i + 3] = v.w;
             }
-            *reinterpret_cast<uint32_t *>(out + j) = pack_bf16x2(v[0], v[1]);
+            uint32_t o[16];
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 2)
+                o[jj / 2] = pack_bf16x2((expf(lv[jj] - mx) * inv_z) * -pdp, (expf(lv[jj + 1] - mx) * inv_z) * -pdp);
+            uint4 *o4 = reinterpret_cast<uint4 *>(out + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
+#pragma unroll
+        for (int k = 0; k < MOE_MAXK; ++k)
+            if (k < g.K) out[ix[k]] = __float2bfloat16_rn((expf(__ldcg(l + ix[k]) - mx) * inv_z) * (dpk[k] - pdp));
     }
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
