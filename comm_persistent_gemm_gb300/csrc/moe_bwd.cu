@@ -14,9 +14,9 @@
 //   RBWD(b)         router backward of the block once its K slots are in:
 //                   dl = softmax' of the renormalised top-K gates;
 //   RDX(b, hc)      dx_router = dl . W_router^T (256 columns of hidden);
-//   expert tiles    per expert j, grouped like the forward with lags of one
-//                   and two experts:
-//                   DH(j) | DWD(j) | DGU(j-1) | DWGU(j-2)
+//   expert tiles    per expert j, grouped like the forward with a lag of one
+//                   expert:
+//                   DH(j) | DWD(j) | DGU(j-1) | DWGU(j-1)
 //                   DH:   dh = dy . W_down^T (256 columns of inter) with the
 //                         SwiGLU backward in the epilogue: dg, du;
 //                   DWD:  dW_down = h^T . dy over the expert's rows;
@@ -45,7 +45,7 @@ enum BwdKind : int {
 __device__ __forceinline__ bool bwd_is_mma(int k) {
     return k == KB_RDX || k == KB_DH || k == KB_DGU || k == KB_DWD || k == KB_DWGU || k == KB_DWR;
 }
-constexpr int BWD_LAG = 2;
+constexpr int BWD_LAG = 1;  // experts between an expert's DH tiles and its DWGU tiles (DGU: always 1)
 constexpr int BWD_GROUP = 4;  // weight-gradient tiles per rail ticket (at most)
 // A DH tile's SwiGLU inputs g and u reach its epilogue through three more
 // pipeline stages after its K loop: per 32-column chunk of the tile, the
@@ -237,7 +237,7 @@ __device__ __forceinline__ void bwd_load_tables(const BwdParams &p, const BwdTab
 
 // Expert-tile rail of rank q (tt = ticket - n_head).  Group j holds
 //   DH(j): NIC x u_j (column block outer, row block inner), DWD(j): T1
-//   (j < Eq), DGU(j-1): NHC x u_{j-1}, DWGU(j-2): T2 (0 <= j-2 < Eq)
+//   (j < Eq), DGU(j-1): NHC x u_{j-1}, DWGU(j-1): T2 (0 <= j-1 < Eq)
 // with u_j the row blocks of expert j and U(j) their prefix.  A DH or DGU
 // ticket is one tile; a DWD / DWGU ticket is G1 / G2 consecutive tiles
 // (cnt), taken by one CTA: these tiles are short, and one atomic claim per
@@ -250,7 +250,7 @@ __device__ __forceinline__ void bwd_decode_tile(const BwdGeom &b, const int32_t 
     const MoeGeom &g = b.f;
     auto U = [&](int j) { return j <= 0 ? 0 : us[j < g.Eq ? j : g.Eq]; };
     auto clampEq = [&](int v) { return v < 0 ? 0 : (v > g.Eq ? g.Eq : v); };
-    auto gstart = [&](int j) { return b.NIC * U(j) + b.T1 * clampEq(j) + b.NHC * U(j - 1) + b.T2 * clampEq(j - 2); };
+    auto gstart = [&](int j) { return b.NIC * U(j) + b.T1 * clampEq(j) + b.NHC * U(j - 1) + b.T2 * clampEq(j - BWD_LAG); };
     kind = 0;
     cnt = 1;
     if (tt < 0) return;
@@ -263,7 +263,7 @@ __device__ __forceinline__ void bwd_decode_tile(const BwdGeom &b, const int32_t 
         const int n_dwd = j < g.Eq ? b.T1 : 0;
         const int uj1 = (j >= 1 && j - 1 < g.Eq) ? U(j) - U(j - 1) : 0;
         const int n_dgu = b.NHC * uj1;
-        const int n_dwgu = (j >= 2 && j - 2 < g.Eq) ? b.T2 : 0;
+        const int n_dwgu = (j >= BWD_LAG && j - BWD_LAG < g.Eq) ? b.T2 : 0;
         const int start = gstart(j);
         int r = tt - start;
         if (r < 0) return;
@@ -279,7 +279,7 @@ __device__ __forceinline__ void bwd_decode_tile(const BwdGeom &b, const int32_t 
         r -= n_dgu;
         if (r < n_dwgu) {  // first tile of the group: x = hb, y = ib
             const int t0 = r * b.G2;
-            kind = KB_DWGU; le = j - 2; x = t0 / b.NWI; y = t0 % b.NWI; cnt = b.G2;
+            kind = KB_DWGU; le = j - BWD_LAG; x = t0 / b.NWI; y = t0 % b.NWI; cnt = b.G2;
             return;
         }
     }
