@@ -192,7 +192,7 @@ __device__ __forceinline__ void moe_decode_tile(const MoeParams &p, const int32_
 // Lane 0 of the producer warp: claims and issues one piece of work.  Returns
 // ACT_DISPATCH (with v0 = b, v1 = k, v2 = ticket) when the whole warp must
 // help, ACT_EXIT when this CTA is finished.
-__device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoeProdState &st, uint32_t epoch, int &v0,
+__device__ __forceinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoeProdState &st, uint32_t epoch, int &v0,
                                        int &v1, int &v2) {
     const MoeGeom &g = p.g;
     const int q = blockIdx.x % g.P;
@@ -444,7 +444,7 @@ __device__ __noinline__ int moe_decide(const MoeParams &p, const Smem &sm, MoePr
 // rows are the block's quantised rows (once its QUANT entries are done), and
 // the lanes first copy each row's scale words (4 K-blocks each) into the
 // tiled scale atoms of the destination row.
-__device__ __noinline__ void moe_dispatch(const MoeParams &p, const Smem &sm, MoeProdState &st, uint8_t *pscr,
+__device__ __noinline__ MoeProdState moe_dispatch(const MoeParams &p, const Smem &sm, MoeProdState st, uint8_t *pscr,
                                           int lane, int b, int k, int ticket, uint32_t epoch) {
     const MoeGeom &g = p.g;
     const int q = blockIdx.x % g.P;
@@ -542,6 +542,7 @@ __device__ __noinline__ void moe_dispatch(const MoeParams &p, const Smem &sm, Mo
         if (TraceRec *rec = trace_rec(p.trace, blockIdx.x, slot)) rec->t_done = static_cast<int64_t>(globaltimer());
     }
     __syncwarp();
+    return st;
 }
 
 __device__ __forceinline__ void moe_producer(const MoeParams &p, const Smem &sm, uint8_t *pscr, uint8_t *sf,
@@ -561,7 +562,7 @@ __device__ __forceinline__ void moe_producer(const MoeParams &p, const Smem &sm,
         v2 = __shfl_sync(0xFFFFFFFFu, v2, 0);
         if (act == ACT_EXIT) break;
         if (act == ACT_PLAN) load_plan_table(p, st, lane);
-        if (act == ACT_DISPATCH) moe_dispatch(p, sm, st, pscr, lane, v0, v1, v2, epoch);
+        if (act == ACT_DISPATCH) st = moe_dispatch(p, sm, st, pscr, lane, v0, v1, v2, epoch);
     }
     if (lane == 0) {
         SchedEntry done;
