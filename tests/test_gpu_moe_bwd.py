@@ -79,7 +79,7 @@ def same_slots(kern_idx, ref_idx, e):
 
 @pytest.mark.parametrize("P,T,H,E,topk,I", [(2, 256, 256, 64, 4, 256), (4, 512, 512, 64, 8, 512),
                                             (1, 128, 256, 64, 2, 256), (8, 1024, 256, 128, 8, 256),
-                                            (2, 320, 512, 64, 3, 256)])
+                                            (2, 384, 512, 64, 3, 256)])
 def test_moe_bwd_small_full_compare(K, orc, P, T, H, E, topk, I):
     inp = moe_inputs(T, H, E, I, seed=900 + T + E + topk)
     dout = dout_for(T, H, seed=T + H)
