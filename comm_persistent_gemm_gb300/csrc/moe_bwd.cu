@@ -75,6 +75,7 @@ struct BwdGeom {
     int n_head;     // 1 + RB*K + RB + RB*NHC
     int nkb_h, nkb_gu, nkb_e;  // K stages: H/64, 2I/64, E/64
     int fold_tps;
+    int rbwd_tps;   // RBWD: tokens' fp32 logit rows per 32 KB stage
 };
 
 inline BwdGeom bwd_geom(int P, int64_t T, int64_t H, int E, int K, int64_t I) {
@@ -97,7 +98,8 @@ inline BwdGeom bwd_geom(int P, int64_t T, int64_t H, int E, int K, int64_t I) {
     b.nkb_h = static_cast<int>(H / BK);
     b.nkb_gu = static_cast<int>(2 * I / BK);
     b.nkb_e = E / BK;
-    b.fold_tps = 64 / K < 16 ? 64 / K : 16;  // a stage: tps x K slot rows (bf16) + tps router rows (fp32)
+    b.fold_tps = 64 / K < 16 ? 64 / K : 16;
+    b.rbwd_tps = 32768 / (E * 4);  // a stage: tps x K slot rows (bf16) + tps router rows (fp32)
     return b;
 }
 
@@ -160,6 +162,7 @@ struct BwdParams {
     CUtensorMap tmDslot;             // dx slots [T*K, H]: FOLD, box {256, fold_tps*K}, no swizzle
     CUtensorMap tmDxr;               // dx router part [T, H] fp32: FOLD, box {256, fold_tps}, no swizzle
     CUtensorMap tmDxbP;              // dx_e rows [rows16, H]: PUSH, box {256, 64}, no swizzle
+    CUtensorMap tmLogits;            // forward logits [T, E] fp32: RBWD, box {E, rbwd_tps}, no swizzle
     CUtensorMap tmDxbS;              // dx_e rows (3-d, depth 1): DGU epilogue stores, box {32, 16, 1}, 64-byte swizzle
     CUtensorMap tmWdT[KOSMOS_MAX_P]; // W_down[q] [Eq, I, H] as K-major B of DH: dims {H, I, Eq}, box {64, 256, 1}
     CUtensorMap tmWgT[KOSMOS_MAX_P]; // W_gate[q] [Eq, H, I] as K-major B of DGU: dims {I, H, Eq}, box {64, 256, 1}
@@ -420,9 +423,21 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
             const int bb = static_cast<int>(t) - 1 - RB * K;
             if (!wait_flag_eq(p.ws, &p.dgate_cnt[q * RB + bb], static_cast<uint32_t>(K), p.wait_limit_ns, t))
                 return false;
+            // the block's fp32 logits come by TMA, rbwd_tps tokens per stage
+            const int64_t left = g.Tq - static_cast<int64_t>(bb) * BM;
+            const int ntok = static_cast<int>(left < BM ? left : BM);
+            const int nst = (ntok + b.rbwd_tps - 1) / b.rbwd_tps;
             SchedEntry en;
-            fill_entry(en, KB_RBWD, q, bb, 0, 0, t, bwd_trace_open(p, st, KB_RBWD, t));
-            ring_push(sm, st.rs, en, p.ws);
+            fill_entry(en, KB_RBWD, q, bb, 0, nst, t, bwd_trace_open(p, st, KB_RBWD, t));
+            if (!ring_push(sm, st.rs, en, p.ws)) return false;
+            const int32_t tok0 = static_cast<int32_t>(q * g.Tq + static_cast<int64_t>(bb) * BM);
+            for (int s2 = 0; s2 < nst; ++s2) {
+                if (!bwd_wait_stage(p, sm, st.ps, t)) return false;
+                uint64_t *bar = &sm.full[st.ps.stage];
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(b.rbwd_tps * g.E * 4));
+                tma_load_2d(sm.stages + st.ps.stage * STAGE_BYTES, &p.tmLogits, bar, 0, tok0 + s2 * b.rbwd_tps);
+                st.ps.advance();
+            }
             st.idle_t0 = 0;
             return true;
         }
@@ -851,40 +866,43 @@ __device__ __noinline__ bool bwd_gradin(const BwdParams &p, const Smem &sm, Pipe
 // RBWD(b): one token per thread.  p = softmax(l) (fp32, the forward's
 // logits), S = sum over the top-K of p; dp_j = (dgate_k - sum_k dgate_k
 // gate_k) / S for j = e_k; dl = p * (dp - <p, dp>), written as bf16.
-__device__ __noinline__ void bwd_rbwd(const BwdParams &p, const SchedEntry &e, int et) {
+__device__ __noinline__ bool bwd_rbwd(const BwdParams &p, const Smem &sm, PipeState &ps, const SchedEntry &e, int et) {
     const MoeGeom &g = p.b.f;
     const int q = e.a, bb = e.b;
     const int64_t left = g.Tq - static_cast<int64_t>(bb) * BM;
     const int ntok = static_cast<int>(left < BM ? left : BM);
+    const int tps = p.b.rbwd_tps;
+    // the block's logits arrive by TMA, tps tokens per stage; all of them are
+    // held until the block is done
+    PipeState s0 = ps;
+    for (int s2 = 0; s2 < e.nstage; ++s2) {
+        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+            set_error(p.ws, KOSMOS_ERR_DEVICE, -35);
+            return false;
+        }
+        ps.advance();
+    }
     if (et < ntok) {
         const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bb) * BM + et;
-        // the token's logits are read 32 at a time (eight 16-byte loads in
-        // flight; one at a time they cost a memory latency each), the sums
-        // still run in ascending expert order
-        const float *l = p.logits + t * g.E;
+        PipeState sp = s0;
+        sp.advance(et / tps);
+        const float *l = reinterpret_cast<const float *>(sm.stages + sp.stage * STAGE_BYTES) +
+                         static_cast<int64_t>(et % tps) * g.E;
         const float4 *l4 = reinterpret_cast<const float4 *>(l);
         float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < g.E / 32; ++c) {
-            float4 v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldcg(l4 + c * 8 + i);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx = fmaxf(fmaxf(fmaxf(fmaxf(mx, v[i].x), v[i].y), v[i].z), v[i].w);
+#pragma unroll 4
+        for (int i = 0; i < g.E / 4; ++i) {
+            const float4 v = l4[i];
+            mx = fmaxf(fmaxf(fmaxf(fmaxf(mx, v.x), v.y), v.z), v.w);
         }
-        float z = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < g.E / 32; ++c) {
-            float4 v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldcg(l4 + c * 8 + i);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                z += expf(v[i].x - mx);
-                z += expf(v[i].y - mx);
-                z += expf(v[i].z - mx);
-                z += expf(v[i].w - mx);
-            }
+        float z = 0.f;  // ascending expert order, as the forward's softmax
+#pragma unroll 4
+        for (int i = 0; i < g.E / 4; ++i) {
+            const float4 v = l4[i];
+            z += expf(v.x - mx);
+            z += expf(v.y - mx);
+            z += expf(v.z - mx);
+            z += expf(v.w - mx);
         }
         int ix[MOE_MAXK];
         float pk[MOE_MAXK], dgk[MOE_MAXK];
@@ -893,7 +911,7 @@ __device__ __noinline__ void bwd_rbwd(const BwdParams &p, const SchedEntry &e, i
         for (int k = 0; k < MOE_MAXK; ++k) {
             if (k < g.K) {
                 ix[k] = __ldg(&p.topk_idx[t * g.K + k]);
-                pk[k] = expf(__ldcg(l + ix[k]) - mx) / z;
+                pk[k] = expf(l[ix[k]] - mx) / z;
                 dgk[k] = __ldcg(&p.dgate[t * g.K + k]);
                 S += pk[k];
             }
@@ -918,30 +936,33 @@ __device__ __noinline__ void bwd_rbwd(const BwdParams &p, const SchedEntry &e, i
         const float inv_z = 1.0f / z;
 #pragma unroll 1
         for (int c = 0; c < g.E / 32; ++c) {
-            float lv[32];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = __ldcg(l4 + c * 8 + i);
-                lv[4 * i] = v.x; lv[4 * i + 1] = v.y; lv[4 * i + 2] = v.z; lv[4 * i + 3] = v.w;
-            }
             uint32_t o[16];
 #pragma unroll
-            for (int jj = 0; jj < 32; jj += 2)
-                o[jj / 2] = pack_bf16x2((expf(lv[jj] - mx) * inv_z) * -pdp, (expf(lv[jj + 1] - mx) * inv_z) * -pdp);
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = l4[c * 8 + i];
+                o[2 * i] = pack_bf16x2((expf(v.x - mx) * inv_z) * -pdp, (expf(v.y - mx) * inv_z) * -pdp);
+                o[2 * i + 1] = pack_bf16x2((expf(v.z - mx) * inv_z) * -pdp, (expf(v.w - mx) * inv_z) * -pdp);
+            }
             uint4 *o4 = reinterpret_cast<uint4 *>(out + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) o4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
 #pragma unroll
         for (int k = 0; k < MOE_MAXK; ++k)
-            if (k < g.K) out[ix[k]] = __float2bfloat16_rn((expf(__ldcg(l + ix[k]) - mx) * inv_z) * (dpk[k] - pdp));
+            if (k < g.K) out[ix[k]] = __float2bfloat16_rn((expf(l[ix[k]] - mx) * inv_z) * (dpk[k] - pdp));
     }
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
     if (et == 0) {
+        PipeState sp = s0;
+        for (int s2 = 0; s2 < e.nstage; ++s2) {  // the logits' stages go back to the producer
+            mbar_arrive(&sm.empty[sp.stage]);
+            sp.advance();
+        }
         st_release_gpu(&p.rbwd_flag[q * g.RB + bb], 1u);
         red_release_add_gpu(p.rbwd_done, 1u);
     }
+    return true;
 }
 
 // One arrival on the fold counter of (token block gb, column tile hc); the
@@ -1345,7 +1366,7 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
         } else if (e.kind == KB_GRADIN) {
             if (!bwd_gradin(p, sm, ps, tb, e, lane, et)) break;
         } else if (e.kind == KB_RBWD) {
-            bwd_rbwd(p, e, et);
+            if (!bwd_rbwd(p, sm, ps, e, et)) break;
         } else if (e.kind == K_PUSH) {
             if (!bwd_push(p, sm, ps, e, et, lane, epoch)) break;
         } else if (e.kind == K_FOLD) {
@@ -1561,6 +1582,13 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
         const uint32_t box[3] = {32, 16, 1};
         ok = encode_tmap(&p.tmDgS, BF, 3, p.dg, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B) &&
              encode_tmap(&p.tmDuS, BF, 3, p.du, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+    if (ok) {
+        const uint64_t dims[2] = {E, T};
+        const uint64_t st[1] = {E * 4};
+        const uint32_t box[2] = {static_cast<uint32_t>(E), static_cast<uint32_t>(b.rbwd_tps)};
+        ok = encode_tmap(&p.tmLogits, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(p.logits), dims, st, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (ok) {
         const uint64_t dims[3] = {H, R16, 1};
