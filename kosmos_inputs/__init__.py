@@ -176,6 +176,18 @@ def workload_inputs(w: Workload) -> Dict[str, object]:
     raise ValueError(w.op)
 
 
+def per_block_indices(n_total: int, block: int, per_block: int, seed: int) -> np.ndarray:
+    """Sorted distinct indices: per_block of every run of `block` indices (a
+    shorter last run included), plus the first and last index, drawn from
+    their own generator."""
+    rng = np.random.default_rng(seed + 104729)
+    pick = {0, n_total - 1}
+    for b0 in range(0, n_total, block):
+        n = min(block, n_total - b0)
+        pick.update((b0 + rng.choice(n, size=min(per_block, n), replace=False)).tolist())
+    return np.array(sorted(pick), dtype=np.int64)
+
+
 def sample_indices(n_total: int, n_sample: int, seed: int) -> np.ndarray:
     """Sorted distinct indices in [0, n_total), always including the first and
     last index (edges and the ragged tail), drawn from their own generator."""

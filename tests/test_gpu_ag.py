@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from _helpers import bf16_tensor_to_f64, kosmos, rel_err
-from kosmos_inputs import WORKLOADS, ag_inputs, bf16_bits, sample_indices
+from kosmos_inputs import WORKLOADS, ag_inputs, bf16_bits, per_block_indices, sample_indices
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
@@ -152,12 +152,12 @@ def test_ag_pair_and_single_agree(K, orc):
 @pytest.mark.parametrize("sched", list(SCHEDS))
 def test_ag_full_size_sampled(K, orc, sched):
     """The 8-rank 1024x8192 . 8192x3584 workload in the benchmark's launch
-    configuration, checked on sampled rows (every shard's first and last row
-    included) and for bit-identical reruns."""
+    configuration, checked on one row of every 128-row tile row plus every
+    shard's first and last row, and for bit-identical reruns."""
     w = WORKLOADS["ag_bf16_p8"]
     inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
     xs, xg, outs, _ = _run(K, inp, K.opts(sched=SCHEDS[sched]), reps=2)
-    rows = np.unique(np.concatenate([sample_indices(w.P * w.m, 24, seed=1),
+    rows = np.unique(np.concatenate([per_block_indices(w.P * w.m, 128, 1, seed=1),
                                      np.arange(w.P) * w.m, np.arange(w.P) * w.m + w.m - 1]))
     ref = orc.ag_gemm([bf16_bits(x) for x in inp["x"]], bf16_bits(inp["w"]), rows=rows)
     got = bf16_tensor_to_f64(outs[0][torch.from_numpy(rows).cuda()])

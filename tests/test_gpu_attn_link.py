@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from _helpers import bf16_tensor_to_f64, kosmos, rel_err
-from kosmos_inputs import WORKLOADS, ag_inputs, bf16_bits, rs_inputs, sample_indices
+from kosmos_inputs import WORKLOADS, ag_inputs, bf16_bits, per_block_indices, rs_inputs
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
@@ -109,7 +109,7 @@ def test_ag_qkv_full_size(K, orc):
         assert torch.equal(y, y2)
     _, us = run_ag(K, inp, K.opts(link_gbs=LINK_GBS))
     assert us >= 0.97 * (w.P - 1) * w.m * w.k * 2 / LINK_GBS / 1e3
-    rows = np.unique(np.concatenate([sample_indices(w.P * w.m, 16, seed=7), np.arange(w.P) * w.m,
+    rows = np.unique(np.concatenate([per_block_indices(w.P * w.m, 128, 1, seed=7), np.arange(w.P) * w.m,
                                      np.arange(w.P) * w.m + w.m - 1]))
     ref = orc.ag_gemm([bf16_bits(x) for x in inp["x"]], bf16_bits(inp["w"]), rows=rows)
     got = bf16_tensor_to_f64(y[torch.from_numpy(rows).cuda()])
@@ -126,7 +126,7 @@ def test_rs_oproj_full_size(K, orc):
         y2, _ = run_rs(K, inp, o)
         assert torch.equal(y, y2)
     mc = w.m // w.P
-    rows = np.unique(np.concatenate([sample_indices(w.m, 12, seed=8), np.arange(w.P) * mc,
+    rows = np.unique(np.concatenate([per_block_indices(w.m, 128, 1, seed=8), np.arange(w.P) * mc,
                                      np.arange(w.P) * mc + mc - 1]))
     ref = orc.gemm_rs([bf16_bits(x) for x in inp["x"]], [bf16_bits(x) for x in inp["w"]], rows=rows)
     got = bf16_tensor_to_f64(y[torch.from_numpy(rows).cuda()])

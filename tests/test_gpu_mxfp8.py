@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from _helpers import bf16_tensor_to_f64, kosmos, rel_err
-from kosmos_inputs import WORKLOADS, ag_inputs, bf16_bits, sample_indices
+from kosmos_inputs import WORKLOADS, ag_inputs, bf16_bits, per_block_indices
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -117,7 +117,7 @@ def test_ag_mxfp8_full_size_sampled(K, orc, mode):
     w = WORKLOADS["ag_mxfp8_p8"]
     inp = ag_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
     qs, xg, outs = run_f8(K, inp, K.opts(cta_pair=PAIR[mode]), reps=2)
-    rows = np.unique(np.concatenate([sample_indices(w.P * w.m, 16, seed=3), np.arange(w.P) * w.m,
+    rows = np.unique(np.concatenate([per_block_indices(w.P * w.m, 128, 1, seed=3), np.arange(w.P) * w.m,
                                      np.arange(w.P) * w.m + w.m - 1]))
     ref = oracle_f8(orc, inp, rows=rows)
     got = bf16_tensor_to_f64(outs[0][torch.from_numpy(rows).cuda()])

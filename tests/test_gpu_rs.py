@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from _helpers import bf16_tensor_to_f64, kosmos, rel_err
-from kosmos_inputs import WORKLOADS, bf16_bits, rs_inputs, sample_indices
+from kosmos_inputs import WORKLOADS, bf16_bits, per_block_indices, rs_inputs
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
@@ -81,8 +81,8 @@ def test_rs_reducer_counts_and_few_ctas(K, orc):
 
 
 def test_rs_full_size_sampled_band_and_row(K, orc):
-    """The 8-rank 8192x3584 . 3584x8192 workload: sampled rows (every chunk's
-    first and last row included) against the oracle; band order, row order
+    """The 8-rank 8192x3584 . 3584x8192 workload: one row of every 128-row
+    tile row plus every chunk's first and last row against the oracle; band order, row order
     and the unfused baseline agree bit for bit."""
     w = WORKLOADS["rs_bf16_p8"]
     inp = rs_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
@@ -95,7 +95,7 @@ def test_rs_full_size_sampled_band_and_row(K, orc):
     assert torch.equal(band[0], unf[0])
     assert rel_err(bf16_tensor_to_f64(single[0]), bf16_tensor_to_f64(band[0])) <= TOL
     mc = w.m // w.P
-    rows = np.unique(np.concatenate([sample_indices(w.m, 12, seed=2), np.arange(w.P) * mc,
+    rows = np.unique(np.concatenate([per_block_indices(w.m, 128, 1, seed=2), np.arange(w.P) * mc,
                                      np.arange(w.P) * mc + mc - 1]))
     ref = orc.gemm_rs([bf16_bits(x) for x in inp["x"]], [bf16_bits(x) for x in inp["w"]], rows=rows)
     got = bf16_tensor_to_f64(band[0][torch.from_numpy(rows).cuda()])

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from _helpers import bf16_tensor_to_f64, kosmos, rel_err
-from kosmos_inputs import WORKLOADS, bf16_bits, rs_inputs, sample_indices
+from kosmos_inputs import WORKLOADS, bf16_bits, per_block_indices, rs_inputs
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -74,14 +74,16 @@ def test_rs_mxfp8_small_all_schedules(K, orc, P, m, k, n):
 
 
 def test_rs_mxfp8_full_size_sampled(K, orc):
-    """The 8-rank 8192x3584 . 3584x8192 shapes in MXFP8: sampled rows (every
-    chunk's first and last row) against the oracle."""
+    """The 8-rank 8192x3584 . 3584x8192 shapes in MXFP8: one row of every
+    128-row tile row plus every chunk's first and last row against the
+    oracle."""
     w = WORKLOADS["rs_mxfp8_p8"]
     inp = rs_inputs(w.P, w.m, w.k, w.n, w.seed, w.var_x, w.var_w)
     outs = run(K, inp, K.opts(), reps=2)
     assert torch.equal(outs[0], outs[1])
     mc = w.m // w.P
-    rows = np.unique(np.concatenate([sample_indices(w.m, 8, seed=4), np.arange(w.P) * mc, np.arange(w.P) * mc + mc - 1]))
+    rows = np.unique(np.concatenate([per_block_indices(w.m, 128, 1, seed=4), np.arange(w.P) * mc,
+                                     np.arange(w.P) * mc + mc - 1]))
     ref = oracle(orc, inp, rows=rows)
     got = bf16_tensor_to_f64(outs[0][torch.from_numpy(rows).cuda()])
     assert rel_err(got, ref) <= TOL, rel_err(got, ref)
