@@ -9,12 +9,12 @@
 // status word in the file-scope array below instead of a caller workspace.
 //
 // The array is a __device__ symbol: in host code its name is only a host-side
-// stand-in, never a device address.  The device address is obtained once per
-// device with cudaGetSymbolAddress (with that device current) and passed to
-// the kernel like any workspace pointer.
+// stand-in, never a device address.  Every call looks the device address up
+// with cudaGetSymbolAddress (with the caller's device current) and passes it to
+// the kernel like any workspace pointer.  The lookup is not cached: after a
+// cudaDeviceReset, or in a new primary context, the module is loaded again and
+// the array may live at another address.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "../../include/kosmos.h"
 
@@ -23,29 +23,17 @@ namespace {
 // Held by every GPU that loads this library until the process exits.
 __device__ __align__(256) unsigned char g_kosmos_static_ws[KOSMOS_STATIC_WS_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_ws_ptr[kMaxDevices] = {};
-
-// Device address of g_kosmos_static_ws on the current device, looked up on
-// the first call made with that device current.
+// Device address of g_kosmos_static_ws in the current device's context.  The
+// first lookup in a context loads the module (lazy loading), which is why the
+// first call on a device should come before any stream capture.
 kosmos_status static_ws_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_kosmos_static_ws);
+    if (e != cudaSuccess || p == nullptr) {
         (void)cudaGetLastError();
         return KOSMOS_ERR_CUDA;
     }
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_ws_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_kosmos_static_ws);
-        if (e != cudaSuccess || p == nullptr) {
-            (void)cudaGetLastError();
-            return KOSMOS_ERR_CUDA;
-        }
-        g_ws_ptr[dev] = p;
-    }
-    *out = g_ws_ptr[dev];
+    *out = p;
     return KOSMOS_OK;
 }
 

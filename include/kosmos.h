@@ -408,9 +408,10 @@ KOSMOS_API kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int6
  * kosmos_workspace_bytes) return KOSMOS_ERR_WORKSPACE; opts.trace is not
  * supported (KOSMOS_ERR_UNSUPPORTED).  The 8-rank 1024 x 8192 x 3584 call
  * needs 512 bytes.
- * Set-up: the first call on a device, with that device current, looks up the
- * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture.
+ * Set-up: every call looks up the array's device address in the current
+ * device's context (cudaGetSymbolAddress; nothing is cached, so a reset device
+ * or a new context is picked up).  The first lookup in a context loads the
+ * module, so make the first call on a device before any stream capture.
  * Every call shares the one array per device: each call first clears the part
  * it uses on `stream`, so calls that overlap on the GPU (different streams,
  * or different host threads without ordering) race and give wrong results.
