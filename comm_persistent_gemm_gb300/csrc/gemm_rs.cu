@@ -224,14 +224,13 @@ __device__ __forceinline__ void rs_epilogue(const RsParams &p, const Smem &sm, u
             const int64_t col = static_cast<int64_t>(tcol) * BN + cg * 8;
             bool ok = true;
             for (int s = 0; s < e.nstage; ++s) {
-                if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
-                    set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
-                    ok = false;
-                    break;
-                }
+                // a thread whose wait runs out skips the stage and still takes
+                // its barrier, which makes the decision to stop for all threads
+                const bool got = mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS);
+                if (!got) set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
                 const uint8_t *buf = sm.stages + ps.stage * STAGE_BYTES;
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
+                for (int rr = 0; got && rr < 2; ++rr) {
                     const int r8 = (et >> 5) * 2 + rr;  // row within the 8-row stage
                     float a[8];
 #pragma unroll
@@ -255,7 +254,10 @@ __device__ __forceinline__ void rs_epilogue(const RsParams &p, const Smem &sm, u
                         *reinterpret_cast<uint4 *>(p.y[chunk] + grow * p.g.n + col) = o;
                     }
                 }
-                named_bar_sync(1, NUM_EPI_THREADS);
+                if (!named_bar_and(1, NUM_EPI_THREADS, got)) {
+                    ok = false;
+                    break;
+                }
                 if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
                 ps.advance();
             }
@@ -561,14 +563,13 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
         const int64_t col = static_cast<int64_t>(tcol) * BN + cg * 8;
         bool ok = true;
         for (int sidx = 0; sidx < e.nstage; ++sidx) {
-            if (!mbar_wait(&rr.rfull[rp.stage], rp.phase, PIPE_LIMIT_NS)) {
-                set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
-                ok = false;
-                break;
-            }
+            // a thread whose wait runs out skips the stage and still takes its
+            // barrier, which makes the decision to stop for all threads
+            const bool got = mbar_wait(&rr.rfull[rp.stage], rp.phase, PIPE_LIMIT_NS);
+            if (!got) set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
             const uint8_t *buf = sm.stages + rp.stage * STAGE2_BYTES;
 #pragma unroll
-            for (int r2 = 0; r2 < 2; ++r2) {
+            for (int r2 = 0; got && r2 < 2; ++r2) {
                 const int r8 = (et >> 5) * 2 + r2;
                 float a[8];
 #pragma unroll
@@ -592,7 +593,10 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
                     *reinterpret_cast<uint4 *>(p.y[chunk] + grow * p.g.n + col) = o;
                 }
             }
-            named_bar_sync(1, NUM_EPI_THREADS);
+            if (!named_bar_and(1, NUM_EPI_THREADS, got)) {
+                ok = false;
+                break;
+            }
             if (et == 0) mbar_arrive(&rr.rempty[rp.stage]);
             rp.advance();
         }

@@ -761,6 +761,7 @@ __device__ __noinline__ void bwd_zpad(const BwdParams &p, const BwdTables &tb, i
             reinterpret_cast<uint4 *>(p.dy + row * g.H)[i % H8] = make_uint4(0, 0, 0, 0);
         }
     }
+    fence_proxy_async_global();  // generic stores, read by the tiles' tensor copies
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
     if (et < g.Eq) {
@@ -804,13 +805,13 @@ __device__ __noinline__ bool bwd_gradin(const BwdParams &p, const Smem &sm, Pipe
                 prow = static_cast<int64_t>(pos) - __ldg(&p.offl[ex]) + tb.offp[ex];
             }
         }
-        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
-            set_error(p.ws, KOSMOS_ERR_DEVICE, -34);
-            return false;
-        }
+        // a thread whose wait runs out skips the stage's work and still takes
+        // the stage's barrier, which makes the decision to stop for all
+        const bool ok = mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS);
+        if (!ok) set_error(p.ws, KOSMOS_ERR_DEVICE, -34);
         uint8_t *drow = sm.stages + ps.stage * STAGE_BYTES + tl * 512;
         const uint8_t *yrow = drow + 32 * 512;
-        if (real) {
+        if (ok && real) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int off = seg * 128 + ((i + lane) & 7) * 16;
@@ -829,13 +830,16 @@ __device__ __noinline__ bool bwd_gradin(const BwdParams &p, const Smem &sm, Pipe
         }
         fence_proxy_async_smem();  // the dy values in the stage, for the bulk copy
         __syncwarp();              // the token's four threads are lanes of one warp
-        if (seg == 0 && real) {
+        if (ok && seg == 0 && real) {
             bulk_s2g(p.dy + prow * g.H + cc * 256, drow, 512);
             bulk_commit();
             bulk_wait_read<0>();
             sent = true;
         }
-        named_bar_sync(1, NUM_EPI_THREADS);
+        if (!named_bar_and(1, NUM_EPI_THREADS, ok)) {
+            if (sent) bulk_wait<0>();
+            return false;
+        }
         if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
         ps.advance();
         if (cc == nch - 1) {  // the token's dot product: its four threads' parts
@@ -850,13 +854,16 @@ __device__ __noinline__ bool bwd_gradin(const BwdParams &p, const Smem &sm, Pipe
     }
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
-    // one arrival per row on its unit; then the block's slot-k count
+    // one arrival per row on its unit; then the block's slot-k count.  The
+    // thread that counts token et's row is not the one that copied it: a
+    // release add carries the copier's writes (ordered before the barrier)
+    // to the tile that acquires the count.
     if (et < ntok) {
         const int64_t tt = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bb) * BM + et;
         const int ex = __ldg(&p.topk_idx[tt * g.K + k]);
         const int pos = ldcg_i32(&p.base[gblk * g.E + ex]) + ldcg_i32(&p.rank_in_blk[tt * g.K + k]);
         const int rb = (pos - __ldg(&p.offl[ex])) / BM;
-        red_relaxed_add_gpu(&p.dy_cnt[ex * g.MAXRB + rb], 1u);
+        red_release_add_gpu(&p.dy_cnt[ex * g.MAXRB + rb], 1u);
     }
     named_bar_sync(1, NUM_EPI_THREADS);
     if (et == 0) red_release_add_gpu(&p.dgate_cnt[gblk], 1u);
@@ -875,13 +882,15 @@ __device__ __noinline__ bool bwd_rbwd(const BwdParams &p, const Smem &sm, PipeSt
     // the block's logits arrive by TMA, tps tokens per stage; all of them are
     // held until the block is done
     PipeState s0 = ps;
+    bool ok = true;
     for (int s2 = 0; s2 < e.nstage; ++s2) {
-        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+        if (ok && !mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
             set_error(p.ws, KOSMOS_ERR_DEVICE, -35);
-            return false;
+            ok = false;
         }
         ps.advance();
     }
+    if (!named_bar_and(1, NUM_EPI_THREADS, ok)) return false;  // one decision for all threads
     if (et < ntok) {
         const int64_t t = static_cast<int64_t>(q) * g.Tq + static_cast<int64_t>(bb) * BM + et;
         PipeState sp = s0;
@@ -951,6 +960,7 @@ __device__ __noinline__ bool bwd_rbwd(const BwdParams &p, const Smem &sm, PipeSt
         for (int k = 0; k < MOE_MAXK; ++k)
             if (k < g.K) out[ix[k]] = __float2bfloat16_rn((expf(l[ix[k]] - mx) * inv_z) * (dpk[k] - pdp));
     }
+    fence_proxy_async_global();  // dl is read by tensor copies (RDX, DWR)
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
     if (et == 0) {
@@ -991,17 +1001,18 @@ __device__ __noinline__ bool bwd_push(const BwdParams &p, const Smem &sm, PipeSt
     // the rows arrive by TMA, 64 to a stage; thread et sends row et with one
     // 512-byte bulk copy to its token slot
     for (int s = 0; s < e.nstage; ++s) {
-        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
-            set_error(p.ws, KOSMOS_ERR_DEVICE, -33);
-            return false;
-        }
-        if ((et >> 6) == s && my_sl >= 0) {
+        const bool ok = mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS);
+        if (!ok) set_error(p.ws, KOSMOS_ERR_DEVICE, -33);
+        if (ok && (et >> 6) == s && my_sl >= 0) {
             bulk_s2g(p.dslot + static_cast<int64_t>(my_sl) * g.H + hc * 256,
                      sm.stages + ps.stage * STAGE_BYTES + (et & 63) * 512, 512);
             bulk_commit();
             bulk_wait_read<0>();
         }
-        named_bar_sync(1, NUM_EPI_THREADS);
+        if (!named_bar_and(1, NUM_EPI_THREADS, ok)) {  // one decision for all threads
+            bulk_wait<0>();
+            return false;
+        }
         if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
         ps.advance();
     }
@@ -1038,12 +1049,10 @@ __device__ __noinline__ bool bwd_fold(const BwdParams &p, const Smem &sm, PipeSt
     const int ntok = static_cast<int>(left < BM ? left : BM);
     const int c0 = (et & 15) * 16;
     for (int s = 0; s < e.nstage; ++s) {
-        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
-            set_error(p.ws, KOSMOS_ERR_DEVICE, -32);
-            return false;
-        }
+        const bool ok = mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS);
+        if (!ok) set_error(p.ws, KOSMOS_ERR_DEVICE, -32);
         const uint8_t *buf = sm.stages + ps.stage * STAGE_BYTES;
-        for (int u = et >> 4; u < tps; u += NUM_EPI_THREADS / 16) {
+        for (int u = et >> 4; ok && u < tps; u += NUM_EPI_THREADS / 16) {
             const int r = s * tps + u;
             if (r >= ntok) break;
             float acc[16];
@@ -1084,7 +1093,7 @@ __device__ __noinline__ bool bwd_fold(const BwdParams &p, const Smem &sm, PipeSt
             dst[0] = o[0];
             dst[1] = o[1];
         }
-        named_bar_sync(1, NUM_EPI_THREADS);
+        if (!named_bar_and(1, NUM_EPI_THREADS, ok)) return false;  // one decision for all threads
         if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
         ps.advance();
     }
@@ -1157,16 +1166,17 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
 #pragma unroll 1
                 for (int ch = 0; ch < 8; ++ch) {
                     const int j = ch % 3;
-                    if (j == 0 && !mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
+                    // a thread whose wait runs out computes zeros up to the
+                    // stage's barrier, which makes the decision to stop for all
+                    if (j == 0 && ok && !mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
                         set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
                         ok = false;
-                        break;
                     }
                     const uint8_t *cs = sm.stages + ps.stage * STAGE_BYTES + j * DH_CH_BYTES + row * 64;
                     float dh[32];
                     acc_chunk(taddr + ch * 32, false, dh);
                     uint32_t dgp[16], dup[16];  // bf16 pairs of dg, du
-                    if (is_real) {
+                    if (ok && is_real) {
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             const uint4 gv = *reinterpret_cast<const uint4 *>(cs + (q4 ^ sw) * 16);
@@ -1193,7 +1203,10 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
                         for (int w = 0; w < 16; ++w) { dgp[w] = 0u; dup[w] = 0u; }
                     }
                     if (j == 2 || ch == 7) {  // every epilogue warp has read its rows of the stage
-                        named_bar_sync(1, NUM_EPI_THREADS);
+                        if (!named_bar_and(1, NUM_EPI_THREADS, ok)) {
+                            ok = false;
+                            break;
+                        }
                         if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
                         ps.advance();
                     }
@@ -1347,6 +1360,7 @@ __device__ __forceinline__ void bwd_epilogue(const BwdParams &p, const Smem &sm,
             if (lane == 0) mbar_arrive(&sm.tempty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             if (e.kind == KB_DH || e.kind == KB_DGU || e.kind == KB_RDX) {
+                if (e.kind == KB_RDX) fence_proxy_async_global();  // dxr: generic stores, read by FOLD's tensor copies
                 __threadfence();
                 named_bar_sync(1, NUM_EPI_THREADS);
                 if (et == 0) {

@@ -813,12 +813,12 @@ __device__ __noinline__ bool moe_fold(const MoeParams &p, const Smem &sm, PipeSt
     named_bar_sync(1, NUM_EPI_THREADS);
     const int c0 = (et & 15) * 16;
     for (int s = 0; s < e.nstage; ++s) {
-        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
-            set_error(p.ws, KOSMOS_ERR_DEVICE, -9);
-            return false;
-        }
+        // a thread whose wait runs out skips the stage and still takes its
+        // barrier, which makes the decision to stop for all threads
+        const bool ok = mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS);
+        if (!ok) set_error(p.ws, KOSMOS_ERR_DEVICE, -9);
         const uint8_t *buf = sm.stages + ps.stage * STAGE_BYTES;
-        for (int u = et >> 4; u < p.fold_tps; u += NUM_EPI_THREADS / 16) {
+        for (int u = et >> 4; ok && u < p.fold_tps; u += NUM_EPI_THREADS / 16) {
             const int r = s * p.fold_tps + u;  // token within the block
             if (r >= ntok) break;
             float acc[16];
@@ -851,7 +851,7 @@ __device__ __noinline__ bool moe_fold(const MoeParams &p, const Smem &sm, PipeSt
             dst[0] = o[0];
             dst[1] = o[1];
         }
-        named_bar_sync(1, NUM_EPI_THREADS);
+        if (!named_bar_and(1, NUM_EPI_THREADS, ok)) return false;
         if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
         ps.advance();
     }
@@ -870,13 +870,11 @@ __device__ __noinline__ bool moe_quant(const MoeParams &p, const Smem &sm, PipeS
     const int rps = STAGE_BYTES / rbytes;
     const int HB = static_cast<int>(g.H / 32);
     for (int s = 0; s < e.nstage; ++s) {
-        if (!mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS)) {
-            set_error(p.ws, KOSMOS_ERR_DEVICE, -13);
-            return false;
-        }
+        const bool ok = mbar_wait(&sm.full[ps.stage], ps.phase, PIPE_LIMIT_NS);
+        if (!ok) set_error(p.ws, KOSMOS_ERR_DEVICE, -13);
         const uint8_t *buf = sm.stages + ps.stage * STAGE_BYTES;
         const int n = (rows - s * rps) < rps ? (rows - s * rps) : rps;
-        for (int bi = et; bi < n * HB; bi += NUM_EPI_THREADS) {
+        for (int bi = et; ok && bi < n * HB; bi += NUM_EPI_THREADS) {
             const int r = bi / HB, kb = bi % HB;
             const uint4 *src = reinterpret_cast<const uint4 *>(buf + r * rbytes + kb * 64);
             float v[32];
@@ -898,10 +896,11 @@ __device__ __noinline__ bool moe_quant(const MoeParams &p, const Smem &sm, PipeS
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
             p.xs[t * HB + kb] = static_cast<uint8_t>(sc);
         }
-        named_bar_sync(1, NUM_EPI_THREADS);
+        if (!named_bar_and(1, NUM_EPI_THREADS, ok)) return false;  // one decision for all threads
         if (et == 0) mbar_arrive(&sm.empty[ps.stage]);
         ps.advance();
     }
+    fence_proxy_async_global();  // xq: generic stores, copied by DISPATCH's bulk copies
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
     if (et == 0) red_release_add_gpu(&p.quant_cnt[q * g.RB + (j * MOE_QR) / BM], static_cast<uint32_t>(rows));
