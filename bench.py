@@ -587,32 +587,112 @@ def bench_attn(K, dev, steps, warmup, flush, stream, peak):
     return out
 
 
+def workload_config(w):
+    """The `config` of both arms' lines: the workload and how the timed region
+    treats L2 (identical dicts, so that the two arms compare)."""
+    return {"workload": w.name, "P": w.P, "m_per_shard": w.m, "k": w.k, "n": w.n,
+            "l2": "flushed (256 MiB write) before every GPU step"}
+
+
 def run_reference(args):
+    """The reference arm: the oracle (plain fp64 C, OpenMP) timed on the host
+    cores.  Every step computes a bounded sample of the workload's output rows
+    (the same sample in every step); ms_per_step is the measured time of that
+    sample, and value is its TFLOP/s."""
+    import numpy as np
+    import oracle
+    from kosmos_inputs import WORKLOADS, bf16_bits, workload_inputs
     ws, rank, local = dist_env()
     if ws > 1 and rank != 0:
         return 0
-    from kosmos_inputs import WORKLOADS, workload_inputs
     w = WORKLOADS[WORKLOAD]
     inp = workload_inputs(w)
-    vals = []
-    info = None
+    oracle.build()
+    xs = [bf16_bits(x) for x in inp["x"]]
+    wb = bf16_bits(inp["w"])
+    P, m, k, n = w.P, w.m, w.k, w.n
+    # size the sample so that warm-up and timed steps take about 90 s in all
+    probe = np.arange(0, P * m, (P * m) // 32, dtype=np.int64)[:32]
+    t0 = time.perf_counter()
+    oracle.ag_gemm(xs, wb, rows=probe)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    budget_s = 90.0 / max(1, args.steps + args.warmup)
+    nrows = int(min(P * m, max(16, budget_s / max(per_row, 1e-6))))
+    rows = np.linspace(0, P * m - 1, nrows).astype(np.int64)
     for _ in range(args.warmup):
-        time_oracle_ag(inp, target_s=2.0)
+        oracle.ag_gemm(xs, wb, rows=rows)
+    times = []
     for _ in range(args.steps):
-        info = time_oracle_ag(inp, target_s=max(2.0, 60.0 / max(args.steps, 1)))
-        vals.append(info["value"])
-    v = statistics.mean(vals)
-    tflop = w.flops() / 1e12
+        t0 = time.perf_counter()
+        oracle.ag_gemm(xs, wb, rows=rows)
+        times.append(time.perf_counter() - t0)
+    step_s = statistics.mean(times)
+    v = 2.0 * nrows * k * n / step_s / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tflop / v * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded N(0,var) bf16)",
-            "config": {"workload": WORKLOAD, "P": w.P, "m_per_shard": w.m, "k": w.k, "n": w.n},
-            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
-                             "sample": info["sample"]},
+            "data": "synthetic (seeded N(0,var) bf16)", "config": workload_config(w),
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{nrows} of {P * m} output rows of Y = concat(X_r) W per step (fp64); "
+                                       f"ms_per_step is the time of that sample"},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def sig(x, n=4):
+    """x rounded to n significant digits (keeps the JSON line short)."""
+    return float(f"{x:.{n}g}") if isinstance(x, float) else x
+
+
+def compact_baselines(base):
+    return {"fixed_split_best": {"tflops": sig(base["fixed_split_best"]["tflops"]),
+                                 "crew": base["fixed_split_best"]["crew"]},
+            "fixed_sweep": {c: sig(v) for c, v in base["fixed_split_best"]["sweep"].items()},
+            "unfused": sig(base["unfused"]["tflops"]),
+            "one_sm_tiles": sig(base["self_single_sm_tiles"]["tflops"]),
+            "n_comm0_sweep": {c: sig(v) for c, v in base["self_n_comm0_sweep"].items()}}
+
+
+def compact_also(also):
+    """Every other workload's key figures, short enough that the whole result
+    line survives a log tail (TFLOP/s unless named otherwise; frac = fraction
+    of the measured peak of the kernel's bound)."""
+    out = {}
+    r = also.get("gemm_rs")
+    if r:
+        out["rs_bf16_p8"] = {"tflops": sig(r["tflops"]), "frac": sig(r["frac_of_peak"], 3), "ms": sig(r["ms"]),
+                             "row_over_band": sig(r["row_over_band"], 3),
+                             "fixed_best": sig(r["fixed_split_best"]["tflops"]),
+                             "unfused": sig(r["unfused"]["tflops"]),
+                             "one_sm_tiles": sig(r["self_single_sm_tiles_tflops"])}
+    r = also.get("ag_mxfp8")
+    if r:
+        out["ag_mxfp8_p8"] = {"tflops": sig(r["tflops"]), "frac": sig(r["frac_of_peak"], 3), "ms": sig(r["ms"]),
+                              "fixed_best": sig(r["fixed_split_tflops"]), "unfused": sig(r["unfused_tflops"])}
+    r = also.get("rs_mxfp8")
+    if r:
+        out["rs_mxfp8_p8"] = {"tflops": sig(r["tflops"]), "frac": sig(r["frac_of_peak"], 3), "ms": sig(r["ms"]),
+                              "row_over_band": sig(r.get("row_over_band"), 3),
+                              "fixed_best": sig(r.get("fixed_split_tflops")), "unfused": sig(r.get("unfused_tflops"))}
+    for key, name in (("moe_fwd", "moe_fwd_p8"), ("moe_fwd_mxfp8", "moe_fwd_mxfp8_p8"), ("moe_bwd", "moe_bwd_p8")):
+        r = also.get(key)
+        if r:
+            d = {"ms": sig(r["ms"]), "tok_s": sig(r["tokens_per_s"]), "tflops": sig(r["tflops"]),
+                 "hbm_frac": sig(r["roofline"]["frac"], 3), "gbs": sig(r["roofline"]["achieved"])}
+            if "unfused" in r:
+                d["unfused_ms"] = sig(r["unfused"]["ms"])
+                d["unfused_launches"] = r["unfused"]["launches_per_step"]
+            out[name] = d
+    r = also.get("attention")
+    if r:
+        a = {}
+        for wl, k in (("ag_qkv_p8", "self"), ("rs_oproj_p8", "band")):
+            for tag in ("free", "link"):
+                t = r[wl]["tflops"][tag]
+                a[f"{wl}_{tag}"] = [sig(t[k]), sig(t["fixed_best"]), sig(t["unfused"])]
+        out["attention_self_fixedbest_unfused"] = a
+    return out
 
 
 def run_quick_other(args):
@@ -791,14 +871,17 @@ def run_kosmos(args):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,var) bf16)",
-                "config": {"workload": WORKLOAD, "P": P, "m_per_shard": m, "k": k, "n": n, "sched": "self",
-                           "n_comm0": "ceil(S/P)", "sms": sms, "l2": "flushed (256 MiB write) before every step"},
+                "config": workload_config(w),
+                "launch": {"sched": "self", "n_comm0": "ceil(S/P)", "sms": sms},
                 "frac_of_peak": achieved / peak,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-                "gpu_launches": args.steps, "baselines": base,
+                "gpu_launches": args.steps, "baselines": compact_baselines(base),
                 "vs_fixed_split_best": value / world / base["fixed_split_best"]["tflops"],
-                "vs_unfused": value / world / base["unfused"]["tflops"], "also": also}
-        print(json.dumps(line))
+                "vs_unfused": value / world / base["unfused"]["tflops"], "also": compact_also(also)}
+        if args.detail:
+            with open(args.detail, "w") as fh:
+                json.dump({**line, "baselines": base, "also": also}, fh, indent=1)
+        print(json.dumps(line, separators=(",", ":")))
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -819,6 +902,7 @@ def main():
                     help="with --quick: persistent grid size (0 = one CTA per SM)")
     ap.add_argument("--plain-launch", action="store_true",
                     help="with --quick: launch without the cooperative attribute (for profilers)")
+    ap.add_argument("--detail", default="", help="also write the full results (every sweep point) to this JSON file")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed region of the fused kernel (no baselines, e2e or CPU oracle): "
                          "a short launch list for profilers")

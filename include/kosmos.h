@@ -204,29 +204,6 @@ KOSMOS_API kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *co
                              void *stream, void *h2d_stream, void *d2h_stream);
 
 /*
- * All-gather + GEMM with the shards in host memory (BF16): the copies to the
- * device run on h2d_stream, shard by shard (the local shard first), each
- * followed by an arrival word the kernel's movers (and, for the local shard,
- * builders) wait on, so the copies overlap the multiplication; the output
- * rows of each shard are copied back on d2h_stream as soon as all its tiles
- * are written (a stream wait on a per-shard tile count).  Same result as
- * kosmos_ag_gemm on x_dev.
- *   x_host[r]     : X_r [m_per_shard, k] bf16 in pinned host memory.
- *   x_dev[r]      : device buffers [m_per_shard, k] the shards are copied to.
- *   y_dev, y_host : [P * m_per_shard, n] bf16, device and pinned host.
- *   stream        : the kernel's stream; on return, work enqueued on it
- *                   waits for both copy streams, so its completion means the
- *                   whole call (copies included) is done.
- *   h2d_stream, d2h_stream : two further streams, distinct from `stream`.
- *   Requirements as kosmos_ag_gemm (BF16); opts.tail_split is ignored.  If
- *   the kernel fails, the output waits are released (the status tells).
- */
-KOSMOS_API kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev, int P,
-                             int64_t m_per_shard, int64_t k, int64_t n, const void *w, void *x_gathered,
-                             void *y_dev, void *y_host, void *ws, size_t ws_bytes, const kosmos_opts *opts,
-                             void *stream, void *h2d_stream, void *d2h_stream);
-
-/*
  * GEMM + reduce-scatter  (explainer, "Start with the problem": scatter and
  * add the partial results; "KOSMOS removes the manager": builders join the
  * reduction when the multiplication tiles run out).
