@@ -126,6 +126,71 @@ __device__ __forceinline__ bool ag_mover_phase(const AgParams &p, uint8_t *stage
     return stream_mover<NS, CH, 2>(stages, cbar, cphase, p.ws, claim, done) && !failed(p.ws);
 }
 
+// Readiness-driven role switching on the builder side (self-scheduling only):
+// a builder whose next tile waits for a piece that has not arrived takes the
+// transfer rail's next unclaimed part -- a piece some tile waits for, its own
+// or a later one -- instead of spinning, one part at a time, re-checking its
+// piece after each, while its piece is missing and parts remain.  One part at
+// a time: claiming several in a row (or streaming the next part ahead of the
+// current one) made a helper copy its own piece part after part, later than
+// the movers would have delivered it.  It does not claim while the emulated
+// link is backlogged beyond one part's copy time: then the link, not the
+// number of movers, sets the pace, and a part claimed now would only wait in
+// the link's queue.  Its stage buffers carry the copies: drain() first waits
+// until the tile pipeline has consumed every stage it loaded (the previous
+// tiles' MMAs keep running meanwhile).  Returns false after a device error.
+constexpr uint64_t HELP_LINK_SLACK_NS = 16000;  // about one 32-row part's copy time by one SM
+template <int NS, int CH, class Drain>
+__device__ __forceinline__ bool ag_help_until_ready(const AgParams &p, uint8_t *stages, uint64_t *cbar,
+                                                    uint32_t &cphase, int &nrec, int s, int pc, uint32_t target,
+                                                    Drain &&drain) {
+    if (p.sched != KOSMOS_SCHED_SELF || p.ext_ready != nullptr || s == 0) return true;
+    const uint32_t *flag = &p.flags[s * p.g.pieces + pc];
+    auto link_free = [&] {
+        if (p.link_gbs <= 0) return true;
+        const uint64_t t0 = *reinterpret_cast<const volatile uint64_t *>(&p.ws->link_t0);
+        if (t0 == 0) return true;
+        const uint64_t queued = *reinterpret_cast<const volatile uint64_t *>(&p.ws->link_bytes);
+        return t0 + queued / static_cast<uint64_t>(p.link_gbs) <= globaltimer() + HELP_LINK_SLACK_NS;
+    };
+    auto wanted = [&] {
+        return ld_acquire_gpu(flag) != target &&
+               ld_relaxed_gpu(&p.ws->tickets[0]) < static_cast<uint32_t>(p.g.n_transfer) && link_free();
+    };
+    if (!wanted()) return true;
+    if (!drain()) return false;
+    auto done = [&](int32_t ticket, int64_t t_claim) {
+        if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
+            r->t_claim = t_claim; r->t_ready = t_claim; r->t_done = static_cast<int64_t>(globaltimer());
+            r->kind = K_TRANSFER; r->ticket = ticket; r->cta = blockIdx.x;
+        }
+        ++nrec;
+    };
+    while (wanted()) {
+        bool taken = false;
+        auto claim = [&](MoveEntry &e) {
+            if (taken) return false;
+            taken = true;
+            return ag_claim_transfer(p, e);
+        };
+        if (!stream_mover<NS, CH, 2>(stages, cbar, cphase, p.ws, claim, done) || failed(p.ws)) return false;
+    }
+    return true;
+}
+
+// Waits until every stage of the one-SM pipeline has been consumed.
+__device__ __forceinline__ bool drain_stages1(const Smem &sm, const PipeState &ps, WsHeader *ws) {
+    for (int i = 0; i < NSTAGE; ++i) {
+        uint32_t st = ps.stage + i, ph = ps.phase;
+        if (st >= NSTAGE) { st -= NSTAGE; ph ^= 1u; }
+        if (!mbar_wait(&sm.empty[st], ph ^ 1u, PIPE_LIMIT_NS)) {
+            set_error(ws, KOSMOS_ERR_DEVICE, -11);
+            return false;
+        }
+    }
+    return true;
+}
+
 __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, uint32_t epoch) {
     const int cta = blockIdx.x;
     bool mover = (p.sched != KOSMOS_SCHED_UNFUSED) && cta < p.n_comm;
@@ -147,6 +212,10 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
         const int s = w.s, i = w.i;
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
         if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0) {
+            if (!ag_help_until_ready<NSTAGE, STAGE_BYTES>(p, sm.stages, sm.cbar, cphase, nrec, s, i,
+                                                          ag_piece_ready(p.g, epoch),
+                                                          [&] { return drain_stages1(sm, ps, p.ws); }))
+                break;
             if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], ag_piece_ready(p.g, epoch), p.wait_limit_ns, t))
                 break;
         }
@@ -337,19 +406,18 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             const int s = w.s, i2 = w.i;
             const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
             const int pc = 2 * i2;  // the leader's 128-row piece
-            if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
-                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch), p.wait_limit_ns,
-                                  t))
-                    break;
-            }
+            const bool remote = p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces;
             if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0 && !local_in) {
                 if (!ag_ext_wait(p, 0, t)) break;
                 local_in = true;
             }
+            // the entry is published before the readiness wait, so that the
+            // peer can take transfer parts for its own piece meanwhile
             int slot = -1;
-            if (TraceRec *r = trace_rec(p.trace, blockIdx.x, nrec)) {
-                r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
-                r->kind = K_TILE; r->ticket = static_cast<int32_t>(t); r->cta = blockIdx.x;
+            TraceRec *rec = trace_rec(p.trace, blockIdx.x, nrec);
+            if (rec) {
+                rec->t_claim = tc; rec->t_ready = tc; rec->t_done = 0;
+                rec->kind = K_TILE; rec->ticket = static_cast<int32_t>(t); rec->cta = blockIdx.x;
                 slot = nrec;
             }
             ++nrec;
@@ -358,6 +426,16 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             e.kind = K_TILE; e.a = s; e.b = i2; e.c = w.col0; e.d = w.kb0; e.nstage = w.nk;
             e.ticket = static_cast<int32_t>(t); e.slot = slot; e.x1 = w.slot;
             if (!ring2_push(sm, rs, e, p.ws)) break;
+            if (remote) {
+                if (!ag_help_until_ready<NSTAGE2, STAGE2_BYTES>(p, sm.stages, sm.cbar, cphase, nrec, s, pc,
+                                                                ag_piece_ready(p.g, epoch),
+                                                                [&] { return drain_stages2(sm, ps, p.ws); }))
+                    break;
+                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch),
+                                  p.wait_limit_ns, t))
+                    break;
+            }
+            if (rec) rec->t_ready = static_cast<int64_t>(globaltimer());
             const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
             bool ok = true;
             for (int kk = 0; kk < w.nk; ++kk) {
@@ -385,8 +463,12 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             const int s = e.a, i2 = e.b;
             const int pc = 2 * i2 + 1;  // the peer's 128-row piece
             if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
-                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch), p.wait_limit_ns,
-                                  e.ticket))
+                if (!ag_help_until_ready<NSTAGE2, STAGE2_BYTES>(p, sm.stages, sm.cbar, cphase, nrec, s, pc,
+                                                                ag_piece_ready(p.g, epoch),
+                                                                [&] { return drain_stages2(sm, ps, p.ws); }))
+                    break;
+                if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + pc], ag_piece_ready(p.g, epoch),
+                                  p.wait_limit_ns, e.ticket))
                     break;
             }
             const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;

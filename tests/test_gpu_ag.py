@@ -192,6 +192,42 @@ def test_ag_trace_every_entry_once(K, orc, mode):
     assert np.all(t["t_done"] >= t["t_ready"]) and np.all(t["t_ready"] >= t["t_claim"])
 
 
+@pytest.mark.parametrize("mode", list(PAIR))
+def test_ag_blocked_builders_take_transfers(K, orc, mode):
+    """One initial mover (pair) for 8 ranks: builders whose piece has not
+    arrived take transfer parts themselves (self-scheduling only).  Every
+    transfer and tile entry runs exactly once, the result matches the oracle,
+    and the trace shows transfers run by CTAs that started as builders."""
+    P, m, k, n = 8, 512, 512, 1024
+    inp = ag_inputs(P, m, k, n, seed=91, var_w=1.0 / k)
+    o = K.opts(trace=1, n_comm0=1, cta_pair=PAIR[mode])
+    _check_full(orc, K, inp, K.opts(n_comm0=1, cta_pair=PAIR[mode]))
+    xs, xg, outs, ws = _run(K, inp, o)
+    recs = K.trace_records(K.OP_AG_GEMM, P, m, n, k, ws, o)
+    split, tm = K.ag_tile_plan(P, m, k, n, o)
+    tr, tl = orc.rail_ag(P, m, n, TR=tm, XS=split)
+    assert np.array_equal(np.sort(recs["ticket"][recs["kind"] == 2]), np.arange(len(tl)))
+    assert np.array_equal(np.sort(recs["ticket"][recs["kind"] == 1]), np.arange(len(tr)))
+    first_builder = 2 if PAIR[mode] else 1  # CTAs below this one start as movers
+    helpers = recs[(recs["kind"] == 1) & (recs["cta"] >= first_builder)]
+    assert len(helpers) > 0, "no builder took a transfer part"
+    assert torch.equal(xg.cpu(), torch.cat(inp["x"], 0))
+    ref = orc.ag_gemm([bf16_bits(x) for x in inp["x"]], bf16_bits(inp["w"]))
+    assert rel_err(bf16_tensor_to_f64(outs[0]), ref) <= TOL
+
+
+def test_ag_fixed_crew_builders_never_move(K):
+    """The fixed-split baseline keeps its partition: no transfer is run by a
+    CTA outside the crew."""
+    P, m, k, n = 8, 512, 512, 1024
+    inp = ag_inputs(P, m, k, n, seed=92, var_w=1.0 / k)
+    o = K.opts(trace=1, sched=K.SCHED_FIXED, fixed_comm_ctas=2)
+    xs, xg, outs, ws = _run(K, inp, o)
+    recs = K.trace_records(K.OP_AG_GEMM, P, m, n, k, ws, o)
+    assert np.all(recs["cta"][recs["kind"] == 1] < 2)
+    assert np.all(recs["cta"][recs["kind"] == 2] >= 2)
+
+
 def test_ag_dropped_transfer_times_out_then_recovers(K, orc):
     """A transfer whose flag is never released: the waiting tile's bounded wait
     runs out, the call reports TIMEOUT with that tile's ticket, and after a
