@@ -572,7 +572,9 @@ kosmos_status kosmos_moe_fwd(const void *const *x_shards, const void *w_router, 
         return KOSMOS_ERR_INVALID_ARG;
     if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
     const kosmos_opts o = resolve_opts(opts);
-    if (o.sched != KOSMOS_SCHED_SELF) return KOSMOS_ERR_UNSUPPORTED;
+    // SELF: one launch; UNFUSED: the baseline of one launch per phase (no role trace: each launch would
+    // overwrite the previous one's records)
+    if (o.sched == KOSMOS_SCHED_FIXED || (o.sched == KOSMOS_SCHED_UNFUSED && o.trace)) return KOSMOS_ERR_UNSUPPORTED;
     if (o.link_gbs != 0) return KOSMOS_ERR_UNSUPPORTED;
     if (mx && (o.inject & KOSMOS_INJECT_IDENTITY_EXPERTS)) return KOSMOS_ERR_UNSUPPORTED;
     if (ws_bytes < kosmos_moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, dtype, &o))
@@ -644,7 +646,10 @@ kosmos_status kosmos_moe_bwd(const void *const *x_shards, const void *w_router, 
         return KOSMOS_ERR_INVALID_ARG;
     if (!aligned16(ws)) return KOSMOS_ERR_WORKSPACE;
     const kosmos_opts o = resolve_opts(opts);
-    if (o.sched != KOSMOS_SCHED_SELF || o.link_gbs != 0 || o.inject != 0) return KOSMOS_ERR_UNSUPPORTED;
+    // SELF: one launch; UNFUSED: the baseline of one launch per phase (no role trace)
+    if (o.sched == KOSMOS_SCHED_FIXED || (o.sched == KOSMOS_SCHED_UNFUSED && o.trace) || o.link_gbs != 0 ||
+        o.inject != 0)
+        return KOSMOS_ERR_UNSUPPORTED;
     if (fwd_ws_bytes < moe_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, false, false))
         return KOSMOS_ERR_WORKSPACE;
     if (ws_bytes < kosmos_moe_bwd_workspace_bytes(P, tokens, hidden, n_experts, topk, inter, &o))
@@ -669,6 +674,7 @@ kosmos_status kosmos_moe_bwd(const void *const *x_shards, const void *w_router, 
     L.wr = w_router;
     L.topk_idx = topk_idx; L.topk_gate = topk_gate; L.fwd_ws = fwd_ws; L.dwr = dw_router;
     L.ws = ws; L.trace = o.trace; L.grid = grid; L.plain_launch = o.plain_launch; L.wait_limit_ns = o.wait_limit_ns;
+    L.sched = o.sched;
     return launch_moe_bwd(L, static_cast<cudaStream_t>(stream));
 }
 

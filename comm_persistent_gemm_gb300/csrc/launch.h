@@ -127,6 +127,7 @@ struct MoeBwdLaunch {
     void *dwu[KOSMOS_MAX_P];
     void *dwd[KOSMOS_MAX_P];
     void *ws;
+    int sched;   // KOSMOS_SCHED_SELF (one launch) or KOSMOS_SCHED_UNFUSED (one launch per phase)
     int trace;
     int grid;
     int plain_launch;

@@ -198,6 +198,7 @@ struct BwdParams {
     TraceRec *trace;
     BwdGeom b;
     uint64_t wait_limit_ns;
+    int phase;  // 0: the whole backward in this launch; 1-7: one phase of the unfused baseline
 };
 
 // Per-CTA tables in shared memory (producer scratch), filled once at the
@@ -352,10 +353,15 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
     // the status word is a round trip to L2: read on every eighth call (the
     // waits below read it as well)
     if ((st.calls++ & 7u) == 0 && failed(p.ws)) return false;
+    // unfused baseline: phase 1 the head (ZPAD, GRADIN, RBWD, RDX), 2 DH,
+    // 3 DWD, 4 DGU, 5 DWGU, 6 DWR, 7 PUSH + FOLD; 0 = everything in one launch
+    const int ph = p.phase;
+    const bool combine = ph == 0 || ph == 7;
+    if (ph == 7) st.main_done = true;
     // 1) a ready PUSH (polled on every fourth call while rail entries remain:
     //    each poll is a round trip to L2, and the short weight-gradient
     //    tiles would otherwise wait on it)
-    if (st.main_done || (st.polls++ & 3u) == 0) {
+    if (combine && (st.main_done || (st.polls++ & 3u) == 0)) {
         int32_t code;
         if (queue_try_take(&qc[1], &qc[0], p.push_items + q * b.push_cap, p.push_flags + q * b.push_cap, epoch, code,
                            p.ws)) {
@@ -385,9 +391,15 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
     }
     // 2) the next entry of this rank's rail
     if (!st.main_done) {
-        const uint32_t t = atomicAdd(&p.ws->tickets[q], 1u);
         const int nh = b.n_head;
         const int RB = g.RB, K = g.K;
+        // a phase of the unfused baseline counts from its own first ticket
+        const uint32_t base = ph <= 1 ? 0u
+                                      : static_cast<uint32_t>(nh + (ph == 6 ? bwd_expert_tickets(b, tb.us) : 0));
+        const uint32_t t = base + atomicAdd(&p.ws->tickets[q], 1u);
+        if (ph == 1 && t >= static_cast<uint32_t>(nh)) return false;  // the head is done
+        if (ph >= 2 && ph <= 5 && t - static_cast<uint32_t>(nh) >= static_cast<uint32_t>(bwd_expert_tickets(b, tb.us)))
+            return false;  // the expert tiles are done
         if (t == 0) {  // ZPAD
             SchedEntry en;
             fill_entry(en, KB_ZPAD, q, 0, 0, 0, t, bwd_trace_open(p, st, KB_ZPAD, t));
@@ -467,6 +479,7 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
             const int hb = q + (tt - ntile) * g.P;
             if (hb >= b.NWH) {
                 st.main_done = true;
+                if (ph != 0) return false;
             } else {
                 if (!wait_flag_eq(p.ws, p.rbwd_done, static_cast<uint32_t>(g.NB), p.wait_limit_ns, t)) return false;
                 SchedEntry en;
@@ -500,6 +513,8 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
                 set_error(p.ws, KOSMOS_ERR_DEVICE, -30);
                 return false;
             }
+            if (ph >= 2 && ph <= 5 && kind != (ph == 2 ? KB_DH : ph == 3 ? KB_DWD : ph == 4 ? KB_DGU : KB_DWGU))
+                return true;  // another phase's tile
             const int e = q * g.Eq + le;
             const int c = tb.cnt[le];
             const int c16 = (c + 15) / 16 * 16;
@@ -613,7 +628,7 @@ __device__ __forceinline__ bool bwd_decide(const BwdParams &p, const Smem &sm, B
         }
     }
     // 3) a ready FOLD of this rank's tokens
-    {
+    if (combine) {
         int32_t code;
         if (queue_try_take(&qc[3], &qc[2], p.fold_items + q * b.fold_cap, p.fold_flags + q * b.fold_cap, epoch, code,
                            p.ws)) {
@@ -1430,7 +1445,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_bwd_kernel(const __grid_co
         s_last = (atomicAdd(&p.ws->done_ctas, 1u) == gridDim.x - 1) ? 1 : 0;
     }
     __syncthreads();
-    if (s_last) {
+    if (s_last && p.phase >= 1 && p.phase <= 6) {
+        // a phase of the unfused baseline: the next launch goes on with the
+        // counters and flags as they are, from fresh tickets
+        if (threadIdx.x == 0) {
+            volatile uint32_t *t = p.ws->tickets;
+            for (int i = 0; i < KOSMOS_MAX_P; ++i) t[i] = 0u;
+            *reinterpret_cast<volatile uint32_t *>(&p.ws->done_ctas) = 0u;
+            __threadfence();
+        }
+    } else if (s_last) {
         __threadfence();
         uint4 *c = reinterpret_cast<uint4 *>(p.ctr);
         const int n16 = p.ctr_bytes / 16;
@@ -1624,8 +1648,18 @@ kosmos_status launch_moe_bwd(const MoeBwdLaunch &Lc, cudaStream_t stream) {
                          CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (!ok) return KOSMOS_ERR_CUDA;
-    return launch_persistent(reinterpret_cast<const void *>(&moe_bwd_kernel), &p, Lc.grid, BWD_SMEM_BYTES, stream,
-                             Lc.plain_launch != 0);
+    if (Lc.sched != KOSMOS_SCHED_UNFUSED)
+        return launch_persistent(reinterpret_cast<const void *>(&moe_bwd_kernel), &p, Lc.grid, BWD_SMEM_BYTES, stream,
+                                 Lc.plain_launch != 0);
+    // unfused baseline: the same kernel once per phase, each launch running
+    // only its phase's entries to completion before the next starts
+    for (int ph = 1; ph <= 7; ++ph) {
+        p.phase = ph;
+        const kosmos_status st = launch_persistent(reinterpret_cast<const void *>(&moe_bwd_kernel), &p, Lc.grid,
+                                                   BWD_SMEM_BYTES, stream, Lc.plain_launch != 0);
+        if (st != KOSMOS_OK) return st;
+    }
+    return KOSMOS_OK;
 }
 
 }  // namespace kosmos

@@ -92,7 +92,8 @@ struct MoeParams {
     TraceRec *trace;
     MoeGeom g;
     int fold_tps;                    // FOLD: tokens per pipeline stage (64 / K)
-    int pad;
+    int phase;                       // 0: the whole layer in this launch; 1-5: one phase of the unfused
+                                     // baseline (ROUTE+PLAN[+QUANT] | DISPATCH | TILE_GU | TILE_D | PUSH+FOLD)
     uint64_t wait_limit_ns;
     uint64_t inject;
 };
@@ -198,8 +199,19 @@ __device__ __forceinline__ int moe_decide(const MoeParams &p, const Smem &sm, Mo
     const int q = blockIdx.x % g.P;
     uint32_t *qc = p.qctl + 4 * q;
     if (failed(p.ws)) return ACT_EXIT;
+    const int ph = p.phase;
+    if (ph == 5 && !st.plan_seen) {  // the combine alone: the plan of the earlier launches, no main rail
+        if (!wait_flag_eq(p.ws, &p.ws->aux[1], epoch + 1u, p.wait_limit_ns, -10)) return ACT_EXIT;
+        st.main_done = true;
+        return ACT_PLAN;
+    }
+    // main-rail tickets: one counter per rank; a phase of the unfused baseline
+    // counts from its own first ticket (the counters start from zero in
+    // every launch)
+    const uint32_t base = ph == 2 ? static_cast<uint32_t>(g.RB + g.NQ) : (ph >= 3 ? static_cast<uint32_t>(g.n_head) : 0u);
+    uint32_t *tctr = &p.ws->tickets[q];
     // 1) a ready result to push back to its source rank
-    if (st.plan_seen) {
+    if (st.plan_seen && (ph == 0 || ph == 5)) {
         int32_t code;
         if (queue_try_take(&qc[1], &qc[0], p.push_items + q * g.push_cap, p.push_flags + q * g.push_cap, epoch,
                            code, p.ws)) {
@@ -225,10 +237,12 @@ __device__ __forceinline__ int moe_decide(const MoeParams &p, const Smem &sm, Mo
         } else if (st.ahead >= 0) {
             t = static_cast<uint32_t>(st.ahead);
         } else {
-            t = atomicAdd(&p.ws->tickets[q], 1u);
+            t = base + atomicAdd(tctr, 1u);
         }
         st.pending = -1;
         st.ahead = -1;
+        if ((ph == 1 && t >= static_cast<uint32_t>(g.RB + g.NQ)) || (ph == 2 && t >= static_cast<uint32_t>(g.n_head)))
+            return ACT_EXIT;  // this launch's phase of the rail is done
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
         if (t < static_cast<uint32_t>(g.RB)) {  // ROUTE(b)
             const int b = static_cast<int>(t);
@@ -297,10 +311,14 @@ __device__ __forceinline__ int moe_decide(const MoeParams &p, const Smem &sm, Mo
         moe_decode_tile(p, st.us, tt, kind, le, rb, col);
         if (kind == 0) {
             st.main_done = true;
+            if (ph != 0) return ACT_EXIT;
+        } else if ((ph == 3 && kind != K_TILE_GU) || (ph == 4 && kind != K_TILE_D)) {
+            st.ahead = base + atomicAdd(tctr, 1u);  // another phase's tile: take the next ticket
+            return ACT_NONE;
         } else {
             // claim the next tile ticket now; its value is first needed after this
             // entry's loads are issued, so the atomic's round trip overlaps them
-            const uint32_t nxt = atomicAdd(&p.ws->tickets[q], 1u);
+            const uint32_t nxt = base + atomicAdd(tctr, 1u);
             const int e = q * g.Eq + le;
             const int row0 = st.off[le] + rb * BM;
             const int left = st.cnt[le] - rb * BM;
@@ -388,7 +406,7 @@ __device__ __forceinline__ int moe_decide(const MoeParams &p, const Smem &sm, Mo
         }
     }
     // 3) a ready fold of this rank's tokens
-    if (st.plan_seen) {
+    if (st.plan_seen && (ph == 0 || ph == 5)) {
         int32_t code;
         if (queue_try_take(&qc[3], &qc[2], p.fold_items + q * g.fold_cap, p.fold_flags + q * g.fold_cap, epoch, code,
                            p.ws)) {
@@ -1164,7 +1182,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) moe_fwd_kernel(const __grid_co
         s_last = (atomicAdd(&p.ws->done_ctas, 1u) == gridDim.x - 1) ? 1 : 0;
     }
     __syncthreads();
-    if (s_last) {
+    if (s_last && p.phase >= 1 && p.phase <= 4) {
+        // a phase of the unfused baseline: the next launch goes on with the
+        // counters and flags as they are, from fresh tickets
+        if (threadIdx.x == 0) {
+            volatile uint32_t *t = p.ws->tickets;
+            for (int i = 0; i < KOSMOS_MAX_P; ++i) t[i] = 0u;
+            *reinterpret_cast<volatile uint32_t *>(&p.ws->done_ctas) = 0u;
+            __threadfence();
+        }
+    } else if (s_last) {
         __threadfence();
         uint4 *c = reinterpret_cast<uint4 *>(p.ctr);
         const int n16 = p.ctr_bytes / 16;
@@ -1364,8 +1391,18 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return KOSMOS_ERR_CUDA;
     }
-    return launch_persistent(reinterpret_cast<const void *>(&moe_fwd_kernel), &p, Lc.grid, MOE_SMEM_BYTES, stream,
-                             Lc.plain_launch != 0);
+    if (Lc.sched != KOSMOS_SCHED_UNFUSED)
+        return launch_persistent(reinterpret_cast<const void *>(&moe_fwd_kernel), &p, Lc.grid, MOE_SMEM_BYTES, stream,
+                                 Lc.plain_launch != 0);
+    // unfused baseline: the same kernel once per phase, each launch running
+    // only its phase's entries to completion before the next starts
+    for (int ph = 1; ph <= 5; ++ph) {
+        p.phase = ph;
+        const kosmos_status st = launch_persistent(reinterpret_cast<const void *>(&moe_fwd_kernel), &p, Lc.grid,
+                                                   MOE_SMEM_BYTES, stream, Lc.plain_launch != 0);
+        if (st != KOSMOS_OK) return st;
+    }
+    return KOSMOS_OK;
 }
 
 }  // namespace kosmos

@@ -239,3 +239,19 @@ def test_moe_full_size_sampled(K, orc):
     ref = oracle_experts(orc, inp, kernel_route(out), w.P, tokens=tokens)
     got = bf16_tensor_to_f64(out["y"][0][torch.from_numpy(tokens).cuda()])
     assert rel_err(got, ref) <= TOL, rel_err(got, ref)
+
+
+@pytest.mark.parametrize("P,T,H,E,topk,I", [(4, 512, 512, 64, 4, 256), (2, 400, 256, 64, 8, 128),
+                                            (8, 2048, 4096, 128, 8, 1536)])
+def test_moe_unfused_phases_match_one_launch(K, P, T, H, E, topk, I):
+    """The unfused baseline runs the same kernel once per phase (route and
+    plan | dispatch | gate/up tiles | down tiles | push and fold): every
+    output and routing table equals the one-launch layer's bit for bit, and
+    reruns are bit-identical."""
+    inp = moe_inputs(T, H, E, I, seed=500 + T + E)
+    one = run_moe(K, inp, P, topk)
+    unf = run_moe(K, inp, P, topk, o=K.opts(sched=K.SCHED_UNFUSED), reps=2)
+    assert torch.equal(unf["y"][0], unf["y"][1])
+    assert torch.equal(one["y"][0], unf["y"][0])
+    for key in ("idx", "gate", "counts", "pos"):
+        assert np.array_equal(one[key], unf[key]), key

@@ -257,3 +257,26 @@ def test_moe_bwd_refuses_a_context_that_is_not_a_complete_bf16_forward(K):
     K.moe_bwd(xs, wr, wg, wu, wd, idx, gate, fws, dys, dxs, dwr, dwg, dwu, dwd, bws)
     st, _ = K.status_sync(bws)
     assert st == K.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("P,T,H,E,topk,I", [(4, 512, 512, 64, 8, 512), (2, 384, 512, 64, 3, 256)])
+def test_moe_bwd_unfused_phases_match_one_launch(K, P, T, H, E, topk, I):
+    """The unfused backward runs the same kernel once per phase (head |
+    DH | DWD | DGU | DWGU | DWR | push and fold): every gradient equals the
+    one-launch backward's bit for bit."""
+    inp = moe_inputs(T, H, E, I, seed=960 + T + topk)
+    dout = dout_for(T, H, seed=9)
+    one, _, bws1 = run_fwd_bwd(K, inp, dout, P, topk)
+    unf, _, bws2 = run_fwd_bwd(K, inp, dout, P, topk, reps=2, o=K.opts(sched=K.SCHED_UNFUSED))
+    check_reruns(K, bws2, unf)
+    for key in ("dx", "dwr", "dwg", "dwu", "dwd"):
+        assert torch.equal(one[0][key], unf[0][key]), f"{key}: {first_diff(one[0][key], unf[0][key])}; {diag(K, bws2)}"
+
+
+def test_moe_rejects_fixed_schedule_and_unfused_trace(K):
+    P, T, H, E, topk, I = 2, 256, 256, 64, 2, 256
+    inp = moe_inputs(T, H, E, I, seed=6)
+    with pytest.raises(K.KosmosError):
+        run_fwd_bwd(K, inp, dout_for(T, H, 1), P, topk, o=K.opts(sched=K.SCHED_FIXED))
+    with pytest.raises(K.KosmosError):
+        run_fwd_bwd(K, inp, dout_for(T, H, 1), P, topk, o=K.opts(sched=K.SCHED_UNFUSED, trace=1))

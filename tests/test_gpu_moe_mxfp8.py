@@ -197,3 +197,15 @@ def test_moe_mxfp8_full_size_sampled(K, orc):
     ref = oracle_mx(orc, inp, kernel_route(out), w.P, tokens=tokens)
     got = bf16_tensor_to_f64(out["y"][0][torch.from_numpy(tokens).cuda()])
     assert rel_err(got, ref) <= TOL, rel_err(got, ref)
+
+
+def test_moe_mxfp8_unfused_phases_match_one_launch(K):
+    """MXFP8 layer, unfused baseline (the QUANT entries run in the first
+    launch with the router): outputs bit-identical to the one-launch layer."""
+    P, T, H, E, topk, I = 4, 512, 512, 64, 4, 256
+    inp = moe_inputs(T, H, E, I, seed=41)
+    one = run_moe_mx(K, inp, P, topk)
+    unf = run_moe_mx(K, inp, P, topk, o=K.opts(sched=K.SCHED_UNFUSED), reps=2)
+    assert torch.equal(unf["y"][0], unf["y"][1])
+    assert torch.equal(one["y"][0], unf["y"][0])
+    assert np.array_equal(one["idx"], unf["idx"]) and np.array_equal(one["pos"], unf["pos"])
