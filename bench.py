@@ -220,9 +220,15 @@ def bench_rs(K, dev, steps, warmup, flush, stream, peak):
         fixed[str(crew)] = flops / (timed(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=crew)) * 1e-3) / 1e12
     unf = timed(K.opts(sched=K.SCHED_UNFUSED))
     single = timed(K.opts(cta_pair=0))
+    tfl = lambda ms: flops / (ms * 1e-3) / 1e12
+    link = {"self": tfl(timed(K.opts(link_gbs=LINK_GBS))),
+            "fixed_sweep": {str(c): tfl(timed(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=c, link_gbs=LINK_GBS)))
+                            for c in (1, 2, 3)},
+            "unfused": tfl(timed(K.opts(sched=K.SCHED_UNFUSED, link_gbs=LINK_GBS)))}
+    link["fixed_best"] = max(link["fixed_sweep"].values())
     tf = flops / (band * 1e-3) / 1e12
     best = max(fixed, key=fixed.get)
-    return {"workload": "rs_bf16_p8", "ms": band, "tflops": tf, "frac_of_peak": tf / peak,
+    return {"workload": "rs_bf16_p8", "ms": band, "tflops": tf, "frac_of_peak": tf / peak, "link": link,
             "row_order_ms": row, "row_over_band": row / band,
             "fixed_split_best": {"tflops": fixed[best], "crew_per_rank": int(best), "sweep": fixed},
             "unfused": {"tflops": flops / (unf * 1e-3) / 1e12, "launches_per_step": 2},
@@ -325,7 +331,7 @@ def moe_bwd_algorithmic_bytes(T, H, E, K, I):
     return 2 * w + token + dh + dgu + wgrad_in + push_fold + router
 
 
-def bench_moe_bwd(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0):
+def bench_moe_bwd(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0, unfused=False):
     """MoE layer backward (2048 tokens, hidden 4096, 128 experts top-8, 8 EP
     ranks, inter 1536) in one launch; the forward runs once untimed to fill
     the saved context."""
@@ -367,14 +373,25 @@ def bench_moe_bwd(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, e
     byt = moe_bwd_algorithmic_bytes(T, H, E, Kt, I)
     flops = 12.0 * T * Kt * H * I + 4.0 * T * E * H
     gbs = byt / (t * 1e-3) / 1e9
-    return {"workload": w.name.replace("moe_fwd", "moe_bwd"), "ms": t, "tokens_per_s": T / (t * 1e-3), "tflops": flops / (t * 1e-3) / 1e12,
-            "frac_of_tensor_peak": flops / (t * 1e-3) / 1e12 / tensor_peak,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-                         "bytes_per_launch": byt},
-            "launches_per_step": 1}
+    r = {"workload": w.name.replace("moe_fwd", "moe_bwd"), "ms": t, "tokens_per_s": T / (t * 1e-3),
+         "tflops": flops / (t * 1e-3) / 1e12, "frac_of_tensor_peak": flops / (t * 1e-3) / 1e12 / tensor_peak,
+         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                      "bytes_per_launch": byt},
+         "launches_per_step": 1}
+    if unfused:  # head | DH | DWD | DGU | DWGU | DWR | push + fold, one launch each
+        ou = K.opts(sched=K.SCHED_UNFUSED)
+        fu = lambda: K.moe_bwd(xs, wr, wg, wu, wd, idx, gate, fws, dys, dxs, dwr, dwg, dwu, dwd, bws, ou,
+                               stream=stream)
+        fu()
+        K.check(bws, "moe_bwd unfused")
+        tu = statistics.mean(time_kernel_steps(fu, steps, warmup, flush, stream))
+        K.check(bws, "moe_bwd unfused")
+        r["unfused"] = {"ms": tu, "tokens_per_s": T / (tu * 1e-3), "launches_per_step": 7}
+        r["vs_unfused"] = tu / t
+    return r
 
 
-def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0, mx=False):
+def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, experts=0, mx=False, unfused=False):
     import dataclasses
     import torch
     from kosmos_inputs import WORKLOADS, workload_inputs
@@ -411,11 +428,21 @@ def bench_moe(K, dev, steps, warmup, flush, stream, hbm_peak, tensor_peak, exper
     K.check(wsb, "moe_fwd")
     byt = (moe_algorithmic_bytes_mxfp8 if mx else moe_algorithmic_bytes)(T, H, E, Kt, I)
     gbs = byt / (t * 1e-3) / 1e9
-    return {"workload": w.name, "ms": t, "tokens_per_s": T / (t * 1e-3),
-            "tflops": w.flops() / (t * 1e-3) / 1e12, "frac_of_tensor_peak": w.flops() / (t * 1e-3) / 1e12 / tensor_peak,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-                         "bytes_per_launch": byt},
-            "launches_per_step": 1}
+    r = {"workload": w.name, "ms": t, "tokens_per_s": T / (t * 1e-3),
+         "tflops": w.flops() / (t * 1e-3) / 1e12, "frac_of_tensor_peak": w.flops() / (t * 1e-3) / 1e12 / tensor_peak,
+         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                      "bytes_per_launch": byt},
+         "launches_per_step": 1}
+    if unfused:  # the same kernel once per phase: route | dispatch | gate/up tiles | down tiles | push + fold
+        ou = K.opts(sched=K.SCHED_UNFUSED)
+        fu = lambda: K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, wsb, Kt, ou, stream=stream, **kw)
+        fu()
+        K.check(wsb, "moe_fwd unfused")
+        tu = statistics.mean(time_kernel_steps(fu, steps, warmup, flush, stream))
+        K.check(wsb, "moe_fwd unfused")
+        r["unfused"] = {"ms": tu, "tokens_per_s": T / (tu * 1e-3), "launches_per_step": 5}
+        r["vs_unfused"] = tu / t
+    return r
 
 
 def bench_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=True):
@@ -459,9 +486,16 @@ def bench_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=True)
         return {"workload": "ag_mxfp8_p8", "ms": ms, "tflops": tf, "peak": peak, "frac_of_peak": tf / peak}
     fx, _ = timed(K.opts(sched=K.SCHED_FIXED))
     un, _ = timed(K.opts(sched=K.SCHED_UNFUSED))
+    sms = K.num_sms()
+    link = {"self": timed(K.opts(link_gbs=LINK_GBS))[0],
+            "fixed_sweep": {str(c): timed(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=c, link_gbs=LINK_GBS))[0]
+                            for c in sorted({max(1, sms // 8), max(1, sms // 4), max(1, 3 * sms // 8)})},
+            "unfused": timed(K.opts(sched=K.SCHED_UNFUSED, link_gbs=LINK_GBS))[0]}
+    link["fixed_best"] = max(link["fixed_sweep"].values())
     return {"workload": "ag_mxfp8_p8", "ms": ms, "tflops": tf, "peak": peak,
             "peak_source": "measured bf16 dense x 2 (nominal fp8/bf16 ratio)", "frac_of_peak": tf / peak,
-            "fixed_split_tflops": fx, "unfused_tflops": un, "vs_fixed_split": tf / fx, "vs_unfused": tf / un}
+            "fixed_split_tflops": fx, "unfused_tflops": un, "vs_fixed_split": tf / fx, "vs_unfused": tf / un,
+            "link": link}
 
 
 def bench_rs_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=True):
@@ -506,6 +540,12 @@ def bench_rs_mxfp8(K, dev, steps, warmup, flush, stream, bf16_peak, baselines=Tr
     row, row_ms = timed(K.opts(order=K.ORDER_ROW))
     fx, _ = timed(K.opts(sched=K.SCHED_FIXED))
     un, _ = timed(K.opts(sched=K.SCHED_UNFUSED))
+    link = {"self": timed(K.opts(link_gbs=LINK_GBS))[0],
+            "fixed_sweep": {str(c): timed(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=c, link_gbs=LINK_GBS))[0]
+                            for c in (1, 2, 3)},
+            "unfused": timed(K.opts(sched=K.SCHED_UNFUSED, link_gbs=LINK_GBS))[0]}
+    link["fixed_best"] = max(link["fixed_sweep"].values())
+    r["link"] = link
     r.update({"peak_source": "measured bf16 dense x 2 (nominal fp8/bf16 ratio)", "row_order_ms": row_ms,
               "row_over_band": row_ms / ms, "fixed_split_tflops": fx, "unfused_tflops": un,
               "vs_fixed_split": tf / fx, "vs_unfused": tf / un})
@@ -651,7 +691,9 @@ def compact_baselines(base):
             "fixed_sweep": {c: sig(v) for c, v in base["fixed_split_best"]["sweep"].items()},
             "unfused": sig(base["unfused"]["tflops"]),
             "one_sm_tiles": sig(base["self_single_sm_tiles"]["tflops"]),
-            "n_comm0_sweep": {c: sig(v) for c, v in base["self_n_comm0_sweep"].items()}}
+            "n_comm0_sweep": {c: sig(v) for c, v in base["self_n_comm0_sweep"].items()},
+            "link_self_fixedbest_unfused": [sig(base["link"]["self"]), sig(base["link"]["fixed_best"]),
+                                            sig(base["link"]["unfused"])]}
 
 
 def compact_also(also):
@@ -665,16 +707,24 @@ def compact_also(also):
                              "row_over_band": sig(r["row_over_band"], 3),
                              "fixed_best": sig(r["fixed_split_best"]["tflops"]),
                              "unfused": sig(r["unfused"]["tflops"]),
-                             "one_sm_tiles": sig(r["self_single_sm_tiles_tflops"])}
+                             "one_sm_tiles": sig(r["self_single_sm_tiles_tflops"]),
+                             "link_self_fixedbest_unfused": [sig(r["link"]["self"]), sig(r["link"]["fixed_best"]),
+                                                             sig(r["link"]["unfused"])]}
     r = also.get("ag_mxfp8")
     if r:
         out["ag_mxfp8_p8"] = {"tflops": sig(r["tflops"]), "frac": sig(r["frac_of_peak"], 3), "ms": sig(r["ms"]),
                               "fixed_best": sig(r["fixed_split_tflops"]), "unfused": sig(r["unfused_tflops"])}
+        if "link" in r:
+            out["ag_mxfp8_p8"]["link_self_fixedbest_unfused"] = [sig(r["link"]["self"]), sig(r["link"]["fixed_best"]),
+                                                                 sig(r["link"]["unfused"])]
     r = also.get("rs_mxfp8")
     if r:
         out["rs_mxfp8_p8"] = {"tflops": sig(r["tflops"]), "frac": sig(r["frac_of_peak"], 3), "ms": sig(r["ms"]),
                               "row_over_band": sig(r.get("row_over_band"), 3),
                               "fixed_best": sig(r.get("fixed_split_tflops")), "unfused": sig(r.get("unfused_tflops"))}
+        if "link" in r:
+            out["rs_mxfp8_p8"]["link_self_fixedbest_unfused"] = [sig(r["link"]["self"]), sig(r["link"]["fixed_best"]),
+                                                                 sig(r["link"]["unfused"])]
     for key, name in (("moe_fwd", "moe_fwd_p8"), ("moe_fwd_mxfp8", "moe_fwd_mxfp8_p8"), ("moe_bwd", "moe_bwd_p8")):
         r = also.get(key)
         if r:
@@ -815,6 +865,26 @@ def run_kosmos(args):
         K.check(wsb, "ag_gemm n_comm0")
         sweep[str(nc)] = flops / (statistics.mean(tt) * 1e-3) / 1e12
     base["self_n_comm0_sweep"] = sweep
+    # the same comparison with every remote piece crossing an emulated link
+    # (one GPU's per-direction NVLink 5 bandwidth): role dynamics of a slow link
+    link = {}
+    f, wsb = make(K.opts(link_gbs=LINK_GBS))
+    tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
+    K.check(wsb, "ag_gemm link")
+    link["self"] = flops / (statistics.mean(tt) * 1e-3) / 1e12
+    lfixed = {}
+    for crew in sorted({max(1, sms // 8), max(1, sms // 4), max(1, 3 * sms // 8)}):
+        f, wsb = make(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=crew, link_gbs=LINK_GBS))
+        tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
+        K.check(wsb, "ag_gemm link fixed")
+        lfixed[str(crew)] = flops / (statistics.mean(tt) * 1e-3) / 1e12
+    link["fixed_sweep"] = lfixed
+    link["fixed_best"] = max(lfixed.values())
+    f, wsb = make(K.opts(sched=K.SCHED_UNFUSED, link_gbs=LINK_GBS))
+    tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
+    K.check(wsb, "ag_gemm link unfused")
+    link["unfused"] = flops / (statistics.mean(tt) * 1e-3) / 1e12
+    base["link"] = link
 
     # ---- e2e through the C ABI with host buffers (pinned), copies inside the timed region
     hx = [x.pin_memory() for x in inp["x"]]
@@ -851,18 +921,20 @@ def run_kosmos(args):
     if not args.ag_only:
         also["gemm_rs"] = bench_rs(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
-        also["moe_fwd"] = bench_moe(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"], peak)
+        also["moe_fwd"] = bench_moe(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"], peak,
+                                    unfused=True)
         torch.cuda.empty_cache()
         also["ag_mxfp8"] = bench_mxfp8(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
         also["rs_mxfp8"] = bench_rs_mxfp8(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
         also["moe_fwd_mxfp8"] = bench_moe(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"],
-                                          2 * peak, mx=True)
+                                          2 * peak, mx=True, unfused=True)
         torch.cuda.empty_cache()
         also["attention"] = bench_attn(K, dev, max(3, args.steps // 2), 3, flush, stream, peak)
         torch.cuda.empty_cache()
-        also["moe_bwd"] = bench_moe_bwd(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"], peak)
+        also["moe_bwd"] = bench_moe_bwd(K, dev, max(3, args.steps // 2), 3, flush, stream, peaks["hbm_gbs"], peak,
+                                        unfused=True)
         torch.cuda.empty_cache()
 
     line = None
