@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
@@ -29,6 +30,10 @@ static PFN_encodeTiled_t get_encode_fn() {
     }
     return fn;
 }
+
+// Tokens of the host-input all-gather calls: the value its streams exchange
+// through the workspace's join words, distinct from the previous call's.
+static std::atomic<uint32_t> g_host_flow_token{0};
 
 // Stream memory operations (write / wait on a 32-bit word in device memory).
 typedef CUresult (*PFN_streamValue32_t)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
@@ -401,12 +406,19 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
                                                   (pl.pair ? 2 : 1));
     cudaStream_t s = static_cast<cudaStream_t>(stream), h = static_cast<cudaStream_t>(h2d_stream),
                  d = static_cast<cudaStream_t>(d2h_stream);
-    cudaEvent_t ev[4];
-    for (int i = 0; i < 4; ++i)
-        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return KOSMOS_ERR_CUDA;
-    bool ok = cudaEventRecord(ev[0], s) == cudaSuccess && cudaStreamWaitEvent(h, ev[0], 0) == cudaSuccess &&
-              cudaMemsetAsync(ext, 0, 8 * KOSMOS_MAX_P, h) == cudaSuccess && cudaEventRecord(ev[1], h) == cudaSuccess &&
-              cudaStreamWaitEvent(s, ev[1], 0) == cudaSuccess && cudaStreamWaitEvent(d, ev[1], 0) == cudaSuccess;
+    CUstream cs = reinterpret_cast<CUstream>(s), ch = reinterpret_cast<CUstream>(h), cd = reinterpret_cast<CUstream>(d);
+    // The three streams join through three words of the workspace (no CUDA
+    // events to create per call): `stream` publishes this call's token once
+    // its earlier work (the previous kernel reading x_dev) is done and the
+    // arrival and output words are zeroed; the copy streams wait for it; at
+    // the end each copy stream publishes the token and `stream` waits for both.
+    const CUdeviceptr sync = done + 4 * KOSMOS_MAX_P;  // [0] stream ready, [1] h2d done, [2] d2h done
+    uint32_t tok = g_host_flow_token.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    if (tok == 0u) tok = g_host_flow_token.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    bool ok = cudaMemsetAsync(ext, 0, 8 * KOSMOS_MAX_P, s) == cudaSuccess &&
+              wr(cs, sync, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
+              wt(ch, sync, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS &&
+              wt(cd, sync, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS;
     // shard r to the device, then its arrival word (the local shard first)
     const size_t xb = static_cast<size_t>(m_per_shard * k * 2), yb = static_cast<size_t>(m_per_shard * n * 2);
     for (int r = 0; ok && r < P; ++r)
@@ -423,9 +435,10 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
         ok = wt(reinterpret_cast<CUstream>(d), done + 4 * r, target, CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS &&
              cudaMemcpyAsync(static_cast<uint8_t *>(y_host) + r * yb, static_cast<uint8_t *>(y_dev) + r * yb, yb,
                              cudaMemcpyDeviceToHost, d) == cudaSuccess;
-    ok = ok && cudaEventRecord(ev[2], h) == cudaSuccess && cudaEventRecord(ev[3], d) == cudaSuccess &&
-         cudaStreamWaitEvent(s, ev[2], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev[3], 0) == cudaSuccess;
-    for (int i = 0; i < 4; ++i) cudaEventDestroy(ev[i]);
+    ok = ok && wr(ch, sync + 4, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
+         wr(cd, sync + 8, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
+         wt(cs, sync + 4, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS &&
+         wt(cs, sync + 8, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS;
     if (st != KOSMOS_OK) return st;
     return ok ? KOSMOS_OK : KOSMOS_ERR_CUDA;
 }
