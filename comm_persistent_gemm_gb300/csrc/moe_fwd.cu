@@ -555,7 +555,8 @@ __device__ __noinline__ MoeProdState moe_dispatch(const MoeParams &p, const Smem
         bulk_wait<0>();
         fence_proxy_async_global();
         __threadfence();  // orders the row copies before the relaxed arrival adds below
-        if (ok)
+        const bool drop = (p.inject & KOSMOS_INJECT_DROP_DISPATCH) && static_cast<int64_t>(p.inject >> 32) == ticket;
+        if (ok && !drop)
             for (int r = 0; r < nrows; ++r) red_relaxed_add_gpu(&p.disp_cnt[s_ci[r]], 1u);
         if (TraceRec *rec = trace_rec(p.trace, blockIdx.x, slot)) rec->t_done = static_cast<int64_t>(globaltimer());
     }

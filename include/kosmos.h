@@ -90,6 +90,8 @@ enum { KOSMOS_ORDER_BAND = 0, KOSMOS_ORDER_ROW = 1 };
  * never released, so the waiting side's bounded wait runs out). */
 #define KOSMOS_INJECT_DROP_TRANSFER 0x1ull  /* AG: transfer ticket (inject >> 32) never releases its flag */
 #define KOSMOS_INJECT_DROP_PARTIAL  0x2ull  /* RS: rank (inject >> 32) never signals its partial tiles */
+#define KOSMOS_INJECT_DROP_DISPATCH 0x8ull  /* MoE forward: the DISPATCH entry of main-rail ticket (inject >> 32)
+                                               copies its rows but never counts them as arrived */
 /* MoE debug mode: every expert is the identity map (no expert GEMMs; the
  * pushed rows are the dispatched token rows), which isolates router,
  * dispatch, push and fold.  Not a fault: the output is x * sum of gates. */

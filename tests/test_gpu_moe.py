@@ -255,3 +255,36 @@ def test_moe_unfused_phases_match_one_launch(K, P, T, H, E, topk, I):
     assert torch.equal(one["y"][0], unf["y"][0])
     for key in ("idx", "gate", "counts", "pos"):
         assert np.array_equal(one[key], unf[key]), key
+
+
+def test_moe_dropped_dispatch_times_out_then_recovers(K, orc):
+    """A dispatch whose rows are never counted as arrived: the gate/up tiles
+    waiting for them run out of their bounded wait, the call reports TIMEOUT
+    (every CTA leaves; nothing hangs), and after a workspace re-init the next
+    call matches the oracle."""
+    P, T, H, E, topk, I = 2, 256, 256, 64, 2, 128
+    inp = moe_inputs(T, H, E, I, seed=17)
+    first_dispatch = (T // P + 127) // 128  # main-rail tickets: ROUTE entries first, then DISPATCH
+    o = K.opts(inject=K.INJECT_DROP_DISPATCH | (first_dispatch << 32), wait_limit_ns=2_000_000)
+    dev = "cuda"
+    xs = [t.to(dev) for t in torch.chunk(inp["x"], P, 0)]
+    wr = inp["w_router"].to(dev)
+    wg = [t.to(dev) for t in _split(inp["w_gate"], P)]
+    wu = [t.to(dev) for t in _split(inp["w_up"], P)]
+    wd = [t.to(dev) for t in _split(inp["w_down"], P)]
+    ys = [torch.empty(T // P, H, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    idx = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    gate = torch.empty(T, topk, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    pos = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    ws = K.moe_workspace(P, T, H, E, topk, I, o)
+    K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, ws, topk, o)
+    st, entry = K.status_sync(ws)
+    assert st == K.ERR_TIMEOUT, (st, entry)
+    K.workspace_init(ws)
+    K.moe_fwd(xs, wr, wg, wu, wd, ys, idx, gate, counts, pos, ws, topk, K.opts())
+    K.check(ws, "moe_fwd after re-init")
+    logits = K.moe_debug_view(K.MOE_VIEW_LOGITS, P, T, H, E, topk, I, ws).view(torch.float32).view(T, E)
+    out = {"idx": idx.cpu().numpy(), "gate": gate.cpu().numpy(), "logits": logits.cpu().numpy()}
+    ref = oracle_experts(orc, inp, kernel_route(out), P)
+    assert rel_err(bf16_tensor_to_f64(torch.cat(ys, 0)), ref) <= TOL
