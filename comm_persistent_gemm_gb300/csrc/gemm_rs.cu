@@ -520,15 +520,46 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
         __nv_bfloat16 *dst = p.part + (static_cast<int64_t>(rank) * p.g.m + static_cast<int64_t>(chunk) * p.g.mc +
                                        (valid ? rloc : 0)) * p.g.n;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
+        if constexpr (Cfg::NACC == 1) {
+            // One accumulator (the scale atoms take the other's columns): the
+            // row is copied into registers as bf16 and the accumulator released
+            // before the global stores, so the next tile's MMAs run under them.
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    pk[ch * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            }
+            acc_release(sm, acc, leader, lane);
+            if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
+            if (valid) {
+#pragma unroll
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    const int64_t col0 = static_cast<int64_t>(tcol) * BN + ch * 32;
+                    const int64_t left = p.g.n - col0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q * 8 < left)
+                            *reinterpret_cast<uint4 *>(dst + col0 + q * 8) =
+                                make_uint4(pk[ch * 16 + q * 4], pk[ch * 16 + q * 4 + 1], pk[ch * 16 + q * 4 + 2],
+                                           pk[ch * 16 + q * 4 + 3]);
+                }
+            }
+        } else {
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-            const int64_t col0 = static_cast<int64_t>(tcol) * BN + ch * 32;
-            if (col0 >= p.g.n) break;
-            const int64_t left = p.g.n - col0;
-            tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + col0, left < 32 ? static_cast<int>(left) : 32);
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                const int64_t col0 = static_cast<int64_t>(tcol) * BN + ch * 32;
+                if (col0 >= p.g.n) break;
+                const int64_t left = p.g.n - col0;
+                tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + col0, left < 32 ? static_cast<int>(left) : 32);
+            }
+            acc_release(sm, acc, leader, lane);
+            if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
         }
-        acc_release(sm, acc, leader, lane);
-        if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
         if (p.mode == RS_FUSED) {
             __threadfence();
             named_bar_sync(1, NUM_EPI_THREADS);
