@@ -594,10 +594,14 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
         const int64_t col = static_cast<int64_t>(tcol) * BN + cg * 8;
         bool ok = true;
         for (int sidx = 0; sidx < e.nstage; ++sidx) {
-            // a thread whose wait runs out skips the stage and still takes its
-            // barrier, which makes the decision to stop for all threads
-            const bool got = mbar_wait(&rr.rfull[rp.stage], rp.phase, PIPE_LIMIT_NS);
-            if (!got) set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
+            // each warp releases the stage once its lanes have read it (no
+            // group barrier per stage); a wait that runs out stops the warp
+            const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&rr.rfull[rp.stage], rp.phase, PIPE_LIMIT_NS));
+            if (!got) {
+                set_error(p.ws, KOSMOS_ERR_DEVICE, -8);
+                ok = false;
+                break;
+            }
             const uint8_t *buf = sm.stages + rp.stage * STAGE2_BYTES;
 #pragma unroll
             for (int r2 = 0; got && r2 < 2; ++r2) {
@@ -624,11 +628,8 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
                     *reinterpret_cast<uint4 *>(p.y[chunk] + grow * p.g.n + col) = o;
                 }
             }
-            if (!named_bar_and(1, NUM_EPI_THREADS, got)) {
-                ok = false;
-                break;
-            }
-            if (et == 0) mbar_arrive(&rr.rempty[rp.stage]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rr.rempty[rp.stage]);
             rp.advance();
         }
         if (!ok) break;
@@ -658,7 +659,7 @@ __device__ __forceinline__ void rs_pair_body(const RsParams &p, uint8_t *smem_ra
     if (threadIdx.x == 0) {
         for (int i = 0; i < Cfg::NS; ++i) {
             mbar_init(&rr.rfull[i], 1);
-            mbar_init(&rr.rempty[i], 1);
+            mbar_init(&rr.rempty[i], NUM_EPI_THREADS / 32);  // each epilogue warp releases the stage
         }
         for (int i = 0; i < NSCHED; ++i) {
             mbar_init(&rr.rsfull[i], 1);
