@@ -36,9 +36,9 @@ struct AgF8Params {
     CUtensorMap tmA_gath;   // x_gathered: dims {k, m, P}, box {128, 128, 1}
     CUtensorMap tmB;        // W: dims {n, k}, box {128, 128}
     // SM-pair kernel only: the tiled scales as rows of 16 bytes, one 512-byte atom per box
-    CUtensorMap tmSA_local; // x_scales[0]: dims {16, pieces * nkb * 32}, box {16, 32}
-    CUtensorMap tmSA_gath;  // gathered scales: dims {16, P * pieces * nkb * 32}, box {16, 32}
-    CUtensorMap tmSW;       // W scales: dims {16, nb_w * nkb * 32}, box {16, 32}
+    CUtensorMap tmSA_local; // x_scales[0]: pieces * nkb atoms (encode_sf_tmap)
+    CUtensorMap tmSA_gath;  // gathered scales: P * pieces * nkb atoms
+    CUtensorMap tmSW;       // W scales: nb_w * nkb atoms
     const uint8_t *x_src[KOSMOS_MAX_P];
     const uint8_t *sx_src[KOSMOS_MAX_P];  // tiled scales of each shard
     const uint8_t *sw;                    // tiled scales of W
@@ -322,14 +322,14 @@ __device__ __forceinline__ void f2_load_half(const AgF8Params &p, const F2Smem &
     const int32_t row0 = pc * BM;
     if (local) {
         tma_load_2d_pair(sa, &p.tmA_local, leader_full, kb * FBK, row0);
-        tma_load_2d_pair(sf, &p.tmSA_local, leader_full, 0, (pc * p.nkb + kb) * 32);
+        tma_load_2d_pair(sf, &p.tmSA_local, leader_full, 0, (pc * p.nkb + kb) * SF_ATOM_ROWS);
     } else {
         tma_load_3d_pair(sa, &p.tmA_gath, leader_full, kb * FBK, row0, s);
-        tma_load_2d_pair(sf, &p.tmSA_gath, leader_full, 0, ((s * p.g.pieces + pc) * p.nkb + kb) * 32);
+        tma_load_2d_pair(sf, &p.tmSA_gath, leader_full, 0, ((s * p.g.pieces + pc) * p.nkb + kb) * SF_ATOM_ROWS);
     }
     tma_load_2d_pair(sb, &p.tmB, leader_full, static_cast<int32_t>(col0), kb * FBK);
-    tma_load_2d_pair(sf + 512, &p.tmSW, leader_full, 0, ((2 * tile_c) * p.nkb + kb) * 32);
-    tma_load_2d_pair(sf + 1024, &p.tmSW, leader_full, 0, ((2 * tile_c + 1) * p.nkb + kb) * 32);
+    tma_load_2d_pair(sf + 512, &p.tmSW, leader_full, 0, ((2 * tile_c) * p.nkb + kb) * SF_ATOM_ROWS);
+    tma_load_2d_pair(sf + 1024, &p.tmSW, leader_full, 0, ((2 * tile_c + 1) * p.nkb + kb) * SF_ATOM_ROWS);
 }
 
 __device__ __forceinline__ void f2_producer(const AgF8Params &p, const F2Smem &fs, uint32_t epoch, uint32_t rank) {
@@ -594,26 +594,10 @@ kosmos_status launch_ag_mxfp8(const AgLaunch &L, cudaStream_t stream) {
     if (L.pair) {
         p.g = ag_geom(L.P, L.m, L.k, L.n, PBM);
         p.n_comm = (L.n_comm + 1) / 2;  // mover pairs
-        const uint32_t box[2] = {16, 32};
-        const uint64_t st[1] = {16};
-        {
-            const uint64_t dims[2] = {16, static_cast<uint64_t>(p.g.pieces) * p.nkb * 32};
-            if (!encode_tmap(&p.tmSA_local, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.xs[0]), dims, st, box,
-                             CU_TENSOR_MAP_SWIZZLE_NONE))
-                return KOSMOS_ERR_CUDA;
-        }
-        {
-            const uint64_t dims[2] = {16, static_cast<uint64_t>(L.P) * p.g.pieces * p.nkb * 32};
-            if (!encode_tmap(&p.tmSA_gath, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.sx_gath, dims, st, box,
-                             CU_TENSOR_MAP_SWIZZLE_NONE))
-                return KOSMOS_ERR_CUDA;
-        }
-        {
-            const uint64_t dims[2] = {16, static_cast<uint64_t>(p.nb_w) * p.nkb * 32};
-            if (!encode_tmap(&p.tmSW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.wsc), dims, st, box,
-                             CU_TENSOR_MAP_SWIZZLE_NONE))
-                return KOSMOS_ERR_CUDA;
-        }
+        if (!encode_sf_tmap(&p.tmSA_local, const_cast<void *>(L.xs[0]), static_cast<uint64_t>(p.g.pieces) * p.nkb) ||
+            !encode_sf_tmap(&p.tmSA_gath, p.sx_gath, static_cast<uint64_t>(L.P) * p.g.pieces * p.nkb) ||
+            !encode_sf_tmap(&p.tmSW, const_cast<void *>(L.wsc), static_cast<uint64_t>(p.nb_w) * p.nkb))
+            return KOSMOS_ERR_CUDA;
     }
     if (L.sched == KOSMOS_SCHED_UNFUSED) {
         ag_f8_gather_copy_kernel<<<L.grid * 4, 256, 0, stream>>>(p);

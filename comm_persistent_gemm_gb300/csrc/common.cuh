@@ -37,6 +37,7 @@ constexpr int NUM_THREADS = 192;   // warp 0 scheduler/producer, warp 1 MMA, war
 constexpr int NUM_EPI_THREADS = 128;
 constexpr int TMEM_COLS = 512;     // two 128x256 fp32 accumulators
 constexpr int RED_ROWS = 8;        // rows of one reduce stage (P x 8 x 256 bf16 <= 32 KB)
+constexpr int SF_ATOM_ROWS = 4;    // an MXFP8 scale atom (512 bytes) as tensor-map rows of 128 bytes
 constexpr int MAX_CTAS = 256;
 constexpr int TRACE_CAP = 1024;    // trace records per CTA
 

@@ -30,9 +30,9 @@ struct RsParams {
     CUtensorMap tmW[KOSMOS_MAX_P];  // W_r: dims {n, k}, box {64, 64}, 128B swizzle
     CUtensorMap tmPart;             // partials [rank][chunk][mc][n]: dims {n, mc, P, P}, box {256, 8, 1, P}
     // MXFP8 (SM pairs): tmX/tmW hold E4M3 bytes (boxes {128, 128, 1} / {128, 128}) and these the
-    // tiled scales as rows of 16 bytes, one 512-byte atom per box {16, 32}
-    CUtensorMap tmSX[KOSMOS_MAX_P]; // X_r scales: dims {16, (m / 128) * nkb * 32}
-    CUtensorMap tmSW[KOSMOS_MAX_P]; // W_r scales: dims {16, ceil(n / 128) * nkb * 32}
+    // tiled scales, one 512-byte atom per box (encode_sf_tmap)
+    CUtensorMap tmSX[KOSMOS_MAX_P]; // X_r scales: (m / 128) * nkb atoms
+    CUtensorMap tmSW[KOSMOS_MAX_P]; // W_r scales: ceil(n / 128) * nkb atoms
     __nv_bfloat16 *part;            // [P ranks][m][n]
     __nv_bfloat16 *y[KOSMOS_MAX_P]; // chunk c: [mc][n]
     WsHeader *ws;
@@ -351,9 +351,9 @@ __device__ __forceinline__ void rs2_load_half(const RsParams &p, const Smem2 &sm
         const int rb = static_cast<int>((static_cast<int64_t>(chunk) * p.g.mc + row0) / BM);  // 128-row scale block
         tma_load_3d_pair(sa, &p.tmX[q], fb, kb * FBK, row0, chunk);
         tma_load_2d_pair(sb, &p.tmW[q], fb, col0, kb * FBK);
-        tma_load_2d_pair(sfs, &p.tmSX[q], fb, 0, (rb * p.nkb + kb) * 32);
-        tma_load_2d_pair(sfs + 512, &p.tmSW[q], fb, 0, ((2 * tile_c) * p.nkb + kb) * 32);
-        tma_load_2d_pair(sfs + 1024, &p.tmSW[q], fb, 0, ((2 * tile_c + 1) * p.nkb + kb) * 32);
+        tma_load_2d_pair(sfs, &p.tmSX[q], fb, 0, (rb * p.nkb + kb) * SF_ATOM_ROWS);
+        tma_load_2d_pair(sfs + 512, &p.tmSW[q], fb, 0, ((2 * tile_c) * p.nkb + kb) * SF_ATOM_ROWS);
+        tma_load_2d_pair(sfs + 1024, &p.tmSW[q], fb, 0, ((2 * tile_c + 1) * p.nkb + kb) * SF_ATOM_ROWS);
     } else {
         uint8_t *sb = sa + A2_BYTES;
         tma_load_3d_pair(sa, &p.tmX[q], fb, kb * BK, row0, chunk);
@@ -732,15 +732,8 @@ kosmos_status launch_rs_bf16(const RsLaunch &L, cudaStream_t stream) {
         }
         if (mx) {
             const uint64_t nkb = static_cast<uint64_t>(L.k / FBK);
-            const uint64_t st[1] = {16};
-            const uint32_t box[2] = {16, 32};
-            const uint64_t dx[2] = {16, static_cast<uint64_t>(L.m / BM) * nkb * 32};
-            if (!encode_tmap(&p.tmSX[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.xs[r]), dx, st, box,
-                             CU_TENSOR_MAP_SWIZZLE_NONE))
-                return KOSMOS_ERR_CUDA;
-            const uint64_t dw[2] = {16, static_cast<uint64_t>(cdiv(L.n, 128)) * nkb * 32};
-            if (!encode_tmap(&p.tmSW[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(L.ws_[r]), dw, st, box,
-                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            if (!encode_sf_tmap(&p.tmSX[r], const_cast<void *>(L.xs[r]), static_cast<uint64_t>(L.m / BM) * nkb) ||
+                !encode_sf_tmap(&p.tmSW[r], const_cast<void *>(L.ws_[r]), static_cast<uint64_t>(cdiv(L.n, 128)) * nkb))
                 return KOSMOS_ERR_CUDA;
         }
         p.y[r] = static_cast<__nv_bfloat16 *>(L.y[r]);

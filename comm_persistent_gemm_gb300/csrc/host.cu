@@ -68,6 +68,13 @@ bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, void *base,
     return r == CUDA_SUCCESS;
 }
 
+bool encode_sf_tmap(CUtensorMap *map, void *base, uint64_t atoms) {
+    const uint64_t dims[2] = {128, atoms * SF_ATOM_ROWS};
+    const uint64_t st[1] = {128};
+    const uint32_t box[2] = {128, SF_ATOM_ROWS};
+    return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream,
                                 bool plain) {
     if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)

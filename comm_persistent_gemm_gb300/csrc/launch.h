@@ -89,6 +89,13 @@ struct MoeLaunch {
 bool encode_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, void *base, const uint64_t *dims,
                  const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
 
+// Tensor map over `atoms` MXFP8 scale atoms stored one after another from
+// `base` (512 contiguous bytes each): four rows of 128 bytes per atom, box
+// = one atom.  The copy unit's cost follows the rows of a box, so an atom
+// costs four rows here instead of the 32 of its 16-byte scale rows.  Atom a
+// starts at row a * SF_ATOM_ROWS.
+bool encode_sf_tmap(CUtensorMap *map, void *base, uint64_t atoms);
+
 // Cooperative launch of a persistent kernel whose only argument is *params
 // (plain = true: the same grid without the cooperative attribute).
 kosmos_status launch_persistent(const void *func, void *params, int grid, int smem_bytes, cudaStream_t stream,

@@ -62,7 +62,7 @@ struct MoeParams {
     CUtensorMap tmSlot;              // slot buffer: dims {H, T*K}, box {256, fold_tps*K}, no swizzle
     // MXFP8 (the maps above then hold E4M3 bytes: tmRecv, tmH box {128, 128};
     // tmWg, tmWu, tmWd box {128, 128, 1}): tiled scales as rows of 16 bytes,
-    // one 512-byte atom per box {16, 32}
+    // one 512-byte atom per box (encode_sf_tmap)
     CUtensorMap tmSRecv;             // receive-row scales, K = H
     CUtensorMap tmSH;                // h scales, K = I
     CUtensorMap tmSWg[KOSMOS_MAX_P]; // per expert: I/128 column atoms x H/128 K atoms
@@ -370,17 +370,17 @@ __device__ __forceinline__ int moe_decide(const MoeParams &p, const Smem &sm, Mo
                         tma_load_2d(sa, &p.tmRecv, bar, kb * FBK, row0);
                         tma_load_3d(sb, &p.tmWg[q], bar, col * 128, kb * FBK, le);
                         tma_load_3d(sb + 16384, &p.tmWu[q], bar, col * 128, kb * FBK, le);
-                        tma_load_2d(sfs, &p.tmSRecv, bar, 0, ((row0 / BM) * g.nkb_h + kb) * 32);
-                        tma_load_2d(sfs + 512, &p.tmSWg[q], bar, 0, wa * 32);
-                        tma_load_2d(sfs + 1024, &p.tmSWu[q], bar, 0, wa * 32);
+                        tma_load_2d(sfs, &p.tmSRecv, bar, 0, ((row0 / BM) * g.nkb_h + kb) * SF_ATOM_ROWS);
+                        tma_load_2d(sfs + 512, &p.tmSWg[q], bar, 0, wa * SF_ATOM_ROWS);
+                        tma_load_2d(sfs + 1024, &p.tmSWu[q], bar, 0, wa * SF_ATOM_ROWS);
                     } else {
                         const int wa = (le * 2 * g.ND + 2 * col) * g.nkb_i + kb;  // down atoms of columns 2col, 2col+1
                         tma_load_2d(sa, &p.tmH, bar, kb * FBK, row0);
                         tma_load_3d(sb, &p.tmWd[q], bar, col * BN, kb * FBK, le);
                         tma_load_3d(sb + 16384, &p.tmWd[q], bar, col * BN + 128, kb * FBK, le);
-                        tma_load_2d(sfs, &p.tmSH, bar, 0, ((row0 / BM) * g.nkb_i + kb) * 32);
-                        tma_load_2d(sfs + 512, &p.tmSWd[q], bar, 0, wa * 32);
-                        tma_load_2d(sfs + 1024, &p.tmSWd[q], bar, 0, (wa + g.nkb_i) * 32);
+                        tma_load_2d(sfs, &p.tmSH, bar, 0, ((row0 / BM) * g.nkb_i + kb) * SF_ATOM_ROWS);
+                        tma_load_2d(sfs + 512, &p.tmSWd[q], bar, 0, wa * SF_ATOM_ROWS);
+                        tma_load_2d(sfs + 1024, &p.tmSWd[q], bar, 0, (wa + g.nkb_i) * SF_ATOM_ROWS);
                     }
                     st.ps.advance();
                     continue;
@@ -1332,15 +1332,10 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
         }
         if (mx) {
             // tiled weight scales, experts one after the other: I*H/32 bytes each
-            const uint64_t st[1] = {16};
-            const uint32_t box[2] = {16, 32};
-            const uint64_t dims[2] = {16, Eq * I * H / 32 / 16};
-            if (!encode_tmap(&p.tmSWg[q], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Lc.wgs[q]), dims, st,
-                             box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-                !encode_tmap(&p.tmSWu[q], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Lc.wus[q]), dims, st,
-                             box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-                !encode_tmap(&p.tmSWd[q], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Lc.wds[q]), dims, st,
-                             box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            const uint64_t atoms = Eq * I * H / 32 / 512;
+            if (!encode_sf_tmap(&p.tmSWg[q], const_cast<void *>(Lc.wgs[q]), atoms) ||
+                !encode_sf_tmap(&p.tmSWu[q], const_cast<void *>(Lc.wus[q]), atoms) ||
+                !encode_sf_tmap(&p.tmSWd[q], const_cast<void *>(Lc.wds[q]), atoms))
                 return KOSMOS_ERR_CUDA;
         }
     }
@@ -1364,13 +1359,8 @@ kosmos_status launch_moe_fwd(const MoeLaunch &Lc, cudaStream_t stream) {
             !encode_tmap(&p.tmH, adt, 2, p.h, dh, sh, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return KOSMOS_ERR_CUDA;
         if (mx) {
-            const uint64_t st[1] = {16};
-            const uint32_t sbox[2] = {16, 32};
-            const uint64_t dsr[2] = {16, RC * H / 32 / 16}, dsh[2] = {16, RC * I / 32 / 16};
-            if (!encode_tmap(&p.tmSRecv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.recv_sf, dsr, st, sbox,
-                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
-                !encode_tmap(&p.tmSH, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.h_sf, dsh, st, sbox,
-                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            if (!encode_sf_tmap(&p.tmSRecv, p.recv_sf, RC * H / 32 / 512) ||
+                !encode_sf_tmap(&p.tmSH, p.h_sf, RC * I / 32 / 512))
                 return KOSMOS_ERR_CUDA;
         }
     }
