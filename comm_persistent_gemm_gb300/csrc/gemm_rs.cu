@@ -13,8 +13,11 @@
 //                acquire counter == P arrivals, sum the P partials in rank
 //                order 0..P-1 in fp32, round once to bf16 into y_chunks[r].
 // CTA c reduces for rank c mod P.  Builders whose tile rail runs out join
-// that rank's reduction (one-way, explainer "KOSMOS removes the manager");
-// n_comm CTAs per rank reduce from the start.
+// that rank's reduction (one-way, explainer "KOSMOS removes the manager").
+// n_comm CTAs per rank are the rank's first reducers: with self-scheduling
+// they build until the rank's next reduce entry has all its arrivals and
+// then switch (data readiness, not a start-up split); in the fixed split
+// they reduce from the start.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -59,18 +62,33 @@ __device__ __forceinline__ uint64_t rs_tile_bytes(const RsParams &p, int64_t r0,
     return static_cast<uint64_t>(rows * cols * 2);
 }
 
+// True when the next unclaimed entry of rank r's reduce rail has `need`
+// arrivals (relaxed reads: a hint for the switch; the reducer acquires the
+// counter itself before it reads the partials).
+__device__ __forceinline__ bool rs_reduce_ready(const RsParams &p, int r, uint32_t need) {
+    const uint32_t t = ld_relaxed_gpu(&p.ws->tickets[KOSMOS_MAX_P + r]);
+    if (t >= static_cast<uint32_t>(p.g.n_reduce)) return false;
+    int band, tcol;
+    rs_decode_reduce(p.g, static_cast<int>(t), band, tcol);
+    return ld_relaxed_gpu(&p.arrive[(static_cast<int64_t>(r) * p.g.bands + band) * p.g.tiles_n + tcol]) >= need;
+}
+
 __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
     const int cta = blockIdx.x;
     const int P = p.g.P;
     const int rank = cta % P;
     const int local = cta / P;
-    bool reducer = (p.mode == RS_REDUCE_ONLY) || (p.mode == RS_FUSED && local < p.n_red);
+    // first reducers: from the start in the fixed split, on the first ready entry when self-scheduled
+    const bool first = p.mode == RS_FUSED && local < p.n_red;
+    const bool on_ready = first && p.sched == KOSMOS_SCHED_SELF;
+    bool reducer = (p.mode == RS_REDUCE_ONLY) || (first && !on_ready);
     PipeState ps;
     RingState rs;
     int nrec = 0;
     const uint32_t red_bytes = static_cast<uint32_t>(BN * RED_ROWS * 2 * P);
     while (true) {
         if (failed(p.ws)) break;
+        if (!reducer && on_ready && rs_reduce_ready(p, rank, static_cast<uint32_t>(P))) reducer = true;
         if (!reducer) {
             const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
             if (t < static_cast<uint32_t>(p.g.n_tile)) {
@@ -369,9 +387,13 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
     const int P = p.g.P;
     const int pair = blockIdx.x / 2;
     const bool leader = crank == 0;
-    // the first n_red pairs reduce from the start, each of their CTAs for rank (CTA index mod P);
-    // builder pairs build tiles of any rank and reduce for rank (pair index mod P) after the switch
-    const bool reducer_pair = (p.mode == RS_REDUCE_ONLY) || (p.mode == RS_FUSED && pair < p.n_red);
+    // the first n_red pairs are the first reducers, each of their CTAs for rank (CTA index mod P):
+    // from the start in the fixed split; self-scheduled, they build until either CTA's rank has a
+    // ready reduce entry.  Builder pairs build tiles of any rank and reduce for rank (pair index
+    // mod P) after the switch.
+    const bool first = p.mode == RS_FUSED && pair < p.n_red;
+    const bool on_ready = first && p.sched == KOSMOS_SCHED_SELF;
+    const bool reducer_pair = (p.mode == RS_REDUCE_ONLY) || first;
     const int rank = (reducer_pair && p.mode == RS_FUSED) ? static_cast<int>(blockIdx.x) % P : pair % P;
     PipeStateN<Cfg::NS> ps;
     RingPair rs;
@@ -379,7 +401,11 @@ __device__ __forceinline__ void rs2_producer(const RsParams &p, const Smem2 &sm,
     // ---- tile phase (pair)
     if (leader) {
         const uint32_t my_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
-        while (!reducer_pair && !failed(p.ws)) {
+        const int r_peer = static_cast<int>(blockIdx.x + 1) % P;
+        while ((!reducer_pair || on_ready) && !failed(p.ws)) {
+            if (on_ready && (rs_reduce_ready(p, rank, static_cast<uint32_t>(2 * P)) ||
+                             rs_reduce_ready(p, r_peer, static_cast<uint32_t>(2 * P))))
+                break;
             const uint32_t t = atomicAdd(&p.ws->tickets[0], 1u);
             if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
             int q, chunk, band, tcol;

@@ -99,7 +99,8 @@ enum { KOSMOS_ORDER_BAND = 0, KOSMOS_ORDER_ROW = 1 };
 
 typedef struct kosmos_opts {
     int32_t sched;            /* KOSMOS_SCHED_* */
-    int32_t n_comm0;          /* CTAs that start as movers (AG) / reducers per rank (RS); -1 = default */
+    int32_t n_comm0;          /* CTAs that start as movers (AG) / first reducers per rank (RS: self-scheduled,
+                                 they build until their rank has a ready reduce entry); -1 = default */
     int32_t fixed_comm_ctas;  /* FIXED: size of the static mover / reducer crew (per rank for RS); -1 = n_comm0 */
     int32_t order;            /* KOSMOS_ORDER_* (GEMM+RS) */
     int32_t num_ctas;         /* -1 = one CTA per SM */
