@@ -297,12 +297,17 @@ __device__ __forceinline__ void ag_epilogue(const AgParams &p, const Smem &sm, u
             khalf_epilogue(taddr, valid, yrow, e.c, p.g.n, p.kpart + cs * (BM * BN / 4), &p.ksync[cs * 2],
                            &p.ksync[cs * 2 + 1], epoch, p.ws, p.wait_limit_ns, e.ticket, row, sm.tmem_slot + 1);
         } else {
+            const int64_t rw = static_cast<int64_t>(i) * BM + grp * 32;  // the warp's first row
+            const int64_t rleft = p.g.m - rw;
+            const int rows_w = rleft <= 0 ? 0 : (rleft >= 32 ? 32 : static_cast<int>(rleft));
+            __nv_bfloat16 *base = p.y + (static_cast<int64_t>(s) * p.g.m + (rows_w > 0 ? rw : 0)) * p.g.n;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                const int64_t col0 = static_cast<int64_t>(e.c) + ch * 32;
+            for (int c64 = 0; c64 < BN / 64; ++c64) {
+                const int64_t col0 = static_cast<int64_t>(e.c) + c64 * 64;
                 if (col0 >= p.g.n) break;
                 const int64_t left = p.g.n - col0;
-                tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
+                tmem_rows64_to_bf16_lines(taddr + c64 * 64, base + col0, p.g.n, rows_w,
+                                          left < 64 ? static_cast<int>(left) : 64, lane);
             }
         }
         tc_fence_before();
@@ -515,12 +520,17 @@ __device__ __forceinline__ void ag2_epilogue(const AgParams &p, const Smem2 &sm,
             khalf_epilogue(taddr, valid, yrow, e.c, p.g.n, p.kpart + cs * (BM * BN / 4), &p.ksync[cs * 2],
                            &p.ksync[cs * 2 + 1], epoch, p.ws, p.wait_limit_ns, e.ticket, row, sm.tmem_slot + 1);
         } else {
+            const int64_t rw = static_cast<int64_t>(i2) * PBM + rank * HBM_ROWS + grp * 32;  // the warp's first row
+            const int64_t rleft = p.g.m - rw;
+            const int rows_w = rleft <= 0 ? 0 : (rleft >= 32 ? 32 : static_cast<int>(rleft));
+            __nv_bfloat16 *base = p.y + (static_cast<int64_t>(s) * p.g.m + (rows_w > 0 ? rw : 0)) * p.g.n;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                const int64_t col0 = static_cast<int64_t>(e.c) + ch * 32;
+            for (int c64 = 0; c64 < BN / 64; ++c64) {
+                const int64_t col0 = static_cast<int64_t>(e.c) + c64 * 64;
                 if (col0 >= p.g.n) break;
                 const int64_t left = p.g.n - col0;
-                tmem_row_chunk_to_bf16(taddr + ch * 32, valid, yrow + col0, left < 32 ? static_cast<int>(left) : 32);
+                tmem_rows64_to_bf16_lines(taddr + c64 * 64, base + col0, p.g.n, rows_w,
+                                          left < 64 ? static_cast<int>(left) : 64, lane);
             }
         }
         acc_release(sm, acc, leader, lane);

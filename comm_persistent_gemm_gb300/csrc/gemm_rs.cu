@@ -181,8 +181,7 @@ __device__ __forceinline__ void rs_producer(const RsParams &p, const Smem &sm) {
 
 __device__ __forceinline__ void rs_epilogue(const RsParams &p, const Smem &sm, uint32_t tmem_base, int warp,
                                             int lane) {
-    const int grp = warp & 3;
-    const int row = grp * 32 + lane;       // accumulator row of this thread
+    const int grp = warp & 3;              // TMEM lanes 32 grp .. 32 grp + 31 (accumulator rows)
     const int et = (warp - 2) * 32 + lane; // 0..127 within the epilogue warps
     const int P = p.g.P;
     RingState rs;
@@ -205,17 +204,19 @@ __device__ __forceinline__ void rs_epilogue(const RsParams &p, const Smem &sm, u
             }
             tc_fence_after();
             const int chunk = e.a, band = e.b, tcol = e.c, rank = e.d;
-            const int64_t rloc = static_cast<int64_t>(band) * BM + row;
-            const bool valid = rloc < p.g.mc;
-            __nv_bfloat16 *dst = p.part + (static_cast<int64_t>(rank) * p.g.m + static_cast<int64_t>(chunk) * p.g.mc +
-                                           (valid ? rloc : 0)) * p.g.n;
+            const int64_t rw = static_cast<int64_t>(band) * BM + grp * 32;  // the warp's first row
+            const int64_t rleft = p.g.mc - rw;
+            const int rows_w = rleft <= 0 ? 0 : (rleft >= 32 ? 32 : static_cast<int>(rleft));
+            __nv_bfloat16 *base = p.part + (static_cast<int64_t>(rank) * p.g.m + static_cast<int64_t>(chunk) * p.g.mc +
+                                            (rows_w > 0 ? rw : 0)) * p.g.n;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                const int64_t col0 = static_cast<int64_t>(tcol) * BN + ch * 32;
+            for (int c64 = 0; c64 < BN / 64; ++c64) {
+                const int64_t col0 = static_cast<int64_t>(tcol) * BN + c64 * 64;
                 if (col0 >= p.g.n) break;
                 const int64_t left = p.g.n - col0;
-                tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + col0, left < 32 ? static_cast<int>(left) : 32);
+                tmem_rows64_to_bf16_lines(taddr + c64 * 64, base + col0, p.g.n, rows_w,
+                                          left < 64 ? static_cast<int>(left) : 64, lane);
             }
             tc_fence_before();
             __syncwarp();
@@ -576,12 +577,18 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
                 }
             }
         } else {
+            const int64_t rw = static_cast<int64_t>(band) * PBM + crank * HBM_ROWS + grp * 32;  // the warp's first row
+            const int64_t rleft = p.g.mc - rw;
+            const int rows_w = rleft <= 0 ? 0 : (rleft >= 32 ? 32 : static_cast<int>(rleft));
+            __nv_bfloat16 *base = p.part + (static_cast<int64_t>(rank) * p.g.m + static_cast<int64_t>(chunk) * p.g.mc +
+                                            (rows_w > 0 ? rw : 0)) * p.g.n;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                const int64_t col0 = static_cast<int64_t>(tcol) * BN + ch * 32;
+            for (int c64 = 0; c64 < BN / 64; ++c64) {
+                const int64_t col0 = static_cast<int64_t>(tcol) * BN + c64 * 64;
                 if (col0 >= p.g.n) break;
                 const int64_t left = p.g.n - col0;
-                tmem_row_chunk_to_bf16(taddr + ch * 32, valid, dst + col0, left < 32 ? static_cast<int>(left) : 32);
+                tmem_rows64_to_bf16_lines(taddr + c64 * 64, base + col0, p.g.n, rows_w,
+                                          left < 64 ? static_cast<int>(left) : 64, lane);
             }
             acc_release(sm, acc, leader, lane);
             if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
