@@ -227,11 +227,29 @@ __device__ __forceinline__ void f8_mma_loop(const F8Smem &fs, uint32_t tmem_base
     }
 }
 
+// A warp's 32 drained rows (row-per-lane, four 64-column blocks of bf16
+// pairs) stored as 128-byte row segments of Y: shard s, the warp's first
+// row rw, column tile c.  All 32 lanes call it.
+__device__ __forceinline__ void ag_f8_store_rows(const AgF8Params &p, uint32_t (&packed)[BN / 64][32], int s,
+                                                 int64_t rw, int c, int lane) {
+    const int64_t rleft = p.g.m - rw;
+    const int rows_w = rleft <= 0 ? 0 : (rleft >= 32 ? 32 : static_cast<int>(rleft));
+    __nv_bfloat16 *base = p.y + (static_cast<int64_t>(s) * p.g.m + (rows_w > 0 ? rw : 0)) * p.g.n;
+#pragma unroll
+    for (int c64 = 0; c64 < BN / 64; ++c64) {
+        const int64_t col0 = static_cast<int64_t>(c) * BN + c64 * 64;
+        const int64_t left = p.g.n - col0;
+        if (left > 0) {  // warp-uniform
+            lane_transpose8_16B(packed[c64], lane);
+            store_row_lines(packed[c64], base + col0, p.g.n, rows_w, left < 64 ? static_cast<int>(left) : 64, lane);
+        }
+    }
+}
+
 // Drains the accumulator into registers (bf16-packed), releases it, then stores.
 __device__ __forceinline__ void f8_epilogue(const AgF8Params &p, const Smem &sm, uint32_t tmem_base, int warp,
                                             int lane) {
-    const int grp = warp & 3;
-    const int row = grp * 32 + lane;
+    const int grp = warp & 3;  // TMEM lanes (accumulator rows) 32 grp .. 32 grp + 31
     RingState rs;
     uint32_t acc_phase = 0;
     while (true) {
@@ -251,7 +269,7 @@ __device__ __forceinline__ void f8_epilogue(const AgF8Params &p, const Smem &sm,
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16);
-        uint32_t packed[BN / 2];
+        uint32_t packed[BN / 64][32];
 #pragma unroll
         for (int ch = 0; ch < BN / 32; ++ch) {
             uint32_t r[32];
@@ -259,24 +277,14 @@ __device__ __forceinline__ void f8_epilogue(const AgF8Params &p, const Smem &sm,
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                packed[ch * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                packed[ch / 2][(ch % 2) * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tempty[0]);
         acc_phase ^= 1u;
         const int s = e.a, i = e.b, c = e.c;
-        const int64_t rloc = static_cast<int64_t>(i) * BM + row;
-        if (rloc < p.g.m) {
-            __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + rloc) * p.g.n;
-#pragma unroll
-            for (int q = 0; q < BN / 8; ++q) {
-                const int64_t col = static_cast<int64_t>(c) * BN + q * 8;
-                if (col < p.g.n)
-                    *reinterpret_cast<uint4 *>(yrow + col) =
-                        make_uint4(packed[q * 4], packed[q * 4 + 1], packed[q * 4 + 2], packed[q * 4 + 3]);
-            }
-        }
+        ag_f8_store_rows(p, packed, s, static_cast<int64_t>(i) * BM + grp * 32, c, lane);
         if (e.slot >= 0 && lane == 0 && grp == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
         }
@@ -443,8 +451,7 @@ __device__ __forceinline__ void f2_producer(const AgF8Params &p, const F2Smem &f
 __device__ __forceinline__ void f2_epilogue(const AgF8Params &p, const Smem2 &sm, uint32_t tmem_base, int warp, int lane,
                                             uint32_t rank) {
     const bool leader = rank == 0;
-    const int grp = warp & 3;
-    const int row = grp * 32 + lane;
+    const int grp = warp & 3;  // TMEM lanes (accumulator rows) 32 grp .. 32 grp + 31
     RingPair rs;
     uint32_t acc_phase = 0;
     while (true) {
@@ -458,7 +465,7 @@ __device__ __forceinline__ void f2_epilogue(const AgF8Params &p, const Smem2 &sm
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16);
-        uint32_t packed[BN / 2];
+        uint32_t packed[BN / 64][32];
 #pragma unroll
         for (int ch = 0; ch < BN / 32; ++ch) {
             uint32_t r[32];
@@ -466,22 +473,12 @@ __device__ __forceinline__ void f2_epilogue(const AgF8Params &p, const Smem2 &sm
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                packed[ch * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                packed[ch / 2][(ch % 2) * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
         }
         acc_release(sm, 0, leader, lane);
         acc_phase ^= 1u;
         const int s = e.a, i2 = e.b, c = e.c;
-        const int64_t rloc = static_cast<int64_t>(i2) * PBM + rank * HBM_ROWS + row;
-        if (rloc < p.g.m) {
-            __nv_bfloat16 *yrow = p.y + (static_cast<int64_t>(s) * p.g.m + rloc) * p.g.n;
-#pragma unroll
-            for (int q = 0; q < BN / 8; ++q) {
-                const int64_t col = static_cast<int64_t>(c) * BN + q * 8;
-                if (col < p.g.n)
-                    *reinterpret_cast<uint4 *>(yrow + col) =
-                        make_uint4(packed[q * 4], packed[q * 4 + 1], packed[q * 4 + 2], packed[q * 4 + 3]);
-            }
-        }
+        ag_f8_store_rows(p, packed, s, static_cast<int64_t>(i2) * PBM + rank * HBM_ROWS + grp * 32, c, lane);
         if (leader && e.slot >= 0 && lane == 0 && grp == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
         }

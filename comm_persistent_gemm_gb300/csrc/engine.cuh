@@ -482,14 +482,48 @@ __device__ __forceinline__ void tmem_row_chunk_to_bf16(uint32_t taddr, bool row_
     }
 }
 
-// 64 accumulator columns of this thread's row (lane = row of the warp's 32)
-// to bf16, then an 8 x 8 transpose of 16-byte units among lanes 8g..8g+7
-// (three butterfly stages of shuffles): afterwards lane 8g+i holds unit i
-// (columns 8i..8i+7) of rows 8g..8g+7, so each warp store instruction
-// writes four whole 128-byte row segments instead of 16 bytes of 32 rows.
-// dst0: the warp's first row at the chunk's first column; ld: row stride;
-// rows / ncols: valid rows of the warp's 32 and valid columns of the 64.
-// All 32 lanes must call it (shuffles).
+// Row-segment stores from the epilogue's row-per-lane layout.  Each
+// epilogue thread holds one accumulator row (lane = row of the warp's 32).
+// v holds eight 16-byte units (4 words each: 8 bf16 columns) of this lane's
+// row; after an 8 x 8 transpose of units among lanes 8g..8g+7 (three
+// butterfly stages of shuffles) lane 8g+i holds unit i of rows 8g..8g+7, so
+// each warp store instruction writes four whole 128-byte row segments
+// instead of 16 bytes of 32 rows.  All 32 lanes must call it (shuffles).
+__device__ __forceinline__ void lane_transpose8_16B(uint32_t (&v)[32], int lane) {
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+        const bool up = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j & m) continue;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t send = up ? v[4 * j + w] : v[4 * (j + m) + w];
+                const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
+                if (up) v[4 * j + w] = recv;
+                else v[4 * (j + m) + w] = recv;
+            }
+        }
+    }
+}
+// Stores the transposed block: dst0 = the warp's first row at the block's
+// first column, ld = row stride, rows / ncols = valid rows of the warp's 32
+// and valid columns of the 64 (a multiple of 8).
+__device__ __forceinline__ void store_row_lines(const uint32_t (&v)[32], __nv_bfloat16 *dst0, int64_t ld, int rows,
+                                                int ncols, int lane) {
+    const int g = lane >> 3, i = lane & 7;
+    if (8 * i < ncols) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int r = 8 * g + s;
+            if (r < rows)
+                *reinterpret_cast<uint4 *>(dst0 + r * ld + 8 * i) =
+                    make_uint4(v[4 * s], v[4 * s + 1], v[4 * s + 2], v[4 * s + 3]);
+        }
+    }
+}
+// 64 accumulator columns of this thread's row to bf16, stored as row
+// segments (arguments as for store_row_lines).
 __device__ __forceinline__ void tmem_rows64_to_bf16_lines(uint32_t taddr, __nv_bfloat16 *dst0, int64_t ld, int rows,
                                                           int ncols, int lane) {
     uint32_t pk[32];
@@ -504,31 +538,8 @@ __device__ __forceinline__ void tmem_rows64_to_bf16_lines(uint32_t taddr, __nv_b
             pk[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
         }
     }
-#pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {
-        const bool up = (lane & m) != 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j & m) continue;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t send = up ? pk[4 * j + w] : pk[4 * (j + m) + w];
-                const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
-                if (up) pk[4 * j + w] = recv;
-                else pk[4 * (j + m) + w] = recv;
-            }
-        }
-    }
-    const int g = lane >> 3, i = lane & 7;
-    if (8 * i < ncols) {
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const int r = 8 * g + s;
-            if (r < rows)
-                *reinterpret_cast<uint4 *>(dst0 + r * ld + 8 * i) =
-                    make_uint4(pk[4 * s], pk[4 * s + 1], pk[4 * s + 2], pk[4 * s + 3]);
-        }
-    }
+    lane_transpose8_16B(pk, lane);
+    store_row_lines(pk, dst0, ld, rows, ncols, lane);
 }
 
 // Epilogue of one CTA's 128 x 256 accumulator for a tile computed as two K

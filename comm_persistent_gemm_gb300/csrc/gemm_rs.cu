@@ -524,8 +524,7 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
                                              int warp, int lane, uint32_t crank) {
     using Cfg = RsPairCfg<MX>;
     const bool leader = crank == 0;
-    const int grp = warp & 3;
-    const int row = grp * 32 + lane;
+    const int grp = warp & 3;  // TMEM lanes (accumulator rows) 32 grp .. 32 grp + 31
     const int et = (warp - 2) * 32 + lane;
     const int P = p.g.P;
     RingPair rs;
@@ -542,16 +541,12 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
         }
         tc_fence_after();
         const int chunk = e.a, band = e.b, tcol = e.c, rank = e.d;
-        const int64_t rloc = static_cast<int64_t>(band) * PBM + crank * HBM_ROWS + row;
-        const bool valid = rloc < p.g.mc;
-        __nv_bfloat16 *dst = p.part + (static_cast<int64_t>(rank) * p.g.m + static_cast<int64_t>(chunk) * p.g.mc +
-                                       (valid ? rloc : 0)) * p.g.n;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(grp * 32) << 16) + acc * BN;
         if constexpr (Cfg::NACC == 1) {
             // One accumulator (the scale atoms take the other's columns): the
             // row is copied into registers as bf16 and the accumulator released
             // before the global stores, so the next tile's MMAs run under them.
-            uint32_t pk[BN / 2];
+            uint32_t pk[BN / 64][32];
 #pragma unroll
             for (int ch = 0; ch < BN / 32; ++ch) {
                 uint32_t r[32];
@@ -559,21 +554,22 @@ __device__ __forceinline__ void rs2_epilogue(const RsParams &p, const Smem2 &sm,
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    pk[ch * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                    pk[ch / 2][(ch % 2) * 16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
             }
             acc_release(sm, acc, leader, lane);
             if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
-            if (valid) {
+            const int64_t rw = static_cast<int64_t>(band) * PBM + crank * HBM_ROWS + grp * 32;  // the warp's first row
+            const int64_t rleft = p.g.mc - rw;
+            const int rows_w = rleft <= 0 ? 0 : (rleft >= 32 ? 32 : static_cast<int>(rleft));
+            __nv_bfloat16 *base = p.part + (static_cast<int64_t>(rank) * p.g.m + static_cast<int64_t>(chunk) * p.g.mc +
+                                            (rows_w > 0 ? rw : 0)) * p.g.n;
 #pragma unroll
-                for (int ch = 0; ch < BN / 32; ++ch) {
-                    const int64_t col0 = static_cast<int64_t>(tcol) * BN + ch * 32;
-                    const int64_t left = p.g.n - col0;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q * 8 < left)
-                            *reinterpret_cast<uint4 *>(dst + col0 + q * 8) =
-                                make_uint4(pk[ch * 16 + q * 4], pk[ch * 16 + q * 4 + 1], pk[ch * 16 + q * 4 + 2],
-                                           pk[ch * 16 + q * 4 + 3]);
+            for (int c64 = 0; c64 < BN / 64; ++c64) {
+                const int64_t col0 = static_cast<int64_t>(tcol) * BN + c64 * 64;
+                const int64_t left = p.g.n - col0;
+                if (left > 0) {  // warp-uniform
+                    lane_transpose8_16B(pk[c64], lane);
+                    store_row_lines(pk[c64], base + col0, p.g.n, rows_w, left < 64 ? static_cast<int>(left) : 64, lane);
                 }
             }
         } else {
