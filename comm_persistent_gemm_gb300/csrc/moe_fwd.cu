@@ -984,43 +984,44 @@ __device__ __forceinline__ void moe_epilogue(const MoeParams &p, const Smem &sm,
                 }
                 if (valid) *reinterpret_cast<uint32_t *>(p.h_sf + sf_tiled_offset(r, 4 * e.c, g.I / 32)) = sw;
             } else if (e.kind == K_TILE_GU) {
-                const bool valid = row < e.x1;
-                const int64_t hoff = static_cast<int64_t>(e.x0 + (valid ? row : 0)) * g.I + e.c * 128;
-                __nv_bfloat16 *dst = p.h + hoff;
+                // h = silu(gate) * up, and gate and up saved for the backward, as
+                // bf16 rows of 128 columns; each 64-column block of each output
+                // leaves through the lane transpose (whole 128-byte row segments
+                // per store instruction), gate and up re-read from tensor memory
+                const int rows_w = e.x1 - grp * 32 <= 0 ? 0 : (e.x1 - grp * 32 >= 32 ? 32 : e.x1 - grp * 32);
+                const int64_t off = static_cast<int64_t>(e.x0 + (rows_w > 0 ? grp * 32 : 0)) * g.I + e.c * 128;
 #pragma unroll 1
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t gr[32], ur[32];
-                    tmem_ld_32x32b_x32(taddr + ch * 32, gr);
-                    tmem_ld_32x32b_x32(taddr + 128 + ch * 32, ur);
-                    tmem_ld_wait();
-                    if (valid) {
+                for (int b = 0; b < 2; ++b) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            float hv[8];
+                    for (int gu = 0; gu < 2; ++gu) {  // gate, then up
+                        uint32_t vk[32];
+                        uint32_t r0[32], r1[32];
+                        tmem_ld_32x32b_x32(taddr + gu * 128 + b * 64, r0);
+                        tmem_ld_32x32b_x32(taddr + gu * 128 + b * 64 + 32, r1);
+                        tmem_ld_wait();
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                hv[j] = silu_f(__uint_as_float(gr[q4 * 8 + j])) * __uint_as_float(ur[q4 * 8 + j]);
-                            uint4 o;
-                            o.x = pack_bf16x2(hv[0], hv[1]);
-                            o.y = pack_bf16x2(hv[2], hv[3]);
-                            o.z = pack_bf16x2(hv[4], hv[5]);
-                            o.w = pack_bf16x2(hv[6], hv[7]);
-                            *reinterpret_cast<uint4 *>(dst + ch * 32 + q4 * 8) = o;
-                            const uint32_t *gq = gr + q4 * 8, *uq = ur + q4 * 8;
-                            const uint4 go = make_uint4(
-                                pack_bf16x2(__uint_as_float(gq[0]), __uint_as_float(gq[1])),
-                                pack_bf16x2(__uint_as_float(gq[2]), __uint_as_float(gq[3])),
-                                pack_bf16x2(__uint_as_float(gq[4]), __uint_as_float(gq[5])),
-                                pack_bf16x2(__uint_as_float(gq[6]), __uint_as_float(gq[7])));
-                            const uint4 uo = make_uint4(
-                                pack_bf16x2(__uint_as_float(uq[0]), __uint_as_float(uq[1])),
-                                pack_bf16x2(__uint_as_float(uq[2]), __uint_as_float(uq[3])),
-                                pack_bf16x2(__uint_as_float(uq[4]), __uint_as_float(uq[5])),
-                                pack_bf16x2(__uint_as_float(uq[6]), __uint_as_float(uq[7])));
-                            *reinterpret_cast<uint4 *>(p.gsave + hoff + ch * 32 + q4 * 8) = go;
-                            *reinterpret_cast<uint4 *>(p.usave + hoff + ch * 32 + q4 * 8) = uo;
+                        for (int j = 0; j < 16; ++j) {
+                            vk[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+                            vk[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
                         }
+                        lane_transpose8_16B(vk, lane);
+                        store_row_lines(vk, (gu == 0 ? p.gsave : p.usave) + off + b * 64, g.I, rows_w, 64, lane);
                     }
+                    uint32_t hk[32];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t gr[32], ur[32];
+                        tmem_ld_32x32b_x32(taddr + b * 64 + hh * 32, gr);
+                        tmem_ld_32x32b_x32(taddr + 128 + b * 64 + hh * 32, ur);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            hk[hh * 16 + j] =
+                                pack_bf16x2(silu_f(__uint_as_float(gr[2 * j])) * __uint_as_float(ur[2 * j]),
+                                            silu_f(__uint_as_float(gr[2 * j + 1])) * __uint_as_float(ur[2 * j + 1]));
+                    }
+                    lane_transpose8_16B(hk, lane);
+                    store_row_lines(hk, p.h + off + b * 64, g.I, rows_w, 64, lane);
                 }
             } else if (!g.mx && grp * 32 + 32 > e.x1) {  // K_TILE_D, bf16, a warp with rows past the
                 // unit's end: plain stores of its real rows (in the bf16 layout the
