@@ -491,24 +491,28 @@ __device__ __noinline__ MoeProdState moe_dispatch(const MoeParams &p, const Smem
         qok = __shfl_sync(0xFFFFFFFFu, qok ? 1 : 0, 0) != 0;
         __syncwarp();
         if (qok) {
+            // the block's scale words into the receive rows' tiled atoms: word c
+            // of a row (K-blocks 4c .. 4c+3) goes to atom (pos / 128, c) at the
+            // row's place inside it; 32 rows in flight per lane, one row's words
+            // across the lanes (coalesced loads)
             const int W = static_cast<int>(g.H / 128);  // scale words per row
-            const int nw = nrows * W;
-            const uint32_t *xs = reinterpret_cast<const uint32_t *>(p.xs);
-            constexpr int U = 16;
-            for (int i0 = 0; i0 < nw; i0 += 32 * U) {
-                uint32_t v[U];
+            const uint32_t *xs = reinterpret_cast<const uint32_t *>(p.xs) + tok0 * W;
+            constexpr int R = 32;
+            for (int r0 = 0; r0 < nrows; r0 += R) {
+                for (int c0 = 0; c0 < W; c0 += 32) {
+                    const int c = c0 + lane;
+                    uint32_t v[R];
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int i = i0 + u * 32 + lane;
-                    if (i < nw) v[u] = __ldcg(xs + (tok0 + i / W) * W + i % W);
-                }
+                    for (int u = 0; u < R; ++u)
+                        if (r0 + u < nrows && c < W) v[u] = __ldcg(xs + (r0 + u) * W + c);
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int i = i0 + u * 32 + lane;
-                    if (i < nw) {
-                        const int64_t pos = s_pos[i / W];
-                        *reinterpret_cast<uint32_t *>(p.recv_sf + sf_tiled_offset(pos, 4 * (i % W), 4 * W)) = v[u];
-                    }
+                    for (int u = 0; u < R; ++u)
+                        if (r0 + u < nrows && c < W) {
+                            const int pos = s_pos[r0 + u];
+                            const int64_t off = (static_cast<int64_t>(pos >> 7) * W + c) * 512 + (pos & 31) * 16 +
+                                                ((pos >> 5) & 3) * 4;
+                            *reinterpret_cast<uint32_t *>(p.recv_sf + off) = v[u];
+                        }
                 }
             }
             __threadfence();
