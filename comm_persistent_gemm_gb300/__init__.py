@@ -36,7 +36,8 @@ EXPORTS = ["kosmos_default_opts", "kosmos_num_sms", "kosmos_workspace_bytes", "k
            "kosmos_ag_gemm", "kosmos_gemm_rs", "kosmos_moe_fwd", "kosmos_mxfp8_quantize", "kosmos_status_sync",
            "kosmos_trace_info", "kosmos_rail_decode", "kosmos_rail_decode_device", "kosmos_ag_gemm_noalloc",
            "kosmos_moe_workspace_bytes", "kosmos_moe_debug_view", "kosmos_ag_tile_plan", "kosmos_moe_bwd",
-           "kosmos_moe_bwd_workspace_bytes", "kosmos_moe_bwd_debug_view", "kosmos_ag_gemm_host"]
+           "kosmos_moe_bwd_workspace_bytes", "kosmos_moe_bwd_debug_view", "kosmos_ag_gemm_host",
+           "kosmos_noalloc_status_sync"]
 
 
 class KosmosError(RuntimeError):
@@ -105,6 +106,8 @@ def lib():
     L.kosmos_rail_decode_device.restype = i64
     L.kosmos_ag_gemm_noalloc.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, i32, vp, vp, C.POINTER(Opts), vp]
     L.kosmos_ag_gemm_noalloc.restype = i32
+    L.kosmos_noalloc_status_sync.argtypes = [vp, C.POINTER(i64)]
+    L.kosmos_noalloc_status_sync.restype = i32
     L.kosmos_moe_workspace_bytes.argtypes = [i32, i64, i64, i32, i32, i64, i32, C.POINTER(Opts)]
     L.kosmos_moe_workspace_bytes.restype = C.c_size_t
     L.kosmos_moe_debug_view.argtypes = [i32, i32, i64, i64, i32, i32, i64, i32, vp, C.POINTER(vp), C.POINTER(i64)]
@@ -366,6 +369,14 @@ def status_sync(ws, stream=None):
     """(status, failing_entry) of the last call that used ws (synchronises)."""
     e = C.c_int64(-1)
     rc = lib().kosmos_status_sync(ws.data_ptr(), _stream(stream), C.byref(e))
+    return int(rc), int(e.value)
+
+
+def noalloc_status_sync(stream=None):
+    """(status, failing_entry) of the last ag_gemm_noalloc call on the current
+    device (synchronises); valid until the next such call."""
+    e = C.c_int64(-1)
+    rc = lib().kosmos_noalloc_status_sync(_stream(stream), C.byref(e))
     return int(rc), int(e.value)
 
 

@@ -64,3 +64,10 @@ extern "C" KOSMOS_API kosmos_status kosmos_ag_gemm_noalloc(const void *const *x_
     return kosmos_ag_gemm(x_shards, x_scales, P, m_per_shard, k, n, w, w_scales, dtype, x_gathered, y, ws,
                           static_cast<size_t>(KOSMOS_STATIC_WS_BYTES), &o, stream);
 }
+
+extern "C" KOSMOS_API kosmos_status kosmos_noalloc_status_sync(void *stream, int64_t *failing_entry) {
+    void *ws = nullptr;
+    const kosmos_status s = static_ws_address(&ws);
+    if (s != KOSMOS_OK) return s;
+    return kosmos_status_sync(ws, stream, failing_entry);
+}

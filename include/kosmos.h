@@ -395,10 +395,10 @@ KOSMOS_API kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int6
  * Every call shares the one array per device: each call first clears the part
  * it uses on `stream`, so calls that overlap on the GPU (different streams,
  * or different host threads without ordering) race and give wrong results.
- * Device-side wait failures are not reported back (the array is cleared by
- * the next call); use kosmos_ag_gemm with a workspace when the device status
- * is needed.  Allocates no memory: no cudaMalloc, cudaFree or allocating
- * library routine.
+ * Device-side wait failures are written to the array's status word like a
+ * workspace's: read them with kosmos_noalloc_status_sync() before the next
+ * call on the device clears the array.  Allocates no memory: no cudaMalloc,
+ * cudaFree or allocating library routine.
  */
 KOSMOS_API kosmos_status kosmos_ag_gemm_noalloc(const void *const *x_shards, const void *const *x_scales, int P,
                                                 int64_t m_per_shard, int64_t k, int64_t n,
@@ -411,6 +411,15 @@ KOSMOS_API kosmos_status kosmos_ag_gemm_noalloc(const void *const *x_shards, con
  * if failing_entry is not NULL, the ticket of the entry that failed (-1 if
  * none). */
 KOSMOS_API kosmos_status kosmos_status_sync(void *ws, void *stream, int64_t *failing_entry);
+
+/* kosmos_status_sync for kosmos_ag_gemm_noalloc: synchronises `stream`, then
+ * returns the device status of the last no-allocation call on the current
+ * device (KOSMOS_OK, KOSMOS_ERR_TIMEOUT or KOSMOS_ERR_DEVICE) and, if
+ * failing_entry is not NULL, the ticket of the entry that failed (-1 if none).
+ * Valid until the next kosmos_ag_gemm_noalloc call on the device, which
+ * clears the status; KOSMOS_ERR_CUDA if the library's array cannot be found
+ * in the current context.  Allocates no memory. */
+KOSMOS_API kosmos_status kosmos_noalloc_status_sync(void *stream, int64_t *failing_entry);
 
 /* Role trace.  When opts.trace is set, every claimed entry appends one record
  * to its CTA's ring in the workspace:

@@ -6,8 +6,11 @@ Called through the C ABI (ctypes) twice in a row, on two different problems.
 Both entry points run the same kernel with the same plan, so each result must
 equal kosmos_ag_gemm's (with a caller workspace, same inputs) bit for bit;
 the small problem is also checked against the oracle's fp64 all-gather +
-GEMM within max|y - ref| <= 1e-2 * max|ref|.  Collected last so that a
-failure here comes after every other test.
+GEMM within max|y - ref| <= 1e-2 * max|ref|.  A transfer whose flag is
+never released (host-set injection, a bounded wait of 2 ms) must come back
+as TIMEOUT through kosmos_noalloc_status_sync, and the next call must be
+correct again.  Collected last so that a failure here comes after every
+other test.
 """
 import ctypes as C
 
@@ -15,6 +18,8 @@ import pytest
 import torch
 
 from _helpers import bf16_tensor_to_f64, kosmos, rel_err
+import numpy as np
+
 from kosmos_inputs import ag_inputs, bf16_bits
 
 pytestmark = pytest.mark.gpu
@@ -71,3 +76,36 @@ def test_noalloc_rejects_oversized_and_trace():
     rc = lib.kosmos_ag_gemm_noalloc(xs, None, 2, 64, 64, 64, dummy.data_ptr(), None, K.BF16,
                                     dummy.data_ptr(), dummy.data_ptr(), C.byref(o), None)
     assert rc == K.ERR_UNSUPPORTED
+
+
+def test_noalloc_reports_device_status(orc):
+    """The static scratch's status word through kosmos_noalloc_status_sync: OK
+    after a clean call; TIMEOUT with the waiting tile's ticket after a call
+    whose first transfer never releases its flag; OK and bit-equal results
+    on the next clean call (each call clears the part of the array it uses)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    K = kosmos()
+    P, m, k, n = 2, 128, 128, 256
+    inp = ag_inputs(P, m, k, n, seed=9, var_w=1.0 / k)
+    xs = [x.cuda() for x in inp["x"]]
+    w = inp["w"].cuda()
+    xg = torch.empty(P * m, k, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(P * m, n, dtype=torch.bfloat16, device="cuda")
+    K.ag_gemm_noalloc(xs, w, xg, y)
+    assert K.noalloc_status_sync() == (K.OK, -1)
+    y_ok = y.clone()
+    o = K.opts(inject=K.INJECT_DROP_TRANSFER | (0 << 32), wait_limit_ns=2_000_000)
+    K.ag_gemm_noalloc(xs, w, xg, y, o)
+    st, entry = K.noalloc_status_sync()
+    assert st == K.ERR_TIMEOUT, (st, entry)
+    # transfer 0 is part 0 of shard 1's piece 0; the first tile of shard 1 waits for it
+    split, tm = K.ag_tile_plan(P, m, k, n, o)
+    _, tl = orc.rail_ag(P, m, n, TR=tm, XS=split)
+    assert entry == int(np.flatnonzero(tl[:, 1] == 1)[0]), entry
+    y.fill_(float("nan"))
+    K.ag_gemm_noalloc(xs, w, xg, y)
+    assert K.noalloc_status_sync() == (K.OK, -1)
+    assert torch.equal(y, y_ok)
+    ref = orc.ag_gemm([bf16_bits(x) for x in inp["x"]], bf16_bits(inp["w"]))
+    assert rel_err(bf16_tensor_to_f64(y), ref) <= TOL
