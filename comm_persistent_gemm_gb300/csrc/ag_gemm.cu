@@ -40,25 +40,37 @@ struct AgParams {
     uint64_t wait_limit_ns;
     uint64_t inject;
     int64_t link_gbs;  // emulated link for the remote pieces; 0 = uncapped
-    // host-input flow (null otherwise): ext_ready[s] becomes 1 once shard s has
-    // been copied to its device buffer (by a copy stream); ydone[s] counts the
-    // output tiles of shard s written (per CTA of a tile engine)
+    // host-input flow (null otherwise): ext_ready[s * AG_EXT_STRIDE + c] becomes
+    // 1 once chunk c of shard s (ag_host_cpp pieces) has been copied to its
+    // device buffer (by a copy stream); ydone[s * AG_EXT_STRIDE + j] counts the
+    // output tiles of tile-row group j of shard s written (per CTA of a tile
+    // engine)
     const uint32_t *ext_ready;
     uint32_t *ydone;
 };
 
-// Host-input flow: waits until shard s is on the device.
-__device__ __forceinline__ bool ag_ext_wait(const AgParams &p, int s, int64_t entry) {
-    return p.ext_ready == nullptr ||
-           wait_flag_eq(p.ws, const_cast<uint32_t *>(&p.ext_ready[s]), 1u, p.wait_limit_ns, entry);
+// Host-input flow: waits until the chunk holding piece `piece` of shard s is
+// on the device.
+__device__ __forceinline__ bool ag_ext_wait(const AgParams &p, int s, int piece, int64_t entry) {
+    if (p.ext_ready == nullptr) return true;
+    const int c = piece / ag_host_cpp(p.g);
+    return wait_flag_eq(p.ws, const_cast<uint32_t *>(&p.ext_ready[s * AG_EXT_STRIDE + c]), 1u, p.wait_limit_ns,
+                        entry);
 }
 
-// Host-input flow: one output tile of shard s written by this CTA's epilogue warps.
-__device__ __forceinline__ void ag_ydone(const AgParams &p, int s, int grp, int lane) {
+// Host-input flow: one output tile of tile row `trow` of shard s written by
+// this CTA's epilogue warps.
+__device__ __forceinline__ void ag_ydone(const AgParams &p, int s, int trow, int grp, int lane) {
     if (p.ydone == nullptr) return;
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
-    if (grp == 0 && lane == 0) red_release_add_gpu(&p.ydone[s], 1u);
+    if (grp == 0 && lane == 0) red_release_add_gpu(&p.ydone[s * AG_EXT_STRIDE + trow / ag_host_tpg(p.g)], 1u);
+}
+
+// Host-input flow: a failed launch releases every output wait of the host.
+__device__ __forceinline__ void ag_ydone_release(const AgParams &p) {
+    if (p.ydone == nullptr || !failed(p.ws)) return;
+    for (int i = 0; i < p.g.P * AG_EXT_STRIDE; ++i) st_release_gpu(&p.ydone[i], AG_YDONE_RELEASE);
 }
 
 // Tile-rail entry -> what the engine runs: output columns [col0, col0 + BN)
@@ -94,7 +106,7 @@ __device__ __forceinline__ bool ag_claim_transfer(const AgParams &p, MoveEntry &
     if (t >= static_cast<uint32_t>(p.g.n_transfer)) return false;
     int shard, piece, part;
     ag_decode_transfer(p.g, static_cast<int>(t), shard, piece, part);
-    if (!ag_ext_wait(p, shard, t)) return false;
+    if (!ag_ext_wait(p, shard, piece, t)) return false;
     int64_t row0, rows;
     ag_part_rows(p.g, piece, part, row0, rows);
     const int64_t row_bytes = p.g.k * 2;
@@ -198,7 +210,6 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
     PipeState ps;
     RingState rs;
     int nrec = 0;
-    bool local_in = false;  // host-input flow: shard 0 seen on the device
     while (true) {
         if (failed(p.ws)) break;
         if (mover) {
@@ -219,10 +230,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
             if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], ag_piece_ready(p.g, epoch), p.wait_limit_ns, t))
                 break;
         }
-        if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0 && !local_in) {
-            if (!ag_ext_wait(p, 0, t)) break;
-            local_in = true;
-        }
+        if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0 && !ag_ext_wait(p, 0, i, t)) break;  // host-input flow
         int slot = -1;
         if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
             r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
@@ -314,7 +322,7 @@ __device__ __forceinline__ void ag_epilogue(const AgParams &p, const Smem &sm, u
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tempty[acc]);
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-        ag_ydone(p, s, grp, lane);
+        ag_ydone(p, s, i, grp, lane);
         if (e.slot >= 0 && lane == 0 && grp == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
         }
@@ -342,8 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_kernel(const __grid_co
         ag_epilogue(p, sm, tmem_base, warp, lane, epoch);
     }
     engine_teardown(sm, warp, tmem_base);
-    if (threadIdx.x == 0 && p.ydone != nullptr && failed(p.ws))  // release the host's output waits
-        for (int s = 0; s < p.g.P; ++s) st_release_gpu(&p.ydone[s], AG_YDONE_RELEASE);
+    if (threadIdx.x == 0) ag_ydone_release(p);
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
 }
 
@@ -402,8 +409,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
     }
     if (leader) {
         const uint32_t my_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
-        bool local_in = false;  // host-input flow: shard 0 seen on the device
-        while (true) {
+            while (true) {
             if (failed(p.ws)) break;
             const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
             if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
@@ -412,9 +418,9 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
             const int pc = 2 * i2;  // the leader's 128-row piece
             const bool remote = p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces;
-            if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0 && !local_in) {
-                if (!ag_ext_wait(p, 0, t)) break;
-                local_in = true;
+            if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0) {  // host-input flow: both 128-row pieces
+                if (!ag_ext_wait(p, 0, pc, t)) break;
+                if (pc + 1 < p.g.pieces && !ag_ext_wait(p, 0, pc + 1, t)) break;
             }
             // the entry is published before the readiness wait, so that the
             // peer can take transfer parts for its own piece meanwhile
@@ -535,7 +541,7 @@ __device__ __forceinline__ void ag2_epilogue(const AgParams &p, const Smem2 &sm,
         }
         acc_release(sm, acc, leader, lane);
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-        ag_ydone(p, s, grp, lane);
+        ag_ydone(p, s, i2, grp, lane);
         if (leader && e.slot >= 0 && lane == 0 && grp == 0) {
             if (TraceRec *r = trace_rec(p.trace, blockIdx.x, e.slot)) r->t_done = static_cast<int64_t>(globaltimer());
         }
@@ -564,8 +570,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_pair_kernel(const __gr
         ag2_epilogue(p, sm, tmem_base, warp, lane, rank, epoch);
     }
     engine2_teardown(sm, warp, tmem_base);
-    if (threadIdx.x == 0 && p.ydone != nullptr && failed(p.ws))  // release the host's output waits
-        for (int s = 0; s < p.g.P; ++s) st_release_gpu(&p.ydone[s], AG_YDONE_RELEASE);
+    if (threadIdx.x == 0) ag_ydone_release(p);
     if (threadIdx.x == 0) engine_finish(p.ws, epoch, 3);
 }
 
@@ -574,7 +579,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_pair_kernel(const __gr
 __global__ void __launch_bounds__(256) ag_gather_copy_kernel(const AgParams p) {
     if (p.ext_ready != nullptr) {  // host-input flow: every shard must be on the device
         if (threadIdx.x == 0)
-            for (int s = 0; s < p.g.P; ++s) ag_ext_wait(p, s, -40);
+            for (int s = 0; s < p.g.P; ++s)
+                for (int pc = 0; pc < p.g.pieces; pc += ag_host_cpp(p.g)) ag_ext_wait(p, s, pc, -40);
         __syncthreads();
         if (failed(p.ws)) return;
     }
@@ -635,7 +641,7 @@ kosmos_status launch_ag_bf16(const AgLaunch &L, cudaStream_t stream) {
     p.trace = L.trace ? reinterpret_cast<TraceRec *>(ws + W.trace_off) : nullptr;
     if (L.host_flow) {
         p.ext_ready = reinterpret_cast<const uint32_t *>(ws + W.ext_off);
-        p.ydone = reinterpret_cast<uint32_t *>(ws + W.ext_off) + KOSMOS_MAX_P;
+        p.ydone = reinterpret_cast<uint32_t *>(ws + W.ext_off) + AG_EXT_WORDS;
     }
     p.nkb = static_cast<int>(L.k / BK);
     p.sched = L.sched;

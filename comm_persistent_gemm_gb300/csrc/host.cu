@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 
@@ -407,10 +408,15 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
     const AgWsLayout W = ag_ws_layout(ag_geom(P, m_per_shard, k, n), o.trace != 0, 0);
     uint8_t *ext = static_cast<uint8_t *>(ws) + W.ext_off;
     const CUdeviceptr ready = reinterpret_cast<CUdeviceptr>(ext);
-    const CUdeviceptr done = ready + 4 * KOSMOS_MAX_P;
-    // output tiles of one shard, counted per CTA of a tile engine
-    const uint32_t target = static_cast<uint32_t>(cdiv(m_per_shard, pl.pair ? PBM : BM) * cdiv(n, BN) *
-                                                  (pl.pair ? 2 : 1));
+    const CUdeviceptr done = ready + 4 * AG_EXT_WORDS;
+    // A shard arrives in chunks of whole 128-row pieces and its output rows go
+    // back in groups of whole tile rows (at most AG_HOST_CHUNKS and AG_HOST_GROUPS), so
+    // that the kernel starts on a shard's first rows before the rest are in
+    // and the host receives the first output rows of the last shard while its
+    // other tile rows are still being built.  The same geometry as the kernel's.
+    const AgGeom tg = ag_geom(P, m_per_shard, k, n, pl.pair ? PBM : BM);
+    const int cpp = ag_host_cpp(tg), tpg = ag_host_tpg(tg);
+    const int nch = static_cast<int>(cdiv(tg.pieces, cpp)), ngr = static_cast<int>(cdiv(tg.tiles_m, tpg));
     cudaStream_t s = static_cast<cudaStream_t>(stream), h = static_cast<cudaStream_t>(h2d_stream),
                  d = static_cast<cudaStream_t>(d2h_stream);
     CUstream cs = reinterpret_cast<CUstream>(s), ch = reinterpret_cast<CUstream>(h), cd = reinterpret_cast<CUstream>(d);
@@ -419,29 +425,49 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
     // its earlier work (the previous kernel reading x_dev) is done and the
     // arrival and output words are zeroed; the copy streams wait for it; at
     // the end each copy stream publishes the token and `stream` waits for both.
-    const CUdeviceptr sync = done + 4 * KOSMOS_MAX_P;  // [0] stream ready, [1] h2d done, [2] d2h done
+    const CUdeviceptr sync = done + 4 * AG_EXT_WORDS;  // [0] stream ready, [1] h2d done, [2] d2h done
     uint32_t tok = g_host_flow_token.fetch_add(1u, std::memory_order_relaxed) + 1u;
     if (tok == 0u) tok = g_host_flow_token.fetch_add(1u, std::memory_order_relaxed) + 1u;
-    bool ok = cudaMemsetAsync(ext, 0, 8 * KOSMOS_MAX_P, s) == cudaSuccess &&
+    bool ok = cudaMemsetAsync(ext, 0, 2 * 4 * AG_EXT_WORDS, s) == cudaSuccess &&
               wr(cs, sync, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
               wt(ch, sync, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS &&
               wt(cd, sync, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS;
-    // shard r to the device, then its arrival word (the local shard first)
-    const size_t xb = static_cast<size_t>(m_per_shard * k * 2), yb = static_cast<size_t>(m_per_shard * n * 2);
-    for (int r = 0; ok && r < P; ++r)
-        ok = cudaMemcpyAsync(x_dev[r], x_host[r], xb, cudaMemcpyHostToDevice, h) == cudaSuccess &&
-             wr(reinterpret_cast<CUstream>(h), ready + 4 * r, 1u, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+    // The kernel is enqueued first: its movers and local-shard builders wait
+    // for the arrival words, so it starts on the first chunks while the host
+    // is still enqueueing the later ones.  If an enqueue below fails, the
+    // kernel's bounded waits end it with a status and it releases the
+    // output waits.
     kosmos_status st = ok ? launch_ag_bf16(L, s) : KOSMOS_ERR_CUDA;
     if (st != KOSMOS_OK) {
         // no kernel: release the output waits below so that no stream blocks
-        for (int r = 0; r < P; ++r)
-            wr(reinterpret_cast<CUstream>(h), done + 4 * r, AG_YDONE_RELEASE, CU_STREAM_WRITE_VALUE_DEFAULT);
+        for (int i = 0; i < P * AG_EXT_STRIDE; ++i)
+            wr(ch, done + 4 * i, AG_YDONE_RELEASE, CU_STREAM_WRITE_VALUE_DEFAULT);
     }
-    // shard r's output rows back to the host once all its tiles are written
+    // shard r to the device chunk by chunk, each followed by its arrival word (the local shard first)
+    const int64_t xrow = k * 2, yrow = n * 2;
     for (int r = 0; ok && r < P; ++r)
-        ok = wt(reinterpret_cast<CUstream>(d), done + 4 * r, target, CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS &&
-             cudaMemcpyAsync(static_cast<uint8_t *>(y_host) + r * yb, static_cast<uint8_t *>(y_dev) + r * yb, yb,
-                             cudaMemcpyDeviceToHost, d) == cudaSuccess;
+        for (int c = 0; ok && c < nch; ++c) {
+            const int64_t r0 = static_cast<int64_t>(c) * cpp * PIECE_ROWS;
+            const int64_t r1 = std::min<int64_t>(m_per_shard, r0 + static_cast<int64_t>(cpp) * PIECE_ROWS);
+            ok = cudaMemcpyAsync(static_cast<uint8_t *>(x_dev[r]) + r0 * xrow,
+                                 static_cast<const uint8_t *>(x_host[r]) + r0 * xrow, static_cast<size_t>((r1 - r0) * xrow),
+                                 cudaMemcpyHostToDevice, h) == cudaSuccess &&
+                 wr(ch, ready + 4 * (r * AG_EXT_STRIDE + c), 1u, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+        }
+    // each group of shard r's output rows back to the host once all its tiles
+    // are written (output tiles counted per CTA of a tile engine)
+    const int64_t tr = pl.pair ? PBM : BM;
+    const uint32_t per_row = static_cast<uint32_t>(cdiv(n, BN) * (pl.pair ? 2 : 1));
+    for (int r = 0; ok && r < P; ++r)
+        for (int j = 0; ok && j < ngr; ++j) {
+            const int t0 = j * tpg, t1 = std::min(tg.tiles_m, t0 + tpg);
+            const int64_t r0 = t0 * tr, r1 = std::min<int64_t>(m_per_shard, t1 * tr);
+            const size_t off = static_cast<size_t>((static_cast<int64_t>(r) * m_per_shard + r0) * yrow);
+            ok = wt(cd, done + 4 * (r * AG_EXT_STRIDE + j), static_cast<uint32_t>(t1 - t0) * per_row,
+                    CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS &&
+                 cudaMemcpyAsync(static_cast<uint8_t *>(y_host) + off, static_cast<uint8_t *>(y_dev) + off,
+                                 static_cast<size_t>((r1 - r0) * yrow), cudaMemcpyDeviceToHost, d) == cudaSuccess;
+        }
     ok = ok && wr(ch, sync + 4, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
          wr(cd, sync + 8, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
          wt(cs, sync + 4, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS &&

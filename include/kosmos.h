@@ -187,10 +187,11 @@ KOSMOS_API int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t k, int64_
  * All-gather + GEMM with the shards in host memory (BF16): the copies to the
  * device run on h2d_stream, shard by shard (the local shard first), each
  * followed by an arrival word the kernel's movers (and, for the local shard,
- * builders) wait on, so the copies overlap the multiplication; the output
- * rows of each shard are copied back on d2h_stream as soon as all its tiles
- * are written (a stream wait on a per-shard tile count).  Same result as
- * kosmos_ag_gemm on x_dev.
+ * builders) wait on, so the copies overlap the multiplication; each shard's
+ * output rows go back on d2h_stream in two groups of tile rows, each as soon
+ * as its tiles are written (a stream wait on the group's tile count).  The
+ * kernel is enqueued before the copies.  Same result as kosmos_ag_gemm on
+ * x_dev.
  *   x_host[r]     : X_r [m_per_shard, k] bf16 in pinned host memory.
  *   x_dev[r]      : device buffers [m_per_shard, k] the shards are copied to.
  *   y_dev, y_host : [P * m_per_shard, n] bf16, device and pinned host.
@@ -387,7 +388,7 @@ KOSMOS_API kosmos_status kosmos_mxfp8_quantize(const void *x, int64_t rows, int6
  * process exits.  Calls whose workspace would exceed it (see
  * kosmos_workspace_bytes) return KOSMOS_ERR_WORKSPACE; opts.trace is not
  * supported (KOSMOS_ERR_UNSUPPORTED).  The 8-rank 1024 x 8192 x 3584 call
- * needs 512 bytes.
+ * needs 1536 bytes.
  * Set-up: every call looks up the array's device address in the current
  * device's context (cudaGetSymbolAddress; nothing is cached, so a reset device
  * or a new context is picked up).  The first lookup in a context loads the

@@ -1,6 +1,7 @@
 """The all-gather + GEMM from pinned host shards (kosmos_ag_gemm_host): the
 shard copies and output copies run on two copy streams and overlap the
-kernel through per-shard arrival words and output-tile counts.  Results must
+kernel through per-shard arrival words and output-tile counts per group of
+tile rows.  Results must
 equal kosmos_ag_gemm on the same shards bit for bit (every schedule, both
 tile engines, full size); a failed kernel releases the output waits so that
 no stream blocks, and the status reports the failure."""
