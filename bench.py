@@ -183,6 +183,18 @@ def time_kernel_steps(fn, steps, warmup, flush, stream):
     return times
 
 
+def paired_medians(fn_a, fn_b, flush, stream, rounds=5, steps=10):
+    """Median per-round mean step time (ms) of two configurations timed in
+    alternation (a, b, a, b, ...).  A sweep's best point is the maximum of
+    noisy samples, biased upward against a configuration timed once; the
+    paired comparison of the sweep's choice removes that bias."""
+    ta, tb = [], []
+    for _ in range(rounds):
+        ta.append(statistics.mean(time_kernel_steps(fn_a, steps, 2, flush, stream)))
+        tb.append(statistics.mean(time_kernel_steps(fn_b, steps, 2, flush, stream)))
+    return statistics.median(ta), statistics.median(tb)
+
+
 def _split_experts(w, P):
     E = w.shape[0]
     return [w[q * (E // P):(q + 1) * (E // P)].contiguous() for q in range(P)]
@@ -575,10 +587,13 @@ def bench_attn(K, dev, steps, warmup, flush, stream, peak):
     xg = torch.empty(P * m, k, dtype=torch.bfloat16, device=dev)
     y = torch.empty(P * m, n, dtype=torch.bfloat16, device=dev)
 
-    def t_ag(**kw):
+    def mk_ag(**kw):
         o = K.opts(**kw)
         wsb = K.workspace(K.OP_AG_GEMM, P, m, n, k, o=o, device=dev)
-        f = lambda: K.ag_gemm(xs, W, xg, y, wsb, o, stream=stream)
+        return (lambda: K.ag_gemm(xs, W, xg, y, wsb, o, stream=stream)), wsb
+
+    def t_ag(**kw):
+        f, wsb = mk_ag(**kw)
         f()
         K.check(wsb, "ag_gemm")
         t = statistics.mean(time_kernel_steps(f, steps, warmup, flush, stream))
@@ -591,6 +606,13 @@ def bench_attn(K, dev, steps, warmup, flush, stream, peak):
         fixed = {str(c): t_ag(sched=K.SCHED_FIXED, fixed_comm_ctas=c, link_gbs=cap) for c in (20, 40, 60)}
         res[tag] = {"self": t_ag(link_gbs=cap), "fixed_best": max(fixed.values()), "fixed_sweep": fixed,
                     "unfused": t_ag(sched=K.SCHED_UNFUSED, link_gbs=cap)}
+        crew = int(max(fixed, key=fixed.get))
+        (fa, wa), (fb, wb) = mk_ag(link_gbs=cap), mk_ag(sched=K.SCHED_FIXED, fixed_comm_ctas=crew, link_gbs=cap)
+        ma, mb = paired_medians(fa, fb, flush, stream)
+        K.check(wa, "ag_gemm paired")
+        K.check(wb, "ag_gemm fixed paired")
+        res[tag]["paired_self_fixed"] = {"crew": crew, "self": w.flops() / (ma * 1e-3) / 1e12,
+                                         "fixed": w.flops() / (mb * 1e-3) / 1e12, "ratio": mb / ma}
     out["ag_qkv_p8"] = {"tflops": res, "frac_of_peak_free": res["free"]["self"] / peak,
                         "link_bound_us": (P - 1) * m * k * 2 / LINK_GBS / 1e3,
                         "gemm_at_peak_us": w.flops() / (peak * 1e12) * 1e6}
@@ -693,7 +715,9 @@ def compact_baselines(base):
             "one_sm_tiles": sig(base["self_single_sm_tiles"]["tflops"]),
             "n_comm0_sweep": {c: sig(v) for c, v in base["self_n_comm0_sweep"].items()},
             "link_self_fixedbest_unfused": [sig(base["link"]["self"]), sig(base["link"]["fixed_best"]),
-                                            sig(base["link"]["unfused"])]}
+                                            sig(base["link"]["unfused"])],
+            "paired_self_over_fixed": {"free": sig(base["paired_self_fixed"]["ratio"], 3),
+                                       "link": sig(base["link"]["paired_self_fixed"]["ratio"], 3)}}
 
 
 def compact_also(also):
@@ -742,6 +766,8 @@ def compact_also(also):
                 t = r[wl]["tflops"][tag]
                 a[f"{wl}_{tag}"] = [sig(t[k]), sig(t["fixed_best"]), sig(t["unfused"])]
         out["attention_self_fixedbest_unfused"] = a
+        out["qkv_paired_self_over_fixed"] = {tag: sig(r["ag_qkv_p8"]["tflops"][tag]["paired_self_fixed"]["ratio"], 3)
+                                             for tag in ("free", "link")}
     return out
 
 
@@ -848,6 +874,12 @@ def run_kosmos(args):
         fixed[str(crew)] = flops / (statistics.mean(tt) * 1e-3) / 1e12
     best_crew = max(fixed, key=fixed.get)
     base["fixed_split_best"] = {"tflops": fixed[best_crew], "crew": int(best_crew), "sweep": fixed}
+    f_fix, ws_fix = make(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=int(best_crew)))
+    ma, mb = paired_medians(f_self, f_fix, flush, stream)
+    K.check(ws_self, "ag_gemm paired")
+    K.check(ws_fix, "ag_gemm fixed paired")
+    base["paired_self_fixed"] = {"crew": int(best_crew), "self": flops / (ma * 1e-3) / 1e12,
+                                 "fixed": flops / (mb * 1e-3) / 1e12, "ratio": mb / ma}
     f, wsb = make(K.opts(sched=K.SCHED_UNFUSED))
     tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
     K.check(wsb, "ag_gemm unfused")
@@ -880,6 +912,14 @@ def run_kosmos(args):
         lfixed[str(crew)] = flops / (statistics.mean(tt) * 1e-3) / 1e12
     link["fixed_sweep"] = lfixed
     link["fixed_best"] = max(lfixed.values())
+    lcrew = int(max(lfixed, key=lfixed.get))
+    f_ls, ws_ls = make(K.opts(link_gbs=LINK_GBS))
+    f_lf, ws_lf = make(K.opts(sched=K.SCHED_FIXED, fixed_comm_ctas=lcrew, link_gbs=LINK_GBS))
+    ma, mb = paired_medians(f_ls, f_lf, flush, stream)
+    K.check(ws_ls, "ag_gemm link paired")
+    K.check(ws_lf, "ag_gemm link fixed paired")
+    link["paired_self_fixed"] = {"crew": lcrew, "self": flops / (ma * 1e-3) / 1e12,
+                                 "fixed": flops / (mb * 1e-3) / 1e12, "ratio": mb / ma}
     f, wsb = make(K.opts(sched=K.SCHED_UNFUSED, link_gbs=LINK_GBS))
     tt = time_kernel_steps(f, max(3, args.steps // 2), 2, flush, stream)
     K.check(wsb, "ag_gemm link unfused")
