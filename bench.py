@@ -71,9 +71,17 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            # the timed region starts once nvidia-smi has initialised and
+            # written its first sample (its start-up would otherwise overlap
+            # the first timed steps), between two of its 200 ms queries
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and self.proc.poll() is None:
+                if os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.01)
+            time.sleep(0.05)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
