@@ -56,26 +56,87 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """SM clock and throttle-reason samples taken during the timed region.
+
+    A thread of this process reads NVML every 2 ms (read-only queries: the SM
+    clock, the maximum SM clock and the active clock-event reasons), so a
+    timed region of a few milliseconds still holds samples.  Where the NVML
+    library cannot be loaded, nvidia-smi polling every 200 ms is used instead."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock-event reason bits of NVML's public header
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
+    NVML_CLOCK_SM = 1
+    PERIOD_S = 0.002
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, device):
+        import torch
+        self.index = device.index if device.index is not None else 0
+        try:
+            self.uuid = "GPU-" + str(torch.cuda.get_device_properties(self.index).uuid)
+        except (AttributeError, RuntimeError):
+            self.uuid = None
         self.proc = None
+        self.nvml = None
+        self.samples = []
         self.path = os.path.join("/tmp", f"kosmos_clocks_{os.getpid()}.csv")
 
+    # ---- NVML in-process sampler
+    def _nvml_open(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = self.uuid is not None and nv.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            nv.nvmlShutdown()
+            return False
+        mx = ctypes.c_uint()
+        self.sm_max = (float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0
+                       else None)
+        try:
+            self.reasons_fn = nv.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.nvml, self.handle = nv, h
+        return True
+
+    def _poll(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while True:
+            if (self.nvml.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0
+                    and self.reasons_fn(self.handle, ctypes.byref(rs)) == 0):
+                self.samples.append((float(clk.value), int(rs.value)))
+            if self.stop.wait(self.PERIOD_S):
+                return
+
     def __enter__(self):
+        import threading
+        try:
+            opened = self._nvml_open()
+        except (OSError, AttributeError):
+            opened = False
+        if opened:
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 1.0:
+                time.sleep(0.001)
+            return self
         try:
             self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.uuid or str(self.index),
+                                          f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
-            # the timed region starts once nvidia-smi has initialised and
-            # written its first sample (its start-up would otherwise overlap
-            # the first timed steps), between two of its 200 ms queries
+            # the timed region starts once nvidia-smi has written its first
+            # sample (its start-up would otherwise overlap the first steps)
             t0 = time.time()
             while time.time() - t0 < 5.0 and self.proc.poll() is None:
                 if os.path.getsize(self.path) > 0:
@@ -87,6 +148,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
+        if self.nvml is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+            self.nvml.nvmlShutdown()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -95,9 +160,19 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
+    @staticmethod
+    def _summarise(sm, smax, reasons, source):
+        busy = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm), "source": source}
+
     def summary(self):
+        if self.nvml is not None:
+            reasons = {nm for nm, bit in self.REASON_BITS.items() for _, r in self.samples if r & bit}
+            return self._summarise([s for s, _ in self.samples], self.sm_max, reasons,
+                                   f"NVML every {self.PERIOD_S * 1e3:.0f} ms")
         if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
@@ -113,9 +188,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         os.unlink(self.path)
-        busy = [s for s in sm if smax and s > 0.5 * smax] or sm
-        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return self._summarise(sm, smax, reasons, "nvidia-smi every 200 ms")
 
 
 def dist_max(value: float, device=None) -> float:
@@ -856,7 +929,7 @@ def run_kosmos(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+    with ClockSampler(dev) as clk:
         times = time_kernel_steps(f_self, args.steps, args.warmup, flush, stream)
     torch.cuda.synchronize()
     if world > 1:
