@@ -26,6 +26,7 @@ INJECT_DROP_TRANSFER = 0x1
 INJECT_DROP_PARTIAL = 0x2
 INJECT_IDENTITY_EXPERTS = 0x4
 INJECT_DROP_DISPATCH = 0x8
+INJECT_DROP_ARRIVAL = 0x10
 MOE_VIEW_LOGITS, MOE_VIEW_RECV, MOE_VIEW_H, MOE_VIEW_Y, MOE_VIEW_SLOT, MOE_VIEW_OFFSETS, MOE_VIEW_TRACE = range(7)
 MOE_VIEW_RECV_SCALES, MOE_VIEW_XQ, MOE_VIEW_XS = 7, 8, 9  # MXFP8 only
 KIND_NAMES = {1: "TRANSFER", 2: "TILE", 3: "REDUCE", 4: "ROUTE", 5: "DISPATCH", 6: "TILE_GU", 7: "TILE_D",

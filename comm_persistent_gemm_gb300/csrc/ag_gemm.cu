@@ -41,10 +41,13 @@ struct AgParams {
     uint64_t inject;
     int64_t link_gbs;  // emulated link for the remote pieces; 0 = uncapped
     // host-input flow (null otherwise): ext_ready[s * AG_EXT_STRIDE + c] becomes
-    // 1 once chunk c of shard s (ag_host_cpp pieces) has been copied to its
-    // device buffer (by a copy stream); ydone[s * AG_EXT_STRIDE + j] counts the
-    // output tiles of tile-row group j of shard s written (per CTA of a tile
-    // engine)
+    // 1 once chunk c of shard s (ag_host_cpp(g, s) pieces) has been copied into its
+    // slot of x_gathered (by a copy stream); ydone[s * AG_EXT_STRIDE + j]
+    // counts the output tiles of tile-row group j of shard s written (per CTA
+    // of a tile engine).  In this flow the tiles read every shard from
+    // x_gathered once its chunk has arrived, and the transfers run the other
+    // way: each copies its part from x_gathered into the shard's device
+    // buffer (x_src), beside the tiles rather than ahead of them.
     const uint32_t *ext_ready;
     uint32_t *ydone;
 };
@@ -53,9 +56,29 @@ struct AgParams {
 // on the device.
 __device__ __forceinline__ bool ag_ext_wait(const AgParams &p, int s, int piece, int64_t entry) {
     if (p.ext_ready == nullptr) return true;
-    const int c = piece / ag_host_cpp(p.g);
+    const int c = piece / ag_host_cpp(p.g, s);
     return wait_flag_eq(p.ws, const_cast<uint32_t *>(&p.ext_ready[s * AG_EXT_STRIDE + c]), 1u, p.wait_limit_ns,
                         entry);
+}
+
+// Whether tiles of shard s read A from the local shard buffer (tmA_local)
+// rather than from x_gathered: the local shard of a fused call on device
+// inputs.  The unfused baseline gathers first; the host-input flow lands
+// every shard in x_gathered.
+__device__ __forceinline__ bool ag_reads_local(const AgParams &p, int s) {
+    return s == 0 && p.sched != KOSMOS_SCHED_UNFUSED && p.ext_ready == nullptr;
+}
+
+// Whether a tile of shard s waits for its pieces' flags (released by the
+// transfers into x_gathered): remote shards of a fused call on device inputs.
+__device__ __forceinline__ bool ag_waits_flags(const AgParams &p, int s) {
+    return s != 0 && p.sched != KOSMOS_SCHED_UNFUSED && p.ext_ready == nullptr;
+}
+
+// Whether a tile of shard s waits for its chunk's arrival word: every shard
+// of a fused host-input call (the unfused baseline's gather waits instead).
+__device__ __forceinline__ bool ag_waits_arrival(const AgParams &p) {
+    return p.ext_ready != nullptr && p.sched != KOSMOS_SCHED_UNFUSED;
 }
 
 // Host-input flow: one output tile of tile row `trow` of shard s written by
@@ -64,7 +87,7 @@ __device__ __forceinline__ void ag_ydone(const AgParams &p, int s, int trow, int
     if (p.ydone == nullptr) return;
     __threadfence();
     named_bar_sync(1, NUM_EPI_THREADS);
-    if (grp == 0 && lane == 0) red_release_add_gpu(&p.ydone[s * AG_EXT_STRIDE + trow / ag_host_tpg(p.g)], 1u);
+    if (grp == 0 && lane == 0) red_release_add_gpu(&p.ydone[s * AG_EXT_STRIDE + trow / ag_host_tpg(p.g, s)], 1u);
 }
 
 // Host-input flow: a failed launch releases every output wait of the host.
@@ -110,8 +133,11 @@ __device__ __forceinline__ bool ag_claim_transfer(const AgParams &p, MoveEntry &
     int64_t row0, rows;
     ag_part_rows(p.g, piece, part, row0, rows);
     const int64_t row_bytes = p.g.k * 2;
-    e.src[0] = p.x_src[shard] + row0 * row_bytes;
-    e.dst[0] = p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes;
+    uint8_t *gath = p.x_gath + (static_cast<int64_t>(shard) * p.g.m + row0) * row_bytes;
+    uint8_t *shard_buf = const_cast<uint8_t *>(p.x_src[shard]) + row0 * row_bytes;
+    const bool to_shard = p.ext_ready != nullptr;  // host-input flow: x_gathered -> the shard's device buffer
+    e.src[0] = to_shard ? gath : shard_buf;
+    e.dst[0] = to_shard ? shard_buf : gath;
     e.bytes[0] = rows * row_bytes;
     e.src[1] = nullptr; e.dst[1] = nullptr; e.bytes[1] = 0;
     const bool drop = (p.inject & KOSMOS_INJECT_DROP_TRANSFER) && static_cast<int64_t>(p.inject >> 32) == t;
@@ -222,7 +248,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
         const AgTileWork w = ag_tile_work(p, static_cast<int>(t));
         const int s = w.s, i = w.i;
         const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
-        if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0) {
+        if (ag_waits_flags(p, s)) {
             if (!ag_help_until_ready<NSTAGE, STAGE_BYTES>(p, sm.stages, sm.cbar, cphase, nrec, s, i,
                                                           ag_piece_ready(p.g, epoch),
                                                           [&] { return drain_stages1(sm, ps, p.ws); }))
@@ -230,7 +256,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
             if (!wait_flag_eq(p.ws, &p.flags[s * p.g.pieces + i], ag_piece_ready(p.g, epoch), p.wait_limit_ns, t))
                 break;
         }
-        if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0 && !ag_ext_wait(p, 0, i, t)) break;  // host-input flow
+        if (ag_waits_arrival(p) && !ag_ext_wait(p, s, i, t)) break;  // host-input flow
         int slot = -1;
         if (TraceRec *r = trace_rec(p.trace, cta, nrec)) {
             r->t_claim = tc; r->t_ready = static_cast<int64_t>(globaltimer()); r->t_done = 0;
@@ -243,7 +269,7 @@ __device__ __forceinline__ void ag_producer(const AgParams &p, const Smem &sm, u
         e.kind = K_TILE; e.a = s; e.b = i; e.c = w.col0; e.d = w.kb0; e.nstage = w.nk;
         e.ticket = static_cast<int32_t>(t); e.slot = slot; e.x1 = w.slot;
         if (!ring_push(sm, rs, e, p.ws)) break;
-        const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+        const bool local = ag_reads_local(p, s);
         bool ok = true;
         for (int kk = 0; kk < w.nk; ++kk) {
             const int kb = w.kb0 + kk;
@@ -409,7 +435,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
     }
     if (leader) {
         const uint32_t my_full0 = mapa_u32(smem_u32(&sm.full[0]), 0);
-            while (true) {
+        while (true) {
             if (failed(p.ws)) break;
             const uint32_t t = atomicAdd(&p.ws->tickets[1], 1u);
             if (t >= static_cast<uint32_t>(p.g.n_tile)) break;
@@ -417,13 +443,10 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             const int s = w.s, i2 = w.i;
             const int64_t tc = p.trace ? static_cast<int64_t>(globaltimer()) : 0;
             const int pc = 2 * i2;  // the leader's 128-row piece
-            const bool remote = p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces;
-            if (p.sched != KOSMOS_SCHED_UNFUSED && s == 0) {  // host-input flow: both 128-row pieces
-                if (!ag_ext_wait(p, 0, pc, t)) break;
-                if (pc + 1 < p.g.pieces && !ag_ext_wait(p, 0, pc + 1, t)) break;
-            }
+            const bool remote = ag_waits_flags(p, s) && pc < p.g.pieces;
             // the entry is published before the readiness wait, so that the
-            // peer can take transfer parts for its own piece meanwhile
+            // peer can take transfer parts (or wait for the arrival of its
+            // own piece) meanwhile
             int slot = -1;
             TraceRec *rec = trace_rec(p.trace, blockIdx.x, nrec);
             if (rec) {
@@ -446,8 +469,9 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
                                   p.wait_limit_ns, t))
                     break;
             }
+            if (ag_waits_arrival(p) && !ag_ext_wait(p, s, pc, t)) break;  // host-input flow
             if (rec) rec->t_ready = static_cast<int64_t>(globaltimer());
-            const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+            const bool local = ag_reads_local(p, s);
             bool ok = true;
             for (int kk = 0; kk < w.nk; ++kk) {
                 if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
@@ -473,7 +497,7 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
             if (e.kind == K_DONE) break;
             const int s = e.a, i2 = e.b;
             const int pc = 2 * i2 + 1;  // the peer's 128-row piece
-            if (p.sched != KOSMOS_SCHED_UNFUSED && s != 0 && pc < p.g.pieces) {
+            if (ag_waits_flags(p, s) && pc < p.g.pieces) {
                 if (!ag_help_until_ready<NSTAGE2, STAGE2_BYTES>(p, sm.stages, sm.cbar, cphase, nrec, s, pc,
                                                                 ag_piece_ready(p.g, epoch),
                                                                 [&] { return drain_stages2(sm, ps, p.ws); }))
@@ -482,7 +506,8 @@ __device__ __forceinline__ void ag2_producer(const AgParams &p, const Smem2 &sm,
                                   p.wait_limit_ns, e.ticket))
                     break;
             }
-            const bool local = (s == 0) && p.sched != KOSMOS_SCHED_UNFUSED;
+            if (ag_waits_arrival(p) && pc < p.g.pieces && !ag_ext_wait(p, s, pc, e.ticket)) break;
+            const bool local = ag_reads_local(p, s);
             bool ok = true;
             for (int kb = 0; kb < e.nstage; ++kb) {
                 if (!mbar_wait(&sm.empty[ps.stage], ps.phase ^ 1u, PIPE_LIMIT_NS)) {
@@ -575,12 +600,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ag_gemm_pair_kernel(const __gr
 }
 
 // Unfused baseline, first launch: gather every shard into x_gathered with
-// plain 16-byte vector copies over all SMs.
+// plain 16-byte vector copies over all SMs (in the host-input flow, where the
+// shards land in x_gathered, copy each on into its device buffer instead).
 __global__ void __launch_bounds__(256) ag_gather_copy_kernel(const AgParams p) {
     if (p.ext_ready != nullptr) {  // host-input flow: every shard must be on the device
         if (threadIdx.x == 0)
             for (int s = 0; s < p.g.P; ++s)
-                for (int pc = 0; pc < p.g.pieces; pc += ag_host_cpp(p.g)) ag_ext_wait(p, s, pc, -40);
+                for (int pc = 0; pc < p.g.pieces; pc += ag_host_cpp(p.g, s)) ag_ext_wait(p, s, pc, -40);
         __syncthreads();
         if (failed(p.ws)) return;
     }
@@ -588,11 +614,16 @@ __global__ void __launch_bounds__(256) ag_gather_copy_kernel(const AgParams p) {
     const int64_t per = shard_bytes / 16;
     const int64_t total = per * p.g.P;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const bool to_shard = p.ext_ready != nullptr;  // host-input flow: x_gathered -> the shard buffers
     for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += stride) {
         const int64_t s = v / per;
         const int64_t o = v - s * per;
-        const uint4 x = reinterpret_cast<const uint4 *>(p.x_src[s])[o];
-        reinterpret_cast<uint4 *>(p.x_gath + s * shard_bytes)[o] = x;
+        uint4 *gath = reinterpret_cast<uint4 *>(p.x_gath + s * shard_bytes) + o;
+        uint4 *shard = reinterpret_cast<uint4 *>(const_cast<uint8_t *>(p.x_src[s])) + o;
+        if (to_shard)
+            *shard = *gath;
+        else
+            *gath = *shard;
     }
     if (p.link_gbs > 0) ag_copy_link_pace(p.ws, per, total, p.link_gbs);
 }

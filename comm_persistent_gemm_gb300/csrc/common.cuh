@@ -220,17 +220,28 @@ struct AgWsLayout {
 // Host-input flow: a shard arrives from the host in at most AG_HOST_CHUNKS
 // chunks of whole 128-row pieces, each with an arrival word, and its output
 // rows go back in at most AG_HOST_GROUPS groups of whole tile rows, each with
-// an output-tile count.  Region: [KOSMOS_MAX_P][AG_EXT_STRIDE] arrival words,
-// the same for the counts, then three stream-join words.
+// an output-tile count (the last shard, whose tiles and output copies end the
+// call, in at most AG_HOST_LAST_CHUNKS and AG_HOST_LAST_GROUPS).  Region:
+// [KOSMOS_MAX_P][AG_EXT_STRIDE] arrival words, the same for the counts, then
+// three stream-join words.
 constexpr int AG_HOST_CHUNKS = 1;
 constexpr int AG_HOST_GROUPS = 2;
+constexpr int AG_HOST_LAST_CHUNKS = 2;
+constexpr int AG_HOST_LAST_GROUPS = 2;
 constexpr int AG_EXT_STRIDE = 8;                              // words per shard in each array
 constexpr int AG_EXT_WORDS = KOSMOS_MAX_P * AG_EXT_STRIDE;    // words of each of the two arrays
 constexpr int AG_EXT_BYTES = 1024;
-static_assert(AG_HOST_CHUNKS <= AG_EXT_STRIDE && AG_HOST_GROUPS <= AG_EXT_STRIDE, "host-flow words per shard");
+static_assert(AG_HOST_CHUNKS <= AG_EXT_STRIDE && AG_HOST_GROUPS <= AG_EXT_STRIDE &&
+                  AG_HOST_LAST_CHUNKS <= AG_EXT_STRIDE && AG_HOST_LAST_GROUPS <= AG_EXT_STRIDE,
+              "host-flow words per shard");
 static_assert(2 * AG_EXT_WORDS * 4 + 3 * 4 <= AG_EXT_BYTES, "host-flow words exceed their region");
-KOS_HD int ag_host_cpp(const AgGeom &g) { return static_cast<int>(cdiv(g.pieces, AG_HOST_CHUNKS)); }   // pieces / chunk
-KOS_HD int ag_host_tpg(const AgGeom &g) { return static_cast<int>(cdiv(g.tiles_m, AG_HOST_GROUPS)); }  // tile rows / group
+// pieces per arrival chunk and tile rows per output group of shard s
+KOS_HD int ag_host_cpp(const AgGeom &g, int s) {
+    return static_cast<int>(cdiv(g.pieces, s == g.P - 1 ? AG_HOST_LAST_CHUNKS : AG_HOST_CHUNKS));
+}
+KOS_HD int ag_host_tpg(const AgGeom &g, int s) {
+    return static_cast<int>(cdiv(g.tiles_m, s == g.P - 1 ? AG_HOST_LAST_GROUPS : AG_HOST_GROUPS));
+}
 // Written to the output-done counters when a launch fails or never starts: a
 // stream wait "value >= target" compares (int32_t)(word - target) >= 0, so the
 // release value must stay below 2^31 above any target.

@@ -410,13 +410,11 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
     const CUdeviceptr ready = reinterpret_cast<CUdeviceptr>(ext);
     const CUdeviceptr done = ready + 4 * AG_EXT_WORDS;
     // A shard arrives in chunks of whole 128-row pieces and its output rows go
-    // back in groups of whole tile rows (at most AG_HOST_CHUNKS and AG_HOST_GROUPS), so
-    // that the kernel starts on a shard's first rows before the rest are in
-    // and the host receives the first output rows of the last shard while its
-    // other tile rows are still being built.  The same geometry as the kernel's.
+    // back in groups of whole tile rows (ag_host_cpp / ag_host_tpg: the same
+    // geometry as the kernel's), so that the kernel starts on a shard's first
+    // rows before the rest are in and the host receives a shard's first
+    // output rows while its other tile rows are still being built.
     const AgGeom tg = ag_geom(P, m_per_shard, k, n, pl.pair ? PBM : BM);
-    const int cpp = ag_host_cpp(tg), tpg = ag_host_tpg(tg);
-    const int nch = static_cast<int>(cdiv(tg.pieces, cpp)), ngr = static_cast<int>(cdiv(tg.tiles_m, tpg));
     cudaStream_t s = static_cast<cudaStream_t>(stream), h = static_cast<cudaStream_t>(h2d_stream),
                  d = static_cast<cudaStream_t>(d2h_stream);
     CUstream cs = reinterpret_cast<CUstream>(s), ch = reinterpret_cast<CUstream>(h), cd = reinterpret_cast<CUstream>(d);
@@ -432,8 +430,8 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
               wr(cs, sync, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
               wt(ch, sync, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS &&
               wt(cd, sync, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS;
-    // The kernel is enqueued first: its movers and local-shard builders wait
-    // for the arrival words, so it starts on the first chunks while the host
+    // The kernel is enqueued first: its tiles and movers wait for the
+    // arrival words, so it starts on the first chunks while the host
     // is still enqueueing the later ones.  If an enqueue below fails, the
     // kernel's bounded waits end it with a status and it releases the
     // output waits.
@@ -443,22 +441,29 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
         for (int i = 0; i < P * AG_EXT_STRIDE; ++i)
             wr(ch, done + 4 * i, AG_YDONE_RELEASE, CU_STREAM_WRITE_VALUE_DEFAULT);
     }
-    // shard r to the device chunk by chunk, each followed by its arrival word (the local shard first)
+    // shard r into its slot of x_gathered chunk by chunk, each followed by its
+    // arrival word (the local shard first); the kernel's tiles read the slot
+    // as soon as the word is set, and its movers copy the slot on into x_dev[r]
     const int64_t xrow = k * 2, yrow = n * 2;
-    for (int r = 0; ok && r < P; ++r)
+    const bool drop = (o.inject & KOSMOS_INJECT_DROP_ARRIVAL) != 0;
+    for (int r = 0; ok && r < P; ++r) {
+        const int cpp = ag_host_cpp(tg, r), nch = static_cast<int>(cdiv(tg.pieces, cpp));
         for (int c = 0; ok && c < nch; ++c) {
             const int64_t r0 = static_cast<int64_t>(c) * cpp * PIECE_ROWS;
             const int64_t r1 = std::min<int64_t>(m_per_shard, r0 + static_cast<int64_t>(cpp) * PIECE_ROWS);
-            ok = cudaMemcpyAsync(static_cast<uint8_t *>(x_dev[r]) + r0 * xrow,
+            ok = cudaMemcpyAsync(static_cast<uint8_t *>(x_gathered) + (static_cast<int64_t>(r) * m_per_shard + r0) * xrow,
                                  static_cast<const uint8_t *>(x_host[r]) + r0 * xrow, static_cast<size_t>((r1 - r0) * xrow),
-                                 cudaMemcpyHostToDevice, h) == cudaSuccess &&
-                 wr(ch, ready + 4 * (r * AG_EXT_STRIDE + c), 1u, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+                                 cudaMemcpyHostToDevice, h) == cudaSuccess;
+            if (ok && !(drop && static_cast<int64_t>(o.inject >> 32) == r))
+                ok = wr(ch, ready + 4 * (r * AG_EXT_STRIDE + c), 1u, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
         }
+    }
     // each group of shard r's output rows back to the host once all its tiles
     // are written (output tiles counted per CTA of a tile engine)
     const int64_t tr = pl.pair ? PBM : BM;
     const uint32_t per_row = static_cast<uint32_t>(cdiv(n, BN) * (pl.pair ? 2 : 1));
-    for (int r = 0; ok && r < P; ++r)
+    for (int r = 0; ok && r < P; ++r) {
+        const int tpg = ag_host_tpg(tg, r), ngr = static_cast<int>(cdiv(tg.tiles_m, tpg));
         for (int j = 0; ok && j < ngr; ++j) {
             const int t0 = j * tpg, t1 = std::min(tg.tiles_m, t0 + tpg);
             const int64_t r0 = t0 * tr, r1 = std::min<int64_t>(m_per_shard, t1 * tr);
@@ -468,6 +473,7 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
                  cudaMemcpyAsync(static_cast<uint8_t *>(y_host) + off, static_cast<uint8_t *>(y_dev) + off,
                                  static_cast<size_t>((r1 - r0) * yrow), cudaMemcpyDeviceToHost, d) == cudaSuccess;
         }
+    }
     ok = ok && wr(ch, sync + 4, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
          wr(cd, sync + 8, tok, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS &&
          wt(cs, sync + 4, tok, CU_STREAM_WAIT_VALUE_EQ) == CUDA_SUCCESS &&

@@ -92,6 +92,8 @@ enum { KOSMOS_ORDER_BAND = 0, KOSMOS_ORDER_ROW = 1 };
 #define KOSMOS_INJECT_DROP_PARTIAL  0x2ull  /* RS: rank (inject >> 32) never signals its partial tiles */
 #define KOSMOS_INJECT_DROP_DISPATCH 0x8ull  /* MoE forward: the DISPATCH entry of main-rail ticket (inject >> 32)
                                                copies its rows but never counts them as arrived */
+#define KOSMOS_INJECT_DROP_ARRIVAL  0x10ull /* AG host-input call: shard (inject >> 32) is copied to the device
+                                               but its arrival words are never written */
 /* MoE debug mode: every expert is the identity map (no expert GEMMs; the
  * pushed rows are the dispatched token rows), which isolates router,
  * dispatch, push and fold.  Not a fault: the output is x * sum of gates. */
@@ -185,15 +187,16 @@ KOSMOS_API int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t k, int64_
 
 /*
  * All-gather + GEMM with the shards in host memory (BF16): the copies to the
- * device run on h2d_stream, shard by shard (the local shard first), each
- * followed by an arrival word the kernel's movers (and, for the local shard,
- * builders) wait on, so the copies overlap the multiplication; each shard's
- * output rows go back on d2h_stream in two groups of tile rows, each as soon
- * as its tiles are written (a stream wait on the group's tile count).  The
- * kernel is enqueued before the copies.  Same result as kosmos_ag_gemm on
- * x_dev.
+ * device run on h2d_stream, shard by shard (the local shard first), each into
+ * its slot of x_gathered and followed by an arrival word; the kernel's tiles
+ * read a shard as soon as its word is set, so the copies overlap the
+ * multiplication, and its movers copy each shard on into x_dev[r] beside the
+ * tiles.  Each shard's output rows go back on d2h_stream in two groups of
+ * tile rows, each as soon as its tiles are written (a stream wait on the
+ * group's tile count).  The kernel is enqueued before the copies.  Same
+ * result as kosmos_ag_gemm on x_dev (Y and x_gathered bit for bit).
  *   x_host[r]     : X_r [m_per_shard, k] bf16 in pinned host memory.
- *   x_dev[r]      : device buffers [m_per_shard, k] the shards are copied to.
+ *   x_dev[r]      : out, device buffers [m_per_shard, k] that receive X_r.
  *   y_dev, y_host : [P * m_per_shard, n] bf16, device and pinned host.
  *   stream        : the kernel's stream; on return, work enqueued on it
  *                   waits for both copy streams, so its completion means the
