@@ -32,7 +32,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one ag_gemm_pair_kernel launch on the 8-rank AG
 # workload, from an ncu capture; valid only while the kernel sources hash to
 # src_sha (otherwise the bench reports traffic = null).
-TRAFFIC_CAPTURE = {"bytes": 823246592, "src_sha": "db300732db71432b"}
+TRAFFIC_CAPTURE = {"bytes": 830933248, "src_sha": "5fac42c3390fb242"}
 KERNEL_SOURCES = ["comm_persistent_gemm_gb300/csrc/ag_gemm.cu", "comm_persistent_gemm_gb300/csrc/engine.cuh",
                   "comm_persistent_gemm_gb300/csrc/engine2.cuh", "comm_persistent_gemm_gb300/csrc/ptx.cuh",
                   "comm_persistent_gemm_gb300/csrc/common.cuh"]
