@@ -61,6 +61,33 @@ def test_binding_argument_lists_match_the_header(K):
                 assert a in (C.c_int, C.c_int32), (name, decl, a)
 
 
+def test_binding_constants_match_the_header(K):
+    """Every numeric #define and enum value of include/kosmos.h that the
+    binding exposes (under its name without the KOSMOS_ prefix) is equal, and
+    every fault-injection bit is exposed."""
+    import os
+    import re
+    from _helpers import ROOT
+    src = open(os.path.join(ROOT, "include", "kosmos.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    vals = {}
+    for m in re.finditer(r"#define\s+KOSMOS_(\w+)\s+(0x[0-9a-fA-F]+|\d+)(?:ull|u|ll)?\b", src):
+        vals[m.group(1)] = int(m.group(2), 0)
+    for body in re.findall(r"enum\s*(?:\w+\s*)?\{([^}]*)\}", src):
+        for m in re.finditer(r"KOSMOS_(\w+)\s*=\s*(-?(?:0x[0-9a-fA-F]+|\d+))", body):
+            vals[m.group(1)] = int(m.group(2), 0)
+    inject = [n for n in vals if n.startswith("INJECT_")]
+    assert len(inject) >= 5
+    for n in inject:
+        assert hasattr(K, n), n
+    checked = 0
+    for n, v in vals.items():
+        if hasattr(K, n) and isinstance(getattr(K, n), int):
+            assert getattr(K, n) == v, n
+            checked += 1
+    assert checked >= 15
+
+
 def test_default_opts(K):
     o = K.opts()
     assert o.sched == K.SCHED_SELF and o.n_comm0 == -1 and o.order == K.ORDER_BAND
