@@ -36,6 +36,27 @@ static PFN_encodeTiled_t get_encode_fn() {
 // through the workspace's join words, distinct from the previous call's.
 static std::atomic<uint32_t> g_host_flow_token{0};
 
+// The arrival words of the host-input all-gather are set by a 4-byte copy of
+// this pinned word (value 1) after each chunk's copy on the same stream: the
+// copy starts once the chunk's copy has completed, and costs the copy engine
+// less than a stream write operation.  Allocated once, never freed.
+static const uint32_t *host_one_word() {
+    static std::atomic<uint32_t *> word{nullptr};
+    uint32_t *w = word.load(std::memory_order_acquire);
+    if (w == nullptr) {
+        void *p = nullptr;
+        if (cudaHostAlloc(&p, 16, cudaHostAllocPortable) != cudaSuccess) return nullptr;
+        static_cast<uint32_t *>(p)[0] = 1u;
+        uint32_t *expected = nullptr;
+        if (!word.compare_exchange_strong(expected, static_cast<uint32_t *>(p), std::memory_order_acq_rel)) {
+            cudaFreeHost(p);  // another thread installed its word first
+            return expected;
+        }
+        w = static_cast<uint32_t *>(p);
+    }
+    return w;
+}
+
 // Stream memory operations (write / wait on a 32-bit word in device memory).
 typedef CUresult (*PFN_streamValue32_t)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 static PFN_streamValue32_t get_stream_value_fn(bool wait) {
@@ -446,6 +467,7 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
     // as soon as the word is set, and its movers copy the slot on into x_dev[r]
     const int64_t xrow = k * 2, yrow = n * 2;
     const bool drop = (o.inject & KOSMOS_INJECT_DROP_ARRIVAL) != 0;
+    const uint32_t *one = host_one_word();
     for (int r = 0; ok && r < P; ++r) {
         const int cpp = ag_host_cpp(tg, r), nch = static_cast<int>(cdiv(tg.pieces, cpp));
         for (int c = 0; ok && c < nch; ++c) {
@@ -454,8 +476,12 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
             ok = cudaMemcpyAsync(static_cast<uint8_t *>(x_gathered) + (static_cast<int64_t>(r) * m_per_shard + r0) * xrow,
                                  static_cast<const uint8_t *>(x_host[r]) + r0 * xrow, static_cast<size_t>((r1 - r0) * xrow),
                                  cudaMemcpyHostToDevice, h) == cudaSuccess;
-            if (ok && !(drop && static_cast<int64_t>(o.inject >> 32) == r))
-                ok = wr(ch, ready + 4 * (r * AG_EXT_STRIDE + c), 1u, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+            if (ok && !(drop && static_cast<int64_t>(o.inject >> 32) == r)) {
+                const CUdeviceptr word = ready + 4 * (r * AG_EXT_STRIDE + c);
+                ok = one != nullptr ? cudaMemcpyAsync(reinterpret_cast<void *>(word), one, 4, cudaMemcpyHostToDevice,
+                                                      h) == cudaSuccess
+                                    : wr(ch, word, 1u, CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+            }
         }
     }
     // each group of shard r's output rows back to the host once all its tiles

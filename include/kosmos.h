@@ -188,7 +188,8 @@ KOSMOS_API int kosmos_ag_tile_plan(int P, int64_t m_per_shard, int64_t k, int64_
 /*
  * All-gather + GEMM with the shards in host memory (BF16): the copies to the
  * device run on h2d_stream, shard by shard (the local shard first), each into
- * its slot of x_gathered and followed by an arrival word; the kernel's tiles
+ * its slot of x_gathered and followed by a 4-byte copy that sets its arrival
+ * word (from a pinned word the library allocates once); the kernel's tiles
  * read a shard as soon as its word is set, so the copies overlap the
  * multiplication, and its movers copy each shard on into x_dev[r] beside the
  * tiles.  Each shard's output rows go back on d2h_stream in two groups of
