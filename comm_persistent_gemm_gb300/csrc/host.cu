@@ -441,8 +441,9 @@ kosmos_status kosmos_ag_gemm_host(const void *const *x_host, void *const *x_dev,
     CUstream cs = reinterpret_cast<CUstream>(s), ch = reinterpret_cast<CUstream>(h), cd = reinterpret_cast<CUstream>(d);
     // The three streams join through three words of the workspace (no CUDA
     // events to create per call): `stream` publishes this call's token once
-    // its earlier work (the previous kernel reading x_dev) is done and the
-    // arrival and output words are zeroed; the copy streams wait for it; at
+    // its earlier work (a previous call's kernel, which reads x_gathered and
+    // writes x_dev) is done and the arrival and output words are zeroed; the
+    // copy streams wait for it before they overwrite x_gathered or y_host; at
     // the end each copy stream publishes the token and `stream` waits for both.
     const CUdeviceptr sync = done + 4 * AG_EXT_WORDS;  // [0] stream ready, [1] h2d done, [2] d2h done
     uint32_t tok = g_host_flow_token.fetch_add(1u, std::memory_order_relaxed) + 1u;
