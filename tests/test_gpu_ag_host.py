@@ -59,10 +59,11 @@ def run_dev(K, inp, o=None):
     return y.cpu()
 
 
+@pytest.mark.parametrize("shape", [(4, 384, 256, 768), (3, 200, 192, 264)])  # whole and ragged 128-row pieces
 @pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("sched", [0, 1, 2])
-def test_ag_host_small_matches_device_call(K, orc, sched, pair):
-    P, m, k, n = 4, 384, 256, 768
+def test_ag_host_small_matches_device_call(K, orc, sched, pair, shape):
+    P, m, k, n = shape
     inp = ag_inputs(P, m, k, n, seed=41, var_w=1.0 / k)
     o = K.opts(sched=sched, cta_pair=pair)
     outs, ws, xg, xd = run_host(K, inp, o, reps=2)
