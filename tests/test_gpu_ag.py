@@ -65,7 +65,7 @@ def test_ag_tiny_workload(K, orc, sched, mode):
 @pytest.mark.parametrize("mode", list(PAIR))
 @pytest.mark.parametrize("sched", list(SCHEDS))
 @pytest.mark.parametrize("P,m,k,n", [(3, 200, 192, 264), (1, 130, 128, 256), (4, 128, 320, 512),
-                                     (2, 37, 64, 8), (2, 300, 128, 520)])
+                                     (2, 37, 64, 8), (2, 300, 128, 520), (2, 1, 64, 8)])
 def test_ag_ragged_multi_tile(K, orc, sched, P, m, k, n, mode):
     inp = ag_inputs(P, m, k, n, seed=1000 + P * m + n, var_w=1.0 / k)
     _check_full(orc, K, inp, K.opts(sched=SCHEDS[sched], cta_pair=PAIR[mode]))

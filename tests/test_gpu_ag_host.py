@@ -59,7 +59,7 @@ def run_dev(K, inp, o=None):
     return y.cpu()
 
 
-@pytest.mark.parametrize("shape", [(4, 384, 256, 768), (3, 200, 192, 264)])  # whole and ragged 128-row pieces
+@pytest.mark.parametrize("shape", [(4, 384, 256, 768), (3, 200, 192, 264), (2, 1, 64, 8)])  # whole, ragged, one row
 @pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("sched", [0, 1, 2])
 def test_ag_host_small_matches_device_call(K, orc, sched, pair, shape):
